@@ -1,0 +1,125 @@
+"""fp64 CPU oracle (plain C, ``oracle.c``) and its ctypes binding.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  It
+shares no code with the CUDA library; the two sides meet only in the seeded
+input generators of ``workloads``.
+
+``token_logprob``  -- the selected-token logprob by the definition (icarus
+"RL: Training Inference Mismatch", section "log p"): z = h W^T in fp64,
+lse = log sum exp z, logp = z[a] - lse.
+``mismatch_stats`` -- delta, r, k1/k2/k3, truncated-IS weight, masked
+per-sequence and batch means and the rejection flag (VeXact summary eq. (1)
+and "KL Estimators"; llm-infra-atlas section 2; icarus "KL estimators",
+monitoring steps and compute_consistency_and_kl_metrics; LoongSage sections
+4-5).  Field orders are ``SEQ_FIELDS`` and ``BATCH_FIELDS``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+SEQ_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
+              "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel")
+BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
+                "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel",
+                "seqmean_k1", "seqmean_k2", "seqmean_k3", "clip_ratio", "nan_ratio",
+                "reject_ratio", "n_seqs_nonempty", "n_rejected")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with plain gcc -O2 (no fast-math) into _liboracle.so."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            lib.oracle_token_logprob.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int64, P, P, ctypes.c_int]
+            lib.oracle_token_logprob.restype = ctypes.c_int
+            lib.oracle_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int64,
+                                                  ctypes.c_double, ctypes.c_double, ctypes.c_int32,
+                                                  P, P, P, P]
+            lib.oracle_mismatch_stats.restype = ctypes.c_int
+            assert lib.oracle_seq_fields() == len(SEQ_FIELDS)
+            assert lib.oracle_batch_fields() == len(BATCH_FIELDS)
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def token_logprob(h_bf16: np.ndarray, W_bf16: np.ndarray, targets: np.ndarray,
+                  rows=None, nthreads: int | None = None):
+    """(logp, lse) as float64 arrays, for `rows` of h (all rows if None).
+
+    h_bf16 uint16 [N, D], W_bf16 uint16 [V, D] (bf16 bit patterns),
+    targets int32 [N]."""
+    lib = _load()
+    h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    a = np.ascontiguousarray(targets, dtype=np.int32)
+    N, D = h.shape
+    V, D2 = W.shape
+    assert D == D2 and a.shape == (N,)
+    if rows is None:
+        r = None
+        R = N
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        assert r.ndim == 1 and (r.size == 0 or (r.min() >= 0 and r.max() < N))
+        R = r.size
+    logp = np.empty(R, dtype=np.float64)
+    lse = np.empty(R, dtype=np.float64)
+    nt = nthreads or max(1, len(os.sched_getaffinity(0)))
+    rc = lib.oracle_token_logprob(_ptr(h), _ptr(W), _ptr(a), None if r is None else _ptr(r), R,
+                                  D, V, _ptr(logp), _ptr(lse), nt)
+    if rc != 0:
+        raise RuntimeError("oracle_token_logprob failed")
+    return logp, lse
+
+
+def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
+                   tau_seq: float = float("nan"), seq_estimator: int = 3):
+    """dict with token_weight [N], seq_stats [S, 12], seq_flags [S], batch [20]
+    (all float64 except seq_flags int32)."""
+    lib = _load()
+    lt = np.ascontiguousarray(logp_train, dtype=np.float32)
+    lr = np.ascontiguousarray(logp_rollout, dtype=np.float32)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    off = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+    N = lt.size
+    S = off.size - 1
+    assert lr.size == N and m.size == N and S >= 0
+    w = np.empty(N, dtype=np.float64)
+    seq = np.empty((S, len(SEQ_FIELDS)), dtype=np.float64)
+    flags = np.empty(S, dtype=np.int32)
+    batch = np.empty(len(BATCH_FIELDS), dtype=np.float64)
+    rc = lib.oracle_mismatch_stats(_ptr(lt), _ptr(lr), _ptr(m), _ptr(off), S, N, float(C),
+                                   float(tau_seq), int(seq_estimator), _ptr(w), _ptr(seq),
+                                   _ptr(flags), _ptr(batch))
+    if rc != 0:
+        raise ValueError("oracle_mismatch_stats rejected its arguments")
+    return {"token_weight": w, "seq_stats": seq, "seq_flags": flags, "batch": batch}

@@ -1,0 +1,333 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle for the selected-token logprob and
+ * the train/rollout mismatch statistics.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load or call this code.  It
+ * shares nothing with the CUDA library (no header, no helper, no table) and
+ * neither side includes or links the other.
+ *
+ * Everything is computed in double from the exact values of the inputs
+ * (bf16 and fp32 convert to double exactly).  No blocking, fusion or
+ * reordering: every sum runs in index order exactly as the definition reads.
+ *
+ * Sources (page title + section):
+ *  - token logprob: icarus "RL: Training Inference Mismatch", section "log p"
+ *    (hidden state -> LM head -> log-softmax -> gather at the token id, and
+ *    its PyTorch statement log_softmax(logits, -1).gather(-1, ids)); LoongSage
+ *    "Train-Inference Consistency" section 3 "FP32 LM head" (the head is
+ *    computed at higher precision than bf16).  The pages' head has a bias;
+ *    the library's call has none, so neither has this oracle.
+ *  - mismatch: VeXact summary page, "Formal Definition" eq. (1)
+ *    (delta = log pi_train - log pi_rollout) and "KL Estimators" (K1 = -log r,
+ *    K3 = (r - 1) - log r); llm-infra-atlas section 2 (Delta = l_theta - l_mu,
+ *    r = e^Delta); icarus "KL estimators" table (k2 = 0.5 (log r)^2) and
+ *    "monitoring" steps 2-3 (mean over a completion's tokens, then mean over
+ *    completions); icarus compute_consistency_and_kl_metrics
+ *    (rel_diff = |delta| / (|logp_train| + 1e-8), masked mean); LoongSage
+ *    section 4 (IS weight pi_old/pi_rollout, clipped when out of bounds) and
+ *    section 5 (is_approx_k3_kl, is_clip_ratio, is_nan_ratio); VeXact
+ *    "Algorithmic TIM Compensation" (sequence rejection on K3 / K1 of
+ *    r_corr = pi_train / pi_rollout, thresholds tau_seq).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - w = min(r, C) (one-sided truncation), clip = r > C (strict);
+ *  - a token "used" = mask != 0 and delta finite; a masked token with a
+ *    non-finite delta counts as nan, gets w = 0 and is left out of the means;
+ *  - integer decisions (finite, clip) use delta rounded to fp32, the
+ *    precision the device computes it in; values use the exact fp64 delta;
+ *  - log r is taken as delta itself (r = e^delta by definition), and
+ *    r - 1 as expm1(delta), so that k3 does not lose digits to cancellation;
+ *  - a sequence with no used token has all means 0, flag 0, and is left out
+ *    of the mean over sequences;
+ *  - rejection: mean k3 > tau (estimator 3) or |mean k1| > tau (estimator 1),
+ *    strict; tau NaN means the default k3(C) = (C - 1) - ln C.
+ *  - target outside [0, V) (the -100 ignore label): logp = NaN, lse valid.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ token logprob */
+
+static double bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One row of the definition: z_v = sum_d h_d W[v, d]  (d ascending),
+ * m = max_v z_v, S = sum_v exp(z_v - m) (v ascending), lse = m + log S,
+ * logp = z_a - lse. */
+static void oracle_row(const uint16_t *h_row, const uint16_t *W, int32_t a,
+                       int64_t D, int64_t V, double *hd, double *z,
+                       double *out_logp, double *out_lse)
+{
+    for (int64_t d = 0; d < D; ++d)
+        hd[d] = bf16_value(h_row[d]);
+    for (int64_t v = 0; v < V; ++v) {
+        const uint16_t *w = W + v * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            acc += hd[d] * bf16_value(w[d]);
+        z[v] = acc;
+    }
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v)
+        if (z[v] > m)
+            m = z[v];
+    double S = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        S += exp(z[v] - m);
+    double lse = m + log(S);
+    *out_lse = lse;
+    *out_logp = (a >= 0 && (int64_t)a < V) ? z[a] - lse : NAN;
+}
+
+typedef struct {
+    const uint16_t *h, *W;
+    const int32_t *targets;
+    const int64_t *rows;
+    int64_t R, D, V;
+    double *out_logp, *out_lse;
+    int tid, nthreads, failed;
+} row_job;
+
+static void *row_worker(void *p)
+{
+    row_job *j = (row_job *)p;
+    double *hd = (double *)malloc(sizeof(double) * (size_t)j->D);
+    double *z = (double *)malloc(sizeof(double) * (size_t)j->V);
+    if (!hd || !z) {
+        j->failed = 1;
+        free(hd);
+        free(z);
+        return NULL;
+    }
+    for (int64_t i = j->tid; i < j->R; i += j->nthreads) {
+        int64_t t = j->rows ? j->rows[i] : i;
+        oracle_row(j->h + t * j->D, j->W, j->targets[t], j->D, j->V, hd, z,
+                   j->out_logp + i, j->out_lse + i);
+    }
+    free(hd);
+    free(z);
+    return NULL;
+}
+
+/* Rows `rows[0..R)` of h (all N rows when rows == NULL, then R = N).
+ * h bf16 [N, D], W bf16 [V, D], targets int32 [N]; outputs double [R].
+ * Rows are spread over `nthreads` threads; each row is computed alone.
+ * Returns 0, or -1 on bad arguments / allocation failure. */
+int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *targets,
+                         const int64_t *rows, int64_t R, int64_t D, int64_t V,
+                         double *out_logp, double *out_lse, int nthreads)
+{
+    if (R < 0 || D <= 0 || V <= 0 || !h || !W || !targets || !out_logp || !out_lse)
+        return -1;
+    if (R == 0)
+        return 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > R)
+        nthreads = (int)R;
+    row_job *jobs = (row_job *)calloc((size_t)nthreads, sizeof(row_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -1;
+    }
+    int rc = 0;
+    for (int k = 0; k < nthreads; ++k) {
+        jobs[k] = (row_job){h, W, targets, rows, R, D, V, out_logp, out_lse, k, nthreads, 0};
+        if (pthread_create(&th[k], NULL, row_worker, &jobs[k]) != 0) {
+            row_worker(&jobs[k]); /* run inline if no thread could be made */
+            th[k] = 0;
+        }
+    }
+    for (int k = 0; k < nthreads; ++k) {
+        if (th[k])
+            pthread_join(th[k], NULL);
+        if (jobs[k].failed)
+            rc = -1;
+    }
+    free(jobs);
+    free(th);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ mismatch stats */
+
+enum { /* per-sequence record, in this order */
+    SQ_N_MASK, SQ_N_USED, SQ_N_NAN, SQ_N_CLIP, SQ_MEAN_DELTA, SQ_MEAN_ABS_DELTA,
+    SQ_MAX_ABS_DELTA, SQ_MEAN_K1, SQ_MEAN_K2, SQ_MEAN_K3, SQ_MEAN_W, SQ_MEAN_REL,
+    SQ_FIELDS
+};
+enum { /* batch record, in this order */
+    BT_N_MASK, BT_N_USED, BT_N_NAN, BT_N_CLIP, BT_MEAN_DELTA, BT_MEAN_ABS_DELTA,
+    BT_MAX_ABS_DELTA, BT_MEAN_K1, BT_MEAN_K2, BT_MEAN_K3, BT_MEAN_W, BT_MEAN_REL,
+    BT_SEQMEAN_K1, BT_SEQMEAN_K2, BT_SEQMEAN_K3, BT_CLIP_RATIO, BT_NAN_RATIO,
+    BT_REJECT_RATIO, BT_N_SEQS_NONEMPTY, BT_N_REJECTED, BT_FIELDS
+};
+
+int oracle_seq_fields(void) { return SQ_FIELDS; }
+int oracle_batch_fields(void) { return BT_FIELDS; }
+
+/* sum / count, or 0 for an empty set. */
+static double mean_or_zero(double sum, double count) { return count > 0 ? sum / count : 0.0; }
+
+/* Per-token quantities of the definition. */
+typedef struct {
+    int used, nan, clip;
+    double delta, k1, k2, k3, w, rel;
+} token_terms;
+
+static token_terms oracle_token(float l_tr, float l_ro, uint8_t mask, double C, double logC)
+{
+    token_terms q;
+    memset(&q, 0, sizeof q);
+    float d32 = l_tr - l_ro;                     /* device precision, decisions only */
+    int in = mask != 0;
+    int fin = isfinite(d32);
+    q.used = in && fin;
+    q.nan = in && !fin;
+    if (!q.used)
+        return q;
+    double d = (double)l_tr - (double)l_ro;      /* delta = log pi_train - log pi_rollout */
+    double log_r = d;                            /* r = e^delta, so log r = delta */
+    double r = exp(d);
+    double r_minus_1 = expm1(d);                 /* r - 1 without cancellation */
+    q.delta = d;
+    q.k1 = -log_r;
+    q.k2 = 0.5 * log_r * log_r;
+    q.k3 = r_minus_1 - log_r;
+    q.w = r < C ? r : C;                         /* truncated IS weight min(r, C) */
+    q.clip = (double)d32 > logC;                 /* r > C, decided on the fp32 delta */
+    q.rel = fabs(d) / (fabs((double)l_tr) + 1e-8);
+    return q;
+}
+
+/* logp_train, logp_rollout fp32 [N]; mask uint8 [N]; seq_offsets int32 [S+1].
+ * Outputs: token_weight double [N] (may be NULL), seq_stats double [S][SQ_FIELDS],
+ * seq_flags int32 [S], batch double [BT_FIELDS].
+ * Returns 0, or -1 on bad arguments / bad offsets. */
+int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                          const int32_t *seq_offsets, int32_t S, int64_t N, double C,
+                          double tau_seq, int32_t seq_estimator, double *token_weight,
+                          double *seq_stats, int32_t *seq_flags, double *batch)
+{
+    if (S < 0 || N < 0 || !(C > 0.0) || !seq_offsets || !batch)
+        return -1;
+    if (N > 0 && (!logp_train || !logp_rollout || !mask))
+        return -1;
+    if (S > 0 && (!seq_stats || !seq_flags))
+        return -1;
+    if (seq_estimator != 1 && seq_estimator != 3)
+        return -1;
+    if (seq_offsets[0] != 0 || (int64_t)seq_offsets[S] != N)
+        return -1;
+    for (int32_t s = 0; s < S; ++s)
+        if (seq_offsets[s + 1] < seq_offsets[s])
+            return -1;
+
+    const double logC = log(C);
+    const double tau = isnan(tau_seq) ? (C - 1.0) - logC : tau_seq;
+
+    if (token_weight)
+        for (int64_t t = 0; t < N; ++t)
+            token_weight[t] = 0.0;
+
+    /* batch totals, accumulated sequence by sequence in index order */
+    double b_mask = 0, b_used = 0, b_nan = 0, b_clip = 0;
+    double b_sd = 0, b_sad = 0, b_sk1 = 0, b_sk2 = 0, b_sk3 = 0, b_sw = 0, b_srel = 0, b_max = 0;
+    double b_mk1 = 0, b_mk2 = 0, b_mk3 = 0, b_nonempty = 0, b_rej = 0;
+
+    for (int32_t s = 0; s < S; ++s) {
+        double n_mask = 0, n_used = 0, n_nan = 0, n_clip = 0;
+        double sd = 0, sad = 0, sk1 = 0, sk2 = 0, sk3 = 0, sw = 0, srel = 0, mx = 0;
+        for (int64_t t = seq_offsets[s]; t < seq_offsets[s + 1]; ++t) {
+            token_terms q = oracle_token(logp_train[t], logp_rollout[t], mask[t], C, logC);
+            n_mask += mask[t] != 0;
+            n_nan += q.nan;
+            if (!q.used)
+                continue;
+            n_used += 1;
+            n_clip += q.clip;
+            sd += q.delta;
+            sad += fabs(q.delta);
+            sk1 += q.k1;
+            sk2 += q.k2;
+            sk3 += q.k3;
+            sw += q.w;
+            srel += q.rel;
+            if (fabs(q.delta) > mx)
+                mx = fabs(q.delta);
+            if (token_weight)
+                token_weight[t] = q.w;
+        }
+        double *o = seq_stats + (size_t)s * SQ_FIELDS;
+        o[SQ_N_MASK] = n_mask;
+        o[SQ_N_USED] = n_used;
+        o[SQ_N_NAN] = n_nan;
+        o[SQ_N_CLIP] = n_clip;
+        o[SQ_MAX_ABS_DELTA] = mx;
+        o[SQ_MEAN_DELTA] = mean_or_zero(sd, n_used);
+        o[SQ_MEAN_ABS_DELTA] = mean_or_zero(sad, n_used);
+        o[SQ_MEAN_K1] = mean_or_zero(sk1, n_used);
+        o[SQ_MEAN_K2] = mean_or_zero(sk2, n_used);
+        o[SQ_MEAN_K3] = mean_or_zero(sk3, n_used);
+        o[SQ_MEAN_W] = mean_or_zero(sw, n_used);
+        o[SQ_MEAN_REL] = mean_or_zero(srel, n_used);
+        int flag = 0;
+        if (n_used > 0) {
+            double stat = seq_estimator == 3 ? o[SQ_MEAN_K3] : fabs(o[SQ_MEAN_K1]);
+            flag = stat > tau;
+            b_nonempty += 1;
+            b_mk1 += o[SQ_MEAN_K1];
+            b_mk2 += o[SQ_MEAN_K2];
+            b_mk3 += o[SQ_MEAN_K3];
+            b_rej += flag;
+        }
+        seq_flags[s] = flag;
+
+        b_mask += n_mask;
+        b_used += n_used;
+        b_nan += n_nan;
+        b_clip += n_clip;
+        b_sd += sd;
+        b_sad += sad;
+        b_sk1 += sk1;
+        b_sk2 += sk2;
+        b_sk3 += sk3;
+        b_sw += sw;
+        b_srel += srel;
+        if (mx > b_max)
+            b_max = mx;
+    }
+
+    batch[BT_N_MASK] = b_mask;
+    batch[BT_N_USED] = b_used;
+    batch[BT_N_NAN] = b_nan;
+    batch[BT_N_CLIP] = b_clip;
+    batch[BT_MEAN_DELTA] = mean_or_zero(b_sd, b_used);
+    batch[BT_MEAN_ABS_DELTA] = mean_or_zero(b_sad, b_used);
+    batch[BT_MAX_ABS_DELTA] = b_max;
+    batch[BT_MEAN_K1] = mean_or_zero(b_sk1, b_used);
+    batch[BT_MEAN_K2] = mean_or_zero(b_sk2, b_used);
+    batch[BT_MEAN_K3] = mean_or_zero(b_sk3, b_used);
+    batch[BT_MEAN_W] = mean_or_zero(b_sw, b_used);
+    batch[BT_MEAN_REL] = mean_or_zero(b_srel, b_used);
+    batch[BT_SEQMEAN_K1] = mean_or_zero(b_mk1, b_nonempty);
+    batch[BT_SEQMEAN_K2] = mean_or_zero(b_mk2, b_nonempty);
+    batch[BT_SEQMEAN_K3] = mean_or_zero(b_mk3, b_nonempty);
+    batch[BT_CLIP_RATIO] = mean_or_zero(b_clip, b_mask);
+    batch[BT_NAN_RATIO] = mean_or_zero(b_nan, b_mask);
+    batch[BT_REJECT_RATIO] = mean_or_zero(b_rej, b_nonempty);
+    batch[BT_N_SEQS_NONEMPTY] = b_nonempty;
+    batch[BT_N_REJECTED] = b_rej;
+    return 0;
+}
