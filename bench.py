@@ -1,0 +1,435 @@
+"""Benchmark of the hot path: fused selected-token logprob + mismatch statistics.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+One step = tim_token_logprob over a Qwen3-8B-shaped LM head (N = 8192 tokens,
+D = 4096, V = 151936, bf16 operands, fp32 accumulation) followed by
+tim_mismatch_stats over its output against synthetic rollout logprobs (16
+sequences x 512 tokens, first 128 of each masked as prompt, C = 2).  The head
+weight (1.2 GB) is larger than L2, and L2 is also flushed (a 256 MiB write)
+before every timed step.  Steps are timed with CUDA events on the launching
+stream; the timed region is bracketed by a barrier and a device synchronise;
+the max over ranks is reported.  With --gpus N > 1 (under torchrun) every rank
+runs its own replica of the workload: the path shards by rows with no
+exchange, so value = N x tokens / max-rank time ("scaling": "weak").
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method) on the host cores over a bounded row sample of the same workload.
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused selected-token logprob tokens/s and TFLOP/s vs GB300 dense bf16 peak"
+UNIT = "tokens/s"
+WORKLOAD = "qwen3_8b"
+K2_BW_TOKENS = 1 << 27
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- dist helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+def make_workload(seed: int = 0):
+    cfg = wl.CONFIGS[WORKLOAD]
+    h, W = wl.draw_head(cfg, seed=seed)
+    a = wl.draw_targets(cfg, cfg.N, seed=seed)
+    off = wl.draw_segments(cfg, seed=seed)
+    mask = wl.draw_mask(cfg, off, seed=seed)
+    return cfg, h, W, a, off, mask
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(cfg, h, W, a, off, mask, budget_s: float, seed: int = 0):
+    """The oracle on a bounded sample: token logprob on R rows (all host
+    threads), mismatch statistics on the whole batch.  Returns (tokens/s,
+    description, threads, seconds spent)."""
+    import oracle
+    threads = cpu_threads()
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    probe_rows = rng.choice(cfg.N, size=min(cfg.N, threads), replace=False)
+    oracle.token_logprob(h, W, a, rows=probe_rows, nthreads=threads)
+    t_round = time.perf_counter() - t0          # one row on every thread
+    rounds = max(1, int(budget_s / max(t_round, 1e-3)))
+    R = min(cfg.N, rounds * threads)
+    rows = rng.choice(cfg.N, size=R, replace=False)
+    t0 = time.perf_counter()
+    lp, _ = oracle.token_logprob(h, W, a, rows=rows, nthreads=threads)
+    t_k1 = time.perf_counter() - t0
+    l_tr = np.full(cfg.N, -1.0, np.float32)
+    l_tr[rows] = lp.astype(np.float32)
+    l_ro = wl.draw_rollout(cfg, l_tr, seed=seed)
+    t0 = time.perf_counter()
+    oracle.mismatch_stats(l_tr, l_ro, mask, off, C=cfg.C)
+    t_k2 = time.perf_counter() - t0
+    sec_per_token = t_k1 / R + t_k2 / cfg.N
+    desc = ("token logprob on %d of %d rows (%d threads, %.1f s) + mismatch stats on all %d tokens "
+            "(1 thread, %.3f s), extrapolated to tokens/s" % (R, cfg.N, threads, t_k1, cfg.N, t_k2))
+    return 1.0 / sec_per_token, desc, threads, t_k1 + t_k2
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg, h, W, a, off, mask = make_workload()
+    budget = float(os.environ.get("TIM_BENCH_ORACLE_SECONDS", "8"))
+    vals = []
+    desc, threads = "", 1
+    for i in range(args.warmup + args.steps):
+        v, desc, threads, _ = time_oracle(cfg, h, W, a, off, mask, budget / max(1, args.steps), seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": cfg.N / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg):
+    return {"workload": "%s_head+mismatch" % cfg.name, "N": cfg.N, "D": cfg.D, "V": cfg.V,
+            "num_seqs": cfg.num_seqs, "seq_len": cfg.seq_len, "prompt_len": cfg.prompt_len, "C": cfg.C,
+            "operands": "bf16 h[N,D], bf16 W[V,D], fp32 accumulate",
+            "l2": "weights 1.2 GB > L2, and L2 flushed (256 MiB write) before each timed step"}
+
+
+# ----------------------------------------------------------------------------- gb300 arm
+def run_gb300(args):
+    import torch
+    import rollout_logprob_mismatch_gb300 as tim
+    from rollout_logprob_mismatch_gb300 import build as tim_build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = dist_init(world, "nccl")
+    if rank == 0 or dist is None:
+        tim_build.build()
+    barrier(dist, dev)
+    tim.load()
+    peaks = load_peaks()
+
+    cfg, h, W, a, off, mask = make_workload(seed=rank)
+    N, D, V = cfg.N, cfg.D, cfg.V
+    stream = torch.cuda.current_stream(dev)
+    hd = torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16)
+    Wd = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    ad = torch.from_numpy(a).to(dev)
+    offd = torch.from_numpy(off).to(dev)
+    maskd = torch.from_numpy(mask).to(dev)
+    lp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    # rollout logprobs = trainer logprobs + N(0, 0.01^2), drawn once from a first pass
+    tim.token_logprob(hd, Wd, ad, lp, lse)
+    l_ro = wl.draw_rollout(cfg, lp.cpu().numpy(), seed=rank)
+    rod = torch.from_numpy(l_ro).to(dev)
+    S = len(off) - 1
+    k2out = {"seq_stats": torch.empty((S, 12), dtype=torch.float32, device=dev),
+             "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
+             "batch": torch.empty(20, dtype=torch.float64, device=dev), "token_weight": None}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        tim.token_logprob(hd, Wd, ad, lp, lse)
+        tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    tim.check()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            tim.token_logprob(hd, Wd, ad, lp, lse)
+            ev[i][1].record(stream)
+            tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    tim.check()
+    t_k1 = [ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(K)]
+    t_k2 = [ev[i][1].elapsed_time(ev[i][2]) * 1e-3 for i in range(K)]
+    t_step = sum(t_k1) + sum(t_k2)
+    t_max = max_over_ranks(t_step, dist, dev)
+    value = world * N * K / t_max
+    k1_avg = float(np.mean(t_k1))
+    k2_avg = float(np.mean(t_k2))
+    flops = 2.0 * N * V * D
+    achieved = flops / k1_avg / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    h_host = torch.from_numpy(h.view(np.int16)).pin_memory()
+    a_host = torch.from_numpy(a).pin_memory()
+    ro_host = torch.from_numpy(l_ro).pin_memory()
+    m_host = torch.from_numpy(mask).pin_memory()
+    o_host = torch.from_numpy(off).pin_memory()
+    b_host = torch.empty(20, dtype=torch.float64).pin_memory()
+    s_host = torch.empty((S, 12), dtype=torch.float32).pin_memory()
+    f_host = torch.empty(S, dtype=torch.int32).pin_memory()
+    h_in = torch.empty((N, D), dtype=torch.int16, device=dev)
+    a_in = torch.empty(N, dtype=torch.int32, device=dev)
+    ro_in = torch.empty(N, dtype=torch.float32, device=dev)
+    m_in = torch.empty(N, dtype=torch.uint8, device=dev)
+    o_in = torch.empty(S + 1, dtype=torch.int32, device=dev)
+
+    def e2e_step():
+        h_in.copy_(h_host, non_blocking=True)
+        a_in.copy_(a_host, non_blocking=True)
+        ro_in.copy_(ro_host, non_blocking=True)
+        m_in.copy_(m_host, non_blocking=True)
+        o_in.copy_(o_host, non_blocking=True)
+        tim.token_logprob(h_in.view(torch.bfloat16), Wd, a_in, lp, lse)
+        tim.mismatch_stats(lp, ro_in, m_in, o_in, C=cfg.C, out=k2out)
+        b_host.copy_(k2out["batch"], non_blocking=True)
+        s_host.copy_(k2out["seq_stats"], non_blocking=True)
+        f_host.copy_(k2out["seq_flags"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    barrier(dist, dev)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = sum(e2e_ev[i][0].elapsed_time(e2e_ev[i][1]) * 1e-3 for i in range(K))
+    t_e2e = max_over_ranks(t_e2e, dist, dev)
+    h2d = h_host.numel() * 2 + a_host.numel() * 4 + ro_host.numel() * 4 + m_host.numel() + o_host.numel() * 4
+    d2h = b_host.numel() * 8 + s_host.numel() * 4 + f_host.numel() * 4
+
+    k2_bw = mismatch_bandwidth(tim, dev, stream, peaks, args) if not args.skip_k2_bandwidth else None
+    tim.check()
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        v, desc, threads, _ = time_oracle(cfg, h, W, a, off, mask,
+                                          float(os.environ.get("TIM_BENCH_ORACLE_SECONDS", "12")))
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(cfg),
+        "tflops": world * flops * K / t_max / 1e12,
+        "roofline": {"kernel": "tim_token_logprob (fused LM head + online LSE + gather)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": "%s bf16 burst" % peaks["source"],
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": k1_avg * 1e3},
+        "mismatch_pass": {"avg_launch_us": k2_avg * 1e6,
+                          "algorithmic_bytes": 9 * N + 4 * (S + 1) + 52 * S + 160},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * N * K / t_e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+    }
+    if k2_bw is not None:
+        line["mismatch_bandwidth"] = k2_bw
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def mismatch_bandwidth(tim, dev, stream, peaks, args):
+    """tim_mismatch_stats alone on 2^27 tokens in Llama-like segments (lognormal
+    lengths, median 1024, clipped to [128, 4096]), 30% masked, with per-token
+    weights written; L2 flushed before each launch.  Reports HBM GB/s."""
+    import torch
+    Nt = K2_BW_TOKENS
+    cfg = wl.HeadConfig("bw", N=Nt, D=8, V=8, seq_layout="lognormal", mask_drop=0.3)
+    off = wl.draw_segments(cfg, seed=7)
+    S = len(off) - 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    l_tr = torch.log(torch.rand(Nt, device=dev, generator=g).clamp_min_(1e-30))
+    l_ro = l_tr + 0.02 * torch.randn(Nt, device=dev, generator=g)
+    mask = (torch.rand(Nt, device=dev, generator=g) >= 0.3).to(torch.uint8)
+    offd = torch.from_numpy(off).to(dev)
+    out = {"seq_stats": torch.empty((S, 12), dtype=torch.float32, device=dev),
+           "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
+           "batch": torch.empty(20, dtype=torch.float64, device=dev),
+           "token_weight": torch.empty(Nt, dtype=torch.float32, device=dev)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        tim.mismatch_stats(l_tr, l_ro, mask, offd, out=out)
+    reps = 10
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        flush.fill_(i)
+        ev[i][0].record(stream)
+        tim.mismatch_stats(l_tr, l_ro, mask, offd, out=out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
+    algo = 9 * Nt + 4 * Nt + 4 * (S + 1) + 52 * S + 160
+    gbs = algo / t / 1e9
+    return {"tokens": Nt, "num_seqs": S, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo,
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "frac_of_8000": gbs / 8000.0, "bound": "hbm"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-k2-bandwidth", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+/*
+ * tim.h -- C ABI of the GB300 (sm_103a) train/rollout logprob-mismatch library
+ * (libtim.so).
+ *
+ * Two calls make up the hot path of a trainer's mismatch check:
+ *
+ *   tim_token_logprob   the trainer-side selected-token log-probability
+ *                       l_t = log softmax(h_t W^T)[a_t], computed as one fused
+ *                       pass (bf16 x bf16 -> fp32 LM head, online
+ *                       log-sum-exp over the vocabulary, gather at the target
+ *                       id) that never writes the [N, V] logits to memory;
+ *   tim_mismatch_stats  the segmented pass that scores l_train against the
+ *                       rollout engine's logprobs: delta, r, k1/k2/k3, the
+ *                       truncated importance weight and masked per-sequence /
+ *                       per-batch means with a sequence rejection flag.
+ *
+ * Determinism and batch invariance.  Every reduction runs in an order fixed by
+ * D and V (token logprob) or by a token's index inside its own sequence
+ * (mismatch statistics); no split depends on N, S or on where a row or a
+ * sequence sits in the batch.  A row's outputs, and a sequence's record, are
+ * bit-identical whatever else is in the batch, and from run to run.
+ *
+ * Conventions for every call:
+ *  - all array arguments are caller-owned DEVICE pointers of the current CUDA
+ *    device; nothing is retained after the call returns;
+ *  - calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream); a non-zero return means nothing was launched and the outputs are
+ *    untouched;
+ *  - host-side argument errors return TIM_ERR_INVALID_ARG; a device that is
+ *    not sm_103 returns TIM_ERR_UNSUPPORTED_DEVICE; a failing CUDA runtime call
+ *    returns TIM_ERR_CUDA; tim_last_error() gives a message for the calling
+ *    thread;
+ *  - bad DATA found on the device (bad sequence offsets; a pipeline wait that
+ *    ran out of time) never traps: the kernel records a status word that
+ *    tim_check() returns, and writes NaN into the affected outputs.
+ */
+#ifndef TIM_H
+#define TIM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TIM_API __attribute__((visibility("default")))
+#else
+#define TIM_API
+#endif
+
+/* Same object as cudaStream_t; declared here so that this header needs no CUDA header. */
+typedef struct CUstream_st *tim_stream_t;
+
+typedef enum {
+    TIM_OK = 0,
+    TIM_ERR_INVALID_ARG = -1,        /* host-side argument check failed */
+    TIM_ERR_UNSUPPORTED_DEVICE = -2, /* current device is not sm_103 (GB300) */
+    TIM_ERR_CUDA = -3,               /* a CUDA runtime call failed */
+    TIM_ERR_TIMEOUT = -4,            /* a pipeline wait inside a kernel ran out of time */
+    TIM_ERR_BAD_INPUT = -5           /* the device found bad data (sequence offsets) */
+} tim_status;
+
+/* ------------------------------------------------------------------ token logprob
+ *
+ * l_t = log softmax(h_t W^T)[a_t] and lse_t = log sum_v exp(h_t . W_v).
+ *
+ * Defined by the icarus page "RL: Training Inference Mismatch", section "log p"
+ * (final hidden states -> LM head -> log-softmax -> gather at the token id, and
+ * its PyTorch statement log_softmax(logits, -1).gather(-1, ids)); the head is
+ * kept above bf16 precision as in LoongSage "Train-Inference Consistency"
+ * section 3 "FP32 LM head" -- here as bf16 operands with fp32 accumulation.
+ * The pages' head has a bias; this call has none.  Temperature is 1 (raw
+ * logits, icarus section "logits processor").  Batch invariance and fixed
+ * reduction order: llm-infra-atlas "训推一致性与 determinism" sections 1.2 and 6.
+ *
+ *   h        bf16 [N, D] row-major (final hidden states), 16-byte aligned
+ *   W        bf16 [V, D] row-major (LM-head weight, one row per vocabulary id),
+ *            16-byte aligned
+ *   targets  int32 [N]: a_t, already shifted by the caller so that row t of h
+ *            predicts targets[t] (icarus section "shift and mask"); an id
+ *            outside [0, V) (e.g. the -100 ignore label) gives out_logp = NaN
+ *   N        rows, N >= 0 (N = 0 is a no-op returning TIM_OK), N < 2^31
+ *   D        hidden size, D > 0 and D % 8 == 0 (16-byte row stride), D <= 65536
+ *   V        vocabulary size, 0 < V < 2^31
+ *   out_logp fp32 [N]: l_t in nats
+ *   out_lse  fp32 [N]: log-sum-exp of the raw logits, in nats
+ *
+ * Scratch: the call takes a split-V workspace of about 8 * N * ceil(V / 1024)
+ * bytes from a stream-ordered memory pool of its own (cudaMallocFromPoolAsync
+ * on `stream`) and gives it back on the same stream; the pool keeps the memory
+ * for the next call.  Tolerance against an fp64 evaluation of the definition:
+ * a few 1e-6 absolute on l_t and lse for the pages' head shapes.
+ */
+TIM_API int tim_token_logprob(const void *h, const void *W, const int32_t *targets,
+                      int64_t N, int64_t D, int64_t V,
+                      float *out_logp, float *out_lse, tim_stream_t stream);
+
+/* ------------------------------------------------------------------ mismatch stats
+ *
+ * Per token t with mask_t != 0 (VeXact summary eq. (1); llm-infra-atlas
+ * section 2; icarus KL-estimator table; LoongSage sections 4-5):
+ *   delta = l_train - l_rollout,  r = e^delta,
+ *   k1 = -log r,  k2 = (log r)^2 / 2,  k3 = (r - 1) - log r,
+ *   w = min(r, C)  (truncated importance weight; 0 for tokens not used),
+ *   clip = r > C,  rel = |delta| / (|l_train| + 1e-8).
+ * A token is "used" when mask != 0 and delta is finite; a masked-in token with a
+ * non-finite delta is counted as nan and left out of every mean.
+ * Per sequence s (tokens seq_offsets[s] .. seq_offsets[s+1]-1): means over its
+ * used tokens, then the rejection flag (VeXact "Algorithmic TIM Compensation"):
+ *   estimator 3: mean k3 > tau_seq;  estimator 1: |mean k1| > tau_seq.
+ * Per batch: token means over all used tokens, the mean over non-empty sequences
+ * of the per-sequence means (icarus monitoring steps 2-3), clip / nan ratios
+ * over masked-in tokens and the rejected fraction of non-empty sequences.
+ * A sequence with no used token has all means 0 and flag 0.
+ */
+#define TIM_SEQ_FIELDS 12
+enum tim_seq_field {
+    TIM_SEQ_N_MASK = 0,        /* masked-in tokens */
+    TIM_SEQ_N_USED,            /* masked-in tokens with finite delta */
+    TIM_SEQ_N_NAN,             /* masked-in tokens with non-finite delta */
+    TIM_SEQ_N_CLIP,            /* used tokens with r > C */
+    TIM_SEQ_MEAN_DELTA,
+    TIM_SEQ_MEAN_ABS_DELTA,
+    TIM_SEQ_MAX_ABS_DELTA,
+    TIM_SEQ_MEAN_K1,
+    TIM_SEQ_MEAN_K2,
+    TIM_SEQ_MEAN_K3,
+    TIM_SEQ_MEAN_W,
+    TIM_SEQ_MEAN_REL
+};
+
+#define TIM_BATCH_FIELDS 20
+enum tim_batch_field {
+    TIM_BATCH_N_MASK = 0,
+    TIM_BATCH_N_USED,
+    TIM_BATCH_N_NAN,
+    TIM_BATCH_N_CLIP,
+    TIM_BATCH_MEAN_DELTA,      /* token means over all used tokens ... */
+    TIM_BATCH_MEAN_ABS_DELTA,
+    TIM_BATCH_MAX_ABS_DELTA,
+    TIM_BATCH_MEAN_K1,
+    TIM_BATCH_MEAN_K2,
+    TIM_BATCH_MEAN_K3,         /* is_approx_k3_kl */
+    TIM_BATCH_MEAN_W,
+    TIM_BATCH_MEAN_REL,        /* consistency_rel_diff */
+    TIM_BATCH_SEQMEAN_K1,      /* mean over non-empty sequences of the sequence means */
+    TIM_BATCH_SEQMEAN_K2,
+    TIM_BATCH_SEQMEAN_K3,
+    TIM_BATCH_CLIP_RATIO,      /* n_clip / n_mask (is_clip_ratio) */
+    TIM_BATCH_NAN_RATIO,       /* n_nan / n_mask (is_nan_ratio) */
+    TIM_BATCH_REJECT_RATIO,    /* rejected / non-empty sequences */
+    TIM_BATCH_N_SEQS_NONEMPTY,
+    TIM_BATCH_N_REJECTED
+};
+
+/* Sizes and outputs of tim_mismatch_stats.  The struct lives in host memory;
+ * the pointers in it are device pointers.  It carries N and S so that the host
+ * never has to read seq_offsets back from the device. */
+typedef struct {
+    int32_t num_seqs;        /* in: S >= 0 (S = 0: only batch_stats is written, all 0) */
+    int64_t num_tokens;      /* in: N >= 0; must equal seq_offsets[S] (checked on device) */
+    float tau_seq;           /* in: rejection threshold; NaN selects (C - 1) - ln C,
+                                k3 at r = C (a reading: the pages give no value) */
+    int32_t seq_estimator;   /* in: 3 = K3 (default when 0), 1 = |K1| */
+    float *token_weight;     /* out, optional (NULL = not written): fp32 [N], w_t */
+    float *seq_stats;        /* out: fp32 [S][TIM_SEQ_FIELDS] */
+    int32_t *seq_flags;      /* out: int32 [S], 1 = rejected */
+    double *batch_stats;     /* out: fp64 [TIM_BATCH_FIELDS] */
+} tim_mismatch_out;
+
+/*   logp_train, logp_rollout  fp32 [N]
+ *   mask                      uint8 [N]: 0 = not counted (prompt / padding), else counted
+ *   seq_offsets               int32 [S + 1]: seq_offsets[0] = 0, non-decreasing,
+ *                             seq_offsets[S] = N (sequences packed back to back)
+ *   C                         truncation cap of the importance weight, C > 0, finite
+ *   out                       host struct described above
+ * Bad offsets found on the device set TIM_ERR_BAD_INPUT (see tim_check) and
+ * make every output NaN for the affected sequences and for the batch record.
+ * Scratch: about 128 * S bytes from the library's stream-ordered pool. */
+TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollout,
+                       const uint8_t *mask, const int32_t *seq_offsets, float C,
+                       const tim_mismatch_out *out, tim_stream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronises `stream`, then returns and clears the status word the kernels
+ * of the current device recorded since the last tim_check (TIM_OK if none). */
+TIM_API int tim_check(tim_stream_t stream);
+
+/* Message for the last non-OK return on the calling thread ("" if none). */
+TIM_API const char *tim_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+TIM_API int tim_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIM_H */

@@ -1,0 +1,227 @@
+"""GB300 (sm_103a) fused selected-token logprob and train/rollout mismatch statistics.
+
+A thin ctypes binding over ``libtim.so`` (C ABI in ``include/tim.h``).  The
+functions named like the C entry points (``tim_token_logprob``,
+``tim_mismatch_stats``, ``tim_check``) take raw device pointers and sizes;
+``token_logprob`` and ``mismatch_stats`` take torch CUDA tensors and only
+marshal them.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU fallback: if ``libtim.so`` is missing, importing the
+binding succeeds but every call raises ``TimError``.
+
+Method: the trainer recomputes l_t = log softmax(h_t W^T)[a_t] from its final
+hidden states (icarus "RL: Training Inference Mismatch", section "log p") and
+compares it with the rollout engine's logprob through delta = l_train -
+l_rollout, r = e^delta, the k1/k2/k3 KL estimators, the truncated importance
+weight min(r, C) and masked per-sequence / per-batch means with a sequence
+rejection flag (VeXact summary, eq. (1) and "Algorithmic TIM Compensation";
+LoongSage "Train-Inference Consistency", sections 4-5).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "tim_mismatch_out", "lib_path", "load",
+    "tim_token_logprob", "tim_mismatch_stats", "tim_check", "tim_last_error", "tim_version",
+    "token_logprob", "mismatch_stats", "check",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libtim.so")
+
+TIM_OK = 0
+TIM_ERR_INVALID_ARG = -1
+TIM_ERR_UNSUPPORTED_DEVICE = -2
+TIM_ERR_CUDA = -3
+TIM_ERR_TIMEOUT = -4
+TIM_ERR_BAD_INPUT = -5
+
+SEQ_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
+              "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel")
+BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
+                "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel",
+                "seqmean_k1", "seqmean_k2", "seqmean_k3", "clip_ratio", "nan_ratio",
+                "reject_ratio", "n_seqs_nonempty", "n_rejected")
+
+
+class TimError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("tim error %d: %s" % (code, msg))
+        self.code = code
+
+
+class tim_mismatch_out(ctypes.Structure):
+    """Mirror of the C struct tim_mismatch_out (host struct of device pointers)."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("num_tokens", ctypes.c_int64),
+        ("tau_seq", ctypes.c_float),
+        ("seq_estimator", ctypes.c_int32),
+        ("token_weight", ctypes.c_void_p),
+        ("seq_stats", ctypes.c_void_p),
+        ("seq_flags", ctypes.c_void_p),
+        ("batch_stats", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """The loaded libtim.so; raises TimError when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise TimError(TIM_ERR_CUDA, "libtim.so is not built (%s); run "
+                               "`python -m rollout_logprob_mismatch_gb300.build`" % _LIB_PATH)
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I64 = ctypes.c_void_p, ctypes.c_int64
+            lib.tim_token_logprob.argtypes = [P, P, P, I64, I64, I64, P, P, P]
+            lib.tim_token_logprob.restype = ctypes.c_int
+            lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
+                                               ctypes.POINTER(tim_mismatch_out), P]
+            lib.tim_mismatch_stats.restype = ctypes.c_int
+            lib.tim_check.argtypes = [P]
+            lib.tim_check.restype = ctypes.c_int
+            lib.tim_last_error.argtypes = []
+            lib.tim_last_error.restype = ctypes.c_char_p
+            lib.tim_version.argtypes = []
+            lib.tim_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+# ----------------------------------------------------------------------------- raw C ABI
+def tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream) -> int:
+    """C ABI call with integer device addresses; returns the tim_status code."""
+    return load().tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream)
+
+
+def tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C, out: tim_mismatch_out,
+                       stream) -> int:
+    return load().tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, float(C),
+                                     ctypes.byref(out), stream)
+
+
+def tim_check(stream) -> int:
+    return load().tim_check(stream)
+
+
+def tim_last_error() -> str:
+    return load().tim_last_error().decode(errors="replace")
+
+
+def tim_version() -> int:
+    return load().tim_version()
+
+
+def _raise_if(rc: int):
+    if rc != TIM_OK:
+        raise TimError(rc, tim_last_error())
+
+
+# ----------------------------------------------------------------------------- torch wrappers
+def _stream_handle(stream, device):
+    import torch
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, name, dtype, ndim, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != ndim:
+        raise ValueError("%s must be %d-D" % (name, ndim))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None):
+    """(logp [N] fp32, lse [N] fp32) for bf16 h [N, D], bf16 W [V, D], int32 targets [N]."""
+    import torch
+    _need(h, "h", torch.bfloat16, 2)
+    dev = h.device
+    _need(W, "W", torch.bfloat16, 2, dev)
+    _need(targets, "targets", torch.int32, 1, dev)
+    N, D = h.shape
+    V = W.shape[0]
+    if W.shape[1] != D or targets.shape[0] != N:
+        raise ValueError("shape mismatch: h %s, W %s, targets %s" % (tuple(h.shape), tuple(W.shape),
+                                                                       tuple(targets.shape)))
+    if out_logp is None:
+        out_logp = torch.empty(N, dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(N, dtype=torch.float32, device=dev)
+    _need(out_logp, "out_logp", torch.float32, 1, dev)
+    _need(out_lse, "out_lse", torch.float32, 1, dev)
+    with torch.cuda.device(dev):
+        rc = tim_token_logprob(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
+                               out_logp.data_ptr(), out_lse.data_ptr(), _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out_logp, out_lse
+
+
+def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
+                   tau_seq: float = math.nan, seq_estimator: int = 3, token_weight: bool = False,
+                   stream=None, out=None):
+    """Mismatch statistics of packed sequences.
+
+    logp_train, logp_rollout fp32 [N]; mask bool/uint8 [N]; seq_offsets int32 [S + 1].
+    Returns a dict: seq_stats fp32 [S, 12] (SEQ_FIELDS), seq_flags int32 [S],
+    batch fp64 [20] (BATCH_FIELDS), token_weight fp32 [N] or None.
+    """
+    import torch
+    _need(logp_train, "logp_train", torch.float32, 1)
+    dev = logp_train.device
+    _need(logp_rollout, "logp_rollout", torch.float32, 1, dev)
+    _need(mask, "mask", (torch.uint8, torch.bool), 1, dev)
+    _need(seq_offsets, "seq_offsets", torch.int32, 1, dev)
+    N = logp_train.shape[0]
+    S = seq_offsets.shape[0] - 1
+    if logp_rollout.shape[0] != N or mask.shape[0] != N or S < 0:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = {
+            "seq_stats": torch.empty((S, len(SEQ_FIELDS)), dtype=torch.float32, device=dev),
+            "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
+            "batch": torch.empty(len(BATCH_FIELDS), dtype=torch.float64, device=dev),
+            "token_weight": torch.empty(N, dtype=torch.float32, device=dev) if token_weight else None,
+        }
+    d = tim_mismatch_out()
+    d.num_seqs = S
+    d.num_tokens = N
+    d.tau_seq = float(tau_seq)
+    d.seq_estimator = int(seq_estimator)
+    d.token_weight = out["token_weight"].data_ptr() if out.get("token_weight") is not None else None
+    d.seq_stats = out["seq_stats"].data_ptr()
+    d.seq_flags = out["seq_flags"].data_ptr()
+    d.batch_stats = out["batch"].data_ptr()
+    with torch.cuda.device(dev):
+        rc = tim_mismatch_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(),
+                                seq_offsets.data_ptr(), C, d, _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out
+
+
+def check(stream=None, device=None):
+    """Synchronises the stream and raises TimError if a kernel recorded a status."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _raise_if(tim_check(_stream_handle(stream, dev)))

@@ -1,0 +1,350 @@
+// k1_token_logprob.cu -- fused selected-token logprob for sm_103a.
+//
+// l_t = z_t[a_t] - log sum_v exp(z_t[v]),  z_t = h_t W^T   (icarus "RL: Training
+// Inference Mismatch", section "log p"; LoongSage "Train-Inference Consistency"
+// section 3, FP32 LM head: here bf16 operands with fp32 accumulation).
+//
+// One persistent CTA per SM walks work units (m-tile of 128 tokens, vocabulary
+// chunk of 1024 ids).  Per unit and 256-column tile:
+//   warp 0     TMA: h tile [128 x 64] and W tile [256 x 64] per k-block, 128-byte
+//              swizzle, into a 4-stage shared-memory ring;
+//   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
+//              into one of two TMEM accumulators (2 x 256 columns), k ascending;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
+//              token row) per thread, an online max / sum-of-exp over the columns
+//              in ascending order, and the target logit picked from the exact
+//              accumulator value.  The [N, V] logits never leave the SM.
+// Each unit writes its chunk's (max, sum) per row; a second small kernel folds
+// the chunks of a row in chunk order.  The split is a function of V alone and
+// every row is reduced in the same order whatever the batch holds, so a row's
+// outputs are bit-identical across batch sizes and compositions (llm-infra-atlas
+// "训推一致性与 determinism", sections 1.2 and 6: batch-invariant GEMM with a
+// fixed reduction order).
+#include "tim_internal.h"
+#include "tim_ptx.cuh"
+#include "../../include/tim.h"
+
+namespace tim {
+namespace {
+
+constexpr uint32_t IDESC = idesc_bf16_f32(K1_BM, K1_BN);
+constexpr uint32_t TMEM_COLS = 2 * K1_BN;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int SUBCOLS = 32;
+
+struct Unit {
+    int mt, ch;
+};
+
+// Units run m-tile fastest inside a band of `band` m-tiles, so the CTAs that are
+// resident together share the same W chunk (read once from HBM, then from L2)
+// while the band's h rows stay in L2.  The order affects speed only.
+__device__ __forceinline__ Unit unit_of(int u, const K1Args &a)
+{
+    const int per_band = a.band * a.num_chunks;
+    const int b = u / per_band;
+    const int rem = u - b * per_band;
+    const int m0 = b * a.band;
+    const int mb = min(a.band, a.num_m_tiles - m0);
+    Unit r;
+    r.ch = rem / mb;
+    r.mt = m0 + (rem - r.ch * mb);
+    return r;
+}
+
+__device__ __forceinline__ int tiles_in_chunk(int ch, int V)
+{
+    const int lo = ch * K1_VCHUNK;
+    const int hi = min(V, lo + K1_VCHUNK);
+    return (hi - lo + K1_BN - 1) / K1_BN;
+}
+
+// Bounded wait that ignores the abort flag: used only to drain in-flight
+// asynchronous work before the CTA releases its shared memory and TMEM.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns)
+{
+    if (mbar_try(bar, parity))
+        return;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(bar, parity))
+        if (global_ns() - t0 > budget_ns)
+            return;
+}
+
+__global__ void __launch_bounds__(K1_THREADS, 1)
+    k1_main_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                   const K1Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + K1_STAGES * K1_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K1_STAGES * K1_STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (K1_STAGES + s); };
+    auto tfull = [&](int b) { return bar0 + 8u * (2 * K1_STAGES + b); };
+    auto tempty = [&](int b) { return bar0 + 8u * (2 * K1_STAGES + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * K1_STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * K1_STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < K1_STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_h);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int KB = (a.D + K1_BK - 1) / K1_BK;
+    const uint64_t budget = a.wait_budget_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            const uint64_t pol_h = l2_policy_evict_last();
+            const uint64_t pol_w = l2_policy_evict_normal();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+                const Unit w = unit_of(u, a);
+                const int nt = tiles_in_chunk(w.ch, a.V);
+                for (int j = 0; ok && j < nt; ++j) {
+                    const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full(stage), K1_STAGE_BYTES);
+                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kb * K1_BK,
+                                    w.mt * K1_BM, pol_h);
+                        tma_load_2d(sB + stage * K1_B_BYTES, &tmap_w, full(stage), kb * K1_BK, v0,
+                                    pol_w);
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == K1_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // no TMA write may still be landing in shared memory when the CTA exits
+            for (int s = 0; s < K1_STAGES; ++s)
+                if (issued & (1u << s))
+                    drain_wait(full(s), (last_par >> s) & 1u, budget);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ UMMA issuer
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+                const Unit w = unit_of(u, a);
+                const int nt = tiles_in_chunk(w.ch, a.V);
+                for (int j = 0; ok && j < nt; ++j) {
+                    if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag, budget)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(acc * K1_BN);
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!mbar_wait(full(stage), phase, abort_flag, budget)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = sdesc_kmajor_sw128(sA + stage * K1_A_BYTES);
+                        const uint64_t bd = sdesc_kmajor_sw128(sB + stage * K1_B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < K1_BK / 16; ++k)   // +32 bytes along K per step
+                            umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
+                        umma_commit(empty(stage));
+                        if (++stage == K1_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(tfull(acc));
+                    acc ^= 1;
+                    if (acc == 0)
+                        acc_phase ^= 1u;
+                }
+            }
+            // every UMMA issued has finished before TMEM is released
+            umma_commit(drain);
+            drain_wait(drain, 0, budget);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue, warps 2..5
+        const int q = warp & 3;                 // TMEM lane quarter this warp may read
+        const int r_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+            const Unit w = unit_of(u, a);
+            const int nt = tiles_in_chunk(w.ch, a.V);
+            const int row = w.mt * K1_BM + r_in_tile;
+            const int tgt = row < a.N ? __ldg(a.targets + row) : -1;
+            float run_m = -INFINITY, run_s = 0.f, zt = 0.f;
+            bool found = false;
+            for (int j = 0; j < nt; ++j) {
+                if (!mbar_wait(tfull(acc), acc_phase, abort_flag, budget)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int c0 = w.ch * K1_VCHUNK + j * K1_BN;
+                const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * K1_BN);
+#pragma unroll 1
+                for (int sc = 0; sc < K1_BN / SUBCOLS; ++sc) {
+                    const int col0 = c0 + sc * SUBCOLS;
+                    if (col0 >= a.V)
+                        break;
+                    float v[SUBCOLS];
+                    __syncwarp();   // tcgen05.ld is .sync.aligned: the warp must be converged
+                    tmem_load32(tb + static_cast<uint32_t>(sc * SUBCOLS), v);
+                    if (col0 + SUBCOLS > a.V) {
+#pragma unroll
+                        for (int jj = 0; jj < SUBCOLS; ++jj)
+                            if (col0 + jj >= a.V)
+                                v[jj] = -INFINITY;
+                    }
+                    float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+#pragma unroll
+                    for (int jj = 4; jj < SUBCOLS; jj += 4) {
+                        m0 = fmaxf(m0, v[jj]);
+                        m1 = fmaxf(m1, v[jj + 1]);
+                        m2 = fmaxf(m2, v[jj + 2]);
+                        m3 = fmaxf(m3, v[jj + 3]);
+                    }
+                    const float new_m = fmaxf(run_m, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+                    const float nm = new_m * LOG2E;
+                    const float rescale = ex2(fmaf(run_m, LOG2E, -nm));
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < SUBCOLS; jj += 4) {
+                        s0 += ex2(fmaf(v[jj], LOG2E, -nm));
+                        s1 += ex2(fmaf(v[jj + 1], LOG2E, -nm));
+                        s2 += ex2(fmaf(v[jj + 2], LOG2E, -nm));
+                        s3 += ex2(fmaf(v[jj + 3], LOG2E, -nm));
+                    }
+                    run_s = fmaf(run_s, rescale, (s0 + s1) + (s2 + s3));
+                    run_m = new_m;
+                    const unsigned off = static_cast<unsigned>(tgt - col0);
+                    if (off < static_cast<unsigned>(SUBCOLS)) {
+#pragma unroll
+                        for (int jj = 0; jj < SUBCOLS; ++jj)
+                            if (off == static_cast<unsigned>(jj))
+                                zt = v[jj];
+                        found = true;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty(acc));
+                acc ^= 1;
+                if (acc == 0)
+                    acc_phase ^= 1u;
+            }
+            if (!ok)
+                break;
+            if (row < a.N) {
+                a.part[static_cast<size_t>(w.ch) * a.N + row] = make_float2(run_m, run_s);
+                if (found)
+                    a.za[row] = zt;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
+}
+
+// Folds the per-chunk (max, sum) pairs of a row in chunk order:
+// M = max_c m_c, S = sum_c s_c e^(m_c - M), lse = M + ln S, l = z_a - lse.
+__global__ void __launch_bounds__(256)
+    k1_combine_kernel(const float2 *__restrict__ part, const float *__restrict__ za,
+                      const int32_t *__restrict__ targets, int32_t N, int32_t V, int32_t num_chunks,
+                      float *__restrict__ out_logp, float *__restrict__ out_lse)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= N)
+        return;
+    float M = -INFINITY;
+    for (int c = 0; c < num_chunks; ++c)
+        M = fmaxf(M, part[static_cast<size_t>(c) * N + t].x);
+    float S = 0.f;
+    for (int c = 0; c < num_chunks; ++c) {
+        const float2 p = part[static_cast<size_t>(c) * N + t];
+        S = fmaf(p.y, expf(p.x - M), S);
+    }
+    const float lse = M + logf(S);
+    out_lse[t] = lse;
+    const int a = targets[t];
+    out_logp[t] = (a >= 0 && a < V) ? za[t] - lse : __int_as_float(0x7fc00000);
+}
+
+} // namespace
+
+cudaError_t k1_prepare_device()
+{
+    return cudaFuncSetAttribute(k1_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(K1_SMEM_BYTES));
+}
+
+cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
+                           int grid, cudaStream_t stream)
+{
+    k1_main_kernel<<<grid, K1_THREADS, K1_SMEM_BYTES, stream>>>(tmap_h, tmap_w, a);
+    return cudaGetLastError();
+}
+
+cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
+                              int32_t N, int32_t V, int32_t num_chunks, float *out_logp,
+                              float *out_lse, cudaStream_t stream)
+{
+    const int threads = 256;
+    const int blocks = (N + threads - 1) / threads;
+    k1_combine_kernel<<<blocks, threads, 0, stream>>>(part, za, targets, N, V, num_chunks, out_logp,
+                                                      out_lse);
+    return cudaGetLastError();
+}
+
+} // namespace tim

@@ -1,0 +1,317 @@
+// tim_api.cu -- the C ABI declared in include/tim.h: argument checks, per-device
+// set-up (sm_103 check, memory pool, tensor-map encoder), workspace, launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/tim.h"
+#include "tim_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 100;   // 0.1.0
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(TIM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Status word written by the kernels of this library (first error wins).
+__device__ int g_status;
+
+struct DeviceState {
+    bool ready = false;
+    int status_code = TIM_OK;   // why the device is unusable, if it is
+    int sms = 0;
+    int *status = nullptr;      // device address of g_status
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+uint64_t wait_budget_ns()
+{
+    static const uint64_t v = [] {
+        const char *s = std::getenv("TIM_WAIT_BUDGET_MS");
+        const long long ms = s ? std::atoll(s) : 0;
+        return ms > 0 ? static_cast<uint64_t>(ms) * 1000000ull : 4000000000ull;
+    }();
+    return v;
+}
+
+// Set-up of the current device, once: sm_103 check, SM count, the status word's
+// device address, a stream-ordered memory pool that keeps its memory, kernel
+// attributes, and the driver's tensor-map encoder.
+int device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TIM_ERR_UNSUPPORTED_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (d.ready) {
+        *out = &d;
+        return TIM_OK;
+    }
+    if (d.status_code != TIM_OK)
+        return fail(d.status_code, "device %d is not usable by this library", dev);
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) {
+        d.status_code = TIM_ERR_UNSUPPORTED_DEVICE;
+        return fail(TIM_ERR_UNSUPPORTED_DEVICE,
+                    "device %d is sm_%d%d; this library is built for sm_103a (GB300) only", dev, major, minor);
+    }
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = ~0ull;
+    if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemPoolSetAttribute");
+    if ((e = tim::k1_prepare_device()) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(TIM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+    *out = &d;
+    return TIM_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a box of
+// [box_rows, 64] and 128-byte swizzling; out-of-range elements read as zero.
+int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(tim::K1_BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TIM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return TIM_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+} // namespace
+
+extern "C" {
+
+int tim_version(void) { return kVersion; }
+
+const char *tim_last_error(void) { return g_msg; }
+
+int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D,
+                      int64_t V, float *out_logp, float *out_lse, tim_stream_t stream)
+{
+    if (N < 0 || N >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "N = %lld out of range [0, 2^31)", static_cast<long long>(N));
+    if (D <= 0 || D % 8 != 0 || D > 65536)
+        return fail(TIM_ERR_INVALID_ARG, "D = %lld must be positive, a multiple of 8 and <= 65536",
+                    static_cast<long long>(D));
+    if (V <= 0 || V >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "V = %lld out of range (0, 2^31)", static_cast<long long>(V));
+    if (N == 0) {
+        g_msg[0] = 0;
+        return TIM_OK;
+    }
+    if (!h || !W || !targets || !out_logp || !out_lse)
+        return fail(TIM_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(h, 16) || !aligned(W, 16))
+        return fail(TIM_ERR_INVALID_ARG, "h and W must be 16-byte aligned");
+    if (!aligned(targets, 4) || !aligned(out_logp, 4) || !aligned(out_lse, 4))
+        return fail(TIM_ERR_INVALID_ARG, "targets / outputs must be 4-byte aligned");
+    const int64_t m_tiles = (N + tim::K1_BM - 1) / tim::K1_BM;
+    const int64_t chunks = tim::k1_num_chunks(V);
+    if (m_tiles * chunks >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "N x V too large for one call");
+
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    CUtensorMap th, tw;
+    if ((rc = encode_bf16(&th, h, N, D, tim::K1_BM)) != TIM_OK)
+        return rc;
+    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_BN)) != TIM_OK)
+        return rc;
+
+    const size_t part_bytes = round_up(static_cast<size_t>(chunks) * N * sizeof(float2), 256);
+    const size_t za_bytes = round_up(static_cast<size_t>(N) * sizeof(float), 256);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + za_bytes, dev->pool, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMallocFromPoolAsync(token_logprob workspace)");
+
+    tim::K1Args a;
+    a.targets = targets;
+    a.part = static_cast<float2 *>(ws);
+    a.za = reinterpret_cast<float *>(static_cast<char *>(ws) + part_bytes);
+    a.status = dev->status;
+    a.N = static_cast<int32_t>(N);
+    a.D = static_cast<int32_t>(D);
+    a.V = static_cast<int32_t>(V);
+    a.num_m_tiles = static_cast<int32_t>(m_tiles);
+    a.num_chunks = static_cast<int32_t>(chunks);
+    // h rows of one band stay L2-resident (about 48 MiB) while the band walks V
+    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_BM) * D * 2));
+    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_tiles));
+    a.units = static_cast<int32_t>(m_tiles * chunks);
+    a.wait_budget_ns = wait_budget_ns();
+    const int grid = static_cast<int>(std::min<int64_t>(a.units, dev->sms));
+
+    e = tim::k1_launch_main(th, tw, a, grid, s);
+    if (e == cudaSuccess)
+        e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, out_logp, out_lse, s);
+    const cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "token_logprob launch");
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(token_logprob workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                       const int32_t *seq_offsets, float C, const tim_mismatch_out *out,
+                       tim_stream_t stream)
+{
+    if (!out)
+        return fail(TIM_ERR_INVALID_ARG, "out is null");
+    const int32_t S = out->num_seqs;
+    const int64_t N = out->num_tokens;
+    if (S < 0 || N < 0)
+        return fail(TIM_ERR_INVALID_ARG, "num_seqs / num_tokens must be >= 0");
+    if (S == 0 && N != 0)
+        return fail(TIM_ERR_INVALID_ARG, "num_tokens must be 0 when num_seqs is 0");
+    if (!(C > 0.f) || !std::isfinite(C))
+        return fail(TIM_ERR_INVALID_ARG, "C must be positive and finite");
+    const int32_t est = out->seq_estimator == 0 ? 3 : out->seq_estimator;
+    if (est != 1 && est != 3)
+        return fail(TIM_ERR_INVALID_ARG, "seq_estimator must be 1 or 3");
+    if (!seq_offsets || !out->batch_stats)
+        return fail(TIM_ERR_INVALID_ARG, "seq_offsets and batch_stats are required");
+    if (S > 0 && (!out->seq_stats || !out->seq_flags))
+        return fail(TIM_ERR_INVALID_ARG, "seq_stats and seq_flags are required when num_seqs > 0");
+    if (N > 0 && (!logp_train || !logp_rollout || !mask))
+        return fail(TIM_ERR_INVALID_ARG, "null token array");
+    if (!aligned(logp_train, 4) || !aligned(logp_rollout, 4) || !aligned(seq_offsets, 4) ||
+        !aligned(out->seq_stats, 4) || !aligned(out->seq_flags, 4) || !aligned(out->token_weight, 4) ||
+        !aligned(out->batch_stats, 8))
+        return fail(TIM_ERR_INVALID_ARG, "misaligned array");
+
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+
+    const double lc = std::log(static_cast<double>(C));
+    float lcd = static_cast<float>(lc);
+    if (static_cast<double>(lcd) > lc)
+        lcd = std::nextafter(lcd, -INFINITY);
+    const double tau = std::isnan(out->tau_seq) ? (static_cast<double>(C) - 1.0) - lc
+                                                : static_cast<double>(out->tau_seq);
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    const size_t rec_bytes = round_up(static_cast<size_t>(S) * tim::K2_REC * sizeof(double), 256);
+    if (rec_bytes > 0) {
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, rec_bytes, dev->pool, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMallocFromPoolAsync(mismatch workspace)");
+    }
+    tim::K2Args a;
+    a.l_tr = logp_train;
+    a.l_ro = logp_rollout;
+    a.mask = mask;
+    a.off = seq_offsets;
+    a.S = S;
+    a.N = N;
+    a.C = C;
+    a.log_c_down = lcd;
+    a.tau = tau;
+    a.estimator = est;
+    a.token_weight = out->token_weight;
+    a.seq_stats = out->seq_stats;
+    a.seq_flags = out->seq_flags;
+    a.batch = out->batch_stats;
+    a.rec = static_cast<double *>(ws);
+    a.status = dev->status;
+    cudaError_t e = tim::k2_launch(a, dev->sms, s);
+    cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "mismatch_stats launch");
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(mismatch workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_check(tim_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    int v = 0;
+    if ((e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof v, 0, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "read status");
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "clear status");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    if (v != TIM_OK)
+        return fail(v, "a kernel recorded status %d (%s)", v,
+                    v == TIM_ERR_TIMEOUT ? "pipeline wait ran out of time" : "bad input data");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,119 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol include/tim.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute call is made here)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+import rollout_logprob_mismatch_gb300 as tim
+from rollout_logprob_mismatch_gb300 import build as tim_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tim.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tim_build.build()
+    return tim.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"TIM_API\s+[\w\s\*]*?\b(tim_\w+)\s*\(", text)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    assert {"tim_token_logprob", "tim_mismatch_stats", "tim_check", "tim_last_error",
+            "tim_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", tim.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c_and_struct_layout_matches(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "tim.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(tim_mismatch_out),"
+        "offsetof(tim_mismatch_out,num_seqs),offsetof(tim_mismatch_out,num_tokens),"
+        "offsetof(tim_mismatch_out,tau_seq),offsetof(tim_mismatch_out,seq_estimator),"
+        "offsetof(tim_mismatch_out,token_weight),offsetof(tim_mismatch_out,seq_stats),"
+        "offsetof(tim_mismatch_out,seq_flags),offsetof(tim_mismatch_out,batch_stats));"
+        "return TIM_SEQ_FIELDS == 12 && TIM_BATCH_FIELDS == 20 ? 0 : 1;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                    "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    S = tim.tim_mismatch_out
+    want = [ctypes.sizeof(S)] + [getattr(S, f).offset for f in
+                                 ("num_seqs", "num_tokens", "tau_seq", "seq_estimator", "token_weight",
+                                  "seq_stats", "seq_flags", "batch_stats")]
+    assert vals == want
+    assert len(tim.SEQ_FIELDS) == 12 and len(tim.BATCH_FIELDS) == 20
+
+
+def test_version(lib):
+    assert tim.tim_version() >= 100
+
+
+@pytest.mark.parametrize("N,D,V", [(-1, 64, 10), (4, 0, 10), (4, 12, 10), (4, 64, 0), (4, 64, 1 << 31),
+                                   (1 << 31, 64, 10), (4, 65544, 10)])
+def test_token_logprob_rejects_bad_sizes(lib, N, D, V):
+    rc = tim.tim_token_logprob(16, 16, 16, N, D, V, 16, 16, None)
+    assert rc == tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_last_error()
+
+
+def test_token_logprob_rejects_null_and_misaligned(lib):
+    assert tim.tim_token_logprob(None, 16, 16, 4, 64, 10, 16, 16, None) == tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_token_logprob(16, 16, 16, 4, 64, 10, None, 16, None) == tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_token_logprob(8, 16, 16, 4, 64, 10, 16, 16, None) == tim.TIM_ERR_INVALID_ARG
+    assert "aligned" in tim.tim_last_error()
+
+
+def test_token_logprob_empty_is_noop(lib):
+    assert tim.tim_token_logprob(None, None, None, 0, 64, 10, None, None, None) == tim.TIM_OK
+
+
+def _out(S=1, N=4, est=3, batch=16, seq=16, flags=16):
+    d = tim.tim_mismatch_out()
+    d.num_seqs, d.num_tokens, d.tau_seq, d.seq_estimator = S, N, math.nan, est
+    d.token_weight, d.seq_stats, d.seq_flags, d.batch_stats = None, seq, flags, batch
+    return d
+
+
+def test_mismatch_stats_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    ok_ptrs = (16, 16, 16, 16)
+    assert lib.tim_mismatch_stats(*ok_ptrs, 2.0, None, None) == E
+    for C in (0.0, -1.0, math.nan, math.inf):
+        assert tim.tim_mismatch_stats(*ok_ptrs, C, _out(), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(S=-1), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(S=0, N=5), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(est=2), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(batch=None), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(seq=None), None) == E
+    assert tim.tim_mismatch_stats(None, 16, 16, 16, 2.0, _out(), None) == E
+    assert tim.tim_mismatch_stats(16, 16, 16, None, 2.0, _out(), None) == E
+    assert tim.tim_mismatch_stats(18, 16, 16, 16, 2.0, _out(), None) == E
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(batch=20), None) == E
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(tim, "_lib", None)
+    with pytest.raises(tim.TimError):
+        tim.load()
