@@ -96,6 +96,31 @@ TIM_API int tim_token_logprob(const void *h, const void *W, const int32_t *targe
                       int64_t N, int64_t D, int64_t V,
                       float *out_logp, float *out_lse, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ token logprob, no allocation
+ *
+ * No counterpart on the pages: a library-side variant of tim_token_logprob for
+ * callers that cannot have the library allocate device memory -- an engine that
+ * has reserved its whole device-memory budget for its own allocator (where a
+ * hidden allocation fails or escapes its accounting), or code where the
+ * stream-ordered allocator is unavailable.  Same arguments, results and
+ * tolerance as tim_token_logprob; it calls no cudaMalloc / cudaFree / pool
+ * routine.  Its split-V scratch is one fixed device array inside libtim.so of
+ * TIM_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
+ * until the process exits.  Calls with
+ *   ceil(8 * N * ceil(V / 1024) / 256) * 256 + ceil(4 * N / 256) * 256
+ * bytes above that limit (e.g. N > 14000 for V = 151936) return
+ * TIM_ERR_INVALID_ARG without launching anything.
+ * The first call on a device sets that device up (it looks up the array's
+ * device address, sets the kernel's shared-memory size and fetches the
+ * tensor-map encoder); make that first call before any stream capture.
+ * Every call shares the array; two calls whose kernels overlap on the GPU
+ * (different streams or threads) race on it, so callers must order them.
+ */
+#define TIM_NOALLOC_SCRATCH_BYTES (16u << 20)
+TIM_API int tim_token_logprob_noalloc(const void *h, const void *W, const int32_t *targets,
+                                      int64_t N, int64_t D, int64_t V,
+                                      float *out_logp, float *out_lse, tim_stream_t stream);
+
 /* ------------------------------------------------------------------ mismatch stats
  *
  * Per token t with mask_t != 0 (VeXact summary eq. (1); llm-infra-atlas

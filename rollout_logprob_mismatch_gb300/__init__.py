@@ -25,7 +25,7 @@ import threading
 
 __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "tim_mismatch_out", "lib_path", "load",
-    "tim_token_logprob", "tim_mismatch_stats", "tim_check", "tim_last_error", "tim_version",
+    "tim_token_logprob", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_check", "tim_last_error", "tim_version",
     "token_logprob", "mismatch_stats", "check",
 ]
 
@@ -38,6 +38,7 @@ TIM_ERR_UNSUPPORTED_DEVICE = -2
 TIM_ERR_CUDA = -3
 TIM_ERR_TIMEOUT = -4
 TIM_ERR_BAD_INPUT = -5
+NOALLOC_SCRATCH_BYTES = 16 << 20   # TIM_NOALLOC_SCRATCH_BYTES in include/tim.h
 
 SEQ_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
               "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel")
@@ -87,6 +88,8 @@ def load():
             P, I64 = ctypes.c_void_p, ctypes.c_int64
             lib.tim_token_logprob.argtypes = [P, P, P, I64, I64, I64, P, P, P]
             lib.tim_token_logprob.restype = ctypes.c_int
+            lib.tim_token_logprob_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, P]
+            lib.tim_token_logprob_noalloc.restype = ctypes.c_int
             lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
                                                ctypes.POINTER(tim_mismatch_out), P]
             lib.tim_mismatch_stats.restype = ctypes.c_int
@@ -104,6 +107,12 @@ def load():
 def tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream) -> int:
     """C ABI call with integer device addresses; returns the tim_status code."""
     return load().tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream)
+
+
+def tim_token_logprob_noalloc(h, W, targets, N, D, V, out_logp, out_lse, stream) -> int:
+    """C ABI call of the variant that allocates nothing (its scratch is a fixed
+    NOALLOC_SCRATCH_BYTES device array of the library); returns the tim_status code."""
+    return load().tim_token_logprob_noalloc(h, W, targets, N, D, V, out_logp, out_lse, stream)
 
 
 def tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C, out: tim_mismatch_out,

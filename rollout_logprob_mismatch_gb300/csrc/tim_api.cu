@@ -136,6 +136,26 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 } // namespace
 
+namespace tim {
+
+// Device address of the library's status word on the current device.
+cudaError_t status_word_address(int **out)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_status);
+}
+
+// Records a message for tim_last_error() on the calling thread; returns code.
+int record_error(int code, const char *msg)
+{
+    if (code == TIM_OK) {
+        g_msg[0] = 0;
+        return code;
+    }
+    return fail(code, "%s", msg);
+}
+
+} // namespace tim
+
 extern "C" {
 
 int tim_version(void) { return kVersion; }

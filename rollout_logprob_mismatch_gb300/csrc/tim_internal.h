@@ -69,4 +69,8 @@ struct K2Args {
 
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream);
 
+// ---------------------------------------------------------------- shared by the C-ABI files
+cudaError_t status_word_address(int **out);   // the library's device status word
+int record_error(int code, const char *msg);  // message for tim_last_error()
+
 } // namespace tim
