@@ -20,6 +20,7 @@ Rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -90,7 +91,7 @@ def barrier(dist, device=None):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -104,7 +105,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -148,13 +149,21 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
-def make_workload(seed: int = 0):
+def make_workload(seed: int = 0, tokens: int | None = None):
     cfg = wl.CONFIGS[WORKLOAD]
+    if tokens:   # a smaller batch of the same head, for profiling runs (whole sequences of 512)
+        n = max(512, tokens // 512 * 512)
+        cfg = dataclasses.replace(cfg, N=n, num_seqs=n // 512)
     h, W = wl.draw_head(cfg, seed=seed)
     a = wl.draw_targets(cfg, cfg.N, seed=seed)
     off = wl.draw_segments(cfg, seed=seed)
     mask = wl.draw_mask(cfg, off, seed=seed)
     return cfg, h, W, a, off, mask
+
+
+def stream_of(dev):
+    import torch
+    return torch.cuda.current_stream(dev)
 
 
 def cpu_threads():
@@ -244,7 +253,15 @@ def run_gb300(args):
     tim.load()
     peaks = load_peaks()
 
-    cfg, h, W, a, off, mask = make_workload(seed=rank)
+    if args.only == "k2bw":
+        # the mismatch pass alone on a large batch (profiling runs)
+        r = mismatch_bandwidth(tim, dev, stream_of(dev), peaks, tokens=args.tokens or K2_BW_TOKENS,
+                               reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
+    cfg, h, W, a, off, mask = make_workload(seed=rank, tokens=args.tokens)
     N, D, V = cfg.N, cfg.D, cfg.V
     stream = torch.cuda.current_stream(dev)
     hd = torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -268,6 +285,22 @@ def run_gb300(args):
         tim.token_logprob(hd, Wd, ad, lp, lse)
         tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
 
+    if args.only:
+        # one kernel family alone (profiling runs): warm-up, then timed launches
+        fn = (lambda: tim.token_logprob(hd, Wd, ad, lp, lse)) if args.only == "k1" else \
+             (lambda: tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out))
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tim.check()
+        if rank == 0:
+            print(json.dumps({"only": args.only, "N": N, "avg_launch_ms": e0.elapsed_time(e1) / args.steps}))
+        return 0
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
@@ -276,15 +309,15 @@ def run_gb300(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clocks:
-        for i in range(K):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            tim.token_logprob(hd, Wd, ad, lp, lse)
-            ev[i][1].record(stream)
-            tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
-            ev[i][2].record(stream)
-        torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index).__enter__()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        tim.token_logprob(hd, Wd, ad, lp, lse)
+        ev[i][1].record(stream)
+        tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
     barrier(dist, dev)
     tim.check()
     t_k1 = [ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(K)]
@@ -335,12 +368,13 @@ def run_gb300(args):
         e2e_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.__exit__(None, None, None)   # sampled over both timed regions
     t_e2e = sum(e2e_ev[i][0].elapsed_time(e2e_ev[i][1]) * 1e-3 for i in range(K))
     t_e2e = max_over_ranks(t_e2e, dist, dev)
     h2d = h_host.numel() * 2 + a_host.numel() * 4 + ro_host.numel() * 4 + m_host.numel() + o_host.numel() * 4
     d2h = b_host.numel() * 8 + s_host.numel() * 4 + f_host.numel() * 4
 
-    k2_bw = mismatch_bandwidth(tim, dev, stream, peaks, args) if not args.skip_k2_bandwidth else None
+    k2_bw = mismatch_bandwidth(tim, dev, stream, peaks) if not args.skip_k2_bandwidth else None
     tim.check()
 
     if rank != 0:
@@ -377,12 +411,13 @@ def run_gb300(args):
     return 0
 
 
-def mismatch_bandwidth(tim, dev, stream, peaks, args):
-    """tim_mismatch_stats alone on 2^27 tokens in Llama-like segments (lognormal
-    lengths, median 1024, clipped to [128, 4096]), 30% masked, with per-token
-    weights written; L2 flushed before each launch.  Reports HBM GB/s."""
+def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
+    """tim_mismatch_stats alone on `tokens` tokens (2^27 by default) in
+    Llama-like segments (lognormal lengths, median 1024, clipped to
+    [128, 4096]), 30% masked, with per-token weights written; L2 flushed before
+    each launch.  Reports HBM GB/s."""
     import torch
-    Nt = K2_BW_TOKENS
+    Nt = tokens
     cfg = wl.HeadConfig("bw", N=Nt, D=8, V=8, seq_layout="lognormal", mask_drop=0.3)
     off = wl.draw_segments(cfg, seed=7)
     S = len(off) - 1
@@ -397,9 +432,8 @@ def mismatch_bandwidth(tim, dev, stream, peaks, args):
            "batch": torch.empty(20, dtype=torch.float64, device=dev),
            "token_weight": torch.empty(Nt, dtype=torch.float32, device=dev)}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(3):
+    for _ in range(warmup):
         tim.mismatch_stats(l_tr, l_ro, mask, offd, out=out)
-    reps = 10
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
     torch.cuda.synchronize(dev)
     for i in range(reps):
@@ -419,11 +453,15 @@ def mismatch_bandwidth(tim, dev, stream, peaks, args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-k2-bandwidth", action="store_true")
+    ap.add_argument("--only", choices=["k1", "k2", "k2bw"], default=None,
+                    help="time one call alone (for profiling); prints a short line, not the contract line")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="smaller batch of the same head (profiling runs only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     if args.impl == "reference":

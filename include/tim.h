@@ -194,8 +194,8 @@ typedef struct {
     double *batch_stats;     /* out: fp64 [TIM_BATCH_FIELDS] */
 } tim_mismatch_out;
 
-/*   logp_train, logp_rollout  fp32 [N]
- *   mask                      uint8 [N]: 0 = not counted (prompt / padding), else counted
+/*   logp_train, logp_rollout  fp32 [N], 16-byte aligned
+ *   mask                      uint8 [N], 16-byte aligned: 0 = not counted (prompt / padding), else counted
  *   seq_offsets               int32 [S + 1]: seq_offsets[0] = 0, non-decreasing,
  *                             seq_offsets[S] = N (sequences packed back to back)
  *   C                         truncation cap of the importance weight, C > 0, finite

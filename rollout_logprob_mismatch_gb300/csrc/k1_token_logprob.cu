@@ -15,7 +15,7 @@
 //              in ascending order, and the target logit picked from the exact
 //              accumulator value.  The [N, V] logits never leave the SM.
 // Each unit writes its chunk's (max, sum) per row; a second small kernel folds
-// the chunks of a row in chunk order.  The split is a function of V alone and
+// the chunks of a row in a fixed order.  The split is a function of V alone and
 // every row is reduced in the same order whatever the batch holds, so a row's
 // outputs are bit-identical across batch sizes and compositions (llm-infra-atlas
 // "训推一致性与 determinism", sections 1.2 and 6: batch-invariant GEMM with a
@@ -57,18 +57,6 @@ __device__ __forceinline__ int tiles_in_chunk(int ch, int V)
     const int lo = ch * K1_VCHUNK;
     const int hi = min(V, lo + K1_VCHUNK);
     return (hi - lo + K1_BN - 1) / K1_BN;
-}
-
-// Bounded wait that ignores the abort flag: used only to drain in-flight
-// asynchronous work before the CTA releases its shared memory and TMEM.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns)
-{
-    if (mbar_try(bar, parity))
-        return;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try(bar, parity))
-        if (global_ns() - t0 > budget_ns)
-            return;
 }
 
 __global__ void __launch_bounds__(K1_THREADS, 1)
@@ -279,7 +267,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             if (!ok)
                 break;
             if (row < a.N) {
-                a.part[static_cast<size_t>(w.ch) * a.N + row] = make_float2(run_m, run_s);
+                a.part[static_cast<size_t>(row) * a.num_chunks + w.ch] = make_float2(run_m, run_s);
                 if (found)
                     a.za[row] = zt;
             }
@@ -297,28 +285,41 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
 }
 
-// Folds the per-chunk (max, sum) pairs of a row in chunk order:
-// M = max_c m_c, S = sum_c s_c e^(m_c - M), lse = M + ln S, l = z_a - lse.
+// Folds the per-chunk (max, sum) pairs of a row: M = max_c m_c,
+// S = sum_c s_c e^(m_c - M), lse = M + ln S, l = z_a - lse.  One warp per row:
+// lane i takes chunks i, i + 32, ... in order, then a fixed xor-shuffle tree sums
+// the lanes and lane 0's value is used.  The order depends on the number of
+// chunks (a function of V) only.
 __global__ void __launch_bounds__(256)
     k1_combine_kernel(const float2 *__restrict__ part, const float *__restrict__ za,
                       const int32_t *__restrict__ targets, int32_t N, int32_t V, int32_t num_chunks,
                       float *__restrict__ out_logp, float *__restrict__ out_lse)
 {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (t >= N)
-        return;
+        return;   // uniform over the warp
+    const float2 *p = part + t * num_chunks;
     float M = -INFINITY;
-    for (int c = 0; c < num_chunks; ++c)
-        M = fmaxf(M, part[static_cast<size_t>(c) * N + t].x);
+    for (int c = lane; c < num_chunks; c += 32)
+        M = fmaxf(M, p[c].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float S = 0.f;
-    for (int c = 0; c < num_chunks; ++c) {
-        const float2 p = part[static_cast<size_t>(c) * N + t];
-        S = fmaf(p.y, expf(p.x - M), S);
+    for (int c = lane; c < num_chunks; c += 32) {
+        const float2 q = p[c];
+        S = fmaf(q.y, expf(q.x - M), S);
     }
-    const float lse = M + logf(S);
-    out_lse[t] = lse;
-    const int a = targets[t];
-    out_logp[t] = (a >= 0 && a < V) ? za[t] - lse : __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        S += __shfl_xor_sync(0xffffffffu, S, o);
+    if (lane == 0) {
+        const float lse = M + logf(S);
+        out_lse[t] = lse;
+        const int a = targets[t];
+        out_logp[t] = (a >= 0 && a < V) ? za[t] - lse : __int_as_float(0x7fc00000);
+    }
 }
 
 } // namespace
@@ -340,8 +341,8 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
                               int32_t N, int32_t V, int32_t num_chunks, float *out_logp,
                               float *out_lse, cudaStream_t stream)
 {
-    const int threads = 256;
-    const int blocks = (N + threads - 1) / threads;
+    const int threads = 256;   // 8 rows per CTA, one warp each
+    const int blocks = static_cast<int>((static_cast<int64_t>(N) * 32 + threads - 1) / threads);
     k1_combine_kernel<<<blocks, threads, 0, stream>>>(part, za, targets, N, V, num_chunks, out_logp,
                                                       out_lse);
     return cudaGetLastError();

@@ -10,18 +10,31 @@
 // "Algorithmic TIM Compensation"); per batch: token means, mean of sequence means
 // (icarus monitoring steps 2-3) and ratios.
 //
-// One CTA reduces one sequence at a time (grid-stride over sequences).  Thread i
-// owns the tokens whose index inside the sequence is i, i + 256, i + 512, ...,
-// sums them in that order (fp32, folded every 16 rounds into a compensated
-// fp32 total), then a fixed shuffle tree and a warp-ordered fp64 sum give the
-// sequence totals.  The order depends only on a token's index inside its own
-// sequence, so a sequence's record is bit-identical wherever it is packed and
-// whatever else is in the batch.  A single CTA then folds the sequence records
-// in index order (fp64) into the batch record.
+// Two or three launches, in fp32 and integer arithmetic only (GB300 has very
+// little fp64 throughput):
+//  1. k2_seq_kernel, two 512-thread CTAs per SM.  A sequence of at most 8192
+//     tokens is reduced by one warp, a longer one by a whole CTA.  Each warp
+//     stages its sequence through shared memory in chunks of 256 tokens with 1-D
+//     bulk copies (double-buffered: the next chunk is in flight while this one is
+//     reduced), so a few instructions keep ~75 KB per SM in flight.  Inside a
+//     chunk, lane i owns the tokens at index 64 p + i and 64 p + 32 + i
+//     (p = 0..3), processed two at a time with packed f32x2 arithmetic and
+//     summed in that order; chunks follow in order and each chunk's sums are
+//     added to the lane's totals.  A fixed shuffle tree (and for a CTA a
+//     warp-ordered sum) gives the sequence totals; the lanes of one warp write
+//     the record.  The order depends only on a token's index inside its own
+//     sequence and on the sequence's length, so a sequence's record has the same
+//     bits wherever it is packed and whatever else is in the batch.
+//  2. k2_fold_kernel: CTA j folds sequences 1024 j .. 1024 j + 1023 (4 per
+//     thread, structure-of-arrays records, coalesced) with float-float (TwoSum)
+//     sums and integer counts in a fixed tree.
+//  3. k2_final_kernel (only when S > 1024): one CTA folds the partials in order.
+// The batch record depends on S and the sequence records only.
 #include <algorithm>
 #include <cfloat>
 
 #include "tim_internal.h"
+#include "tim_ptx.cuh"
 #include "../../include/tim.h"
 
 namespace tim {
@@ -29,326 +42,822 @@ namespace {
 
 enum { F_D = 0, F_AD, F_K2, F_K3, F_W, F_REL, NSUM };
 
-// Workspace record of one sequence (doubles).
+// Sequence record, structure of arrays: word f of sequence s is rec[f * S + s].
 enum {
-    R_VALID = 0, R_N_MASK, R_N_USED, R_N_NAN, R_N_CLIP, R_SD, R_SAD, R_SK2, R_SK3, R_SW, R_SREL,
-    R_MAX, R_MK1, R_MK2, R_MK3, R_FLAG
+    R_VALID = 0, R_N_MASK, R_N_USED, R_N_NAN, R_N_CLIP, R_FLAG,   // int32
+    R_SD, R_SAD, R_SK2, R_SK3, R_SW, R_SREL, R_MAX, R_MK1, R_MK2, R_MK3,   // float
 };
-static_assert(R_FLAG + 1 == K2_REC, "record layout");
+static_assert(R_MK3 + 1 == K2_REC_WORDS, "record layout");
 
-// e^d - 1 - d.  For |d| < 0.5 the Taylor series sum_{n>=2} d^n / n! through n = 9
-// (truncation below 2e-9 relative); above, expm1f(d) - d loses no digits.
-__device__ __forceinline__ float k3_of(float d)
-{
-    if (fabsf(d) < 0.5f) {
-        float p = 1.f / 362880.f;
-        p = fmaf(p, d, 1.f / 40320.f);
-        p = fmaf(p, d, 1.f / 5040.f);
-        p = fmaf(p, d, 1.f / 720.f);
-        p = fmaf(p, d, 1.f / 120.f);
-        p = fmaf(p, d, 1.f / 24.f);
-        p = fmaf(p, d, 1.f / 6.f);
-        p = fmaf(p, d, 0.5f);
-        return d * d * p;
-    }
-    return expm1f(d) - d;
-}
+// Fold partial: 7 int64 counts, 9 float-float sums, 1 max (words).
+enum { P_N_MASK = 0, P_N_USED, P_N_NAN, P_N_CLIP, P_NONEMPTY, P_REJ, P_INVALID, NCNT };
+enum { S_SD = 0, S_SAD, S_SK2, S_SK3, S_SW, S_SREL, S_MK1, S_MK2, S_MK3, NDF };
+static_assert(2 * NCNT + 2 * NDF + 1 <= K2_PART_WORDS, "partial layout");
 
-// Neumaier's compensated addition of x into (sum, comp).
-__device__ __forceinline__ void neumaier(float &sum, float &comp, float x)
+// Float-float value hi + lo and its addition (Knuth's TwoSum on the high
+// parts, low parts added to the error term, renormalised).
+struct ff {
+    float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_add(ff a, ff b)
 {
-    const float t = sum + x;
-    if (fabsf(sum) >= fabsf(x))
-        comp += (sum - t) + x;
-    else
-        comp += (x - t) + sum;
-    sum = t;
+    const float s = a.hi + b.hi;
+    const float v = s - a.hi;
+    float e = (a.hi - (s - v)) + (b.hi - v);
+    e += a.lo + b.lo;
+    const float hi = s + e;
+    return {hi, e - (hi - s)};
 }
 
 __device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
 
-__global__ void __launch_bounds__(K2_THREADS) k2_seq_kernel(const K2Args a)
+// Per-lane sums of one chunk (two tokens in lockstep: .x and .y) and the
+// lane's running totals over chunks.
+struct TokenAcc {
+    float2 inner[NSUM];
+    float outer[NSUM];
+    float mx;
+    int n_mask, n_used, n_clip;
+};
+
+__device__ __forceinline__ float rcp_approx(float x)
 {
-    constexpr int NW = K2_THREADS / 32;
-    __shared__ float red_f[NW][NSUM];
-    __shared__ int red_i[NW][4];
-    __shared__ float red_mx[NW];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-    for (int s = blockIdx.x; s < a.S; s += gridDim.x) {
-        const int64_t b = a.off[s], e = a.off[s + 1];
-        bool valid = b >= 0 && e >= b && e <= a.N;
-        if (s == 0 && b != 0)
-            valid = false;
-        if (s == a.S - 1 && e != a.N)
-            valid = false;
-        if (!valid) {   // uniform over the CTA: every thread read the same offsets
-            if (tid == 0) {
-                atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
-                for (int f = 0; f < TIM_SEQ_FIELDS; ++f)
-                    a.seq_stats[static_cast<size_t>(s) * TIM_SEQ_FIELDS + f] = qnan();
-                a.seq_flags[s] = 0;
-                for (int f = 0; f < K2_REC; ++f)
-                    a.rec[static_cast<size_t>(s) * K2_REC + f] = 0.0;
-            }
-            continue;
-        }
-        const int64_t len = e - b;
-        const int64_t nrounds = (len + K2_THREADS - 1) / K2_THREADS;
-        float outer[NSUM], comp[NSUM];
-#pragma unroll
-        for (int f = 0; f < NSUM; ++f)
-            outer[f] = comp[f] = 0.f;
-        float mx = 0.f;
-        int n_mask = 0, n_used = 0, n_nan = 0, n_clip = 0;
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
-        for (int64_t r0 = 0; r0 < nrounds; r0 += K2_GROUP) {
-            const int64_t r1 = min(nrounds, r0 + static_cast<int64_t>(K2_GROUP));
-            float inner[NSUM];
-#pragma unroll
-            for (int f = 0; f < NSUM; ++f)
-                inner[f] = 0.f;
-            for (int64_t r = r0; r < r1; r += 4) {
-                float lt[4], lr[4];
-                uint32_t mk[4];
-                bool in[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int64_t rel = (r + k) * K2_THREADS + tid;
-                    in[k] = (r + k < r1) && (rel < len);
-                    const int64_t t = b + rel;
-                    lt[k] = in[k] ? __ldcs(a.l_tr + t) : 0.f;
-                    lr[k] = in[k] ? __ldcs(a.l_ro + t) : 0.f;
-                    mk[k] = in[k] ? static_cast<uint32_t>(__ldcs(a.mask + t)) : 0u;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (!in[k])
-                        continue;
-                    const bool m = mk[k] != 0u;
-                    const float d = lt[k] - lr[k];
-                    const bool fin = fabsf(d) <= FLT_MAX;   // false for inf and NaN
-                    n_mask += m;
-                    n_nan += m && !fin;
-                    float w = 0.f;
-                    if (m && fin) {
-                        const float r_ = expf(d);
-                        const float ad = fabsf(d);
-                        w = fminf(r_, a.C);
-                        n_used += 1;
-                        n_clip += d > a.log_c_down;
-                        inner[F_D] += d;
-                        inner[F_AD] += ad;
-                        inner[F_K2] += 0.5f * d * d;
-                        inner[F_K3] += k3_of(d);
-                        inner[F_W] += w;
-                        inner[F_REL] += ad / (fabsf(lt[k]) + 1e-8f);
-                        mx = fmaxf(mx, ad);
-                    }
-                    if (a.token_weight)
-                        a.token_weight[b + (r + k) * K2_THREADS + tid] = w;
-                }
-            }
-#pragma unroll
-            for (int f = 0; f < NSUM; ++f)
-                neumaier(outer[f], comp[f], inner[f]);
-        }
+// Two tokens at once (packed f32x2 arithmetic, round-to-nearest per component,
+// so each component has the bits the scalar formula would give).  Tokens that
+// are not used (masked out, past the chunk, or non-finite delta) contribute
+// exact zeros.  Returns the two truncated IS weights (0 when not used).
+__device__ __forceinline__ float2 token_pair(TokenAcc &t, float2 lt, float2 lr, bool m0, bool m1, float C,
+                                             float lcd)
+{
+    const float2 d = __ffma2_rn(lr, f2(-1.f), lt);   // lt - lr, rounded once
+    const bool f0 = fabsf(d.x) <= FLT_MAX, f1 = fabsf(d.y) <= FLT_MAX;   // false for inf, NaN
+    const bool u0 = m0 && f0, u1 = m1 && f1;
+    t.n_mask += static_cast<int>(m0) + static_cast<int>(m1);
+    t.n_used += static_cast<int>(u0) + static_cast<int>(u1);   // n_nan = n_mask - n_used
+    t.n_clip += static_cast<int>(u0 && d.x > lcd) + static_cast<int>(u1 && d.y > lcd);
+    const float2 du = make_float2(u0 ? d.x : 0.f, u1 ? d.y : 0.f);
+    const float2 ad = make_float2(fabsf(du.x), fabsf(du.y));
+    const float2 e = __fmul2_rn(du, f2(1.4426950408889634f));   // e^d = 2^(d log2 e)
+    const float2 r = make_float2(ex2(e.x), ex2(e.y));
+    const float2 w = make_float2(u0 ? fminf(r.x, C) : 0.f, u1 ? fminf(r.y, C) : 0.f);
+    const float2 dd = __fmul2_rn(du, du);
+    // k3 = e^d - 1 - d: Taylor series sum_{n>=2} d^n / n! through n = 9 for
+    // |d| < 0.5 (truncation below 2e-9 relative), (r - 1) - d above
+    float2 p = f2(1.f / 362880.f);
+    p = __ffma2_rn(p, du, f2(1.f / 40320.f));
+    p = __ffma2_rn(p, du, f2(1.f / 5040.f));
+    p = __ffma2_rn(p, du, f2(1.f / 720.f));
+    p = __ffma2_rn(p, du, f2(1.f / 120.f));
+    p = __ffma2_rn(p, du, f2(1.f / 24.f));
+    p = __ffma2_rn(p, du, f2(1.f / 6.f));
+    p = __ffma2_rn(p, du, f2(0.5f));
+    const float2 small = __fmul2_rn(dd, p);
+    const float2 large = __fadd2_rn(__fadd2_rn(r, f2(-1.f)), make_float2(-du.x, -du.y));
+    const float2 k3 = make_float2(ad.x < 0.5f ? small.x : large.x, ad.y < 0.5f ? small.y : large.y);
+    const float2 den = __fadd2_rn(make_float2(u0 ? fabsf(lt.x) : 1.f, u1 ? fabsf(lt.y) : 1.f), f2(1e-8f));
+    const float2 rel = __fmul2_rn(ad, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+    t.inner[F_D] = __fadd2_rn(t.inner[F_D], du);
+    t.inner[F_AD] = __fadd2_rn(t.inner[F_AD], ad);
+    t.inner[F_K2] = __ffma2_rn(dd, f2(0.5f), t.inner[F_K2]);
+    t.inner[F_K3] = __fadd2_rn(t.inner[F_K3], k3);
+    t.inner[F_W] = __fadd2_rn(t.inner[F_W], w);
+    t.inner[F_REL] = __fadd2_rn(t.inner[F_REL], rel);
+    t.mx = fmaxf(t.mx, fmaxf(ad.x, ad.y));
+    return w;
+}
 
-        float tot[NSUM];
-#pragma unroll
-        for (int f = 0; f < NSUM; ++f) {
-            tot[f] = outer[f] + comp[f];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                tot[f] += __shfl_xor_sync(0xffffffffu, tot[f], o);
+// Totals of one sequence.
+struct SeqTot {
+    float sum[NSUM];
+    int cnt[4];   // n_mask, n_used, n_nan, n_clip
+    float mx;
+};
+
+// Where a staged chunk sits in its stage: tokens [t0, t0 + n) of the arrays,
+// token t0 at float index off_f of the fp32 regions and byte off_m of the mask.
+struct ChunkView {
+    int64_t t0;   // first token of the chunk
+    int n;        // tokens in the chunk
+    int off_f;    // t0 & 3: index of token t0 in the staged fp32 regions
+    int off_m;    // t0 & 15: byte of token t0 in the staged mask region
+};
+
+// Stages tokens [t0, t1) (at most K2_CHUNK) into the stage at `stp`: lane 0
+// bulk-copies the 16-byte-aligned blocks that cover them (completion on
+// `bar`); the few elements past the last whole 16-byte block of an array,
+// which a bulk copy may not read, are copied by plain loads.  Called by a
+// full warp.
+__device__ __forceinline__ ChunkView stage_chunk(const K2Args &a, uint8_t *stp, uint32_t bar, int64_t t0,
+                                                 int64_t t1, int lane, uint64_t pol)
+{
+    ChunkView v;
+    v.t0 = t0;
+    v.n = static_cast<int>(t1 - t0);
+    v.off_f = static_cast<int>(t0 & 3);
+    v.off_m = static_cast<int>(t0 & 15);
+    const int64_t flim = a.N & ~int64_t(3);    // tokens below this lie in whole 16-byte fp32 blocks
+    const int64_t mlim = a.N & ~int64_t(15);   // same for the mask bytes
+    if (lane == 0) {
+        const int64_t A = t0 & ~int64_t(3);
+        const int64_t fend = min((t1 + 3) & ~int64_t(3), flim);
+        const int fbytes = fend > A ? static_cast<int>(fend - A) * 4 : 0;
+        const int64_t Am = t0 & ~int64_t(15);
+        const int64_t mend = min((t1 + 15) & ~int64_t(15), mlim);
+        const int mbytes = mend > Am ? static_cast<int>(mend - Am) : 0;
+        const uint32_t st = smem_u32(stp);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, 2u * fbytes + mbytes);
+        if (fbytes > 0) {
+            bulk_load(st, a.l_tr + A, fbytes, bar, pol);
+            bulk_load(st + K2_F_BYTES, a.l_ro + A, fbytes, bar, pol);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        n_mask = __reduce_add_sync(0xffffffffu, n_mask);
-        n_used = __reduce_add_sync(0xffffffffu, n_used);
-        n_nan = __reduce_add_sync(0xffffffffu, n_nan);
-        n_clip = __reduce_add_sync(0xffffffffu, n_clip);
-        if (lane == 0) {
-#pragma unroll
-            for (int f = 0; f < NSUM; ++f)
-                red_f[warp][f] = tot[f];
-            red_i[warp][0] = n_mask;
-            red_i[warp][1] = n_used;
-            red_i[warp][2] = n_nan;
-            red_i[warp][3] = n_clip;
-            red_mx[warp] = mx;
+        if (mbytes > 0)
+            bulk_load(st + 2 * K2_F_BYTES, a.mask + Am, mbytes, bar, pol);
+    }
+    if (t1 > flim) {   // the last few elements of the arrays only
+        float *lt_s = reinterpret_cast<float *>(stp) + v.off_f;
+        float *lr_s = reinterpret_cast<float *>(stp + K2_F_BYTES) + v.off_f;
+        for (int64_t t = max(t0, flim) + lane; t < t1; t += 32) {
+            lt_s[t - t0] = a.l_tr[t];
+            lr_s[t - t0] = a.l_ro[t];
         }
-        __syncthreads();
-        if (tid == 0) {
-            double sum[NSUM] = {0, 0, 0, 0, 0, 0};
-            long long cnt[4] = {0, 0, 0, 0};
-            float m = 0.f;
-            for (int w = 0; w < NW; ++w) {
-                for (int f = 0; f < NSUM; ++f)
-                    sum[f] += static_cast<double>(red_f[w][f]);
-                for (int c = 0; c < 4; ++c)
-                    cnt[c] += red_i[w][c];
-                m = fmaxf(m, red_mx[w]);
+    }
+    if (t1 > mlim) {
+        uint8_t *mk_s = stp + 2 * K2_F_BYTES + v.off_m;
+        for (int64_t t = max(t0, mlim) + lane; t < t1; t += 32)
+            mk_s[t - t0] = a.mask[t];
+    }
+    return v;
+}
+
+// The lane's tokens of one staged chunk: index 64 q + lane (.x) and
+// 64 q + 32 + lane (.y) for q = 0..3, in that order; writes their weights.
+__device__ __forceinline__ void reduce_chunk(TokenAcc &acc, const K2Args &a, const uint8_t *stp,
+                                             const ChunkView &v, int lane)
+{
+    const float *lt_s = reinterpret_cast<const float *>(stp) + v.off_f + lane;
+    const float *lr_s = reinterpret_cast<const float *>(stp + K2_F_BYTES) + v.off_f + lane;
+    const uint8_t *mk_s = stp + 2 * K2_F_BYTES + v.off_m + lane;
+    float *wout = a.token_weight ? a.token_weight + v.t0 + lane : nullptr;
+    if (v.n == K2_CHUNK) {   // full chunk: no bounds checks
+#pragma unroll
+        for (int q = 0; q < K2_CHUNK / 64; ++q) {
+            const float2 lt = make_float2(lt_s[64 * q], lt_s[64 * q + 32]);
+            const float2 lr = make_float2(lr_s[64 * q], lr_s[64 * q + 32]);
+            const float2 w = token_pair(acc, lt, lr, mk_s[64 * q] != 0, mk_s[64 * q + 32] != 0, a.C, a.log_c_down);
+            if (wout) {
+                __stcs(wout + 64 * q, w.x);
+                __stcs(wout + 64 * q + 32, w.y);
             }
-            const double nu = static_cast<double>(cnt[1]);
-            auto mean = [&](double x) { return cnt[1] > 0 ? x / nu : 0.0; };
-            const double md = mean(sum[F_D]);
-            const double mk1 = -md;
-            const double mk2 = mean(sum[F_K2]);
-            const double mk3 = mean(sum[F_K3]);
-            float *o = a.seq_stats + static_cast<size_t>(s) * TIM_SEQ_FIELDS;
-            o[TIM_SEQ_N_MASK] = static_cast<float>(cnt[0]);
-            o[TIM_SEQ_N_USED] = static_cast<float>(cnt[1]);
-            o[TIM_SEQ_N_NAN] = static_cast<float>(cnt[2]);
-            o[TIM_SEQ_N_CLIP] = static_cast<float>(cnt[3]);
-            o[TIM_SEQ_MEAN_DELTA] = static_cast<float>(md);
-            o[TIM_SEQ_MEAN_ABS_DELTA] = static_cast<float>(mean(sum[F_AD]));
-            o[TIM_SEQ_MAX_ABS_DELTA] = m;
-            o[TIM_SEQ_MEAN_K1] = static_cast<float>(mk1);
-            o[TIM_SEQ_MEAN_K2] = static_cast<float>(mk2);
-            o[TIM_SEQ_MEAN_K3] = static_cast<float>(mk3);
-            o[TIM_SEQ_MEAN_W] = static_cast<float>(mean(sum[F_W]));
-            o[TIM_SEQ_MEAN_REL] = static_cast<float>(mean(sum[F_REL]));
-            int flag = 0;
-            if (cnt[1] > 0)
-                flag = (a.estimator == 3 ? mk3 : fabs(mk1)) > a.tau;
-            a.seq_flags[s] = flag;
-            double *rc = a.rec + static_cast<size_t>(s) * K2_REC;
-            rc[R_VALID] = 1.0;
-            rc[R_N_MASK] = static_cast<double>(cnt[0]);
-            rc[R_N_USED] = nu;
-            rc[R_N_NAN] = static_cast<double>(cnt[2]);
-            rc[R_N_CLIP] = static_cast<double>(cnt[3]);
-            rc[R_SD] = sum[F_D];
-            rc[R_SAD] = sum[F_AD];
-            rc[R_SK2] = sum[F_K2];
-            rc[R_SK3] = sum[F_K3];
-            rc[R_SW] = sum[F_W];
-            rc[R_SREL] = sum[F_REL];
-            rc[R_MAX] = static_cast<double>(m);
-            rc[R_MK1] = mk1;
-            rc[R_MK2] = mk2;
-            rc[R_MK3] = mk3;
-            rc[R_FLAG] = static_cast<double>(flag);
         }
-        __syncthreads();
+    } else {
+#pragma unroll
+        for (int q = 0; q < K2_CHUNK / 64; ++q) {
+            const int j0 = 64 * q + lane, j1 = j0 + 32;
+            const bool in0 = j0 < v.n, in1 = j1 < v.n;
+            const float2 lt = make_float2(in0 ? lt_s[64 * q] : 0.f, in1 ? lt_s[64 * q + 32] : 0.f);
+            const float2 lr = make_float2(in0 ? lr_s[64 * q] : 0.f, in1 ? lr_s[64 * q + 32] : 0.f);
+            const bool m0 = in0 && mk_s[64 * q] != 0;
+            const bool m1 = in1 && mk_s[64 * q + 32] != 0;
+            const float2 w = token_pair(acc, lt, lr, m0, m1, a.C, a.log_c_down);
+            if (wout) {
+                if (in0)
+                    __stcs(wout + 64 * q, w.x);
+                if (in1)
+                    __stcs(wout + 64 * q + 32, w.y);
+            }
+        }
     }
 }
 
-// Batch record from the sequence records: thread t folds a contiguous slice of
-// sequences in index order (fp64), then a fixed shuffle tree and a warp-ordered
-// sum finish it.  The result depends on S and the records only.
-__global__ void __launch_bounds__(K2_BATCH_THREADS) k2_batch_kernel(const K2Args a)
+// Adds the chunk's sums (at most 8 tokens per lane) into the lane's totals:
+// two plain fp32 levels keep the rounding error within (8 + chunks) ulps.
+__device__ __forceinline__ void fold_chunk(TokenAcc &acc)
 {
-    enum { B_MASK = 0, B_USED, B_NAN, B_CLIP, B_SD, B_SAD, B_SK2, B_SK3, B_SW, B_SREL, B_MK1,
-           B_MK2, B_MK3, B_NONEMPTY, B_REJ, B_INVALID, NB };
-    constexpr int NW = K2_BATCH_THREADS / 32;
-    __shared__ double red[NW][NB];
-    __shared__ double red_mx[NW];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    double acc[NB];
 #pragma unroll
-    for (int f = 0; f < NB; ++f)
-        acc[f] = 0.0;
-    double mx = 0.0;
-    const int64_t s_lo = static_cast<int64_t>(a.S) * tid / K2_BATCH_THREADS;
-    const int64_t s_hi = static_cast<int64_t>(a.S) * (tid + 1) / K2_BATCH_THREADS;
-    for (int64_t s = s_lo; s < s_hi; ++s) {
-        const double *rc = a.rec + s * K2_REC;
-        if (rc[R_VALID] == 0.0) {
-            acc[B_INVALID] += 1.0;
-            continue;
-        }
-        acc[B_MASK] += rc[R_N_MASK];
-        acc[B_USED] += rc[R_N_USED];
-        acc[B_NAN] += rc[R_N_NAN];
-        acc[B_CLIP] += rc[R_N_CLIP];
-        acc[B_SD] += rc[R_SD];
-        acc[B_SAD] += rc[R_SAD];
-        acc[B_SK2] += rc[R_SK2];
-        acc[B_SK3] += rc[R_SK3];
-        acc[B_SW] += rc[R_SW];
-        acc[B_SREL] += rc[R_SREL];
-        mx = fmax(mx, rc[R_MAX]);
-        if (rc[R_N_USED] > 0.0) {
-            acc[B_MK1] += rc[R_MK1];
-            acc[B_MK2] += rc[R_MK2];
-            acc[B_MK3] += rc[R_MK3];
-            acc[B_NONEMPTY] += 1.0;
-            acc[B_REJ] += rc[R_FLAG];
-        }
+    for (int f = 0; f < NSUM; ++f) {
+        acc.outer[f] += acc.inner[f].x + acc.inner[f].y;
+        acc.inner[f] = make_float2(0.f, 0.f);
     }
+}
+
+__device__ __forceinline__ SeqTot lane_total(const TokenAcc &acc)
+{
+    SeqTot t;
 #pragma unroll
-    for (int f = 0; f < NB; ++f)
+    for (int f = 0; f < NSUM; ++f)
+        t.sum[f] = acc.outer[f];
+    t.cnt[0] = acc.n_mask;
+    t.cnt[1] = acc.n_used;
+    t.cnt[2] = acc.n_mask - acc.n_used;   // a masked-in token is either used or non-finite
+    t.cnt[3] = acc.n_clip;
+    t.mx = acc.mx;
+    return t;
+}
+
+__device__ __forceinline__ void acc_zero(TokenAcc &acc)
+{
+#pragma unroll
+    for (int f = 0; f < NSUM; ++f) {
+        acc.inner[f] = make_float2(0.f, 0.f);
+        acc.outer[f] = 0.f;
+    }
+    acc.mx = 0.f;
+    acc.n_mask = acc.n_used = acc.n_clip = 0;
+}
+
+// Fixed xor-shuffle tree over a warp; the result is taken from lane 0 and
+// broadcast, so every lane holds the same bits.
+__device__ __forceinline__ SeqTot warp_total(SeqTot t)
+{
+#pragma unroll
+    for (int f = 0; f < NSUM; ++f) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
-            acc[f] += __shfl_xor_sync(0xffffffffu, acc[f], o);
+            t.sum[f] += __shfl_xor_sync(0xffffffffu, t.sum[f], o);
+        t.sum[f] = __shfl_sync(0xffffffffu, t.sum[f], 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        t.cnt[c] = __reduce_add_sync(0xffffffffu, t.cnt[c]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
-        mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        t.mx = fmaxf(t.mx, __shfl_xor_sync(0xffffffffu, t.mx, o));
+    return t;
+}
+
+__device__ __forceinline__ float pick(const float (&v)[16], int i)
+{
+    float r = v[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k)
+        r = i == k ? v[k] : r;
+    return r;
+}
+
+// Means, flag, output record and workspace record of sequence s, written by
+// one full warp whose lanes all hold the same totals (lane i writes word i).
+__device__ __forceinline__ void write_seq(const K2Args &a, int s, const SeqTot &t, int lane)
+{
+    const float nu = static_cast<float>(t.cnt[1]);
+    const float inv = t.cnt[1] > 0 ? 1.f / nu : 0.f;
+    auto mean = [&](float x) { return x * inv; };
+    const float md = mean(t.sum[F_D]);
+    const float mk2 = mean(t.sum[F_K2]);
+    const float mk3 = mean(t.sum[F_K3]);
+    const int flag = t.cnt[1] > 0 && (a.estimator == 3 ? mk3 : fabsf(md)) > a.tau;
+    float o[16];
+    o[TIM_SEQ_N_MASK] = static_cast<float>(t.cnt[0]);
+    o[TIM_SEQ_N_USED] = nu;
+    o[TIM_SEQ_N_NAN] = static_cast<float>(t.cnt[2]);
+    o[TIM_SEQ_N_CLIP] = static_cast<float>(t.cnt[3]);
+    o[TIM_SEQ_MEAN_DELTA] = md;
+    o[TIM_SEQ_MEAN_ABS_DELTA] = mean(t.sum[F_AD]);
+    o[TIM_SEQ_MAX_ABS_DELTA] = t.mx;
+    o[TIM_SEQ_MEAN_K1] = -md;
+    o[TIM_SEQ_MEAN_K2] = mk2;
+    o[TIM_SEQ_MEAN_K3] = mk3;
+    o[TIM_SEQ_MEAN_W] = mean(t.sum[F_W]);
+    o[TIM_SEQ_MEAN_REL] = mean(t.sum[F_REL]);
+    o[12] = o[13] = o[14] = o[15] = 0.f;
+    if (lane < TIM_SEQ_FIELDS)
+        a.seq_stats[static_cast<size_t>(s) * TIM_SEQ_FIELDS + lane] = pick(o, lane);
+    float r[16];
+    r[R_VALID] = __uint_as_float(1u);
+    r[R_N_MASK] = __uint_as_float(static_cast<uint32_t>(t.cnt[0]));
+    r[R_N_USED] = __uint_as_float(static_cast<uint32_t>(t.cnt[1]));
+    r[R_N_NAN] = __uint_as_float(static_cast<uint32_t>(t.cnt[2]));
+    r[R_N_CLIP] = __uint_as_float(static_cast<uint32_t>(t.cnt[3]));
+    r[R_FLAG] = __uint_as_float(static_cast<uint32_t>(flag));
+    r[R_SD] = t.sum[F_D];
+    r[R_SAD] = t.sum[F_AD];
+    r[R_SK2] = t.sum[F_K2];
+    r[R_SK3] = t.sum[F_K3];
+    r[R_SW] = t.sum[F_W];
+    r[R_SREL] = t.sum[F_REL];
+    r[R_MAX] = t.mx;
+    r[R_MK1] = -md;
+    r[R_MK2] = mk2;
+    r[R_MK3] = mk3;
+    if (lane < K2_REC_WORDS)
+        a.rec[static_cast<size_t>(lane) * a.S + s] = __float_as_uint(pick(r, lane));
+    if (lane == 0)
+        a.seq_flags[s] = flag;
+}
+
+__device__ __forceinline__ bool offsets_ok(const K2Args &a, int s, int64_t b, int64_t e)
+{
+    bool ok = b >= 0 && e >= b && e <= a.N;
+    if (s == 0 && b != 0)
+        ok = false;
+    if (s == a.S - 1 && e != a.N)
+        ok = false;
+    return ok;
+}
+
+// Bounded wait on a stage barrier; raises the CTA's abort flag on expiry.
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t budget)
+{
+    return mbar_wait(bar, parity, abort, budget);
+}
+
+// Lane-parallel record of a sequence that is skipped by the staged path:
+// bad offsets (NaN record, status) or no tokens (all zero).
+__device__ __forceinline__ void write_plain(const K2Args &a, int s, bool bad, int lane)
+{
+    if (bad) {
+        if (lane == 0)
+            atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
+        if (lane < TIM_SEQ_FIELDS)
+            a.seq_stats[static_cast<size_t>(s) * TIM_SEQ_FIELDS + lane] = qnan();
+        if (lane < K2_REC_WORDS)
+            a.rec[static_cast<size_t>(lane) * a.S + s] = 0u;
+        if (lane == 0)
+            a.seq_flags[s] = 0;
+    } else {
+        SeqTot z;
+#pragma unroll
+        for (int f = 0; f < NSUM; ++f)
+            z.sum[f] = 0.f;
+        z.cnt[0] = z.cnt[1] = z.cnt[2] = z.cnt[3] = 0;
+        z.mx = 0.f;
+        write_seq(a, s, z, lane);
+    }
+}
+
+// Next sequence from s on (stride `step`) that the warp reduces itself;
+// records of empty or bad sequences met on the way are written at once, long
+// ones are left for the CTA phase.  Returns S when there is none.
+__device__ __forceinline__ int next_short(const K2Args &a, int s, int step, int lane)
+{
+    for (; s < a.S; s += step) {
+        const int64_t b = a.off[s], e = a.off[s + 1];
+        if (!offsets_ok(a, s, b, e)) {
+            write_plain(a, s, true, lane);
+            continue;
+        }
+        if (e - b > K2_LONG)
+            continue;
+        if (e == b) {
+            write_plain(a, s, false, lane);
+            continue;
+        }
+        return s;
+    }
+    return a.S;
+}
+
+__global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(const K2Args a)
+{
+    extern __shared__ __align__(16) uint8_t k2_smem[];
+    __shared__ float red_f[K2_WARPS][NSUM];
+    __shared__ int red_i[K2_WARPS][4];
+    __shared__ float red_mx[K2_WARPS];
+    __shared__ int abort_flag_s;
+    volatile int *abort_flag = &abort_flag_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t bar0 = smem_u32(k2_smem) + 8u * (K2_STAGES * warp);
+    uint8_t *const st0 = k2_smem + K2_BAR_BYTES + K2_STAGES * K2_STAGE_BYTES * warp;
     if (lane == 0) {
-        for (int f = 0; f < NB; ++f)
-            red[warp][f] = acc[f];
-        red_mx[warp] = mx;
+        for (int i = 0; i < K2_STAGES; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_mbar_init();
     }
+    if (tid == 0)
+        abort_flag_s = 0;
     __syncthreads();
-    if (tid != 0)
-        return;
-    double t[NB];
-    for (int f = 0; f < NB; ++f)
-        t[f] = 0.0;
-    double m = 0.0;
-    for (int w = 0; w < NW; ++w) {
-        for (int f = 0; f < NB; ++f)
-            t[f] += red[w][f];
-        m = fmax(m, red_mx[w]);
+    const uint64_t pol = l2_policy_evict_first();
+    const uint64_t budget = a.wait_budget_ns;
+    uint32_t parity = 0;    // bit i: parity of stage i's next completion
+    uint32_t pending = 0;   // bit i: stage i has a staged chunk not yet waited for
+    int stage = 0;
+    bool ok = true;
+
+    // ---- phase 1: sequences of at most K2_LONG tokens, one warp each.  Warp w
+    // of CTA c takes sequences w * gridDim + c, + warps in the grid, ...
+    const int step = gridDim.x * K2_WARPS;
+    int s = next_short(a, warp * gridDim.x + blockIdx.x, step, lane);
+    ChunkView cur;
+    if (s < a.S) {
+        const int64_t b = a.off[s], e = a.off[s + 1];
+        cur = stage_chunk(a, st0, bar0, b, min(e, b + K2_CHUNK), lane, pol);
+        pending |= 1u;
     }
-    // the offsets must cover exactly [0, N); a sequence kernel that found a bad
-    // sequence left its record invalid
-    const bool bad = t[B_INVALID] > 0.0 || a.off[0] != 0 || static_cast<int64_t>(a.off[a.S]) != a.N;
+    while (ok && s < a.S) {
+        const int64_t b = a.off[s], e = a.off[s + 1];
+        const int64_t nch = (e - b + K2_CHUNK - 1) / K2_CHUNK;
+        TokenAcc acc;
+        acc_zero(acc);
+        int nxt = s;
+        for (int64_t c = 0; c < nch; ++c) {
+            ChunkView nv;
+            uint8_t *const nst = st0 + (stage ^ 1) * K2_STAGE_BYTES;
+            const uint32_t nbar = bar0 + 8u * (stage ^ 1);
+            if (c + 1 < nch) {
+                const int64_t t0 = b + (c + 1) * K2_CHUNK;
+                nv = stage_chunk(a, nst, nbar, t0, min(e, t0 + K2_CHUNK), lane, pol);
+                pending |= 1u << (stage ^ 1);
+            } else {
+                nxt = next_short(a, s + step, step, lane);
+                if (nxt < a.S) {
+                    const int64_t nb = a.off[nxt], ne = a.off[nxt + 1];
+                    nv = stage_chunk(a, nst, nbar, nb, min(ne, nb + K2_CHUNK), lane, pol);
+                    pending |= 1u << (stage ^ 1);
+                }
+            }
+            if (!stage_wait(bar0 + 8u * stage, (parity >> stage) & 1u, abort_flag, budget)) {
+                ok = false;
+                break;
+            }
+            parity ^= 1u << stage;
+            pending &= ~(1u << stage);
+            reduce_chunk(acc, a, st0 + stage * K2_STAGE_BYTES, cur, lane);
+            fold_chunk(acc);
+            __syncwarp();
+            stage ^= 1;
+            cur = nv;
+        }
+        if (!ok)
+            break;
+        write_seq(a, s, warp_total(lane_total(acc)), lane);
+        s = nxt;
+    }
+    if (!ok) {
+        // staged copies may still be landing: give them their time before the CTA exits
+        for (int i = 0; i < K2_STAGES; ++i)
+            if (pending & (1u << i))
+                drain_wait(bar0 + 8u * i, (parity >> i) & 1u, budget);
+        pending = 0;
+        if (lane == 0)
+            atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
+    }
+
+    // ---- phase 2: longer sequences, one CTA each; warp w takes chunks w, w + 16, ...
+    // (the CTA's phase-1 warps met exactly the sequences q = blockIdx.x + k gridDim.x)
+    if (!ok)
+        *abort_flag = 1;
+    __syncthreads();
+    for (int q = blockIdx.x; q < a.S && !*abort_flag; q += gridDim.x) {
+        const int64_t b = a.off[q], e = a.off[q + 1];
+        if (!offsets_ok(a, q, b, e) || e - b <= K2_LONG)   // uniform over the CTA
+            continue;
+        __syncthreads();   // the previous long sequence's reduction buffers are free
+        const int64_t nch = (e - b + K2_CHUNK - 1) / K2_CHUNK;
+        TokenAcc acc;
+        acc_zero(acc);
+        int64_t c = warp;
+        if (c < nch) {
+            cur = stage_chunk(a, st0 + stage * K2_STAGE_BYTES, bar0 + 8u * stage,
+                              b + c * K2_CHUNK, min(e, b + (c + 1) * K2_CHUNK), lane, pol);
+            pending |= 1u << stage;
+        }
+        for (; c < nch; c += K2_WARPS) {
+            ChunkView nv;
+            const int64_t cn = c + K2_WARPS;
+            if (cn < nch) {
+                nv = stage_chunk(a, st0 + (stage ^ 1) * K2_STAGE_BYTES,
+                                 bar0 + 8u * (stage ^ 1), b + cn * K2_CHUNK, min(e, b + (cn + 1) * K2_CHUNK),
+                                 lane, pol);
+                pending |= 1u << (stage ^ 1);
+            }
+            if (!stage_wait(bar0 + 8u * stage, (parity >> stage) & 1u, abort_flag, budget)) {
+                ok = false;
+                break;
+            }
+            parity ^= 1u << stage;
+            pending &= ~(1u << stage);
+            reduce_chunk(acc, a, st0 + stage * K2_STAGE_BYTES, cur, lane);
+            fold_chunk(acc);
+            __syncwarp();
+            stage ^= 1;
+            cur = nv;
+        }
+        if (!ok) {
+            for (int i = 0; i < K2_STAGES; ++i)
+                if (pending & (1u << i))
+                    drain_wait(bar0 + 8u * i, (parity >> i) & 1u, budget);
+            pending = 0;
+            if (lane == 0)
+                atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
+        }
+        const SeqTot t = warp_total(lane_total(acc));
+        if (lane == 0) {
+#pragma unroll
+            for (int f = 0; f < NSUM; ++f)
+                red_f[warp][f] = t.sum[f];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                red_i[warp][k] = t.cnt[k];
+            red_mx[warp] = t.mx;
+        }
+        __syncthreads();
+        if (warp == 0) {   // every lane folds the warps in order: the same bits on all lanes
+            SeqTot c2;
+#pragma unroll
+            for (int f = 0; f < NSUM; ++f)
+                c2.sum[f] = 0.f;
+            c2.cnt[0] = c2.cnt[1] = c2.cnt[2] = c2.cnt[3] = 0;
+            c2.mx = 0.f;
+            for (int w = 0; w < K2_WARPS; ++w) {
+#pragma unroll
+                for (int f = 0; f < NSUM; ++f)
+                    c2.sum[f] += red_f[w][f];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    c2.cnt[k] += red_i[w][k];
+                c2.mx = fmaxf(c2.mx, red_mx[w]);
+            }
+            write_seq(a, q, c2, lane);
+        }
+    }
+}
+
+struct FoldAcc {
+    long long cnt[NCNT];
+    ff sum[NDF];
+    float mx;
+};
+
+__device__ __forceinline__ void fold_zero(FoldAcc &f)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        f.cnt[i] = 0;
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        f.sum[i] = {0.f, 0.f};
+    f.mx = 0.f;
+}
+
+__device__ __forceinline__ void fold_add(FoldAcc &x, const FoldAcc &y)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        x.cnt[i] += y.cnt[i];
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        x.sum[i] = ff_add(x.sum[i], y.sum[i]);
+    x.mx = fmaxf(x.mx, y.mx);
+}
+
+__device__ __forceinline__ FoldAcc fold_shfl_xor(const FoldAcc &x, int o)
+{
+    FoldAcc y;
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        y.cnt[i] = __shfl_xor_sync(0xffffffffu, x.cnt[i], o);
+#pragma unroll
+    for (int i = 0; i < NDF; ++i) {
+        y.sum[i].hi = __shfl_xor_sync(0xffffffffu, x.sum[i].hi, o);
+        y.sum[i].lo = __shfl_xor_sync(0xffffffffu, x.sum[i].lo, o);
+    }
+    y.mx = __shfl_xor_sync(0xffffffffu, x.mx, o);
+    return y;
+}
+
+__device__ __forceinline__ void fold_store(uint32_t *p, const FoldAcc &f)
+{
+    for (int i = 0; i < NCNT; ++i) {
+        p[2 * i] = static_cast<uint32_t>(static_cast<unsigned long long>(f.cnt[i]));
+        p[2 * i + 1] = static_cast<uint32_t>(static_cast<unsigned long long>(f.cnt[i]) >> 32);
+    }
+    for (int i = 0; i < NDF; ++i) {
+        p[2 * NCNT + 2 * i] = __float_as_uint(f.sum[i].hi);
+        p[2 * NCNT + 2 * i + 1] = __float_as_uint(f.sum[i].lo);
+    }
+    p[2 * NCNT + 2 * NDF] = __float_as_uint(f.mx);
+}
+
+__device__ __forceinline__ void fold_load(FoldAcc &f, const uint32_t *p)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        f.cnt[i] = static_cast<long long>(static_cast<unsigned long long>(p[2 * i]) |
+                                          (static_cast<unsigned long long>(p[2 * i + 1]) << 32));
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        f.sum[i] = {__uint_as_float(p[2 * NCNT + 2 * i]), __uint_as_float(p[2 * NCNT + 2 * i + 1])};
+    f.mx = __uint_as_float(p[2 * NCNT + 2 * NDF]);
+}
+
+// Fixed tree over a CTA: xor shuffles inside each warp (lane 0's value is
+// deterministic), then the same over the warp totals in warp 0.  Returns the
+// total on thread 0.
+template <int NTHREADS>
+__device__ __forceinline__ FoldAcc fold_cta(FoldAcc x)
+{
+    constexpr int NW = NTHREADS / 32;
+    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "warps per CTA");
+    __shared__ uint32_t sh[NW][K2_PART_WORDS];
+#pragma unroll 1
+    for (int o = 16; o > 0; o >>= 1) {
+        const FoldAcc y = fold_shfl_xor(x, o);
+        fold_add(x, y);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0)
+        fold_store(sh[warp], x);
+    __syncthreads();
+    FoldAcc t;
+    fold_zero(t);
+    if (warp == 0) {
+        if (lane < NW)
+            fold_load(t, sh[lane]);
+#pragma unroll 1
+        for (int o = NW / 2; o > 0; o >>= 1) {
+            const FoldAcc y = fold_shfl_xor(t, o);
+            fold_add(t, y);
+        }
+    }
+    return t;
+}
+
+// fp32 -> fp64 by moving bits (exact; fp32 subnormals are renormalised).  The
+// batch record is written without fp64 arithmetic, which GB300 runs slowly.
+__device__ __forceinline__ double widen(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint64_t sign = static_cast<uint64_t>(u >> 31) << 63;
+    const uint32_t e = (u >> 23) & 0xffu, m = u & 0x7fffffu;
+    uint64_t bits;
+    if (e == 0u && m == 0u) {
+        bits = sign;
+    } else if (e == 0u) {
+        const int msb = 31 - __clz(static_cast<int>(m));   // value = m * 2^-149
+        bits = sign | (static_cast<uint64_t>(msb - 149 + 1023) << 52) |
+               ((static_cast<uint64_t>(m) << (52 - msb)) & ((uint64_t(1) << 52) - 1));
+    } else if (e == 255u) {
+        bits = sign | (uint64_t(0x7ff) << 52) | (static_cast<uint64_t>(m) << 29);
+    } else {
+        bits = sign | (static_cast<uint64_t>(e - 127 + 1023) << 52) | (static_cast<uint64_t>(m) << 29);
+    }
+    return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// A count (< 2^53) as fp64, by moving bits.
+__device__ __forceinline__ double widen_count(long long n)
+{
+    if (n <= 0)
+        return 0.0;
+    const uint64_t v = static_cast<uint64_t>(n);
+    const int lz = __clzll(static_cast<long long>(v));
+    const uint64_t frac = ((v << lz) << 1) >> 12;
+    return __longlong_as_double(static_cast<long long>((static_cast<uint64_t>(63 - lz + 1023) << 52) | frac));
+}
+
+// The batch record from the folded totals (thread 0).  Means and ratios are
+// fp32 quotients (relative error ~1e-7) of the float-float sums and counts.
+__device__ void write_batch(const K2Args &a, const FoldAcc &t, bool check_offsets)
+{
+    bool bad = t.cnt[P_INVALID] > 0;
+    if (check_offsets)
+        bad = bad || a.off[0] != 0 || static_cast<int64_t>(a.off[a.S]) != a.N;
     if (bad)
         atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
-    auto div = [](double x, double n) { return n > 0.0 ? x / n : 0.0; };
+    const float n_used = static_cast<float>(t.cnt[P_N_USED]);
+    const float n_ne = static_cast<float>(t.cnt[P_NONEMPTY]);
+    const float n_mask = static_cast<float>(t.cnt[P_N_MASK]);
+    auto mean = [&](int i, float n) { return n > 0.f ? widen((t.sum[i].hi + t.sum[i].lo) / n) : 0.0; };
+    auto ratio = [](long long x, float n) { return n > 0.f ? widen(static_cast<float>(x) / n) : 0.0; };
     double *o = a.batch;
-    o[TIM_BATCH_N_MASK] = t[B_MASK];
-    o[TIM_BATCH_N_USED] = t[B_USED];
-    o[TIM_BATCH_N_NAN] = t[B_NAN];
-    o[TIM_BATCH_N_CLIP] = t[B_CLIP];
-    o[TIM_BATCH_MEAN_DELTA] = div(t[B_SD], t[B_USED]);
-    o[TIM_BATCH_MEAN_ABS_DELTA] = div(t[B_SAD], t[B_USED]);
-    o[TIM_BATCH_MAX_ABS_DELTA] = m;
-    o[TIM_BATCH_MEAN_K1] = -div(t[B_SD], t[B_USED]);
-    o[TIM_BATCH_MEAN_K2] = div(t[B_SK2], t[B_USED]);
-    o[TIM_BATCH_MEAN_K3] = div(t[B_SK3], t[B_USED]);
-    o[TIM_BATCH_MEAN_W] = div(t[B_SW], t[B_USED]);
-    o[TIM_BATCH_MEAN_REL] = div(t[B_SREL], t[B_USED]);
-    o[TIM_BATCH_SEQMEAN_K1] = div(t[B_MK1], t[B_NONEMPTY]);
-    o[TIM_BATCH_SEQMEAN_K2] = div(t[B_MK2], t[B_NONEMPTY]);
-    o[TIM_BATCH_SEQMEAN_K3] = div(t[B_MK3], t[B_NONEMPTY]);
-    o[TIM_BATCH_CLIP_RATIO] = div(t[B_CLIP], t[B_MASK]);
-    o[TIM_BATCH_NAN_RATIO] = div(t[B_NAN], t[B_MASK]);
-    o[TIM_BATCH_REJECT_RATIO] = div(t[B_REJ], t[B_NONEMPTY]);
-    o[TIM_BATCH_N_SEQS_NONEMPTY] = t[B_NONEMPTY];
-    o[TIM_BATCH_N_REJECTED] = t[B_REJ];
+    o[TIM_BATCH_N_MASK] = widen_count(t.cnt[P_N_MASK]);
+    o[TIM_BATCH_N_USED] = widen_count(t.cnt[P_N_USED]);
+    o[TIM_BATCH_N_NAN] = widen_count(t.cnt[P_N_NAN]);
+    o[TIM_BATCH_N_CLIP] = widen_count(t.cnt[P_N_CLIP]);
+    o[TIM_BATCH_MEAN_DELTA] = mean(S_SD, n_used);
+    o[TIM_BATCH_MEAN_ABS_DELTA] = mean(S_SAD, n_used);
+    o[TIM_BATCH_MAX_ABS_DELTA] = widen(t.mx);
+    o[TIM_BATCH_MEAN_K1] = n_used > 0.f ? widen(-((t.sum[S_SD].hi + t.sum[S_SD].lo) / n_used)) : 0.0;
+    o[TIM_BATCH_MEAN_K2] = mean(S_SK2, n_used);
+    o[TIM_BATCH_MEAN_K3] = mean(S_SK3, n_used);
+    o[TIM_BATCH_MEAN_W] = mean(S_SW, n_used);
+    o[TIM_BATCH_MEAN_REL] = mean(S_SREL, n_used);
+    o[TIM_BATCH_SEQMEAN_K1] = mean(S_MK1, n_ne);
+    o[TIM_BATCH_SEQMEAN_K2] = mean(S_MK2, n_ne);
+    o[TIM_BATCH_SEQMEAN_K3] = mean(S_MK3, n_ne);
+    o[TIM_BATCH_CLIP_RATIO] = ratio(t.cnt[P_N_CLIP], n_mask);
+    o[TIM_BATCH_NAN_RATIO] = ratio(t.cnt[P_N_NAN], n_mask);
+    o[TIM_BATCH_REJECT_RATIO] = ratio(t.cnt[P_REJ], n_ne);
+    o[TIM_BATCH_N_SEQS_NONEMPTY] = widen_count(t.cnt[P_NONEMPTY]);
+    o[TIM_BATCH_N_REJECTED] = widen_count(t.cnt[P_REJ]);
     if (bad)
         for (int f = 0; f < TIM_BATCH_FIELDS; ++f)
             o[f] = __longlong_as_double(0x7ff8000000000000ll);
 }
 
+// The fold term of sequence s (structure-of-arrays record).
+__device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
+{
+    const size_t S = static_cast<size_t>(a.S);
+    const uint32_t *rc = a.rec + s;
+    FoldAcc y;
+    fold_zero(y);
+    if (rc[R_VALID * S] == 0u) {
+        y.cnt[P_INVALID] = 1;
+    } else {
+        const uint32_t nu = rc[R_N_USED * S];
+        y.cnt[P_N_MASK] = rc[R_N_MASK * S];
+        y.cnt[P_N_USED] = nu;
+        y.cnt[P_N_NAN] = rc[R_N_NAN * S];
+        y.cnt[P_N_CLIP] = rc[R_N_CLIP * S];
+        y.sum[S_SD] = {__uint_as_float(rc[R_SD * S]), 0.f};
+        y.sum[S_SAD] = {__uint_as_float(rc[R_SAD * S]), 0.f};
+        y.sum[S_SK2] = {__uint_as_float(rc[R_SK2 * S]), 0.f};
+        y.sum[S_SK3] = {__uint_as_float(rc[R_SK3 * S]), 0.f};
+        y.sum[S_SW] = {__uint_as_float(rc[R_SW * S]), 0.f};
+        y.sum[S_SREL] = {__uint_as_float(rc[R_SREL * S]), 0.f};
+        y.mx = __uint_as_float(rc[R_MAX * S]);
+        if (nu > 0u) {
+            y.cnt[P_NONEMPTY] = 1;
+            y.cnt[P_REJ] = rc[R_FLAG * S];
+            y.sum[S_MK1] = {__uint_as_float(rc[R_MK1 * S]), 0.f};
+            y.sum[S_MK2] = {__uint_as_float(rc[R_MK2 * S]), 0.f};
+            y.sum[S_MK3] = {__uint_as_float(rc[R_MK3 * S]), 0.f};
+        }
+    }
+    fold_add(x, y);
+}
+
+// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i;
+// with a single CTA it writes the batch record directly.
+__global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a)
+{
+    FoldAcc x;
+    fold_zero(x);
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x;
+#pragma unroll 1
+    for (int k = 0; k < K2_FOLD_SEQS / K2_FOLD_THREADS; ++k) {
+        const int64_t s = base + static_cast<int64_t>(k) * K2_FOLD_THREADS;
+        if (s < a.S)
+            fold_seq(x, a, s);
+    }
+    const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
+    if (threadIdx.x == 0) {
+        if (gridDim.x == 1)
+            write_batch(a, t, false);
+        else
+            fold_store(a.part + static_cast<size_t>(blockIdx.x) * K2_PART_WORDS, t);
+    }
+}
+
+// One CTA folds the partials: thread i takes partials i, i + 256, ... in order.
+__global__ void __launch_bounds__(K2_FOLD_THREADS) k2_final_kernel(const K2Args a, int parts)
+{
+    FoldAcc x;
+    fold_zero(x);
+    for (int p = threadIdx.x; p < parts; p += K2_FOLD_THREADS) {
+        FoldAcc y;
+        fold_load(y, a.part + static_cast<size_t>(p) * K2_PART_WORDS);
+        fold_add(x, y);
+    }
+    const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
+    if (threadIdx.x == 0)
+        write_batch(a, t, false);
+}
+
+// S = 0: only the (all-zero) batch record, after checking the offsets cover [0, N).
+__global__ void k2_empty_kernel(const K2Args a)
+{
+    FoldAcc t;
+    fold_zero(t);
+    write_batch(a, t, true);
+}
+
 } // namespace
+
+cudaError_t k2_prepare_device()
+{
+    return cudaFuncSetAttribute(k2_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K2_SMEM_BYTES);
+}
 
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream)
 {
-    if (a.S > 0) {
-        const int grid = static_cast<int>(std::min<int64_t>(a.S, static_cast<int64_t>(num_sms) * 8));
-        k2_seq_kernel<<<grid, K2_THREADS, 0, stream>>>(a);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return e;
+    if (a.S == 0) {
+        k2_empty_kernel<<<1, 1, 0, stream>>>(a);
+        return cudaGetLastError();
     }
-    k2_batch_kernel<<<1, K2_BATCH_THREADS, 0, stream>>>(a);
-    return cudaGetLastError();
+    const int grid = std::min(a.S, num_sms * K2_CTAS_PER_SM);
+    k2_seq_kernel<<<grid, K2_THREADS, K2_SMEM_BYTES, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int parts = (a.S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
+    k2_fold_kernel<<<parts, K2_FOLD_THREADS, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    if (parts > 1) {
+        k2_final_kernel<<<1, K2_FOLD_THREADS, 0, stream>>>(a, parts);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 } // namespace tim

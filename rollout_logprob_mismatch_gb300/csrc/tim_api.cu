@@ -99,7 +99,7 @@ int device_state(DeviceState **out)
     uint64_t keep = ~0ull;
     if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
         return cuda_fail(e, "cudaMemPoolSetAttribute");
-    if ((e = tim::k1_prepare_device()) != cudaSuccess)
+    if ((e = tim::k1_prepare_device()) != cudaSuccess || (e = tim::k2_prepare_device()) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
     if (!g_encode) {
         void *fn = nullptr;
@@ -257,7 +257,9 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return fail(TIM_ERR_INVALID_ARG, "seq_stats and seq_flags are required when num_seqs > 0");
     if (N > 0 && (!logp_train || !logp_rollout || !mask))
         return fail(TIM_ERR_INVALID_ARG, "null token array");
-    if (!aligned(logp_train, 4) || !aligned(logp_rollout, 4) || !aligned(seq_offsets, 4) ||
+    if (!aligned(logp_train, 16) || !aligned(logp_rollout, 16) || !aligned(mask, 16))
+        return fail(TIM_ERR_INVALID_ARG, "logp_train, logp_rollout and mask must be 16-byte aligned");
+    if (!aligned(seq_offsets, 4) ||
         !aligned(out->seq_stats, 4) || !aligned(out->seq_flags, 4) || !aligned(out->token_weight, 4) ||
         !aligned(out->batch_stats, 8))
         return fail(TIM_ERR_INVALID_ARG, "misaligned array");
@@ -271,12 +273,12 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
     float lcd = static_cast<float>(lc);
     if (static_cast<double>(lcd) > lc)
         lcd = std::nextafter(lcd, -INFINITY);
-    const double tau = std::isnan(out->tau_seq) ? (static_cast<double>(C) - 1.0) - lc
-                                                : static_cast<double>(out->tau_seq);
+    const float tau = std::isnan(out->tau_seq) ? static_cast<float>((static_cast<double>(C) - 1.0) - lc)
+                                               : out->tau_seq;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    const size_t rec_bytes = round_up(static_cast<size_t>(S) * tim::K2_REC * sizeof(double), 256);
+    const size_t rec_bytes = S > 0 ? tim::k2_workspace_bytes(S) : 0;
     if (rec_bytes > 0) {
         cudaError_t e = cudaMallocFromPoolAsync(&ws, rec_bytes, dev->pool, s);
         if (e != cudaSuccess)
@@ -292,12 +294,14 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
     a.C = C;
     a.log_c_down = lcd;
     a.tau = tau;
+    a.wait_budget_ns = wait_budget_ns();
     a.estimator = est;
     a.token_weight = out->token_weight;
     a.seq_stats = out->seq_stats;
     a.seq_flags = out->seq_flags;
     a.batch = out->batch_stats;
-    a.rec = static_cast<double *>(ws);
+    a.rec = static_cast<uint32_t *>(ws);
+    a.part = S > 0 ? a.rec + round_up(static_cast<size_t>(S) * tim::K2_REC_WORDS, 64) : nullptr;
     a.status = dev->status;
     cudaError_t e = tim::k2_launch(a, dev->sms, s);
     cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;

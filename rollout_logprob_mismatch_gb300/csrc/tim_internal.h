@@ -28,7 +28,7 @@ inline int64_t k1_num_chunks(int64_t V) { return (V + K1_VCHUNK - 1) / K1_VCHUNK
 
 struct K1Args {
     const int32_t *targets;   // [N]
-    float2 *part;             // [num_chunks][N]: per-chunk (max, sum of exp(z - max))
+    float2 *part;             // [N][num_chunks]: per-chunk (max, sum of exp(z - max))
     float *za;                // [N]: the target's logit, written by the chunk holding it
     int *status;              // device status word
     int32_t N, D, V;
@@ -44,10 +44,28 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
 cudaError_t k1_prepare_device();   // per-device function attributes
 
 // ---------------------------------------------------------------- mismatch stats (K2)
-constexpr int K2_THREADS = 256;        // tokens per round of one sequence
-constexpr int K2_GROUP = 16;           // rounds summed plainly before the compensated fold
-constexpr int K2_BATCH_THREADS = 512;
-constexpr int K2_REC = 16;             // doubles per sequence record in the workspace
+constexpr int K2_WARPS = 16;                       // warps per CTA (two CTAs per SM)
+constexpr int K2_CTAS_PER_SM = 2;
+constexpr int K2_THREADS = K2_WARPS * 32;
+constexpr int K2_CHUNK = 256;                      // tokens per staged chunk (2 rounds of 128)
+constexpr int K2_STAGES = 2;                       // staged chunks per warp (double buffer)
+constexpr int K2_F_BYTES = K2_CHUNK * 4 + 32;      // one fp32 array's chunk + 16-byte alignment slack
+constexpr int K2_M_BYTES = K2_CHUNK + 32;          // the mask's chunk + slack
+constexpr int K2_STAGE_BYTES = 2 * K2_F_BYTES + K2_M_BYTES;
+constexpr int K2_BAR_BYTES = K2_WARPS * K2_STAGES * 8;
+constexpr int K2_SMEM_BYTES = K2_BAR_BYTES + K2_WARPS * K2_STAGES * K2_STAGE_BYTES;
+constexpr int64_t K2_LONG = 8192;                  // longer sequences are reduced by a whole CTA
+constexpr int K2_FOLD_THREADS = 256;               // fold CTA
+constexpr int K2_FOLD_SEQS = 4 * K2_FOLD_THREADS;  // sequences per fold CTA
+constexpr int K2_REC_WORDS = 16;                   // 4-byte words per sequence record (structure of arrays)
+constexpr int K2_PART_WORDS = 40;                  // 4-byte words per fold partial
+static_assert(K2_STAGE_BYTES % 16 == 0 && K2_BAR_BYTES % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
+
+inline size_t k2_workspace_bytes(int64_t S)
+{
+    const int64_t parts = (S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
+    return static_cast<size_t>(S) * K2_REC_WORDS * 4 + static_cast<size_t>(parts) * K2_PART_WORDS * 4 + 256;
+}
 
 struct K2Args {
     const float *l_tr, *l_ro;
@@ -57,17 +75,20 @@ struct K2Args {
     int64_t N;
     float C;
     float log_c_down;      // largest float <= ln C: delta > this  <=>  r > C
-    double tau;            // rejection threshold (already defaulted)
+    float tau;             // rejection threshold (already defaulted)
+    uint64_t wait_budget_ns;
     int32_t estimator;     // 3 or 1
     float *token_weight;   // optional
     float *seq_stats;      // [S][12]
     int32_t *seq_flags;    // [S]
     double *batch;         // [20]
-    double *rec;           // workspace [S][K2_REC]
+    uint32_t *rec;         // workspace: sequence records, [K2_REC_WORDS][S]
+    uint32_t *part;        // workspace: fold partials, [ceil(S / K2_FOLD_SEQS)][K2_PART_WORDS]
     int *status;
 };
 
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream);
+cudaError_t k2_prepare_device();   // per-device function attributes
 
 // ---------------------------------------------------------------- shared by the C-ABI files
 cudaError_t status_word_address(int **out);   // the library's device status word

@@ -2,8 +2,8 @@
 
 Tolerances (written here, used by every GPU test):
   * token logprob and lse: 2e-3 absolute (the stated contract), per element;
-  * mismatch statistics: 1e-5 relative.  Counts and ratios of counts must be
-    exact.  Signed means (mean delta, mean k1) compare against the natural
+  * mismatch statistics: 1e-5 relative.  Counts must be exact; ratios of
+    counts within 1e-6 relative (the device divides in fp32).  Signed means (mean delta, mean k1) compare against the natural
     scale of their cancellation, max(|oracle|, oracle mean |delta|).  The
     rejection flag may differ only where the oracle's statistic is within
     1e-5 relative of the threshold.
@@ -59,8 +59,10 @@ def assert_flags_match(g_flags, o_flags, o_seq, tau, estimator=3):
 def assert_batch_match(g_b, o_b):
     g = np.asarray(g_b, np.float64)
     o = np.asarray(o_b, np.float64)
-    for f in ("n_mask", "n_used", "n_nan", "n_clip", "clip_ratio", "nan_ratio", "n_seqs_nonempty"):
+    for f in ("n_mask", "n_used", "n_nan", "n_clip", "n_seqs_nonempty"):
         assert g[BF[f]] == o[BF[f]], (f, g[BF[f]], o[BF[f]])
+    for f in ("clip_ratio", "nan_ratio", "reject_ratio"):   # quotients of exact counts
+        _close(g[BF[f]], o[BF[f]], abs(o[BF[f]]) * 0.1, f)
     for f in ("mean_delta", "mean_k1"):
         _close(g[BF[f]], o[BF[f]], max(abs(o[BF[f]]), o[BF["mean_abs_delta"]]), f)
     for f in ("mean_abs_delta", "max_abs_delta", "mean_k2", "mean_k3", "mean_w", "mean_rel",

@@ -73,7 +73,7 @@ def test_tiny_config_from_oracle_logprobs():
 
 def test_edge_cases_empty_masked_nonfinite():
     rng = np.random.default_rng(7)
-    lens = [0, 1, 5, 0, 300, 257, 0, 1024, 3]
+    lens = [0, 1, 5, 0, 300, 257, 0, 1024, 3, 8192, 8193, 9000, 2]
     off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     N = int(off[-1])
     l_tr = wl.draw_train_logprobs(N, 3)
@@ -143,6 +143,7 @@ def test_sequence_records_do_not_depend_on_packing():
     index inside its own sequence)."""
     rng = np.random.default_rng(21)
     lens = rng.integers(1, 3000, size=25)
+    lens[[3, 11]] = [8193, 20000]            # two sequences take the whole-CTA path
     seqs = []
     for i, L in enumerate(lens):
         lt = wl.draw_train_logprobs(int(L), 100 + i)
