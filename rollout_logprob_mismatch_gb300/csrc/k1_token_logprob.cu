@@ -4,10 +4,14 @@
 // Inference Mismatch", section "log p"; LoongSage "Train-Inference Consistency"
 // section 3, FP32 LM head: here bf16 operands with fp32 accumulation).
 //
-// One persistent CTA per SM walks work units (m-tile of 128 tokens, vocabulary
-// chunk of 1024 ids).  Per unit and 256-column tile:
-//   warp 0     TMA: h tile [128 x 64] and W tile [256 x 64] per k-block, 128-byte
-//              swizzle, into a 4-stage shared-memory ring;
+// Persistent clusters of two CTAs (one CTA per SM) walk work units (two
+// m-tiles of 128 tokens, one per CTA, and a vocabulary chunk of 1024 ids).  Per
+// unit and 256-column tile:
+//   warp 0     TMA: the CTA's h tile [128 x 64] and half of the W tile
+//              [128 x 64], multicast to both CTAs of the cluster (each W byte
+//              leaves L2 once per cluster), 128-byte swizzle, into a 4-stage
+//              shared-memory ring; a stage is refilled only when the UMMA of
+//              both CTAs has released it;
 //   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
 //              into one of two TMEM accumulators (2 x 256 columns), k ascending;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
@@ -20,6 +24,8 @@
 // outputs are bit-identical across batch sizes and compositions (llm-infra-atlas
 // "训推一致性与 determinism", sections 1.2 and 6: batch-invariant GEMM with a
 // fixed reduction order).
+#include <algorithm>
+
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
 #include "../../include/tim.h"
@@ -39,13 +45,15 @@ struct Unit {
 // Units run m-tile fastest inside a band of `band` m-tiles, so the CTAs that are
 // resident together share the same W chunk (read once from HBM, then from L2)
 // while the band's h rows stay in L2.  The order affects speed only.
+// Returns the unit's m-group (K1_CLUSTER consecutive m-tiles, one per CTA of
+// the cluster) in .mt and its vocabulary chunk in .ch.
 __device__ __forceinline__ Unit unit_of(int u, const K1Args &a)
 {
     const int per_band = a.band * a.num_chunks;
     const int b = u / per_band;
     const int rem = u - b * per_band;
     const int m0 = b * a.band;
-    const int mb = min(a.band, a.num_m_tiles - m0);
+    const int mb = min(a.band, a.num_m_groups - m0);
     Unit r;
     r.ch = rem / mb;
     r.mt = m0 + (rem - r.ch * mb);
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < K1_STAGES; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(empty(s), K1_CLUSTER);   // released by the UMMA of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
@@ -102,9 +110,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync();   // every CTA's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = blockIdx.x / K1_CLUSTER;
+    const int ncl = gridDim.x / K1_CLUSTER;
+    constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << K1_CLUSTER) - 1);
     const int KB = (a.D + K1_BK - 1) / K1_BK;
     const uint64_t budget = a.wait_budget_ns;
 
@@ -116,21 +129,26 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+            for (int u = cid; ok && u < a.units; u += ncl) {
                 const Unit w = unit_of(u, a);
+                const int mt = w.mt * K1_CLUSTER + static_cast<int>(rank);
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
                     const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
                     for (int kb = 0; kb < KB; ++kb) {
+                        // the stage is free once the UMMA of every CTA of the cluster is done with it
                         if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget)) {
                             ok = false;
                             break;
                         }
+                        // own h tile + this CTA's rows of the W tile, multicast to the whole
+                        // cluster; the barrier counts the W rows the other CTAs send as well
                         mbar_arrive_expect_tx(full(stage), K1_STAGE_BYTES);
-                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kb * K1_BK,
-                                    w.mt * K1_BM, pol_h);
-                        tma_load_2d(sB + stage * K1_B_BYTES, &tmap_w, full(stage), kb * K1_BK, v0,
-                                    pol_w);
+                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kb * K1_BK, mt * K1_BM,
+                                    pol_h);
+                        tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / K1_CLUSTER),
+                                              &tmap_w, full(stage), kb * K1_BK,
+                                              v0 + static_cast<int>(rank) * K1_W_BOX_ROWS, kAllCtas, pol_w);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == K1_STAGES) {
@@ -151,7 +169,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+            for (int u = cid; ok && u < a.units; u += ncl) {
                 const Unit w = unit_of(u, a);
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < K1_BK / 16; ++k)   // +32 bytes along K per step
                             umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
-                        umma_commit(empty(stage));
+                        umma_commit_multicast(empty(stage), kAllCtas);
                         if (++stage == K1_STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -197,10 +215,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+        for (int u = cid; ok && u < a.units; u += ncl) {
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
-            const int row = w.mt * K1_BM + r_in_tile;
+            const int row = (w.mt * K1_CLUSTER + static_cast<int>(rank)) * K1_BM + r_in_tile;
             const int tgt = row < a.N ? __ldg(a.targets + row) : -1;
             float run_m = -INFINITY, run_s = 0.f, zt = 0.f;
             bool found = false;
@@ -275,7 +293,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while another CTA of the cluster may still multicast into its
+    // shared memory or arrive on its barriers
+    __syncwarp();
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -331,10 +352,35 @@ cudaError_t k1_prepare_device()
 }
 
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
-                           int grid, cudaStream_t stream)
+                           cudaStream_t stream)
 {
-    k1_main_kernel<<<grid, K1_THREADS, K1_SMEM_BYTES, stream>>>(tmap_h, tmap_w, a);
-    return cudaGetLastError();
+    static int max_clusters[64] = {0};   // per device, found once (the same value from any thread)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = K1_CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(K1_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = K1_SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
+        int n = 0;
+        cfg.gridDim = dim3(K1_CLUSTER * 1024, 1, 1);
+        e = cudaOccupancyMaxActiveClusters(&n, k1_main_kernel, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        max_clusters[dev] = n > 0 ? n : 1;
+    }
+    const int clusters = static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[dev] : 1));
+    cfg.gridDim = dim3(K1_CLUSTER * clusters, 1, 1);
+    return cudaLaunchKernelEx(&cfg, k1_main_kernel, tmap_h, tmap_w, a);
 }
 
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,

@@ -194,7 +194,7 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
     CUtensorMap th, tw;
     if ((rc = encode_bf16(&th, h, N, D, tim::K1_BM)) != TIM_OK)
         return rc;
-    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_BN)) != TIM_OK)
+    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK)
         return rc;
 
     const size_t part_bytes = round_up(static_cast<size_t>(chunks) * N * sizeof(float2), 256);
@@ -215,14 +215,14 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
     a.V = static_cast<int32_t>(V);
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);
+    const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
+    a.num_m_groups = static_cast<int32_t>(m_groups);
     // h rows of one band stay L2-resident (about 48 MiB) while the band walks V
-    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_BM) * D * 2));
-    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_tiles));
-    a.units = static_cast<int32_t>(m_tiles * chunks);
+    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
+    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
+    a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();
-    const int grid = static_cast<int>(std::min<int64_t>(a.units, dev->sms));
-
-    e = tim::k1_launch_main(th, tw, a, grid, s);
+    e = tim::k1_launch_main(th, tw, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, out_logp, out_lse, s);
     const cudaError_t ef = cudaFreeAsync(ws, s);

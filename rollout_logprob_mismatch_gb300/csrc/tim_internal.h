@@ -17,6 +17,8 @@ constexpr int K1_BK = 64;         // bf16 elements per 128-byte swizzled row
 constexpr int K1_STAGES = 4;      // TMA -> UMMA pipeline depth
 constexpr int K1_VCHUNK = 1024;   // vocabulary columns per split-V partial
 constexpr int K1_THREADS = 192;   // warp 0 TMA, warp 1 UMMA + TMEM, warps 2-5 epilogue
+constexpr int K1_CLUSTER = 2;     // CTAs per cluster: m-tiles sharing (multicasting) one W tile
+constexpr int K1_W_BOX_ROWS = K1_BN / K1_CLUSTER;   // W rows each CTA of a cluster loads
 
 constexpr uint32_t K1_A_BYTES = K1_BM * K1_BK * 2;
 constexpr uint32_t K1_B_BYTES = K1_BN * K1_BK * 2;
@@ -32,12 +34,16 @@ struct K1Args {
     float *za;                // [N]: the target's logit, written by the chunk holding it
     int *status;              // device status word
     int32_t N, D, V;
-    int32_t num_m_tiles, num_chunks, band, units;
+    int32_t num_m_tiles, num_chunks;
+    int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
+    int32_t band, units;      // units = num_m_groups * num_chunks, one per cluster
     uint64_t wait_budget_ns;
 };
 
+// Launches one cluster of K1_CLUSTER CTAs per unit, at most as many clusters
+// as fit on the device at once (persistent).
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
-                           int grid, cudaStream_t stream);
+                           cudaStream_t stream);
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float *out_logp,
                               float *out_lse, cudaStream_t stream);

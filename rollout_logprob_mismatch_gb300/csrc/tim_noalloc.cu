@@ -164,7 +164,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     CUtensorMap th, tw;
     if ((rc = encode(&th, h, N, D, tim::K1_BM)) != TIM_OK)
         return rc;
-    if ((rc = encode(&tw, W, V, D, tim::K1_BN)) != TIM_OK)
+    if ((rc = encode(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK)
         return rc;
 
     tim::K1Args a;
@@ -177,13 +177,14 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.V = static_cast<int32_t>(V);
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);
-    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_BM) * D * 2));
-    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_tiles));
-    a.units = static_cast<int32_t>(m_tiles * chunks);
+    const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
+    a.num_m_groups = static_cast<int32_t>(m_groups);
+    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
+    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
+    a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();
-    const int grid = static_cast<int>(std::min<int64_t>(a.units, dev->sms));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = tim::k1_launch_main(th, tw, a, grid, s);
+    cudaError_t e = tim::k1_launch_main(th, tw, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, out_logp, out_lse, s);
     if (e != cudaSuccess)
