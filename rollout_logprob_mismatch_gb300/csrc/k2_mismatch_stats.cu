@@ -12,13 +12,13 @@
 //
 // Two or three launches, in fp32 and integer arithmetic only (GB300 has very
 // little fp64 throughput):
-//  1. k2_seq_kernel, two 512-thread CTAs per SM.  A sequence of at most 8192
+//  1. k2_seq_kernel, three 256-thread CTAs per SM.  A sequence of at most 8192
 //     tokens is reduced by one warp, a longer one by a whole CTA.  Each warp
-//     stages its sequence through shared memory in chunks of 256 tokens with 1-D
+//     stages its sequence through shared memory in chunks of 448 tokens with 1-D
 //     bulk copies (double-buffered: the next chunk is in flight while this one is
 //     reduced), so a few instructions keep ~75 KB per SM in flight.  Inside a
 //     chunk, lane i owns the tokens at index 64 p + i and 64 p + 32 + i
-//     (p = 0..3), processed two at a time with packed f32x2 arithmetic and
+//     (p = 0..6), processed two at a time with packed f32x2 arithmetic and
 //     summed in that order; chunks follow in order and each chunk's sums are
 //     added to the lane's totals.  A fixed shuffle tree (and for a CTA a
 //     warp-ordered sum) gives the sequence totals; the lanes of one warp write
@@ -199,21 +199,23 @@ __device__ __forceinline__ ChunkView stage_chunk(const K2Args &a, uint8_t *stp, 
 }
 
 // The lane's tokens of one staged chunk: index 64 q + lane (.x) and
-// 64 q + 32 + lane (.y) for q = 0..3, in that order; writes their weights.
-__device__ __forceinline__ void reduce_chunk(TokenAcc &acc, const K2Args &a, const uint8_t *stp,
-                                             const ChunkView &v, int lane)
+// 64 q + 32 + lane (.y) for q = 0 .. K2_CHUNK / 64 - 1, in that order;
+// writes their weights when WEIGHTS.
+template <bool WEIGHTS>
+__device__ __forceinline__ void reduce_chunk_t(TokenAcc &acc, const K2Args &a, const uint8_t *stp,
+                                               const ChunkView &v, int lane)
 {
     const float *lt_s = reinterpret_cast<const float *>(stp) + v.off_f + lane;
     const float *lr_s = reinterpret_cast<const float *>(stp + K2_F_BYTES) + v.off_f + lane;
     const uint8_t *mk_s = stp + 2 * K2_F_BYTES + v.off_m + lane;
-    float *wout = a.token_weight ? a.token_weight + v.t0 + lane : nullptr;
+    float *wout = WEIGHTS ? a.token_weight + v.t0 + lane : nullptr;
     if (v.n == K2_CHUNK) {   // full chunk: no bounds checks
 #pragma unroll
         for (int q = 0; q < K2_CHUNK / 64; ++q) {
             const float2 lt = make_float2(lt_s[64 * q], lt_s[64 * q + 32]);
             const float2 lr = make_float2(lr_s[64 * q], lr_s[64 * q + 32]);
             const float2 w = token_pair(acc, lt, lr, mk_s[64 * q] != 0, mk_s[64 * q + 32] != 0, a.C, a.log_c_down);
-            if (wout) {
+            if (WEIGHTS) {
                 __stcs(wout + 64 * q, w.x);
                 __stcs(wout + 64 * q + 32, w.y);
             }
@@ -228,7 +230,7 @@ __device__ __forceinline__ void reduce_chunk(TokenAcc &acc, const K2Args &a, con
             const bool m0 = in0 && mk_s[64 * q] != 0;
             const bool m1 = in1 && mk_s[64 * q + 32] != 0;
             const float2 w = token_pair(acc, lt, lr, m0, m1, a.C, a.log_c_down);
-            if (wout) {
+            if (WEIGHTS) {
                 if (in0)
                     __stcs(wout + 64 * q, w.x);
                 if (in1)
@@ -238,8 +240,17 @@ __device__ __forceinline__ void reduce_chunk(TokenAcc &acc, const K2Args &a, con
     }
 }
 
-// Adds the chunk's sums (at most 8 tokens per lane) into the lane's totals:
-// two plain fp32 levels keep the rounding error within (8 + chunks) ulps.
+__device__ __forceinline__ void reduce_chunk(TokenAcc &acc, const K2Args &a, const uint8_t *stp,
+                                             const ChunkView &v, int lane)
+{
+    if (a.token_weight)
+        reduce_chunk_t<true>(acc, a, stp, v, lane);
+    else
+        reduce_chunk_t<false>(acc, a, stp, v, lane);
+}
+
+// Adds the chunk's sums (at most 8 tokens per lane and half) into the lane's
+// totals: two plain fp32 levels keep the rounding error within (8 + chunks) ulps.
 __device__ __forceinline__ void fold_chunk(TokenAcc &acc)
 {
 #pragma unroll
@@ -366,7 +377,7 @@ __device__ __forceinline__ bool offsets_ok(const K2Args &a, int s, int64_t b, in
 // Bounded wait on a stage barrier; raises the CTA's abort flag on expiry.
 __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t budget)
 {
-    return mbar_wait(bar, parity, abort, budget);
+    return mbar_wait_sleep(bar, parity, abort, budget);
 }
 
 // Lane-parallel record of a sequence that is skipped by the staged path:
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
             atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
     }
 
-    // ---- phase 2: longer sequences, one CTA each; warp w takes chunks w, w + 16, ...
+    // ---- phase 2: longer sequences, one CTA each; warp w takes chunks w, w + K2_WARPS, ...
     // (the CTA's phase-1 warps met exactly the sequences q = blockIdx.x + k gridDim.x)
     if (!ok)
         *abort_flag = 1;

@@ -50,10 +50,10 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
 cudaError_t k1_prepare_device();   // per-device function attributes
 
 // ---------------------------------------------------------------- mismatch stats (K2)
-constexpr int K2_WARPS = 16;                       // warps per CTA (two CTAs per SM)
-constexpr int K2_CTAS_PER_SM = 2;
+constexpr int K2_WARPS = 8;                        // warps per CTA (three CTAs per SM)
+constexpr int K2_CTAS_PER_SM = 3;
 constexpr int K2_THREADS = K2_WARPS * 32;
-constexpr int K2_CHUNK = 256;                      // tokens per staged chunk (2 rounds of 128)
+constexpr int K2_CHUNK = 448;                      // tokens per staged chunk (a multiple of 64)
 constexpr int K2_STAGES = 2;                       // staged chunks per warp (double buffer)
 constexpr int K2_F_BYTES = K2_CHUNK * 4 + 32;      // one fp32 array's chunk + 16-byte alignment slack
 constexpr int K2_M_BYTES = K2_CHUNK + 32;          // the mask's chunk + slack

@@ -58,6 +58,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Like mbar_try, but the thread may sleep (up to `hint_ns`) until the phase
+// completes instead of returning at once.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (and raises *abort) when `budget_ns` passes first, or false at once
 // when another role has raised *abort.
@@ -77,6 +92,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                 *abort = 1;
                 return false;
             }
+        }
+    }
+}
+
+// mbar_wait for consumers of bulk copies: sleeps in try_wait (hint 20 us) so
+// that a waiting warp does not take issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                uint64_t budget_ns)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_sleep(bar, parity, 20000u))
+            return true;
+        if (*abort)
+            return false;
+        if (global_ns() - t0 > budget_ns) {
+            *abort = 1;
+            return false;
         }
     }
 }
