@@ -25,6 +25,7 @@
 // "训推一致性与 determinism", sections 1.2 and 6: batch-invariant GEMM with a
 // fixed reduction order).
 #include <algorithm>
+#include <cstdlib>
 
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
@@ -344,6 +345,16 @@ __global__ void __launch_bounds__(256)
 }
 
 } // namespace
+
+int64_t k1_band_bytes()
+{
+    static const int64_t v = [] {
+        const char *e = std::getenv("TIM_K1_BAND_MB");
+        const long long mb = e ? std::atoll(e) : 0;
+        return mb > 0 ? static_cast<int64_t>(mb) << 20 : K1_BAND_BYTES;
+    }();
+    return v;
+}
 
 cudaError_t k1_prepare_device()
 {

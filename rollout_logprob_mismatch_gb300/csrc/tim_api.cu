@@ -217,8 +217,7 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
     a.num_chunks = static_cast<int32_t>(chunks);
     const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
     a.num_m_groups = static_cast<int32_t>(m_groups);
-    // h rows of one band stay L2-resident (about 48 MiB) while the band walks V
-    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
+    const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
     a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
     a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();

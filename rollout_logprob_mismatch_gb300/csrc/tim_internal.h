@@ -19,6 +19,11 @@ constexpr int K1_VCHUNK = 1024;   // vocabulary columns per split-V partial
 constexpr int K1_THREADS = 192;   // warp 0 TMA, warp 1 UMMA + TMEM, warps 2-5 epilogue
 constexpr int K1_CLUSTER = 2;     // CTAs per cluster: m-tiles sharing (multicasting) one W tile
 constexpr int K1_W_BOX_ROWS = K1_BN / K1_CLUSTER;   // W rows each CTA of a cluster loads
+// Units walk the vocabulary in bands of m-tiles whose h rows (at most this many
+// bytes) stay in L2 while the band's clusters stream each W chunk from HBM once.
+// (TIM_K1_BAND_MB overrides it; the band changes the order of work, never a result.)
+constexpr int64_t K1_BAND_BYTES = int64_t(32) << 20;   // measured best on the 8192 x 4096 x 151936 head
+int64_t k1_band_bytes();
 
 constexpr uint32_t K1_A_BYTES = K1_BM * K1_BK * 2;
 constexpr uint32_t K1_B_BYTES = K1_BN * K1_BK * 2;

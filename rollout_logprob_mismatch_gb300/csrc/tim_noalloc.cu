@@ -179,7 +179,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.num_chunks = static_cast<int32_t>(chunks);
     const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
     a.num_m_groups = static_cast<int32_t>(m_groups);
-    const int64_t band = std::max<int64_t>(1, (int64_t(48) << 20) / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
+    const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
     a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
     a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();
