@@ -43,6 +43,34 @@ WORKLOAD = "qwen3_8b"
 K2_BW_TOKENS = 1 << 27
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
+# the kernel, keyed by a hash of the kernel's sources at capture time; reported as `traffic`
+# only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
+# profiles/k2_seq_kernel_2e25_tokens.md).
+MEASURED_TRAFFIC = {
+    # token logprob, N = 8192, D = 4096, V = 151936: 3075988736 read + 25264640 written
+    ("k1", "01b23b8a012901ea"): 3075988736 + 25264640,
+    # mismatch pass, 2^25 tokens: 304738048 read + 98114304 written (traffic scales with tokens)
+    ("k2", "5ad5f3910133215d"): 304738048 + 98114304,
+}
+K2_TRAFFIC_TOKENS = 1 << 25
+
+
+def source_hash(kind: str) -> str:
+    import hashlib
+    d = os.path.join(ROOT, "rollout_logprob_mismatch_gb300", "csrc")
+    main = "k1_token_logprob.cu" if kind == "k1" else "k2_mismatch_stats.cu"
+    m = hashlib.sha1()
+    for f in (main, "tim_ptx.cuh", "tim_internal.h"):
+        with open(os.path.join(d, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def measured_traffic(kind: str):
+    return MEASURED_TRAFFIC.get((kind, source_hash(kind)))
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -79,6 +107,12 @@ def max_over_ranks(x: float, dist, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_value(world: int, tokens_per_rank: int, steps: int, t_max: float) -> float:
+    """Whole-job tokens/s: every rank processed `tokens_per_rank` tokens per step;
+    the job took the slowest rank's time."""
+    return world * tokens_per_rank * steps / t_max
 
 
 def barrier(dist, device=None):
@@ -324,7 +358,7 @@ def run_gb300(args):
     t_k2 = [ev[i][1].elapsed_time(ev[i][2]) * 1e-3 for i in range(K)]
     t_step = sum(t_k1) + sum(t_k2)
     t_max = max_over_ranks(t_step, dist, dev)
-    value = world * N * K / t_max
+    value = aggregate_value(world, N, K, t_max)
     k1_avg = float(np.mean(t_k1))
     k2_avg = float(np.mean(t_k2))
     flops = 2.0 * N * V * D
@@ -375,6 +409,7 @@ def run_gb300(args):
     d2h = b_host.numel() * 8 + s_host.numel() * 4 + f_host.numel() * 4
 
     k2_bw = mismatch_bandwidth(tim, dev, stream, peaks) if not args.skip_k2_bandwidth else None
+    sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
     tim.check()
 
     if rank != 0:
@@ -395,20 +430,57 @@ def run_gb300(args):
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": "%s bf16 burst" % peaks["source"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "traffic": measured_traffic("k1") if (N, D, V) == (8192, 4096, 151936) else None,
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "algorithmic_bytes_per_launch": 2 * N * D + 2 * V * D + 12 * N,
+                     "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": k1_avg * 1e3},
         "mismatch_pass": {"avg_launch_us": k2_avg * 1e6,
                           "algorithmic_bytes": 9 * N + 4 * (S + 1) + 52 * S + 160},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * N * K / t_e2e, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": aggregate_value(world, N, K, t_e2e), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": 4 * K,
         "clocks": clocks.summary(),
     }
     if k2_bw is not None:
         line["mismatch_bandwidth"] = k2_bw
+    if sweep is not None:
+        line["sweep"] = sweep
     print(json.dumps(line), flush=True)
     return 0
+
+
+def batch_size_sweep(tim, dev, stream, Wd, D, V, peaks, sizes=(1, 7, 512, 4096, 32768), reps=5):
+    """tim_token_logprob alone on the same head at the batch-invariance sweep's
+    batch sizes (random rows; L2 flushed before each launch).  Small batches
+    are bound by reading W from HBM, so GB/s of W + h is reported beside TFLOP/s."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = []
+    for n in sizes:
+        h = torch.randn((n, D), generator=g, device=dev).to(torch.bfloat16)
+        a = torch.randint(0, V, (n,), generator=g, device=dev, dtype=torch.int32)
+        lp = torch.empty(n, dtype=torch.float32, device=dev)
+        lse = torch.empty(n, dtype=torch.float32, device=dev)
+        for _ in range(2):
+            tim.token_logprob(h, Wd, a, lp, lse)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(i)
+            ev[i][0].record(stream)
+            tim.token_logprob(h, Wd, a, lp, lse)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t = float(np.mean([e0.elapsed_time(e1) * 1e-3 for e0, e1 in ev]))
+        bytes_ = 2.0 * V * D + 2.0 * n * D + 12.0 * n
+        out.append({"N": n, "avg_launch_us": t * 1e6, "tokens_per_s": n / t,
+                    "tflops": 2.0 * n * V * D / t / 1e12, "hbm_gbs": bytes_ / t / 1e9,
+                    "hbm_frac": bytes_ / t / 1e9 / peaks["hbm_gbs"]})
+        del h, a, lp, lse
+    return out
 
 
 def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
@@ -445,9 +517,11 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
     t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
     algo = 9 * Nt + 4 * Nt + 4 * (S + 1) + 52 * S + 160
     gbs = algo / t / 1e9
+    tr = measured_traffic("k2")
     return {"tokens": Nt, "num_seqs": S, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo,
             "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-            "frac_of_8000": gbs / 8000.0, "bound": "hbm"}
+            "frac_of_8000": gbs / 8000.0, "bound": "hbm",
+            "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
 
 
 def main(argv=None):
@@ -458,6 +532,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-k2-bandwidth", action="store_true")
+    ap.add_argument("--skip-sweep", action="store_true")
     ap.add_argument("--only", choices=["k1", "k2", "k2bw"], default=None,
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,

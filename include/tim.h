@@ -207,6 +207,17 @@ TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollou
                        const uint8_t *mask, const int32_t *seq_offsets, float C,
                        const tim_mismatch_out *out, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ failure-detection self-test
+ *
+ * No counterpart on the pages.  Runs the library's bounded-wait path on purpose,
+ * without any fault: one warp waits on an mbarrier that nothing arrives on and
+ * gives up after budget_us microseconds (1 .. 1000000), recording
+ * TIM_ERR_TIMEOUT in the status word exactly as an expired pipeline wait in
+ * the compute kernels does.  Asynchronous on `stream`; tim_check() then
+ * returns TIM_ERR_TIMEOUT, and the device stays usable.
+ */
+TIM_API int tim_selftest_wait_timeout(uint32_t budget_us, tim_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronises `stream`, then returns and clears the status word the kernels

@@ -25,7 +25,7 @@ import threading
 
 __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "tim_mismatch_out", "lib_path", "load",
-    "tim_token_logprob", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_check", "tim_last_error", "tim_version",
+    "tim_token_logprob", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
     "token_logprob", "mismatch_stats", "check",
 ]
 
@@ -93,6 +93,8 @@ def load():
             lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
                                                ctypes.POINTER(tim_mismatch_out), P]
             lib.tim_mismatch_stats.restype = ctypes.c_int
+            lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+            lib.tim_selftest_wait_timeout.restype = ctypes.c_int
             lib.tim_check.argtypes = [P]
             lib.tim_check.restype = ctypes.c_int
             lib.tim_last_error.argtypes = []
@@ -119,6 +121,12 @@ def tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C, out: tim_
                        stream) -> int:
     return load().tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, float(C),
                                      ctypes.byref(out), stream)
+
+
+def tim_selftest_wait_timeout(budget_us, stream) -> int:
+    """C ABI: a kernel waits on a barrier nothing arrives on, for budget_us
+    microseconds, and records TIM_ERR_TIMEOUT (no fault; see include/tim.h)."""
+    return load().tim_selftest_wait_timeout(budget_us, stream)
 
 
 def tim_check(stream) -> int:

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             // no TMA write may still be landing in shared memory when the CTA exits
             for (int s = 0; s < K1_STAGES; ++s)
                 if (issued & (1u << s))
-                    drain_wait(full(s), (last_par >> s) & 1u, budget);
+                    drain_wait(full(s), (last_par >> s) & 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             }
             // every UMMA issued has finished before TMEM is released
             umma_commit(drain);
-            drain_wait(drain, 0, budget);
+            drain_wait(drain, 0);
         }
     } else {
         // ---------------------------------------------------- epilogue, warps 2..5

@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
         // staged copies may still be landing: give them their time before the CTA exits
         for (int i = 0; i < K2_STAGES; ++i)
             if (pending & (1u << i))
-                drain_wait(bar0 + 8u * i, (parity >> i) & 1u, budget);
+                drain_wait(bar0 + 8u * i, (parity >> i) & 1u);
         pending = 0;
         if (lane == 0)
             atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
         if (!ok) {
             for (int i = 0; i < K2_STAGES; ++i)
                 if (pending & (1u << i))
-                    drain_wait(bar0 + 8u * i, (parity >> i) & 1u, budget);
+                    drain_wait(bar0 + 8u * i, (parity >> i) & 1u);
             pending = 0;
             if (lane == 0)
                 atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));

@@ -116,9 +116,13 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
     }
 }
 
+// How long a CTA lets its in-flight asynchronous copies land after an abort
+// (independent of the abort budget, so a short abort budget never cuts it).
+constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+
 // Bounded wait that ignores the abort flag: used only to let in-flight
 // asynchronous work land before a CTA releases its shared memory or TMEM.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns)
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns = kDrainBudgetNs)
 {
     if (mbar_try(bar, parity))
         return;

@@ -1,0 +1,60 @@
+"""The multi-process side of bench.py on CPU ranks (gloo, world size 2): the
+timed region's barrier, the max over ranks and the whole-job aggregate, and the
+reference arm's rank behaviour.  The data path itself has no collective: each
+rank runs its own replica (rows and sequences shard with no exchange)."""
+import os
+import socket
+
+import pytest
+
+import bench
+
+torch = pytest.importorskip("torch")
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    d = bench.dist_init(world, "gloo")
+    t = bench.max_over_ranks(1.0 + rank, d)      # rank r took 1 + r seconds
+    bench.barrier(d)
+    q.put((rank, t, bench.aggregate_value(world, 8192, 10, t)))
+    dist.destroy_process_group()
+
+
+def test_two_ranks_report_the_slowest_rank_and_the_whole_job():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [o[1] for o in out] == [2.0, 2.0]
+    assert all(o[2] == pytest.approx(2 * 8192 * 10 / 2.0) for o in out)
+
+
+def test_reference_arm_prints_only_on_rank_zero(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.dist_init(1, "gloo") is None
+    assert bench.max_over_ranks(3.5, None) == 3.5
+    assert bench.aggregate_value(1, 8192, 30, 0.2) == pytest.approx(8192 * 30 / 0.2)
