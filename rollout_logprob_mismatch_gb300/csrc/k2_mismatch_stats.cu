@@ -444,7 +444,14 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     }
     if (tid == 0)
         abort_flag_s = 0;
-    __syncthreads();
+    // Does this CTA have a sequence longer than K2_LONG (phase 2)?  Most batches
+    // have none, and then no warp waits for the others at the phase boundary.
+    bool mine = false;
+    for (int q = blockIdx.x + tid * gridDim.x; q < a.S; q += K2_THREADS * gridDim.x) {
+        const int64_t b = a.off[q], e = a.off[q + 1];
+        mine = mine || (offsets_ok(a, q, b, e) && e - b > K2_LONG);
+    }
+    const bool has_long = __syncthreads_or(mine) != 0;
     const uint64_t pol = l2_policy_evict_first();
     const uint64_t budget = a.wait_budget_ns;
     uint32_t parity = 0;    // bit i: parity of stage i's next completion
@@ -513,6 +520,8 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
 
     // ---- phase 2: longer sequences, one CTA each; warp w takes chunks w, w + K2_WARPS, ...
     // (the CTA's phase-1 warps met exactly the sequences q = blockIdx.x + k gridDim.x)
+    if (!has_long)   // uniform over the CTA
+        return;
     if (!ok)
         *abort_flag = 1;
     __syncthreads();
