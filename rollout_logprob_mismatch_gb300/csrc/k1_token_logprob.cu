@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         tma_prefetch_desc(&tmap_h);
         tma_prefetch_desc(&tmap_w);
     }
+    pdl_wait();                // h, W, targets may be written by the previous kernel
+    pdl_launch_dependents();   // the combine kernel may start launching
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
@@ -317,6 +319,8 @@ __global__ void __launch_bounds__(256)
                       const int32_t *__restrict__ targets, int32_t N, int32_t V, int32_t num_chunks,
                       float *__restrict__ out_logp, float *__restrict__ out_lse)
 {
+    pdl_wait();   // the partials come from k1_main_kernel
+    pdl_launch_dependents();
     const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= N)
@@ -371,11 +375,12 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = K1_CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.blockDim = dim3(K1_THREADS, 1, 1);
     cfg.dynamicSmemBytes = K1_SMEM_BYTES;
     cfg.stream = stream;
@@ -391,6 +396,7 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     }
     const int clusters = static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[dev] : 1));
     cfg.gridDim = dim3(K1_CLUSTER * clusters, 1, 1);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k1_main_kernel, tmap_h, tmap_w, a);
 }
 
@@ -400,9 +406,14 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
 {
     const int threads = 256;   // 8 rows per CTA, one warp each
     const int blocks = static_cast<int>((static_cast<int64_t>(N) * 32 + threads - 1) / threads);
-    k1_combine_kernel<<<blocks, threads, 0, stream>>>(part, za, targets, N, V, num_chunks, out_logp,
-                                                      out_lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k1_combine_kernel, part, za, targets, N, V, num_chunks, out_logp, out_lse);
 }
 
 } // namespace tim

@@ -444,6 +444,8 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     }
     if (tid == 0)
         abort_flag_s = 0;
+    pdl_wait();                // the inputs may be written by the previous kernel
+    pdl_launch_dependents();   // the fold kernel may start launching
     // Does this CTA have a sequence longer than K2_LONG (phase 2)?  Most batches
     // have none, and then no warp waits for the others at the phase boundary.
     bool mine = false;
@@ -810,6 +812,8 @@ __device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
 // with a single CTA it writes the batch record directly.
 __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a)
 {
+    pdl_wait();   // the records come from k2_seq_kernel
+    pdl_launch_dependents();
     FoldAcc x;
     fold_zero(x);
     const int64_t base = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x;
@@ -831,6 +835,7 @@ __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a
 // One CTA folds the partials: thread i takes partials i, i + 256, ... in order.
 __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_final_kernel(const K2Args a, int parts)
 {
+    pdl_wait();   // the partials come from k2_fold_kernel
     FoldAcc x;
     fold_zero(x);
     for (int p = threadIdx.x; p < parts; p += K2_FOLD_THREADS) {
@@ -864,18 +869,26 @@ cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream)
         k2_empty_kernel<<<1, 1, 0, stream>>>(a);
         return cudaGetLastError();
     }
-    const int grid = std::min(a.S, num_sms * K2_CTAS_PER_SM);
-    k2_seq_kernel<<<grid, K2_THREADS, K2_SMEM_BYTES, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(std::min(a.S, num_sms * K2_CTAS_PER_SM), 1, 1);
+    cfg.blockDim = dim3(K2_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = K2_SMEM_BYTES;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k2_seq_kernel, a);
     if (e != cudaSuccess)
         return e;
     const int parts = (a.S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
-    k2_fold_kernel<<<parts, K2_FOLD_THREADS, 0, stream>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    cfg.gridDim = dim3(parts, 1, 1);
+    cfg.blockDim = dim3(K2_FOLD_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    if ((e = cudaLaunchKernelEx(&cfg, k2_fold_kernel, a)) != cudaSuccess)
         return e;
     if (parts > 1) {
-        k2_final_kernel<<<1, K2_FOLD_THREADS, 0, stream>>>(a, parts);
-        e = cudaGetLastError();
+        cfg.gridDim = dim3(1, 1, 1);
+        e = cudaLaunchKernelEx(&cfg, k2_final_kernel, a, parts);
     }
     return e;
 }

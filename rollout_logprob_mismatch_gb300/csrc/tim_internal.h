@@ -101,6 +101,16 @@ struct K2Args {
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream);
 cudaError_t k2_prepare_device();   // per-device function attributes
 
+// Launch attribute list that makes a launch a programmatic dependent of the
+// previous kernel in its stream (its kernel calls pdl_wait() before reading).
+inline cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
+}
+
 // ---------------------------------------------------------------- shared by the C-ABI files
 cudaError_t status_word_address(int **out);   // the library's device status word
 int record_error(int code, const char *msg);  // message for tim_last_error()

@@ -22,6 +22,23 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before its predecessor in the
+// stream ends; it must wait here before it reads anything the predecessor (or
+// any earlier work) wrote.  Without the attribute this returns at once.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream (if launched as a dependent) start its
+// launch now; it still waits in pdl_wait() until this grid has finished.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
