@@ -55,7 +55,7 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             lib.oracle_token_logprob.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64,
-                                                 ctypes.c_int64, P, P, ctypes.c_int]
+                                                 ctypes.c_int64, ctypes.c_double, P, P, ctypes.c_int]
             lib.oracle_token_logprob.restype = ctypes.c_int
             lib.oracle_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int64,
                                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32,
@@ -72,8 +72,9 @@ def _ptr(a: np.ndarray):
 
 
 def token_logprob(h_bf16: np.ndarray, W_bf16: np.ndarray, targets: np.ndarray,
-                  rows=None, nthreads: int | None = None):
-    """(logp, lse) as float64 arrays, for `rows` of h (all rows if None).
+                  rows=None, nthreads: int | None = None, temperature: float = 1.0):
+    """(logp, lse) as float64 arrays, for `rows` of h (all rows if None), of
+    log softmax(h W^T / temperature) at the targets.
 
     h_bf16 uint16 [N, D], W_bf16 uint16 [V, D] (bf16 bit patterns),
     targets int32 [N]."""
@@ -95,7 +96,7 @@ def token_logprob(h_bf16: np.ndarray, W_bf16: np.ndarray, targets: np.ndarray,
     lse = np.empty(R, dtype=np.float64)
     nt = nthreads or max(1, len(os.sched_getaffinity(0)))
     rc = lib.oracle_token_logprob(_ptr(h), _ptr(W), _ptr(a), None if r is None else _ptr(r), R,
-                                  D, V, _ptr(logp), _ptr(lse), nt)
+                                  D, V, float(temperature), _ptr(logp), _ptr(lse), nt)
     if rc != 0:
         raise RuntimeError("oracle_token_logprob failed")
     return logp, lse

@@ -60,11 +60,12 @@ static double bf16_value(uint16_t b)
     return (double)f;
 }
 
-/* One row of the definition: z_v = sum_d h_d W[v, d]  (d ascending),
- * m = max_v z_v, S = sum_v exp(z_v - m) (v ascending), lse = m + log S,
- * logp = z_a - lse. */
+/* One row of the definition: z_v = (sum_d h_d W[v, d]) / temperature
+ * (d ascending; the sampling distribution softmax(z / tau) of the icarus
+ * "logits processor" section, tau = 1 for raw logits), m = max_v z_v,
+ * S = sum_v exp(z_v - m) (v ascending), lse = m + log S, logp = z_a - lse. */
 static void oracle_row(const uint16_t *h_row, const uint16_t *W, int32_t a,
-                       int64_t D, int64_t V, double *hd, double *z,
+                       int64_t D, int64_t V, double temperature, double *hd, double *z,
                        double *out_logp, double *out_lse)
 {
     for (int64_t d = 0; d < D; ++d)
@@ -74,7 +75,7 @@ static void oracle_row(const uint16_t *h_row, const uint16_t *W, int32_t a,
         double acc = 0.0;
         for (int64_t d = 0; d < D; ++d)
             acc += hd[d] * bf16_value(w[d]);
-        z[v] = acc;
+        z[v] = acc / temperature;
     }
     double m = -INFINITY;
     for (int64_t v = 0; v < V; ++v)
@@ -93,6 +94,7 @@ typedef struct {
     const int32_t *targets;
     const int64_t *rows;
     int64_t R, D, V;
+    double temperature;
     double *out_logp, *out_lse;
     int tid, nthreads, failed;
 } row_job;
@@ -110,7 +112,7 @@ static void *row_worker(void *p)
     }
     for (int64_t i = j->tid; i < j->R; i += j->nthreads) {
         int64_t t = j->rows ? j->rows[i] : i;
-        oracle_row(j->h + t * j->D, j->W, j->targets[t], j->D, j->V, hd, z,
+        oracle_row(j->h + t * j->D, j->W, j->targets[t], j->D, j->V, j->temperature, hd, z,
                    j->out_logp + i, j->out_lse + i);
     }
     free(hd);
@@ -119,14 +121,17 @@ static void *row_worker(void *p)
 }
 
 /* Rows `rows[0..R)` of h (all N rows when rows == NULL, then R = N).
- * h bf16 [N, D], W bf16 [V, D], targets int32 [N]; outputs double [R].
+ * h bf16 [N, D], W bf16 [V, D], targets int32 [N], temperature > 0 (1 for raw
+ * logits); outputs double [R].
  * Rows are spread over `nthreads` threads; each row is computed alone.
  * Returns 0, or -1 on bad arguments / allocation failure. */
 int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *targets,
-                         const int64_t *rows, int64_t R, int64_t D, int64_t V,
+                         const int64_t *rows, int64_t R, int64_t D, int64_t V, double temperature,
                          double *out_logp, double *out_lse, int nthreads)
 {
     if (R < 0 || D <= 0 || V <= 0 || !h || !W || !targets || !out_logp || !out_lse)
+        return -1;
+    if (!(temperature > 0.0) || !isfinite(temperature))
         return -1;
     if (R == 0)
         return 0;
@@ -143,7 +148,7 @@ int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *ta
     }
     int rc = 0;
     for (int k = 0; k < nthreads; ++k) {
-        jobs[k] = (row_job){h, W, targets, rows, R, D, V, out_logp, out_lse, k, nthreads, 0};
+        jobs[k] = (row_job){h, W, targets, rows, R, D, V, temperature, out_logp, out_lse, k, nthreads, 0};
         if (pthread_create(&th[k], NULL, row_worker, &jobs[k]) != 0) {
             row_worker(&jobs[k]); /* run inline if no thread could be made */
             th[k] = 0;

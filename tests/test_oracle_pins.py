@@ -16,6 +16,7 @@ import scipy.special
 import scipy.stats
 
 import oracle
+import workloads as wl
 from workloads import bf16_round, bf16_to_f32
 
 F = {n: i for i, n in enumerate(oracle.SEQ_FIELDS)}
@@ -332,3 +333,29 @@ def test_row_subset_matches_full():
     rows = np.array([19, 0, 7])
     lr, sr = oracle.token_logprob(h, W, a, rows=rows, nthreads=2)
     assert np.array_equal(lr, lf[rows]) and np.array_equal(sr, sf[rows])
+
+
+# --------------------------------------------------------------- temperature
+def test_temperature_matches_scaled_weights_exactly():
+    """softmax(z / 2) with W equals softmax(z) with W / 2 (an exact bf16 scale):
+    the temperature divides the logits, not the probabilities (icarus, section
+    "logits processor": sampling uses softmax(z / tau))."""
+    h, W, a = _rand_head(9, 48, 700, 21, w_std=0.3)
+    W_half = wl.bf16_round(wl.bf16_to_f32(W) * np.float32(0.5))
+    l2, s2 = oracle.token_logprob(h, W, a, temperature=2.0)
+    l1, s1 = oracle.token_logprob(h, W_half, a)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(s2, s1, rtol=0, atol=1e-13)
+
+
+def test_temperature_limits_and_two_class_form():
+    """tau -> infinity flattens to -log V; V = 2 gives log sigmoid((z1 - z0) / tau)."""
+    h, W, a = _rand_head(5, 32, 300, 22, w_std=0.5)
+    l, _ = oracle.token_logprob(h, W, a, temperature=1e9)
+    assert np.max(np.abs(l + math.log(300))) < 1e-6
+    h2, W2, _ = _rand_head(16, 16, 2, 23, w_std=0.5)
+    lp, _ = oracle.token_logprob(h2, W2, np.ones(16, np.int32), temperature=0.7)
+    z = bf16_to_f32(h2).astype(np.float64) @ bf16_to_f32(W2).astype(np.float64).T
+    np.testing.assert_allclose(lp, scipy.special.log_expit((z[:, 1] - z[:, 0]) / 0.7), rtol=0, atol=1e-12)
+    with pytest.raises(RuntimeError):
+        oracle.token_logprob(h2, W2, np.ones(16, np.int32), temperature=0.0)
