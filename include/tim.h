@@ -96,6 +96,15 @@ TIM_API int tim_token_logprob(const void *h, const void *W, const int32_t *targe
                       int64_t N, int64_t D, int64_t V,
                       float *out_logp, float *out_lse, tim_stream_t stream);
 
+/* Same, at a sampling temperature: l_t = log softmax(h_t W^T / temperature)[a_t]
+ * and lse_t = log sum_v exp(h_t . W_v / temperature).  The rollout engine samples
+ * from softmax(z / tau) (icarus page, section "logits processor"), and both sides
+ * must use the same tau.  temperature > 0 and finite (else TIM_ERR_INVALID_ARG);
+ * temperature = 1 gives the bits of tim_token_logprob.  Everything else as above. */
+TIM_API int tim_token_logprob_temperature(const void *h, const void *W, const int32_t *targets,
+                                          int64_t N, int64_t D, int64_t V, float temperature,
+                                          float *out_logp, float *out_lse, tim_stream_t stream);
+
 /* ------------------------------------------------------------------ token logprob, no allocation
  *
  * No counterpart on the pages: a library-side variant of tim_token_logprob for

@@ -25,7 +25,7 @@ import threading
 
 __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "tim_mismatch_out", "lib_path", "load",
-    "tim_token_logprob", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
     "token_logprob", "mismatch_stats", "check",
 ]
 
@@ -88,6 +88,8 @@ def load():
             P, I64 = ctypes.c_void_p, ctypes.c_int64
             lib.tim_token_logprob.argtypes = [P, P, P, I64, I64, I64, P, P, P]
             lib.tim_token_logprob.restype = ctypes.c_int
+            lib.tim_token_logprob_temperature.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
+            lib.tim_token_logprob_temperature.restype = ctypes.c_int
             lib.tim_token_logprob_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, P]
             lib.tim_token_logprob_noalloc.restype = ctypes.c_int
             lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
@@ -109,6 +111,12 @@ def load():
 def tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream) -> int:
     """C ABI call with integer device addresses; returns the tim_status code."""
     return load().tim_token_logprob(h, W, targets, N, D, V, out_logp, out_lse, stream)
+
+
+def tim_token_logprob_temperature(h, W, targets, N, D, V, temperature, out_logp, out_lse, stream) -> int:
+    """C ABI call of the token logprob at a sampling temperature; returns the tim_status code."""
+    return load().tim_token_logprob_temperature(h, W, targets, N, D, V, float(temperature), out_logp,
+                                                out_lse, stream)
 
 
 def tim_token_logprob_noalloc(h, W, targets, N, D, V, out_logp, out_lse, stream) -> int:
@@ -169,8 +177,9 @@ def _need(t, name, dtype, ndim, device=None):
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
 
 
-def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None):
-    """(logp [N] fp32, lse [N] fp32) for bf16 h [N, D], bf16 W [V, D], int32 targets [N]."""
+def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None, temperature: float = 1.0):
+    """(logp [N] fp32, lse [N] fp32) for bf16 h [N, D], bf16 W [V, D], int32 targets [N]:
+    log softmax(h W^T / temperature) at the targets (temperature 1: raw logits)."""
     import torch
     _need(h, "h", torch.bfloat16, 2)
     dev = h.device
@@ -188,8 +197,13 @@ def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None):
     _need(out_logp, "out_logp", torch.float32, 1, dev)
     _need(out_lse, "out_lse", torch.float32, 1, dev)
     with torch.cuda.device(dev):
-        rc = tim_token_logprob(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
-                               out_logp.data_ptr(), out_lse.data_ptr(), _stream_handle(stream, dev))
+        if temperature == 1.0:
+            rc = tim_token_logprob(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
+                                   out_logp.data_ptr(), out_lse.data_ptr(), _stream_handle(stream, dev))
+        else:
+            rc = tim_token_logprob_temperature(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
+                                               temperature, out_logp.data_ptr(), out_lse.data_ptr(),
+                                               _stream_handle(stream, dev))
     _raise_if(rc)
     return out_logp, out_lse
 

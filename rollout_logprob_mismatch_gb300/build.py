@@ -25,7 +25,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+          "--expt-relaxed-constexpr", "-Werror", "all-warnings", "-I", INCLUDE, "-I", CSRC]
 
 
 def nvcc() -> str:

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         // ---------------------------------------------------- epilogue, warps 2..5
         const int q = warp & 3;                 // TMEM lane quarter this warp may read
         const int r_in_tile = q * 32 + lane;
+        const float zscale = LOG2E * a.inv_temp;   // e^(z / tau) = 2^(z zscale)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -256,15 +257,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         m3 = fmaxf(m3, v[jj + 3]);
                     }
                     const float new_m = fmaxf(run_m, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
-                    const float nm = new_m * LOG2E;
-                    const float rescale = ex2(fmaf(run_m, LOG2E, -nm));
+                    const float nm = new_m * zscale;
+                    const float rescale = ex2(fmaf(run_m, zscale, -nm));
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int jj = 0; jj < SUBCOLS; jj += 4) {
-                        s0 += ex2(fmaf(v[jj], LOG2E, -nm));
-                        s1 += ex2(fmaf(v[jj + 1], LOG2E, -nm));
-                        s2 += ex2(fmaf(v[jj + 2], LOG2E, -nm));
-                        s3 += ex2(fmaf(v[jj + 3], LOG2E, -nm));
+                        s0 += ex2(fmaf(v[jj], zscale, -nm));
+                        s1 += ex2(fmaf(v[jj + 1], zscale, -nm));
+                        s2 += ex2(fmaf(v[jj + 2], zscale, -nm));
+                        s3 += ex2(fmaf(v[jj + 3], zscale, -nm));
                     }
                     run_s = fmaf(run_s, rescale, (s0 + s1) + (s2 + s3));
                     run_m = new_m;
@@ -309,15 +310,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
 }
 
-// Folds the per-chunk (max, sum) pairs of a row: M = max_c m_c,
-// S = sum_c s_c e^(m_c - M), lse = M + ln S, l = z_a - lse.  One warp per row:
+// Folds the per-chunk (max, sum) pairs of a row (m_c is a max of raw logits,
+// s_c a sum of e^((z - m_c) / tau)): M = max_c m_c, S = sum_c s_c e^((m_c - M) / tau),
+// lse = M / tau + ln S, l = z_a / tau - lse.  One warp per row:
 // lane i takes chunks i, i + 32, ... in order, then a fixed xor-shuffle tree sums
 // the lanes and lane 0's value is used.  The order depends on the number of
 // chunks (a function of V) only.
 __global__ void __launch_bounds__(256)
     k1_combine_kernel(const float2 *__restrict__ part, const float *__restrict__ za,
                       const int32_t *__restrict__ targets, int32_t N, int32_t V, int32_t num_chunks,
-                      float *__restrict__ out_logp, float *__restrict__ out_lse)
+                      float inv_temp, float *__restrict__ out_logp, float *__restrict__ out_lse)
 {
     pdl_wait();   // the partials come from k1_main_kernel
     pdl_launch_dependents();
@@ -335,16 +337,16 @@ __global__ void __launch_bounds__(256)
     float S = 0.f;
     for (int c = lane; c < num_chunks; c += 32) {
         const float2 q = p[c];
-        S = fmaf(q.y, expf(q.x - M), S);
+        S = fmaf(q.y, expf((q.x - M) * inv_temp), S);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         S += __shfl_xor_sync(0xffffffffu, S, o);
     if (lane == 0) {
-        const float lse = M + logf(S);
+        const float lse = M * inv_temp + logf(S);
         out_lse[t] = lse;
         const int a = targets[t];
-        out_logp[t] = (a >= 0 && a < V) ? za[t] - lse : __int_as_float(0x7fc00000);
+        out_logp[t] = (a >= 0 && a < V) ? za[t] * inv_temp - lse : __int_as_float(0x7fc00000);
     }
 }
 
@@ -401,7 +403,7 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
 }
 
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
-                              int32_t N, int32_t V, int32_t num_chunks, float *out_logp,
+                              int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream)
 {
     const int threads = 256;   // 8 rows per CTA, one warp each
@@ -413,7 +415,8 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k1_combine_kernel, part, za, targets, N, V, num_chunks, out_logp, out_lse);
+    return cudaLaunchKernelEx(&cfg, k1_combine_kernel, part, za, targets, N, V, num_chunks, inv_temp, out_logp,
+                              out_lse);
 }
 
 } // namespace tim

@@ -162,8 +162,13 @@ int tim_version(void) { return kVersion; }
 
 const char *tim_last_error(void) { return g_msg; }
 
-int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D,
-                      int64_t V, float *out_logp, float *out_lse, tim_stream_t stream)
+} // extern "C"
+
+namespace {
+
+// The fused token logprob at 1 / temperature `inv_temp` (both entry points).
+int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D, int64_t V,
+                  float inv_temp, float *out_logp, float *out_lse, tim_stream_t stream)
 {
     if (N < 0 || N >= (int64_t(1) << 31))
         return fail(TIM_ERR_INVALID_ARG, "N = %lld out of range [0, 2^31)", static_cast<long long>(N));
@@ -210,6 +215,7 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
     a.part = static_cast<float2 *>(ws);
     a.za = reinterpret_cast<float *>(static_cast<char *>(ws) + part_bytes);
     a.status = dev->status;
+    a.inv_temp = inv_temp;
     a.N = static_cast<int32_t>(N);
     a.D = static_cast<int32_t>(D);
     a.V = static_cast<int32_t>(V);
@@ -223,7 +229,8 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
     a.wait_budget_ns = wait_budget_ns();
     e = tim::k1_launch_main(th, tw, a, s);
     if (e == cudaSuccess)
-        e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, out_logp, out_lse, s);
+        e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
+                                   s);
     const cudaError_t ef = cudaFreeAsync(ws, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "token_logprob launch");
@@ -231,6 +238,25 @@ int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int6
         return cuda_fail(ef, "cudaFreeAsync(token_logprob workspace)");
     g_msg[0] = 0;
     return TIM_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int tim_token_logprob(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D,
+                      int64_t V, float *out_logp, float *out_lse, tim_stream_t stream)
+{
+    return token_logprob(h, W, targets, N, D, V, 1.f, out_logp, out_lse, stream);
+}
+
+int tim_token_logprob_temperature(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D,
+                                  int64_t V, float temperature, float *out_logp, float *out_lse,
+                                  tim_stream_t stream)
+{
+    if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature))
+        return fail(TIM_ERR_INVALID_ARG, "temperature must be positive and finite");
+    return token_logprob(h, W, targets, N, D, V, 1.f / temperature, out_logp, out_lse, stream);
 }
 
 int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const uint8_t *mask,

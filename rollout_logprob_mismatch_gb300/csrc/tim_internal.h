@@ -38,6 +38,7 @@ struct K1Args {
     float2 *part;             // [N][num_chunks]: per-chunk (max, sum of exp(z - max))
     float *za;                // [N]: the target's logit, written by the chunk holding it
     int *status;              // device status word
+    float inv_temp;           // 1 / temperature (1 for raw logits)
     int32_t N, D, V;
     int32_t num_m_tiles, num_chunks;
     int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
@@ -50,7 +51,7 @@ struct K1Args {
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
                            cudaStream_t stream);
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
-                              int32_t N, int32_t V, int32_t num_chunks, float *out_logp,
+                              int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream);
 cudaError_t k1_prepare_device();   // per-device function attributes
 

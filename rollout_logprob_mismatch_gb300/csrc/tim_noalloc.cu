@@ -172,6 +172,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.part = reinterpret_cast<float2 *>(dev->scratch);
     a.za = reinterpret_cast<float *>(dev->scratch + part_bytes);
     a.status = dev->status;
+    a.inv_temp = 1.f;
     a.N = static_cast<int32_t>(N);
     a.D = static_cast<int32_t>(D);
     a.V = static_cast<int32_t>(V);
@@ -186,7 +187,8 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = tim::k1_launch_main(th, tw, a, s);
     if (e == cudaSuccess)
-        e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, out_logp, out_lse, s);
+        e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
+                                   s);
     if (e != cudaSuccess)
         return cuda_err(e, "token_logprob_noalloc launch");
     return tim::record_error(TIM_OK, "");

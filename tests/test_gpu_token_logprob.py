@@ -146,3 +146,39 @@ def top5_ids(hd, Wd, chunk=2048):
         out.append(torch.topk(z.float(), 5, dim=-1).indices.int().cpu())
         del z
     return torch.cat(out).numpy()
+
+
+# --------------------------------------------------------------- temperature
+@pytest.mark.parametrize("tau", [0.7, 2.5])
+def test_temperature_parity(tau):
+    """log softmax(h W^T / tau) against the oracle (icarus, "logits processor")."""
+    h, W, a = _rand(300, 512, 5000, 31, w_std=0.05)
+    lp, lse = tim.token_logprob(_bf16_dev(h), _bf16_dev(W), _dev(a), temperature=tau)
+    tim.check()
+    o_lp, o_lse = oracle.token_logprob(h, W, a, temperature=tau)
+    assert_parity(lp.cpu().numpy(), lse.cpu().numpy(), o_lp, o_lse, tau)
+
+
+def test_temperature_one_and_power_of_two_are_exact():
+    """tau = 1 gives the bits of the plain call; tau = 2 on W gives the bits of
+    tau = 1 on W / 2 (an exact rescale of every logit)."""
+    h, W, a = _rand(1000, 1024, 9000, 32)
+    hd, Wd, ad = _bf16_dev(h), _bf16_dev(W), _dev(a)
+    p0 = tim.token_logprob(hd, Wd, ad)
+    p1 = tim.token_logprob(hd, Wd, ad, temperature=1.0)
+    lp_bits = torch.empty_like(p0[0])
+    rc = tim.tim_token_logprob_temperature(hd.data_ptr(), Wd.data_ptr(), ad.data_ptr(), 1000, 1024, 9000, 1.0,
+                                           lp_bits.data_ptr(), p1[1].data_ptr(),
+                                           torch.cuda.current_stream().cuda_stream)
+    assert rc == tim.TIM_OK
+    Wh = (Wd.float() * 0.5).to(torch.bfloat16)
+    q2 = tim.token_logprob(hd, Wd, ad, temperature=2.0)
+    q1 = tim.token_logprob(hd, Wh, ad)
+    tim.check()
+    assert torch.equal(p0[0], lp_bits) and torch.equal(p0[1], p1[1])
+    assert torch.equal(q2[0], q1[0]) and torch.equal(q2[1], q1[1])
+
+
+def test_temperature_rejects_bad_values():
+    for tau in (0.0, -1.0, float("inf"), float("nan")):
+        assert tim.tim_token_logprob_temperature(16, 16, 16, 4, 64, 10, tau, 16, 16, None) == tim.TIM_ERR_INVALID_ARG
