@@ -48,10 +48,10 @@ K2_BW_TOKENS = 1 << 27
 # only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
 # profiles/k2_seq_kernel_2e25_tokens.md).
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3075988736 read + 25264640 written
-    ("k1", "01b23b8a012901ea"): 3075988736 + 25264640,
-    # mismatch pass, 2^25 tokens: 304738048 read + 98114304 written (traffic scales with tokens)
-    ("k2", "5ad5f3910133215d"): 304738048 + 98114304,
+    # token logprob, N = 8192, D = 4096, V = 151936: 3050926592 read + 18969088 written
+    ("k1", "006ea2b16082c21a"): 3050926592 + 18969088,
+    # mismatch pass, 2^25 tokens: 305292544 read + 97732352 written (traffic scales with tokens)
+    ("k2", "4f3f821e3a24f689"): 305292544 + 97732352,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 
