@@ -8,6 +8,8 @@ input generators of ``workloads``.
 ``token_logprob``  -- the selected-token logprob by the definition (icarus
 "RL: Training Inference Mismatch", section "log p"): z = h W^T in fp64,
 lse = log sum exp z, logp = z[a] - lse.
+``tis_ppo``        -- the TIS-weighted PPO clipped surrogate, its gradient and
+masked means (VeXact summary eq. (2)-(3); HN "Clipped importance ratios").
 ``mismatch_stats`` -- delta, r, k1/k2/k3, truncated-IS weight, masked
 per-sequence and batch means and the rejection flag (VeXact summary eq. (1)
 and "KL Estimators"; llm-infra-atlas section 2; icarus "KL estimators",
@@ -37,6 +39,10 @@ BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_d
                 "reject_ratio", "n_seqs_nonempty", "n_rejected")
 
 
+PPO_FIELDS = ("n_mask", "n_used", "n_ppo_clipped", "n_tis_clipped", "mean_loss", "seqmean_loss",
+              "ppo_clip_ratio", "tis_clip_ratio", "n_seqs_nonempty")
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c with plain gcc -O2 (no fast-math) into _liboracle.so."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
@@ -61,6 +67,10 @@ def _load():
                                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32,
                                                   P, P, P, P]
             lib.oracle_mismatch_stats.restype = ctypes.c_int
+            lib.oracle_tis_ppo.argtypes = [P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
+                                           ctypes.c_double, ctypes.c_double, P, P, P, P]
+            lib.oracle_tis_ppo.restype = ctypes.c_int
+            assert lib.oracle_ppo_fields() == len(PPO_FIELDS)
             assert lib.oracle_seq_fields() == len(SEQ_FIELDS)
             assert lib.oracle_batch_fields() == len(BATCH_FIELDS)
             _lib = lib
@@ -124,3 +134,27 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
     if rc != 0:
         raise ValueError("oracle_mismatch_stats rejected its arguments")
     return {"token_weight": w, "seq_stats": seq, "seq_flags": flags, "batch": batch}
+
+
+def tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, eps_low: float = 0.2,
+            eps_high: float = 0.2, C: float = 2.0):
+    """TIS-weighted PPO clipped surrogate (VeXact summary eq. (2)-(3), TIS by
+    r_corr truncated at C; HN page, clipped importance ratios).  dict with
+    token_loss [N], token_grad [N] (d loss / d logp_theta), seq_loss [S],
+    batch [9] (PPO_FIELDS), all float64."""
+    lib = _load()
+    arrs = [np.ascontiguousarray(x, dtype=np.float32) for x in (logp_theta, logp_old, logp_rollout, advantages)]
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    off = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+    N = arrs[0].size
+    S = off.size - 1
+    assert all(x.size == N for x in arrs) and m.size == N and S >= 0
+    loss = np.empty(N, dtype=np.float64)
+    grad = np.empty(N, dtype=np.float64)
+    seq = np.empty(S, dtype=np.float64)
+    batch = np.empty(len(PPO_FIELDS), dtype=np.float64)
+    rc = lib.oracle_tis_ppo(*[_ptr(x) for x in arrs], _ptr(m), _ptr(off), S, N, float(eps_low), float(eps_high),
+                            float(C), _ptr(loss), _ptr(grad), _ptr(seq), _ptr(batch))
+    if rc != 0:
+        raise ValueError("oracle_tis_ppo rejected its arguments")
+    return {"token_loss": loss, "token_grad": grad, "seq_loss": seq, "batch": batch}

@@ -336,3 +336,99 @@ int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, co
     batch[BT_N_REJECTED] = b_rej;
     return 0;
 }
+
+/* ------------------------------------------------------------------ TIS-weighted PPO surrogate
+ *
+ * VeXact summary, eq. (2): L_ppo(r, A) = -min(r A, clip(r, 1 - eps, 1 + eps) A),
+ * recompute mode eq. (3): r = pi_theta / pi_old^train; "TIS is effective: it
+ * corrects the PPO ratio ... by multiplying with r_corr" with r_corr =
+ * pi_old^train / pi_old^rollout truncated at C (LoongSage section 4: the IS
+ * weight pi_old / pi_rollout, clipped when out of bounds); HN page, "Clipped
+ * importance ratios": asymmetric eps_low / eps_high, and the gradient of a
+ * token is dropped where the clipped term is the minimum.
+ *
+ * Per token with mask != 0 and finite inputs ("used"):
+ *   r = exp(l_theta - l_old), w = min(exp(l_old - l_rollout), C),
+ *   loss = -w min(r A, clip(r, 1 - eps_low, 1 + eps_high) A),
+ *   grad = d loss / d l_theta = -w r A where r A is the minimum, else 0.
+ * Readings: the clipped branch is taken only where it is strictly smaller
+ * (ties keep the gradient); the decisions (clipped PPO branch, w capped) are
+ * taken on the log-ratios rounded to fp32, the precision the device computes
+ * them in, against the exact thresholds log(1 + eps_high), log(1 - eps_low),
+ * log C; values use the exact fp64 log-ratios.  Unused tokens: loss 0, grad 0.
+ * Outputs: token_loss, token_grad [N] (may be NULL), seq_loss [S] = mean loss
+ * over the sequence's used tokens (0 if none), batch [PPO_FIELDS]. */
+enum {
+    PB_N_MASK, PB_N_USED, PB_N_PPO_CLIPPED, PB_N_TIS_CLIPPED, PB_MEAN_LOSS, PB_SEQMEAN_LOSS,
+    PB_PPO_CLIP_RATIO, PB_TIS_CLIP_RATIO, PB_N_SEQS_NONEMPTY, PB_FIELDS
+};
+
+int oracle_ppo_fields(void) { return PB_FIELDS; }
+
+int oracle_tis_ppo(const float *l_theta, const float *l_old, const float *l_rollout, const float *adv,
+                   const uint8_t *mask, const int32_t *seq_offsets, int32_t S, int64_t N, double eps_low,
+                   double eps_high, double C, double *token_loss, double *token_grad, double *seq_loss,
+                   double *batch)
+{
+    if (S < 0 || N < 0 || !(C > 0.0) || !(eps_low >= 0.0 && eps_low < 1.0) || !(eps_high >= 0.0) ||
+        !seq_offsets || !batch)
+        return -1;
+    if (N > 0 && (!l_theta || !l_old || !l_rollout || !adv || !mask))
+        return -1;
+    if (S > 0 && !seq_loss)
+        return -1;
+    if (seq_offsets[0] != 0 || (int64_t)seq_offsets[S] != N)
+        return -1;
+    for (int32_t s = 0; s < S; ++s)
+        if (seq_offsets[s + 1] < seq_offsets[s])
+            return -1;
+    const double log_hi = log1p(eps_high), log_lo = log1p(-eps_low), log_c = log(C);
+    double b_mask = 0, b_used = 0, b_ppo = 0, b_tis = 0, b_loss = 0, b_seqmean = 0, b_nonempty = 0;
+    for (int32_t s = 0; s < S; ++s) {
+        double n_used = 0, sum_loss = 0;
+        for (int64_t t = seq_offsets[s]; t < seq_offsets[s + 1]; ++t) {
+            double loss = 0.0, grad = 0.0;
+            const int in = mask[t] != 0;
+            b_mask += in;
+            const float dt32 = l_theta[t] - l_old[t];     /* decisions in fp32 */
+            const float dc32 = l_old[t] - l_rollout[t];
+            const int used = in && isfinite(dt32) && isfinite(dc32) && isfinite(adv[t]);
+            if (used) {
+                const double A = adv[t];
+                const double r = exp((double)l_theta[t] - (double)l_old[t]);
+                const double rc = exp((double)l_old[t] - (double)l_rollout[t]);
+                const double w = rc < C ? rc : C;
+                const int tis_clipped = (double)dc32 > log_c;
+                const int ppo_clipped = (A > 0.0 && (double)dt32 > log_hi) || (A < 0.0 && (double)dt32 < log_lo);
+                const double rclip = A > 0.0 ? 1.0 + eps_high : 1.0 - eps_low;
+                loss = ppo_clipped ? -w * rclip * A : -w * r * A;
+                grad = ppo_clipped ? 0.0 : -w * r * A;
+                n_used += 1;
+                sum_loss += loss;
+                b_ppo += ppo_clipped;
+                b_tis += tis_clipped;
+            }
+            if (token_loss)
+                token_loss[t] = loss;
+            if (token_grad)
+                token_grad[t] = grad;
+        }
+        seq_loss[s] = mean_or_zero(sum_loss, n_used);
+        b_used += n_used;
+        b_loss += sum_loss;
+        if (n_used > 0) {
+            b_nonempty += 1;
+            b_seqmean += seq_loss[s];
+        }
+    }
+    batch[PB_N_MASK] = b_mask;
+    batch[PB_N_USED] = b_used;
+    batch[PB_N_PPO_CLIPPED] = b_ppo;
+    batch[PB_N_TIS_CLIPPED] = b_tis;
+    batch[PB_MEAN_LOSS] = mean_or_zero(b_loss, b_used);
+    batch[PB_SEQMEAN_LOSS] = mean_or_zero(b_seqmean, b_nonempty);
+    batch[PB_PPO_CLIP_RATIO] = mean_or_zero(b_ppo, b_used);
+    batch[PB_TIS_CLIP_RATIO] = mean_or_zero(b_tis, b_used);
+    batch[PB_N_SEQS_NONEMPTY] = b_nonempty;
+    return 0;
+}

@@ -359,3 +359,140 @@ def test_temperature_limits_and_two_class_form():
     np.testing.assert_allclose(lp, scipy.special.log_expit((z[:, 1] - z[:, 0]) / 0.7), rtol=0, atol=1e-12)
     with pytest.raises(RuntimeError):
         oracle.token_logprob(h2, W2, np.ones(16, np.int32), temperature=0.0)
+
+
+# --------------------------------------------------------------- TIS-weighted PPO surrogate
+P = {n: i for i, n in enumerate(oracle.PPO_FIELDS)}
+NO_CLIP = dict(eps_low=0.999999, eps_high=1e9, C=1e30)
+
+
+def _ppo(lt, lo, lr, A, mask=None, offsets=None, **kw):
+    lt, lo, lr, A = (np.asarray(x, np.float32) for x in (lt, lo, lr, A))
+    n = lt.size
+    m = np.ones(n, np.uint8) if mask is None else np.asarray(mask, np.uint8)
+    off = np.array([0, n], np.int32) if offsets is None else np.asarray(offsets, np.int32)
+    return oracle.tis_ppo(lt, lo, lr, A, m, off, **kw)
+
+
+def test_ppo_importance_sampling_identity():
+    """Tokens drawn from the rollout policy, weighted by pi_old / pi_rollout
+    (TIS with no truncation) and by r = pi_theta / pi_old: the mean surrogate
+    is -E_{pi_theta}[A], the on-policy objective (VeXact summary eq. (3) and
+    the TIS correction; LoongSage section 4).  The rollout distribution is
+    realised exactly by token counts; swapping old and rollout, or theta and
+    old, moves the mean far off."""
+    counts = np.array([400, 250, 200, 100, 50])            # p_rollout = counts / 1000
+    p_ro = counts / 1000.0
+    p_old = np.array([0.30, 0.30, 0.15, 0.15, 0.10])
+    p_th = np.array([0.20, 0.35, 0.25, 0.05, 0.15])
+    A = np.array([1.5, -0.5, 2.0, -3.0, 0.75])
+    tok = np.repeat(np.arange(5), counts)
+    o = _ppo(np.log(p_th)[tok], np.log(p_old)[tok], np.log(p_ro)[tok], A[tok], **NO_CLIP)
+    exact = -float(np.dot(p_th, A))
+    assert abs(o["batch"][P["mean_loss"]] - exact) < 1e-6
+    assert o["batch"][P["n_ppo_clipped"]] == 0 and o["batch"][P["n_tis_clipped"]] == 0
+    swapped = _ppo(np.log(p_th)[tok], np.log(p_ro)[tok], np.log(p_old)[tok], A[tok], **NO_CLIP)
+    assert abs(swapped["batch"][P["mean_loss"]] - exact) > 0.05
+
+
+def test_ppo_on_policy_is_minus_advantage():
+    """r = 1 and w = 1 (theta = old = rollout): the surrogate of every token is
+    -A and its gradient -A (eq. (2) at r = 1, whatever eps)."""
+    rng = np.random.default_rng(40)
+    l = -rng.gamma(0.6, 3.0, 64).astype(np.float32)
+    A = rng.standard_normal(64).astype(np.float32)
+    o = _ppo(l, l, l, A, eps_low=0.1, eps_high=0.3, C=1.5)
+    np.testing.assert_array_equal(o["token_loss"], -A.astype(np.float64))
+    np.testing.assert_array_equal(o["token_grad"], -A.astype(np.float64))
+    assert o["batch"][P["n_ppo_clipped"]] == 0 and o["batch"][P["n_tis_clipped"]] == 0
+
+
+def test_ppo_case_form_of_the_clipped_objective():
+    """The clipped surrogate as a function of r (eq. (2)): for A > 0 it is
+    -A min(r, 1 + eps_high), for A < 0 it is -A max(r, 1 - eps_low); the
+    gradient is zero exactly where the clipped value is the one taken (HN
+    page, "Clipped importance ratios"); eps_low and eps_high act on their own
+    sides.  w = 1 here (old = rollout)."""
+    eps_low, eps_high = 0.2, 0.28
+    r = np.array([0.3, 0.79, 0.81, 1.0, 1.27, 1.29, 3.0])
+    lo = np.full(r.size, -1.0)
+    lt = (np.log(r) + lo).astype(np.float32)
+    r32 = np.exp(lt.astype(np.float64) - np.float32(-1.0))
+    for sign in (1.0, -1.0):
+        A = np.full(r.size, 1.7 * sign, np.float32).astype(np.float64)
+        o = _ppo(lt, lo, lo, A, eps_low=eps_low, eps_high=eps_high, C=2.0)
+        taken = np.minimum(r32, 1 + eps_high) if sign > 0 else np.maximum(r32, 1 - eps_low)
+        np.testing.assert_allclose(o["token_loss"], -A * taken, rtol=1e-15, atol=0)
+        flat = r32 > 1 + eps_high if sign > 0 else r32 < 1 - eps_low
+        assert np.array_equal(o["token_grad"] == 0, flat)
+        assert o["batch"][P["n_ppo_clipped"]] == flat.sum()
+        np.testing.assert_allclose(o["batch"][P["ppo_clip_ratio"]], flat.mean(), rtol=1e-15)
+
+
+def test_ppo_gradient_is_the_derivative_of_the_loss():
+    """token_grad = d token_loss / d logp_theta, checked by central differences
+    of the oracle's own loss (step 2^-9, tokens at least 4 steps away from a
+    clip boundary)."""
+    rng = np.random.default_rng(41)
+    n = 400
+    lo = -rng.gamma(0.6, 3.0, n).astype(np.float32)
+    lt = (lo + rng.normal(0, 0.25, n)).astype(np.float32)
+    lr = (lo + rng.normal(0, 0.4, n)).astype(np.float32)
+    A = rng.standard_normal(n).astype(np.float32)
+    kw = dict(eps_low=0.2, eps_high=0.28, C=1.8)
+    hstep = np.float32(2.0 ** -9)
+    d = lt.astype(np.float64) - lo
+    far = (np.abs(d - math.log1p(0.28)) > 4 * hstep) & (np.abs(d - math.log1p(-0.2)) > 4 * hstep)
+    o = _ppo(lt, lo, lr, A, **kw)
+    up = _ppo(lt + hstep, lo, lr, A, **kw)["token_loss"]
+    dn = _ppo(lt - hstep, lo, lr, A, **kw)["token_loss"]
+    fd = (up - dn) / (2 * float(hstep))
+    exact_steps = ((lt + hstep) - (lt - hstep)).astype(np.float64) == 2 * float(hstep)
+    sel = far & exact_steps
+    assert sel.sum() > 300
+    np.testing.assert_allclose(o["token_grad"][sel], fd[sel], rtol=2e-5, atol=1e-9)
+
+
+def test_ppo_tis_weight_truncation():
+    """w = min(pi_old / pi_rollout, C) (LoongSage section 4): below the cap the
+    loss scales with 1 / pi_rollout; above it, lowering pi_rollout further
+    changes nothing, and the token counts as TIS-clipped."""
+    lt = np.array([-1.0, -2.0], np.float32)
+    lo = np.array([-1.1, -2.2], np.float32)
+    A = np.array([0.5, -2.0], np.float32)
+    C = 3.0
+    base = _ppo(lt, lo, lo + np.float32(0.25), A, eps_low=0.2, eps_high=0.2, C=C)
+    down = _ppo(lt, lo, lo - np.float32(0.25), A, eps_low=0.2, eps_high=0.2, C=C)
+    np.testing.assert_allclose(down["token_loss"], base["token_loss"] * math.exp(0.5), rtol=1e-6)
+    capped = _ppo(lt, lo, lo - np.float32(2.0), A, eps_low=0.2, eps_high=0.2, C=C)
+    capped2 = _ppo(lt, lo, lo - np.float32(5.0), A, eps_low=0.2, eps_high=0.2, C=C)
+    np.testing.assert_array_equal(capped["token_loss"], capped2["token_loss"])
+    w1 = _ppo(lt, lo, lo, A, eps_low=0.2, eps_high=0.2, C=C)
+    np.testing.assert_allclose(capped["token_loss"], C * w1["token_loss"], rtol=1e-15)
+    assert capped["batch"][P["n_tis_clipped"]] == 2 and base["batch"][P["n_tis_clipped"]] == 0
+
+
+def test_ppo_masks_nonfinite_and_means():
+    """Masked and non-finite tokens contribute nothing; the token mean divides
+    by used tokens, the sequence mean averages non-empty sequences."""
+    lt = np.array([-1.0, -1.0, np.nan, -1.0, -1.0, -1.0, -1.0], np.float32)
+    lo = lt.copy()
+    lo[2] = -1.0
+    A = np.array([1.0, 2.0, 5.0, 7.0, 3.0, 3.0, 100.0], np.float32)
+    mask = np.array([1, 1, 1, 0, 1, 1, 0], np.uint8)
+    off = np.array([0, 4, 4, 6, 7], np.int32)     # seq 1 empty, seq 3 fully masked
+    o = _ppo(lt, lo, lo, A, mask=mask, offsets=off, eps_low=0.2, eps_high=0.2, C=2.0)
+    assert o["token_loss"][2] == 0 and o["token_loss"][3] == 0 and o["token_grad"][6] == 0
+    np.testing.assert_array_equal(o["seq_loss"], [-1.5, 0.0, -3.0, 0.0])
+    b = o["batch"]
+    assert (b[P["n_mask"]], b[P["n_used"]], b[P["n_seqs_nonempty"]]) == (5, 4, 2)
+    assert b[P["mean_loss"]] == -9.0 / 4 and b[P["seqmean_loss"]] == -2.25
+
+
+def test_ppo_bad_arguments_rejected():
+    z = np.zeros(3, np.float32)
+    for kw in (dict(eps_low=1.0), dict(eps_low=-0.1), dict(eps_high=-0.1), dict(C=0.0), dict(C=float("nan"))):
+        with pytest.raises(ValueError):
+            oracle.tis_ppo(z, z, z, z, np.ones(3, np.uint8), np.array([0, 3], np.int32), **kw)
+    with pytest.raises(ValueError):
+        oracle.tis_ppo(z, z, z, z, np.ones(3, np.uint8), np.array([0, 2], np.int32))
