@@ -339,13 +339,13 @@ int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, co
 
 /* ------------------------------------------------------------------ TIS-weighted PPO surrogate
  *
- * VeXact summary, eq. (2): L_ppo(r, A) = -min(r A, clip(r, 1 - eps, 1 + eps) A),
- * recompute mode eq. (3): r = pi_theta / pi_old^train; "TIS is effective: it
- * corrects the PPO ratio ... by multiplying with r_corr" with r_corr =
- * pi_old^train / pi_old^rollout truncated at C (LoongSage section 4: the IS
- * weight pi_old / pi_rollout, clipped when out of bounds); HN page, "Clipped
- * importance ratios": asymmetric eps_low / eps_high, and the gradient of a
- * token is dropped where the clipped term is the minimum.
+ * VeXact summary, eq. (2): the clipped PPO surrogate of ratio r and advantage
+ * A; eq. (3), recompute mode: r = pi_theta / pi_old^train, and the TIS
+ * correction multiplies the surrogate by the correction ratio pi_old^train /
+ * pi_old^rollout truncated at C (LoongSage section 4 clips the same IS weight
+ * when it leaves its bounds); HN page, section on clipped importance ratios:
+ * separate eps_low / eps_high, and no gradient flows from a token whose
+ * clipped term is the one taken.
  *
  * Per token with mask != 0 and finite inputs ("used"):
  *   r = exp(l_theta - l_old), w = min(exp(l_old - l_rollout), C),
