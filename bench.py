@@ -54,14 +54,17 @@ MEASURED_TRAFFIC = {
     ("k2", "4f3f821e3a24f689"): 305292544 + 97732352,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
+PPO_TRAFFIC_TOKENS = 1 << 25
 
 
 def source_hash(kind: str) -> str:
     import hashlib
     d = os.path.join(ROOT, "rollout_logprob_mismatch_gb300", "csrc")
-    main = "k1_token_logprob.cu" if kind == "k1" else "k2_mismatch_stats.cu"
+    files = {"k1": ("k1_token_logprob.cu", "tim_ptx.cuh", "tim_internal.h"),
+             "k2": ("k2_mismatch_stats.cu", "tim_ptx.cuh", "tim_internal.h"),
+             "ppo": ("tis_ppo.cu", "ppo_internal.h", "tim_ptx.cuh", "tim_internal.h")}[kind]
     m = hashlib.sha1()
-    for f in (main, "tim_ptx.cuh", "tim_internal.h"):
+    for f in files:
         with open(os.path.join(d, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]
@@ -287,6 +290,13 @@ def run_gb300(args):
     tim.load()
     peaks = load_peaks()
 
+    if args.only == "ppo":
+        r = ppo_bandwidth(tim, dev, stream_of(dev), peaks, tokens=args.tokens or K2_BW_TOKENS,
+                          reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
     if args.only == "k2bw":
         # the mismatch pass alone on a large batch (profiling runs)
         r = mismatch_bandwidth(tim, dev, stream_of(dev), peaks, tokens=args.tokens or K2_BW_TOKENS,
@@ -409,6 +419,7 @@ def run_gb300(args):
     d2h = b_host.numel() * 8 + s_host.numel() * 4 + f_host.numel() * 4
 
     k2_bw = mismatch_bandwidth(tim, dev, stream, peaks) if not args.skip_k2_bandwidth else None
+    ppo_bw = ppo_bandwidth(tim, dev, stream, peaks) if not args.skip_ppo else None
     sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
     tim.check()
 
@@ -445,6 +456,8 @@ def run_gb300(args):
     }
     if k2_bw is not None:
         line["mismatch_bandwidth"] = k2_bw
+    if ppo_bw is not None:
+        line["tis_ppo"] = ppo_bw
     if sweep is not None:
         line["sweep"] = sweep
     print(json.dumps(line), flush=True)
@@ -524,6 +537,56 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
             "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
 
 
+def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
+    """tim_tis_ppo alone on `tokens` tokens (2^27 by default): the segments of
+    workloads.draw_ppo_inputs (lognormal lengths, median 1024, clipped to
+    [128, 4096]) with the same laws for the other inputs drawn on the device
+    (30% masked, l_old = -Gamma(0.6, 3), rollout and current policy as
+    N(0, 0.02^2) / N(0, 0.1^2) drifts, per-sequence N(0, 1) advantages);
+    token loss and gradient written; L2 flushed before each launch."""
+    import torch
+    Nt = tokens
+    cfg = wl.HeadConfig("ppo", N=Nt, D=8, V=8, seq_layout="lognormal", mask_drop=0.3, seed=9)
+    off = wl.draw_segments(cfg)
+    S = len(off) - 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    torch.manual_seed(9)   # the gamma sampler draws from the default generator
+    gamma = torch.distributions.Gamma(torch.tensor(0.6, device=dev), torch.tensor(1.0 / 3.0, device=dev))
+    l_old = -gamma.sample((Nt,))
+    l_ro = l_old + 0.02 * torch.randn(Nt, device=dev, generator=g)
+    l_th = l_old + 0.1 * torch.randn(Nt, device=dev, generator=g)
+    mask = (torch.rand(Nt, device=dev, generator=g) >= 0.3).to(torch.uint8)
+    offd = torch.from_numpy(off).to(dev)
+    lens = offd[1:] - offd[:-1]
+    adv = torch.repeat_interleave(torch.randn(S, device=dev, generator=g), lens.long())
+    out = {"token_loss": torch.empty(Nt, dtype=torch.float32, device=dev),
+           "token_grad": torch.empty(Nt, dtype=torch.float32, device=dev),
+           "seq_loss": torch.empty(S, dtype=torch.float32, device=dev),
+           "batch": torch.empty(9, dtype=torch.float64, device=dev)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    call = lambda: tim.tis_ppo(l_th, l_old, l_ro, adv, mask, offd, eps_low=0.2, eps_high=0.28, C=2.0,  # noqa: E731
+                               out=out)
+    for _ in range(warmup):
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        flush.fill_(i)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
+    algo = 25 * Nt + 4 * (S + 1) + 4 * S + 72
+    gbs = algo / t / 1e9
+    tr = measured_traffic("ppo")
+    return {"tokens": Nt, "num_seqs": S, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo,
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+            "bound": "hbm", "tokens_per_s": Nt / t,
+            "traffic": None if tr is None else tr * Nt / PPO_TRAFFIC_TOKENS}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,7 +596,8 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-k2-bandwidth", action="store_true")
     ap.add_argument("--skip-sweep", action="store_true")
-    ap.add_argument("--only", choices=["k1", "k2", "k2bw"], default=None,
+    ap.add_argument("--skip-ppo", action="store_true")
+    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo"], default=None,
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller batch of the same head (profiling runs only)")

@@ -216,6 +216,69 @@ TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollou
                        const uint8_t *mask, const int32_t *seq_offsets, float C,
                        const tim_mismatch_out *out, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ TIS-weighted PPO surrogate
+ *
+ * The clipped PPO surrogate of VeXact summary eq. (2) in recompute mode
+ * (eq. (3): r = pi_theta / pi_old^train), multiplied by the truncated
+ * importance weight that corrects for the rollout engine (TIS: the ratio
+ * pi_old^train / pi_old^rollout truncated at C; LoongSage section 4), with
+ * separate lower and upper clip ranges and no gradient through a token whose
+ * clipped term is taken (HN page, section on clipped importance ratios).
+ * Per token t with mask_t != 0 and finite logp_theta - logp_old,
+ * logp_old - logp_rollout and A_t ("used"):
+ *   r = e^(l_theta - l_old),  w = min(e^(l_old - l_rollout), C),
+ *   loss = -w min(r A, clip(r, 1 - eps_low, 1 + eps_high) A),
+ *   grad = d loss / d l_theta = -w r A where r A is the minimum, else 0.
+ * The clipped branch is taken only where it is strictly smaller (A > 0 and
+ * r > 1 + eps_high, or A < 0 and r < 1 - eps_low); both decisions, and
+ * w = C, are taken on the fp32 log-ratios against the exact thresholds
+ * log(1 + eps_high), log(1 - eps_low), log C.  Tokens not used: loss 0, grad 0.
+ * Per sequence: the mean loss over its used tokens (0 if none).  Per batch: the
+ * mean over used tokens, the mean of the sequence means over non-empty
+ * sequences, and the fractions of used tokens whose PPO term or TIS weight
+ * was clipped.
+ */
+#define TIM_PPO_FIELDS 9
+enum tim_ppo_field {
+    TIM_PPO_N_MASK = 0,        /* masked-in tokens */
+    TIM_PPO_N_USED,            /* masked-in tokens with finite inputs */
+    TIM_PPO_N_PPO_CLIPPED,     /* used tokens on the clipped (zero-gradient) branch */
+    TIM_PPO_N_TIS_CLIPPED,     /* used tokens with w = C, i.e. l_old - l_rollout > log C */
+    TIM_PPO_MEAN_LOSS,         /* token mean over used tokens */
+    TIM_PPO_SEQMEAN_LOSS,      /* mean over non-empty sequences of the sequence means */
+    TIM_PPO_PPO_CLIP_RATIO,    /* n_ppo_clipped / n_used */
+    TIM_PPO_TIS_CLIP_RATIO,    /* n_tis_clipped / n_used */
+    TIM_PPO_N_SEQS_NONEMPTY
+};
+
+/* Sizes and outputs of tim_tis_ppo.  Host struct; the pointers are device
+ * pointers. */
+typedef struct {
+    int32_t num_seqs;        /* in: S >= 0 (S = 0: only batch_stats is written, all 0) */
+    int64_t num_tokens;      /* in: N >= 0; must equal seq_offsets[S] (checked on device) */
+    float *token_loss;       /* out, optional (NULL = not written): fp32 [N] */
+    float *token_grad;       /* out, optional (NULL = not written): fp32 [N], d token_loss / d logp_theta */
+    float *seq_loss;         /* out: fp32 [S] */
+    double *batch_stats;     /* out: fp64 [TIM_PPO_FIELDS] */
+} tim_ppo_out;
+
+/*   logp_theta, logp_old, logp_rollout  fp32 [N]: current policy, trainer's
+ *                             recompute of the rollout policy, rollout engine
+ *   advantages                fp32 [N], A_t (a per-sequence advantage is broadcast by the caller)
+ *   mask                      uint8 [N]: 0 = not counted (prompt / padding), else counted
+ *   seq_offsets               int32 [S + 1]: seq_offsets[0] = 0, non-decreasing, seq_offsets[S] = N
+ *   eps_low                   lower clip range, 0 <= eps_low < 1
+ *   eps_high                  upper clip range, 0 <= eps_high, finite
+ *   C                         truncation cap of the TIS weight, C > 0, finite
+ * Token arrays need 4-byte alignment only.  Bad offsets found on the device set
+ * TIM_ERR_BAD_INPUT (see tim_check) and make the affected sequences' seq_loss
+ * and the whole batch record NaN.  Scratch: about 24 * S bytes from the
+ * library's stream-ordered pool. */
+TIM_API int tim_tis_ppo(const float *logp_theta, const float *logp_old, const float *logp_rollout,
+                        const float *advantages, const uint8_t *mask, const int32_t *seq_offsets,
+                        float eps_low, float eps_high, float C, const tim_ppo_out *out,
+                        tim_stream_t stream);
+
 /* ------------------------------------------------------------------ failure-detection self-test
  *
  * No counterpart on the pages.  Runs the library's bounded-wait path on purpose,

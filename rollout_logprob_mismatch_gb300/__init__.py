@@ -14,7 +14,9 @@ compares it with the rollout engine's logprob through delta = l_train -
 l_rollout, r = e^delta, the k1/k2/k3 KL estimators, the truncated importance
 weight min(r, C) and masked per-sequence / per-batch means with a sequence
 rejection flag (VeXact summary, eq. (1) and "Algorithmic TIM Compensation";
-LoongSage "Train-Inference Consistency", sections 4-5).
+LoongSage "Train-Inference Consistency", sections 4-5).  ``tis_ppo`` gives the
+clipped PPO surrogate weighted by the truncated importance weight, its
+gradient and masked means (VeXact summary eq. (2)-(3)).
 """
 from __future__ import annotations
 
@@ -24,9 +26,10 @@ import os
 import threading
 
 __all__ = [
-    "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "tim_mismatch_out", "lib_path", "load",
-    "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
-    "token_logprob", "mismatch_stats", "check",
+    "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
+    "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
+    "tim_tis_ppo", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "token_logprob", "mismatch_stats", "tis_ppo", "check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +50,9 @@ BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_d
                 "seqmean_k1", "seqmean_k2", "seqmean_k3", "clip_ratio", "nan_ratio",
                 "reject_ratio", "n_seqs_nonempty", "n_rejected")
 
+PPO_FIELDS = ("n_mask", "n_used", "n_ppo_clipped", "n_tis_clipped", "mean_loss", "seqmean_loss",
+              "ppo_clip_ratio", "tis_clip_ratio", "n_seqs_nonempty")
+
 
 class TimError(RuntimeError):
     def __init__(self, code: int, msg: str):
@@ -64,6 +70,18 @@ class tim_mismatch_out(ctypes.Structure):
         ("token_weight", ctypes.c_void_p),
         ("seq_stats", ctypes.c_void_p),
         ("seq_flags", ctypes.c_void_p),
+        ("batch_stats", ctypes.c_void_p),
+    ]
+
+
+class tim_ppo_out(ctypes.Structure):
+    """Mirror of the C struct tim_ppo_out (host struct of device pointers)."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("num_tokens", ctypes.c_int64),
+        ("token_loss", ctypes.c_void_p),
+        ("token_grad", ctypes.c_void_p),
+        ("seq_loss", ctypes.c_void_p),
         ("batch_stats", ctypes.c_void_p),
     ]
 
@@ -95,6 +113,9 @@ def load():
             lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
                                                ctypes.POINTER(tim_mismatch_out), P]
             lib.tim_mismatch_stats.restype = ctypes.c_int
+            F = ctypes.c_float
+            lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
+            lib.tim_tis_ppo.restype = ctypes.c_int
             lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
             lib.tim_selftest_wait_timeout.restype = ctypes.c_int
             lib.tim_check.argtypes = [P]
@@ -129,6 +150,12 @@ def tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C, out: tim_
                        stream) -> int:
     return load().tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, float(C),
                                      ctypes.byref(out), stream)
+
+
+def tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, eps_low, eps_high, C,
+                out: tim_ppo_out, stream) -> int:
+    return load().tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets,
+                              float(eps_low), float(eps_high), float(C), ctypes.byref(out), stream)
 
 
 def tim_selftest_wait_timeout(budget_us, stream) -> int:
@@ -246,6 +273,47 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
     with torch.cuda.device(dev):
         rc = tim_mismatch_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(),
                                 seq_offsets.data_ptr(), C, d, _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out
+
+
+def tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, eps_low: float = 0.2,
+            eps_high: float = 0.2, C: float = 2.0, token_outputs: bool = True, stream=None, out=None):
+    """TIS-weighted PPO clipped surrogate of packed sequences.
+
+    logp_theta, logp_old, logp_rollout, advantages fp32 [N]; mask bool/uint8 [N];
+    seq_offsets int32 [S + 1].  Returns a dict: token_loss, token_grad fp32 [N]
+    (None unless token_outputs), seq_loss fp32 [S], batch fp64 [9] (PPO_FIELDS).
+    """
+    import torch
+    _need(logp_theta, "logp_theta", torch.float32, 1)
+    dev = logp_theta.device
+    for name, t in (("logp_old", logp_old), ("logp_rollout", logp_rollout), ("advantages", advantages)):
+        _need(t, name, torch.float32, 1, dev)
+    _need(mask, "mask", (torch.uint8, torch.bool), 1, dev)
+    _need(seq_offsets, "seq_offsets", torch.int32, 1, dev)
+    N = logp_theta.shape[0]
+    S = seq_offsets.shape[0] - 1
+    if any(t.shape[0] != N for t in (logp_old, logp_rollout, advantages, mask)) or S < 0:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = {
+            "token_loss": torch.empty(N, dtype=torch.float32, device=dev) if token_outputs else None,
+            "token_grad": torch.empty(N, dtype=torch.float32, device=dev) if token_outputs else None,
+            "seq_loss": torch.empty(S, dtype=torch.float32, device=dev),
+            "batch": torch.empty(len(PPO_FIELDS), dtype=torch.float64, device=dev),
+        }
+    d = tim_ppo_out()
+    d.num_seqs = S
+    d.num_tokens = N
+    d.token_loss = out["token_loss"].data_ptr() if out.get("token_loss") is not None else None
+    d.token_grad = out["token_grad"].data_ptr() if out.get("token_grad") is not None else None
+    d.seq_loss = out["seq_loss"].data_ptr()
+    d.batch_stats = out["batch"].data_ptr()
+    with torch.cuda.device(dev):
+        rc = tim_tis_ppo(logp_theta.data_ptr(), logp_old.data_ptr(), logp_rollout.data_ptr(),
+                         advantages.data_ptr(), mask.data_ptr(), seq_offsets.data_ptr(), eps_low, eps_high, C,
+                         d, _stream_handle(stream, dev))
     _raise_if(rc)
     return out
 

@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/tim.h"
+#include "ppo_internal.h"
 #include "tim_internal.h"
 
 namespace {
@@ -133,6 +134,24 @@ int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, ui
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Largest float <= v, and smallest float >= v: a float x then satisfies
+// x > float_down(v) <=> x > v, and x < float_up(v) <=> x < v.
+float float_down(double v)
+{
+    float f = static_cast<float>(v);
+    if (static_cast<double>(f) > v)
+        f = std::nextafter(f, -INFINITY);
+    return f;
+}
+
+float float_up(double v)
+{
+    float f = static_cast<float>(v);
+    if (static_cast<double>(f) < v)
+        f = std::nextafter(f, INFINITY);
+    return f;
+}
 
 } // namespace
 
@@ -295,9 +314,7 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return rc;
 
     const double lc = std::log(static_cast<double>(C));
-    float lcd = static_cast<float>(lc);
-    if (static_cast<double>(lcd) > lc)
-        lcd = std::nextafter(lcd, -INFINITY);
+    const float lcd = float_down(lc);
     const float tau = std::isnan(out->tau_seq) ? static_cast<float>((static_cast<double>(C) - 1.0) - lc)
                                                : out->tau_seq;
 
@@ -334,6 +351,79 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return cuda_fail(e, "mismatch_stats launch");
     if (ef != cudaSuccess)
         return cuda_fail(ef, "cudaFreeAsync(mismatch workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_tis_ppo(const float *logp_theta, const float *logp_old, const float *logp_rollout, const float *advantages,
+                const uint8_t *mask, const int32_t *seq_offsets, float eps_low, float eps_high, float C,
+                const tim_ppo_out *out, tim_stream_t stream)
+{
+    if (!out)
+        return fail(TIM_ERR_INVALID_ARG, "out is null");
+    const int32_t S = out->num_seqs;
+    const int64_t N = out->num_tokens;
+    if (S < 0 || N < 0)
+        return fail(TIM_ERR_INVALID_ARG, "num_seqs / num_tokens must be >= 0");
+    if (S == 0 && N != 0)
+        return fail(TIM_ERR_INVALID_ARG, "num_tokens must be 0 when num_seqs is 0");
+    if (!(C > 0.f) || !std::isfinite(C))
+        return fail(TIM_ERR_INVALID_ARG, "C must be positive and finite");
+    if (!(eps_low >= 0.f && eps_low < 1.f))
+        return fail(TIM_ERR_INVALID_ARG, "eps_low must be in [0, 1)");
+    if (!(eps_high >= 0.f) || !std::isfinite(eps_high))
+        return fail(TIM_ERR_INVALID_ARG, "eps_high must be >= 0 and finite");
+    if (!seq_offsets || !out->batch_stats)
+        return fail(TIM_ERR_INVALID_ARG, "seq_offsets and batch_stats are required");
+    if (S > 0 && !out->seq_loss)
+        return fail(TIM_ERR_INVALID_ARG, "seq_loss is required when num_seqs > 0");
+    if (N > 0 && (!logp_theta || !logp_old || !logp_rollout || !advantages || !mask))
+        return fail(TIM_ERR_INVALID_ARG, "null token array");
+    if (!aligned(logp_theta, 4) || !aligned(logp_old, 4) || !aligned(logp_rollout, 4) || !aligned(advantages, 4) ||
+        !aligned(seq_offsets, 4) || !aligned(out->token_loss, 4) || !aligned(out->token_grad, 4) ||
+        !aligned(out->seq_loss, 4) || !aligned(out->batch_stats, 8))
+        return fail(TIM_ERR_INVALID_ARG, "misaligned array");
+
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (S > 0) {
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, tim::ppo_workspace_bytes(S), dev->pool, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMallocFromPoolAsync(ppo workspace)");
+    }
+    tim::PpoArgs a;
+    a.l_th = logp_theta;
+    a.l_old = logp_old;
+    a.l_ro = logp_rollout;
+    a.adv = advantages;
+    a.mask = mask;
+    a.off = seq_offsets;
+    a.S = S;
+    a.N = N;
+    a.C = C;
+    a.log_c_down = float_down(std::log(static_cast<double>(C)));
+    a.log_hi_down = float_down(std::log1p(static_cast<double>(eps_high)));
+    a.log_lo_up = float_up(std::log1p(-static_cast<double>(eps_low)));
+    a.r_hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+    a.r_lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+    a.token_loss = out->token_loss;
+    a.token_grad = out->token_grad;
+    a.seq_loss = out->seq_loss;
+    a.batch = out->batch_stats;
+    a.rec = static_cast<uint32_t *>(ws);
+    a.part = S > 0 ? a.rec + round_up(static_cast<size_t>(S) * tim::PPO_REC_WORDS, 64) : nullptr;
+    a.status = dev->status;
+    cudaError_t e = tim::ppo_launch(a, dev->sms, s);
+    cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "tis_ppo launch");
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(ppo workspace)");
     g_msg[0] = 0;
     return TIM_OK;
 }

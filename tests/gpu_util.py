@@ -7,6 +7,11 @@ Tolerances (written here, used by every GPU test):
     scale of their cancellation, max(|oracle|, oracle mean |delta|).  The
     rejection flag may differ only where the oracle's statistic is within
     1e-5 relative of the threshold.
+  * TIS-weighted PPO surrogate: token loss and gradient 1e-5 relative per
+    element (fp32 exp2 and three roundings stay below 2e-6 for |log-ratio| < 10);
+    the clip decisions exact (same zero-gradient tokens, same counts); sequence
+    and batch means 1e-5 of the matching mean |loss| (advantages of both signs
+    cancel in the sums).
 """
 import math
 
@@ -75,3 +80,38 @@ def assert_batch_match(g_b, o_b):
 
 def default_tau(C):
     return (C - 1.0) - math.log(C)
+
+
+PF = {n: i for i, n in enumerate(oracle.PPO_FIELDS)}
+
+
+def assert_ppo_match(g, o, off, what=""):
+    """g: dict of numpy arrays from the device (token_loss / token_grad may be
+    None); o: the oracle's dict on the same inputs."""
+    o_loss = o["token_loss"]
+    if g.get("token_loss") is not None:
+        _close(g["token_loss"], o_loss, np.abs(o_loss), what + " token_loss")
+    if g.get("token_grad") is not None:
+        assert np.array_equal(g["token_grad"] == 0, o["token_grad"] == 0), what + " clipped set"
+        _close(g["token_grad"], o["token_grad"], np.abs(o["token_grad"]), what + " token_grad")
+    off = np.asarray(off, np.int64)
+    S = off.size - 1
+    abs_loss = np.abs(o_loss)
+    csum = np.concatenate([[0.0], np.cumsum(abs_loss)])
+    cnz = np.concatenate([[0], np.cumsum(o_loss != 0)])
+    # a sequence's scale: the mean |loss| over its tokens with a nonzero loss
+    seq_scale = (csum[off[1:]] - csum[off[:-1]]) / np.maximum(cnz[off[1:]] - cnz[off[:-1]], 1)
+    o_seq = o["seq_loss"]
+    _close(g["seq_loss"], o_seq, np.maximum(np.abs(o_seq), seq_scale), what + " seq_loss")
+    gb, ob = np.asarray(g["batch"], np.float64), o["batch"]
+    for f in ("n_mask", "n_used", "n_ppo_clipped", "n_tis_clipped", "n_seqs_nonempty"):
+        assert gb[PF[f]] == ob[PF[f]], (what, f, gb[PF[f]], ob[PF[f]])
+    for f in ("ppo_clip_ratio", "tis_clip_ratio"):
+        _close(gb[PF[f]], ob[PF[f]], abs(ob[PF[f]]) * 0.1, what + " " + f)
+    n_used = max(ob[PF["n_used"]], 1.0)
+    _close(gb[PF["mean_loss"]], ob[PF["mean_loss"]], max(abs(ob[PF["mean_loss"]]), abs_loss.sum() / n_used),
+           what + " mean_loss")
+    ne = max(ob[PF["n_seqs_nonempty"]], 1.0)
+    _close(gb[PF["seqmean_loss"]], ob[PF["seqmean_loss"]],
+           max(abs(ob[PF["seqmean_loss"]]), np.abs(o_seq).sum() / ne), what + " seqmean_loss")
+    assert S == len(o_seq)

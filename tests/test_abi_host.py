@@ -112,6 +112,52 @@ def test_mismatch_stats_rejects_bad_arguments(lib):
     assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(batch=20), None) == E
 
 
+def test_ppo_struct_layout_matches(tmp_path):
+    src = tmp_path / "ppo_layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "tim.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(tim_ppo_out),"
+        "offsetof(tim_ppo_out,num_seqs),offsetof(tim_ppo_out,num_tokens),offsetof(tim_ppo_out,token_loss),"
+        "offsetof(tim_ppo_out,token_grad),offsetof(tim_ppo_out,seq_loss),offsetof(tim_ppo_out,batch_stats));"
+        "return TIM_PPO_FIELDS == 9 && TIM_PPO_N_SEQS_NONEMPTY == 8 ? 0 : 1;}\n")
+    exe = tmp_path / "ppo_layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                    "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    S = tim.tim_ppo_out
+    want = [ctypes.sizeof(S)] + [getattr(S, f).offset for f in
+                                 ("num_seqs", "num_tokens", "token_loss", "token_grad", "seq_loss", "batch_stats")]
+    assert vals == want
+    assert len(tim.PPO_FIELDS) == 9
+
+
+def _ppo_out(S=1, N=4, seq=16, batch=16, loss=None, grad=None):
+    d = tim.tim_ppo_out()
+    d.num_seqs, d.num_tokens = S, N
+    d.token_loss, d.token_grad, d.seq_loss, d.batch_stats = loss, grad, seq, batch
+    return d
+
+
+def test_tis_ppo_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    p6 = (16, 16, 16, 16, 16, 16)
+    assert lib.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, None, None) == E
+    for lo, hi, C in ((1.0, 0.2, 2.0), (-0.1, 0.2, 2.0), (math.nan, 0.2, 2.0), (0.2, -0.1, 2.0),
+                      (0.2, math.inf, 2.0), (0.2, math.nan, 2.0), (0.2, 0.2, 0.0), (0.2, 0.2, math.inf)):
+        assert tim.tim_tis_ppo(*p6, lo, hi, C, _ppo_out(), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(S=-1), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(S=0, N=3), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(seq=None), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(batch=None), None) == E
+    assert tim.tim_tis_ppo(None, 16, 16, 16, 16, 16, 0.2, 0.2, 2.0, _ppo_out(), None) == E
+    assert tim.tim_tis_ppo(16, 16, 16, 16, 16, None, 0.2, 0.2, 2.0, _ppo_out(), None) == E
+    assert tim.tim_tis_ppo(18, 16, 16, 16, 16, 16, 0.2, 0.2, 2.0, _ppo_out(), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(grad=18), None) == E
+    assert tim.tim_tis_ppo(*p6, 0.2, 0.2, 2.0, _ppo_out(batch=20), None) == E
+    assert "aligned" in tim.tim_last_error()
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(tim, "_lib", None)

@@ -198,13 +198,15 @@ def draw_rollout(cfg: HeadConfig, logp_train: np.ndarray, seed: int | None = Non
     outlier tokens shifted by +-outlier_shift with a fair sign)."""
     seed = cfg.seed if seed is None else seed
     rng = np.random.default_rng([seed, 5])
-    lt = np.asarray(logp_train, dtype=np.float64)
+    lt = np.asarray(logp_train)
     noise = rng.normal(0.0, cfg.rollout_std, size=lt.shape)
     if cfg.outlier_frac > 0.0:
         hit = rng.random(lt.shape) < cfg.outlier_frac
-        sign = np.where(rng.random(lt.shape) < 0.5, -1.0, 1.0)
-        noise = noise + hit * sign * cfg.outlier_shift
-    return (lt + noise).astype(np.float32)
+        u = rng.random(lt.shape)
+        noise[hit] += np.where(u[hit] < 0.5, -1.0, 1.0) * cfg.outlier_shift
+        del u, hit
+    noise += lt
+    return noise.astype(np.float32)
 
 
 def draw_train_logprobs(N: int, seed: int) -> np.ndarray:
@@ -212,3 +214,42 @@ def draw_train_logprobs(N: int, seed: int) -> np.ndarray:
     <= 0, most mass near 0 with a long tail (a Gamma(0.6, 3) magnitude)."""
     rng = np.random.default_rng([seed, 6])
     return (-rng.gamma(0.6, 3.0, size=N)).astype(np.float32)
+
+
+def draw_policy_update(logp_old: np.ndarray, std: float, seed: int) -> np.ndarray:
+    """Stand-in current-policy logprobs for the PPO surrogate: fp32
+    logp_old + N(0, std^2), the drift of a few optimiser steps since the
+    rollout policy's snapshot."""
+    rng = np.random.default_rng([seed, 7])
+    lo = np.asarray(logp_old, dtype=np.float64)
+    return (lo + rng.normal(0.0, std, size=lo.shape)).astype(np.float32)
+
+
+def draw_advantages(seq_offsets: np.ndarray, seed: int) -> np.ndarray:
+    """fp32 [N] advantages, one N(0, 1) value per sequence broadcast to its
+    tokens (an outcome reward normalised over its group, as in GRPO)."""
+    off = np.asarray(seq_offsets, dtype=np.int64)
+    rng = np.random.default_rng([seed, 8])
+    per_seq = rng.standard_normal(len(off) - 1)
+    return np.repeat(per_seq, np.diff(off)).astype(np.float32)
+
+
+def draw_ppo_inputs(N: int, seed: int, update_std: float = 0.1):
+    """Packed inputs of the TIS-weighted PPO surrogate, N tokens: Llama-like
+    segments (lognormal lengths, median 1024, clipped to [128, 4096]), 30% of
+    tokens masked out, trainer logprobs l_old as in ``draw_train_logprobs``,
+    rollout logprobs l_old + N(0, 0.02^2) with 0.5% outliers shifted by +-1
+    (l_old has the law of ``draw_train_logprobs``, drawn in fp32 for speed),
+    current-policy logprobs l_old + N(0, update_std^2), per-sequence N(0, 1)
+    advantages.  Returns (seq_offsets, mask, l_theta, l_old, l_rollout, adv)."""
+    cfg = HeadConfig("ppo", N=N, D=8, V=8, seq_layout="lognormal", mask_drop=0.3, rollout_std=0.02,
+                     outlier_frac=0.005, outlier_shift=1.0, seed=seed)
+    off = draw_segments(cfg)
+    mask = draw_mask(cfg, off)
+    rng = np.random.default_rng([seed, 9])
+    l_old = rng.standard_gamma(0.6, size=N, dtype=np.float32)
+    l_old *= np.float32(-3.0)
+    l_ro = draw_rollout(cfg, l_old)
+    l_th = draw_policy_update(l_old, update_std, seed)
+    adv = draw_advantages(off, seed)
+    return off, mask, l_th, l_old, l_ro, adv
