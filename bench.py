@@ -55,6 +55,10 @@ MEASURED_TRAFFIC = {
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 PPO_TRAFFIC_TOKENS = 1 << 25
+# L2 flush before each timed launch of a single call: 1 GiB, 8x the L2; its
+# ~0.15 ms fill also lets the host enqueue the timed call before the GPU
+# reaches the start event, so host-side call overhead stays out of the time.
+FLUSH_BYTES = 1 << 30
 
 
 def source_hash(kind: str) -> str:
@@ -471,7 +475,7 @@ def batch_size_sweep(tim, dev, stream, Wd, D, V, peaks, sizes=(1, 7, 512, 4096, 
     import torch
     g = torch.Generator(device=dev)
     g.manual_seed(11)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     out = []
     for n in sizes:
         h = torch.randn((n, D), generator=g, device=dev).to(torch.bfloat16)
@@ -516,7 +520,7 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
            "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
            "batch": torch.empty(20, dtype=torch.float64, device=dev),
            "token_weight": torch.empty(Nt, dtype=torch.float32, device=dev)}
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
         tim.mismatch_stats(l_tr, l_ro, mask, offd, out=out)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
@@ -564,7 +568,7 @@ def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=
            "token_grad": torch.empty(Nt, dtype=torch.float32, device=dev),
            "seq_loss": torch.empty(S, dtype=torch.float32, device=dev),
            "batch": torch.empty(9, dtype=torch.float64, device=dev)}
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     call = lambda: tim.tis_ppo(l_th, l_old, l_ro, adv, mask, offd, eps_low=0.2, eps_high=0.28, C=2.0,  # noqa: E731
                                out=out)
     for _ in range(warmup):

@@ -42,6 +42,7 @@ struct PpoArgs {
     double *batch;         // [TIM_PPO_FIELDS]
     uint32_t *rec;         // workspace: sequence records, [PPO_REC_WORDS][S]
     uint32_t *part;        // workspace: fold partials, [ceil(S / PPO_FOLD_SEQS)][PPO_PART_WORDS]
+    unsigned *ticket;      // workspace: fold CTAs finished (zeroed by ppo_seq_kernel)
     int *status;
 };
 

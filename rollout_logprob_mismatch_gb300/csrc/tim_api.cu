@@ -417,6 +417,9 @@ int tim_tis_ppo(const float *logp_theta, const float *logp_old, const float *log
     a.batch = out->batch_stats;
     a.rec = static_cast<uint32_t *>(ws);
     a.part = S > 0 ? a.rec + round_up(static_cast<size_t>(S) * tim::PPO_REC_WORDS, 64) : nullptr;
+    a.ticket = S > 0 ? a.part + round_up(static_cast<size_t>((S + tim::PPO_FOLD_SEQS - 1) / tim::PPO_FOLD_SEQS) *
+                                             tim::PPO_PART_WORDS, 64)
+                     : nullptr;
     a.status = dev->status;
     cudaError_t e = tim::ppo_launch(a, dev->sms, s);
     cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;

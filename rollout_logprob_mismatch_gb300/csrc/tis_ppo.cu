@@ -9,7 +9,7 @@
 // Per sequence: mean loss over its used tokens; per batch: token mean, mean of
 // sequence means, clip fractions.
 //
-// Three launches at most, fp32 and integer arithmetic only:
+// Two launches, fp32 and integer arithmetic only:
 //  1. ppo_seq_kernel, three 256-thread CTAs per SM.  A sequence of at most 8192
 //     tokens is handled by one warp, a longer one by a whole CTA.  A warp steps
 //     through its sequence 256 tokens at a time: lane i owns the tokens at index
@@ -25,8 +25,8 @@
 //     out), so HBM bounds it; there is no staging and no wait to bound.
 //  2. ppo_fold_kernel: CTA j folds sequences 1024 j .. 1024 j + 1023 (4 per
 //     thread, structure-of-arrays records) with float-float (TwoSum) sums and
-//     integer counts in a fixed tree.
-//  3. ppo_final_kernel (only when S > 1024): one CTA folds the partials in order.
+//     integer counts in a fixed tree; when there are several CTAs, the last one
+//     to finish folds their partials in index order.
 // The batch record depends on S and the sequence records only.
 #include <algorithm>
 #include <cfloat>
@@ -144,6 +144,28 @@ __device__ __forceinline__ void ppo_step(PpoAcc &acc, const PpoArgs &a, int64_t 
     acc.inner = make_float2(0.f, 0.f);
 }
 
+// L2 prefetch of tokens [t0, t1) of the five input arrays, one bulk prefetch
+// per array on lanes 0..4.  Each byte range is widened to whole 16-byte
+// granules (the instruction's alignment rule); a granule holding a byte of an
+// array lies in a page of that array, so nothing outside the arrays' pages is
+// touched.  A prefetch is only a hint: the loads that follow stay correct
+// whether or not it has landed.
+__device__ __forceinline__ void prefetch_tokens(const PpoArgs &a, int64_t t0, int64_t t1, int lane)
+{
+    if (lane >= 5 || t1 <= t0)
+        return;
+    const void *base = lane == 0 ? static_cast<const void *>(a.l_th)
+                     : lane == 1 ? static_cast<const void *>(a.l_old)
+                     : lane == 2 ? static_cast<const void *>(a.l_ro)
+                     : lane == 3 ? static_cast<const void *>(a.adv)
+                                 : static_cast<const void *>(a.mask);
+    const int64_t esz = lane == 4 ? 1 : 4;
+    const uintptr_t lo = (reinterpret_cast<uintptr_t>(base) + t0 * esz) & ~uintptr_t(15);
+    const uintptr_t hi = (reinterpret_cast<uintptr_t>(base) + t1 * esz + 15) & ~uintptr_t(15);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(lo), "r"(static_cast<uint32_t>(hi - lo)) : "memory");
+}
+
 __device__ __forceinline__ void ppo_range(PpoAcc &acc, const PpoArgs &a, int64_t t0, int64_t e, int lane)
 {
     if (e - t0 >= PPO_CHUNK)
@@ -227,6 +249,8 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();                // the inputs may be written by the previous kernel
     pdl_launch_dependents();   // the fold kernel may start launching
+    if (blockIdx.x == 0 && tid == 0)
+        *a.ticket = 0u;        // the fold kernel reads it after this grid completes
     bool mine = false;         // does this CTA own a sequence longer than PPO_LONG?
     for (int q = blockIdx.x + tid * gridDim.x; q < a.S; q += PPO_THREADS * gridDim.x) {
         const int64_t b = a.off[q], e = a.off[q + 1];
@@ -236,8 +260,17 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
 
     // ---- phase 1: sequences of at most PPO_LONG tokens, one warp each.  Warp w
     // of CTA c takes sequences w * gridDim + c, + warps in the grid, ...
+    // The warp's token stream is prefetched into L2 ahead of its loads: steps
+    // c + 2 of a sequence during step c, and the first two steps of the warp's
+    // next sequence when a sequence starts.
     const int step = gridDim.x * PPO_WARPS;
-    for (int s = warp * gridDim.x + blockIdx.x; s < a.S; s += step) {
+    const int first = warp * gridDim.x + blockIdx.x;
+    if (first < a.S) {
+        const int64_t b = a.off[first], e = a.off[first + 1];
+        if (offsets_ok(a, first, b, e))
+            prefetch_tokens(a, b, min(e, b + 2 * PPO_CHUNK), lane);
+    }
+    for (int s = first; s < a.S; s += step) {
         const int64_t b = a.off[s], e = a.off[s + 1];
         if (!offsets_ok(a, s, b, e)) {
             write_plain(a, s, true, lane);
@@ -245,10 +278,17 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
         }
         if (e - b > PPO_LONG)
             continue;
+        if (s + step < a.S) {
+            const int64_t nb = a.off[s + step], ne = a.off[s + step + 1];
+            if (offsets_ok(a, s + step, nb, ne))
+                prefetch_tokens(a, nb, min(ne, nb + 2 * PPO_CHUNK), lane);
+        }
         PpoAcc acc;
         acc_zero(acc);
-        for (int64_t t0 = b; t0 < e; t0 += PPO_CHUNK)
+        for (int64_t t0 = b; t0 < e; t0 += PPO_CHUNK) {
+            prefetch_tokens(a, t0 + 2 * PPO_CHUNK, min(e, t0 + 3 * PPO_CHUNK), lane);
             ppo_range(acc, a, t0, e, lane);
+        }
         write_seq(a, s, warp_total(acc), lane);
     }
 
@@ -263,8 +303,11 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
         __syncthreads();   // the previous long sequence's reduction buffers are free
         PpoAcc acc;
         acc_zero(acc);
-        for (int64_t t0 = b + static_cast<int64_t>(warp) * PPO_CHUNK; t0 < e; t0 += PPO_WARPS * PPO_CHUNK)
+        for (int64_t t0 = b + static_cast<int64_t>(warp) * PPO_CHUNK; t0 < e; t0 += PPO_WARPS * PPO_CHUNK) {
+            const int64_t p0 = t0 + PPO_WARPS * PPO_CHUNK;   // this warp's next step
+            prefetch_tokens(a, p0, min(e, p0 + PPO_CHUNK), lane);
             ppo_range(acc, a, t0, e, lane);
+        }
         const SeqTot t = warp_total(acc);
         if (lane == 0) {
             red_f[warp] = t.sum;
@@ -438,67 +481,103 @@ __device__ void write_batch(const PpoArgs &a, const FoldAcc &t, bool check_offse
 }
 
 // The fold term of sequence s.
-__device__ __forceinline__ void fold_seq(FoldAcc &x, const PpoArgs &a, int64_t s)
+// The words of sequence s that the fold reads: its record and its mean.  Every
+// sequence has both (a bad one an all-zero record), so they are loaded
+// unconditionally, all sequences of a thread at once.
+struct SeqWords {
+    uint32_t w[PPO_REC_WORDS];
+    float mean;
+};
+
+__device__ __forceinline__ SeqWords load_seq(const PpoArgs &a, int64_t s)
 {
     const size_t S = static_cast<size_t>(a.S);
-    const uint32_t *rc = a.rec + s;
+    SeqWords v;
+#pragma unroll
+    for (int f = 0; f < PPO_REC_WORDS; ++f)
+        v.w[f] = __ldg(a.rec + f * S + s);
+    v.mean = __ldg(a.seq_loss + s);
+    return v;
+}
+
+// The fold term of one sequence.
+__device__ __forceinline__ void fold_seq(FoldAcc &x, const SeqWords &v)
+{
     FoldAcc y;
     fold_zero(y);
-    if (rc[R_VALID * S] == 0u) {
+    if (v.w[R_VALID] == 0u) {
         y.cnt[P_INVALID] = 1;
     } else {
-        const uint32_t nu = rc[R_N_USED * S];
-        y.cnt[P_N_MASK] = rc[R_N_MASK * S];
+        const uint32_t nu = v.w[R_N_USED];
+        y.cnt[P_N_MASK] = v.w[R_N_MASK];
         y.cnt[P_N_USED] = nu;
-        y.cnt[P_N_PPO] = rc[R_N_PPO * S];
-        y.cnt[P_N_TIS] = rc[R_N_TIS * S];
-        y.sum[S_LOSS] = {__uint_as_float(rc[R_SUM * S]), 0.f};
+        y.cnt[P_N_PPO] = v.w[R_N_PPO];
+        y.cnt[P_N_TIS] = v.w[R_N_TIS];
+        y.sum[S_LOSS] = {__uint_as_float(v.w[R_SUM]), 0.f};
         if (nu > 0u) {
             y.cnt[P_NONEMPTY] = 1;
-            y.sum[S_SEQMEAN] = {a.seq_loss[s], 0.f};
+            y.sum[S_SEQMEAN] = {v.mean, 0.f};
         }
     }
     fold_add(x, y);
 }
 
-// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i;
-// with a single CTA it writes the batch record directly.
+// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i.
+// With a single CTA it writes the batch record directly; otherwise each CTA
+// stores its partial and the CTA that finishes last (a ticket counter) folds
+// the partials in index order, thread i taking partials i, i + 256, ...  The
+// result does not depend on which CTA finishes last.
 __global__ void __launch_bounds__(PPO_FOLD_THREADS) ppo_fold_kernel(const PpoArgs a)
 {
-    pdl_wait();   // the records come from ppo_seq_kernel
+    __shared__ int last_s;
+    pdl_wait();   // the records (and the zeroed ticket) come from ppo_seq_kernel
     pdl_launch_dependents();
     FoldAcc x;
     fold_zero(x);
     const int64_t base = static_cast<int64_t>(blockIdx.x) * PPO_FOLD_SEQS + threadIdx.x;
-#pragma unroll 1
-    for (int k = 0; k < PPO_FOLD_SEQS / PPO_FOLD_THREADS; ++k) {
+    constexpr int KS = PPO_FOLD_SEQS / PPO_FOLD_THREADS;
+    SeqWords v[KS];
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
         const int64_t s = base + static_cast<int64_t>(k) * PPO_FOLD_THREADS;
         if (s < a.S)
-            fold_seq(x, a, s);
+            v[k] = load_seq(a, s);
     }
+#pragma unroll
+    for (int k = 0; k < KS; ++k)
+        if (base + static_cast<int64_t>(k) * PPO_FOLD_THREADS < a.S)
+            fold_seq(x, v[k]);
     const FoldAcc t = fold_cta(x);
     if (threadIdx.x == 0) {
-        if (gridDim.x == 1)
+        if (gridDim.x == 1) {
             write_batch(a, t, false);
-        else
+        } else {
             fold_store(a.part + static_cast<size_t>(blockIdx.x) * PPO_PART_WORDS, t);
+            __threadfence();
+            last_s = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+        }
     }
-}
-
-// One CTA folds the partials: thread i takes partials i, i + 256, ... in order.
-__global__ void __launch_bounds__(PPO_FOLD_THREADS) ppo_final_kernel(const PpoArgs a, int parts)
-{
-    pdl_wait();   // the partials come from ppo_fold_kernel
-    FoldAcc x;
-    fold_zero(x);
-    for (int p = threadIdx.x; p < parts; p += PPO_FOLD_THREADS) {
-        FoldAcc y;
-        fold_load(y, a.part + static_cast<size_t>(p) * PPO_PART_WORDS);
-        fold_add(x, y);
+    if (gridDim.x == 1)
+        return;
+    __syncthreads();
+    if (!last_s)   // uniform over the CTA
+        return;
+    __threadfence();
+    FoldAcc y;
+    fold_zero(y);
+    for (int p = threadIdx.x; p < static_cast<int>(gridDim.x); p += PPO_FOLD_THREADS) {
+        const uint32_t *src = a.part + static_cast<size_t>(p) * PPO_PART_WORDS;
+        uint32_t w[PPO_PART_WORDS];
+#pragma unroll
+        for (int i = 0; i < PPO_PART_WORDS; ++i)
+            w[i] = __ldcg(src + i);   // written by other CTAs: read through L2
+        FoldAcc z;
+        fold_load(z, w);
+        fold_add(y, z);
     }
-    const FoldAcc t = fold_cta(x);
+    const FoldAcc f = fold_cta(y);
     if (threadIdx.x == 0)
-        write_batch(a, t, false);
+        write_batch(a, f, false);
 }
 
 // S = 0: only the (all-zero) batch record, after checking the offsets cover [0, N).
@@ -530,13 +609,7 @@ cudaError_t ppo_launch(const PpoArgs &a, int num_sms, cudaStream_t stream)
     const int parts = (a.S + PPO_FOLD_SEQS - 1) / PPO_FOLD_SEQS;
     cfg.gridDim = dim3(parts, 1, 1);
     cfg.blockDim = dim3(PPO_FOLD_THREADS, 1, 1);
-    if ((e = cudaLaunchKernelEx(&cfg, ppo_fold_kernel, a)) != cudaSuccess)
-        return e;
-    if (parts > 1) {
-        cfg.gridDim = dim3(1, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, ppo_final_kernel, a, parts);
-    }
-    return e;
+    return cudaLaunchKernelEx(&cfg, ppo_fold_kernel, a);
 }
 
 } // namespace tim
