@@ -52,6 +52,8 @@ MEASURED_TRAFFIC = {
     ("k1", "006ea2b16082c21a"): 3050926592 + 18969088,
     # mismatch pass, 2^25 tokens: 305292544 read + 97732352 written (traffic scales with tokens)
     ("k2", "4f3f821e3a24f689"): 305292544 + 97732352,
+    # TIS-weighted PPO surrogate, 2^25 tokens: 612692224 read + 216128768 written (scales with tokens)
+    ("ppo", "e67331ce7a3218ab"): 612692224 + 216128768,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 PPO_TRAFFIC_TOKENS = 1 << 25
