@@ -10,6 +10,8 @@ input generators of ``workloads``.
 lse = log sum exp z, logp = z[a] - lse.
 ``tis_ppo``        -- the TIS-weighted PPO clipped surrogate, its gradient and
 masked means (VeXact summary eq. (2)-(3); HN "Clipped importance ratios").
+``mismatch_monitor`` -- p95 |delta|, ratio quantiles 0.01 / 0.5 / 0.99, extreme
+token fraction and token rejection (llm-infra-atlas section 7; VeXact tau_tok).
 ``mismatch_stats`` -- delta, r, k1/k2/k3, truncated-IS weight, masked
 per-sequence and batch means and the rejection flag (VeXact summary eq. (1)
 and "KL Estimators"; llm-infra-atlas section 2; icarus "KL estimators",
@@ -42,6 +44,9 @@ BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_d
 PPO_FIELDS = ("n_mask", "n_used", "n_ppo_clipped", "n_tis_clipped", "mean_loss", "seqmean_loss",
               "ppo_clip_ratio", "tis_clip_ratio", "n_seqs_nonempty")
 
+MONITOR_FIELDS = ("n_used", "p95_abs_delta", "ratio_q01", "ratio_q50", "ratio_q99", "n_extreme",
+                  "frac_extreme")
+
 
 def build(force: bool = False) -> str:
     """Compile oracle.c with plain gcc -O2 (no fast-math) into _liboracle.so."""
@@ -70,6 +75,9 @@ def _load():
             lib.oracle_tis_ppo.argtypes = [P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
                                            ctypes.c_double, ctypes.c_double, P, P, P, P]
             lib.oracle_tis_ppo.restype = ctypes.c_int
+            lib.oracle_mismatch_monitor.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_double, P, P]
+            lib.oracle_mismatch_monitor.restype = ctypes.c_int
+            assert lib.oracle_monitor_fields() == len(MONITOR_FIELDS)
             assert lib.oracle_ppo_fields() == len(PPO_FIELDS)
             assert lib.oracle_seq_fields() == len(SEQ_FIELDS)
             assert lib.oracle_batch_fields() == len(BATCH_FIELDS)
@@ -158,3 +166,21 @@ def tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, e
     if rc != 0:
         raise ValueError("oracle_tis_ppo rejected its arguments")
     return {"token_loss": loss, "token_grad": grad, "seq_loss": seq, "batch": batch}
+
+
+def mismatch_monitor(logp_train, logp_rollout, mask, tau_tok: float):
+    """Distribution monitor of delta = logp_train - logp_rollout over the used
+    tokens (llm-infra-atlas section 7; VeXact tau_tok): dict with batch
+    [7] (MONITOR_FIELDS, float64) and reject [N] uint8."""
+    lib = _load()
+    lt = np.ascontiguousarray(logp_train, dtype=np.float32)
+    lr = np.ascontiguousarray(logp_rollout, dtype=np.float32)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    N = lt.size
+    assert lr.size == N and m.size == N
+    out = np.empty(len(MONITOR_FIELDS), dtype=np.float64)
+    rej = np.empty(N, dtype=np.uint8)
+    rc = lib.oracle_mismatch_monitor(_ptr(lt), _ptr(lr), _ptr(m), N, float(tau_tok), _ptr(out), _ptr(rej))
+    if rc != 0:
+        raise ValueError("oracle_mismatch_monitor rejected its arguments")
+    return {"batch": out, "reject": rej}

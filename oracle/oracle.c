@@ -432,3 +432,88 @@ int oracle_tis_ppo(const float *l_theta, const float *l_old, const float *l_roll
     batch[PB_N_SEQS_NONEMPTY] = b_nonempty;
     return 0;
 }
+
+/* ------------------------------------------------------------------ mismatch monitor
+ *
+ * llm-infra-atlas section 7, the list of mismatch metrics compared per
+ * response token over a rollout dump: the p95 of |logp_train - logp_rollout|,
+ * the 0.01 / 0.5 / 0.99 quantiles of the ratio r = pi_train / pi_rollout =
+ * e^delta, and the fraction of tokens with |delta| > tau; VeXact summary,
+ * calibration of the token-level threshold tau_tok (a token is rejected when
+ * |delta| > tau_tok).
+ * Readings: the statistics run over the used tokens of the batch (mask != 0,
+ * finite fp32 delta); the quantile of a sample x_(0) <= ... <= x_(n-1) at
+ * level q is the linear interpolation at h = (n - 1) q between x_(floor h)
+ * and the next order statistic (the default of numpy and torch); an empty
+ * sample gives NaN quantiles.  Order statistics of r are those of delta (e^x
+ * is increasing), so r quantiles interpolate e^delta at delta's order
+ * statistics.  Outputs: out[MON_FIELDS]; reject[N] (may be NULL): 1 for a used
+ * token with |delta| > tau_tok, else 0. */
+enum { MO_N_USED, MO_P95_ABS_DELTA, MO_RATIO_Q01, MO_RATIO_Q50, MO_RATIO_Q99, MO_N_EXTREME, MO_FRAC_EXTREME,
+       MO_FIELDS };
+
+int oracle_monitor_fields(void) { return MO_FIELDS; }
+
+static int cmp_double(const void *a, const void *b)
+{
+    const double x = *(const double *)a, y = *(const double *)b;
+    return x < y ? -1 : x > y ? 1 : 0;
+}
+
+/* quantile at level q of the sorted sample x[0..n-1], n > 0 */
+static double quantile_sorted(const double *x, int64_t n, double q, int exp_values)
+{
+    const double h = (double)(n - 1) * q;
+    const double fl = floor(h);
+    const int64_t k = (int64_t)fl;
+    const int64_t k1 = k + 1 < n ? k + 1 : k;
+    const double lo = exp_values ? exp(x[k]) : x[k];
+    const double hi = exp_values ? exp(x[k1]) : x[k1];
+    return lo + (h - fl) * (hi - lo);
+}
+
+int oracle_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask, int64_t N,
+                            double tau_tok, double *out, uint8_t *reject)
+{
+    if (N < 0 || !out || !(tau_tok >= 0.0))
+        return -1;
+    if (N > 0 && (!logp_train || !logp_rollout || !mask))
+        return -1;
+    double *ad = N > 0 ? (double *)malloc(sizeof(double) * (size_t)N) : NULL;
+    double *d = N > 0 ? (double *)malloc(sizeof(double) * (size_t)N) : NULL;
+    if (N > 0 && (!ad || !d)) {
+        free(ad);
+        free(d);
+        return -2;
+    }
+    int64_t n = 0, n_ext = 0;
+    for (int64_t t = 0; t < N; ++t) {
+        const float d32 = logp_train[t] - logp_rollout[t];
+        const int used = mask[t] != 0 && isfinite(d32);
+        const int ext = used && fabs((double)d32) > tau_tok;
+        if (reject)
+            reject[t] = (uint8_t)ext;
+        if (used) {
+            d[n] = (double)d32;
+            ad[n] = fabs((double)d32);
+            ++n;
+            n_ext += ext;
+        }
+    }
+    out[MO_N_USED] = (double)n;
+    out[MO_N_EXTREME] = (double)n_ext;
+    out[MO_FRAC_EXTREME] = mean_or_zero((double)n_ext, (double)n);
+    if (n == 0) {
+        out[MO_P95_ABS_DELTA] = out[MO_RATIO_Q01] = out[MO_RATIO_Q50] = out[MO_RATIO_Q99] = NAN;
+    } else {
+        qsort(ad, (size_t)n, sizeof(double), cmp_double);
+        qsort(d, (size_t)n, sizeof(double), cmp_double);
+        out[MO_P95_ABS_DELTA] = quantile_sorted(ad, n, 0.95, 0);
+        out[MO_RATIO_Q01] = quantile_sorted(d, n, 0.01, 1);
+        out[MO_RATIO_Q50] = quantile_sorted(d, n, 0.5, 1);
+        out[MO_RATIO_Q99] = quantile_sorted(d, n, 0.99, 1);
+    }
+    free(ad);
+    free(d);
+    return 0;
+}

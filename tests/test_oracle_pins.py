@@ -496,3 +496,88 @@ def test_ppo_bad_arguments_rejected():
             oracle.tis_ppo(z, z, z, z, np.ones(3, np.uint8), np.array([0, 3], np.int32), **kw)
     with pytest.raises(ValueError):
         oracle.tis_ppo(z, z, z, z, np.ones(3, np.uint8), np.array([0, 2], np.int32))
+
+
+# --------------------------------------------------------------- mismatch monitor
+MF = {n: i for i, n in enumerate(oracle.MONITOR_FIELDS)}
+
+
+def _delta32(lt, lr):
+    return (np.asarray(lt, np.float32) - np.asarray(lr, np.float32)).astype(np.float64)
+
+
+def test_monitor_quantiles_match_numpy_linear_quantile():
+    """The quantiles are numpy's default ("linear", h = (n - 1) q) over the used
+    tokens: |delta| at 0.95, r = e^delta at 0.01 / 0.5 / 0.99 (llm-infra-atlas
+    section 7's metric list).  Masked and non-finite tokens are left out."""
+    rng = np.random.default_rng(50)
+    for n in (1, 2, 3, 10, 101, 5000):
+        lt = wl.draw_train_logprobs(n, 50 + n)
+        lr = (lt + rng.normal(0, 0.05, n)).astype(np.float32)
+        mask = (rng.random(n) < 0.8).astype(np.uint8)
+        if n > 3:
+            lt[1] = np.nan
+            lr[2] = -np.inf
+            mask[[1, 2]] = 1
+        o = oracle.mismatch_monitor(lt, lr, mask, 0.1)["batch"]
+        d = _delta32(lt, lr)
+        used = (mask != 0) & np.isfinite(d)
+        assert o[MF["n_used"]] == used.sum()
+        if used.sum() == 0:
+            assert np.isnan(o[MF["p95_abs_delta"]])
+            continue
+        du = d[used]
+        np.testing.assert_allclose(o[MF["p95_abs_delta"]], np.quantile(np.abs(du), 0.95), rtol=1e-14)
+        for f, q in (("ratio_q01", 0.01), ("ratio_q50", 0.5), ("ratio_q99", 0.99)):
+            np.testing.assert_allclose(o[MF[f]], np.quantile(np.exp(du), q), rtol=1e-14)
+
+
+def test_monitor_normal_law():
+    """delta ~ N(0, s^2): p95 |delta| -> 1.95996 s, median ratio -> 1,
+    q99 ratio -> e^{2.32635 s}, P(|delta| > tau) -> 2 (1 - Phi(tau / s));
+    tolerances are five standard errors of the sample quantile / fraction."""
+    n, s, tau = 1_000_000, 0.05, 0.08
+    rng = np.random.default_rng(51)
+    lr = wl.draw_train_logprobs(n, 51)
+    lt = (lr.astype(np.float64) + rng.normal(0, s, n)).astype(np.float32)
+    o = oracle.mismatch_monitor(lt, lr, np.ones(n, np.uint8), tau)["batch"]
+    z95 = scipy.stats.norm.ppf(0.975)
+    se = math.sqrt(0.95 * 0.05 / n) / (2 * scipy.stats.norm.pdf(z95) / s)
+    assert abs(o[MF["p95_abs_delta"]] - z95 * s) < 5 * se
+    se50 = math.sqrt(0.25 / n) / (scipy.stats.norm.pdf(0) / s)
+    assert abs(math.log(o[MF["ratio_q50"]])) < 5 * se50
+    z99 = scipy.stats.norm.ppf(0.99)
+    se99 = math.sqrt(0.99 * 0.01 / n) / (scipy.stats.norm.pdf(z99) / s)
+    assert abs(math.log(o[MF["ratio_q99"]]) - z99 * s) < 5 * se99
+    assert abs(math.log(o[MF["ratio_q01"]]) + z99 * s) < 5 * se99
+    p = 2 * scipy.stats.norm.sf(tau / s)
+    assert abs(o[MF["frac_extreme"]] - p) < 5 * math.sqrt(p * (1 - p) / n)
+
+
+def test_monitor_exact_small_cases_and_rejection():
+    """Single token: every quantile is that token; two tokens: the median is
+    the midpoint of the two ratios; the reject flag is |delta| > tau_tok,
+    strict, only for used tokens (VeXact summary, tau_tok)."""
+    one = oracle.mismatch_monitor(np.float32([-1.0]), np.float32([-1.5]), np.uint8([1]), 0.5)
+    b = one["batch"]
+    assert b[MF["p95_abs_delta"]] == 0.5 and b[MF["ratio_q01"]] == b[MF["ratio_q99"]] == math.exp(0.5)
+    assert one["reject"][0] == 0 and b[MF["n_extreme"]] == 0          # |delta| = tau exactly: kept
+    two = oracle.mismatch_monitor(np.float32([-1.0, -2.0]), np.float32([-1.25, -1.5]), np.uint8([1, 1]), 0.3)
+    assert two["batch"][MF["ratio_q50"]] == pytest.approx((math.exp(0.25) + math.exp(-0.5)) / 2, rel=1e-15)
+    assert list(two["reject"]) == [0, 1] and two["batch"][MF["frac_extreme"]] == 0.5
+    masked = oracle.mismatch_monitor(np.float32([0.0, -3.0]), np.float32([-5.0, -3.0]), np.uint8([0, 1]), 0.1)
+    assert list(masked["reject"]) == [0, 0] and masked["batch"][MF["ratio_q50"]] == 1.0
+    empty = oracle.mismatch_monitor(np.float32([np.nan]), np.float32([0.0]), np.uint8([1]), 0.1)["batch"]
+    assert empty[MF["n_used"]] == 0 and np.isnan(empty[MF["ratio_q50"]]) and empty[MF["frac_extreme"]] == 0
+
+
+def test_monitor_is_order_free():
+    rng = np.random.default_rng(52)
+    n = 3001
+    lt = wl.draw_train_logprobs(n, 52)
+    lr = (lt + rng.normal(0, 0.1, n)).astype(np.float32)
+    m = (rng.random(n) < 0.7).astype(np.uint8)
+    p = rng.permutation(n)
+    a = oracle.mismatch_monitor(lt, lr, m, 0.15)
+    b = oracle.mismatch_monitor(lt[p], lr[p], m[p], 0.15)
+    assert np.array_equal(a["batch"], b["batch"]) and np.array_equal(a["reject"][p], b["reject"])
