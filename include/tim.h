@@ -216,6 +216,42 @@ TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollou
                        const uint8_t *mask, const int32_t *seq_offsets, float C,
                        const tim_mismatch_out *out, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ mismatch monitor
+ *
+ * Distribution of the mismatch over the used tokens of a batch (mask != 0 and
+ * finite fp32 delta = logp_train - logp_rollout), as listed among the
+ * per-token mismatch metrics of llm-infra-atlas section 7: the p95 of |delta|,
+ * the 0.01 / 0.5 / 0.99 quantiles of the ratio r = e^delta and the fraction of
+ * tokens with |delta| > tau_tok; plus the token-level rejection of the VeXact
+ * summary (a used token is rejected when |delta| > tau_tok).
+ * Quantile at level q of n values: the linear interpolation at h = (n - 1) q
+ * between the order statistics floor(h) and floor(h) + 1 (numpy's and torch's
+ * default).  The order statistics are selected exactly (the same tokens as a
+ * sort would pick); NaN quantiles when no token is used.
+ */
+#define TIM_MON_FIELDS 7
+enum tim_monitor_field {
+    TIM_MON_N_USED = 0,
+    TIM_MON_P95_ABS_DELTA,
+    TIM_MON_RATIO_Q01,
+    TIM_MON_RATIO_Q50,
+    TIM_MON_RATIO_Q99,
+    TIM_MON_N_EXTREME,          /* used tokens with |delta| > tau_tok */
+    TIM_MON_FRAC_EXTREME        /* n_extreme / n_used (0 when n_used = 0) */
+};
+
+/*   logp_train, logp_rollout  fp32 [N], 16-byte aligned
+ *   mask                      uint8 [N], 16-byte aligned
+ *   N                         tokens, 0 <= N < 2^31
+ *   tau_tok                   rejection threshold on |delta|, >= 0 and finite
+ *   token_reject              out, optional (NULL = not written): uint8 [N], 16-byte aligned
+ *   out                       out: fp64 [TIM_MON_FIELDS]
+ * Three passes over the tokens (9 bytes each per token) and three single-CTA
+ * selection steps.  Scratch: about 115 KB from the library's stream-ordered pool. */
+TIM_API int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                                 int64_t N, float tau_tok, uint8_t *token_reject, double *out,
+                                 tim_stream_t stream);
+
 /* ------------------------------------------------------------------ TIS-weighted PPO surrogate
  *
  * The clipped PPO surrogate of VeXact summary eq. (2) in recompute mode

@@ -26,10 +26,10 @@ import os
 import threading
 
 __all__ = [
-    "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
+    "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "MONITOR_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
     "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
-    "tim_tis_ppo", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
-    "token_logprob", "mismatch_stats", "tis_ppo", "check",
+    "tim_tis_ppo", "tim_mismatch_monitor", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "token_logprob", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +52,9 @@ BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_d
 
 PPO_FIELDS = ("n_mask", "n_used", "n_ppo_clipped", "n_tis_clipped", "mean_loss", "seqmean_loss",
               "ppo_clip_ratio", "tis_clip_ratio", "n_seqs_nonempty")
+
+MONITOR_FIELDS = ("n_used", "p95_abs_delta", "ratio_q01", "ratio_q50", "ratio_q99", "n_extreme",
+                  "frac_extreme")
 
 
 class TimError(RuntimeError):
@@ -116,6 +119,8 @@ def load():
             F = ctypes.c_float
             lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
             lib.tim_tis_ppo.restype = ctypes.c_int
+            lib.tim_mismatch_monitor.argtypes = [P, P, P, I64, F, P, P, P]
+            lib.tim_mismatch_monitor.restype = ctypes.c_int
             lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
             lib.tim_selftest_wait_timeout.restype = ctypes.c_int
             lib.tim_check.argtypes = [P]
@@ -156,6 +161,11 @@ def tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offset
                 out: tim_ppo_out, stream) -> int:
     return load().tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets,
                               float(eps_low), float(eps_high), float(C), ctypes.byref(out), stream)
+
+
+def tim_mismatch_monitor(logp_train, logp_rollout, mask, N, tau_tok, token_reject, out, stream) -> int:
+    return load().tim_mismatch_monitor(logp_train, logp_rollout, mask, N, float(tau_tok), token_reject, out,
+                                       stream)
 
 
 def tim_selftest_wait_timeout(budget_us, stream) -> int:
@@ -273,6 +283,31 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
     with torch.cuda.device(dev):
         rc = tim_mismatch_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(),
                                 seq_offsets.data_ptr(), C, d, _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out
+
+
+def mismatch_monitor(logp_train, logp_rollout, mask, tau_tok: float, token_reject: bool = True, stream=None,
+                     out=None):
+    """Mismatch monitor over the used tokens: batch fp64 [7] (MONITOR_FIELDS:
+    n_used, p95 |delta|, ratio quantiles 0.01 / 0.5 / 0.99, n_extreme,
+    frac_extreme) and token_reject uint8 [N] (None unless requested)."""
+    import torch
+    _need(logp_train, "logp_train", torch.float32, 1)
+    dev = logp_train.device
+    _need(logp_rollout, "logp_rollout", torch.float32, 1, dev)
+    _need(mask, "mask", (torch.uint8, torch.bool), 1, dev)
+    N = logp_train.shape[0]
+    if logp_rollout.shape[0] != N or mask.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = {"batch": torch.empty(len(MONITOR_FIELDS), dtype=torch.float64, device=dev),
+               "token_reject": torch.empty(N, dtype=torch.uint8, device=dev) if token_reject else None}
+    rej = out.get("token_reject")
+    with torch.cuda.device(dev):
+        rc = tim_mismatch_monitor(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(), N, tau_tok,
+                                  None if rej is None else rej.data_ptr(), out["batch"].data_ptr(),
+                                  _stream_handle(stream, dev))
     _raise_if(rc)
     return out
 

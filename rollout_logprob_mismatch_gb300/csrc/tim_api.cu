@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/tim.h"
+#include "monitor_internal.h"
 #include "ppo_internal.h"
 #include "tim_internal.h"
 
@@ -100,7 +101,8 @@ int device_state(DeviceState **out)
     uint64_t keep = ~0ull;
     if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
         return cuda_fail(e, "cudaMemPoolSetAttribute");
-    if ((e = tim::k1_prepare_device()) != cudaSuccess || (e = tim::k2_prepare_device()) != cudaSuccess)
+    if ((e = tim::k1_prepare_device()) != cudaSuccess || (e = tim::k2_prepare_device()) != cudaSuccess ||
+        (e = tim::monitor_prepare_device()) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
     if (!g_encode) {
         void *fn = nullptr;
@@ -351,6 +353,54 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return cuda_fail(e, "mismatch_stats launch");
     if (ef != cudaSuccess)
         return cuda_fail(ef, "cudaFreeAsync(mismatch workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask, int64_t N,
+                         float tau_tok, uint8_t *token_reject, double *out, tim_stream_t stream)
+{
+    if (N < 0 || N >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "N must be in [0, 2^31)");
+    if (!(tau_tok >= 0.f) || !std::isfinite(tau_tok))
+        return fail(TIM_ERR_INVALID_ARG, "tau_tok must be >= 0 and finite");
+    if (!out)
+        return fail(TIM_ERR_INVALID_ARG, "out is required");
+    if (N > 0 && (!logp_train || !logp_rollout || !mask))
+        return fail(TIM_ERR_INVALID_ARG, "null token array");
+    if (!aligned(logp_train, 16) || !aligned(logp_rollout, 16) || !aligned(mask, 16) || !aligned(token_reject, 16))
+        return fail(TIM_ERR_INVALID_ARG, "logp_train, logp_rollout, mask and token_reject must be 16-byte aligned");
+    if (!aligned(out, 8))
+        return fail(TIM_ERR_INVALID_ARG, "misaligned array");
+
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, tim::MON_WORKSPACE_BYTES, dev->pool, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMallocFromPoolAsync(monitor workspace)");
+    tim::MonArgs a;
+    a.l_tr = logp_train;
+    a.l_ro = logp_rollout;
+    a.mask = mask;
+    a.N = N;
+    a.tau_tok = tau_tok;
+    a.reject = token_reject;
+    a.out = out;
+    a.st = static_cast<tim::MonState *>(ws);
+    a.hist1 = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + tim::MON_STATE_BYTES);
+    a.hist2 = a.hist1 + tim::MON_HIST1_WORDS;
+    a.hist3 = a.hist2 + tim::MON_HIST2_WORDS;
+    a.status = dev->status;
+    e = tim::monitor_launch(a, dev->sms, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "mismatch_monitor launch");
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(monitor workspace)");
     g_msg[0] = 0;
     return TIM_OK;
 }

@@ -158,6 +158,21 @@ def test_tis_ppo_rejects_bad_arguments(lib):
     assert "aligned" in tim.tim_last_error()
 
 
+def test_mismatch_monitor_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_mismatch_monitor(16, 16, 16, -1, 0.1, None, 16, None) == E
+    assert tim.tim_mismatch_monitor(16, 16, 16, 1 << 31, 0.1, None, 16, None) == E
+    for tau in (-0.1, math.nan, math.inf):
+        assert tim.tim_mismatch_monitor(16, 16, 16, 4, tau, None, 16, None) == E
+    assert tim.tim_mismatch_monitor(16, 16, 16, 4, 0.1, None, None, None) == E
+    assert tim.tim_mismatch_monitor(None, 16, 16, 4, 0.1, None, 16, None) == E
+    assert tim.tim_mismatch_monitor(16, 16, 20, 4, 0.1, None, 16, None) == E
+    assert tim.tim_mismatch_monitor(16, 16, 16, 4, 0.1, 8, 16, None) == E
+    assert tim.tim_mismatch_monitor(16, 16, 16, 4, 0.1, None, 12, None) == E
+    assert "aligned" in tim.tim_last_error()
+    assert len(tim.MONITOR_FIELDS) == 7
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(tim, "_lib", None)

@@ -1,0 +1,115 @@
+"""GPU parity of tim_mismatch_monitor against the fp64 oracle: exact order
+statistics (the same tokens a sort picks), counts and rejection flags, on
+ragged sizes, ties, empty batches and the full-size batch the benchmark
+times; repeat determinism."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import rollout_logprob_mismatch_gb300 as tim  # noqa: E402
+
+MF = {n: i for i, n in enumerate(oracle.MONITOR_FIELDS)}
+RATIOS = ("ratio_q01", "ratio_q50", "ratio_q99")
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def gpu_monitor(lt, lr, mask, tau):
+    out = tim.mismatch_monitor(_dev(lt), _dev(lr), _dev(mask), tau)
+    tim.check()
+    return out["batch"].cpu().numpy(), out["token_reject"].cpu().numpy()
+
+
+def assert_monitor_match(g, g_rej, o, what=""):
+    ob, orej = o["batch"], o["reject"]
+    for f in ("n_used", "n_extreme"):
+        assert g[MF[f]] == ob[MF[f]], (what, f, g[MF[f]], ob[MF[f]])
+    assert np.array_equal(g_rej, orej), what
+    if ob[MF["n_used"]] == 0:
+        assert all(np.isnan(g[MF[f]]) for f in ("p95_abs_delta",) + RATIOS), what
+        return
+    # |delta| order statistics are fp32 values on both sides and the
+    # interpolation is the same fp64 expression: equal to rounding
+    np.testing.assert_allclose(g[MF["p95_abs_delta"]], ob[MF["p95_abs_delta"]], rtol=1e-15, err_msg=what)
+    for f in RATIOS:   # e^delta: fp32 expf on the device
+        np.testing.assert_allclose(g[MF[f]], ob[MF[f]], rtol=1e-6, err_msg=what + " " + f)
+    np.testing.assert_allclose(g[MF["frac_extreme"]], ob[MF["frac_extreme"]], rtol=1e-15, err_msg=what)
+
+
+def _batch(N, seed, spread=0.05, tau=0.1):
+    rng = np.random.default_rng(seed)
+    lt = wl.draw_train_logprobs(N, seed)
+    lr = (lt + rng.normal(0, spread, N) * (rng.random(N) < 0.9)).astype(np.float32)   # 10% exact ties at 0
+    mask = (rng.random(N) < 0.75).astype(np.uint8)
+    if N > 8:
+        lt[3] = np.nan
+        lr[5] = np.inf
+        mask[[3, 5]] = 1
+    return lt, lr, mask
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 31, 1000, 4099, 100003, 1 << 20])
+def test_ragged_sizes(N):
+    """Sizes that are not multiples of the 4-token groups, below one warp,
+    and across many CTAs; a tenth of the tokens tie at delta = 0."""
+    lt, lr, mask = _batch(N, N)
+    tau = float(np.float32(0.08))
+    g, rej = gpu_monitor(lt, lr, mask, tau)
+    assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, tau), "N=%d" % N)
+
+
+def test_ties_signed_zero_and_empty():
+    N = 5000
+    lt = wl.draw_train_logprobs(N, 3)
+    g, _ = gpu_monitor(lt, lt.copy(), np.ones(N, np.uint8), 0.0)           # every delta = +0
+    assert g[MF["ratio_q01"]] == g[MF["ratio_q99"]] == 1.0 and g[MF["p95_abs_delta"]] == 0.0
+    assert g[MF["n_extreme"]] == 0                                          # |delta| = tau = 0: kept
+    lz = np.zeros(8, np.float32)
+    lz[::2] = -0.0                                                          # -0 - (+0) = -0
+    g2, _ = gpu_monitor(lz, np.zeros(8, np.float32), np.ones(8, np.uint8), 0.1)
+    assert g2[MF["ratio_q50"]] == 1.0
+    g3, rej3 = gpu_monitor(lt, lt, np.zeros(N, np.uint8), 0.1)             # nothing used
+    assert g3[MF["n_used"]] == 0 and np.isnan(g3[MF["ratio_q50"]]) and not rej3.any()
+    e = tim.mismatch_monitor(torch.zeros(0, device="cuda"), torch.zeros(0, device="cuda"),
+                             torch.zeros(0, dtype=torch.uint8, device="cuda"), 0.1)
+    tim.check()
+    assert e["batch"][MF["n_used"]].item() == 0
+
+
+def test_heavy_tail_and_thresholds():
+    """Outliers of +-1 nat on 0.5% of tokens (the Llama-shaped rollout): the
+    p99 / p01 ratios sit in the tail; several thresholds."""
+    cfg = wl.CONFIGS["llama3_8b"]
+    lt = wl.draw_train_logprobs(cfg.N, 4)
+    lr = wl.draw_rollout(cfg, lt, seed=4)
+    off = wl.draw_segments(cfg, seed=4)
+    mask = wl.draw_mask(cfg, off, seed=4)
+    for tau in (0.0, 0.01, 0.05, 0.5, 2.0):
+        t = float(np.float32(tau))
+        g, rej = gpu_monitor(lt, lr, mask, t)
+        assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, t), "tau=%g" % tau)
+
+
+def test_repeat_runs_are_bitwise_identical():
+    lt, lr, mask = _batch(1 << 20, 7)
+    a = tim.mismatch_monitor(_dev(lt), _dev(lr), _dev(mask), 0.1)
+    b = tim.mismatch_monitor(_dev(lt), _dev(lr), _dev(mask), 0.1)
+    tim.check()
+    assert torch.equal(a["batch"], b["batch"]) and torch.equal(a["token_reject"], b["token_reject"])
+
+
+def test_full_size_batch():
+    """2^27 tokens with the benchmark's recipe (30% masked, delta ~ N(0, 0.02^2)
+    on -Gamma(0.6, 3) logprobs), in the launch configuration it times."""
+    N = 1 << 27
+    off, mask, _, lo, lr, _ = wl.draw_ppo_inputs(N, 6)
+    tau = float(np.float32(0.05))
+    g, rej = gpu_monitor(lo, lr, mask, tau)
+    assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^27")
