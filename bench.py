@@ -296,6 +296,13 @@ def run_gb300(args):
     tim.load()
     peaks = load_peaks()
 
+    if args.only == "monitor":
+        r = monitor_bandwidth(tim, dev, stream_of(dev), peaks, tokens=args.tokens or K2_BW_TOKENS,
+                              reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
     if args.only == "ppo":
         r = ppo_bandwidth(tim, dev, stream_of(dev), peaks, tokens=args.tokens or K2_BW_TOKENS,
                           reps=args.steps, warmup=args.warmup)
@@ -426,6 +433,7 @@ def run_gb300(args):
 
     k2_bw = mismatch_bandwidth(tim, dev, stream, peaks) if not args.skip_k2_bandwidth else None
     ppo_bw = ppo_bandwidth(tim, dev, stream, peaks) if not args.skip_ppo else None
+    mon_bw = monitor_bandwidth(tim, dev, stream, peaks) if not args.skip_monitor else None
     sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
     tim.check()
 
@@ -464,6 +472,8 @@ def run_gb300(args):
         line["mismatch_bandwidth"] = k2_bw
     if ppo_bw is not None:
         line["tis_ppo"] = ppo_bw
+    if mon_bw is not None:
+        line["mismatch_monitor"] = mon_bw
     if sweep is not None:
         line["sweep"] = sweep
     print(json.dumps(line), flush=True)
@@ -543,6 +553,42 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
             "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
 
 
+def monitor_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
+    """tim_mismatch_monitor alone on `tokens` tokens (2^27 by default), inputs
+    drawn on the device like the mismatch pass's (30% masked, delta ~
+    N(0, 0.02^2)), rejection flags written; L2 flushed before each call.
+    Algorithmic bytes: one read of the inputs and the flags written (10 B per
+    token); the design reads the inputs three times (radix passes)."""
+    import torch
+    Nt = tokens
+    g = torch.Generator(device=dev)
+    g.manual_seed(8)
+    l_tr = torch.log(torch.rand(Nt, device=dev, generator=g).clamp_min_(1e-30))
+    l_ro = l_tr + 0.02 * torch.randn(Nt, device=dev, generator=g)
+    mask = (torch.rand(Nt, device=dev, generator=g) >= 0.3).to(torch.uint8)
+    out = {"batch": torch.empty(7, dtype=torch.float64, device=dev),
+           "token_reject": torch.empty(Nt, dtype=torch.uint8, device=dev)}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    call = lambda: tim.mismatch_monitor(l_tr, l_ro, mask, 0.05, out=out)  # noqa: E731
+    for _ in range(warmup):
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        flush.fill_(i)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
+    algo = 10 * Nt + 56
+    gbs = algo / t / 1e9
+    return {"tokens": Nt, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo, "achieved": gbs,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
+            "passes_over_inputs": 3, "design_bytes": 28 * Nt, "design_gbs": 28 * Nt / t / 1e9,
+            "tokens_per_s": Nt / t, "traffic": None}
+
+
 def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
     """tim_tis_ppo alone on `tokens` tokens (2^27 by default): the segments of
     workloads.draw_ppo_inputs (lognormal lengths, median 1024, clipped to
@@ -603,7 +649,8 @@ def main(argv=None):
     ap.add_argument("--skip-k2-bandwidth", action="store_true")
     ap.add_argument("--skip-sweep", action="store_true")
     ap.add_argument("--skip-ppo", action="store_true")
-    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo"], default=None,
+    ap.add_argument("--skip-monitor", action="store_true")
+    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo", "monitor"], default=None,
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller batch of the same head (profiling runs only)")

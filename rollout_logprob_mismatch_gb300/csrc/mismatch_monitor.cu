@@ -13,8 +13,9 @@
 // selection on 32-bit keys that order like the values (|delta|: its bits;
 // delta: sign-flipped bits), in three passes over the tokens of 11, 11 and 10
 // key bits:
-//   mon_pass_kernel<1>   histograms of the top 11 bits of both keys, n_used,
-//                        n_extreme and the rejection flags;
+//   mon_pass_kernel<1>   histogram of the top 11 bits of delta's key (that of
+//                        |delta| follows from it), n_used, n_extreme and the
+//                        rejection flags;
 //   mon_select_kernel<1> ranks from n_used; per target, the bin that holds
 //                        its rank and the rank left inside that bin;
 //   mon_pass_kernel<2>   per target, histogram of bits 20..10 of the keys in
@@ -23,9 +24,8 @@
 //                        keys and writes the record.
 // Counts are integers, so the result does not depend on the order in which
 // threads add them: the selected tokens are exactly the oracle's.  Each pass
-// reads 9 bytes per token; a CTA counts into shared-memory histograms (lanes
-// of a warp that hit the same bin add once, through match.any) and adds the
-// non-zero bins to the global ones at the end.
+// reads 9 bytes per token; a CTA counts into shared-memory histograms and adds
+// the non-zero bins to the global ones at the end.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
@@ -58,21 +58,20 @@ __device__ __forceinline__ float unkey_signed(uint32_t k)
     return __uint_as_float(k ^ ((k >> 31) ? 0x80000000u : 0xffffffffu));
 }
 
-// One count per valid lane into h[bin]; lanes of the warp with the same bin
-// add together.  Called by all 32 lanes.
+// One count per valid lane into h[bin].  (Adding the lanes of a warp that
+// share a bin first, through match.any, was measured slower: 1844 against
+// 1257 us per call at 2^27 tokens.)
 __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool valid)
 {
-    const uint32_t tag = valid ? bin : 0xffffffffu;
-    const unsigned peers = __match_any_sync(0xffffffffu, tag);
-    if (valid && static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1)
-        atomicAdd(h + bin, static_cast<uint32_t>(__popc(peers)));
+    if (valid)
+        atomicAdd(h + bin, 1u);
 }
 
 template <int PASS>
 struct PassShape;
 template <>
 struct PassShape<1> {
-    static constexpr int NH = 2, NB = MON_BINS1, SHIFT = 21, KEEP = 32;   // KEEP: prefix bits compared
+    static constexpr int NH = 1, NB = MON_BINS1, SHIFT = 21, KEEP = 32;   // KEEP: prefix bits compared
 };
 template <>
 struct PassShape<2> {
@@ -88,15 +87,15 @@ constexpr int pass_smem_bytes() { return PassShape<PASS>::NH * PassShape<PASS>::
 
 // One token of pass PASS (all lanes call it; `valid` false past the end).
 template <int PASS>
-__device__ __forceinline__ void pass_token(uint32_t *sh, const uint32_t *pref, float d, bool m, bool valid,
+__device__ __forceinline__ void pass_token(uint32_t *sh, const uint32_t (&pref)[MON_TARGETS], float d, bool m,
+                                           bool valid,
                                            float tau, int &n_used, int &n_ext)
 {
     using P = PassShape<PASS>;
     const bool used = valid && m && fabsf(d) <= FLT_MAX;
     const uint32_t ka = key_abs(d), kd = key_signed(d);
-    if (PASS == 1) {
-        hist_add(sh, ka >> P::SHIFT, used);
-        hist_add(sh + P::NB, kd >> P::SHIFT, used);
+    if (PASS == 1) {   // the |delta| histogram follows from delta's (see mon_select_kernel<1>)
+        hist_add(sh, kd >> P::SHIFT, used);
         n_used += static_cast<int>(used);
         n_ext += static_cast<int>(used && fabsf(d) > tau);
     } else {
@@ -129,6 +128,10 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
     __syncthreads();
     if (PASS > 1 && empty_s)   // uniform over the CTA
         return;
+    uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
+#pragma unroll
+    for (int j = 0; j < MON_TARGETS; ++j)
+        pr[j] = pref[j];
     const int64_t N = a.N;
     const int64_t G = (N + 3) >> 2;   // 4-token groups; groups below `full` have 4 tokens
     const int64_t full = N >> 2;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
                 const bool valid = g < G && 4 * g + i < N;
                 const bool m = ((mk[u] >> (8 * i)) & 0xffu) != 0u;
                 const int before = n_ext;
-                pass_token<PASS>(mon_sh, pref, d[i], m, valid, a.tau_tok, n_used, n_ext);
+                pass_token<PASS>(mon_sh, pr, d[i], m, valid, a.tau_tok, n_used, n_ext);
                 flags |= static_cast<uint32_t>(n_ext != before) << (8 * i);
             }
             if (PASS == 1 && a.reject) {
@@ -225,14 +228,19 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
         __syncthreads();
     }
     if (!st->empty) {
-        const uint32_t *h = PASS == 1 ? a.hist1 + (j < 2 ? 0 : P::NB)
-                          : PASS == 2 ? a.hist2 + j * P::NB
-                                      : a.hist3 + j * P::NB;
+        // Pass 1 counted delta's key only.  |delta| has a clear top bit, and
+        // its bin b holds the positive deltas of delta-bin 1024 + b and the
+        // negative ones of delta-bin 1023 - b (the sign-flipped key).
+        const bool abs1 = PASS == 1 && j < 2;
+        const uint32_t *h = PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 + j * P::NB : a.hist3 + j * P::NB;
+        auto count = [&](int b) -> long long {
+            return abs1 ? static_cast<long long>(h[1024 + b]) + h[1023 - b] : static_cast<long long>(h[b]);
+        };
         const long long r = st->rank[j];
-        constexpr int SEG = P::NB / 32;   // bins per lane
+        const int SEG = (abs1 ? 1024 : P::NB) / 32;   // bins per lane
         long long c = 0;
         for (int b = 0; b < SEG; ++b)
-            c += h[lane * SEG + b];
+            c += count(lane * SEG + b);
         long long incl = c;   // inclusive prefix over lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
             if (lane == L) {
                 long long cum = incl - c;
                 for (int b = 0; b < SEG; ++b) {
-                    const long long hb = h[lane * SEG + b];
+                    const long long hb = count(lane * SEG + b);
                     if (cum + hb > r) {
                         bin = lane * SEG + b;
                         before = cum;

@@ -29,7 +29,7 @@ struct MonState {
 // Workspace: state, then the histograms of the three passes (32-bit counts).
 constexpr size_t MON_STATE_BYTES = 512;
 static_assert(sizeof(MonState) <= MON_STATE_BYTES, "state block");
-constexpr size_t MON_HIST1_WORDS = 2 * MON_BINS1;             // one per key kind
+constexpr size_t MON_HIST1_WORDS = MON_BINS1;                 // delta's key only
 constexpr size_t MON_HIST2_WORDS = MON_TARGETS * MON_BINS2;   // one per target
 constexpr size_t MON_HIST3_WORDS = MON_TARGETS * MON_BINS3;
 constexpr size_t MON_WORKSPACE_BYTES = MON_STATE_BYTES + 4 * (MON_HIST1_WORDS + MON_HIST2_WORDS + MON_HIST3_WORDS);
