@@ -8,6 +8,8 @@ input generators of ``workloads``.
 ``token_logprob``  -- the selected-token logprob by the definition (icarus
 "RL: Training Inference Mismatch", section "log p"): z = h W^T in fp64,
 lse = log sum exp z, logp = z[a] - lse.
+``token_logprob_f32w`` -- the same with fp32 weights (the FP32 LM head of
+LoongSage "Train-Inference Consistency" section 3).
 ``tis_ppo``        -- the TIS-weighted PPO clipped surrogate, its gradient and
 masked means (VeXact summary eq. (2)-(3); HN "Clipped importance ratios").
 ``mismatch_monitor`` -- p95 |delta|, ratio quantiles 0.01 / 0.5 / 0.99, extreme
@@ -68,6 +70,8 @@ def _load():
             lib.oracle_token_logprob.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64,
                                                  ctypes.c_int64, ctypes.c_double, P, P, ctypes.c_int]
             lib.oracle_token_logprob.restype = ctypes.c_int
+            lib.oracle_token_logprob_f32w.argtypes = lib.oracle_token_logprob.argtypes
+            lib.oracle_token_logprob_f32w.restype = ctypes.c_int
             lib.oracle_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int64,
                                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32,
                                                   P, P, P, P]
@@ -117,6 +121,31 @@ def token_logprob(h_bf16: np.ndarray, W_bf16: np.ndarray, targets: np.ndarray,
                                   D, V, float(temperature), _ptr(logp), _ptr(lse), nt)
     if rc != 0:
         raise RuntimeError("oracle_token_logprob failed")
+    return logp, lse
+
+
+def token_logprob_f32w(h_bf16: np.ndarray, W_f32: np.ndarray, targets: np.ndarray,
+                       rows=None, nthreads: int | None = None, temperature: float = 1.0):
+    """token_logprob with fp32 weights W [V, D] (the FP32 LM head of LoongSage
+    "Train-Inference Consistency" section 3): (logp, lse) float64."""
+    lib = _load()
+    h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
+    W = np.ascontiguousarray(W_f32, dtype=np.float32)
+    a = np.ascontiguousarray(targets, dtype=np.int32)
+    N, D = h.shape
+    V, D2 = W.shape
+    assert D == D2 and a.shape == (N,)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    R = N if r is None else r.size
+    if r is not None:
+        assert r.ndim == 1 and (r.size == 0 or (r.min() >= 0 and r.max() < N))
+    logp = np.empty(R, dtype=np.float64)
+    lse = np.empty(R, dtype=np.float64)
+    nt = nthreads or max(1, len(os.sched_getaffinity(0)))
+    rc = lib.oracle_token_logprob_f32w(_ptr(h), _ptr(W), _ptr(a), None if r is None else _ptr(r), R,
+                                       D, V, float(temperature), _ptr(logp), _ptr(lse), nt)
+    if rc != 0:
+        raise RuntimeError("oracle_token_logprob_f32w failed")
     return logp, lse
 
 

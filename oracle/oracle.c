@@ -63,18 +63,26 @@ static double bf16_value(uint16_t b)
 /* One row of the definition: z_v = (sum_d h_d W[v, d]) / temperature
  * (d ascending; the sampling distribution softmax(z / tau) of the icarus
  * "logits processor" section, tau = 1 for raw logits), m = max_v z_v,
- * S = sum_v exp(z_v - m) (v ascending), lse = m + log S, logp = z_a - lse. */
-static void oracle_row(const uint16_t *h_row, const uint16_t *W, int32_t a,
+ * S = sum_v exp(z_v - m) (v ascending), lse = m + log S, logp = z_a - lse.
+ * W is bf16 (W) or, for the FP32 LM head of LoongSage "Train-Inference
+ * Consistency" section 3, fp32 (Wf, used when not NULL). */
+static void oracle_row(const uint16_t *h_row, const uint16_t *W, const float *Wf, int32_t a,
                        int64_t D, int64_t V, double temperature, double *hd, double *z,
                        double *out_logp, double *out_lse)
 {
     for (int64_t d = 0; d < D; ++d)
         hd[d] = bf16_value(h_row[d]);
     for (int64_t v = 0; v < V; ++v) {
-        const uint16_t *w = W + v * D;
         double acc = 0.0;
-        for (int64_t d = 0; d < D; ++d)
-            acc += hd[d] * bf16_value(w[d]);
+        if (Wf) {
+            const float *w = Wf + v * D;
+            for (int64_t d = 0; d < D; ++d)
+                acc += hd[d] * (double)w[d];
+        } else {
+            const uint16_t *w = W + v * D;
+            for (int64_t d = 0; d < D; ++d)
+                acc += hd[d] * bf16_value(w[d]);
+        }
         z[v] = acc / temperature;
     }
     double m = -INFINITY;
@@ -91,6 +99,7 @@ static void oracle_row(const uint16_t *h_row, const uint16_t *W, int32_t a,
 
 typedef struct {
     const uint16_t *h, *W;
+    const float *Wf;
     const int32_t *targets;
     const int64_t *rows;
     int64_t R, D, V;
@@ -112,7 +121,7 @@ static void *row_worker(void *p)
     }
     for (int64_t i = j->tid; i < j->R; i += j->nthreads) {
         int64_t t = j->rows ? j->rows[i] : i;
-        oracle_row(j->h + t * j->D, j->W, j->targets[t], j->D, j->V, j->temperature, hd, z,
+        oracle_row(j->h + t * j->D, j->W, j->Wf, j->targets[t], j->D, j->V, j->temperature, hd, z,
                    j->out_logp + i, j->out_lse + i);
     }
     free(hd);
@@ -125,11 +134,11 @@ static void *row_worker(void *p)
  * logits); outputs double [R].
  * Rows are spread over `nthreads` threads; each row is computed alone.
  * Returns 0, or -1 on bad arguments / allocation failure. */
-int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *targets,
-                         const int64_t *rows, int64_t R, int64_t D, int64_t V, double temperature,
-                         double *out_logp, double *out_lse, int nthreads)
+static int token_logprob_rows(const uint16_t *h, const uint16_t *W, const float *Wf, const int32_t *targets,
+                              const int64_t *rows, int64_t R, int64_t D, int64_t V, double temperature,
+                              double *out_logp, double *out_lse, int nthreads)
 {
-    if (R < 0 || D <= 0 || V <= 0 || !h || !W || !targets || !out_logp || !out_lse)
+    if (R < 0 || D <= 0 || V <= 0 || !h || (!W && !Wf) || !targets || !out_logp || !out_lse)
         return -1;
     if (!(temperature > 0.0) || !isfinite(temperature))
         return -1;
@@ -148,7 +157,7 @@ int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *ta
     }
     int rc = 0;
     for (int k = 0; k < nthreads; ++k) {
-        jobs[k] = (row_job){h, W, targets, rows, R, D, V, temperature, out_logp, out_lse, k, nthreads, 0};
+        jobs[k] = (row_job){h, W, Wf, targets, rows, R, D, V, temperature, out_logp, out_lse, k, nthreads, 0};
         if (pthread_create(&th[k], NULL, row_worker, &jobs[k]) != 0) {
             row_worker(&jobs[k]); /* run inline if no thread could be made */
             th[k] = 0;
@@ -163,6 +172,26 @@ int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *ta
     free(jobs);
     free(th);
     return rc;
+}
+
+int oracle_token_logprob(const uint16_t *h, const uint16_t *W, const int32_t *targets,
+                         const int64_t *rows, int64_t R, int64_t D, int64_t V, double temperature,
+                         double *out_logp, double *out_lse, int nthreads)
+{
+    if (!W)
+        return -1;
+    return token_logprob_rows(h, W, NULL, targets, rows, R, D, V, temperature, out_logp, out_lse, nthreads);
+}
+
+/* The same with fp32 weights W [V, D] (FP32 LM head): every product of a bf16
+ * hidden value and an fp32 weight is taken exactly in fp64. */
+int oracle_token_logprob_f32w(const uint16_t *h, const float *W, const int32_t *targets,
+                              const int64_t *rows, int64_t R, int64_t D, int64_t V, double temperature,
+                              double *out_logp, double *out_lse, int nthreads)
+{
+    if (!W)
+        return -1;
+    return token_logprob_rows(h, NULL, W, targets, rows, R, D, V, temperature, out_logp, out_lse, nthreads);
 }
 
 /* ------------------------------------------------------------------ mismatch stats */

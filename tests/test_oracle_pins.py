@@ -581,3 +581,43 @@ def test_monitor_is_order_free():
     a = oracle.mismatch_monitor(lt, lr, m, 0.15)
     b = oracle.mismatch_monitor(lt[p], lr[p], m[p], 0.15)
     assert np.array_equal(a["batch"], b["batch"]) and np.array_equal(a["reject"][p], b["reject"])
+
+
+# --------------------------------------------------------------- FP32 LM head
+def test_f32_weights_holding_bf16_values_match_the_bf16_oracle():
+    """fp32 weights that are exactly bf16 values give the bf16 oracle's bits
+    (both sides take the same exact products)."""
+    h, W, a = _rand_head(11, 40, 300, 60, w_std=0.2)
+    l1, s1 = oracle.token_logprob(h, W, a)
+    l2, s2 = oracle.token_logprob_f32w(h, bf16_to_f32(W), a)
+    assert np.array_equal(l1, l2) and np.array_equal(s1, s2)
+
+
+def test_f32_weights_against_torch_float64():
+    """fp32 weights that are not bf16 values: torch float64 log_softmax of
+    h W^T / tau (another route to the same definition), tau 1 and 0.8."""
+    import torch
+    rng = np.random.default_rng(61)
+    N, D, V = 7, 48, 500
+    h = bf16_round(rng.standard_normal((N, D), dtype=np.float32))
+    W = (rng.standard_normal((V, D)) * 0.1).astype(np.float32)
+    a = rng.integers(0, V, N).astype(np.int32)
+    for tau in (1.0, 0.8):
+        lp, lse = oracle.token_logprob_f32w(h, W, a, temperature=tau)
+        z = torch.from_numpy(bf16_to_f32(h).astype(np.float64)) @ torch.from_numpy(W.astype(np.float64)).T / tau
+        ref = torch.log_softmax(z, dim=-1).gather(1, torch.from_numpy(a.astype(np.int64))[:, None])[:, 0]
+        np.testing.assert_allclose(lp, ref.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, torch.logsumexp(z, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_f32_weights_differ_from_their_bf16_rounding():
+    """The fp32 head is not the bf16 head in disguise: rounding W to bf16
+    moves the logprobs by ~1e-3 (the error the FP32 head removes)."""
+    rng = np.random.default_rng(62)
+    N, D, V = 6, 512, 800
+    h = bf16_round(rng.standard_normal((N, D), dtype=np.float32))
+    W = (rng.standard_normal((V, D)) * 0.05).astype(np.float32)
+    a = rng.integers(0, V, N).astype(np.int32)
+    lf, _ = oracle.token_logprob_f32w(h, W, a)
+    lb, _ = oracle.token_logprob(h, bf16_round(W), a)
+    assert 1e-5 < np.max(np.abs(lf - lb)) < 1e-1
