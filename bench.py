@@ -342,6 +342,13 @@ def run_gb300(args):
         tim.token_logprob(hd, Wd, ad, lp, lse)
         tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
 
+    if args.only == "fp32head":
+        r = fp32_head_measure(tim, dev, stream, peaks, hd, ad, V, reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
+
     if args.only:
         # one kernel family alone (profiling runs): warm-up, then timed launches
         fn = (lambda: tim.token_logprob(hd, Wd, ad, lp, lse)) if args.only == "k1" else \
@@ -435,6 +442,7 @@ def run_gb300(args):
     ppo_bw = ppo_bandwidth(tim, dev, stream, peaks) if not args.skip_ppo else None
     mon_bw = monitor_bandwidth(tim, dev, stream, peaks) if not args.skip_monitor else None
     sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
+    fp32h = fp32_head_measure(tim, dev, stream, peaks, hd, ad, V) if not args.skip_fp32_head else None
     tim.check()
 
     if rank != 0:
@@ -474,6 +482,8 @@ def run_gb300(args):
         line["tis_ppo"] = ppo_bw
     if mon_bw is not None:
         line["mismatch_monitor"] = mon_bw
+    if fp32h is not None:
+        line["fp32_head"] = fp32h
     if sweep is not None:
         line["sweep"] = sweep
     print(json.dumps(line), flush=True)
@@ -551,6 +561,48 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
             "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
             "frac_of_8000": gbs / 8000.0, "bound": "hbm",
             "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
+
+
+def fp32_head_measure(tim, dev, stream, peaks, hd, ad, V, reps=5, warmup=3):
+    """The FP32 LM head on the bench's head shape: fp32 W ~ N(0, 0.02^2) drawn
+    on the device, split into three bf16 parts (timed: HBM-bound, 4 B read +
+    6 B written per weight), then the fused token logprob over the parts
+    (timed; L2 flushed before each call).  TFLOP/s are given both as the fp32
+    head's 2NVD and as the 3 x 2NVD bf16 tensor work against the bf16 peak."""
+    import torch
+    N, D = hd.shape
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    Wf = torch.randn((V, D), generator=g, device=dev) * 0.02
+    Ws = tim.split_weight_fp32(Wf)
+    lp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        tim.token_logprob_fp32_head(hd, Ws, ad, lp, lse)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        flush.fill_(i)
+        ev[i][0].record(stream)
+        tim.split_weight_fp32(Wf, out=Ws)
+        ev[i][1].record(stream)
+        flush.fill_(i + 1)
+        ev[i][2].record(stream)
+        tim.token_logprob_fp32_head(hd, Ws, ad, lp, lse)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize(dev)
+    t_split = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
+    t_head = float(np.mean([ev[i][2].elapsed_time(ev[i][3]) * 1e-3 for i in range(reps)]))
+    flops = 2.0 * N * V * D
+    split_bytes = 4 * V * D + Ws.numel() * 2
+    del Wf, Ws
+    return {"N": N, "D": D, "V": V, "avg_launch_ms": t_head * 1e3, "tokens_per_s": N / t_head,
+            "fp32_head_tflops": flops / t_head / 1e12, "tensor_tflops": 3 * flops / t_head / 1e12,
+            "bound": "tensor", "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": 3 * flops / t_head / 1e12 / peaks["bf16_tflops"],
+            "split": {"avg_us": t_split * 1e6, "bytes": split_bytes, "gbs": split_bytes / t_split / 1e9,
+                      "frac_of_hbm": split_bytes / t_split / 1e9 / peaks["hbm_gbs"]}}
 
 
 def monitor_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
@@ -650,7 +702,8 @@ def main(argv=None):
     ap.add_argument("--skip-sweep", action="store_true")
     ap.add_argument("--skip-ppo", action="store_true")
     ap.add_argument("--skip-monitor", action="store_true")
-    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo", "monitor"], default=None,
+    ap.add_argument("--skip-fp32-head", action="store_true")
+    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo", "monitor", "fp32head"], default=None,
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller batch of the same head (profiling runs only)")

@@ -105,6 +105,34 @@ TIM_API int tim_token_logprob_temperature(const void *h, const void *W, const in
                                           int64_t N, int64_t D, int64_t V, float temperature,
                                           float *out_logp, float *out_lse, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ FP32 LM head
+ *
+ * LoongSage "Train-Inference Consistency" section 3: the LM head's weights and
+ * arithmetic stay in fp32, so that rounding to bf16 does not reach the
+ * log-probabilities.  The hidden states stay bf16 (the model's activations;
+ * exact in fp32).  The weights are first cut, once per weight update, into
+ * three bf16 parts whose sum is each fp32 weight exactly; the fused kernel then
+ * runs over the parts (three times the tensor work of the bf16 head) with fp32
+ * accumulation: bf16 x bf16 products are exact in fp32.
+ *
+ * tim_split_weight_bytes(V, D): bytes of the split, V * 3 * Dp * 2 with Dp = D
+ * rounded up to a multiple of 64; -1 for sizes out of range.
+ * tim_split_weight_fp32(W, V, D, W_split, stream):
+ *   W        fp32 [V, D] row-major, 16-byte aligned, D % 8 == 0
+ *   W_split  out: caller-owned device buffer of tim_split_weight_bytes(V, D)
+ *            bytes, 16-byte aligned; row v is [part 1 | part 2 | part 3], each
+ *            Dp bf16 columns, zero past D.  Exact for |w| >= 2^-110 (smaller
+ *            weights lose their last bits, below 2^-133); a non-finite weight
+ *            goes whole into part 1.
+ * tim_token_logprob_fp32_head(h, W_split, targets, N, D, V, temperature,
+ *                             out_logp, out_lse, stream):
+ *   as tim_token_logprob_temperature, with the split weights in place of W. */
+TIM_API int64_t tim_split_weight_bytes(int64_t V, int64_t D);
+TIM_API int tim_split_weight_fp32(const float *W, int64_t V, int64_t D, void *W_split, tim_stream_t stream);
+TIM_API int tim_token_logprob_fp32_head(const void *h, const void *W_split, const int32_t *targets, int64_t N,
+                                        int64_t D, int64_t V, float temperature, float *out_logp,
+                                        float *out_lse, tim_stream_t stream);
+
 /* ------------------------------------------------------------------ token logprob, no allocation
  *
  * No counterpart on the pages: a library-side variant of tim_token_logprob for

@@ -28,8 +28,9 @@ import threading
 __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "MONITOR_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
     "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
-    "tim_tis_ppo", "tim_mismatch_monitor", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
-    "token_logprob", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
+    "tim_tis_ppo", "tim_mismatch_monitor", "tim_split_weight_bytes", "tim_split_weight_fp32",
+    "tim_token_logprob_fp32_head", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "token_logprob", "split_weight_fp32", "token_logprob_fp32_head", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -119,6 +120,12 @@ def load():
             F = ctypes.c_float
             lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
             lib.tim_tis_ppo.restype = ctypes.c_int
+            lib.tim_split_weight_bytes.argtypes = [I64, I64]
+            lib.tim_split_weight_bytes.restype = ctypes.c_int64
+            lib.tim_split_weight_fp32.argtypes = [P, I64, I64, P, P]
+            lib.tim_split_weight_fp32.restype = ctypes.c_int
+            lib.tim_token_logprob_fp32_head.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
+            lib.tim_token_logprob_fp32_head.restype = ctypes.c_int
             lib.tim_mismatch_monitor.argtypes = [P, P, P, I64, F, P, P, P]
             lib.tim_mismatch_monitor.restype = ctypes.c_int
             lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
@@ -161,6 +168,19 @@ def tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offset
                 out: tim_ppo_out, stream) -> int:
     return load().tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets,
                               float(eps_low), float(eps_high), float(C), ctypes.byref(out), stream)
+
+
+def tim_split_weight_bytes(V, D) -> int:
+    return load().tim_split_weight_bytes(V, D)
+
+
+def tim_split_weight_fp32(W, V, D, W_split, stream) -> int:
+    return load().tim_split_weight_fp32(W, V, D, W_split, stream)
+
+
+def tim_token_logprob_fp32_head(h, W_split, targets, N, D, V, temperature, out_logp, out_lse, stream) -> int:
+    return load().tim_token_logprob_fp32_head(h, W_split, targets, N, D, V, float(temperature), out_logp,
+                                              out_lse, stream)
 
 
 def tim_mismatch_monitor(logp_train, logp_rollout, mask, N, tau_tok, token_reject, out, stream) -> int:
@@ -241,6 +261,56 @@ def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None, tempe
             rc = tim_token_logprob_temperature(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
                                                temperature, out_logp.data_ptr(), out_lse.data_ptr(),
                                                _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out_logp, out_lse
+
+
+def split_weight_fp32(W, out=None, stream=None):
+    """fp32 W [V, D] -> its three bf16 parts, a bf16 tensor [V, 3 * Dp]
+    (Dp = D rounded up to 64): the operand of token_logprob_fp32_head."""
+    import torch
+    _need(W, "W", torch.float32, 2)
+    dev = W.device
+    V, D = W.shape
+    nbytes = tim_split_weight_bytes(V, D)
+    if nbytes < 0:
+        raise ValueError("W shape %s out of range" % (tuple(W.shape),))
+    cols = nbytes // (2 * V)
+    if out is None:
+        out = torch.empty((V, cols), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, 2, dev)
+    if tuple(out.shape) != (V, cols):
+        raise ValueError("out must be [%d, %d]" % (V, cols))
+    with torch.cuda.device(dev):
+        rc = tim_split_weight_fp32(W.data_ptr(), V, D, out.data_ptr(), _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out
+
+
+def token_logprob_fp32_head(h, W_split, targets, out_logp=None, out_lse=None, stream=None,
+                            temperature: float = 1.0):
+    """(logp, lse) fp32 [N] of log softmax(h W^T / temperature) at the targets
+    with fp32 weights W, given as split_weight_fp32(W); h bf16 [N, D]."""
+    import torch
+    _need(h, "h", torch.bfloat16, 2)
+    dev = h.device
+    _need(W_split, "W_split", torch.bfloat16, 2, dev)
+    _need(targets, "targets", torch.int32, 1, dev)
+    N, D = h.shape
+    V = W_split.shape[0]
+    if tim_split_weight_bytes(V, D) != W_split.numel() * 2 or targets.shape[0] != N:
+        raise ValueError("shape mismatch: h %s, W_split %s, targets %s"
+                         % (tuple(h.shape), tuple(W_split.shape), tuple(targets.shape)))
+    if out_logp is None:
+        out_logp = torch.empty(N, dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(N, dtype=torch.float32, device=dev)
+    _need(out_logp, "out_logp", torch.float32, 1, dev)
+    _need(out_lse, "out_lse", torch.float32, 1, dev)
+    with torch.cuda.device(dev):
+        rc = tim_token_logprob_fp32_head(h.data_ptr(), W_split.data_ptr(), targets.data_ptr(), N, D, V,
+                                         temperature, out_logp.data_ptr(), out_lse.data_ptr(),
+                                         _stream_handle(stream, dev))
     _raise_if(rc)
     return out_logp, out_lse
 

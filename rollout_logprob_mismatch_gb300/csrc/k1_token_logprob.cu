@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     const int cid = blockIdx.x / K1_CLUSTER;
     const int ncl = gridDim.x / K1_CLUSTER;
     constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << K1_CLUSTER) - 1);
-    const int KB = (a.D + K1_BK - 1) / K1_BK;
+    const int KBH = (a.D + K1_BK - 1) / K1_BK;   // k-tiles of h
+    const int KB = KBH * a.w_segments;          // k-tiles of W: 1 or 3 bf16 parts of each weight
     const uint64_t budget = a.wait_budget_ns;
 
     if (warp == 0) {
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
                     const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
+                    int kh = 0;   // kb mod KBH: the h tile meets each part of W in turn
                     for (int kb = 0; kb < KB; ++kb) {
                         // the stage is free once the UMMA of every CTA of the cluster is done with it
                         if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget)) {
@@ -147,8 +149,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         // own h tile + this CTA's rows of the W tile, multicast to the whole
                         // cluster; the barrier counts the W rows the other CTAs send as well
                         mbar_arrive_expect_tx(full(stage), K1_STAGE_BYTES);
-                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kb * K1_BK, mt * K1_BM,
+                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kh * K1_BK, mt * K1_BM,
                                     pol_h);
+                        if (++kh == KBH)
+                            kh = 0;
                         tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / K1_CLUSTER),
                                               &tmap_w, full(stage), kb * K1_BK,
                                               v0 + static_cast<int>(rank) * K1_W_BOX_ROWS, kAllCtas, pol_w);

@@ -187,9 +187,11 @@ const char *tim_last_error(void) { return g_msg; }
 
 namespace {
 
-// The fused token logprob at 1 / temperature `inv_temp` (both entry points).
+// The fused token logprob at 1 / temperature `inv_temp` (every entry point).
+// w_segments 1: W bf16 [V, D]; 3: fp32 weights split into three bf16 parts
+// [V][3][Dp] (tim_split_weight_fp32).
 int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t N, int64_t D, int64_t V,
-                  float inv_temp, float *out_logp, float *out_lse, tim_stream_t stream)
+                  float inv_temp, float *out_logp, float *out_lse, tim_stream_t stream, int w_segments = 1)
 {
     if (N < 0 || N >= (int64_t(1) << 31))
         return fail(TIM_ERR_INVALID_ARG, "N = %lld out of range [0, 2^31)", static_cast<long long>(N));
@@ -220,7 +222,8 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     CUtensorMap th, tw;
     if ((rc = encode_bf16(&th, h, N, D, tim::K1_BM)) != TIM_OK)
         return rc;
-    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK)
+    const int64_t w_cols = w_segments == 1 ? D : 3 * tim::k1_split_cols(D);
+    if ((rc = encode_bf16(&tw, W, V, w_cols, tim::K1_W_BOX_ROWS)) != TIM_OK)
         return rc;
 
     const size_t part_bytes = round_up(static_cast<size_t>(chunks) * N * sizeof(float2), 256);
@@ -240,6 +243,7 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     a.N = static_cast<int32_t>(N);
     a.D = static_cast<int32_t>(D);
     a.V = static_cast<int32_t>(V);
+    a.w_segments = w_segments;
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);
     const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
@@ -355,6 +359,40 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return cuda_fail(ef, "cudaFreeAsync(mismatch workspace)");
     g_msg[0] = 0;
     return TIM_OK;
+}
+
+int64_t tim_split_weight_bytes(int64_t V, int64_t D)
+{
+    if (V <= 0 || D <= 0 || V >= (int64_t(1) << 31) || D > 65536)
+        return -1;
+    return V * 3 * tim::k1_split_cols(D) * 2;
+}
+
+int tim_split_weight_fp32(const float *W, int64_t V, int64_t D, void *W_split, tim_stream_t stream)
+{
+    if (V <= 0 || V >= (int64_t(1) << 31) || D <= 0 || D % 8 != 0 || D > 65536)
+        return fail(TIM_ERR_INVALID_ARG, "V must be in (0, 2^31), D positive, a multiple of 8 and <= 65536");
+    if (!W || !W_split)
+        return fail(TIM_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(W, 16) || !aligned(W_split, 16))
+        return fail(TIM_ERR_INVALID_ARG, "W and W_split must be 16-byte aligned");
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    const cudaError_t e = tim::k1_launch_split(W, V, D, W_split, dev->sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "split_weight_fp32 launch");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_token_logprob_fp32_head(const void *h, const void *W_split, const int32_t *targets, int64_t N, int64_t D,
+                                int64_t V, float temperature, float *out_logp, float *out_lse, tim_stream_t stream)
+{
+    if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature))
+        return fail(TIM_ERR_INVALID_ARG, "temperature must be positive and finite");
+    return token_logprob(h, W_split, targets, N, D, V, 1.f / temperature, out_logp, out_lse, stream, 3);
 }
 
 int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask, int64_t N,

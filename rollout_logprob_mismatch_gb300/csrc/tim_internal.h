@@ -40,6 +40,7 @@ struct K1Args {
     int *status;              // device status word
     float inv_temp;           // 1 / temperature (1 for raw logits)
     int32_t N, D, V;
+    int32_t w_segments;       // 1: W bf16 [V, D]; 3: fp32 W split into three bf16 parts, [V][3][Dp]
     int32_t num_m_tiles, num_chunks;
     int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
     int32_t band, units;      // units = num_m_groups * num_chunks, one per cluster
@@ -54,6 +55,11 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream);
 cudaError_t k1_prepare_device();   // per-device function attributes
+
+// FP32 LM head: W fp32 [V, D] -> three bf16 parts [V][3][Dp], Dp = D rounded up
+// to K1_BK, padding zero; w = part0 + part1 + part2 exactly.
+inline int64_t k1_split_cols(int64_t D) { return (D + K1_BK - 1) / K1_BK * K1_BK; }
+cudaError_t k1_launch_split(const float *W, int64_t V, int64_t D, void *W_split, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- mismatch stats (K2)
 constexpr int K2_WARPS = 8;                        // warps per CTA (three CTAs per SM)

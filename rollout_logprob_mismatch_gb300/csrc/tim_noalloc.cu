@@ -175,6 +175,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.inv_temp = 1.f;
     a.N = static_cast<int32_t>(N);
     a.D = static_cast<int32_t>(D);
+    a.w_segments = 1;
     a.V = static_cast<int32_t>(V);
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);

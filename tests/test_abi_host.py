@@ -173,6 +173,22 @@ def test_mismatch_monitor_rejects_bad_arguments(lib):
     assert len(tim.MONITOR_FIELDS) == 7
 
 
+def test_fp32_head_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_split_weight_bytes(10, 100) == 10 * 3 * 128 * 2
+    assert tim.tim_split_weight_bytes(10, 64) == 10 * 3 * 64 * 2
+    assert tim.tim_split_weight_bytes(0, 64) == -1 and tim.tim_split_weight_bytes(10, 65537) == -1
+    assert tim.tim_split_weight_fp32(16, 0, 64, 16, None) == E
+    assert tim.tim_split_weight_fp32(16, 10, 12, 16, None) == E
+    assert tim.tim_split_weight_fp32(None, 10, 64, 16, None) == E
+    assert tim.tim_split_weight_fp32(16, 10, 64, 8, None) == E
+    assert tim.tim_split_weight_fp32(20, 10, 64, 16, None) == E
+    for tau in (0.0, -1.0, math.inf, math.nan):
+        assert tim.tim_token_logprob_fp32_head(16, 16, 16, 4, 64, 10, tau, 16, 16, None) == E
+    assert tim.tim_token_logprob_fp32_head(16, 16, 16, 4, 12, 10, 1.0, 16, 16, None) == E
+    assert tim.tim_token_logprob_fp32_head(16, 8, 16, 4, 64, 10, 1.0, 16, 16, None) == E
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(tim, "_lib", None)

@@ -253,3 +253,15 @@ def draw_ppo_inputs(N: int, seed: int, update_std: float = 0.1):
     l_th = draw_policy_update(l_old, update_std, seed)
     adv = draw_advantages(off, seed)
     return off, mask, l_th, l_old, l_ro, adv
+
+
+def draw_weight_f32(cfg: HeadConfig, seed: int | None = None, chunk: int = 1 << 24) -> np.ndarray:
+    """fp32 W [V, D] ~ N(0, w_std^2), not rounded to bf16: the weights of an
+    FP32 LM head (own stream, so the bf16 W of the same config is unchanged)."""
+    seed = cfg.seed if seed is None else seed
+    rng = np.random.default_rng([seed, 10])
+    W = np.empty(cfg.V * cfg.D, dtype=np.float32)
+    for s in range(0, W.size, chunk):
+        n = min(chunk, W.size - s)
+        W[s:s + n] = rng.standard_normal(n, dtype=np.float32) * np.float32(cfg.w_std)
+    return W.reshape(cfg.V, cfg.D)
