@@ -48,10 +48,10 @@ K2_BW_TOKENS = 1 << 27
 # only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
 # profiles/k2_seq_kernel_2e25_tokens.md).
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3050926592 read + 18969088 written
-    ("k1", "006ea2b16082c21a"): 3050926592 + 18969088,
-    # mismatch pass, 2^25 tokens: 305292544 read + 97732352 written (traffic scales with tokens)
-    ("k2", "4f3f821e3a24f689"): 305292544 + 97732352,
+    # token logprob, N = 8192, D = 4096, V = 151936: 3108941568 read + 18808064 written
+    ("k1", "8bd6dd5c4abb13b7"): 3108941568 + 18808064,
+    # mismatch pass, 2^25 tokens: 305358080 read + 98499584 written (traffic scales with tokens)
+    ("k2", "1ede8711c418a02e"): 305358080 + 98499584,
     # TIS-weighted PPO surrogate, 2^25 tokens: 612692224 read + 216128768 written (scales with tokens)
     ("ppo", "e67331ce7a3218ab"): 612692224 + 216128768,
 }
