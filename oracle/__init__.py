@@ -8,6 +8,8 @@ input generators of ``workloads``.
 ``token_logprob``  -- the selected-token logprob by the definition (icarus
 "RL: Training Inference Mismatch", section "log p"): z = h W^T in fp64,
 lse = log sum exp z, logp = z[a] - lse.
+``token_logprob_backward`` -- dh, dW (and dz) of sum_t g_t l_t (Thinking
+Machines page, "Unclipped importance sampling": gradients of log q_t).
 ``token_logprob_f32w`` -- the same with fp32 weights (the FP32 LM head of
 LoongSage "Train-Inference Consistency" section 3).
 ``tis_ppo``        -- the TIS-weighted PPO clipped surrogate, its gradient and
@@ -72,6 +74,9 @@ def _load():
             lib.oracle_token_logprob.restype = ctypes.c_int
             lib.oracle_token_logprob_f32w.argtypes = lib.oracle_token_logprob.argtypes
             lib.oracle_token_logprob_f32w.restype = ctypes.c_int
+            lib.oracle_token_logprob_backward.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64,
+                                                          ctypes.c_int64, ctypes.c_double, P, P, P]
+            lib.oracle_token_logprob_backward.restype = ctypes.c_int
             lib.oracle_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int64,
                                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32,
                                                   P, P, P, P]
@@ -147,6 +152,31 @@ def token_logprob_f32w(h_bf16: np.ndarray, W_f32: np.ndarray, targets: np.ndarra
     if rc != 0:
         raise RuntimeError("oracle_token_logprob_f32w failed")
     return logp, lse
+
+
+def token_logprob_backward(h_bf16, W_bf16, targets, grad, temperature: float = 1.0, want_dz: bool = False):
+    """Gradients of sum_t grad_t l_t with respect to h and W (l_t the token
+    logprob at `temperature`): dict with dh [N, D], dW [V, D] (and dz [N, V]
+    when want_dz), float64.  Cost N V D: small shapes only."""
+    lib = _load()
+    h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    a = np.ascontiguousarray(targets, dtype=np.int32)
+    g = np.ascontiguousarray(grad, dtype=np.float32)
+    N, D = h.shape
+    V, D2 = W.shape
+    assert D == D2 and a.shape == (N,) and g.shape == (N,)
+    dh = np.empty((N, D), dtype=np.float64)
+    dW = np.empty((V, D), dtype=np.float64)
+    dz = np.empty((N, V), dtype=np.float64) if want_dz else None
+    rc = lib.oracle_token_logprob_backward(_ptr(h), _ptr(W), _ptr(a), _ptr(g), N, D, V, float(temperature),
+                                           _ptr(dh), _ptr(dW), None if dz is None else _ptr(dz))
+    if rc != 0:
+        raise ValueError("oracle_token_logprob_backward rejected its arguments")
+    out = {"dh": dh, "dW": dW}
+    if want_dz:
+        out["dz"] = dz
+    return out
 
 
 def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,

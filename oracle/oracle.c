@@ -546,3 +546,55 @@ int oracle_mismatch_monitor(const float *logp_train, const float *logp_rollout, 
     free(d);
     return 0;
 }
+
+/* ------------------------------------------------------------------ token logprob backward
+ *
+ * The trainer differentiates the selected-token logprob (Thinking Machines
+ * page, "Unclipped importance sampling": the token gradient is a weight times
+ * the gradient of log q_t).  With an upstream weight g_t per token and
+ * l_t = z_t[a_t] / tau - log sum_v exp(z_t[v] / tau), z_t = h_t W^T:
+ *   dz_t[v] = d (sum_t g_t l_t) / d z_t[v] = g_t (1[v = a_t] - p_t[v]) / tau,
+ *   p_t = softmax(z_t / tau),  dh = dz W  [N, D],  dW = dz^T h  [V, D].
+ * Written from the definition: z_t and p_t recomputed in fp64 per row (as the
+ * forward oracle), then both products summed in index order.  Rows whose
+ * target lies outside [0, V) take no one-hot term.  dz [N, V] may be NULL. */
+int oracle_token_logprob_backward(const uint16_t *h, const uint16_t *W, const int32_t *targets, const float *grad,
+                                  int64_t N, int64_t D, int64_t V, double temperature, double *dh, double *dW,
+                                  double *dz_out)
+{
+    if (N < 0 || D <= 0 || V <= 0 || !(temperature > 0.0) || !isfinite(temperature))
+        return -1;
+    if (N > 0 && (!h || !W || !targets || !grad || !dh || !dW))
+        return -1;
+    double *hd = (double *)malloc(sizeof(double) * (size_t)D);
+    double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!hd || !z) {
+        free(hd);
+        free(z);
+        return -2;
+    }
+    for (int64_t i = 0; i < V * D; ++i)
+        dW[i] = 0.0;
+    for (int64_t t = 0; t < N; ++t) {
+        double lp, lse;
+        oracle_row(h + t * D, W, NULL, targets[t], D, V, temperature, hd, z, &lp, &lse);
+        double *dht = dh + t * D;
+        for (int64_t d = 0; d < D; ++d)
+            dht[d] = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            const double p = exp(z[v] - lse);
+            const double dzv = (double)grad[t] * ((v == targets[t] ? 1.0 : 0.0) - p) / temperature;
+            if (dz_out)
+                dz_out[t * V + v] = dzv;
+            const uint16_t *w = W + v * D;
+            double *dwv = dW + v * D;
+            for (int64_t d = 0; d < D; ++d) {
+                dht[d] += dzv * bf16_value(w[d]);
+                dwv[d] += dzv * hd[d];
+            }
+        }
+    }
+    free(hd);
+    free(z);
+    return 0;
+}

@@ -621,3 +621,68 @@ def test_f32_weights_differ_from_their_bf16_rounding():
     lf, _ = oracle.token_logprob_f32w(h, W, a)
     lb, _ = oracle.token_logprob(h, bf16_round(W), a)
     assert 1e-5 < np.max(np.abs(lf - lb)) < 1e-1
+
+
+# --------------------------------------------------------------- token logprob backward
+def _bw_case(N, D, V, seed, w_std=0.2):
+    h, W, a = _rand_head(N, D, V, seed, w_std=w_std)
+    g = np.random.default_rng(seed + 1).standard_normal(N).astype(np.float32)
+    return h, W, a, g
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.7])
+def test_backward_against_torch_autograd(tau):
+    """dh and dW equal torch float64 autograd of sum_t g_t log_softmax(h W^T / tau)[a_t]
+    (reverse-mode differentiation: another route than the closed form)."""
+    import torch
+    h, W, a, g = _bw_case(6, 24, 50, 80)
+    o = oracle.token_logprob_backward(h, W, a, g, temperature=tau, want_dz=True)
+    ht = torch.tensor(bf16_to_f32(h).astype(np.float64), requires_grad=True)
+    Wt = torch.tensor(bf16_to_f32(W).astype(np.float64), requires_grad=True)
+    lp = torch.log_softmax(ht @ Wt.T / tau, dim=-1).gather(1, torch.from_numpy(a.astype(np.int64))[:, None])[:, 0]
+    (lp * torch.from_numpy(g.astype(np.float64))).sum().backward()
+    np.testing.assert_allclose(o["dh"], ht.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o["dW"], Wt.grad.numpy(), rtol=0, atol=1e-12)
+    assert np.max(np.abs(o["dz"].sum(axis=1))) < 1e-12   # softmax gradient rows sum to zero
+
+
+def test_backward_dW_by_central_differences():
+    """dW[v, d] = d (sum_t g_t l_t) / d W[v, d] by central differences of the
+    fp32-weight forward oracle (weights on a 2^-12 grid, step 2^-10, exact in
+    fp32); the bf16 weights of the backward are the same values."""
+    rng = np.random.default_rng(81)
+    N, D, V = 5, 16, 40
+    h = bf16_round(rng.standard_normal((N, D), dtype=np.float32))
+    Wq = (np.round(rng.standard_normal((V, D)) * 0.3 * 64) / 64).astype(np.float32)   # bf16-exact, 2^-6 grid
+    W = bf16_round(Wq)
+    assert np.array_equal(bf16_to_f32(W), Wq)
+    a = rng.integers(0, V, N).astype(np.int32)
+    g = rng.standard_normal(N).astype(np.float32)
+    o = oracle.token_logprob_backward(h, W, a, g)
+    step = 2.0 ** -10
+    for (v, d) in [(0, 0), (int(a[0]), 3), (17, 15), (39, 7), (int(a[2]), 0)]:
+        Wp, Wm = Wq.copy(), Wq.copy()
+        Wp[v, d] += np.float32(step)
+        Wm[v, d] -= np.float32(step)
+        lp, _ = oracle.token_logprob_f32w(h, Wp, a)
+        lm, _ = oracle.token_logprob_f32w(h, Wm, a)
+        fd = float(np.dot(g.astype(np.float64), lp - lm)) / (2 * step)
+        assert abs(fd - o["dW"][v, d]) < 1e-6 * max(1.0, abs(fd)), (v, d, fd, o["dW"][v, d])
+
+
+def test_backward_invariants():
+    """Every column sum of dW is zero (each row's softmax gradient sums to
+    zero); <dW, W> = <dh, h> (both equal sum_t sum_v dz z); g = 0 gives zero;
+    a target outside [0, V) drops the one-hot term only."""
+    h, W, a, g = _bw_case(8, 32, 60, 82)
+    o = oracle.token_logprob_backward(h, W, a, g)
+    Wf = bf16_to_f32(W).astype(np.float64)
+    hf = bf16_to_f32(h).astype(np.float64)
+    assert np.max(np.abs(o["dW"].sum(axis=0))) < 1e-12
+    assert abs(np.sum(o["dW"] * Wf) - np.sum(o["dh"] * hf)) < 1e-10
+    z = oracle.token_logprob_backward(h, W, a, np.zeros(8, np.float32))
+    assert not z["dh"].any() and not z["dW"].any()
+    a2 = a.copy()
+    a2[0] = -100
+    o2 = oracle.token_logprob_backward(h, W, a2, g)
+    np.testing.assert_allclose(o2["dh"][0], o["dh"][0] - float(g[0]) * Wf[a[0]], rtol=0, atol=1e-12)
