@@ -105,6 +105,31 @@ TIM_API int tim_token_logprob_temperature(const void *h, const void *W, const in
                                           int64_t N, int64_t D, int64_t V, float temperature,
                                           float *out_logp, float *out_lse, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ token logprob backward
+ *
+ * The trainer's gradient through the selected-token logprob (Thinking Machines
+ * page, "Unclipped importance sampling": each token weights the gradient of
+ * log q_t).  With an upstream gradient g_t = dL / dl_t per token (for example
+ * the TIS-weighted PPO surrogate's token_grad) and the forward's lse:
+ *   dz_t[v] = g_t (1[v = a_t] - p_t[v]) / tau,  p_t = softmax(h_t W^T / tau),
+ *   dh = dz W  (fp32 [N, D]),  dW = dz^T h  (fp32 [V, D]).
+ * The logits are recomputed by the fused kernel and turned into dz (bf16) in
+ * its epilogue, chunk by chunk of at most 4096 rows (the fp32 logits never
+ * reach HBM); per chunk two cuBLAS GEMMs (bf16 operands, fp32 accumulation)
+ * give that chunk's rows of dh and add its share of dW, chunks in row order,
+ * so dW's reduction order is fixed and the results repeat bit for bit.
+ *   h, W, targets, N, D, V, temperature   as tim_token_logprob_temperature
+ *   grad_logp     fp32 [N], 4-byte aligned
+ *   lse           fp32 [N]: out_lse of the forward at the same temperature
+ *   dh            out: fp32 [N, D], 16-byte aligned
+ *   dW            out: fp32 [V, D], 16-byte aligned; accumulate_dW != 0 adds into it
+ * A target outside [0, V) takes no one-hot term.  Scratch: min(N, 4096) rows
+ * x V bf16 from the library's stream-ordered pool (1.2 GB at V = 151936). */
+TIM_API int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targets,
+                                       const float *grad_logp, const float *lse, int64_t N, int64_t D,
+                                       int64_t V, float temperature, float *dh, float *dW, int accumulate_dW,
+                                       tim_stream_t stream);
+
 /* ------------------------------------------------------------------ FP32 LM head
  *
  * LoongSage "Train-Inference Consistency" section 3: the LM head's weights and

@@ -29,8 +29,8 @@ __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "MONITOR_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
     "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
     "tim_tis_ppo", "tim_mismatch_monitor", "tim_split_weight_bytes", "tim_split_weight_fp32",
-    "tim_token_logprob_fp32_head", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
-    "token_logprob", "split_weight_fp32", "token_logprob_fp32_head", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
+    "tim_token_logprob_fp32_head", "tim_token_logprob_backward", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "token_logprob", "token_logprob_backward", "split_weight_fp32", "token_logprob_fp32_head", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -126,6 +126,9 @@ def load():
             lib.tim_split_weight_fp32.restype = ctypes.c_int
             lib.tim_token_logprob_fp32_head.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
             lib.tim_token_logprob_fp32_head.restype = ctypes.c_int
+            lib.tim_token_logprob_backward.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, P, P,
+                                                       ctypes.c_int, P]
+            lib.tim_token_logprob_backward.restype = ctypes.c_int
             lib.tim_mismatch_monitor.argtypes = [P, P, P, I64, F, P, P, P]
             lib.tim_mismatch_monitor.restype = ctypes.c_int
             lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
@@ -168,6 +171,12 @@ def tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offset
                 out: tim_ppo_out, stream) -> int:
     return load().tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets,
                               float(eps_low), float(eps_high), float(C), ctypes.byref(out), stream)
+
+
+def tim_token_logprob_backward(h, W, targets, grad_logp, lse, N, D, V, temperature, dh, dW, accumulate_dW,
+                               stream) -> int:
+    return load().tim_token_logprob_backward(h, W, targets, grad_logp, lse, N, D, V, float(temperature), dh, dW,
+                                             int(accumulate_dW), stream)
 
 
 def tim_split_weight_bytes(V, D) -> int:
@@ -263,6 +272,38 @@ def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None, tempe
                                                _stream_handle(stream, dev))
     _raise_if(rc)
     return out_logp, out_lse
+
+
+def token_logprob_backward(h, W, targets, grad_logp, lse, temperature: float = 1.0, dh=None, dW=None,
+                           accumulate_dW: bool = False, stream=None):
+    """(dh fp32 [N, D], dW fp32 [V, D]): gradients of sum_t grad_logp_t l_t
+    for bf16 h [N, D], bf16 W [V, D], int32 targets, the forward's lse [N]
+    at the same temperature.  With accumulate_dW the gradient is added to dW."""
+    import torch
+    _need(h, "h", torch.bfloat16, 2)
+    dev = h.device
+    _need(W, "W", torch.bfloat16, 2, dev)
+    _need(targets, "targets", torch.int32, 1, dev)
+    _need(grad_logp, "grad_logp", torch.float32, 1, dev)
+    _need(lse, "lse", torch.float32, 1, dev)
+    N, D = h.shape
+    V = W.shape[0]
+    if W.shape[1] != D or any(t.shape[0] != N for t in (targets, grad_logp, lse)):
+        raise ValueError("shape mismatch")
+    if dh is None:
+        dh = torch.empty((N, D), dtype=torch.float32, device=dev)
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs dW")
+        dW = torch.empty((V, D), dtype=torch.float32, device=dev)
+    _need(dh, "dh", torch.float32, 2, dev)
+    _need(dW, "dW", torch.float32, 2, dev)
+    with torch.cuda.device(dev):
+        rc = tim_token_logprob_backward(h.data_ptr(), W.data_ptr(), targets.data_ptr(), grad_logp.data_ptr(),
+                                        lse.data_ptr(), N, D, V, temperature, dh.data_ptr(), dW.data_ptr(),
+                                        accumulate_dW, _stream_handle(stream, dev))
+    _raise_if(rc)
+    return dh, dW
 
 
 def split_weight_fp32(W, out=None, stream=None):

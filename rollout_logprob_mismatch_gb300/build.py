@@ -3,9 +3,9 @@
     python -m rollout_logprob_mismatch_gb300.build [--force] [--ptxas-verbose]
 
 Translation units compile in parallel into ``_build/``; the shared library
-links the CUDA runtime statically, so it loads on a machine without a GPU
-(the CPU tests check its exported symbols) and needs only the NVIDIA driver at
-run time.
+links the CUDA runtime statically and cuBLAS dynamically (the backward's two
+plain GEMMs), with the toolkit's lib64 as run path, so it loads on a machine
+without a GPU (the CPU tests check its exported symbols).
 """
 from __future__ import annotations
 
@@ -68,7 +68,9 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
     if force or _stale(LIB, objs):
         tmp = LIB + ".%d.tmp" % os.getpid()
-        cmd = [exe] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
+        cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(exe))), "lib64")
+        cmd = [exe] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + \
+            ["-lcublas", "-Xlinker", "-rpath=" + cuda_lib, "-lpthread", "-ldl", "-lrt"]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout.decode(errors="replace"))

@@ -27,6 +27,8 @@
 #include <algorithm>
 #include <cstdlib>
 
+#include <cuda_bf16.h>
+
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
 #include "../../include/tim.h"
@@ -68,6 +70,16 @@ __device__ __forceinline__ int tiles_in_chunk(int ch, int V)
     return (hi - lo + K1_BN - 1) / K1_BN;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// MODE 0: the forward (per-chunk max / sum and the target logit).  MODE 1: the
+// backward's logit gradient dz = g (onehot(a) - p) / tau, p = softmax(z / tau)
+// from the forward's lse, written as bf16 rows of length a.dz_ld.
+template <int MODE>
 __global__ void __launch_bounds__(K1_THREADS, 1)
     k1_main_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                    const K1Args a)
@@ -214,6 +226,71 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             // every UMMA issued has finished before TMEM is released
             umma_commit(drain);
             drain_wait(drain, 0);
+        }
+    } else if (MODE == 1) {
+        // ---------------------------------------------------- backward epilogue, warps 2..5
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        const float zscale = LOG2E * a.inv_temp;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = cid; ok && u < a.units; u += ncl) {
+            const Unit w = unit_of(u, a);
+            const int nt = tiles_in_chunk(w.ch, a.V);
+            const int row = (w.mt * K1_CLUSTER + static_cast<int>(rank)) * K1_BM + r_in_tile;
+            const bool live = row < a.N;
+            const int tgt = live ? __ldg(a.targets + row) : -1;
+            const float gs = live ? __ldg(a.grad + row) * a.inv_temp : 0.f;   // g / tau
+            const float l2 = live ? __ldg(a.lse_in + row) * LOG2E : 0.f;     // p = 2^(z zscale - l2)
+            uint16_t *dzrow = a.dz + static_cast<size_t>(live ? row : 0) * static_cast<size_t>(a.dz_ld);
+            for (int j = 0; j < nt; ++j) {
+                if (!mbar_wait(tfull(acc), acc_phase, abort_flag, budget)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int c0 = w.ch * K1_VCHUNK + j * K1_BN;
+                const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * K1_BN);
+#pragma unroll 1
+                for (int sc = 0; sc < K1_BN / SUBCOLS; ++sc) {
+                    const int col0 = c0 + sc * SUBCOLS;
+                    if (col0 >= a.V)
+                        break;
+                    float v[SUBCOLS];
+                    __syncwarp();
+                    tmem_load32(tb + static_cast<uint32_t>(sc * SUBCOLS), v);
+                    uint32_t pk[SUBCOLS / 2];
+#pragma unroll
+                    for (int jj = 0; jj < SUBCOLS; jj += 2) {
+                        const float p0 = ex2(fmaf(v[jj], zscale, -l2));
+                        const float p1 = ex2(fmaf(v[jj + 1], zscale, -l2));
+                        const float d0 = gs * ((col0 + jj == tgt ? 1.f : 0.f) - p0);
+                        const float d1 = gs * ((col0 + jj + 1 == tgt ? 1.f : 0.f) - p1);
+                        pk[jj / 2] = pack_bf16x2(d0, d1);
+                    }
+                    if (live) {
+                        if (col0 + SUBCOLS <= a.V) {   // 64 bytes at a 64-byte offset of a 16-byte aligned row
+                            uint4 *dst = reinterpret_cast<uint4 *>(dzrow + col0);
+#pragma unroll
+                            for (int k = 0; k < SUBCOLS / 8; ++k)
+                                dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < SUBCOLS; ++jj)
+                                if (col0 + jj < a.V)
+                                    dzrow[col0 + jj] = static_cast<uint16_t>(pk[jj / 2] >> (16 * (jj & 1)));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty(acc));
+                acc ^= 1;
+                if (acc == 0)
+                    acc_phase ^= 1u;
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue, warps 2..5
@@ -368,14 +445,20 @@ int64_t k1_band_bytes()
 
 cudaError_t k1_prepare_device()
 {
-    return cudaFuncSetAttribute(k1_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(K1_SMEM_BYTES));
+    cudaError_t e = cudaFuncSetAttribute(k1_main_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(K1_SMEM_BYTES));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k1_main_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(K1_SMEM_BYTES));
+    return e;
 }
 
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
-                           cudaStream_t stream)
+                           cudaStream_t stream, int mode)
 {
-    static int max_clusters[64] = {0};   // per device, found once (the same value from any thread)
+    static int max_clusters[2][64] = {};   // per mode and device, found once (the same value from any thread)
+    auto kernel = mode == 1 ? k1_main_kernel<1> : k1_main_kernel<0>;
+    const int md = mode == 1 ? 1 : 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -392,18 +475,19 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
+    if (dev >= 0 && dev < 64 && max_clusters[md][dev] == 0) {
         int n = 0;
         cfg.gridDim = dim3(K1_CLUSTER * 1024, 1, 1);
-        e = cudaOccupancyMaxActiveClusters(&n, k1_main_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
         if (e != cudaSuccess)
             return e;
-        max_clusters[dev] = n > 0 ? n : 1;
+        max_clusters[md][dev] = n > 0 ? n : 1;
     }
-    const int clusters = static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[dev] : 1));
+    const int clusters =
+        static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[md][dev] : 1));
     cfg.gridDim = dim3(K1_CLUSTER * clusters, 1, 1);
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k1_main_kernel, tmap_h, tmap_w, a);
+    return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, a);
 }
 
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 
+#include <cublas_v2.h>
 #include <cudaTypedefs.h>
 
 #include "../../include/tim.h"
@@ -137,6 +138,33 @@ int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, ui
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Rows of one backward chunk: the bf16 logit gradient of a chunk is rows x V
+// (1.2 GB at V = 151936); dh and dW are then two cuBLAS GEMMs per chunk.
+constexpr int64_t kBackwardRows = 4096;
+
+// cuBLAS handle of the current device, made once (never destroyed: it lives
+// as long as the process, like the device state).
+int cublas_handle(cublasHandle_t *out)
+{
+    static cublasHandle_t handles[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TIM_ERR_UNSUPPORTED_DEVICE, "device index %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!handles[dev]) {
+        const cublasStatus_t bs = cublasCreate(&handles[dev]);
+        if (bs != CUBLAS_STATUS_SUCCESS) {
+            handles[dev] = nullptr;
+            return fail(TIM_ERR_CUDA, "cublasCreate: %d", static_cast<int>(bs));
+        }
+    }
+    *out = handles[dev];
+    return TIM_OK;
+}
+
 // Largest float <= v, and smallest float >= v: a float x then satisfies
 // x > float_down(v) <=> x > v, and x < float_up(v) <=> x < v.
 float float_down(double v)
@@ -234,7 +262,7 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(token_logprob workspace)");
 
-    tim::K1Args a;
+    tim::K1Args a{};
     a.targets = targets;
     a.part = static_cast<float2 *>(ws);
     a.za = reinterpret_cast<float *>(static_cast<char *>(ws) + part_bytes);
@@ -357,6 +385,115 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return cuda_fail(e, "mismatch_stats launch");
     if (ef != cudaSuccess)
         return cuda_fail(ef, "cudaFreeAsync(mismatch workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targets, const float *grad_logp,
+                               const float *lse, int64_t N, int64_t D, int64_t V, float temperature, float *dh,
+                               float *dW, int accumulate_dW, tim_stream_t stream)
+{
+    if (N < 0 || N >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "N = %lld out of range [0, 2^31)", static_cast<long long>(N));
+    if (D <= 0 || D % 8 != 0 || D > 65536)
+        return fail(TIM_ERR_INVALID_ARG, "D = %lld must be positive, a multiple of 8 and <= 65536",
+                    static_cast<long long>(D));
+    if (V <= 0 || V >= (int64_t(1) << 31))
+        return fail(TIM_ERR_INVALID_ARG, "V = %lld out of range (0, 2^31)", static_cast<long long>(V));
+    if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature))
+        return fail(TIM_ERR_INVALID_ARG, "temperature must be positive and finite");
+    if (!W || !dW)
+        return fail(TIM_ERR_INVALID_ARG, "W and dW are required");
+    if (N > 0 && (!h || !targets || !grad_logp || !lse || !dh))
+        return fail(TIM_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dh, 16) || !aligned(dW, 16))
+        return fail(TIM_ERR_INVALID_ARG, "h, W, dh and dW must be 16-byte aligned");
+    if (!aligned(targets, 4) || !aligned(grad_logp, 4) || !aligned(lse, 4))
+        return fail(TIM_ERR_INVALID_ARG, "targets / grad_logp / lse must be 4-byte aligned");
+
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cublasHandle_t cb = nullptr;
+    if ((rc = cublas_handle(&cb)) != TIM_OK)
+        return rc;
+    cublasStatus_t bs = cublasSetStream(cb, s);
+    if (bs != CUBLAS_STATUS_SUCCESS)
+        return fail(TIM_ERR_CUDA, "cublasSetStream: %d", static_cast<int>(bs));
+    if (N == 0) {   // no rows: dW = 0 unless accumulating
+        if (!accumulate_dW) {
+            const cudaError_t e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * D * sizeof(float), s);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMemsetAsync(dW)");
+        }
+        g_msg[0] = 0;
+        return TIM_OK;
+    }
+    // rows in chunks of at most kBackwardRows: dz of one chunk, bf16 [rows][Vp]
+    const int64_t Vp = (V + 7) / 8 * 8;
+    const int64_t rows_max = std::min<int64_t>(kBackwardRows, (N + 255) / 256 * 256);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(rows_max) * Vp * 2, dev->pool, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMallocFromPoolAsync(backward workspace)");
+    CUtensorMap tw;
+    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK) {
+        cudaFreeAsync(ws, s);
+        return rc;
+    }
+    const float one = 1.f, zero = 0.f;
+    const int64_t chunks_v = tim::k1_num_chunks(V);
+    for (int64_t r0 = 0; r0 < N && rc == TIM_OK; r0 += rows_max) {
+        const int64_t n = std::min<int64_t>(rows_max, N - r0);
+        const void *hc = static_cast<const uint16_t *>(h) + r0 * D;
+        CUtensorMap th;
+        if ((rc = encode_bf16(&th, hc, n, D, tim::K1_BM)) != TIM_OK)
+            break;
+        const int64_t m_tiles = (n + tim::K1_BM - 1) / tim::K1_BM;
+        const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
+        tim::K1Args a{};
+        a.targets = targets + r0;
+        a.status = dev->status;
+        a.inv_temp = 1.f / temperature;
+        a.N = static_cast<int32_t>(n);
+        a.D = static_cast<int32_t>(D);
+        a.V = static_cast<int32_t>(V);
+        a.w_segments = 1;
+        a.num_m_tiles = static_cast<int32_t>(m_tiles);
+        a.num_chunks = static_cast<int32_t>(chunks_v);
+        a.num_m_groups = static_cast<int32_t>(m_groups);
+        const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
+        a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
+        a.units = static_cast<int32_t>(m_groups * chunks_v);
+        a.wait_budget_ns = wait_budget_ns();
+        a.grad = grad_logp + r0;
+        a.lse_in = lse + r0;
+        a.dz = static_cast<uint16_t *>(ws);
+        a.dz_ld = Vp;
+        if ((e = tim::k1_launch_main(th, tw, a, s, 1)) != cudaSuccess) {
+            rc = cuda_fail(e, "backward dz launch");
+            break;
+        }
+        // row-major dh[n, D] = dz[n, V] W[V, D]: column-major dh^T = W^T dz^T
+        bs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(D), static_cast<int>(n), static_cast<int>(V),
+                          &one, W, CUDA_R_16BF, static_cast<int>(D), ws, CUDA_R_16BF, static_cast<int>(Vp), &zero,
+                          dh + r0 * D, CUDA_R_32F, static_cast<int>(D), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        // row-major dW[V, D] (+)= dz^T[V, n] h[n, D]: column-major dW^T = h^T dz; chunks in row order
+        if (bs == CUBLAS_STATUS_SUCCESS)
+            bs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(D), static_cast<int>(V), static_cast<int>(n),
+                              &one, hc, CUDA_R_16BF, static_cast<int>(D), ws, CUDA_R_16BF, static_cast<int>(Vp),
+                              (r0 == 0 && !accumulate_dW) ? &zero : &one, dW, CUDA_R_32F, static_cast<int>(D),
+                              CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        if (bs != CUBLAS_STATUS_SUCCESS)
+            rc = fail(TIM_ERR_CUDA, "cublasGemmEx: %d", static_cast<int>(bs));
+    }
+    const cudaError_t ef = cudaFreeAsync(ws, s);
+    if (rc != TIM_OK)
+        return rc;
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(backward workspace)");
     g_msg[0] = 0;
     return TIM_OK;
 }

@@ -45,12 +45,17 @@ struct K1Args {
     int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
     int32_t band, units;      // units = num_m_groups * num_chunks, one per cluster
     uint64_t wait_budget_ns;
+    // backward (mode 1) only
+    const float *grad;        // [N] upstream gradient of each l_t
+    const float *lse_in;      // [N] the forward's lse
+    uint16_t *dz;             // [N][dz_ld] bf16 gradient of the logits
+    int64_t dz_ld;
 };
 
 // Launches one cluster of K1_CLUSTER CTAs per unit, at most as many clusters
-// as fit on the device at once (persistent).
+// as fit on the device at once (persistent).  mode 0: forward; 1: backward dz.
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int mode = 0);
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream);

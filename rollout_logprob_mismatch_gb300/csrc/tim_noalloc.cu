@@ -167,7 +167,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     if ((rc = encode(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK)
         return rc;
 
-    tim::K1Args a;
+    tim::K1Args a{};
     a.targets = targets;
     a.part = reinterpret_cast<float2 *>(dev->scratch);
     a.za = reinterpret_cast<float *>(dev->scratch + part_bytes);

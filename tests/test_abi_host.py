@@ -189,6 +189,20 @@ def test_fp32_head_rejects_bad_arguments(lib):
     assert tim.tim_token_logprob_fp32_head(16, 8, 16, 4, 64, 10, 1.0, 16, 16, None) == E
 
 
+def test_backward_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    ok = dict(h=16, W=16, t=16, g=16, l=16, N=4, D=64, V=10, tau=1.0, dh=16, dW=16)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return tim.tim_token_logprob_backward(a["h"], a["W"], a["t"], a["g"], a["l"], a["N"], a["D"], a["V"],
+                                              a["tau"], a["dh"], a["dW"], 0, None)
+    for bad in (dict(N=-1), dict(D=12), dict(D=0), dict(V=0), dict(tau=0.0), dict(tau=math.nan), dict(W=None),
+                dict(dW=None), dict(h=None), dict(g=None), dict(l=None), dict(dh=None), dict(h=8), dict(dh=24),
+                dict(dW=8), dict(g=18)):
+        assert call(**bad) == E, bad
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(tim, "_lib", None)
