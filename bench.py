@@ -342,6 +342,12 @@ def run_gb300(args):
         tim.token_logprob(hd, Wd, ad, lp, lse)
         tim.mismatch_stats(lp, rod, maskd, offd, C=cfg.C, out=k2out)
 
+    if args.only == "backward":
+        r = backward_measure(tim, dev, stream, peaks, hd, Wd, ad, reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
     if args.only == "fp32head":
         r = fp32_head_measure(tim, dev, stream, peaks, hd, ad, V, reps=args.steps, warmup=args.warmup)
         tim.check()
@@ -443,6 +449,7 @@ def run_gb300(args):
     mon_bw = monitor_bandwidth(tim, dev, stream, peaks) if not args.skip_monitor else None
     sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
     fp32h = fp32_head_measure(tim, dev, stream, peaks, hd, ad, V) if not args.skip_fp32_head else None
+    bwd = backward_measure(tim, dev, stream, peaks, hd, Wd, ad) if not args.skip_backward else None
     tim.check()
 
     if rank != 0:
@@ -484,6 +491,8 @@ def run_gb300(args):
         line["mismatch_monitor"] = mon_bw
     if fp32h is not None:
         line["fp32_head"] = fp32h
+    if bwd is not None:
+        line["backward"] = bwd
     if sweep is not None:
         line["sweep"] = sweep
     print(json.dumps(line), flush=True)
@@ -561,6 +570,41 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
             "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
             "frac_of_8000": gbs / 8000.0, "bound": "hbm",
             "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
+
+
+def backward_measure(tim, dev, stream, peaks, hd, Wd, ad, reps=5, warmup=2):
+    """The token logprob's backward on the bench's head shape: g ~ N(0, 1) per
+    token, lse from the forward; one call = per 4096-row chunk the fused dz
+    kernel (logits recomputed, never stored in fp32) and two cuBLAS GEMMs
+    (dh, dW); L2 flushed before each call.  Work 3 x 2NVD FLOP (recompute, dh,
+    dW) against the bf16 peak."""
+    import torch
+    N, D = hd.shape
+    V = Wd.shape[0]
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    grad = torch.randn(N, generator=g, device=dev)
+    _, lse = tim.token_logprob(hd, Wd, ad)
+    dh = torch.empty((N, D), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        tim.token_logprob_backward(hd, Wd, ad, grad, lse, dh=dh, dW=dW)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        flush.fill_(i)
+        ev[i][0].record(stream)
+        tim.token_logprob_backward(hd, Wd, ad, grad, lse, dh=dh, dW=dW)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
+    flops = 3 * 2.0 * N * V * D
+    del dh, dW
+    return {"N": N, "D": D, "V": V, "avg_call_ms": t * 1e3, "tokens_per_s": N / t,
+            "tflops": flops / t / 1e12, "bound": "tensor", "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": flops / t / 1e12 / peaks["bf16_tflops"],
+            "parts": "per 4096-row chunk: fused dz kernel (ours) + 2 cuBLAS GEMMs"}
 
 
 def fp32_head_measure(tim, dev, stream, peaks, hd, ad, V, reps=5, warmup=3):
@@ -703,7 +747,8 @@ def main(argv=None):
     ap.add_argument("--skip-ppo", action="store_true")
     ap.add_argument("--skip-monitor", action="store_true")
     ap.add_argument("--skip-fp32-head", action="store_true")
-    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo", "monitor", "fp32head"], default=None,
+    ap.add_argument("--skip-backward", action="store_true")
+    ap.add_argument("--only", choices=["k1", "k2", "k2bw", "ppo", "monitor", "fp32head", "backward"], default=None,
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller batch of the same head (profiling runs only)")
