@@ -299,8 +299,10 @@ enum tim_monitor_field {
  *   tau_tok                   rejection threshold on |delta|, >= 0 and finite
  *   token_reject              out, optional (NULL = not written): uint8 [N], 16-byte aligned
  *   out                       out: fp64 [TIM_MON_FIELDS]
- * Three passes over the tokens (9 bytes each per token) and three single-CTA
- * selection steps.  Scratch: about 115 KB from the library's stream-ordered pool. */
+ * One pass over the tokens (9 bytes read per token) after a sample of at most
+ * 2^20 of them; exact selection among the few percent of tokens near each
+ * quantile (over all tokens when a sample-based bound misses).  Scratch:
+ * 525 KB + N / 4 bytes + 1 MB from the library's stream-ordered pool. */
 TIM_API int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
                                  int64_t N, float tau_tok, uint8_t *token_reject, double *out,
                                  tim_stream_t stream);

@@ -9,23 +9,27 @@
 // the order statistics floor(h) and floor(h) + 1; e^x is increasing, so the
 // ratio's order statistics are e^ of delta's.
 //
-// The eight order statistics (two per quantile) are found exactly, by radix
-// selection on 32-bit keys that order like the values (|delta|: its bits;
-// delta: sign-flipped bits), in three passes over the tokens of 11, 11 and 10
-// key bits:
-//   mon_pass_kernel<1>   histogram of the top 11 bits of delta's key (that of
-//                        |delta| follows from it), n_used, n_extreme and the
-//                        rejection flags;
-//   mon_select_kernel<1> ranks from n_used; per target, the bin that holds
-//                        its rank and the rank left inside that bin;
-//   mon_pass_kernel<2>   per target, histogram of bits 20..10 of the keys in
-//                        its bin;  mon_select_kernel<2>;
-//   mon_pass_kernel<3>   bits 9..0;  mon_select_kernel<3> ends with exact
-//                        keys and writes the record.
-// Counts are integers, so the result does not depend on the order in which
-// threads add them: the selected tokens are exactly the oracle's.  Each pass
-// reads 9 bytes per token; a CTA counts into shared-memory histograms and adds
-// the non-zero bins to the global ones at the end.
+// The eight order statistics (two per quantile) are found exactly, on 32-bit
+// keys that order like the values (|delta|: its bits; delta: sign-flipped
+// bits).  Counts are integers, so thread order cannot change them: the
+// selected tokens are exactly the ones a sort would pick.
+//   mon_sample_kernel   histograms (14 key bits) of up to 1024 evenly spaced
+//                       runs of 1024 consecutive tokens;
+//   mon_bounds_kernel   per quantile, key bounds [lo, hi] around the sample's
+//                       quantile, six standard deviations of its rank wide;
+//   mon_scan_kernel     the one full pass: n_used, n_extreme, rejection
+//                       flags and, per quantile, the used tokens below lo and
+//                       the keys inside [lo, hi] (typically a few percent),
+//                       kept in a list;
+//   mon_check_kernel    ranks from n_used; each quantile's order statistics
+//                       must fall inside its list (else, or if a list
+//                       overflowed, the selection runs over all tokens);
+//   mon_pass_kernel<1..3> + mon_select_kernel<1..3>: radix selection in three
+//                       digit passes (11, 11, 10 bits) over the lists, on
+//                       key - lo, or over all tokens; select<3> writes the
+//                       record.
+// The bounds only decide how much work the selection does; the result is the
+// same either way.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
@@ -38,13 +42,18 @@
 namespace tim {
 namespace {
 
-// Quantile levels: |delta| at 0.95 (targets 0, 1), the ratio at 0.01, 0.5, 0.99.
+constexpr int SAMPLE_SHIFT = 18;                         // sample bins: key >> 18
+constexpr int SBD = 1 << (32 - SAMPLE_SHIFT);            // 16384 bins of delta's key
+constexpr int SBA = 1 << (31 - SAMPLE_SHIFT);            // 8192 of |delta|'s key
+static_assert(SBD + SBA <= MON_SBINS_D + MON_SBINS_A, "sample histogram room");
+constexpr double kSigmas = 6.0;                          // width of the bounds in rank standard deviations
+
+// Quantile levels: |delta| at 0.95 (quantile 0), the ratio at 0.01, 0.5, 0.99.
 __device__ __forceinline__ double level(int i)
 {
     return i == 0 ? 0.95 : i == 1 ? 0.01 : i == 2 ? 0.5 : 0.99;
 }
 
-// Key of |delta| (targets 0, 1) and of delta (targets 2..7).
 __device__ __forceinline__ uint32_t key_abs(float d) { return __float_as_uint(fabsf(d)); }
 
 __device__ __forceinline__ uint32_t key_signed(float d)
@@ -58,85 +67,19 @@ __device__ __forceinline__ float unkey_signed(uint32_t k)
     return __uint_as_float(k ^ ((k >> 31) ? 0x80000000u : 0xffffffffu));
 }
 
-// One count per valid lane into h[bin].  (Adding the lanes of a warp that
-// share a bin first, through match.any, was measured slower: 1844 against
-// 1257 us per call at 2^27 tokens.)
-__device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool valid)
+__device__ __forceinline__ bool usable(bool m, float d) { return m && fabsf(d) <= FLT_MAX; }
+
+// Tokens of a grid-stride pass in 4-token groups g (16-byte loads; the ragged
+// last group by plain loads).  Calls f(g, d[4], m[4], valid[4]) on every lane
+// of the warp, MON_UNROLL groups loaded before the first use.
+template <typename F>
+__device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
 {
-    if (valid)
-        atomicAdd(h + bin, 1u);
-}
-
-template <int PASS>
-struct PassShape;
-template <>
-struct PassShape<1> {
-    static constexpr int NH = 1, NB = MON_BINS1, SHIFT = 21, KEEP = 32;   // KEEP: prefix bits compared
-};
-template <>
-struct PassShape<2> {
-    static constexpr int NH = MON_TARGETS, NB = MON_BINS2, SHIFT = 10, KEEP = 11;
-};
-template <>
-struct PassShape<3> {
-    static constexpr int NH = MON_TARGETS, NB = MON_BINS3, SHIFT = 0, KEEP = 22;
-};
-
-template <int PASS>
-constexpr int pass_smem_bytes() { return PassShape<PASS>::NH * PassShape<PASS>::NB * 4; }
-
-// One token of pass PASS (all lanes call it; `valid` false past the end).
-template <int PASS>
-__device__ __forceinline__ void pass_token(uint32_t *sh, const uint32_t (&pref)[MON_TARGETS], float d, bool m,
-                                           bool valid,
-                                           float tau, int &n_used, int &n_ext)
-{
-    using P = PassShape<PASS>;
-    const bool used = valid && m && fabsf(d) <= FLT_MAX;
-    const uint32_t ka = key_abs(d), kd = key_signed(d);
-    if (PASS == 1) {   // the |delta| histogram follows from delta's (see mon_select_kernel<1>)
-        hist_add(sh, kd >> P::SHIFT, used);
-        n_used += static_cast<int>(used);
-        n_ext += static_cast<int>(used && fabsf(d) > tau);
-    } else {
-#pragma unroll
-        for (int j = 0; j < MON_TARGETS; ++j) {
-            const uint32_t k = j < 2 ? ka : kd;
-            const bool in = used && (k >> (32 - P::KEEP)) == (pref[j] >> (32 - P::KEEP));
-            if (__any_sync(0xffffffffu, in))
-                hist_add(sh + j * P::NB, (k >> P::SHIFT) & (P::NB - 1), in);
-        }
-    }
-}
-
-template <int PASS>
-__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(const MonArgs a)
-{
-    using P = PassShape<PASS>;
-    extern __shared__ __align__(16) uint32_t mon_sh[];
-    __shared__ uint32_t pref[MON_TARGETS];
-    __shared__ int empty_s;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < P::NH * P::NB; i += MON_THREADS)
-        mon_sh[i] = 0u;
-    pdl_wait();   // the state comes from the previous kernel (or the memset)
-    pdl_launch_dependents();
-    if (tid < MON_TARGETS)
-        pref[tid] = a.st->prefix[tid];
-    if (tid == 0)
-        empty_s = a.st->empty;
-    __syncthreads();
-    if (PASS > 1 && empty_s)   // uniform over the CTA
-        return;
-    uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
-#pragma unroll
-    for (int j = 0; j < MON_TARGETS; ++j)
-        pr[j] = pref[j];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t N = a.N;
-    const int64_t G = (N + 3) >> 2;   // 4-token groups; groups below `full` have 4 tokens
+    const int64_t G = (N + 3) >> 2;
     const int64_t full = N >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * MON_THREADS;
-    int n_used = 0, n_ext = 0;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * MON_THREADS + warp * 32; base < G;
          base += stride * MON_UNROLL) {   // uniform over the warp
         float4 lt[MON_UNROLL], lr[MON_UNROLL];
@@ -151,7 +94,7 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
             } else {
                 float v[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t mm = 0u;
-                for (int i = 0; i < 4 && g < G && 4 * g + i < N; ++i) {   // the ragged last group
+                for (int i = 0; i < 4 && g < G && 4 * g + i < N; ++i) {
                     v[i] = a.l_tr[4 * g + i];
                     w[i] = a.l_ro[4 * g + i];
                     mm |= static_cast<uint32_t>(a.mask[4 * g + i] != 0) << (8 * i);
@@ -166,82 +109,387 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
             const int64_t g = base + lane + u * stride;
             const float d[4] = {__fsub_rn(lt[u].x, lr[u].x), __fsub_rn(lt[u].y, lr[u].y),
                                 __fsub_rn(lt[u].z, lr[u].z), __fsub_rn(lt[u].w, lr[u].w)};
-            uint32_t flags = 0u;
+            bool m[4], valid[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const bool valid = g < G && 4 * g + i < N;
-                const bool m = ((mk[u] >> (8 * i)) & 0xffu) != 0u;
-                const int before = n_ext;
-                pass_token<PASS>(mon_sh, pr, d[i], m, valid, a.tau_tok, n_used, n_ext);
-                flags |= static_cast<uint32_t>(n_ext != before) << (8 * i);
+                valid[i] = g < G && 4 * g + i < N;
+                m[i] = ((mk[u] >> (8 * i)) & 0xffu) != 0u;
             }
-            if (PASS == 1 && a.reject) {
-                if (g < full)
-                    __stcs(reinterpret_cast<unsigned int *>(a.reject) + g, flags);
-                else
-                    for (int i = 0; i < 4 && g < G && 4 * g + i < N; ++i)
-                        a.reject[4 * g + i] = static_cast<uint8_t>((flags >> (8 * i)) & 1u);
-            }
+            f(g, d, m, valid);
         }
     }
-    if (PASS == 1) {
-        const int wu = __reduce_add_sync(0xffffffffu, n_used);
-        const int we = __reduce_add_sync(0xffffffffu, n_ext);
-        if (lane == 0) {
-            atomicAdd(&a.st->n_used, static_cast<unsigned long long>(wu));
-            atomicAdd(&a.st->n_extreme, static_cast<unsigned long long>(we));
+}
+
+// ---------------------------------------------------------------- sample
+// CTA r histograms run r: tokens [s, s + MON_SAMPLE_RUN), s = r N / runs (runs
+// back to back when they cover the batch), in shared memory; the non-zero
+// bins are added to the global histograms.
+__global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
+{
+    extern __shared__ __align__(16) uint32_t sh[];   // [SBD] delta, then [SBA] |delta|
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < SBD + SBA; i += MON_THREADS)
+        sh[i] = 0u;
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t N = a.N;
+    const int64_t cover = static_cast<int64_t>(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN;
+    const int64_t s0 = N <= cover ? static_cast<int64_t>(blockIdx.x) * MON_SAMPLE_RUN
+                                  : static_cast<int64_t>(blockIdx.x) * N / gridDim.x;
+    const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
+    int used = 0;
+    for (int64_t t = s0 + tid; t < s1; t += MON_THREADS) {
+        const float d = __fsub_rn(a.l_tr[t], a.l_ro[t]);
+        if (usable(a.mask[t] != 0, d)) {
+            atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
+            atomicAdd(sh + SBD + (key_abs(d) >> SAMPLE_SHIFT), 1u);
+            ++used;
+        }
+    }
+    used = __reduce_add_sync(0xffffffffu, used);
+    if (lane == 0 && used)
+        atomicAdd(&a.st->sample_used, static_cast<unsigned long long>(used));
+    __syncthreads();
+    for (int i = tid; i < SBD + SBA; i += MON_THREADS)
+        if (sh[i] != 0u)
+            atomicAdd(a.shist + i, sh[i]);
+}
+
+// ---------------------------------------------------------------- bounds
+// One CTA of 1024 threads.  For quantile q at level L with m sampled used
+// tokens: sample ranks floor(L (m - 1)) - w and ceil(L (m - 1)) + w, w = six
+// standard deviations of a sample quantile's rank (sqrt(m L (1 - L))) + 2;
+// lo = the lowest key of the bin holding the first (0 when that rank is at or
+// below the sample's first), hi = the highest key of the bin holding the
+// second (all ones when at or above the sample's last).
+__global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
+{
+    __shared__ long long wsum[32];
+    __shared__ int bin_s[2 * MON_QUANTILES];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
+    MonState *st = a.st;
+    const long long m = static_cast<long long>(st->sample_used);
+    long long rlo[MON_QUANTILES], rhi[MON_QUANTILES];
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        const double L = level(q);
+        const double j = static_cast<double>(m - 1) * L;
+        const long long w = static_cast<long long>(ceil(kSigmas * sqrt(static_cast<double>(m) * L * (1.0 - L)))) + 2;
+        rlo[q] = static_cast<long long>(floor(j)) - w;
+        rhi[q] = static_cast<long long>(ceil(j)) + w;
+    }
+    if (tid < 2 * MON_QUANTILES)
+        bin_s[tid] = -1;
+    for (int kind = 0; kind < 2; ++kind) {   // 0: delta (quantiles 1..3), 1: |delta| (quantile 0)
+        const int nb = kind == 0 ? SBD : SBA;
+        const uint32_t *h = a.shist + (kind == 0 ? 0 : SBD);
+        const int per = nb / 1024;
+        long long c = 0;
+        for (int b = 0; b < per; ++b)
+            c += h[tid * per + b];
+        long long incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        __syncthreads();   // the previous kind's wsum reads are done
+        if (lane == 31)
+            wsum[warp] = incl;
+        __syncthreads();
+        long long before_warp = 0;
+        for (int w = 0; w < warp; ++w)
+            before_warp += wsum[w];
+        const long long excl = before_warp + incl - c;
+        const int q_first = kind == 0 ? 1 : 0, q_end = kind == 0 ? MON_QUANTILES : 1;
+        for (int q = q_first; q < q_end; ++q) {
+            for (int e = 0; e < 2; ++e) {
+                const long long R = e == 0 ? rlo[q] : rhi[q];
+                if (m > 0 && R > 0 && R < m - 1 && excl <= R && R < excl + c) {
+                    long long cum = excl;
+                    for (int b = 0; b < per; ++b) {
+                        cum += h[tid * per + b];
+                        if (cum > R) {
+                            bin_s[2 * q + e] = tid * per + b;
+                            break;
+                        }
+                    }
+                }
+            }
         }
     }
     __syncthreads();
+    if (tid < MON_QUANTILES) {
+        const int q = tid;
+        const int bl = bin_s[2 * q], bh = bin_s[2 * q + 1];
+        st->lo[q] = bl < 0 ? 0u : static_cast<uint32_t>(bl) << SAMPLE_SHIFT;
+        st->hi[q] = bh < 0 ? 0xffffffffu : (static_cast<uint32_t>(bh) << SAMPLE_SHIFT) | ((1u << SAMPLE_SHIFT) - 1u);
+    }
+}
+
+// ---------------------------------------------------------------- the full pass
+__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(const MonArgs a)
+{
+    __shared__ uint32_t lo_s[MON_QUANTILES], span_s[MON_QUANTILES];
+    const int tid = threadIdx.x, lane = tid & 31;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid < MON_QUANTILES) {
+        lo_s[tid] = a.st->lo[tid];
+        span_s[tid] = a.st->hi[tid] - a.st->lo[tid];
+    }
+    __syncthreads();
+    uint32_t lo[MON_QUANTILES], span[MON_QUANTILES];
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        lo[q] = lo_s[q];
+        span[q] = span_s[q];
+    }
+    const unsigned long long cap = a.cap;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int n_used = 0, n_ext = 0;
+    int below[MON_QUANTILES] = {0, 0, 0, 0};
+    for_token_groups(a, [&](int64_t g, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
+        uint32_t flags = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool used = valid[i] && usable(m[i], d[i]);
+            const bool ext = used && fabsf(d[i]) > a.tau_tok;
+            n_used += static_cast<int>(used);
+            n_ext += static_cast<int>(ext);
+            flags |= static_cast<uint32_t>(ext) << (8 * i);
+            const uint32_t ka = key_abs(d[i]), kd = key_signed(d[i]);
+#pragma unroll
+            for (int q = 0; q < MON_QUANTILES; ++q) {
+                const uint32_t k = q == 0 ? ka : kd;
+                below[q] += static_cast<int>(used && k < lo[q]);
+                const bool in = used && k - lo[q] <= span[q];
+                const unsigned bal = __ballot_sync(0xffffffffu, in);
+                if (bal != 0u) {   // uniform over the warp
+                    const int leader = __ffs(bal) - 1;
+                    unsigned long long base = 0;
+                    if (lane == leader)
+                        base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(__popc(bal)));
+                    base = __shfl_sync(0xffffffffu, base, leader);
+                    const unsigned long long pos = base + static_cast<unsigned>(__popc(bal & lt_mask));
+                    if (in && pos < cap)
+                        a.cand[static_cast<size_t>(q) * cap + pos] = k;
+                }
+            }
+        }
+        if (a.reject) {
+            if (g < (a.N >> 2))
+                __stcs(reinterpret_cast<unsigned int *>(a.reject) + g, flags);
+            else
+                for (int i = 0; i < 4 && valid[i]; ++i)
+                    a.reject[4 * g + i] = static_cast<uint8_t>((flags >> (8 * i)) & 1u);
+        }
+    });
+    const int wu = __reduce_add_sync(0xffffffffu, n_used);
+    const int we = __reduce_add_sync(0xffffffffu, n_ext);
+    int wb[MON_QUANTILES];
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q)
+        wb[q] = __reduce_add_sync(0xffffffffu, below[q]);
+    if (lane == 0) {
+        atomicAdd(&a.st->n_used, static_cast<unsigned long long>(wu));
+        atomicAdd(&a.st->n_extreme, static_cast<unsigned long long>(we));
+#pragma unroll
+        for (int q = 0; q < MON_QUANTILES; ++q)
+            if (wb[q])
+                atomicAdd(&a.st->below[q], static_cast<unsigned long long>(wb[q]));
+    }
+}
+
+// ---------------------------------------------------------------- ranks and mode
+__global__ void mon_check_kernel(const MonArgs a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x != 0)
+        return;
+    MonState *st = a.st;
+    const long long n = static_cast<long long>(st->n_used);
+    st->empty = n == 0;
+    if (n == 0)
+        return;
+    bool ok = true;
+    long long k[MON_QUANTILES], k1[MON_QUANTILES];
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        const double h = static_cast<double>(n - 1) * level(q);
+        const double fl = floor(h);
+        k[q] = static_cast<long long>(fl);
+        k1[q] = k[q] + 1 < n ? k[q] + 1 : k[q];
+        st->frac[q] = h - fl;
+        const long long b = static_cast<long long>(st->below[q]);
+        const long long c = static_cast<long long>(st->count[q]);
+        ok = ok && c <= static_cast<long long>(a.cap) && b <= k[q] && k1[q] < b + c;
+    }
+    st->fallback = ok ? 0 : 1;
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        const long long b = ok ? static_cast<long long>(st->below[q]) : 0;
+        st->rank[2 * q] = k[q] - b;
+        st->rank[2 * q + 1] = k1[q] - b;
+        const uint32_t span = st->hi[q] - st->lo[q];
+        st->span_bits[q] = ok ? (span == 0u ? 0 : 32 - __clz(static_cast<int>(span))) : 32;
+    }
+}
+
+// ---------------------------------------------------------------- radix passes
+// Digits of a value with b significant bits (b = 32 for raw keys): pass 1 the
+// top 11 (bits b-11 .. b-1), pass 2 the next 11, pass 3 the rest (<= 10).
+__device__ __forceinline__ int digit_shift(int pass, int b)
+{
+    return pass == 1 ? max(b - 11, 0) : pass == 2 ? max(b - 22, 0) : 0;
+}
+
+template <int PASS>
+constexpr int pass_bins() { return PASS == 3 ? MON_BINS3 : MON_BINS2; }
+
+template <int PASS>
+constexpr int pass_smem_words()
+{
+    return PASS == 1 ? MON_QUANTILES * MON_BINS1 : MON_TARGETS * pass_bins<PASS>();
+}
+
+// Does v carry the digits that `prefix` fixed in the passes before PASS?
+template <int PASS>
+__device__ __forceinline__ bool in_prefix(uint32_t v, uint32_t prefix, int b)
+{
+    if (PASS == 1)
+        return true;
+    const int s = digit_shift(PASS - 1, b);
+    return (static_cast<uint64_t>(v) >> s) == (static_cast<uint64_t>(prefix) >> s);
+}
+
+template <int PASS>
+__device__ __forceinline__ uint32_t digit_of(uint32_t v, int b)
+{
+    const int s = digit_shift(PASS, b);
+    const int top = PASS == 1 ? b : digit_shift(PASS - 1, b);
+    const int width = top - s;   // <= 11
+    return (v >> s) & ((1u << width) - 1u);
+}
+
+template <int PASS>
+__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(const MonArgs a)
+{
+    constexpr int NB = pass_bins<PASS>();
+    extern __shared__ __align__(16) uint32_t mon_sh[];
+    __shared__ uint32_t pref_s[MON_TARGETS], lo_s[MON_QUANTILES];
+    __shared__ int bits_s[MON_QUANTILES];
+    __shared__ int mode_s;   // 0 nothing to do, 1 the collected lists, 2 all tokens
+    __shared__ unsigned long long cnt_s[MON_QUANTILES];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS)
+        mon_sh[i] = 0u;
+    pdl_wait();
+    pdl_launch_dependents();
+    MonState *st = a.st;
+    if (tid < MON_TARGETS)
+        pref_s[tid] = st->prefix[tid];
+    if (tid < MON_QUANTILES) {
+        lo_s[tid] = st->lo[tid];
+        bits_s[tid] = st->span_bits[tid];
+        cnt_s[tid] = std::min<unsigned long long>(st->count[tid], a.cap);
+    }
+    if (tid == 0)
+        mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
+    __syncthreads();
+    if (mode_s == 0)   // uniform over the CTA
+        return;
+    if (mode_s == 1) {
+        // the collected keys of the four lists, one list after another
+        const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
+        for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i < total;
+             i += static_cast<unsigned long long>(gridDim.x) * MON_THREADS) {
+            int q = 0;
+            unsigned long long off = i;
+            while (off >= cnt_s[q]) {   // ends at q <= 3 because i < total
+                off -= cnt_s[q];
+                ++q;
+            }
+            const uint32_t v = a.cand[static_cast<size_t>(q) * a.cap + off] - lo_s[q];
+            const int b = bits_s[q];
+            if (PASS == 1) {
+                atomicAdd(mon_sh + q * MON_BINS1 + digit_of<1>(v, b), 1u);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 2 * q + e;
+                    if (in_prefix<PASS>(v, pref_s[j], b))
+                        atomicAdd(mon_sh + j * NB + digit_of<PASS>(v, b), 1u);
+                }
+            }
+        }
+    } else {
+        uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
+#pragma unroll
+        for (int j = 0; j < MON_TARGETS; ++j)
+            pr[j] = pref_s[j];
+        for_token_groups(a, [&](int64_t, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool used = valid[i] && usable(m[i], d[i]);
+                const uint32_t kd = key_signed(d[i]);
+                if (PASS == 1) {
+                    if (used)   // delta's key only; |delta|'s histogram follows (mon_select_kernel<1>)
+                        atomicAdd(mon_sh + (kd >> 21), 1u);
+                } else {
+                    const uint32_t ka = key_abs(d[i]);
+#pragma unroll
+                    for (int j = 0; j < MON_TARGETS; ++j) {
+                        const uint32_t k = j < 2 ? ka : kd;
+                        if (used && in_prefix<PASS>(k, pr[j], 32))
+                            atomicAdd(mon_sh + j * NB + digit_of<PASS>(k, 32), 1u);
+                    }
+                }
+            }
+        });
+    }
+    __syncthreads();
     uint32_t *gh = PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 : a.hist3;
-    for (int i = tid; i < P::NH * P::NB; i += MON_THREADS) {
+    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS) {
         const uint32_t c = mon_sh[i];
         if (c != 0u)
             atomicAdd(gh + i, c);
     }
 }
 
-// Per target (warp j): the bin of the current pass that holds the target's
-// rank, and the rank left inside it.  PASS 1 first turns n_used into ranks;
-// PASS 3 then writes the record.  One CTA of MON_TARGETS warps.
+// Per target (warp j): the bin of pass PASS that holds the target's rank, and
+// the rank left inside it; PASS 3 then writes the record.  One CTA of
+// MON_TARGETS warps.
 template <int PASS>
 __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonArgs a)
 {
-    using P = PassShape<PASS>;
-    const int tid = threadIdx.x, lane = tid & 31, j = tid >> 5;
+    constexpr int NB = pass_bins<PASS>();
+    const int tid = threadIdx.x, lane = tid & 31, j = tid >> 5, q = j >> 1;
     MonState *st = a.st;
-    pdl_wait();   // the histograms come from mon_pass_kernel<PASS>
+    pdl_wait();
     pdl_launch_dependents();
-    if (PASS == 1) {
-        if (tid == 0) {
-            const long long n = static_cast<long long>(st->n_used);
-            st->empty = n == 0;
-            for (int i = 0; i < MON_TARGETS / 2 && n > 0; ++i) {
-                const double h = static_cast<double>(n - 1) * level(i);
-                const double fl = floor(h);
-                const long long k = static_cast<long long>(fl);
-                st->rank[2 * i] = k;
-                st->rank[2 * i + 1] = k + 1 < n ? k + 1 : k;
-                st->frac[i] = h - fl;
-            }
-        }
-        __syncthreads();
-    }
     if (!st->empty) {
-        // Pass 1 counted delta's key only.  |delta| has a clear top bit, and
-        // its bin b holds the positive deltas of delta-bin 1024 + b and the
-        // negative ones of delta-bin 1023 - b (the sign-flipped key).
-        const bool abs1 = PASS == 1 && j < 2;
-        const uint32_t *h = PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 + j * P::NB : a.hist3 + j * P::NB;
-        auto count = [&](int b) -> long long {
-            return abs1 ? static_cast<long long>(h[1024 + b]) + h[1023 - b] : static_cast<long long>(h[b]);
+        const bool all_tokens = st->fallback != 0;
+        const int b = all_tokens ? 32 : st->span_bits[q];
+        // The all-token pass 1 counted delta's key only.  |delta| has a clear
+        // top bit, and its bin c holds the positive deltas of delta-bin
+        // 1024 + c and the negative ones of delta-bin 1023 - c.
+        const bool abs1 = PASS == 1 && all_tokens && j < 2;
+        const uint32_t *h = PASS == 1 ? a.hist1 + (all_tokens ? 0 : q * MON_BINS1)
+                          : PASS == 2 ? a.hist2 + j * NB
+                                      : a.hist3 + j * NB;
+        auto count = [&](int c) -> long long {
+            return abs1 ? static_cast<long long>(h[1024 + c]) + h[1023 - c] : static_cast<long long>(h[c]);
         };
         const long long r = st->rank[j];
-        const int SEG = (abs1 ? 1024 : P::NB) / 32;   // bins per lane
+        const int SEG = (abs1 ? 1024 : NB) / 32;   // bins per lane
         long long c = 0;
-        for (int b = 0; b < SEG; ++b)
-            c += count(lane * SEG + b);
-        long long incl = c;   // inclusive prefix over lanes
+        for (int x = 0; x < SEG; ++x)
+            c += count(lane * SEG + x);
+        long long incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const long long v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -255,10 +503,10 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
             const int L = __ffs(hit) - 1;
             if (lane == L) {
                 long long cum = incl - c;
-                for (int b = 0; b < SEG; ++b) {
-                    const long long hb = count(lane * SEG + b);
+                for (int x = 0; x < SEG; ++x) {
+                    const long long hb = count(lane * SEG + x);
                     if (cum + hb > r) {
-                        bin = lane * SEG + b;
+                        bin = lane * SEG + x;
                         before = cum;
                         break;
                     }
@@ -274,7 +522,7 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
                 st->empty = 1;
             } else {
                 st->rank[j] = r - before;
-                st->prefix[j] |= static_cast<uint32_t>(bin) << P::SHIFT;
+                st->prefix[j] |= static_cast<uint32_t>(bin) << digit_shift(PASS, b);
             }
         }
     }
@@ -293,12 +541,15 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
         o[TIM_MON_P95_ABS_DELTA] = o[TIM_MON_RATIO_Q01] = o[TIM_MON_RATIO_Q50] = o[TIM_MON_RATIO_Q99] = nan;
         return;
     }
-    const double a0 = __uint_as_float(st->prefix[0]), a1 = __uint_as_float(st->prefix[1]);
+    uint32_t key[MON_TARGETS];
+    for (int t = 0; t < MON_TARGETS; ++t)
+        key[t] = st->fallback ? st->prefix[t] : st->lo[t >> 1] + st->prefix[t];
+    const double a0 = __uint_as_float(key[0]), a1 = __uint_as_float(key[1]);
     o[TIM_MON_P95_ABS_DELTA] = a0 + st->frac[0] * (a1 - a0);
     const int field[3] = {TIM_MON_RATIO_Q01, TIM_MON_RATIO_Q50, TIM_MON_RATIO_Q99};
-    for (int i = 1; i < MON_TARGETS / 2; ++i) {
-        const double r0 = expf(unkey_signed(st->prefix[2 * i]));
-        const double r1 = expf(unkey_signed(st->prefix[2 * i + 1]));
+    for (int i = 1; i < MON_QUANTILES; ++i) {
+        const double r0 = expf(unkey_signed(key[2 * i]));
+        const double r1 = expf(unkey_signed(key[2 * i + 1]));
         o[field[i - 1]] = r0 + st->frac[i] * (r1 - r0);
     }
 }
@@ -317,35 +568,48 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+constexpr size_t kSampleSmem = 4 * (SBD + SBA);
+
 } // namespace
 
 cudaError_t monitor_prepare_device()
 {
-    cudaError_t e = cudaFuncSetAttribute(mon_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         pass_smem_bytes<1>());
+    cudaError_t e = cudaFuncSetAttribute(mon_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSampleSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 4 * pass_smem_words<1>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mon_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 pass_smem_bytes<2>());
+                                 4 * pass_smem_words<2>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mon_pass_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 pass_smem_bytes<3>());
+                                 4 * pass_smem_words<3>());
     return e;
 }
 
 cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
 {
-    cudaError_t e = cudaMemsetAsync(a.st, 0, MON_WORKSPACE_BYTES, stream);
+    cudaError_t e = cudaMemsetAsync(a.st, 0, MON_ZEROED_BYTES, stream);
     if (e != cudaSuccess)
         return e;
     const int64_t groups = (a.N + 3) / 4;
     const int64_t want = (groups + MON_THREADS - 1) / MON_THREADS;
-    const dim3 grid(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
+    const dim3 grid(static_cast<unsigned>(
+        std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
+    const int64_t runs = std::max<int64_t>(
+        1, std::min<int64_t>(MON_SAMPLE_RUNS, (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN));
     const dim3 block(MON_THREADS), sel(MON_TARGETS * 32);
-    if ((e = launch_pdl(mon_pass_kernel<1>, grid, block, pass_smem_bytes<1>(), stream, a)) != cudaSuccess ||
+    if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(runs)), block, kSampleSmem, stream, a)) !=
+            cudaSuccess ||
+        (e = launch_pdl(mon_bounds_kernel, dim3(1), dim3(1024), 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_scan_kernel, grid, block, 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_check_kernel, dim3(1), dim3(32), 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_pass_kernel<1>, grid, block, 4 * pass_smem_words<1>(), stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_select_kernel<1>, dim3(1), sel, 0, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<2>, grid, block, pass_smem_bytes<2>(), stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_pass_kernel<2>, grid, block, 4 * pass_smem_words<2>(), stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_select_kernel<2>, dim3(1), sel, 0, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<3>, grid, block, pass_smem_bytes<3>(), stream, a)) != cudaSuccess)
+        (e = launch_pdl(mon_pass_kernel<3>, grid, block, 4 * pass_smem_words<3>(), stream, a)) != cudaSuccess)
         return e;
     return launch_pdl(mon_select_kernel<3>, dim3(1), sel, 0, stream, a);
 }

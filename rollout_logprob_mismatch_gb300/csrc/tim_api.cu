@@ -554,7 +554,7 @@ int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, con
         return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, tim::MON_WORKSPACE_BYTES, dev->pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, tim::monitor_workspace_bytes(N), dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(monitor workspace)");
     tim::MonArgs a;
@@ -569,6 +569,9 @@ int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, con
     a.hist1 = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + tim::MON_STATE_BYTES);
     a.hist2 = a.hist1 + tim::MON_HIST1_WORDS;
     a.hist3 = a.hist2 + tim::MON_HIST2_WORDS;
+    a.shist = a.hist3 + tim::MON_HIST3_WORDS;
+    a.cand = a.shist + tim::MON_SHIST_WORDS;
+    a.cap = tim::monitor_cap(N);
     a.status = dev->status;
     e = tim::monitor_launch(a, dev->sms, s);
     cudaError_t ef = cudaFreeAsync(ws, s);

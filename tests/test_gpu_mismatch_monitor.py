@@ -113,3 +113,23 @@ def test_full_size_batch():
     tau = float(np.float32(0.05))
     g, rej = gpu_monitor(lo, lr, mask, tau)
     assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^27")
+
+
+def test_sample_that_misses_the_bulk_and_mass_ties():
+    """Batches larger than the 2^20-token sample where the sample misleads:
+    the sampled runs (the first 1024 of every 2048 tokens at N = 2^21) hold
+    delta = 0 and the rest delta = 1, so the quantiles lie outside the sample's
+    bounds; and a batch of identical deltas, so the collected list overflows.
+    Both take the selection over all tokens and stay exact."""
+    N = 1 << 21
+    rng = np.random.default_rng(9)
+    lr = wl.draw_train_logprobs(N, 9)
+    t = np.arange(N)
+    lt = (lr + np.where((t % 2048) < 1024, np.float32(0.0), np.float32(1.0))).astype(np.float32)
+    mask = (rng.random(N) < 0.9).astype(np.uint8)
+    tau = float(np.float32(0.5))
+    g, rej = gpu_monitor(lt, lr, mask, tau)
+    assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, tau), "misleading sample")
+    same = lr.copy()
+    g2, rej2 = gpu_monitor(same, lr, np.ones(N, np.uint8), tau)
+    assert_monitor_match(g2, rej2, oracle.mismatch_monitor(same, lr, np.ones(N, np.uint8), tau), "all ties")
