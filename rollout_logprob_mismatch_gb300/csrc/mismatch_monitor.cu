@@ -71,8 +71,8 @@ __device__ __forceinline__ bool usable(bool m, float d) { return m && fabsf(d) <
 
 // Tokens of a grid-stride pass in 4-token groups g (16-byte loads; the ragged
 // last group by plain loads).  Calls f(g, d[4], m[4], valid[4]) on every lane
-// of the warp, MON_UNROLL groups loaded before the first use.
-template <typename F>
+// of the warp, UNROLL groups loaded before the first use.
+template <int UNROLL, typename F>
 __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -81,11 +81,11 @@ __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
     const int64_t full = N >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * MON_THREADS;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * MON_THREADS + warp * 32; base < G;
-         base += stride * MON_UNROLL) {   // uniform over the warp
-        float4 lt[MON_UNROLL], lr[MON_UNROLL];
-        uint32_t mk[MON_UNROLL];
+         base += stride * UNROLL) {   // uniform over the warp
+        float4 lt[UNROLL], lr[UNROLL];
+        uint32_t mk[UNROLL];
 #pragma unroll
-        for (int u = 0; u < MON_UNROLL; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int64_t g = base + lane + u * stride;
             if (g < full) {
                 lt[u] = __ldcs(reinterpret_cast<const float4 *>(a.l_tr) + g);
@@ -105,14 +105,15 @@ __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
             }
         }
 #pragma unroll
-        for (int u = 0; u < MON_UNROLL; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int64_t g = base + lane + u * stride;
             const float d[4] = {__fsub_rn(lt[u].x, lr[u].x), __fsub_rn(lt[u].y, lr[u].y),
                                 __fsub_rn(lt[u].z, lr[u].z), __fsub_rn(lt[u].w, lr[u].w)};
             bool m[4], valid[4];
+            const bool whole = g < full;   // all four tokens exist
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                valid[i] = g < G && 4 * g + i < N;
+                valid[i] = whole || (g < G && 4 * g + i < N);
                 m[i] = ((mk[u] >> (8 * i)) & 0xffu) != 0u;
             }
             f(g, d, m, valid);
@@ -121,9 +122,9 @@ __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
 }
 
 // ---------------------------------------------------------------- sample
-// CTA r histograms run r: tokens [s, s + MON_SAMPLE_RUN), s = r N / runs (runs
-// back to back when they cover the batch), in shared memory; the non-zero
-// bins are added to the global histograms.
+// Run r: tokens [s, s + MON_SAMPLE_RUN), s = r N / runs (runs back to back
+// when they cover the batch); CTA c takes runs c, c + gridDim, ... into
+// shared-memory histograms and adds the non-zero bins to the global ones.
 __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
 {
     extern __shared__ __align__(16) uint32_t sh[];   // [SBD] delta, then [SBA] |delta|
@@ -135,16 +136,18 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
     pdl_launch_dependents();
     const int64_t N = a.N;
     const int64_t cover = static_cast<int64_t>(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN;
-    const int64_t s0 = N <= cover ? static_cast<int64_t>(blockIdx.x) * MON_SAMPLE_RUN
-                                  : static_cast<int64_t>(blockIdx.x) * N / gridDim.x;
-    const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
+    const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
     int used = 0;
-    for (int64_t t = s0 + tid; t < s1; t += MON_THREADS) {
-        const float d = __fsub_rn(a.l_tr[t], a.l_ro[t]);
-        if (usable(a.mask[t] != 0, d)) {
-            atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
-            atomicAdd(sh + SBD + (key_abs(d) >> SAMPLE_SHIFT), 1u);
-            ++used;
+    for (int64_t r = blockIdx.x; r < runs; r += gridDim.x) {
+        const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN : r * N / runs;
+        const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
+        for (int64_t t = s0 + tid; t < s1; t += MON_THREADS) {
+            const float d = __fsub_rn(a.l_tr[t], a.l_ro[t]);
+            if (usable(a.mask[t] != 0, d)) {
+                atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
+                atomicAdd(sh + SBD + (key_abs(d) >> SAMPLE_SHIFT), 1u);
+                ++used;
+            }
         }
     }
     used = __reduce_add_sync(0xffffffffu, used);
@@ -165,27 +168,31 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
 // second (all ones when at or above the sample's last).
 __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
 {
+    extern __shared__ __align__(16) uint32_t hs[];   // the sample histograms, copied with coalesced loads
     __shared__ long long wsum[32];
     __shared__ int bin_s[2 * MON_QUANTILES];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_launch_dependents();
     MonState *st = a.st;
+    __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
     const long long m = static_cast<long long>(st->sample_used);
-    long long rlo[MON_QUANTILES], rhi[MON_QUANTILES];
-#pragma unroll
-    for (int q = 0; q < MON_QUANTILES; ++q) {
-        const double L = level(q);
+    if (tid < MON_QUANTILES) {   // fp64 in a few threads only: GB300 runs it slowly
+        const double L = level(tid);
         const double j = static_cast<double>(m - 1) * L;
         const long long w = static_cast<long long>(ceil(kSigmas * sqrt(static_cast<double>(m) * L * (1.0 - L)))) + 2;
-        rlo[q] = static_cast<long long>(floor(j)) - w;
-        rhi[q] = static_cast<long long>(ceil(j)) + w;
+        rlo_s[tid] = static_cast<long long>(floor(j)) - w;
+        rhi_s[tid] = static_cast<long long>(ceil(j)) + w;
     }
     if (tid < 2 * MON_QUANTILES)
         bin_s[tid] = -1;
+#pragma unroll 24
+    for (int i = tid; i < SBD + SBA; i += 1024)
+        hs[i] = a.shist[i];
+    __syncthreads();
     for (int kind = 0; kind < 2; ++kind) {   // 0: delta (quantiles 1..3), 1: |delta| (quantile 0)
         const int nb = kind == 0 ? SBD : SBA;
-        const uint32_t *h = a.shist + (kind == 0 ? 0 : SBD);
+        const uint32_t *h = hs + (kind == 0 ? 0 : SBD);
         const int per = nb / 1024;
         long long c = 0;
         for (int b = 0; b < per; ++b)
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
         const int q_first = kind == 0 ? 1 : 0, q_end = kind == 0 ? MON_QUANTILES : 1;
         for (int q = q_first; q < q_end; ++q) {
             for (int e = 0; e < 2; ++e) {
-                const long long R = e == 0 ? rlo[q] : rhi[q];
+                const long long R = e == 0 ? rlo_s[q] : rhi_s[q];
                 if (m > 0 && R > 0 && R < m - 1 && excl <= R && R < excl + c) {
                     long long cum = excl;
                     for (int b = 0; b < per; ++b) {
@@ -232,10 +239,27 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
 }
 
 // ---------------------------------------------------------------- the full pass
+// Collected keys are staged per warp and quantile in shared memory and go to
+// the global list 32 at a time (one atomic reservation per 32 keys).  (A
+// private buffer per thread, without the warp-wide ballot, was measured 2.3x
+// slower: its appends and flushes diverge inside the warp.)
+constexpr int kStage = 64;
+
+__device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane)
+{
+    unsigned long long base = 0;
+    if (lane == 0)
+        base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(n));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (lane < n && base + lane < a.cap)
+        a.cand[static_cast<size_t>(q) * a.cap + base + lane] = buf[lane];
+}
+
 __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(const MonArgs a)
 {
     __shared__ uint32_t lo_s[MON_QUANTILES], span_s[MON_QUANTILES];
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ uint32_t stage_s[MON_THREADS / 32][MON_QUANTILES][kStage];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_launch_dependents();
     if (tid < MON_QUANTILES) {
@@ -249,11 +273,11 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
         lo[q] = lo_s[q];
         span[q] = span_s[q];
     }
-    const unsigned long long cap = a.cap;
     const unsigned lt_mask = (1u << lane) - 1u;
     int n_used = 0, n_ext = 0;
+    int staged[MON_QUANTILES] = {0, 0, 0, 0};   // uniform over the warp
     int below[MON_QUANTILES] = {0, 0, 0, 0};
-    for_token_groups(a, [&](int64_t g, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
+    for_token_groups<2>(a, [&](int64_t g, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
         uint32_t flags = 0u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -270,14 +294,20 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                 const bool in = used && k - lo[q] <= span[q];
                 const unsigned bal = __ballot_sync(0xffffffffu, in);
                 if (bal != 0u) {   // uniform over the warp
-                    const int leader = __ffs(bal) - 1;
-                    unsigned long long base = 0;
-                    if (lane == leader)
-                        base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(__popc(bal)));
-                    base = __shfl_sync(0xffffffffu, base, leader);
-                    const unsigned long long pos = base + static_cast<unsigned>(__popc(bal & lt_mask));
-                    if (in && pos < cap)
-                        a.cand[static_cast<size_t>(q) * cap + pos] = k;
+                    uint32_t *buf = stage_s[warp][q];
+                    if (in)
+                        buf[staged[q] + __popc(bal & lt_mask)] = k;
+                    staged[q] += __popc(bal);
+                    if (staged[q] >= 32) {
+                        __syncwarp();
+                        flush_stage(a, buf, q, 32, lane);
+                        const uint32_t rest = lane + 32 < staged[q] ? buf[lane + 32] : 0u;
+                        __syncwarp();
+                        if (lane + 32 < staged[q])
+                            buf[lane] = rest;
+                        __syncwarp();
+                        staged[q] -= 32;
+                    }
                 }
             }
         }
@@ -289,6 +319,11 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                     a.reject[4 * g + i] = static_cast<uint8_t>((flags >> (8 * i)) & 1u);
         }
     });
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q)
+        if (staged[q] > 0)
+            flush_stage(a, stage_s[warp][q], q, staged[q], lane);
     const int wu = __reduce_add_sync(0xffffffffu, n_used);
     const int we = __reduce_add_sync(0xffffffffu, n_ext);
     int wb[MON_QUANTILES];
@@ -385,8 +420,6 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
     __shared__ int mode_s;   // 0 nothing to do, 1 the collected lists, 2 all tokens
     __shared__ unsigned long long cnt_s[MON_QUANTILES];
     const int tid = threadIdx.x;
-    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS)
-        mon_sh[i] = 0u;
     pdl_wait();
     pdl_launch_dependents();
     MonState *st = a.st;
@@ -400,11 +433,15 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
     if (tid == 0)
         mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
     __syncthreads();
-    if (mode_s == 0)   // uniform over the CTA
+    const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
+    // uniform over the CTA: nothing to select, or no collected key for this CTA
+    if (mode_s == 0 || (mode_s == 1 && static_cast<unsigned long long>(blockIdx.x) * MON_THREADS >= total))
         return;
+    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS)
+        mon_sh[i] = 0u;
+    __syncthreads();
     if (mode_s == 1) {
         // the collected keys of the four lists, one list after another
-        const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
         for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i < total;
              i += static_cast<unsigned long long>(gridDim.x) * MON_THREADS) {
             int q = 0;
@@ -431,7 +468,7 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
 #pragma unroll
         for (int j = 0; j < MON_TARGETS; ++j)
             pr[j] = pref_s[j];
-        for_token_groups(a, [&](int64_t, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
+        for_token_groups<MON_UNROLL>(a, [&](int64_t, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const bool used = valid[i] && usable(m[i], d[i]);
@@ -467,6 +504,7 @@ template <int PASS>
 __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonArgs a)
 {
     constexpr int NB = pass_bins<PASS>();
+    extern __shared__ __align__(16) uint32_t hist_s[];   // each warp's histogram, copied with coalesced loads
     const int tid = threadIdx.x, lane = tid & 31, j = tid >> 5, q = j >> 1;
     MonState *st = a.st;
     pdl_wait();
@@ -478,9 +516,14 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
         // top bit, and its bin c holds the positive deltas of delta-bin
         // 1024 + c and the negative ones of delta-bin 1023 - c.
         const bool abs1 = PASS == 1 && all_tokens && j < 2;
-        const uint32_t *h = PASS == 1 ? a.hist1 + (all_tokens ? 0 : q * MON_BINS1)
-                          : PASS == 2 ? a.hist2 + j * NB
-                                      : a.hist3 + j * NB;
+        const uint32_t *hg = PASS == 1 ? a.hist1 + (all_tokens ? 0 : q * MON_BINS1)
+                           : PASS == 2 ? a.hist2 + j * NB
+                                       : a.hist3 + j * NB;
+        uint32_t *h = hist_s + j * 2048;
+#pragma unroll 16
+        for (int x = lane; x < NB; x += 32)
+            h[x] = hg[x];
+        __syncwarp();
         auto count = [&](int c) -> long long {
             return abs1 ? static_cast<long long>(h[1024 + c]) + h[1023 - c] : static_cast<long long>(h[c]);
         };
@@ -569,6 +612,7 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 constexpr size_t kSampleSmem = 4 * (SBD + SBA);
+constexpr size_t kSelectSmem = 4 * MON_TARGETS * 2048;
 
 } // namespace
 
@@ -576,6 +620,18 @@ cudaError_t monitor_prepare_device()
 {
     cudaError_t e = cudaFuncSetAttribute(mon_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSampleSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_bounds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSampleSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSelectSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSelectSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_select_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSelectSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mon_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  4 * pass_smem_words<1>());
@@ -598,20 +654,21 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
     const dim3 grid(static_cast<unsigned>(
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
     const int64_t runs = std::max<int64_t>(
-        1, std::min<int64_t>(MON_SAMPLE_RUNS, (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN));
+        1, std::min<int64_t>({static_cast<int64_t>(MON_SAMPLE_RUNS), (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN,
+                              2LL * num_sms}));
     const dim3 block(MON_THREADS), sel(MON_TARGETS * 32);
     if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(runs)), block, kSampleSmem, stream, a)) !=
             cudaSuccess ||
-        (e = launch_pdl(mon_bounds_kernel, dim3(1), dim3(1024), 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_bounds_kernel, dim3(1), dim3(1024), kSampleSmem, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_scan_kernel, grid, block, 0, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_check_kernel, dim3(1), dim3(32), 0, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_pass_kernel<1>, grid, block, 4 * pass_smem_words<1>(), stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_select_kernel<1>, dim3(1), sel, 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_select_kernel<1>, dim3(1), sel, kSelectSmem, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_pass_kernel<2>, grid, block, 4 * pass_smem_words<2>(), stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_select_kernel<2>, dim3(1), sel, 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_select_kernel<2>, dim3(1), sel, kSelectSmem, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_pass_kernel<3>, grid, block, 4 * pass_smem_words<3>(), stream, a)) != cudaSuccess)
         return e;
-    return launch_pdl(mon_select_kernel<3>, dim3(1), sel, 0, stream, a);
+    return launch_pdl(mon_select_kernel<3>, dim3(1), sel, kSelectSmem, stream, a);
 }
 
 } // namespace tim
