@@ -48,12 +48,12 @@ K2_BW_TOKENS = 1 << 27
 # only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
 # profiles/k2_seq_kernel_2e25_tokens.md).
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3108941568 read + 18808064 written
-    ("k1", "8bd6dd5c4abb13b7"): 3108941568 + 18808064,
-    # mismatch pass, 2^25 tokens: 305358080 read + 98499584 written (traffic scales with tokens)
-    ("k2", "1ede8711c418a02e"): 305358080 + 98499584,
-    # TIS-weighted PPO surrogate, 2^25 tokens: 612692224 read + 216128768 written (scales with tokens)
-    ("ppo", "e67331ce7a3218ab"): 612692224 + 216128768,
+    # token logprob, N = 8192, D = 4096, V = 151936: 3094851328 read + 17677056 written
+    ("k1", "c81857fc1e640542"): 3094851328 + 17677056,
+    # mismatch pass, 2^25 tokens: 305308672 read + 98471936 written (traffic scales with tokens)
+    ("k2", "bc64a1d1ce079e05"): 305308672 + 98471936,
+    # TIS-weighted PPO surrogate, 2^25 tokens: 613021696 read + 216199424 written (scales with tokens)
+    ("ppo", "53e498ff1e920547"): 613021696 + 216199424,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 PPO_TRAFFIC_TOKENS = 1 << 25
