@@ -66,8 +66,8 @@ FLUSH_BYTES = 1 << 30
 def source_hash(kind: str) -> str:
     import hashlib
     d = os.path.join(ROOT, "rollout_logprob_mismatch_gb300", "csrc")
-    files = {"k1": ("k1_token_logprob.cu", "tim_ptx.cuh", "tim_internal.h"),
-             "k2": ("k2_mismatch_stats.cu", "tim_ptx.cuh", "tim_internal.h"),
+    files = {"k1": ("k1_token_logprob.cu", "k1_internal.h", "tim_ptx.cuh", "tim_internal.h"),
+             "k2": ("k2_mismatch_stats.cu", "k2_internal.h", "tim_ptx.cuh", "tim_internal.h"),
              "ppo": ("tis_ppo.cu", "ppo_internal.h", "tim_ptx.cuh", "tim_internal.h")}[kind]
     m = hashlib.sha1()
     for f in files:

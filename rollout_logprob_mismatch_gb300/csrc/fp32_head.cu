@@ -19,6 +19,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "k1_internal.h"
 #include "tim_internal.h"
 
 namespace tim {

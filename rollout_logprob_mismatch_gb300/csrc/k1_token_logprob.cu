@@ -29,6 +29,7 @@
 
 #include <cuda_bf16.h>
 
+#include "k1_internal.h"
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
 #include "../../include/tim.h"

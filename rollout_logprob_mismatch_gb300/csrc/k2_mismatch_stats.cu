@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <cfloat>
 
+#include "k2_internal.h"
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
 #include "../../include/tim.h"

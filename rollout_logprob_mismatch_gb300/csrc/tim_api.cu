@@ -13,6 +13,8 @@
 #include "../../include/tim.h"
 #include "monitor_internal.h"
 #include "ppo_internal.h"
+#include "k1_internal.h"
+#include "k2_internal.h"
 #include "tim_internal.h"
 
 namespace {

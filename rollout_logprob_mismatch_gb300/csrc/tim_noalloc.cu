@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/tim.h"
+#include "k1_internal.h"
 #include "tim_internal.h"
 
 namespace {
