@@ -190,3 +190,27 @@ def test_bad_offsets_are_reported_not_trapped():
     # the status word is cleared by the check: a good call afterwards is clean
     tim.mismatch_stats(l, l, m, _dev(np.array([0, 10], np.int32)))
     tim.check()
+
+
+def test_many_sequences_take_the_two_level_fold():
+    """5000 short sequences: more than one fold CTA (1024 sequences each), so
+    the partials go through the final fold kernel."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 40, size=5000)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(off[-1])
+    l_tr = wl.draw_train_logprobs(N, 21)
+    l_ro = (l_tr + rng.normal(0, 0.05, N)).astype(np.float32)
+    mask = (rng.random(N) < 0.8).astype(np.uint8)
+    gs, o = run_both(l_tr, l_ro, mask, off)
+    check_all(gs, o)
+
+
+def test_full_size_bandwidth_batch():
+    """The bandwidth measurement's size: 2^27 tokens in ~116k lognormal
+    sequences (median 1024, clipped to [128, 4096]), 30% masked, weights
+    written, in the same launch configuration; every record against the
+    oracle."""
+    off, mask, _, l_tr, l_ro, _ = wl.draw_ppo_inputs(1 << 27, 22)
+    gs, o = run_both(l_tr, l_ro, mask, off)
+    check_all(gs, o)
