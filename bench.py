@@ -48,12 +48,12 @@ K2_BW_TOKENS = 1 << 27
 # only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
 # profiles/k2_seq_kernel_2e25_tokens.md).
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3094851328 read + 17677056 written
-    ("k1", "c81857fc1e640542"): 3094851328 + 17677056,
-    # mismatch pass, 2^25 tokens: 305308672 read + 98471936 written (traffic scales with tokens)
-    ("k2", "bc64a1d1ce079e05"): 305308672 + 98471936,
-    # TIS-weighted PPO surrogate, 2^25 tokens: 613021696 read + 216199424 written (scales with tokens)
-    ("ppo", "53e498ff1e920547"): 613021696 + 216199424,
+    # token logprob, N = 8192, D = 4096, V = 151936: 3115405568 read + 17896960 written
+    ("k1", "bff286e057c795d1"): 3115405568 + 17896960,
+    # mismatch pass, 2^25 tokens: 305287168 read + 98403840 written (traffic scales with tokens)
+    ("k2", "b52af0477f7a6c75"): 305287168 + 98403840,
+    # TIS-weighted PPO surrogate, 2^25 tokens: 612941056 read + 216222720 written (scales with tokens)
+    ("ppo", "aba850bed7b51939"): 612941056 + 216222720,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 PPO_TRAFFIC_TOKENS = 1 << 25
