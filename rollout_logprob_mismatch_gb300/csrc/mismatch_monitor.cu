@@ -495,8 +495,12 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
         mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
     __syncthreads();
     const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
+    // Collected keys: at least kKeysPerCta per CTA, so that few CTAs pay for
+    // clearing and adding their histograms; the others leave at once.
+    constexpr unsigned long long kKeysPerCta = 16 * MON_THREADS;
+    const unsigned long long ctas = std::min<unsigned long long>(gridDim.x, (total + kKeysPerCta - 1) / kKeysPerCta);
     // uniform over the CTA: nothing to select, or no collected key for this CTA
-    if (mode_s == 0 || (mode_s == 1 && static_cast<unsigned long long>(blockIdx.x) * MON_THREADS >= total))
+    if (mode_s == 0 || (mode_s == 1 && blockIdx.x >= ctas))
         return;
     for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS)
         mon_sh[i] = 0u;
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
     if (mode_s == 1) {
         // the collected keys of the four lists, one list after another
         for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i < total;
-             i += static_cast<unsigned long long>(gridDim.x) * MON_THREADS) {
+             i += ctas * MON_THREADS) {
             int q = 0;
             unsigned long long off = i;
             while (off >= cnt_s[q]) {   // ends at q <= 3 because i < total
