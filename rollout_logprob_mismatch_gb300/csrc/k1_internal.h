@@ -33,6 +33,12 @@ constexpr uint32_t K1_SMEM_BYTES = K1_STAGES * K1_STAGE_BYTES + K1_BAR_BYTES + 1
 
 inline int64_t k1_num_chunks(int64_t V) { return (V + K1_VCHUNK - 1) / K1_VCHUNK; }
 
+// TMA loads of an h tile run markedly slower (measured: 1.4x the whole call at
+// N = 1) when the tensor map's row count is not a multiple of 16, so the last
+// m-tile of such a batch is read from a zero-padded copy of K1_BM rows.
+constexpr int64_t K1_TAIL_ROWS_ALIGN = 16;
+inline bool k1_needs_tail_pad(int64_t N) { return N % K1_TAIL_ROWS_ALIGN != 0; }
+
 struct K1Args {
     const int32_t *targets;   // [N]
     float2 *part;             // [N][num_chunks]: per-chunk (max, sum of exp(z - max))
@@ -44,6 +50,7 @@ struct K1Args {
     int32_t num_m_tiles, num_chunks;
     int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
     int32_t band, units;      // units = num_m_groups * num_chunks, one per cluster
+    int32_t tail_mt;          // m-tile read through the padded tail map, or -1
     uint64_t wait_budget_ns;
     // backward (mode 1) only
     const float *grad;        // [N] upstream gradient of each l_t
@@ -54,8 +61,8 @@ struct K1Args {
 
 // Launches one cluster of K1_CLUSTER CTAs per unit, at most as many clusters
 // as fit on the device at once (persistent).  mode 0: forward; 1: backward dz.
-cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
-                           cudaStream_t stream, int mode = 0);
+cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const CUtensorMap &tmap_h_tail,
+                           const K1Args &a, cudaStream_t stream, int mode = 0);
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream);

@@ -83,7 +83,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 template <int MODE>
 __global__ void __launch_bounds__(K1_THREADS, 1)
     k1_main_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
-                   const K1Args a)
+                   const __grid_constant__ CUtensorMap tmap_h_tail, const K1Args a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_h);
+        if (a.tail_mt >= 0)
+            tma_prefetch_desc(&tmap_h_tail);
         tma_prefetch_desc(&tmap_w);
     }
     pdl_wait();                // h, W, targets may be written by the previous kernel
@@ -149,6 +151,11 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             for (int u = cid; ok && u < a.units; u += ncl) {
                 const Unit w = unit_of(u, a);
                 const int mt = w.mt * K1_CLUSTER + static_cast<int>(rank);
+                // the last m-tile of a batch whose size is not a multiple of 16 rows
+                // reads a zero-padded copy of its rows (same values, fast loads)
+                const bool tail = mt == a.tail_mt;
+                const CUtensorMap *hmap = tail ? &tmap_h_tail : &tmap_h;
+                const int hrow = tail ? 0 : mt * K1_BM;
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
                     const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
@@ -162,8 +169,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         // own h tile + this CTA's rows of the W tile, multicast to the whole
                         // cluster; the barrier counts the W rows the other CTAs send as well
                         mbar_arrive_expect_tx(full(stage), K1_STAGE_BYTES);
-                        tma_load_2d(sA + stage * K1_A_BYTES, &tmap_h, full(stage), kh * K1_BK, mt * K1_BM,
-                                    pol_h);
+                        tma_load_2d(sA + stage * K1_A_BYTES, hmap, full(stage), kh * K1_BK, hrow, pol_h);
                         if (++kh == KBH)
                             kh = 0;
                         tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / K1_CLUSTER),
@@ -454,7 +460,8 @@ cudaError_t k1_prepare_device()
     return e;
 }
 
-cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const K1Args &a,
+cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const CUtensorMap &tmap_h_tail,
+                           const K1Args &a,
                            cudaStream_t stream, int mode)
 {
     static int max_clusters[2][64] = {};   // per mode and device, found once (the same value from any thread)
@@ -488,7 +495,7 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
         static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[md][dev] : 1));
     cfg.gridDim = dim3(K1_CLUSTER * clusters, 1, 1);
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, a);
+    return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, tmap_h_tail, a);
 }
 
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,

@@ -140,6 +140,39 @@ int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, ui
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bytes of the padded copy of a batch's last m-tile (K1_BM rows of h).
+size_t tail_pad_bytes(int64_t N, int64_t D)
+{
+    return tim::k1_needs_tail_pad(N) ? round_up(static_cast<size_t>(tim::K1_BM) * D * 2, 256) : 0;
+}
+
+// When N is not a multiple of 16 rows, copies the last m-tile's rows of h into
+// `pad` (K1_BM rows, zero past N), maps it in *th_tail and names the m-tile in
+// *tail_mt (else *tail_mt = -1 and *th_tail = th).  The kernel reads the same
+// values either way: past N both give zeros.
+int tail_map(const void *h, int64_t N, int64_t D, void *pad, const CUtensorMap &th, cudaStream_t s,
+             CUtensorMap *th_tail, int32_t *tail_mt)
+{
+    *th_tail = th;
+    *tail_mt = -1;
+    if (!tim::k1_needs_tail_pad(N))
+        return TIM_OK;
+    const int64_t m_tiles = (N + tim::K1_BM - 1) / tim::K1_BM;
+    const int64_t r0 = (m_tiles - 1) * tim::K1_BM, rows = N - r0;
+    const size_t row_bytes = static_cast<size_t>(D) * 2;
+    cudaError_t e = cudaMemcpyAsync(pad, static_cast<const char *>(h) + r0 * row_bytes, rows * row_bytes,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(static_cast<char *>(pad) + rows * row_bytes, 0, (tim::K1_BM - rows) * row_bytes, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "tail pad copy");
+    const int rc = encode_bf16(th_tail, pad, tim::K1_BM, D, tim::K1_BM);
+    if (rc != TIM_OK)
+        return rc;
+    *tail_mt = static_cast<int32_t>(m_tiles - 1);
+    return TIM_OK;
+}
+
 // Rows of one backward chunk: the bf16 logit gradient of a chunk is rows x V
 // (1.2 GB at V = 151936); dh and dW are then two cuBLAS GEMMs per chunk.
 constexpr int64_t kBackwardRows = 4096;
@@ -258,11 +291,19 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
 
     const size_t part_bytes = round_up(static_cast<size_t>(chunks) * N * sizeof(float2), 256);
     const size_t za_bytes = round_up(static_cast<size_t>(N) * sizeof(float), 256);
+    const size_t pad_bytes = tail_pad_bytes(N, D);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + za_bytes, dev->pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + za_bytes + pad_bytes, dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(token_logprob workspace)");
+    CUtensorMap th_tail;
+    int32_t tail_mt = -1;
+    if ((rc = tail_map(h, N, D, static_cast<char *>(ws) + part_bytes + za_bytes, th, s, &th_tail, &tail_mt)) !=
+        TIM_OK) {
+        cudaFreeAsync(ws, s);
+        return rc;
+    }
 
     tim::K1Args a{};
     a.targets = targets;
@@ -282,7 +323,8 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
     a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();
-    e = tim::k1_launch_main(th, tw, a, s);
+    a.tail_mt = tail_mt;
+    e = tim::k1_launch_main(th, tw, th_tail, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
                                    s);
@@ -436,8 +478,10 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
     // rows in chunks of at most kBackwardRows: dz of one chunk, bf16 [rows][Vp]
     const int64_t Vp = (V + 7) / 8 * 8;
     const int64_t rows_max = std::min<int64_t>(kBackwardRows, (N + 255) / 256 * 256);
+    const size_t dz_bytes = round_up(static_cast<size_t>(rows_max) * Vp * 2, 256);
+    const size_t pad_bytes = round_up(static_cast<size_t>(tim::K1_BM) * D * 2, 256);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(rows_max) * Vp * 2, dev->pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, dz_bytes + pad_bytes, dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(backward workspace)");
     CUtensorMap tw;
@@ -450,8 +494,10 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
     for (int64_t r0 = 0; r0 < N && rc == TIM_OK; r0 += rows_max) {
         const int64_t n = std::min<int64_t>(rows_max, N - r0);
         const void *hc = static_cast<const uint16_t *>(h) + r0 * D;
-        CUtensorMap th;
-        if ((rc = encode_bf16(&th, hc, n, D, tim::K1_BM)) != TIM_OK)
+        CUtensorMap th, th_tail;
+        int32_t tail_mt = -1;
+        if ((rc = encode_bf16(&th, hc, n, D, tim::K1_BM)) != TIM_OK ||
+            (rc = tail_map(hc, n, D, static_cast<char *>(ws) + dz_bytes, th, s, &th_tail, &tail_mt)) != TIM_OK)
             break;
         const int64_t m_tiles = (n + tim::K1_BM - 1) / tim::K1_BM;
         const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
@@ -474,7 +520,8 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
         a.lse_in = lse + r0;
         a.dz = static_cast<uint16_t *>(ws);
         a.dz_ld = Vp;
-        if ((e = tim::k1_launch_main(th, tw, a, s, 1)) != cudaSuccess) {
+        a.tail_mt = tail_mt;
+        if ((e = tim::k1_launch_main(th, tw, th_tail, a, s, 1)) != cudaSuccess) {
             rc = cuda_fail(e, "backward dz launch");
             break;
         }

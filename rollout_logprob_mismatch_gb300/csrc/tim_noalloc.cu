@@ -187,7 +187,8 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.units = static_cast<int32_t>(m_groups * chunks);
     a.wait_budget_ns = wait_budget_ns();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = tim::k1_launch_main(th, tw, a, s);
+    a.tail_mt = -1;   // no room for a padded tail here: the same values through the plain map
+    cudaError_t e = tim::k1_launch_main(th, tw, th, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
                                    s);
