@@ -67,6 +67,8 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream);
 cudaError_t k1_prepare_device();   // per-device function attributes
+// Copies `rows` rows of h (D bf16 each, 16-byte aligned) into a K1_BM-row pad, zero past them.
+cudaError_t k1_launch_pad_tail(const void *src, int64_t rows, int64_t D, void *dst, cudaStream_t stream);
 
 // FP32 LM head: W fp32 [V, D] -> three bf16 parts [V][3][Dp], Dp = D rounded up
 // to K1_BK, padding zero; w = part0 + part1 + part2 exactly.

@@ -498,6 +498,26 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, tmap_h_tail, a);
 }
 
+// The padded last m-tile: rows [0, rows) of src copied, rows [rows, K1_BM) zero,
+// in 16-byte units (rows of D bf16, D % 8 == 0).
+__global__ void __launch_bounds__(256) k1_pad_tail_kernel(const uint4 *__restrict__ src, int64_t rows, int64_t D,
+                                                         uint4 *__restrict__ dst)
+{
+    const int64_t per_row = D / 8, total = static_cast<int64_t>(K1_BM) * per_row;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        dst[i] = i < rows * per_row ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+cudaError_t k1_launch_pad_tail(const void *src, int64_t rows, int64_t D, void *dst, cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(K1_BM) * (D / 8);
+    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 1024));
+    k1_pad_tail_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(src), rows, D,
+                                                   static_cast<uint4 *>(dst));
+    return cudaGetLastError();
+}
+
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
                               float *out_lse, cudaStream_t stream)

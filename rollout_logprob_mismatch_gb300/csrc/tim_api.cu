@@ -160,10 +160,7 @@ int tail_map(const void *h, int64_t N, int64_t D, void *pad, const CUtensorMap &
     const int64_t m_tiles = (N + tim::K1_BM - 1) / tim::K1_BM;
     const int64_t r0 = (m_tiles - 1) * tim::K1_BM, rows = N - r0;
     const size_t row_bytes = static_cast<size_t>(D) * 2;
-    cudaError_t e = cudaMemcpyAsync(pad, static_cast<const char *>(h) + r0 * row_bytes, rows * row_bytes,
-                                    cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemsetAsync(static_cast<char *>(pad) + rows * row_bytes, 0, (tim::K1_BM - rows) * row_bytes, s);
+    const cudaError_t e = tim::k1_launch_pad_tail(static_cast<const char *>(h) + r0 * row_bytes, rows, D, pad, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "tail pad copy");
     const int rc = encode_bf16(th_tail, pad, tim::K1_BM, D, tim::K1_BM);
