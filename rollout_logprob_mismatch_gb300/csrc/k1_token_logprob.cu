@@ -152,10 +152,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 const Unit w = unit_of(u, a);
                 const int mt = w.mt * K1_CLUSTER + static_cast<int>(rank);
                 // the last m-tile of a batch whose size is not a multiple of 16 rows
-                // reads a zero-padded copy of its rows (same values, fast loads)
-                const bool tail = mt == a.tail_mt;
+                // reads a zero-padded copy of its rows (same values, fast loads); an
+                // m-tile past the batch (the cluster peer of a last odd m-tile) reads
+                // past the end of that copy: zeros, again through a map of 16k rows
+                const bool tail = a.tail_mt >= 0 && mt >= a.tail_mt;
                 const CUtensorMap *hmap = tail ? &tmap_h_tail : &tmap_h;
-                const int hrow = tail ? 0 : mt * K1_BM;
+                const int hrow = tail ? (mt - a.tail_mt) * K1_BM : mt * K1_BM;
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
                     const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
