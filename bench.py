@@ -476,7 +476,7 @@ def run_gb300(args):
     cpu = None
     if world == 1 and not args.skip_cpu_baseline:
         v, desc, threads, _ = time_oracle(cfg, h, W, a, off, mask,
-                                          float(os.environ.get("TIM_BENCH_ORACLE_SECONDS", "12")))
+                                          float(os.environ.get("TIM_BENCH_ORACLE_SECONDS", "16")))
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
     peak = peaks["bf16_tflops"]
     line = {

@@ -147,3 +147,24 @@ def test_full_size_batch(tokens):
     _close(sub["token_grad"], o_sub["token_grad"], np.abs(o_sub["token_grad"]), "sampled token_grad")
     g_rest = {"token_loss": None, "token_grad": None, "seq_loss": g["seq_loss"], "batch": g["batch"]}
     assert_ppo_match(g_rest, o, off, "2^27")
+
+
+def test_four_byte_aligned_views():
+    """The surrogate needs 4-byte alignment only: inputs and outputs as views
+    that start one element into their buffers give the same bits as aligned
+    ones."""
+    off, mask, lt, lo, lr, A = ragged_batch([300, 9000, 41], 17)
+    N = int(off[-1])
+    def shifted(x, dtype):
+        buf = torch.zeros(N + 1, dtype=dtype, device="cuda")
+        buf[1:] = _dev(x)
+        return buf[1:]
+    args = [shifted(lt, torch.float32), shifted(lo, torch.float32), shifted(lr, torch.float32),
+            shifted(A, torch.float32), shifted(mask, torch.uint8), _dev(off)]
+    out = {"token_loss": torch.empty(N + 1, device="cuda")[1:], "token_grad": torch.empty(N + 1, device="cuda")[1:],
+           "seq_loss": torch.empty(len(off), device="cuda")[1:], "batch": torch.empty(9, dtype=torch.float64, device="cuda")}
+    tim.tis_ppo(*args, out=out)
+    tim.check()
+    g = gpu_ppo(lt, lo, lr, A, mask, off)
+    for k in ("token_loss", "token_grad", "seq_loss", "batch"):
+        assert np.array_equal(out[k].cpu().numpy().view(np.uint8), g[k].view(np.uint8)), k
