@@ -29,7 +29,7 @@ static_assert(K2_STAGE_BYTES % 16 == 0 && K2_BAR_BYTES % 16 == 0, "bulk-copy des
 inline size_t k2_workspace_bytes(int64_t S)
 {
     const int64_t parts = (S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
-    return static_cast<size_t>(S) * K2_REC_WORDS * 4 + static_cast<size_t>(parts) * K2_PART_WORDS * 4 + 512;
+    return static_cast<size_t>(S) * K2_REC_WORDS * 4 + static_cast<size_t>(parts) * K2_PART_WORDS * 4 + 256;
 }
 
 struct K2Args {
@@ -49,7 +49,6 @@ struct K2Args {
     double *batch;         // [20]
     uint32_t *rec;         // workspace: sequence records, [K2_REC_WORDS][S]
     uint32_t *part;        // workspace: fold partials, [ceil(S / K2_FOLD_SEQS)][K2_PART_WORDS]
-    unsigned *ticket;      // workspace: fold CTAs finished (zeroed by k2_seq_kernel)
     int *status;
 };
 

@@ -27,8 +27,8 @@
 //     bits wherever it is packed and whatever else is in the batch.
 //  2. k2_fold_kernel: CTA j folds sequences 1024 j .. 1024 j + 1023 (4 per
 //     thread, structure-of-arrays records, coalesced) with float-float (TwoSum)
-//     sums and integer counts in a fixed tree; with several CTAs the last one
-//     to finish folds their partials in index order.
+//     sums and integer counts in a fixed tree.
+//  3. k2_final_kernel (only when S > 1024): one CTA folds the partials in order.
 // The batch record depends on S and the sequence records only.
 #include <algorithm>
 #include <cfloat>
@@ -455,8 +455,6 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
         mine = mine || (offsets_ok(a, q, b, e) && e - b > K2_LONG);
     }
     const bool has_long = __syncthreads_or(mine) != 0;
-    if (blockIdx.x == 0 && tid == 0)
-        *a.ticket = 0u;   // the fold kernel reads it after this grid completes
     const uint64_t pol = l2_policy_evict_first();
     const uint64_t budget = a.wait_budget_ns;
     uint32_t parity = 0;    // bit i: parity of stage i's next completion
@@ -778,105 +776,77 @@ __device__ void write_batch(const K2Args &a, const FoldAcc &t, bool check_offset
             o[f] = __longlong_as_double(0x7ff8000000000000ll);
 }
 
-// The fold term of one sequence from its record words (every sequence has a
-// record: a bad one all zeros), loaded unconditionally so that all of a
-// thread's loads are in flight together.
-__device__ __forceinline__ void load_rec(uint32_t (&w)[K2_REC_WORDS], const K2Args &a, int64_t s)
+// The fold term of sequence s (structure-of-arrays record).
+__device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
 {
     const size_t S = static_cast<size_t>(a.S);
-#pragma unroll
-    for (int f = 0; f < K2_REC_WORDS; ++f)
-        w[f] = __ldg(a.rec + f * S + s);
-}
-
-__device__ __forceinline__ void fold_rec(FoldAcc &x, const uint32_t (&w)[K2_REC_WORDS])
-{
+    const uint32_t *rc = a.rec + s;
     FoldAcc y;
     fold_zero(y);
-    if (w[R_VALID] == 0u) {
+    if (rc[R_VALID * S] == 0u) {
         y.cnt[P_INVALID] = 1;
     } else {
-        const uint32_t nu = w[R_N_USED];
-        y.cnt[P_N_MASK] = w[R_N_MASK];
+        const uint32_t nu = rc[R_N_USED * S];
+        y.cnt[P_N_MASK] = rc[R_N_MASK * S];
         y.cnt[P_N_USED] = nu;
-        y.cnt[P_N_NAN] = w[R_N_NAN];
-        y.cnt[P_N_CLIP] = w[R_N_CLIP];
-        y.sum[S_SD] = {__uint_as_float(w[R_SD]), 0.f};
-        y.sum[S_SAD] = {__uint_as_float(w[R_SAD]), 0.f};
-        y.sum[S_SK2] = {__uint_as_float(w[R_SK2]), 0.f};
-        y.sum[S_SK3] = {__uint_as_float(w[R_SK3]), 0.f};
-        y.sum[S_SW] = {__uint_as_float(w[R_SW]), 0.f};
-        y.sum[S_SREL] = {__uint_as_float(w[R_SREL]), 0.f};
-        y.mx = __uint_as_float(w[R_MAX]);
+        y.cnt[P_N_NAN] = rc[R_N_NAN * S];
+        y.cnt[P_N_CLIP] = rc[R_N_CLIP * S];
+        y.sum[S_SD] = {__uint_as_float(rc[R_SD * S]), 0.f};
+        y.sum[S_SAD] = {__uint_as_float(rc[R_SAD * S]), 0.f};
+        y.sum[S_SK2] = {__uint_as_float(rc[R_SK2 * S]), 0.f};
+        y.sum[S_SK3] = {__uint_as_float(rc[R_SK3 * S]), 0.f};
+        y.sum[S_SW] = {__uint_as_float(rc[R_SW * S]), 0.f};
+        y.sum[S_SREL] = {__uint_as_float(rc[R_SREL * S]), 0.f};
+        y.mx = __uint_as_float(rc[R_MAX * S]);
         if (nu > 0u) {
             y.cnt[P_NONEMPTY] = 1;
-            y.cnt[P_REJ] = w[R_FLAG];
-            y.sum[S_MK1] = {__uint_as_float(w[R_MK1]), 0.f};
-            y.sum[S_MK2] = {__uint_as_float(w[R_MK2]), 0.f};
-            y.sum[S_MK3] = {__uint_as_float(w[R_MK3]), 0.f};
+            y.cnt[P_REJ] = rc[R_FLAG * S];
+            y.sum[S_MK1] = {__uint_as_float(rc[R_MK1 * S]), 0.f};
+            y.sum[S_MK2] = {__uint_as_float(rc[R_MK2 * S]), 0.f};
+            y.sum[S_MK3] = {__uint_as_float(rc[R_MK3 * S]), 0.f};
         }
     }
     fold_add(x, y);
 }
 
-// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i.
-// With a single CTA it writes the batch record directly; otherwise each CTA
-// stores its partial and the CTA that finishes last (a ticket counter that
-// k2_seq_kernel zeroes) folds the partials in index order, thread i taking
-// partials i, i + 256, ...  The result does not depend on which CTA is last.
+// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i;
+// with a single CTA it writes the batch record directly.
 __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a)
 {
-    __shared__ int last_s;
     pdl_wait();   // the records come from k2_seq_kernel
     pdl_launch_dependents();
     FoldAcc x;
     fold_zero(x);
     const int64_t base = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x;
 #pragma unroll 1
-    for (int k = 0; k < K2_FOLD_SEQS / K2_FOLD_THREADS; k += 2) {   // two records in flight at a time
-        const int64_t s0 = base + static_cast<int64_t>(k) * K2_FOLD_THREADS;
-        const int64_t s1 = s0 + K2_FOLD_THREADS;
-        uint32_t w0[K2_REC_WORDS], w1[K2_REC_WORDS];
-        if (s0 < a.S)
-            load_rec(w0, a, s0);
-        if (s1 < a.S)
-            load_rec(w1, a, s1);
-        if (s0 < a.S)
-            fold_rec(x, w0);
-        if (s1 < a.S)
-            fold_rec(x, w1);
+    for (int k = 0; k < K2_FOLD_SEQS / K2_FOLD_THREADS; ++k) {
+        const int64_t s = base + static_cast<int64_t>(k) * K2_FOLD_THREADS;
+        if (s < a.S)
+            fold_seq(x, a, s);
     }
     const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
     if (threadIdx.x == 0) {
-        if (gridDim.x == 1) {
+        if (gridDim.x == 1)
             write_batch(a, t, false);
-        } else {
+        else
             fold_store(a.part + static_cast<size_t>(blockIdx.x) * K2_PART_WORDS, t);
-            __threadfence();
-            last_s = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
-        }
     }
-    if (gridDim.x == 1)
-        return;
-    __syncthreads();
-    if (!last_s)   // uniform over the CTA
-        return;
-    __threadfence();
-    FoldAcc y;
-    fold_zero(y);
-    for (int p = threadIdx.x; p < static_cast<int>(gridDim.x); p += K2_FOLD_THREADS) {
-        const uint32_t *src = a.part + static_cast<size_t>(p) * K2_PART_WORDS;
-        uint32_t w[K2_PART_WORDS];
-#pragma unroll
-        for (int i = 0; i < K2_PART_WORDS; ++i)
-            w[i] = __ldcg(src + i);   // written by other CTAs: read through L2
-        FoldAcc z;
-        fold_load(z, w);
-        fold_add(y, z);
+}
+
+// One CTA folds the partials: thread i takes partials i, i + 256, ... in order.
+__global__ void __launch_bounds__(K2_FOLD_THREADS) k2_final_kernel(const K2Args a, int parts)
+{
+    pdl_wait();   // the partials come from k2_fold_kernel
+    FoldAcc x;
+    fold_zero(x);
+    for (int p = threadIdx.x; p < parts; p += K2_FOLD_THREADS) {
+        FoldAcc y;
+        fold_load(y, a.part + static_cast<size_t>(p) * K2_PART_WORDS);
+        fold_add(x, y);
     }
-    const FoldAcc f = fold_cta<K2_FOLD_THREADS>(y);
+    const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
     if (threadIdx.x == 0)
-        write_batch(a, f, false);
+        write_batch(a, t, false);
 }
 
 // S = 0: only the (all-zero) batch record, after checking the offsets cover [0, N).
@@ -915,7 +885,13 @@ cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream)
     cfg.gridDim = dim3(parts, 1, 1);
     cfg.blockDim = dim3(K2_FOLD_THREADS, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, k2_fold_kernel, a);
+    if ((e = cudaLaunchKernelEx(&cfg, k2_fold_kernel, a)) != cudaSuccess)
+        return e;
+    if (parts > 1) {
+        cfg.gridDim = dim3(1, 1, 1);
+        e = cudaLaunchKernelEx(&cfg, k2_final_kernel, a, parts);
+    }
+    return e;
 }
 
 } // namespace tim

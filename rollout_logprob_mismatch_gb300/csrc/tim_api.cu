@@ -419,9 +419,6 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
     a.batch = out->batch_stats;
     a.rec = static_cast<uint32_t *>(ws);
     a.part = S > 0 ? a.rec + round_up(static_cast<size_t>(S) * tim::K2_REC_WORDS, 64) : nullptr;
-    a.ticket = S > 0 ? a.part + static_cast<size_t>((S + tim::K2_FOLD_SEQS - 1) / tim::K2_FOLD_SEQS) *
-                                    tim::K2_PART_WORDS
-                     : nullptr;
     a.status = dev->status;
     cudaError_t e = tim::k2_launch(a, dev->sms, s);
     cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
