@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "monitor_internal.h"
 #include "tim_internal.h"
@@ -239,14 +240,24 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
 }
 
 // ---------------------------------------------------------------- the full pass
-// Per warp and step of 8 tokens per lane: each lane marks its tokens inside
-// each quantile's bounds (a bit mask), a warp scan of the counts places them,
-// and the keys are staged per warp and quantile in shared memory, going to
-// the global list 32 at a time (one atomic reservation per 32 keys).  (A
-// ballot per token and quantile took 13% longer; a private buffer per thread
-// 2.3x longer: its appends and flushes diverge inside the warp.)
-constexpr int kStepTokens = 8;                        // 2 groups of 4 per lane
-constexpr int kStage = 32 + 32 * kStepTokens;         // room for one full step on top of < 32 staged
+// A warp takes chunks of 32 x kScanGroups consecutive 4-token groups (lane l
+// the groups l, l + 32, ...: every load coalesced, their offsets immediates);
+// whole chunks skip the bounds checks, the ragged last one keeps them.  Per
+// step each lane marks its tokens inside each quantile's bounds (a bit mask);
+// their places follow from a ballot when no lane has two (the usual case), else
+// from a warp scan of the counts; the keys are staged per warp and quantile in
+// shared memory and go to the global list 32 at a time (one atomic reservation
+// per 32 keys).  Unused tokens (masked, non-finite delta, past N) take the
+// largest key (0x7fffffff for |delta|, 0xffffffff for delta), which no used
+// token has and which lies above every bound once hi is clamped below it: they
+// fall in no range, and a lane's used tokens below lo are its slots less its
+// slots at or above lo.  (A ballot per token and quantile took 13% longer; a
+// private buffer per thread 2.3x longer: its appends and flushes diverge
+// inside the warp.)
+constexpr int kScanGroups = 4;                           // 4-token groups per lane and step
+constexpr int kScanTokens = 4 * kScanGroups;
+constexpr int kStage = 32 + 32 * kScanTokens;           // room for one full step on top of < 32 staged
+constexpr size_t kScanSmem = sizeof(uint32_t) * (MON_THREADS / 32) * MON_QUANTILES * kStage;
 
 __device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane)
 {
@@ -258,38 +269,69 @@ __device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *bu
         a.cand[static_cast<size_t>(q) * a.cap + base + lane] = buf[lane];
 }
 
+// t = k - lo; ge += (k >= lo) for lo > 0 (the carry of k + (2^32 - lo); no
+// carry ever when lo = 0); inbits |= bit when t <= span.
+__device__ __forceinline__ void range_test(uint32_t k, uint32_t neg_lo, uint32_t span, uint32_t bit, int &ge,
+                                           uint32_t &inbits)
+{
+    asm("{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+        "add.cc.u32 t, %2, %3;\n\t"
+        "addc.u32 %0, %0, 0;\n\t"
+        "setp.le.u32 p, t, %4;\n\t"
+        "@p or.b32 %1, %1, %5;\n\t}"
+        : "+r"(ge), "+r"(inbits)
+        : "r"(k), "r"(neg_lo), "r"(span), "r"(bit));
+}
+
+__device__ __forceinline__ uint32_t pick(const uint32_t (&k)[kScanTokens], int s)
+{
+    uint32_t v = 0u;
+#pragma unroll
+    for (int t = 0; t < kScanTokens; ++t)
+        if (t == s)
+            v = k[t];
+    return v;
+}
+
 __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(const MonArgs a)
 {
+    extern __shared__ __align__(16) uint32_t stage_all[];   // [warp][quantile][kStage]
     __shared__ uint32_t lo_s[MON_QUANTILES], span_s[MON_QUANTILES];
-    __shared__ uint32_t stage_s[MON_THREADS / 32][MON_QUANTILES][kStage];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lanes_below = (1u << lane) - 1u;
     pdl_wait();
     pdl_launch_dependents();
     if (tid < MON_QUANTILES) {
         lo_s[tid] = a.st->lo[tid];
-        span_s[tid] = a.st->hi[tid] - a.st->lo[tid];
+        // the unused tokens' keys: 0x7fffffff (|delta|) and 0xffffffff (delta)
+        span_s[tid] = min(a.st->hi[tid], (tid == 0 ? 0x7fffffffu : 0xffffffffu) - 1u) - a.st->lo[tid];
     }
     __syncthreads();
-    uint32_t lo[MON_QUANTILES], span[MON_QUANTILES];
+    uint32_t neg_lo[MON_QUANTILES], span[MON_QUANTILES];
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q) {
-        lo[q] = lo_s[q];
+        neg_lo[q] = 0u - lo_s[q];
         span[q] = span_s[q];
     }
     const int64_t N = a.N;
     const int64_t G = (N + 3) >> 2;
     const int64_t full = N >> 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * MON_THREADS;
-    int n_used = 0, n_ext = 0;
+    constexpr int64_t kChunk = 32 * kScanGroups;   // groups per warp and step: lane + 32 u
+    const int64_t chunk_stride = static_cast<int64_t>(gridDim.x) * (MON_THREADS / 32) * kChunk;
+    const float tau = a.tau_tok;
+    int n_used = 0, n_ext = 0, slots = 0;
     int staged[MON_QUANTILES] = {0, 0, 0, 0};   // uniform over the warp
-    int below[MON_QUANTILES] = {0, 0, 0, 0};
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * MON_THREADS + warp * 32; base < G; base += 2 * stride) {
-        float4 lt[2], lr[2];
-        uint32_t mk[2];
+    int at_or_above[MON_QUANTILES] = {0, 0, 0, 0};
+
+    auto step = [&](int64_t g0, auto checked) {
+        constexpr bool CHECK = decltype(checked)::value;
+        const int64_t gl = g0 + lane;
+        float4 lt[kScanGroups], lr[kScanGroups];
+        uint32_t mk[kScanGroups];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t g = base + lane + u * stride;
-            if (g < full) {
+        for (int u = 0; u < kScanGroups; ++u) {
+            const int64_t g = gl + 32 * u;
+            if (!CHECK || g < full) {
                 lt[u] = __ldcs(reinterpret_cast<const float4 *>(a.l_tr) + g);
                 lr[u] = __ldcs(reinterpret_cast<const float4 *>(a.l_ro) + g);
                 mk[u] = __ldcs(reinterpret_cast<const unsigned int *>(a.mask) + g);
@@ -306,65 +348,64 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                 mk[u] = mm;
             }
         }
-        uint32_t ka[kStepTokens], kd[kStepTokens];
+        uint32_t ka[kScanTokens], kd[kScanTokens];
         uint32_t inbits[MON_QUANTILES] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t g = base + lane + u * stride;
-            const bool whole = g < full;
+        for (int u = 0; u < kScanGroups; ++u) {
+            const int64_t g = gl + 32 * u;
             const float d[4] = {__fsub_rn(lt[u].x, lr[u].x), __fsub_rn(lt[u].y, lr[u].y),
                                 __fsub_rn(lt[u].z, lr[u].z), __fsub_rn(lt[u].w, lr[u].w)};
             uint32_t flags = 0u;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int s = 4 * u + i;
-                const bool valid = whole || (g < G && 4 * g + i < N);
+                const bool valid = !CHECK || (g < G && 4 * g + i < N);
                 const bool used = valid && usable(((mk[u] >> (8 * i)) & 0xffu) != 0u, d[i]);
-                const bool ext = used && fabsf(d[i]) > a.tau_tok;
                 n_used += static_cast<int>(used);
-                n_ext += static_cast<int>(ext);
-                flags |= static_cast<uint32_t>(ext) << (8 * i);
-                ka[s] = key_abs(d[i]);
-                kd[s] = key_signed(d[i]);
+                if (used && fabsf(d[i]) > tau)
+                    flags |= 1u << (8 * i);
+                const uint32_t bits = used ? __float_as_uint(d[i]) : 0x7fffffffu;
+                ka[s] = bits & 0x7fffffffu;
+                kd[s] = bits ^ ((bits >> 31) ? 0xffffffffu : 0x80000000u);
 #pragma unroll
-                for (int q = 0; q < MON_QUANTILES; ++q) {
-                    const uint32_t k = q == 0 ? ka[s] : kd[s];
-                    below[q] += static_cast<int>(used && k < lo[q]);
-                    inbits[q] |= static_cast<uint32_t>(used && k - lo[q] <= span[q]) << s;
-                }
+                for (int q = 0; q < MON_QUANTILES; ++q)
+                    range_test(q == 0 ? ka[s] : kd[s], neg_lo[q], span[q], 1u << s, at_or_above[q], inbits[q]);
             }
+            n_ext += __popc(flags);
             if (a.reject) {
-                if (whole)
+                if (!CHECK || g < full)
                     __stcs(reinterpret_cast<unsigned int *>(a.reject) + g, flags);
                 else
                     for (int i = 0; i < 4 && g < G && 4 * g + i < N; ++i)
                         a.reject[4 * g + i] = static_cast<uint8_t>((flags >> (8 * i)) & 1u);
             }
         }
+        slots += kScanTokens;
 #pragma unroll
         for (int q = 0; q < MON_QUANTILES; ++q) {
             const int c = __popc(inbits[q]);
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += v;
-            }
-            const int total = __shfl_sync(0xffffffffu, incl, 31);
-            if (total == 0)   // uniform over the warp
+            const unsigned lanes_with = __ballot_sync(0xffffffffu, c != 0);
+            if (lanes_with == 0u)   // uniform over the warp
                 continue;
-            uint32_t *buf = stage_s[warp][q];
-            int pos = staged[q] + incl - c;
-            for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u) {
-                const int s = __ffs(b) - 1;
-                uint32_t k = 0;
+            int excl, total;
+            if (__ballot_sync(0xffffffffu, c > 1) == 0u) {
+                excl = __popc(lanes_with & lanes_below);
+                total = __popc(lanes_with);
+            } else {
+                int incl = c;
 #pragma unroll
-                for (int t = 0; t < kStepTokens; ++t)
-                    if (t == s)
-                        k = q == 0 ? ka[t] : kd[t];
-                buf[pos++] = k;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o)
+                        incl += v;
+                }
+                total = __shfl_sync(0xffffffffu, incl, 31);
+                excl = incl - c;
             }
+            uint32_t *buf = stage_all + (warp * MON_QUANTILES + q) * kStage;
+            int pos = staged[q] + excl;
+            for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u)
+                buf[pos++] = pick(q == 0 ? ka : kd, __ffs(b) - 1);
             staged[q] += total;
             __syncwarp();
             while (staged[q] >= 32) {   // uniform over the warp
@@ -379,18 +420,25 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                 staged[q] -= 32;
             }
         }
-    }
+    };
+
+    int64_t g0 = (static_cast<int64_t>(blockIdx.x) * (MON_THREADS / 32) + warp) * kChunk;
+    for (; g0 + kChunk <= full; g0 += chunk_stride)   // whole chunks: no bounds checks
+        step(g0, std::false_type{});
+    if (g0 < G)                                       // the ragged last chunk
+        step(g0, std::true_type{});
+
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q)
         if (staged[q] > 0)
-            flush_stage(a, stage_s[warp][q], q, staged[q], lane);
+            flush_stage(a, stage_all + (warp * MON_QUANTILES + q) * kStage, q, staged[q], lane);
     const int wu = __reduce_add_sync(0xffffffffu, n_used);
     const int we = __reduce_add_sync(0xffffffffu, n_ext);
     int wb[MON_QUANTILES];
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q)
-        wb[q] = __reduce_add_sync(0xffffffffu, below[q]);
+        wb[q] = __reduce_add_sync(0xffffffffu, neg_lo[q] == 0u ? 0 : slots - at_or_above[q]);
     if (lane == 0) {
         atomicAdd(&a.st->n_used, static_cast<unsigned long long>(wu));
         atomicAdd(&a.st->n_extreme, static_cast<unsigned long long>(we));
@@ -698,6 +746,9 @@ cudaError_t monitor_prepare_device()
         e = cudaFuncSetAttribute(mon_select_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSelectSmem));
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kScanSmem));
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mon_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  4 * pass_smem_words<1>());
     if (e == cudaSuccess)
@@ -718,6 +769,9 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
     const int64_t want = (groups + MON_THREADS - 1) / MON_THREADS;
     const dim3 grid(static_cast<unsigned>(
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
+    const int64_t scan_want = (groups + (MON_THREADS / 32) * 32 * kScanGroups - 1) / ((MON_THREADS / 32) * 32 * kScanGroups);
+    const dim3 scan_grid(static_cast<unsigned>(
+        std::max<int64_t>(1, std::min<int64_t>(scan_want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
     const int64_t runs = std::max<int64_t>(
         1, std::min<int64_t>({static_cast<int64_t>(MON_SAMPLE_RUNS), (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN,
                               2LL * num_sms}));
@@ -725,7 +779,7 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
     if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(runs)), block, kSampleSmem, stream, a)) !=
             cudaSuccess ||
         (e = launch_pdl(mon_bounds_kernel, dim3(1), dim3(1024), kSampleSmem, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_scan_kernel, grid, block, 0, stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_scan_kernel, scan_grid, block, kScanSmem, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_check_kernel, dim3(1), dim3(32), 0, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_pass_kernel<1>, grid, block, 4 * pass_smem_words<1>(), stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_select_kernel<1>, dim3(1), sel, kSelectSmem, stream, a)) != cudaSuccess ||
