@@ -17,10 +17,10 @@
 //                       runs of 1024 consecutive tokens;
 //   mon_bounds_kernel   per quantile, key bounds [lo, hi] around the sample's
 //                       quantile, six standard deviations of its rank wide;
-//   mon_scan_kernel     the one full pass: n_used, n_extreme, rejection
-//                       flags and, per quantile, the used tokens below lo and
-//                       the keys inside [lo, hi] (typically a few percent),
-//                       kept in a list;
+//   mon_scan_kernel     the one full pass (bulk-copied chunks): n_used,
+//                       n_extreme, rejection flags and, per quantile, the used
+//                       tokens below lo and the keys inside [lo, hi]
+//                       (typically a few percent), kept in a list;
 //   mon_check_kernel    ranks from n_used; each quantile's order statistics
 //                       must fall inside its list (else, or if a list
 //                       overflowed, the selection runs over all tokens);
@@ -70,6 +70,11 @@ __device__ __forceinline__ float unkey_signed(uint32_t k)
 
 __device__ __forceinline__ bool usable(bool m, float d) { return m && fabsf(d) <= FLT_MAX; }
 
+// delta = l_train - l_rollout with a zero always +0: -0 and +0 are the same
+// value (and e^-0 = e^+0), so every kernel below sees one key for zero, and a
+// bound between the two zeros' keys never splits equal values.
+__device__ __forceinline__ float delta_of(float lt, float lr) { return __fadd_rn(__fsub_rn(lt, lr), 0.0f); }
+
 // Tokens of a grid-stride pass in 4-token groups g (16-byte loads; the ragged
 // last group by plain loads).  Calls f(g, d[4], m[4], valid[4]) on every lane
 // of the warp, UNROLL groups loaded before the first use.
@@ -108,8 +113,8 @@ __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t g = base + lane + u * stride;
-            const float d[4] = {__fsub_rn(lt[u].x, lr[u].x), __fsub_rn(lt[u].y, lr[u].y),
-                                __fsub_rn(lt[u].z, lr[u].z), __fsub_rn(lt[u].w, lr[u].w)};
+            const float d[4] = {delta_of(lt[u].x, lr[u].x), delta_of(lt[u].y, lr[u].y),
+                                delta_of(lt[u].z, lr[u].z), delta_of(lt[u].w, lr[u].w)};
             bool m[4], valid[4];
             const bool whole = g < full;   // all four tokens exist
 #pragma unroll
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
         const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN : r * N / runs;
         const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
         for (int64_t t = s0 + tid; t < s1; t += MON_THREADS) {
-            const float d = __fsub_rn(a.l_tr[t], a.l_ro[t]);
+            const float d = delta_of(a.l_tr[t], a.l_ro[t]);
             if (usable(a.mask[t] != 0, d)) {
                 atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
                 atomicAdd(sh + SBD + (key_abs(d) >> SAMPLE_SHIFT), 1u);
@@ -240,24 +245,38 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
 }
 
 // ---------------------------------------------------------------- the full pass
-// A warp takes chunks of 32 x kScanGroups consecutive 4-token groups (lane l
-// the groups l, l + 32, ...: every load coalesced, their offsets immediates);
-// whole chunks skip the bounds checks, the ragged last one keeps them.  Per
-// step each lane marks its tokens inside each quantile's bounds (a bit mask);
-// their places follow from a ballot when no lane has two (the usual case), else
-// from a warp scan of the counts; the keys are staged per warp and quantile in
-// shared memory and go to the global list 32 at a time (one atomic reservation
-// per 32 keys).  Unused tokens (masked, non-finite delta, past N) take the
-// largest key (0x7fffffff for |delta|, 0xffffffff for delta), which no used
-// token has and which lies above every bound once hi is clamped below it: they
-// fall in no range, and a lane's used tokens below lo are its slots less its
-// slots at or above lo.  (A ballot per token and quantile took 13% longer; a
-// private buffer per thread 2.3x longer: its appends and flushes diverge
-// inside the warp.)
+// A warp takes chunks of 512 consecutive tokens (chunk w, w + warps, ...);
+// its lane 0 bulk-copies them (l_train, l_rollout, mask) into a ring of
+// kRing slots in shared memory, one chunk ahead of the one the warp works on;
+// the ragged last chunk is read from global memory.  Lane l takes the 4-token
+// groups l, l + 32, l + 64, l + 96 of the chunk.
+//
+// The tests run on the canonical delta itself (NaN for an unused token), with
+// float thresholds equal to the key bounds: per token and quantile one compare
+// for "at or above lo" (counted; the used tokens below lo are the used tokens
+// less these) and one for "in [lo, hi]" (a bit in the step's mask).  The
+// counts and bits are added by multiplies with `one`, so that they issue on
+// the FMA pipe while the compares take the integer ALU (the ALU alone had
+// bound the pass).  The keys in range are placed by a ballot when no lane has
+// two of a quantile (the usual case), else by a warp scan of the counts; they
+// are staged per warp and quantile in shared memory and go to the global list
+// 32 at a time (one atomic reservation per 32 keys), or straight to the list
+// when a step brings more than the stage holds.  (A ballot per token and
+// quantile took 13% longer; a private buffer per thread 2.3x longer.)
 constexpr int kScanGroups = 4;                           // 4-token groups per lane and step
 constexpr int kScanTokens = 4 * kScanGroups;
-constexpr int kStage = 32 + 32 * kScanTokens;           // room for one full step on top of < 32 staged
-constexpr size_t kScanSmem = sizeof(uint32_t) * (MON_THREADS / 32) * MON_QUANTILES * kStage;
+constexpr int kStage = 64;                              // staged keys per warp and quantile (a step that
+                                                        // does not fit writes its keys straight to the list)
+constexpr int kRing = 2;                                // ring slots per warp
+constexpr int kChunkTokens = 32 * kScanTokens;
+constexpr int kChunkF = 4 * kChunkTokens;               // bytes of one fp32 array's chunk
+constexpr int kChunkBytes = 2 * kChunkF + kChunkTokens; // l_train, l_rollout, mask
+constexpr int kScanWarps = MON_THREADS / 32;
+constexpr int kScanCtasPerSm = 2;                       // the rings and stages: 82 KB of shared memory per CTA
+constexpr size_t kRingBytes = static_cast<size_t>(kScanWarps) * kRing * kChunkBytes;
+constexpr size_t kStageBytes = sizeof(uint32_t) * kScanWarps * MON_QUANTILES * kStage;
+constexpr size_t kScanSmem = kRingBytes + kStageBytes + 8 * kScanWarps * kRing;
+static_assert(kChunkF % 16 == 0 && kChunkBytes % 16 == 0 && kRingBytes % 16 == 0, "bulk copies stay 16-byte aligned");
 
 __device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane)
 {
@@ -269,61 +288,163 @@ __device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *bu
         a.cand[static_cast<size_t>(q) * a.cap + base + lane] = buf[lane];
 }
 
-// t = k - lo; ge += (k >= lo) for lo > 0 (the carry of k + (2^32 - lo); no
-// carry ever when lo = 0); inbits |= bit when t <= span.
-__device__ __forceinline__ void range_test(uint32_t k, uint32_t neg_lo, uint32_t span, uint32_t bit, int &ge,
-                                           uint32_t &inbits)
+// Float thresholds equal to the key bounds on canonical finite deltas:
+// key(delta) >= lo  <=>  delta >= lo_threshold(lo), key(delta) <= hi  <=>
+// delta <= hi_threshold(hi) (-inf / +inf where every or no finite delta
+// qualifies).  Keys of finite canonical deltas: [key(-FLT_MAX), key(-min
+// subnormal)] and [key(+0), key(FLT_MAX)].
+constexpr uint32_t kKeyNegMax = 0x00800000u;   // key(-FLT_MAX)
+constexpr uint32_t kKeyNegMin = 0x7ffffffeu;   // key(-smallest subnormal)
+constexpr uint32_t kKeyZero = 0x80000000u;     // key(+0)
+constexpr uint32_t kKeyPosMax = 0xff7fffffu;   // key(FLT_MAX)
+
+__device__ __forceinline__ float signed_lo_threshold(uint32_t lo)
 {
-    asm("{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
-        "add.cc.u32 t, %2, %3;\n\t"
-        "addc.u32 %0, %0, 0;\n\t"
-        "setp.le.u32 p, t, %4;\n\t"
-        "@p or.b32 %1, %1, %5;\n\t}"
-        : "+r"(ge), "+r"(inbits)
-        : "r"(k), "r"(neg_lo), "r"(span), "r"(bit));
+    if (lo <= kKeyNegMax)
+        return -INFINITY;
+    if (lo > kKeyPosMax)
+        return INFINITY;
+    if (lo > kKeyNegMin && lo <= kKeyZero)
+        return 0.0f;
+    return unkey_signed(lo);
 }
 
-__device__ __forceinline__ uint32_t pick(const uint32_t (&k)[kScanTokens], int s)
+__device__ __forceinline__ float signed_hi_threshold(uint32_t hi)
 {
-    uint32_t v = 0u;
-#pragma unroll
-    for (int t = 0; t < kScanTokens; ++t)
-        if (t == s)
-            v = k[t];
+    if (hi >= kKeyPosMax)
+        return INFINITY;
+    if (hi < kKeyNegMax)
+        return -INFINITY;
+    if (hi >= kKeyNegMin && hi < kKeyZero)
+        return unkey_signed(kKeyNegMin);
+    return unkey_signed(hi);
+}
+
+__device__ __forceinline__ float abs_lo_threshold(uint32_t lo)
+{
+    return lo > 0x7f7fffffu ? INFINITY : __uint_as_float(lo);
+}
+
+__device__ __forceinline__ float abs_hi_threshold(uint32_t hi)
+{
+    return hi >= 0x7f7fffffu ? INFINITY : __uint_as_float(hi);
+}
+
+// Per token: the used test (mask byte and finite delta), the count of used
+// tokens and the rejection flag, both added with a multiply by `one` (= 1, read
+// from memory) so that they issue on the FMA pipe, not the integer ALU; the
+// delta itself, NaN for an unused token (it then passes no test below).
+__device__ __forceinline__ float token_delta(float d, uint32_t mk, uint32_t byte_sel, float tau, uint32_t one,
+                                             uint32_t flag_bit, int &n_used, uint32_t &flags)
+{
+    float v;
+    asm("{\n\t.reg .pred pm, pu, pe;\n\t.reg .u32 b;\n\t.reg .f32 fa;\n\t"
+        "and.b32 b, %4, %5;\n\t"
+        "setp.ne.u32 pm, b, 0;\n\t"
+        "abs.f32 fa, %3;\n\t"
+        "setp.le.and.f32 pu, fa, 0f7F7FFFFF, pm;\n\t"
+        "@pu mad.lo.u32 %0, %7, %7, %0;\n\t"
+        "setp.gt.and.f32 pe, fa, %6, pu;\n\t"
+        "@pe mad.lo.u32 %1, %7, %8, %1;\n\t"
+        "selp.f32 %2, %3, 0f7FFFFFFF, pu;\n\t}"
+        : "+r"(n_used), "+r"(flags), "=f"(v)
+        : "f"(d), "r"(mk), "r"(byte_sel), "f"(tau), "r"(one), "r"(flag_bit));
     return v;
 }
 
-__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(const MonArgs a)
+// ge += (x >= lo); inbits += bit when lo <= x <= hi (x NaN: neither).
+__device__ __forceinline__ void range_test(float x, float lo, float hi, uint32_t bit, uint32_t one, int &ge,
+                                           uint32_t &inbits)
 {
-    extern __shared__ __align__(16) uint32_t stage_all[];   // [warp][quantile][kStage]
-    __shared__ uint32_t lo_s[MON_QUANTILES], span_s[MON_QUANTILES];
+    asm("{\n\t.reg .pred p, r;\n\t"
+        "setp.ge.f32 p, %2, %3;\n\t"
+        "@p mad.lo.u32 %0, %6, %6, %0;\n\t"
+        "setp.le.and.f32 r, %2, %4, p;\n\t"
+        "@r mad.lo.u32 %1, %6, %5, %1;\n\t}"
+        : "+r"(ge), "+r"(inbits)
+        : "f"(x), "f"(lo), "f"(hi), "r"(bit), "r"(one));
+}
+
+// k[s] by a tree of selects on the bits of s.
+__device__ __forceinline__ float pick(const float (&k)[kScanTokens], int s)
+{
+    static_assert((kScanTokens & (kScanTokens - 1)) == 0, "a power-of-two tree");
+    float l[kScanTokens];
+#pragma unroll
+    for (int j = 0; j < kScanTokens; ++j)
+        l[j] = k[j];
+#pragma unroll
+    for (int w = kScanTokens / 2, bit = 0; w >= 1; w >>= 1, ++bit)
+#pragma unroll
+        for (int j = 0; j < w; ++j)
+            l[j] = ((s >> bit) & 1) ? l[2 * j + 1] : l[2 * j];
+    return l[0];
+}
+
+__global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(const MonArgs a)
+{
+    extern __shared__ __align__(16) uint8_t scan_smem[];   // rings [warp][kRing], staging, barriers
+    __shared__ float flo_s[MON_QUANTILES], fhi_s[MON_QUANTILES];
+    __shared__ uint32_t one_s;
+    __shared__ int abort_s;
+    volatile int *abort_flag = &abort_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lanes_below = (1u << lane) - 1u;
+    uint8_t *const ring = scan_smem + static_cast<size_t>(warp) * kRing * kChunkBytes;
+    uint32_t *const stage_all = reinterpret_cast<uint32_t *>(scan_smem + kRingBytes);
+    const uint32_t bar0 = smem_u32(scan_smem + kRingBytes + kStageBytes) + 8u * kRing * warp;
+    if (lane == 0) {
+        for (int i = 0; i < kRing; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_mbar_init();
+    }
+    if (tid == 0) {
+        one_s = 1u;
+        abort_s = 0;
+    }
     pdl_wait();
     pdl_launch_dependents();
     if (tid < MON_QUANTILES) {
-        lo_s[tid] = a.st->lo[tid];
-        // the unused tokens' keys: 0x7fffffff (|delta|) and 0xffffffff (delta)
-        span_s[tid] = min(a.st->hi[tid], (tid == 0 ? 0x7fffffffu : 0xffffffffu) - 1u) - a.st->lo[tid];
+        const uint32_t lo = a.st->lo[tid], hi = a.st->hi[tid];
+        flo_s[tid] = tid == 0 ? abs_lo_threshold(lo) : signed_lo_threshold(lo);
+        fhi_s[tid] = tid == 0 ? abs_hi_threshold(hi) : signed_hi_threshold(hi);
     }
     __syncthreads();
-    uint32_t neg_lo[MON_QUANTILES], span[MON_QUANTILES];
+    float flo[MON_QUANTILES], fhi[MON_QUANTILES];
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q) {
-        neg_lo[q] = 0u - lo_s[q];
-        span[q] = span_s[q];
+        flo[q] = flo_s[q];
+        fhi[q] = fhi_s[q];
     }
+    const uint32_t one = one_s;
     const int64_t N = a.N;
     const int64_t G = (N + 3) >> 2;
     const int64_t full = N >> 2;
     constexpr int64_t kChunk = 32 * kScanGroups;   // groups per warp and step: lane + 32 u
-    const int64_t chunk_stride = static_cast<int64_t>(gridDim.x) * (MON_THREADS / 32) * kChunk;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * kScanWarps;
     const float tau = a.tau_tok;
-    int n_used = 0, n_ext = 0, slots = 0;
+    const uint64_t pol = l2_policy_evict_first();
+    int n_used = 0, n_ext = 0;
     int staged[MON_QUANTILES] = {0, 0, 0, 0};   // uniform over the warp
     int at_or_above[MON_QUANTILES] = {0, 0, 0, 0};
 
-    auto step = [&](int64_t g0, auto checked) {
+    // The warp's k-th chunk: groups [c_k kChunk, (c_k + 1) kChunk), c_k = w + k warps.
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * kScanWarps + warp;
+    auto whole = [&](int64_t k) { return (w + k * warps + 1) * kChunk <= full; };
+    auto issue = [&](int64_t k) {   // lane 0: stage chunk k into ring slot k % kRing
+        if (lane != 0 || !whole(k))
+            return;
+        const int64_t g0 = (w + k * warps) * kChunk;
+        const int slot = static_cast<int>(k % kRing);
+        const uint32_t dst = smem_u32(ring + slot * kChunkBytes), bar = bar0 + 8u * slot;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kChunkBytes);
+        bulk_load(dst, a.l_tr + 4 * g0, kChunkF, bar, pol);
+        bulk_load(dst + kChunkF, a.l_ro + 4 * g0, kChunkF, bar, pol);
+        bulk_load(dst + 2 * kChunkF, a.mask + 4 * g0, kChunkTokens, bar, pol);
+    };
+
+    auto step = [&](int64_t g0, const uint8_t *src, auto checked) {
         constexpr bool CHECK = decltype(checked)::value;
         const int64_t gl = g0 + lane;
         float4 lt[kScanGroups], lr[kScanGroups];
@@ -331,45 +452,39 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
 #pragma unroll
         for (int u = 0; u < kScanGroups; ++u) {
             const int64_t g = gl + 32 * u;
-            if (!CHECK || g < full) {
-                lt[u] = __ldcs(reinterpret_cast<const float4 *>(a.l_tr) + g);
-                lr[u] = __ldcs(reinterpret_cast<const float4 *>(a.l_ro) + g);
-                mk[u] = __ldcs(reinterpret_cast<const unsigned int *>(a.mask) + g);
+            if (!CHECK) {
+                lt[u] = reinterpret_cast<const float4 *>(src)[lane + 32 * u];
+                lr[u] = reinterpret_cast<const float4 *>(src + kChunkF)[lane + 32 * u];
+                mk[u] = reinterpret_cast<const uint32_t *>(src + 2 * kChunkF)[lane + 32 * u];
             } else {
-                float v[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+                float v[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t mm = 0u;
                 for (int i = 0; i < 4 && g < G && 4 * g + i < N; ++i) {
                     v[i] = a.l_tr[4 * g + i];
-                    w[i] = a.l_ro[4 * g + i];
+                    x[i] = a.l_ro[4 * g + i];
                     mm |= static_cast<uint32_t>(a.mask[4 * g + i] != 0) << (8 * i);
                 }
                 lt[u] = make_float4(v[0], v[1], v[2], v[3]);
-                lr[u] = make_float4(w[0], w[1], w[2], w[3]);
+                lr[u] = make_float4(x[0], x[1], x[2], x[3]);
                 mk[u] = mm;
             }
         }
-        uint32_t ka[kScanTokens], kd[kScanTokens];
+        float dv[kScanTokens];   // canonical delta, NaN when unused
         uint32_t inbits[MON_QUANTILES] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int u = 0; u < kScanGroups; ++u) {
             const int64_t g = gl + 32 * u;
-            const float d[4] = {__fsub_rn(lt[u].x, lr[u].x), __fsub_rn(lt[u].y, lr[u].y),
-                                __fsub_rn(lt[u].z, lr[u].z), __fsub_rn(lt[u].w, lr[u].w)};
+            const float d[4] = {delta_of(lt[u].x, lr[u].x), delta_of(lt[u].y, lr[u].y),
+                                delta_of(lt[u].z, lr[u].z), delta_of(lt[u].w, lr[u].w)};
             uint32_t flags = 0u;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int s = 4 * u + i;
-                const bool valid = !CHECK || (g < G && 4 * g + i < N);
-                const bool used = valid && usable(((mk[u] >> (8 * i)) & 0xffu) != 0u, d[i]);
-                n_used += static_cast<int>(used);
-                if (used && fabsf(d[i]) > tau)
-                    flags |= 1u << (8 * i);
-                const uint32_t bits = used ? __float_as_uint(d[i]) : 0x7fffffffu;
-                ka[s] = bits & 0x7fffffffu;
-                kd[s] = bits ^ ((bits >> 31) ? 0xffffffffu : 0x80000000u);
+                dv[s] = token_delta(d[i], mk[u], 0xffu << (8 * i), tau, one, 1u << (8 * i), n_used, flags);
+                range_test(fabsf(dv[s]), flo[0], fhi[0], 1u << s, one, at_or_above[0], inbits[0]);
 #pragma unroll
-                for (int q = 0; q < MON_QUANTILES; ++q)
-                    range_test(q == 0 ? ka[s] : kd[s], neg_lo[q], span[q], 1u << s, at_or_above[q], inbits[q]);
+                for (int q = 1; q < MON_QUANTILES; ++q)
+                    range_test(dv[s], flo[q], fhi[q], 1u << s, one, at_or_above[q], inbits[q]);
             }
             n_ext += __popc(flags);
             if (a.reject) {
@@ -380,7 +495,6 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                         a.reject[4 * g + i] = static_cast<uint8_t>((flags >> (8 * i)) & 1u);
             }
         }
-        slots += kScanTokens;
 #pragma unroll
         for (int q = 0; q < MON_QUANTILES; ++q) {
             const int c = __popc(inbits[q]);
@@ -402,10 +516,24 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
                 total = __shfl_sync(0xffffffffu, incl, 31);
                 excl = incl - c;
             }
+            if (staged[q] + total > kStage) {   // rare: straight to the list, one reservation
+                unsigned long long base = 0;
+                if (lane == 0)
+                    base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(total));
+                base = __shfl_sync(0xffffffffu, base, 0) + static_cast<unsigned long long>(excl);
+                for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u, ++base) {
+                    const float v = pick(dv, __ffs(b) - 1);
+                    if (base < a.cap)
+                        a.cand[static_cast<size_t>(q) * a.cap + base] = q == 0 ? key_abs(v) : key_signed(v);
+                }
+                continue;
+            }
             uint32_t *buf = stage_all + (warp * MON_QUANTILES + q) * kStage;
             int pos = staged[q] + excl;
-            for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u)
-                buf[pos++] = pick(q == 0 ? ka : kd, __ffs(b) - 1);
+            for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u) {
+                const float v = pick(dv, __ffs(b) - 1);
+                buf[pos++] = q == 0 ? key_abs(v) : key_signed(v);
+            }
             staged[q] += total;
             __syncwarp();
             while (staged[q] >= 32) {   // uniform over the warp
@@ -422,11 +550,32 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
         }
     };
 
-    int64_t g0 = (static_cast<int64_t>(blockIdx.x) * (MON_THREADS / 32) + warp) * kChunk;
-    for (; g0 + kChunk <= full; g0 += chunk_stride)   // whole chunks: no bounds checks
-        step(g0, std::false_type{});
-    if (g0 < G)                                       // the ragged last chunk
-        step(g0, std::true_type{});
+    // Whole chunks through the ring; the ragged last one from global memory.
+    for (int k = 0; k < kRing; ++k)
+        issue(k);
+    bool ok = true;
+    int64_t k = 0;
+    for (; whole(k); ++k) {
+        const int slot = static_cast<int>(k % kRing);
+        if (!mbar_wait_sleep(bar0 + 8u * slot, static_cast<uint32_t>((k / kRing) & 1), abort_flag,
+                             a.wait_budget_ns)) {
+            ok = false;
+            break;
+        }
+        step((w + k * warps) * kChunk, ring + slot * kChunkBytes, std::false_type{});
+        __syncwarp();   // every lane has read the slot
+        issue(k + kRing);
+    }
+    if (!ok) {   // copies may still be landing: let them, then report
+        for (int64_t j = k; j < k + kRing; ++j)
+            if (whole(j))
+                drain_wait(bar0 + 8u * static_cast<uint32_t>(j % kRing), static_cast<uint32_t>((j / kRing) & 1));
+        if (lane == 0)
+            atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
+        return;
+    }
+    if ((w + k * warps) * kChunk < G)
+        step((w + k * warps) * kChunk, nullptr, std::true_type{});
 
     __syncwarp();
 #pragma unroll
@@ -438,7 +587,7 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_scan_kernel(
     int wb[MON_QUANTILES];
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q)
-        wb[q] = __reduce_add_sync(0xffffffffu, neg_lo[q] == 0u ? 0 : slots - at_or_above[q]);
+        wb[q] = __reduce_add_sync(0xffffffffu, n_used - at_or_above[q]);
     if (lane == 0) {
         atomicAdd(&a.st->n_used, static_cast<unsigned long long>(wu));
         atomicAdd(&a.st->n_extreme, static_cast<unsigned long long>(we));
@@ -771,7 +920,7 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
     const int64_t scan_want = (groups + (MON_THREADS / 32) * 32 * kScanGroups - 1) / ((MON_THREADS / 32) * 32 * kScanGroups);
     const dim3 scan_grid(static_cast<unsigned>(
-        std::max<int64_t>(1, std::min<int64_t>(scan_want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
+        std::max<int64_t>(1, std::min<int64_t>(scan_want, static_cast<int64_t>(kScanCtasPerSm) * num_sms))));
     const int64_t runs = std::max<int64_t>(
         1, std::min<int64_t>({static_cast<int64_t>(MON_SAMPLE_RUNS), (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN,
                               2LL * num_sms}));

@@ -66,6 +66,7 @@ struct MonArgs {
     uint32_t *cand;      // [MON_QUANTILES][cap] collected keys
     unsigned long long cap;
     int *status;
+    uint64_t wait_budget_ns;   // bound of each pipeline wait in the kernels
 };
 
 cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream);

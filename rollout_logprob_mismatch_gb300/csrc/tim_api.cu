@@ -619,6 +619,7 @@ int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, con
     a.cand = a.shist + tim::MON_SHIST_WORDS;
     a.cap = tim::monitor_cap(N);
     a.status = dev->status;
+    a.wait_budget_ns = wait_budget_ns();
     e = tim::monitor_launch(a, dev->sms, s);
     cudaError_t ef = cudaFreeAsync(ws, s);
     if (e != cudaSuccess)

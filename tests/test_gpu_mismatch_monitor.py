@@ -133,3 +133,24 @@ def test_sample_that_misses_the_bulk_and_mass_ties():
     same = lr.copy()
     g2, rej2 = gpu_monitor(same, lr, np.ones(N, np.uint8), tau)
     assert_monitor_match(g2, rej2, oracle.mismatch_monitor(same, lr, np.ones(N, np.uint8), tau), "all ties")
+
+
+def test_signed_zeros_and_subnormals_at_the_ranks():
+    """Half the deltas are zeros of either sign (-0 - +0 = -0), most of the rest
+    subnormals of either sign, 3% normal: the median sits where -0, +0 and the
+    smallest subnormals meet and p95 |delta| among the subnormals, in a batch
+    larger than the sample so that the collected lists are used."""
+    N = 1 << 21
+    rng = np.random.default_rng(11)
+    u = rng.random(N)
+    tiny = (rng.integers(1, 1000, N) * np.float32(2.0 ** -149)).astype(np.float32)
+    sign = np.where(rng.random(N) < 0.5, np.float32(-1.0), np.float32(1.0))
+    lt = np.where(u < 0.5, np.float32(0.0), np.where(u < 0.97, sign * tiny,
+                  sign * rng.uniform(0.005, 0.05, N).astype(np.float32))).astype(np.float32)
+    lt[(u < 0.5) & (sign < 0)] = -0.0
+    lr = np.zeros(N, np.float32)
+    mask = (rng.random(N) < 0.9).astype(np.uint8)
+    assert np.signbit(lt[u < 0.5]).any() and (lt[(u >= 0.5) & (u < 0.97)] != 0).all()
+    for tau in (0.0, float(np.float32(2.0 ** -140))):
+        g, rej = gpu_monitor(lt, lr, mask, tau)
+        assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, tau), "zeros tau=%g" % tau)
