@@ -13,21 +13,23 @@
 // keys that order like the values (|delta|: its bits; delta: sign-flipped
 // bits).  Counts are integers, so thread order cannot change them: the
 // selected tokens are exactly the ones a sort would pick.
-//   mon_sample_kernel   histograms (14 key bits) of up to 1024 evenly spaced
-//                       runs of 1024 consecutive tokens;
-//   mon_bounds_kernel   per quantile, key bounds [lo, hi] around the sample's
+//   mon_sample_kernel   a histogram (14 key bits) of up to 1024 evenly spaced
+//                       runs of 1024 consecutive tokens; its last CTA sets,
+//                       per quantile, key bounds [lo, hi] around the sample's
 //                       quantile, six standard deviations of its rank wide;
 //   mon_scan_kernel     the one full pass (bulk-copied chunks): n_used,
 //                       n_extreme, rejection flags and, per quantile, the used
 //                       tokens below lo and the keys inside [lo, hi]
-//                       (typically a few percent), kept in a list;
-//   mon_check_kernel    ranks from n_used; each quantile's order statistics
-//                       must fall inside its list (else, or if a list
-//                       overflowed, the selection runs over all tokens);
-//   mon_pass_kernel<1..3> + mon_select_kernel<1..3>: radix selection in three
-//                       digit passes (11, 11, 10 bits) over the lists, on
-//                       key - lo, or over all tokens; select<3> writes the
-//                       record.
+//                       (typically a few percent), kept in a list with the
+//                       histogram of their first radix digit; its last CTA
+//                       takes the ranks from n_used, checks that each
+//                       quantile's order statistics fall inside its list (else,
+//                       or if a list overflowed, the selection runs over all
+//                       tokens) and selects the lists' first digit;
+//   mon_pass_kernel<1..3> radix selection in three digit passes (11, 11, 10
+//                       bits) over the lists, on key - lo, or over all tokens
+//                       (pass 1 only then); the last CTA of each selects the
+//                       digit, that of pass 3 writes the record.
 // The bounds only decide how much work the selection does; the result is the
 // same either way.
 #include <algorithm>
@@ -127,62 +129,118 @@ __device__ __forceinline__ void for_token_groups(const MonArgs &a, F &&f)
     }
 }
 
-// ---------------------------------------------------------------- sample
-// Run r: tokens [s, s + MON_SAMPLE_RUN), s = r N / runs (runs back to back
-// when they cover the batch); CTA c takes runs c, c + gridDim, ... into
-// shared-memory histograms and adds the non-zero bins to the global ones.
-__global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
+// ---------------------------------------------------------------- histogram search
+// Histogram segments in registers, loaded 16 bytes at a time (all in flight
+// at once) from global memory written by atomics (read through L2).
+template <int SEG>
+__device__ __forceinline__ void load_segment(const uint32_t *p, uint32_t (&v)[SEG])   // p 16-byte aligned
 {
-    extern __shared__ __align__(16) uint32_t sh[];   // [SBD] delta, then [SBA] |delta|
-    const int tid = threadIdx.x, lane = tid & 31;
-    for (int i = tid; i < SBD + SBA; i += MON_THREADS)
-        sh[i] = 0u;
-    __syncthreads();
-    pdl_wait();
-    pdl_launch_dependents();
-    const int64_t N = a.N;
-    const int64_t cover = static_cast<int64_t>(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN;
-    const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
-    int used = 0;
-    for (int64_t r = blockIdx.x; r < runs; r += gridDim.x) {
-        const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN : r * N / runs;
-        const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
-        for (int64_t t = s0 + tid; t < s1; t += MON_THREADS) {
-            const float d = delta_of(a.l_tr[t], a.l_ro[t]);
-            if (usable(a.mask[t] != 0, d)) {
-                atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
-                atomicAdd(sh + SBD + (key_abs(d) >> SAMPLE_SHIFT), 1u);
-                ++used;
-            }
-        }
+#pragma unroll
+    for (int i = 0; i < SEG / 4; ++i) {
+        const uint4 x = __ldcg(reinterpret_cast<const uint4 *>(p) + i);
+        v[4 * i] = x.x;
+        v[4 * i + 1] = x.y;
+        v[4 * i + 2] = x.z;
+        v[4 * i + 3] = x.w;
     }
-    used = __reduce_add_sync(0xffffffffu, used);
-    if (lane == 0 && used)
-        atomicAdd(&a.st->sample_used, static_cast<unsigned long long>(used));
-    __syncthreads();
-    for (int i = tid; i < SBD + SBA; i += MON_THREADS)
-        if (sh[i] != 0u)
-            atomicAdd(a.shist + i, sh[i]);
 }
 
-// ---------------------------------------------------------------- bounds
-// One CTA of 1024 threads.  For quantile q at level L with m sampled used
-// tokens: sample ranks floor(L (m - 1)) - w and ceil(L (m - 1)) + w, w = six
-// standard deviations of a sample quantile's rank (sqrt(m L (1 - L))) + 2;
-// lo = the lowest key of the bin holding the first (0 when that rank is at or
-// below the sample's first), hi = the highest key of the bin holding the
-// second (all ones when at or above the sample's last).
-__global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
+// |delta|'s bins [c0, c0 + SEG) from delta's histogram h of 2 half bins: a
+// clear top bit means |delta|'s bin c holds the positive deltas of delta's bin
+// half + c and the negative ones of bin half - 1 - c.
+template <int SEG>
+__device__ __forceinline__ void load_abs_segment(const uint32_t *h, int half, int c0, uint32_t (&v)[SEG])
 {
-    extern __shared__ __align__(16) uint32_t hs[];   // the sample histograms, copied with coalesced loads
-    __shared__ long long wsum[32];
-    __shared__ int bin_s[2 * MON_QUANTILES];
+    uint32_t pos[SEG], neg[SEG];
+    load_segment<SEG>(h + half + c0, pos);
+    load_segment<SEG>(h + half - c0 - SEG, neg);   // neg[SEG - 1 - x] = bin half - 1 - (c0 + x)
+#pragma unroll
+    for (int x = 0; x < SEG; ++x)
+        v[x] = pos[x] + neg[SEG - 1 - x];
+}
+
+// Counts here stay below 2^31 (N < 2^31 tokens, a sample of 2^20), so 32-bit
+// sums and ranks are exact.
+template <int SEG>
+__device__ __forceinline__ uint32_t segment_total(const uint32_t (&v)[SEG])
+{
+    uint32_t c = 0;
+#pragma unroll
+    for (int x = 0; x < SEG; ++x)
+        c += v[x];
+    return c;
+}
+
+// The first bin x of the segment with cum + v[0] + ... + v[x] > r (cum: the
+// count before the segment), or -1; `before` gets the count before bin x.
+template <int SEG>
+__device__ __forceinline__ int find_in_segment(const uint32_t (&v)[SEG], uint32_t cum, uint32_t r, uint32_t &before)
+{
+    int bin = -1;
+#pragma unroll
+    for (int x = 0; x < SEG; ++x) {
+        if (bin < 0 && cum + v[x] > r) {
+            bin = x;
+            before = cum;
+        }
+        cum += v[x];
+    }
+    return bin;
+}
+
+// ---------------------------------------------------------------- sample and bounds
+// One kind of bound (KIND 0: delta's bins, quantiles 1..3; KIND 1: |delta|'s,
+// quantile 0), thread i holding bins [i SEG, (i + 1) SEG) in v: a CTA scan of
+// the segment totals, then the thread whose segment holds a target rank finds
+// its bin.
+template <int KIND, int SEG>
+__device__ __forceinline__ void bounds_kind(const uint32_t (&v)[SEG], long long m, const long long *rlo,
+                                            const long long *rhi, int *bin_s, uint32_t *wsum)
+{
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
-    pdl_launch_dependents();
-    MonState *st = a.st;
+    const uint32_t c = segment_total(v);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += x;
+    }
+    __syncthreads();   // earlier readers of wsum are done
+    if (lane == 31)
+        wsum[warp] = incl;
+    __syncthreads();
+    uint32_t before_warp = 0;
+    for (int w = 0; w < warp; ++w)
+        before_warp += wsum[w];
+    const long long excl = static_cast<long long>(before_warp + incl - c);
+    const int q_first = KIND == 0 ? 1 : 0, q_end = KIND == 0 ? MON_QUANTILES : 1;
+    for (int q = q_first; q < q_end; ++q)
+        for (int e = 0; e < 2; ++e) {
+            const long long R = e == 0 ? rlo[q] : rhi[q];
+            if (m > 0 && R > 0 && R < m - 1 && excl <= R && R < excl + static_cast<long long>(c)) {
+                uint32_t before;
+                bin_s[2 * q + e] = tid * SEG + find_in_segment(v, static_cast<uint32_t>(excl),
+                                                               static_cast<uint32_t>(R), before);
+            }
+        }
+}
+
+// For quantile q at level L with m sampled used tokens: sample ranks
+// floor(L (m - 1)) - w and ceil(L (m - 1)) + w, w = six standard deviations of
+// a sample quantile's rank (sqrt(m L (1 - L))) + 2; lo = the lowest key of the
+// bin holding the first (0 when that rank is at or below the sample's first),
+// hi = the highest key of the bin holding the second (all ones when at or
+// above the sample's last).  Run by one CTA of MON_THREADS threads on the
+// global sample histogram of delta's key.
+__device__ void compute_bounds(const MonArgs &a)
+{
+    __shared__ uint32_t wsum[MON_THREADS / 32];
+    __shared__ int bin_s[2 * MON_QUANTILES];
     __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
-    const long long m = static_cast<long long>(st->sample_used);
+    const int tid = threadIdx.x;
+    MonState *st = a.st;
+    const long long m = static_cast<long long>(__ldcg(&st->sample_used));
     if (tid < MON_QUANTILES) {   // fp64 in a few threads only: GB300 runs it slowly
         const double L = level(tid);
         const double j = static_cast<double>(m - 1) * L;
@@ -192,48 +250,17 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
     }
     if (tid < 2 * MON_QUANTILES)
         bin_s[tid] = -1;
-#pragma unroll 24
-    for (int i = tid; i < SBD + SBA; i += 1024)
-        hs[i] = a.shist[i];
     __syncthreads();
-    for (int kind = 0; kind < 2; ++kind) {   // 0: delta (quantiles 1..3), 1: |delta| (quantile 0)
-        const int nb = kind == 0 ? SBD : SBA;
-        const uint32_t *h = hs + (kind == 0 ? 0 : SBD);
-        const int per = nb / 1024;
-        long long c = 0;
-        for (int b = 0; b < per; ++b)
-            c += h[tid * per + b];
-        long long incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += v;
-        }
-        __syncthreads();   // the previous kind's wsum reads are done
-        if (lane == 31)
-            wsum[warp] = incl;
-        __syncthreads();
-        long long before_warp = 0;
-        for (int w = 0; w < warp; ++w)
-            before_warp += wsum[w];
-        const long long excl = before_warp + incl - c;
-        const int q_first = kind == 0 ? 1 : 0, q_end = kind == 0 ? MON_QUANTILES : 1;
-        for (int q = q_first; q < q_end; ++q) {
-            for (int e = 0; e < 2; ++e) {
-                const long long R = e == 0 ? rlo_s[q] : rhi_s[q];
-                if (m > 0 && R > 0 && R < m - 1 && excl <= R && R < excl + c) {
-                    long long cum = excl;
-                    for (int b = 0; b < per; ++b) {
-                        cum += h[tid * per + b];
-                        if (cum > R) {
-                            bin_s[2 * q + e] = tid * per + b;
-                            break;
-                        }
-                    }
-                }
-            }
-        }
+    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins, 32 |delta| bins per thread");
+    {
+        uint32_t v[64];
+        load_segment<64>(a.shist + tid * 64, v);
+        bounds_kind<0>(v, m, rlo_s, rhi_s, bin_s, wsum);
+    }
+    {
+        uint32_t v[32];
+        load_abs_segment<32>(a.shist, SBA, tid * 32, v);
+        bounds_kind<1>(v, m, rlo_s, rhi_s, bin_s, wsum);
     }
     __syncthreads();
     if (tid < MON_QUANTILES) {
@@ -242,6 +269,126 @@ __global__ void __launch_bounds__(1024) mon_bounds_kernel(const MonArgs a)
         st->lo[q] = bl < 0 ? 0u : static_cast<uint32_t>(bl) << SAMPLE_SHIFT;
         st->hi[q] = bh < 0 ? 0xffffffffu : (static_cast<uint32_t>(bh) << SAMPLE_SHIFT) | ((1u << SAMPLE_SHIFT) - 1u);
     }
+}
+
+// Adds the non-zero words of a shared-memory histogram of `words` bins to
+// the global one (16-byte shared-memory reads, all threads of the CTA).
+template <int WORDS>
+__device__ __forceinline__ void flush_histogram(const uint32_t *sh, uint32_t *gh)
+{
+    static_assert(WORDS % (4 * MON_THREADS) == 0, "whole 16-byte reads per thread");
+#pragma unroll
+    for (int k = 0; k < WORDS / (4 * MON_THREADS); ++k) {
+        const int i = threadIdx.x + k * MON_THREADS;
+        const uint4 x = reinterpret_cast<const uint4 *>(sh)[i];
+        if (x.x != 0u)
+            atomicAdd(gh + 4 * i, x.x);
+        if (x.y != 0u)
+            atomicAdd(gh + 4 * i + 1, x.y);
+        if (x.z != 0u)
+            atomicAdd(gh + 4 * i + 2, x.z);
+        if (x.w != 0u)
+            atomicAdd(gh + 4 * i + 3, x.w);
+    }
+}
+
+template <int WORDS>
+__device__ __forceinline__ void zero_histogram(uint32_t *sh)
+{
+    static_assert(WORDS % (4 * MON_THREADS) == 0, "whole 16-byte writes per thread");
+#pragma unroll
+    for (int k = 0; k < WORDS / (4 * MON_THREADS); ++k)
+        reinterpret_cast<uint4 *>(sh)[threadIdx.x + k * MON_THREADS] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Is this CTA the last of the grid to get here?  Every thread's global writes
+// before the call are ordered before the ticket (a fence per thread, then the
+// barrier); the last CTA fences again before it reads what the others wrote.
+__device__ __forceinline__ bool last_cta(unsigned *ticket)
+{
+    __shared__ int last_s;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        last_s = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last_s)
+        return false;
+    __threadfence();
+    return true;
+}
+
+// Run r: MON_SAMPLE_RUN tokens from s = r N / runs rounded down to a multiple
+// of 4 (runs back to back when they cover the batch); CTA c takes runs c, c +
+// gridDim, ..., kRunsAtOnce of them loaded before any is used, into a
+// shared-memory histogram of delta's key (|delta|'s follows from it), thread
+// i the tokens s + 4i .. s + 4i + 3 (one 16-byte load per array), and adds
+// the non-zero bins to the global histogram.  The CTA that finishes last
+// computes the bounds.
+constexpr int kRunsAtOnce = 4;
+static_assert(MON_SAMPLE_RUN == 4 * MON_THREADS, "a run is one 4-token group per thread");
+__global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
+{
+    extern __shared__ __align__(16) uint32_t sh[];   // [SBD] delta's key
+    const int tid = threadIdx.x, lane = tid & 31;
+    zero_histogram<SBD>(sh);
+    __syncthreads();
+    pdl_wait();
+    const int64_t N = a.N;
+    const int64_t cover = static_cast<int64_t>(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN;
+    const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
+    int used = 0;
+    for (int64_t r0 = blockIdx.x; r0 < runs; r0 += kRunsAtOnce * gridDim.x) {
+        float v[kRunsAtOnce][4], w[kRunsAtOnce][4];
+        uint32_t mm[kRunsAtOnce];
+#pragma unroll
+        for (int k = 0; k < kRunsAtOnce; ++k) {
+            const int64_t r = r0 + k * static_cast<int64_t>(gridDim.x);
+            mm[k] = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[k][i] = w[k][i] = 0.f;
+            if (r >= runs)
+                continue;
+            const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN : (r * N / runs) & ~int64_t(3);
+            const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
+            const int64_t t = s0 + 4 * tid;
+            if (t + 4 <= s1) {
+                const float4 x = __ldcs(reinterpret_cast<const float4 *>(a.l_tr + t));
+                const float4 y = __ldcs(reinterpret_cast<const float4 *>(a.l_ro + t));
+                mm[k] = __ldcs(reinterpret_cast<const unsigned int *>(a.mask + t));
+                v[k][0] = x.x, v[k][1] = x.y, v[k][2] = x.z, v[k][3] = x.w;
+                w[k][0] = y.x, w[k][1] = y.y, w[k][2] = y.z, w[k][3] = y.w;
+            } else {
+                for (int i = 0; i < 4 && t + i < s1; ++i) {
+                    v[k][i] = a.l_tr[t + i];
+                    w[k][i] = a.l_ro[t + i];
+                    mm[k] |= static_cast<uint32_t>(a.mask[t + i] != 0) << (8 * i);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRunsAtOnce; ++k)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float d = delta_of(v[k][i], w[k][i]);
+                if (usable(((mm[k] >> (8 * i)) & 0xffu) != 0u, d)) {
+                    atomicAdd(sh + (key_signed(d) >> SAMPLE_SHIFT), 1u);
+                    ++used;
+                }
+            }
+    }
+    used = __reduce_add_sync(0xffffffffu, used);
+    if (lane == 0 && used)
+        atomicAdd(&a.st->sample_used, static_cast<unsigned long long>(used));
+    __syncthreads();
+    // The full pass may launch now: earlier, its CTAs (82 KB of shared memory
+    // each) took the room of this kernel's second CTA per SM, which then
+    // started ~10 us late.
+    pdl_launch_dependents();
+    flush_histogram<SBD>(sh, a.shist);
+    if (last_cta(&a.st->ticket[0]))
+        compute_bounds(a);
 }
 
 // ---------------------------------------------------------------- the full pass
@@ -278,14 +425,54 @@ constexpr size_t kStageBytes = sizeof(uint32_t) * kScanWarps * MON_QUANTILES * k
 constexpr size_t kScanSmem = kRingBytes + kStageBytes + 8 * kScanWarps * kRing;
 static_assert(kChunkF % 16 == 0 && kChunkBytes % 16 == 0 && kRingBytes % 16 == 0, "bulk copies stay 16-byte aligned");
 
-__device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane)
+// Radix digits of a value with b significant bits (b = 32 for raw keys): pass
+// 1 the top 11 (bits b-11 .. b-1), pass 2 the next 11, pass 3 the rest (<= 10).
+__device__ __forceinline__ int digit_shift(int pass, int b)
+{
+    return pass == 1 ? max(b - 11, 0) : pass == 2 ? max(b - 22, 0) : 0;
+}
+
+template <int PASS>
+__device__ __forceinline__ uint32_t digit_of(uint32_t v, int b)
+{
+    const int s = digit_shift(PASS, b);
+    const int top = PASS == 1 ? b : digit_shift(PASS - 1, b);
+    const int width = top - s;   // <= 11
+    return (v >> s) & ((1u << width) - 1u);
+}
+
+// Significant bits of hi - lo: the width of the collected keys' offsets.
+__device__ __forceinline__ int span_bits_of(uint32_t lo, uint32_t hi)
+{
+    const uint32_t span = hi - lo;
+    return span == 0u ? 0 : 32 - __clz(static_cast<int>(span));
+}
+
+// Collected keys of quantile q, one per lane with `has` set (a full warp
+// calls): each into the list at `at` (when there is room) and into the list's
+// pass-1 histogram of its offset's top digit, lanes with the same digit added
+// by one atomic (the keys near a quantile share few digits).
+__device__ __forceinline__ void collect(const MonArgs &a, int q, bool has, unsigned long long at, uint32_t key,
+                                        uint32_t lo, int bits)
+{
+    const uint32_t dg = has ? digit_of<1>(key - lo, bits) : 0xffffffffu;
+    const unsigned same = __match_any_sync(0xffffffffu, dg);
+    if (has) {
+        if (at < a.cap)
+            a.cand[static_cast<size_t>(q) * a.cap + at] = key;
+        if ((threadIdx.x & 31) == __ffs(same) - 1)
+            atomicAdd(a.hist1 + q * MON_BINS1 + dg, static_cast<uint32_t>(__popc(same)));
+    }
+}
+
+__device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane,
+                                            uint32_t lo, int bits)
 {
     unsigned long long base = 0;
     if (lane == 0)
         base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(n));
     base = __shfl_sync(0xffffffffu, base, 0);
-    if (lane < n && base + lane < a.cap)
-        a.cand[static_cast<size_t>(q) * a.cap + base + lane] = buf[lane];
+    collect(a, q, lane < n, base + lane, lane < n ? buf[lane] : 0u, lo, bits);
 }
 
 // Float thresholds equal to the key bounds on canonical finite deltas:
@@ -381,11 +568,16 @@ __device__ __forceinline__ float pick(const float (&k)[kScanTokens], int s)
     return l[0];
 }
 
+__device__ void check_ranks(const MonArgs &a);
+template <int PASS>
+__device__ void select_digit(const MonArgs &a);
+
 __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(const MonArgs a)
 {
     extern __shared__ __align__(16) uint8_t scan_smem[];   // rings [warp][kRing], staging, barriers
     __shared__ float flo_s[MON_QUANTILES], fhi_s[MON_QUANTILES];
-    __shared__ uint32_t one_s;
+    __shared__ uint32_t one_s, lo_s[MON_QUANTILES];
+    __shared__ int bits_s[MON_QUANTILES];
     __shared__ int abort_s;
     volatile int *abort_flag = &abort_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -408,6 +600,8 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
         const uint32_t lo = a.st->lo[tid], hi = a.st->hi[tid];
         flo_s[tid] = tid == 0 ? abs_lo_threshold(lo) : signed_lo_threshold(lo);
         fhi_s[tid] = tid == 0 ? abs_hi_threshold(hi) : signed_hi_threshold(hi);
+        lo_s[tid] = lo;
+        bits_s[tid] = span_bits_of(lo, hi);
     }
     __syncthreads();
     float flo[MON_QUANTILES], fhi[MON_QUANTILES];
@@ -429,6 +623,8 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
     int at_or_above[MON_QUANTILES] = {0, 0, 0, 0};
 
     // The warp's k-th chunk: groups [c_k kChunk, (c_k + 1) kChunk), c_k = w + k warps.
+    // (Drawing the last fifth of the chunks from a shared counter evened out
+    // the CTAs' finish times but not the pass's: it is bound by HBM.)
     const int64_t w = static_cast<int64_t>(blockIdx.x) * kScanWarps + warp;
     auto whole = [&](int64_t k) { return (w + k * warps + 1) * kChunk <= full; };
     auto issue = [&](int64_t k) {   // lane 0: stage chunk k into ring slot k % kRing
@@ -521,10 +717,9 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
                 if (lane == 0)
                     base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(total));
                 base = __shfl_sync(0xffffffffu, base, 0) + static_cast<unsigned long long>(excl);
-                for (uint32_t b = inbits[q]; b != 0u; b &= b - 1u, ++base) {
-                    const float v = pick(dv, __ffs(b) - 1);
-                    if (base < a.cap)
-                        a.cand[static_cast<size_t>(q) * a.cap + base] = q == 0 ? key_abs(v) : key_signed(v);
+                for (uint32_t b = inbits[q]; __any_sync(0xffffffffu, b != 0u); b &= b - 1u, ++base) {
+                    const float v = b != 0u ? pick(dv, __ffs(b) - 1) : 0.f;
+                    collect(a, q, b != 0u, base, q == 0 ? key_abs(v) : key_signed(v), lo_s[q], bits_s[q]);
                 }
                 continue;
             }
@@ -537,7 +732,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
             staged[q] += total;
             __syncwarp();
             while (staged[q] >= 32) {   // uniform over the warp
-                flush_stage(a, buf, q, 32, lane);
+                flush_stage(a, buf, q, 32, lane, lo_s[q], bits_s[q]);
                 __syncwarp();
                 for (int i = lane; i + 32 < staged[q]; i += 32) {   // move the rest down
                     const uint32_t v = buf[i + 32];
@@ -572,16 +767,15 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
                 drain_wait(bar0 + 8u * static_cast<uint32_t>(j % kRing), static_cast<uint32_t>((j / kRing) & 1));
         if (lane == 0)
             atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
-        return;
-    }
-    if ((w + k * warps) * kChunk < G)
+    } else if ((w + k * warps) * kChunk < G) {
         step((w + k * warps) * kChunk, nullptr, std::true_type{});
+    }
 
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q)
         if (staged[q] > 0)
-            flush_stage(a, stage_all + (warp * MON_QUANTILES + q) * kStage, q, staged[q], lane);
+            flush_stage(a, stage_all + (warp * MON_QUANTILES + q) * kStage, q, staged[q], lane, lo_s[q], bits_s[q]);
     const int wu = __reduce_add_sync(0xffffffffu, n_used);
     const int we = __reduce_add_sync(0xffffffffu, n_ext);
     int wb[MON_QUANTILES];
@@ -596,57 +790,64 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
             if (wb[q])
                 atomicAdd(&a.st->below[q], static_cast<unsigned long long>(wb[q]));
     }
+    // The last CTA: ranks and mode, then (collected lists) the first digit.
+    if (last_cta(&a.st->ticket[1])) {
+        if (tid == 0)
+            check_ranks(a);
+        __syncthreads();
+        if (!a.st->empty && !a.st->fallback)   // uniform over the CTA
+            select_digit<1>(a);
+    }
 }
 
 // ---------------------------------------------------------------- ranks and mode
-__global__ void mon_check_kernel(const MonArgs a)
+// Thread 0 of the full pass's last CTA.  For each quantile at level L over the
+// n used tokens: h = (n - 1) L, ranks floor(h) and floor(h) + 1 (capped at
+// n - 1) and the weight h - floor(h).  Each quantile's two order statistics
+// must fall inside its list (below <= k, k + 1 < below + count, no overflow),
+// else the selection runs over all tokens; the ranks are then taken relative
+// to the list (collected) or to all tokens.
+__device__ void check_ranks(const MonArgs &a)
 {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (threadIdx.x != 0)
-        return;
     MonState *st = a.st;
-    const long long n = static_cast<long long>(st->n_used);
+    const long long n = static_cast<long long>(__ldcg(&st->n_used));
     st->empty = n == 0;
     if (n == 0)
         return;
     bool ok = true;
-    long long k[MON_QUANTILES], k1[MON_QUANTILES];
+    long long k[MON_QUANTILES], k1[MON_QUANTILES], below[MON_QUANTILES], cnt[MON_QUANTILES];
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q) {   // all loads first: they are independent
+        below[q] = static_cast<long long>(__ldcg(&st->below[q]));
+        cnt[q] = static_cast<long long>(__ldcg(&st->count[q]));
+    }
     for (int q = 0; q < MON_QUANTILES; ++q) {
         const double h = static_cast<double>(n - 1) * level(q);
         const double fl = floor(h);
         k[q] = static_cast<long long>(fl);
         k1[q] = k[q] + 1 < n ? k[q] + 1 : k[q];
         st->frac[q] = h - fl;
-        const long long b = static_cast<long long>(st->below[q]);
-        const long long c = static_cast<long long>(st->count[q]);
-        ok = ok && c <= static_cast<long long>(a.cap) && b <= k[q] && k1[q] < b + c;
+        ok = ok && cnt[q] <= static_cast<long long>(a.cap) && below[q] <= k[q] && k1[q] < below[q] + cnt[q];
     }
     st->fallback = ok ? 0 : 1;
     for (int q = 0; q < MON_QUANTILES; ++q) {
-        const long long b = ok ? static_cast<long long>(st->below[q]) : 0;
+        const long long b = ok ? below[q] : 0;
         st->rank[2 * q] = k[q] - b;
         st->rank[2 * q + 1] = k1[q] - b;
-        const uint32_t span = st->hi[q] - st->lo[q];
-        st->span_bits[q] = ok ? (span == 0u ? 0 : 32 - __clz(static_cast<int>(span))) : 32;
+        st->span_bits[q] = ok ? span_bits_of(st->lo[q], st->hi[q]) : 32;
     }
 }
 
 // ---------------------------------------------------------------- radix passes
-// Digits of a value with b significant bits (b = 32 for raw keys): pass 1 the
-// top 11 (bits b-11 .. b-1), pass 2 the next 11, pass 3 the rest (<= 10).
-__device__ __forceinline__ int digit_shift(int pass, int b)
-{
-    return pass == 1 ? max(b - 11, 0) : pass == 2 ? max(b - 22, 0) : 0;
-}
-
 template <int PASS>
 constexpr int pass_bins() { return PASS == 3 ? MON_BINS3 : MON_BINS2; }
 
+// Shared-memory histogram words of a pass: pass 1 runs only over all tokens
+// (delta's key), passes 2 and 3 keep one histogram per target.
 template <int PASS>
 constexpr int pass_smem_words()
 {
-    return PASS == 1 ? MON_QUANTILES * MON_BINS1 : MON_TARGETS * pass_bins<PASS>();
+    return PASS == 1 ? MON_BINS1 : MON_TARGETS * pass_bins<PASS>();
 }
 
 // Does v carry the digits that `prefix` fixed in the passes before PASS?
@@ -659,184 +860,88 @@ __device__ __forceinline__ bool in_prefix(uint32_t v, uint32_t prefix, int b)
     return (static_cast<uint64_t>(v) >> s) == (static_cast<uint64_t>(prefix) >> s);
 }
 
+// Per target (warp j of the calling CTA): the bin of pass PASS that holds the
+// target's rank, and the rank left inside it.  Pass 1 reads the lists'
+// histograms (built by the full pass) or the all-token one.  Lane l owns bins
+// [l seg, (l + 1) seg), read from L2 in chunks of 16: their total, a warp
+// scan, then the lane whose segment holds the rank reads its chunks again to
+// find the bin.  Needs a CTA of MON_TARGETS warps.
 template <int PASS>
-__device__ __forceinline__ uint32_t digit_of(uint32_t v, int b)
-{
-    const int s = digit_shift(PASS, b);
-    const int top = PASS == 1 ? b : digit_shift(PASS - 1, b);
-    const int width = top - s;   // <= 11
-    return (v >> s) & ((1u << width) - 1u);
-}
-
-template <int PASS>
-__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(const MonArgs a)
+__device__ void select_digit(const MonArgs &a)
 {
     constexpr int NB = pass_bins<PASS>();
-    extern __shared__ __align__(16) uint32_t mon_sh[];
-    __shared__ uint32_t pref_s[MON_TARGETS], lo_s[MON_QUANTILES];
-    __shared__ int bits_s[MON_QUANTILES];
-    __shared__ int mode_s;   // 0 nothing to do, 1 the collected lists, 2 all tokens
-    __shared__ unsigned long long cnt_s[MON_QUANTILES];
-    const int tid = threadIdx.x;
-    pdl_wait();
-    pdl_launch_dependents();
-    MonState *st = a.st;
-    if (tid < MON_TARGETS)
-        pref_s[tid] = st->prefix[tid];
-    if (tid < MON_QUANTILES) {
-        lo_s[tid] = st->lo[tid];
-        bits_s[tid] = st->span_bits[tid];
-        cnt_s[tid] = std::min<unsigned long long>(st->count[tid], a.cap);
-    }
-    if (tid == 0)
-        mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
-    __syncthreads();
-    const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
-    // Collected keys: at least kKeysPerCta per CTA, so that few CTAs pay for
-    // clearing and adding their histograms; the others leave at once.
-    constexpr unsigned long long kKeysPerCta = 16 * MON_THREADS;
-    const unsigned long long ctas = std::min<unsigned long long>(gridDim.x, (total + kKeysPerCta - 1) / kKeysPerCta);
-    // uniform over the CTA: nothing to select, or no collected key for this CTA
-    if (mode_s == 0 || (mode_s == 1 && blockIdx.x >= ctas))
-        return;
-    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS)
-        mon_sh[i] = 0u;
-    __syncthreads();
-    if (mode_s == 1) {
-        // the collected keys of the four lists, one list after another
-        for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i < total;
-             i += ctas * MON_THREADS) {
-            int q = 0;
-            unsigned long long off = i;
-            while (off >= cnt_s[q]) {   // ends at q <= 3 because i < total
-                off -= cnt_s[q];
-                ++q;
-            }
-            const uint32_t v = a.cand[static_cast<size_t>(q) * a.cap + off] - lo_s[q];
-            const int b = bits_s[q];
-            if (PASS == 1) {
-                atomicAdd(mon_sh + q * MON_BINS1 + digit_of<1>(v, b), 1u);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 2 * q + e;
-                    if (in_prefix<PASS>(v, pref_s[j], b))
-                        atomicAdd(mon_sh + j * NB + digit_of<PASS>(v, b), 1u);
-                }
-            }
-        }
-    } else {
-        uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
-#pragma unroll
-        for (int j = 0; j < MON_TARGETS; ++j)
-            pr[j] = pref_s[j];
-        for_token_groups<MON_UNROLL>(a, [&](int64_t, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool used = valid[i] && usable(m[i], d[i]);
-                const uint32_t kd = key_signed(d[i]);
-                if (PASS == 1) {
-                    if (used)   // delta's key only; |delta|'s histogram follows (mon_select_kernel<1>)
-                        atomicAdd(mon_sh + (kd >> 21), 1u);
-                } else {
-                    const uint32_t ka = key_abs(d[i]);
-#pragma unroll
-                    for (int j = 0; j < MON_TARGETS; ++j) {
-                        const uint32_t k = j < 2 ? ka : kd;
-                        if (used && in_prefix<PASS>(k, pr[j], 32))
-                            atomicAdd(mon_sh + j * NB + digit_of<PASS>(k, 32), 1u);
-                    }
-                }
-            }
-        });
-    }
-    __syncthreads();
-    uint32_t *gh = PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 : a.hist3;
-    for (int i = tid; i < pass_smem_words<PASS>(); i += MON_THREADS) {
-        const uint32_t c = mon_sh[i];
-        if (c != 0u)
-            atomicAdd(gh + i, c);
-    }
-}
-
-// Per target (warp j): the bin of pass PASS that holds the target's rank, and
-// the rank left inside it; PASS 3 then writes the record.  One CTA of
-// MON_TARGETS warps.
-template <int PASS>
-__global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonArgs a)
-{
-    constexpr int NB = pass_bins<PASS>();
-    extern __shared__ __align__(16) uint32_t hist_s[];   // each warp's histogram, copied with coalesced loads
+    constexpr int CH = 16;
     const int tid = threadIdx.x, lane = tid & 31, j = tid >> 5, q = j >> 1;
     MonState *st = a.st;
-    pdl_wait();
-    pdl_launch_dependents();
-    if (!st->empty) {
-        const bool all_tokens = st->fallback != 0;
-        const int b = all_tokens ? 32 : st->span_bits[q];
-        // The all-token pass 1 counted delta's key only.  |delta| has a clear
-        // top bit, and its bin c holds the positive deltas of delta-bin
-        // 1024 + c and the negative ones of delta-bin 1023 - c.
-        const bool abs1 = PASS == 1 && all_tokens && j < 2;
-        const uint32_t *hg = PASS == 1 ? a.hist1 + (all_tokens ? 0 : q * MON_BINS1)
-                           : PASS == 2 ? a.hist2 + j * NB
-                                       : a.hist3 + j * NB;
-        uint32_t *h = hist_s + j * 2048;
-#pragma unroll 16
-        for (int x = lane; x < NB; x += 32)
-            h[x] = hg[x];
-        __syncwarp();
-        auto count = [&](int c) -> long long {
-            return abs1 ? static_cast<long long>(h[1024 + c]) + h[1023 - c] : static_cast<long long>(h[c]);
-        };
-        const long long r = st->rank[j];
-        const int SEG = (abs1 ? 1024 : NB) / 32;   // bins per lane
-        long long c = 0;
-        for (int x = 0; x < SEG; ++x)
-            c += count(lane * SEG + x);
-        long long incl = c;
+    if (st->empty)
+        return;
+    const bool all_tokens = st->fallback != 0;
+    const int b = all_tokens ? 32 : st->span_bits[q];
+    // The all-token pass 1 counted delta's key only (2048 bins); |delta|'s
+    // 1024 bins follow from it.
+    const bool abs1 = PASS == 1 && all_tokens && j < 2;
+    const uint32_t *hg = PASS == 1 ? a.hist1 + (all_tokens ? MON_QUANTILES : q) * MON_BINS1
+                       : PASS == 2 ? a.hist2 + j * NB
+                                   : a.hist3 + j * NB;
+    const int seg = (abs1 ? 1024 : NB) / 32;
+    auto chunk = [&](int k, uint32_t (&t)[CH]) {
+        const int c0 = lane * seg + CH * k;
+        if (abs1)
+            load_abs_segment<CH>(hg, 1024, c0, t);
+        else
+            load_segment<CH>(hg + c0, t);
+    };
+    const uint32_t r = static_cast<uint32_t>(st->rank[j]);   // < N < 2^31
+    uint32_t c = 0;
+#pragma unroll 1
+    for (int k = 0; k < seg / CH; ++k) {
+        uint32_t t[CH];
+        chunk(k, t);
+        c += segment_total(t);
+    }
+    uint32_t incl = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += v;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
-        int bin = -1;
-        long long before = 0;
-        if (hit != 0u) {
-            const int L = __ffs(hit) - 1;
-            if (lane == L) {
-                long long cum = incl - c;
-                for (int x = 0; x < SEG; ++x) {
-                    const long long hb = count(lane * SEG + x);
-                    if (cum + hb > r) {
-                        bin = lane * SEG + x;
-                        before = cum;
-                        break;
-                    }
-                    cum += hb;
-                }
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += x;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
+    int bin = -1;
+    uint32_t before = 0;
+    if (hit != 0u) {
+        const int L = __ffs(hit) - 1;
+        if (lane == L) {
+            uint32_t cum = incl - c;
+#pragma unroll 1
+            for (int k = 0; k < seg / CH && bin < 0; ++k) {
+                uint32_t t[CH];
+                chunk(k, t);
+                const int x = find_in_segment(t, cum, r, before);
+                if (x >= 0)
+                    bin = lane * seg + CH * k + x;
+                cum += segment_total(t);
             }
-            bin = __shfl_sync(0xffffffffu, bin, L);
-            before = __shfl_sync(0xffffffffu, before, L);
         }
-        if (lane == 0) {
-            if (bin < 0) {   // cannot happen when the counts are consistent
-                atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
-                st->empty = 1;
-            } else {
-                st->rank[j] = r - before;
-                st->prefix[j] |= static_cast<uint32_t>(bin) << digit_shift(PASS, b);
-            }
+        bin = __shfl_sync(0xffffffffu, bin, L);
+        before = __shfl_sync(0xffffffffu, before, L);
+    }
+    if (lane == 0) {
+        if (bin < 0) {   // cannot happen when the counts are consistent
+            atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
+            st->empty = 1;
+        } else {
+            st->rank[j] = static_cast<long long>(r - before);
+            st->prefix[j] |= static_cast<uint32_t>(bin) << digit_shift(PASS, b);
         }
     }
-    if (PASS != 3)
-        return;
-    __syncthreads();
-    if (tid != 0)
-        return;
-    const unsigned long long n = st->n_used, ne = st->n_extreme;
+}
+
+// Thread 0: the batch record from the selected keys.
+__device__ void write_record(const MonArgs &a)
+{
+    MonState *st = a.st;
+    const unsigned long long n = __ldcg(&st->n_used), ne = __ldcg(&st->n_extreme);
     double *o = a.out;
     o[TIM_MON_N_USED] = static_cast<double>(n);
     o[TIM_MON_N_EXTREME] = static_cast<double>(ne);
@@ -859,6 +964,125 @@ __global__ void __launch_bounds__(MON_TARGETS * 32) mon_select_kernel(const MonA
     }
 }
 
+// Radix pass PASS over the collected lists (passes 2 and 3; pass 1 of the
+// lists came with the full pass) or over all tokens (the fallback, all three
+// passes), into shared-memory histograms added to the global ones; the CTA
+// that finishes last then selects the digit, and after pass 3 writes the
+// record.
+template <int PASS>
+__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(const MonArgs a)
+{
+    constexpr int NB = pass_bins<PASS>();
+    extern __shared__ __align__(16) uint32_t mon_sh[];
+    __shared__ uint32_t pref_s[MON_TARGETS], lo_s[MON_QUANTILES];
+    __shared__ int bits_s[MON_QUANTILES];
+    __shared__ int mode_s;   // 0 nothing to do, 1 the collected lists, 2 all tokens
+    __shared__ unsigned long long cnt_s[MON_QUANTILES], start_s[MON_QUANTILES];
+    const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
+    MonState *st = a.st;
+    if (tid < MON_TARGETS)
+        pref_s[tid] = st->prefix[tid];
+    if (tid < MON_QUANTILES) {
+        lo_s[tid] = st->lo[tid];
+        bits_s[tid] = st->span_bits[tid];
+        cnt_s[tid] = std::min<unsigned long long>(st->count[tid], a.cap);
+    }
+    if (tid == 0)
+        mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
+    __syncthreads();
+    if (PASS == 1 && mode_s != 2)   // uniform over the grid
+        return;
+    if (tid == 0) {
+        start_s[0] = 0;
+        for (int q = 1; q < MON_QUANTILES; ++q)
+            start_s[q] = start_s[q - 1] + cnt_s[q - 1];
+    }
+    __syncthreads();
+    const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
+    // Collected keys: at least kKeysPerCta per CTA, so that few CTAs pay for
+    // clearing and adding their histograms; the others only take the ticket.
+    constexpr unsigned long long kKeysPerCta = 16 * MON_THREADS;
+    const unsigned long long ctas = std::min<unsigned long long>(gridDim.x, (total + kKeysPerCta - 1) / kKeysPerCta);
+    const bool work = mode_s == 2 || (mode_s == 1 && blockIdx.x < ctas);   // uniform over the CTA
+    if (work) {
+        zero_histogram<pass_smem_words<PASS>()>(mon_sh);
+        __syncthreads();
+        if (PASS != 1 && mode_s == 1) {
+            // the collected keys of the four lists, one list after another;
+            // kBatch keys per thread loaded before any is used
+            constexpr int kBatch = 16;
+            const unsigned long long stride = ctas * MON_THREADS;
+            for (unsigned long long i0 = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i0 < total;
+                 i0 += kBatch * stride) {
+                uint32_t v[kBatch];
+                int qs[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const unsigned long long i = i0 + u * stride;
+                    qs[u] = -1;
+                    if (i < total) {
+                        const int q = (i >= start_s[1]) + (i >= start_s[2]) + (i >= start_s[3]);
+                        qs[u] = q;
+                        v[u] = __ldcs(a.cand + static_cast<size_t>(q) * a.cap + (i - start_s[q]));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int q = qs[u];
+                    if (q < 0)
+                        continue;
+                    const uint32_t x = v[u] - lo_s[q];
+                    const int b = bits_s[q];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = 2 * q + e;
+                        if (in_prefix<PASS>(x, pref_s[j], b))
+                            atomicAdd(mon_sh + j * NB + digit_of<PASS>(x, b), 1u);
+                    }
+                }
+            }
+        } else {
+            uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
+#pragma unroll
+            for (int j = 0; j < MON_TARGETS; ++j)
+                pr[j] = pref_s[j];
+            for_token_groups<MON_UNROLL>(a, [&](int64_t, const float (&d)[4], const bool (&m)[4],
+                                                const bool (&valid)[4]) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool used = valid[i] && usable(m[i], d[i]);
+                    const uint32_t kd = key_signed(d[i]);
+                    if (PASS == 1) {
+                        if (used)   // delta's key only; |delta|'s histogram follows (select_digit<1>)
+                            atomicAdd(mon_sh + (kd >> 21), 1u);
+                    } else {
+                        const uint32_t ka = key_abs(d[i]);
+#pragma unroll
+                        for (int j = 0; j < MON_TARGETS; ++j) {
+                            const uint32_t k = j < 2 ? ka : kd;
+                            if (used && in_prefix<PASS>(k, pr[j], 32))
+                                atomicAdd(mon_sh + j * NB + digit_of<PASS>(k, 32), 1u);
+                        }
+                    }
+                }
+            });
+        }
+        __syncthreads();
+        flush_histogram<pass_smem_words<PASS>()>(
+            mon_sh, PASS == 1 ? a.hist1 + MON_QUANTILES * MON_BINS1 : PASS == 2 ? a.hist2 : a.hist3);
+    }
+    if (last_cta(&st->ticket[1 + PASS])) {
+        select_digit<PASS>(a);
+        if (PASS == 3) {
+            __syncthreads();
+            if (tid == 0)
+                write_record(a);
+        }
+    }
+}
+
 template <typename K>
 cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const MonArgs &a)
 {
@@ -873,42 +1097,38 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-constexpr size_t kSampleSmem = 4 * (SBD + SBA);
-constexpr size_t kSelectSmem = 4 * MON_TARGETS * 2048;
+constexpr size_t kSampleSmem = 4 * SBD;
+
+template <int PASS>
+constexpr size_t pass_smem() { return 4 * pass_smem_words<PASS>(); }
+
+// Each kernel's dynamic shared memory.  (The largest shared-memory carveout
+// as a hint made the call ~6 us slower.)
+template <typename K>
+cudaError_t smem_attributes(K kernel, size_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
 
 } // namespace
 
 cudaError_t monitor_prepare_device()
 {
-    cudaError_t e = cudaFuncSetAttribute(mon_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSampleSmem));
+    cudaError_t e = smem_attributes(mon_sample_kernel, kSampleSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_bounds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSampleSmem));
+        e = smem_attributes(mon_scan_kernel, kScanSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSelectSmem));
+        e = smem_attributes(mon_pass_kernel<1>, pass_smem<1>());
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSelectSmem));
+        e = smem_attributes(mon_pass_kernel<2>, pass_smem<2>());
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_select_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSelectSmem));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kScanSmem));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 4 * pass_smem_words<1>());
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 4 * pass_smem_words<2>());
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mon_pass_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 4 * pass_smem_words<3>());
+        e = smem_attributes(mon_pass_kernel<3>, pass_smem<3>());
     return e;
 }
 
+// memset of the state and histograms, then sample (+ bounds), the full pass
+// (+ ranks and the lists' first digit), radix passes 1 (all tokens only), 2
+// and 3 (+ their digits and the record), chained by dependent launches.
 cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
 {
     cudaError_t e = cudaMemsetAsync(a.st, 0, MON_ZEROED_BYTES, stream);
@@ -918,25 +1138,19 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
     const int64_t want = (groups + MON_THREADS - 1) / MON_THREADS;
     const dim3 grid(static_cast<unsigned>(
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
-    const int64_t scan_want = (groups + (MON_THREADS / 32) * 32 * kScanGroups - 1) / ((MON_THREADS / 32) * 32 * kScanGroups);
     const dim3 scan_grid(static_cast<unsigned>(
-        std::max<int64_t>(1, std::min<int64_t>(scan_want, static_cast<int64_t>(kScanCtasPerSm) * num_sms))));
-    const int64_t runs = std::max<int64_t>(
-        1, std::min<int64_t>({static_cast<int64_t>(MON_SAMPLE_RUNS), (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN,
-                              2LL * num_sms}));
-    const dim3 block(MON_THREADS), sel(MON_TARGETS * 32);
-    if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(runs)), block, kSampleSmem, stream, a)) !=
+        std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(kScanCtasPerSm) * num_sms))));
+    const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
+    const int64_t sample_ctas =   // one CTA per SM at most: all start at once
+        std::max<int64_t>(1, std::min<int64_t>((runs + kRunsAtOnce - 1) / kRunsAtOnce, num_sms));
+    const dim3 block(MON_THREADS);
+    if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(sample_ctas)), block, kSampleSmem, stream, a)) !=
             cudaSuccess ||
-        (e = launch_pdl(mon_bounds_kernel, dim3(1), dim3(1024), kSampleSmem, stream, a)) != cudaSuccess ||
         (e = launch_pdl(mon_scan_kernel, scan_grid, block, kScanSmem, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_check_kernel, dim3(1), dim3(32), 0, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<1>, grid, block, 4 * pass_smem_words<1>(), stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_select_kernel<1>, dim3(1), sel, kSelectSmem, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<2>, grid, block, 4 * pass_smem_words<2>(), stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_select_kernel<2>, dim3(1), sel, kSelectSmem, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<3>, grid, block, 4 * pass_smem_words<3>(), stream, a)) != cudaSuccess)
+        (e = launch_pdl(mon_pass_kernel<1>, grid, block, pass_smem<1>(), stream, a)) != cudaSuccess ||
+        (e = launch_pdl(mon_pass_kernel<2>, grid, block, pass_smem<2>(), stream, a)) != cudaSuccess)
         return e;
-    return launch_pdl(mon_select_kernel<3>, dim3(1), sel, kSelectSmem, stream, a);
+    return launch_pdl(mon_pass_kernel<3>, grid, block, pass_smem<3>(), stream, a);
 }
 
 } // namespace tim

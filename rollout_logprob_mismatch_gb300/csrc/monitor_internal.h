@@ -33,14 +33,15 @@ struct MonState {
     double frac[MON_QUANTILES];                // interpolation weight of each quantile
     int empty;                                 // no used token
     int fallback;                              // 1: select over all tokens (a bound missed)
+    unsigned ticket[5];                        // CTAs finished: sample, full pass, passes 1..3
 };
 
-// Workspace: state, the radix histograms (pass 1 sized for four candidate
-// lists), the sample histograms (all zeroed per call), then four candidate
-// lists of `cap` keys.
+// Workspace: state, the radix histograms (pass 1: one per candidate list, then
+// the one of the selection over all tokens), the sample histograms (all zeroed
+// per call), then four candidate lists of `cap` keys.
 constexpr size_t MON_STATE_BYTES = 512;
 static_assert(sizeof(MonState) <= MON_STATE_BYTES, "state block");
-constexpr size_t MON_HIST1_WORDS = MON_QUANTILES * MON_BINS1;
+constexpr size_t MON_HIST1_WORDS = (MON_QUANTILES + 1) * MON_BINS1;
 constexpr size_t MON_HIST2_WORDS = MON_TARGETS * MON_BINS2;
 constexpr size_t MON_HIST3_WORDS = MON_TARGETS * MON_BINS3;
 constexpr size_t MON_SHIST_WORDS = MON_SBINS_D + MON_SBINS_A;
