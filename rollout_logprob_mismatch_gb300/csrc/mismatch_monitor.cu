@@ -164,11 +164,15 @@ __device__ __forceinline__ void load_abs_segment(const uint32_t *h, int half, in
 template <int SEG>
 __device__ __forceinline__ uint32_t segment_total(const uint32_t (&v)[SEG])
 {
-    uint32_t c = 0;
+    static_assert(SEG % 8 == 0, "eight partial sums");
+    uint32_t p[8];   // eight independent chains: a short dependency depth
 #pragma unroll
-    for (int x = 0; x < SEG; ++x)
-        c += v[x];
-    return c;
+    for (int t = 0; t < 8; ++t)
+        p[t] = v[t];
+#pragma unroll
+    for (int x = 8; x < SEG; ++x)
+        p[x % 8] += v[x];
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
 // The first bin x of the segment with cum + v[0] + ... + v[x] > r (cum: the
@@ -850,6 +854,13 @@ constexpr int pass_smem_words()
     return PASS == 1 ? MON_BINS1 : MON_TARGETS * pass_bins<PASS>();
 }
 
+// v[q] for a quantile index q in 0..3, by selects (v stays in registers).
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&v)[MON_QUANTILES], int q)
+{
+    const uint32_t lo = (q & 1) ? v[1] : v[0], hi = (q & 1) ? v[3] : v[2];
+    return (q & 2) ? hi : lo;
+}
+
 // Does v carry the digits that `prefix` fixed in the passes before PASS?
 template <int PASS>
 __device__ __forceinline__ bool in_prefix(uint32_t v, uint32_t prefix, int b)
@@ -1012,6 +1023,14 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
         if (PASS != 1 && mode_s == 1) {
             // the collected keys of the four lists, one list after another;
             // kBatch keys per thread loaded before any is used
+            uint32_t lo_r[MON_QUANTILES], bits_r[MON_QUANTILES], pr0[MON_QUANTILES], pr1[MON_QUANTILES];
+#pragma unroll
+            for (int q = 0; q < MON_QUANTILES; ++q) {
+                lo_r[q] = lo_s[q];
+                bits_r[q] = static_cast<uint32_t>(bits_s[q]);
+                pr0[q] = pref_s[2 * q];
+                pr1[q] = pref_s[2 * q + 1];
+            }
             constexpr int kBatch = 16;
             const unsigned long long stride = ctas * MON_THREADS;
             for (unsigned long long i0 = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i0 < total;
@@ -1033,12 +1052,14 @@ __global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(
                     const int q = qs[u];
                     if (q < 0)
                         continue;
-                    const uint32_t x = v[u] - lo_s[q];
-                    const int b = bits_s[q];
+                    // the list's bound, width and the two targets' prefixes, chosen
+                    // from registers (no shared-memory lookup on the key's path)
+                    const uint32_t x = v[u] - pick4(lo_r, q);
+                    const int b = static_cast<int>(pick4(bits_r, q));
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int j = 2 * q + e;
-                        if (in_prefix<PASS>(x, pref_s[j], b))
+                        if (in_prefix<PASS>(x, pick4(e == 0 ? pr0 : pr1, q), b))
                             atomicAdd(mon_sh + j * NB + digit_of<PASS>(x, b), 1u);
                     }
                 }
