@@ -48,7 +48,7 @@ namespace {
 constexpr int SAMPLE_SHIFT = 18;                         // sample bins: key >> 18
 constexpr int SBD = 1 << (32 - SAMPLE_SHIFT);            // 16384 bins of delta's key
 constexpr int SBA = 1 << (31 - SAMPLE_SHIFT);            // 8192 of |delta|'s key
-static_assert(SBD + SBA <= MON_SBINS_D + MON_SBINS_A, "sample histogram room");
+static_assert(SBD == MON_SBINS, "sample histogram room");
 constexpr double kSigmas = 6.0;                          // width of the bounds in rank standard deviations
 
 // Quantile levels: |delta| at 0.95 (quantile 0), the ratio at 0.01, 0.5, 0.99.
@@ -235,8 +235,10 @@ __device__ __forceinline__ void bounds_kind(const uint32_t (&v)[SEG], long long 
 // a sample quantile's rank (sqrt(m L (1 - L))) + 2; lo = the lowest key of the
 // bin holding the first (0 when that rank is at or below the sample's first),
 // hi = the highest key of the bin holding the second (all ones when at or
-// above the sample's last).  Run by one CTA of MON_THREADS threads on the
-// global sample histogram of delta's key.
+// above the sample's last).  The ranks are a heuristic (a rank off by one only
+// moves a bound; the check after the full pass keeps the result exact), so
+// they are taken in fp32.  Run by one CTA of MON_THREADS threads on the
+// global sample histogram of delta's key; both kinds' bins are loaded first.
 __device__ void compute_bounds(const MonArgs &a)
 {
     __shared__ uint32_t wsum[MON_THREADS / 32];
@@ -244,28 +246,24 @@ __device__ void compute_bounds(const MonArgs &a)
     __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
     const int tid = threadIdx.x;
     MonState *st = a.st;
+    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins, 32 |delta| bins per thread");
+    uint32_t vd[64], va[32];
+    load_segment<64>(a.shist + tid * 64, vd);
+    load_abs_segment<32>(a.shist, SBA, tid * 32, va);
     const long long m = static_cast<long long>(__ldcg(&st->sample_used));
-    if (tid < MON_QUANTILES) {   // fp64 in a few threads only: GB300 runs it slowly
-        const double L = level(tid);
-        const double j = static_cast<double>(m - 1) * L;
-        const long long w = static_cast<long long>(ceil(kSigmas * sqrt(static_cast<double>(m) * L * (1.0 - L)))) + 2;
-        rlo_s[tid] = static_cast<long long>(floor(j)) - w;
-        rhi_s[tid] = static_cast<long long>(ceil(j)) + w;
+    if (tid < MON_QUANTILES) {
+        const float L = static_cast<float>(level(tid));
+        const float j = static_cast<float>(m - 1) * L;
+        const long long w = static_cast<long long>(ceilf(static_cast<float>(kSigmas) *
+                                                         sqrtf(static_cast<float>(m) * L * (1.f - L)))) + 2;
+        rlo_s[tid] = static_cast<long long>(floorf(j)) - w;
+        rhi_s[tid] = static_cast<long long>(ceilf(j)) + w;
     }
     if (tid < 2 * MON_QUANTILES)
         bin_s[tid] = -1;
     __syncthreads();
-    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins, 32 |delta| bins per thread");
-    {
-        uint32_t v[64];
-        load_segment<64>(a.shist + tid * 64, v);
-        bounds_kind<0>(v, m, rlo_s, rhi_s, bin_s, wsum);
-    }
-    {
-        uint32_t v[32];
-        load_abs_segment<32>(a.shist, SBA, tid * 32, v);
-        bounds_kind<1>(v, m, rlo_s, rhi_s, bin_s, wsum);
-    }
+    bounds_kind<0>(vd, m, rlo_s, rhi_s, bin_s, wsum);
+    bounds_kind<1>(va, m, rlo_s, rhi_s, bin_s, wsum);
     __syncthreads();
     if (tid < MON_QUANTILES) {
         const int q = tid;

@@ -18,8 +18,7 @@ constexpr int MON_BINS2 = 2048;        // pass 2: 11 bits
 constexpr int MON_BINS3 = 1024;        // pass 3: 10 bits
 constexpr int MON_SAMPLE_RUNS = 1024;  // the sample: up to 1024 runs of MON_SAMPLE_RUN consecutive tokens
 constexpr int MON_SAMPLE_RUN = 1024;
-constexpr int MON_SBINS_D = 65536;     // sample histogram of delta's key >> 16
-constexpr int MON_SBINS_A = 32768;     // of |delta|'s key >> 16 (top bit clear)
+constexpr int MON_SBINS = 16384;       // sample histogram of delta's key >> 18 (|delta|'s follows from it)
 
 // Device state of one call, at the start of the workspace (zeroed before the sample).
 struct MonState {
@@ -37,14 +36,14 @@ struct MonState {
 };
 
 // Workspace: state, the radix histograms (pass 1: one per candidate list, then
-// the one of the selection over all tokens), the sample histograms (all zeroed
+// the one of the selection over all tokens), the sample histogram (all zeroed
 // per call), then four candidate lists of `cap` keys.
 constexpr size_t MON_STATE_BYTES = 512;
 static_assert(sizeof(MonState) <= MON_STATE_BYTES, "state block");
 constexpr size_t MON_HIST1_WORDS = (MON_QUANTILES + 1) * MON_BINS1;
 constexpr size_t MON_HIST2_WORDS = MON_TARGETS * MON_BINS2;
 constexpr size_t MON_HIST3_WORDS = MON_TARGETS * MON_BINS3;
-constexpr size_t MON_SHIST_WORDS = MON_SBINS_D + MON_SBINS_A;
+constexpr size_t MON_SHIST_WORDS = MON_SBINS;
 constexpr size_t MON_ZEROED_BYTES =
     MON_STATE_BYTES + 4 * (MON_HIST1_WORDS + MON_HIST2_WORDS + MON_HIST3_WORDS + MON_SHIST_WORDS);
 
@@ -63,7 +62,7 @@ struct MonArgs {
     double *out;         // [TIM_MON_FIELDS]
     MonState *st;
     uint32_t *hist1, *hist2, *hist3;
-    uint32_t *shist;     // sample histograms: delta [MON_SBINS_D], then |delta| [MON_SBINS_A]
+    uint32_t *shist;     // sample histogram of delta's key [MON_SBINS]
     uint32_t *cand;      // [MON_QUANTILES][cap] collected keys
     unsigned long long cap;
     int *status;
