@@ -302,7 +302,7 @@ enum tim_monitor_field {
  * One pass over the tokens (9 bytes read per token) after a sample of at most
  * 2^20 of them; exact selection among the few percent of tokens near each
  * quantile (over all tokens when a sample-based bound misses).  Scratch:
- * 525 KB + N / 4 bytes + 1 MB from the library's stream-ordered pool. */
+ * 205 KB + N bytes + 1 MB from the library's stream-ordered pool. */
 TIM_API int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
                                  int64_t N, float tau_tok, uint8_t *token_reject, double *out,
                                  tim_stream_t stream);
