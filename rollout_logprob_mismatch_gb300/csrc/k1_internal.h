@@ -18,7 +18,7 @@ constexpr int K1_STAGES = 4;      // TMA -> UMMA pipeline depth
 constexpr int K1_VCHUNK = 1024;   // vocabulary columns per split-V partial
 constexpr int K1_THREADS = 192;   // warp 0 TMA, warp 1 UMMA + TMEM, warps 2-5 epilogue
 constexpr int K1_CLUSTER = 2;     // CTAs per cluster: m-tiles sharing (multicasting) one W tile
-constexpr int K1_W_BOX_ROWS = K1_BN / K1_CLUSTER;   // W rows each CTA of a cluster loads
+constexpr int K1_W_BOX_ROWS = K1_BN / K1_CLUSTER;   // W rows of one TMA box (a CTA of a 2-CTA cluster loads one)
 // Units walk the vocabulary in bands of m-tiles whose h rows (at most this many
 // bytes) stay in L2 while the band's clusters stream each W chunk from HBM once.
 // (TIM_K1_BAND_MB overrides it; the band changes the order of work, never a result.)
@@ -48,7 +48,8 @@ struct K1Args {
     int32_t N, D, V;
     int32_t w_segments;       // 1: W bf16 [V, D]; 3: fp32 W split into three bf16 parts, [V][3][Dp]
     int32_t num_m_tiles, num_chunks;
-    int32_t num_m_groups;     // ceil(num_m_tiles / K1_CLUSTER): m-tiles of one cluster
+    int32_t cluster;          // CTAs per cluster: K1_CLUSTER, or 1 for a batch of one m-tile
+    int32_t num_m_groups;     // ceil(num_m_tiles / cluster): m-tiles of one cluster
     int32_t band, units;      // units = num_m_groups * num_chunks, one per cluster
     int32_t tail_mt;          // m-tile read through the padded tail map, or -1
     uint64_t wait_budget_ns;
@@ -59,7 +60,23 @@ struct K1Args {
     int64_t dz_ld;
 };
 
-// Launches one cluster of K1_CLUSTER CTAs per unit, at most as many clusters
+// A batch of one m-tile (at most K1_BM rows) runs in clusters of one CTA that
+// stream their own W tiles: a cluster peer would only multiply a tile of
+// padding rows (measured: the W stream then left HBM at 0.74 of the copy rate).
+// Larger batches run in clusters of K1_CLUSTER m-tiles that share each W tile.
+// Sets cluster, num_m_groups, band (m-groups whose h rows stay in L2) and units.
+inline void k1_set_units(K1Args &a, int64_t m_tiles, int64_t chunks, int64_t D)
+{
+    const int cl = m_tiles <= 1 ? 1 : K1_CLUSTER;
+    const int64_t m_groups = (m_tiles + cl - 1) / cl;
+    const int64_t band = k1_band_bytes() / (int64_t(cl) * K1_BM * D * 2);
+    a.cluster = cl;
+    a.num_m_groups = static_cast<int32_t>(m_groups);
+    a.band = static_cast<int32_t>(band < 1 ? 1 : band < m_groups ? band : m_groups);
+    a.units = static_cast<int32_t>(m_groups * chunks);
+}
+
+// Launches one cluster of a.cluster CTAs per unit, at most as many clusters
 // as fit on the device at once (persistent).  mode 0: forward; 1: backward dz.
 cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w, const CUtensorMap &tmap_h_tail,
                            const K1Args &a, cudaStream_t stream, int mode = 0);

@@ -11,7 +11,8 @@
 //              [128 x 64], multicast to both CTAs of the cluster (each W byte
 //              leaves L2 once per cluster), 128-byte swizzle, into a 4-stage
 //              shared-memory ring; a stage is refilled only when the UMMA of
-//              both CTAs has released it;
+//              both CTAs has released it (a batch of one m-tile runs in
+//              clusters of one CTA that load both halves of each W tile);
 //   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
 //              into one of two TMEM accumulators (2 x 256 columns), k ascending;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
@@ -49,7 +50,7 @@ struct Unit {
 // Units run m-tile fastest inside a band of `band` m-tiles, so the CTAs that are
 // resident together share the same W chunk (read once from HBM, then from L2)
 // while the band's h rows stay in L2.  The order affects speed only.
-// Returns the unit's m-group (K1_CLUSTER consecutive m-tiles, one per CTA of
+// Returns the unit's m-group (a.cluster consecutive m-tiles, one per CTA of
 // the cluster) in .mt and its vocabulary chunk in .ch.
 __device__ __forceinline__ Unit unit_of(int u, const K1Args &a)
 {
@@ -80,7 +81,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 // MODE 0: the forward (per-chunk max / sum and the target logit).  MODE 1: the
 // backward's logit gradient dz = g (onehot(a) - p) / tau, p = softmax(z / tau)
 // from the forward's lse, written as bf16 rows of length a.dz_ld.
-template <int MODE>
+template <int MODE, int CL>
 __global__ void __launch_bounds__(K1_THREADS, 1)
     k1_main_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_h_tail, const K1Args a)
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < K1_STAGES; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), K1_CLUSTER);   // released by the UMMA of every CTA of the cluster
+            mbar_init(empty(s), CL);   // released by the UMMA of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
@@ -133,9 +134,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t rank = cluster_ctarank();
-    const int cid = blockIdx.x / K1_CLUSTER;
-    const int ncl = gridDim.x / K1_CLUSTER;
-    constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << K1_CLUSTER) - 1);
+    const int cid = blockIdx.x / CL;
+    const int ncl = gridDim.x / CL;
+    constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << CL) - 1);
     const int KBH = (a.D + K1_BK - 1) / K1_BK;   // k-tiles of h
     const int KB = KBH * a.w_segments;          // k-tiles of W: 1 or 3 bf16 parts of each weight
     const uint64_t budget = a.wait_budget_ns;
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             bool ok = true;
             for (int u = cid; ok && u < a.units; u += ncl) {
                 const Unit w = unit_of(u, a);
-                const int mt = w.mt * K1_CLUSTER + static_cast<int>(rank);
+                const int mt = w.mt * CL + static_cast<int>(rank);
                 // the last m-tile of a batch whose size is not a multiple of 16 rows
                 // reads a zero-padded copy of its rows (same values, fast loads); an
                 // m-tile past the batch (the cluster peer of a last odd m-tile) reads
@@ -174,9 +175,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         tma_load_2d(sA + stage * K1_A_BYTES, hmap, full(stage), kh * K1_BK, hrow, pol_h);
                         if (++kh == KBH)
                             kh = 0;
-                        tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / K1_CLUSTER),
-                                              &tmap_w, full(stage), kb * K1_BK,
-                                              v0 + static_cast<int>(rank) * K1_W_BOX_ROWS, kAllCtas, pol_w);
+                        if (CL == 1) {   // both halves of the W tile, same layout as the multicast
+                            tma_load_2d(sB + stage * K1_B_BYTES, &tmap_w, full(stage), kb * K1_BK, v0, pol_w);
+                            tma_load_2d(sB + stage * K1_B_BYTES + K1_B_BYTES / 2, &tmap_w, full(stage),
+                                        kb * K1_BK, v0 + K1_W_BOX_ROWS, pol_w);
+                        } else {
+                            tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / CL), &tmap_w,
+                                                  full(stage), kb * K1_BK, v0 + static_cast<int>(rank) * K1_W_BOX_ROWS,
+                                                  kAllCtas, pol_w);
+                        }
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == K1_STAGES) {
@@ -218,7 +225,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < K1_BK / 16; ++k)   // +32 bytes along K per step
                             umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
-                        umma_commit_multicast(empty(stage), kAllCtas);
+                        if (CL == 1)
+                            umma_commit(empty(stage));
+                        else
+                            umma_commit_multicast(empty(stage), kAllCtas);
                         if (++stage == K1_STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         for (int u = cid; ok && u < a.units; u += ncl) {
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
-            const int row = (w.mt * K1_CLUSTER + static_cast<int>(rank)) * K1_BM + r_in_tile;
+            const int row = (w.mt * CL + static_cast<int>(rank)) * K1_BM + r_in_tile;
             const bool live = row < a.N;
             const int tgt = live ? __ldg(a.targets + row) : -1;
             const float gs = live ? __ldg(a.grad + row) * a.inv_temp : 0.f;   // g / tau
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         for (int u = cid; ok && u < a.units; u += ncl) {
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
-            const int row = (w.mt * K1_CLUSTER + static_cast<int>(rank)) * K1_BM + r_in_tile;
+            const int row = (w.mt * CL + static_cast<int>(rank)) * K1_BM + r_in_tile;
             const int tgt = row < a.N ? __ldg(a.targets + row) : -1;
             float run_m = -INFINITY, run_s = 0.f, zt = 0.f;
             bool found = false;
@@ -454,11 +464,12 @@ int64_t k1_band_bytes()
 
 cudaError_t k1_prepare_device()
 {
-    cudaError_t e = cudaFuncSetAttribute(k1_main_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(K1_SMEM_BYTES));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k1_main_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(K1_SMEM_BYTES));
+    cudaError_t e = cudaSuccess;
+    for (auto kernel : {k1_main_kernel<0, K1_CLUSTER>, k1_main_kernel<1, K1_CLUSTER>, k1_main_kernel<0, 1>,
+                        k1_main_kernel<1, 1>})
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(K1_SMEM_BYTES));
     return e;
 }
 
@@ -466,8 +477,11 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
                            const K1Args &a,
                            cudaStream_t stream, int mode)
 {
-    static int max_clusters[2][64] = {};   // per mode and device, found once (the same value from any thread)
-    auto kernel = mode == 1 ? k1_main_kernel<1> : k1_main_kernel<0>;
+    static int max_clusters[2][2][64] = {};   // per cluster size, mode and device, found once
+    const int cl = a.cluster == 1 ? 1 : K1_CLUSTER;
+    const int ci = cl == 1 ? 1 : 0;
+    auto kernel = cl == 1 ? (mode == 1 ? k1_main_kernel<1, 1> : k1_main_kernel<0, 1>)
+                          : (mode == 1 ? k1_main_kernel<1, K1_CLUSTER> : k1_main_kernel<0, K1_CLUSTER>);
     const int md = mode == 1 ? 1 : 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -476,7 +490,7 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = K1_CLUSTER;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1] = pdl_attribute();
@@ -485,17 +499,17 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev >= 0 && dev < 64 && max_clusters[md][dev] == 0) {
+    if (dev >= 0 && dev < 64 && max_clusters[ci][md][dev] == 0) {
         int n = 0;
-        cfg.gridDim = dim3(K1_CLUSTER * 1024, 1, 1);
+        cfg.gridDim = dim3(cl * 1024, 1, 1);
         e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
         if (e != cudaSuccess)
             return e;
-        max_clusters[md][dev] = n > 0 ? n : 1;
+        max_clusters[ci][md][dev] = n > 0 ? n : 1;
     }
     const int clusters =
-        static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[md][dev] : 1));
-    cfg.gridDim = dim3(K1_CLUSTER * clusters, 1, 1);
+        static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[ci][md][dev] : 1));
+    cfg.gridDim = dim3(cl * clusters, 1, 1);
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, tmap_h_tail, a);
 }

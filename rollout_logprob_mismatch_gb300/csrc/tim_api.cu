@@ -314,11 +314,7 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     a.w_segments = w_segments;
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);
-    const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
-    a.num_m_groups = static_cast<int32_t>(m_groups);
-    const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
-    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
-    a.units = static_cast<int32_t>(m_groups * chunks);
+    tim::k1_set_units(a, m_tiles, chunks, D);
     a.wait_budget_ns = wait_budget_ns();
     a.tail_mt = tail_mt;
     e = tim::k1_launch_main(th, tw, th_tail, a, s);
@@ -497,7 +493,6 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
             (rc = tail_map(hc, n, D, static_cast<char *>(ws) + dz_bytes, th, s, &th_tail, &tail_mt)) != TIM_OK)
             break;
         const int64_t m_tiles = (n + tim::K1_BM - 1) / tim::K1_BM;
-        const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
         tim::K1Args a{};
         a.targets = targets + r0;
         a.status = dev->status;
@@ -508,10 +503,7 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
         a.w_segments = 1;
         a.num_m_tiles = static_cast<int32_t>(m_tiles);
         a.num_chunks = static_cast<int32_t>(chunks_v);
-        a.num_m_groups = static_cast<int32_t>(m_groups);
-        const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
-        a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
-        a.units = static_cast<int32_t>(m_groups * chunks_v);
+        tim::k1_set_units(a, m_tiles, chunks_v, D);
         a.wait_budget_ns = wait_budget_ns();
         a.grad = grad_logp + r0;
         a.lse_in = lse + r0;

@@ -180,11 +180,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.V = static_cast<int32_t>(V);
     a.num_m_tiles = static_cast<int32_t>(m_tiles);
     a.num_chunks = static_cast<int32_t>(chunks);
-    const int64_t m_groups = (m_tiles + tim::K1_CLUSTER - 1) / tim::K1_CLUSTER;
-    a.num_m_groups = static_cast<int32_t>(m_groups);
-    const int64_t band = std::max<int64_t>(1, tim::k1_band_bytes() / (int64_t(tim::K1_CLUSTER) * tim::K1_BM * D * 2));
-    a.band = static_cast<int32_t>(std::min<int64_t>(band, m_groups));
-    a.units = static_cast<int32_t>(m_groups * chunks);
+    tim::k1_set_units(a, m_tiles, chunks, D);
     a.wait_budget_ns = wait_budget_ns();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     a.tail_mt = -1;   // no room for a padded tail here: the same values through the plain map
