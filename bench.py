@@ -48,8 +48,8 @@ K2_BW_TOKENS = 1 << 27
 # only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
 # profiles/k2_seq_kernel_2e25_tokens.md).
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3098470400 read + 17669632 written
-    ("k1", "8734d25bc279ecd0"): 3098470400 + 17669632,
+    # token logprob, N = 8192, D = 4096, V = 151936: 3044126208 read + 18182144 written
+    ("k1", "2ff80d9024b65205"): 3044126208 + 18182144,
     # mismatch pass, 2^25 tokens: 305287168 read + 98403840 written (traffic scales with tokens)
     ("k2", "b52af0477f7a6c75"): 305287168 + 98403840,
     # TIS-weighted PPO surrogate, 2^25 tokens: 612941056 read + 216222720 written (scales with tokens)
