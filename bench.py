@@ -467,6 +467,7 @@ def run_gb300(args):
     ppo_bw = ppo_bandwidth(tim, dev, stream, peaks) if not args.skip_ppo else None
     mon_bw = monitor_bandwidth(tim, dev, stream, peaks) if not args.skip_monitor else None
     sweep = batch_size_sweep(tim, dev, stream, Wd, D, V, peaks) if not args.skip_sweep else None
+    heads = head_shapes_measure(tim, dev, stream, peaks) if not args.skip_heads else None
     fp32h = fp32_head_measure(tim, dev, stream, peaks, hd, ad, V) if not args.skip_fp32_head else None
     bwd = backward_measure(tim, dev, stream, peaks, hd, Wd, ad) if not args.skip_backward else None
     tim.check()
@@ -514,8 +515,64 @@ def run_gb300(args):
         line["backward"] = bwd
     if sweep is not None:
         line["sweep"] = sweep
+    if heads is not None:
+        line["head_shapes"] = heads
     print(json.dumps(line), flush=True)
     return 0
+
+
+def head_shapes_measure(tim, dev, stream, peaks, names=("llama3_8b", "dsv3"), reps=5, warmup=2):
+    """The step (token logprob + mismatch statistics) on the other head shapes
+    of the workloads: the Llama-3-8B-shaped head (N = 32768 in lognormal
+    sequences, 30% masked) and the DeepSeek-V3-shaped one (N = 16384, D = 7168,
+    32 x 512).  h ~ N(0, h_std^2) and W ~ N(0, w_std^2) in bf16 and uniform
+    targets drawn on the device (the values do not change the work), segments
+    and masks from the workload generators, rollout = trainer + N(0,
+    rollout_std^2); L2 flushed before each step."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = []
+    for name in names:
+        cfg = wl.CONFIGS[name]
+        N, D, V = cfg.N, cfg.D, cfg.V
+        h = (torch.randn((N, D), generator=g, device=dev) * cfg.h_std).to(torch.bfloat16)
+        W = (torch.randn((V, D), generator=g, device=dev) * cfg.w_std).to(torch.bfloat16)
+        a = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
+        off = wl.draw_segments(cfg, seed=0)
+        S = len(off) - 1
+        offd = torch.from_numpy(off).to(dev)
+        maskd = torch.from_numpy(wl.draw_mask(cfg, off, seed=0)).to(dev)
+        lp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        tim.token_logprob(h, W, a, lp, lse)
+        ro = lp + cfg.rollout_std * torch.randn(N, generator=g, device=dev)
+        k2out = {"seq_stats": torch.empty((S, 12), dtype=torch.float32, device=dev),
+                 "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
+                 "batch": torch.empty(20, dtype=torch.float64, device=dev), "token_weight": None}
+        for _ in range(warmup):
+            tim.token_logprob(h, W, a, lp, lse)
+            tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(i)
+            ev[i][0].record(stream)
+            tim.token_logprob(h, W, a, lp, lse)
+            ev[i][1].record(stream)
+            tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = float(np.mean([e[0].elapsed_time(e[1]) * 1e-3 for e in ev]))
+        t2 = float(np.mean([e[1].elapsed_time(e[2]) * 1e-3 for e in ev]))
+        flops = 2.0 * N * V * D
+        out.append({"workload": "%s_head+mismatch" % name, "N": N, "D": D, "V": V, "num_seqs": S,
+                    "step_ms": (t1 + t2) * 1e3, "tokens_per_s": N / (t1 + t2),
+                    "token_logprob_ms": t1 * 1e3, "tflops": flops / t1 / 1e12,
+                    "frac": flops / t1 / 1e12 / peaks["bf16_tflops"], "bound": "tensor",
+                    "mismatch_pass_us": t2 * 1e6})
+        del h, W, a, lp, lse, ro
+    return out
 
 
 def batch_size_sweep(tim, dev, stream, Wd, D, V, peaks, sizes=(1, 7, 512, 4096, 32768), reps=5):
@@ -764,6 +821,7 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-k2-bandwidth", action="store_true")
     ap.add_argument("--skip-sweep", action="store_true")
+    ap.add_argument("--skip-heads", action="store_true", help="skip the Llama- and DeepSeek-shaped heads")
     ap.add_argument("--skip-ppo", action="store_true")
     ap.add_argument("--skip-monitor", action="store_true")
     ap.add_argument("--skip-fp32-head", action="store_true")
