@@ -570,6 +570,7 @@ def head_shapes_measure(tim, dev, stream, peaks, names=("llama3_8b", "dsv3"), re
                     "step_ms": (t1 + t2) * 1e3, "tokens_per_s": N / (t1 + t2),
                     "token_logprob_ms": t1 * 1e3, "tflops": flops / t1 / 1e12,
                     "frac": flops / t1 / 1e12 / peaks["bf16_tflops"], "bound": "tensor",
+                    "frac_of_sustained": flops / t1 / 1e12 / peaks["bf16_tflops_sustained"],
                     "mismatch_pass_us": t2 * 1e6})
         del h, W, a, lp, lse, ro
     return out
