@@ -243,6 +243,14 @@ def _need(t, name, dtype, ndim, device=None):
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
 
 
+def _need_out(t, name, dtype, shape, device):
+    """An output buffer the kernels write in full: exact dtype, shape, device,
+    contiguous (a shorter buffer would be written past its end)."""
+    _need(t, name, dtype, len(shape), device)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
 def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None, temperature: float = 1.0):
     """(logp [N] fp32, lse [N] fp32) for bf16 h [N, D], bf16 W [V, D], int32 targets [N]:
     log softmax(h W^T / temperature) at the targets (temperature 1: raw logits)."""
@@ -260,8 +268,8 @@ def token_logprob(h, W, targets, out_logp=None, out_lse=None, stream=None, tempe
         out_logp = torch.empty(N, dtype=torch.float32, device=dev)
     if out_lse is None:
         out_lse = torch.empty(N, dtype=torch.float32, device=dev)
-    _need(out_logp, "out_logp", torch.float32, 1, dev)
-    _need(out_lse, "out_lse", torch.float32, 1, dev)
+    _need_out(out_logp, "out_logp", torch.float32, (N,), dev)
+    _need_out(out_lse, "out_lse", torch.float32, (N,), dev)
     with torch.cuda.device(dev):
         if temperature == 1.0:
             rc = tim_token_logprob(h.data_ptr(), W.data_ptr(), targets.data_ptr(), N, D, V,
@@ -296,8 +304,8 @@ def token_logprob_backward(h, W, targets, grad_logp, lse, temperature: float = 1
         if accumulate_dW:
             raise ValueError("accumulate_dW needs dW")
         dW = torch.empty((V, D), dtype=torch.float32, device=dev)
-    _need(dh, "dh", torch.float32, 2, dev)
-    _need(dW, "dW", torch.float32, 2, dev)
+    _need_out(dh, "dh", torch.float32, (N, D), dev)
+    _need_out(dW, "dW", torch.float32, (V, D), dev)
     with torch.cuda.device(dev):
         rc = tim_token_logprob_backward(h.data_ptr(), W.data_ptr(), targets.data_ptr(), grad_logp.data_ptr(),
                                         lse.data_ptr(), N, D, V, temperature, dh.data_ptr(), dW.data_ptr(),
@@ -346,8 +354,8 @@ def token_logprob_fp32_head(h, W_split, targets, out_logp=None, out_lse=None, st
         out_logp = torch.empty(N, dtype=torch.float32, device=dev)
     if out_lse is None:
         out_lse = torch.empty(N, dtype=torch.float32, device=dev)
-    _need(out_logp, "out_logp", torch.float32, 1, dev)
-    _need(out_lse, "out_lse", torch.float32, 1, dev)
+    _need_out(out_logp, "out_logp", torch.float32, (N,), dev)
+    _need_out(out_lse, "out_lse", torch.float32, (N,), dev)
     with torch.cuda.device(dev):
         rc = tim_token_logprob_fp32_head(h.data_ptr(), W_split.data_ptr(), targets.data_ptr(), N, D, V,
                                          temperature, out_logp.data_ptr(), out_lse.data_ptr(),
@@ -382,6 +390,11 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
             "batch": torch.empty(len(BATCH_FIELDS), dtype=torch.float64, device=dev),
             "token_weight": torch.empty(N, dtype=torch.float32, device=dev) if token_weight else None,
         }
+    _need_out(out["seq_stats"], "seq_stats", torch.float32, (S, len(SEQ_FIELDS)), dev)
+    _need_out(out["seq_flags"], "seq_flags", torch.int32, (S,), dev)
+    _need_out(out["batch"], "batch", torch.float64, (len(BATCH_FIELDS),), dev)
+    if out.get("token_weight") is not None:
+        _need_out(out["token_weight"], "token_weight", torch.float32, (N,), dev)
     d = tim_mismatch_out()
     d.num_seqs = S
     d.num_tokens = N
@@ -414,7 +427,10 @@ def mismatch_monitor(logp_train, logp_rollout, mask, tau_tok: float, token_rejec
     if out is None:
         out = {"batch": torch.empty(len(MONITOR_FIELDS), dtype=torch.float64, device=dev),
                "token_reject": torch.empty(N, dtype=torch.uint8, device=dev) if token_reject else None}
+    _need_out(out["batch"], "batch", torch.float64, (len(MONITOR_FIELDS),), dev)
     rej = out.get("token_reject")
+    if rej is not None:
+        _need_out(rej, "token_reject", torch.uint8, (N,), dev)
     with torch.cuda.device(dev):
         rc = tim_mismatch_monitor(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(), N, tau_tok,
                                   None if rej is None else rej.data_ptr(), out["batch"].data_ptr(),
@@ -449,6 +465,11 @@ def tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, e
             "seq_loss": torch.empty(S, dtype=torch.float32, device=dev),
             "batch": torch.empty(len(PPO_FIELDS), dtype=torch.float64, device=dev),
         }
+    for name in ("token_loss", "token_grad"):
+        if out.get(name) is not None:
+            _need_out(out[name], name, torch.float32, (N,), dev)
+    _need_out(out["seq_loss"], "seq_loss", torch.float32, (S,), dev)
+    _need_out(out["batch"], "batch", torch.float64, (len(PPO_FIELDS),), dev)
     d = tim_ppo_out()
     d.num_seqs = S
     d.num_tokens = N

@@ -91,3 +91,52 @@ def test_forward_stats_surrogate_backward_chain():
         # bf16 dz scale rule, plus the upstream gradient's own relative error (2e-5)
         bound = 2.0 ** -7 * scale + 3e-5 * np.abs(o_arr) + 1e-6 * np.max(np.abs(o_arr))
         assert np.all(np.abs(g_arr - o_arr) <= bound), what
+
+
+def test_wrappers_reject_wrong_output_buffers():
+    """Every torch wrapper checks the caller's output buffers (dtype, shape,
+    device) before anything is launched: a buffer shorter than the outputs
+    raises instead of being written past its end."""
+    f32 = dict(dtype=torch.float32, device="cuda")
+    N, D, V, S = 64, 64, 300, 2
+    h = torch.zeros((N, D), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((V, D), dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros(N, dtype=torch.int32, device="cuda")
+    l = torch.zeros(N, **f32)
+    m = torch.ones(N, dtype=torch.uint8, device="cuda")
+    off = torch.tensor([0, 32, N], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        tim.token_logprob(h, W, a, out_logp=torch.empty(N - 1, **f32))
+    with pytest.raises(ValueError):
+        tim.token_logprob(h, W, a, out_lse=torch.empty(N + 1, **f32))
+    with pytest.raises(TypeError):
+        tim.token_logprob(h, W, a, out_logp=torch.empty(N, dtype=torch.float64, device="cuda"))
+    with pytest.raises(ValueError):
+        tim.token_logprob_backward(h, W, a, l, l, dh=torch.empty((N, D - 8), **f32))
+    with pytest.raises(ValueError):
+        tim.token_logprob_backward(h, W, a, l, l, dW=torch.empty((V - 1, D), **f32))
+    good = {"seq_stats": torch.empty((S, 12), **f32), "seq_flags": torch.empty(S, dtype=torch.int32, device="cuda"),
+            "batch": torch.empty(20, dtype=torch.float64, device="cuda"), "token_weight": None}
+    for key, bad in (("seq_stats", torch.empty((S - 1, 12), **f32)),
+                     ("seq_flags", torch.empty(S, **f32)),
+                     ("batch", torch.empty(19, dtype=torch.float64, device="cuda")),
+                     ("token_weight", torch.empty(N - 4, **f32))):
+        with pytest.raises((ValueError, TypeError)):
+            tim.mismatch_stats(l, l, m, off, out=dict(good, **{key: bad}))
+    with pytest.raises(ValueError):
+        tim.mismatch_monitor(l, l, m, 0.1, out={"batch": torch.empty(6, dtype=torch.float64, device="cuda"),
+                                                "token_reject": None})
+    with pytest.raises(ValueError):
+        tim.mismatch_monitor(l, l, m, 0.1, out={"batch": torch.empty(7, dtype=torch.float64, device="cuda"),
+                                                "token_reject": torch.empty(N - 1, dtype=torch.uint8, device="cuda")})
+    ppo = {"token_loss": None, "token_grad": None, "seq_loss": torch.empty(S, **f32),
+           "batch": torch.empty(9, dtype=torch.float64, device="cuda")}
+    with pytest.raises(ValueError):
+        tim.tis_ppo(l, l, l, l, m, off, out=dict(ppo, seq_loss=torch.empty(S + 1, **f32)))
+    with pytest.raises(ValueError):
+        tim.tis_ppo(l, l, l, l, m, off, out=dict(ppo, token_grad=torch.empty(N // 2, **f32)))
+    # the same buffers at the right sizes are accepted and computed into
+    r = tim.mismatch_stats(l, l, m, off, out=good)
+    tim.tis_ppo(l, l, l, l, m, off, out=ppo)
+    tim.check()
+    assert r["batch"][1].item() == N
