@@ -208,3 +208,27 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_lib", None)
     with pytest.raises(tim.TimError):
         tim.load()
+
+
+def test_torch_wrappers_reject_host_tensors_and_wrong_types():
+    """The torch wrappers check their tensors before any library call: host
+    tensors, wrong dtypes and non-tensors raise (there is no CPU path)."""
+    torch = pytest.importorskip("torch")
+    h = torch.zeros((4, 64), dtype=torch.bfloat16)
+    W = torch.zeros((10, 64), dtype=torch.bfloat16)
+    a = torch.zeros(4, dtype=torch.int32)
+    l = torch.zeros(4, dtype=torch.float32)
+    m = torch.ones(4, dtype=torch.uint8)
+    off = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tim.token_logprob(h, W, a)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tim.mismatch_stats(l, l, m, off)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tim.mismatch_monitor(l, l, m, 0.1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tim.tis_ppo(l, l, l, l, m, off)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        tim.split_weight_fp32(torch.zeros((10, 64)))
+    with pytest.raises(TypeError):
+        tim.token_logprob([[0.0]], W, a)
