@@ -318,6 +318,12 @@ def run_gb300(args):
         if rank == 0:
             print(json.dumps(r))
         return 0
+    if args.only == "k1" and args.head != WORKLOAD:
+        r = k1_head_only(tim, dev, stream_of(dev), args.head, reps=args.steps, warmup=args.warmup)
+        tim.check()
+        if rank == 0:
+            print(json.dumps(r))
+        return 0
     cfg, h, W, a, off, mask = make_workload(seed=rank, tokens=args.tokens)
     N, D, V = cfg.N, cfg.D, cfg.V
     stream = torch.cuda.current_stream(dev)
@@ -519,6 +525,33 @@ def run_gb300(args):
         line["head_shapes"] = heads
     print(json.dumps(line), flush=True)
     return 0
+
+
+def k1_head_only(tim, dev, stream, name, reps, warmup):
+    """The token logprob alone on another head shape of the workloads (profiling
+    runs): h ~ N(0, 1), W ~ N(0, w_std^2) in bf16 and uniform targets drawn on
+    the device, as in head_shapes_measure."""
+    import torch
+    cfg = wl.CONFIGS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    N, D, V = cfg.N, cfg.D, cfg.V
+    h = (torch.randn((N, D), generator=g, device=dev) * cfg.h_std).to(torch.bfloat16)
+    W = (torch.randn((V, D), generator=g, device=dev) * cfg.w_std).to(torch.bfloat16)
+    a = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
+    lp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        tim.token_logprob(h, W, a, lp, lse)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        tim.token_logprob(h, W, a, lp, lse)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) * 1e-3 / reps
+    return {"only": "k1", "head": name, "N": N, "D": D, "V": V, "avg_launch_ms": t * 1e3,
+            "tflops": 2.0 * N * V * D / t / 1e12}
 
 
 def head_shapes_measure(tim, dev, stream, peaks, names=("llama3_8b", "dsv3"), reps=5, warmup=2):
@@ -831,6 +864,8 @@ def main(argv=None):
                     help="time one call alone (for profiling); prints a short line, not the contract line")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller batch of the same head (profiling runs only)")
+    ap.add_argument("--head", choices=["qwen3_8b", "llama3_8b", "dsv3"], default=WORKLOAD,
+                    help="with --only k1: the head shape (profiling runs only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     if args.impl == "reference":
