@@ -54,9 +54,12 @@ MEASURED_TRAFFIC = {
     ("k2", "b52af0477f7a6c75"): 305287168 + 98403840,
     # TIS-weighted PPO surrogate, 2^25 tokens: 612941056 read + 216222720 written (scales with tokens)
     ("ppo", "aba850bed7b51939"): 612941056 + 216222720,
+    # mismatch monitor, 2^25 tokens, its five kernels: 316319232 read + 22924544 written (scales with tokens)
+    ("monitor", "778c660759a21d96"): 316319232 + 22924544,
 }
 K2_TRAFFIC_TOKENS = 1 << 25
 PPO_TRAFFIC_TOKENS = 1 << 25
+MONITOR_TRAFFIC_TOKENS = 1 << 25
 # L2 flush before each timed launch of a single call: 1 GiB, 8x the L2; its
 # ~0.15 ms fill also lets the host enqueue the timed call before the GPU
 # reaches the start event, so host-side call overhead stays out of the time.
@@ -68,7 +71,8 @@ def source_hash(kind: str) -> str:
     d = os.path.join(ROOT, "rollout_logprob_mismatch_gb300", "csrc")
     files = {"k1": ("k1_token_logprob.cu", "k1_internal.h", "tim_ptx.cuh", "tim_internal.h"),
              "k2": ("k2_mismatch_stats.cu", "k2_internal.h", "tim_ptx.cuh", "tim_internal.h"),
-             "ppo": ("tis_ppo.cu", "ppo_internal.h", "tim_ptx.cuh", "tim_internal.h")}[kind]
+             "ppo": ("tis_ppo.cu", "ppo_internal.h", "tim_ptx.cuh", "tim_internal.h"),
+             "monitor": ("mismatch_monitor.cu", "monitor_internal.h", "tim_ptx.cuh", "tim_internal.h")}[kind]
     m = hashlib.sha1()
     for f in files:
         with open(os.path.join(d, f), "rb") as fh:
@@ -790,10 +794,12 @@ def monitor_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, war
     t = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) * 1e-3 for i in range(reps)]))
     algo = 10 * Nt + 56
     gbs = algo / t / 1e9
+    tr = measured_traffic("monitor")
     return {"tokens": Nt, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo, "achieved": gbs,
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
             "passes_over_inputs": 1, "sample_tokens": min(Nt, 1 << 20),
-            "tokens_per_s": Nt / t, "traffic": None}
+            "tokens_per_s": Nt / t,
+            "traffic": None if tr is None else tr * Nt / MONITOR_TRAFFIC_TOKENS}
 
 
 def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
