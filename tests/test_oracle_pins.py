@@ -236,6 +236,31 @@ def test_clip_is_strict_and_decided_on_fp32_delta():
     assert list(out["seq_stats"][:, F["n_clip"]]) == [0, 1]
 
 
+def test_clip_is_strict_at_C_equal_one():
+    """C = 1 is the one cap whose log (0) an fp32 delta can equal: a token with
+    delta = 0 has r = C exactly and is not clipped (r > C is strict); the next
+    fp32 delta above it is.  Both weights are min(r, C) = 1."""
+    l_ro = np.full(2, -3.0, np.float32)
+    l_tr = np.array([-3.0, np.nextafter(np.float32(-3.0), np.float32(0))], np.float32)
+    out = oracle.mismatch_stats(l_tr, l_ro, np.ones(2, np.uint8), np.array([0, 1, 2], np.int32), C=1.0)
+    assert list(out["seq_stats"][:, F["n_clip"]]) == [0, 1]
+    assert list(out["token_weight"]) == [1.0, 1.0]
+
+
+def test_clip_and_nan_ratios_count_every_masked_in_token():
+    """LoongSage sections 4-5, is_clip_ratio and is_nan_ratio over the same
+    population, the masked-in tokens: four masked-in tokens, one clipped
+    (delta = 1 > ln 2), one non-finite, two at delta = 0, and one masked-out
+    clipped token -> both ratios 1/4."""
+    l_ro = np.full(5, -1.0, np.float32)
+    l_tr = np.array([-1.0, 0.0, np.nan, -1.0, 0.0], np.float32)
+    mask = np.array([1, 1, 1, 1, 0], np.uint8)
+    out = oracle.mismatch_stats(l_tr, l_ro, mask, np.array([0, 5], np.int32), C=2.0)
+    b = out["batch"]
+    assert (b[B["n_mask"]], b[B["n_used"]], b[B["n_nan"]], b[B["n_clip"]]) == (4, 3, 1, 1)
+    assert b[B["clip_ratio"]] == 0.25 and b[B["nan_ratio"]] == 0.25
+
+
 def test_bad_offsets_rejected():
     l = np.zeros(4, np.float32)
     with pytest.raises(ValueError):
