@@ -105,6 +105,28 @@ def test_caps_thresholds_estimators(C, tau, est):
     check_all(gs, o, C=C, tau=tau, est=est)
 
 
+def test_cap_one_with_exact_ties():
+    """C = 1: a token with delta = 0 exactly has r = C and is not clipped (r > C
+    is strict), any delta above 0 is; the default threshold (C - 1) - ln C is 0,
+    so only sequences of exact ties stay unflagged.  Non-finite tokens mixed in."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 300, size=30)
+    lens[:3] = (1, 64, 257)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(off[-1])
+    l_tr = wl.draw_train_logprobs(N, 8)
+    l_ro = (l_tr + rng.normal(0, 0.05, N)).astype(np.float32)
+    tie = rng.random(N) < 0.3
+    tie[off[0]:off[3]] = True                       # three sequences of exact ties only
+    l_ro[tie] = l_tr[tie]
+    mask = (rng.random(N) < 0.9).astype(np.uint8)
+    l_tr[off[5]] = np.nan
+    mask[off[5]] = 1
+    gs, o = run_both(l_tr, l_ro, mask, off, C=1.0)
+    check_all(gs, o, C=1.0)
+    assert np.all(gs["seq_flags"][:3] == 0) and gs["batch"][BF["n_clip"]] > 0
+
+
 def test_long_sequence_and_without_weights():
     """One 300k-token sequence (many compensated folds) next to short ones."""
     N = 300_000 + 77
