@@ -47,6 +47,22 @@ MUTATIONS = {
                             "batch[BT_NAN_RATIO] = mean_or_zero(b_nan, b_used);"),
     "p95_on_signed_delta": ("out[MO_P95_ABS_DELTA] = quantile_sorted(ad, n, 0.95, 0);",
                             "out[MO_P95_ABS_DELTA] = quantile_sorted(d, n, 0.95, 0);"),
+    "backward_softmax_sign": ("((v == targets[t] ? 1.0 : 0.0) - p) / temperature;",
+                              "(p - (v == targets[t] ? 1.0 : 0.0)) / temperature;"),
+    "backward_without_temperature": ("((v == targets[t] ? 1.0 : 0.0) - p) / temperature;",
+                                     "((v == targets[t] ? 1.0 : 0.0) - p);"),
+    "backward_dh_times_h": ("dht[d] += dzv * bf16_value(w[d]);", "dht[d] += dzv * hd[d];"),
+    "backward_dw_times_w": ("dwv[d] += dzv * hd[d];", "dwv[d] += dzv * bf16_value(w[d]);"),
+    "target_off_by_one": ("*out_logp = (a >= 0 && (int64_t)a < V) ? z[a] - lse : NAN;",
+                          "*out_logp = (a >= 0 && (int64_t)a < V) ? z[a > 0 ? a - 1 : a] - lse : NAN;"),
+    "seqmean_over_all_sequences": ("batch[BT_SEQMEAN_K3] = mean_or_zero(b_mk3, b_nonempty);",
+                                   "batch[BT_SEQMEAN_K3] = mean_or_zero(b_mk3, (double)S);"),
+    "rejection_on_k2": ("double stat = seq_estimator == 3 ? o[SQ_MEAN_K3] : fabs(o[SQ_MEAN_K1]);",
+                        "double stat = seq_estimator == 3 ? o[SQ_MEAN_K2] : fabs(o[SQ_MEAN_K1]);"),
+    "token_rejection_ignores_mask": ("const int ext = used && fabs((double)d32) > tau_tok;",
+                                     "const int ext = isfinite(d32) && fabs((double)d32) > tau_tok;"),
+    "ppo_loss_sign": ("loss = ppo_clipped ? -w * rclip * A : -w * r * A;",
+                      "loss = ppo_clipped ? w * rclip * A : w * r * A;"),
 }
 
 

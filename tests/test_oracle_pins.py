@@ -203,6 +203,11 @@ def test_empty_and_all_masked_sequences():
     assert np.all(s[[0, 1, 2]] == 0)                  # empty, all-masked, empty
     assert s[3, F["n_used"]] == 3
     assert out["batch"][B["n_seqs_nonempty"]] == 1
+    # the mean over sequences of per-sequence means (icarus monitoring steps 2-3)
+    # leaves out sequences without a used token (the reading for them: no mean
+    # to take): with one non-empty sequence it is that sequence's own mean
+    for k in ("k1", "k2", "k3"):
+        assert out["batch"][B["seqmean_" + k]] == s[3, F["mean_" + k]] != 0
     z = oracle.mismatch_stats(np.zeros(0, np.float32), np.zeros(0, np.float32),
                               np.zeros(0, np.uint8), np.array([0], np.int32))
     assert np.all(z["batch"] == 0)
