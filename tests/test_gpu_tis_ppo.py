@@ -61,6 +61,22 @@ def test_ragged_full(eps_low, eps_high, C):
     assert o["batch"][PF["n_ppo_clipped"]] > 0 or eps_high > 1
 
 
+def test_exact_ties_at_zero_eps_and_unit_cap():
+    """eps = 0 and C = 1: tokens whose log-ratios are exactly 0 sit on the clip
+    bounds and on the cap; they keep their gradient and are not counted as
+    clipped (both decisions are strict), like the oracle."""
+    off, mask, lt, lo, lr, A = ragged_batch(LENS, 23)
+    rng = np.random.default_rng(23)
+    tie = rng.random(lt.size) < 0.3
+    lt[tie] = lo[tie]
+    tie_c = rng.random(lt.size) < 0.3
+    lr[tie_c] = lo[tie_c]
+    g = gpu_ppo(lt, lo, lr, A, mask, off, 0.0, 0.0, 1.0)
+    o = oracle_ppo(lt, lo, lr, A, mask, off, 0.0, 0.0, 1.0)
+    assert_ppo_match(g, o, off, "ties at eps 0, C 1")
+    used_tie = tie & (mask != 0) & (A != 0)
+    assert np.all(g["token_grad"][used_tie] != 0)
+
 def test_nonfinite_zero_advantage_and_extremes():
     """NaN / inf inputs are not used (loss and gradient 0); A = 0 gives 0 even
     where r overflows fp32; large log-ratios stay finite where the oracle's are."""

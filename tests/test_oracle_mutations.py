@@ -63,6 +63,12 @@ MUTATIONS = {
                                      "const int ext = isfinite(d32) && fabs((double)d32) > tau_tok;"),
     "ppo_loss_sign": ("loss = ppo_clipped ? -w * rclip * A : -w * r * A;",
                       "loss = ppo_clipped ? w * rclip * A : w * r * A;"),
+    "ppo_clip_on_ties": ("(A > 0.0 && (double)dt32 > log_hi) || (A < 0.0 && (double)dt32 < log_lo)",
+                         "(A > 0.0 && (double)dt32 >= log_hi) || (A < 0.0 && (double)dt32 <= log_lo)"),
+    "max_of_signed_delta": ("            if (fabs(q.delta) > mx)\n                mx = fabs(q.delta);",
+                            "            if (q.delta > mx)\n                mx = q.delta;"),
+    "nan_counted_when_masked_out": ("q.nan = in && !fin;", "q.nan = !fin;"),
+    "quantile_interpolation_sign": ("return lo + (h - fl) * (hi - lo);", "return lo + (h - fl) * (hi + lo);"),
 }
 
 

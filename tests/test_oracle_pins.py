@@ -459,6 +459,21 @@ def test_ppo_case_form_of_the_clipped_objective():
         np.testing.assert_allclose(o["batch"][P["ppo_clip_ratio"]], flat.mean(), rtol=1e-15)
 
 
+def test_ppo_ties_keep_the_gradient():
+    """With eps = 0 the ratio r = 1 sits on both clip bounds: both terms of the
+    min are equal there and the token keeps its gradient (the reading: the
+    clipped branch is taken only where it is strictly smaller); the next fp32
+    log-ratio above 0 is clipped for A > 0 and not for A < 0."""
+    lo = np.full(4, -2.0, np.float32)
+    up = np.nextafter(np.float32(-2.0), np.float32(0))
+    lt = np.array([-2.0, -2.0, up, up], np.float32)
+    A = np.array([1.5, -1.5, 1.5, -1.5])
+    o = _ppo(lt, lo, lo, A, eps_low=0.0, eps_high=0.0, C=2.0)
+    assert o["token_grad"][0] == -1.5 and o["token_grad"][1] == 1.5
+    assert o["token_grad"][2] == 0 and o["token_grad"][3] != 0
+    assert o["batch"][P["n_ppo_clipped"]] == 1
+
+
 def test_ppo_gradient_is_the_derivative_of_the_loss():
     """token_grad = d token_loss / d logp_theta, checked by central differences
     of the oracle's own loss (step 2^-9, tokens at least 4 steps away from a
