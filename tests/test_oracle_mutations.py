@@ -69,6 +69,12 @@ MUTATIONS = {
                             "            if (q.delta > mx)\n                mx = q.delta;"),
     "nan_counted_when_masked_out": ("q.nan = in && !fin;", "q.nan = !fin;"),
     "quantile_interpolation_sign": ("return lo + (h - fl) * (hi - lo);", "return lo + (h - fl) * (hi + lo);"),
+    "extreme_on_signed_delta": ("const int ext = used && fabs((double)d32) > tau_tok;",
+                                "const int ext = used && (double)d32 > tau_tok;"),
+    "extreme_fraction_over_all_tokens": ("out[MO_FRAC_EXTREME] = mean_or_zero((double)n_ext, (double)n);",
+                                         "out[MO_FRAC_EXTREME] = mean_or_zero((double)n_ext, (double)N);"),
+    "median_ratio_of_abs_delta": ("out[MO_RATIO_Q50] = quantile_sorted(d, n, 0.5, 1);",
+                                  "out[MO_RATIO_Q50] = quantile_sorted(ad, n, 0.5, 1);"),
 }
 
 

@@ -579,13 +579,18 @@ def test_monitor_quantiles_match_numpy_linear_quantile():
 
 def test_monitor_normal_law():
     """delta ~ N(0, s^2): p95 |delta| -> 1.95996 s, median ratio -> 1,
-    q99 ratio -> e^{2.32635 s}, P(|delta| > tau) -> 2 (1 - Phi(tau / s));
+    q99 ratio -> e^{2.32635 s}, P(|delta| > tau) -> 2 (1 - Phi(tau / s)) among
+    the used tokens (30 % of the batch masked out, with |delta| = 1 there);
     tolerances are five standard errors of the sample quantile / fraction."""
-    n, s, tau = 1_000_000, 0.05, 0.08
+    N, s, tau = 1_400_000, 0.05, 0.08
     rng = np.random.default_rng(51)
-    lr = wl.draw_train_logprobs(n, 51)
-    lt = (lr.astype(np.float64) + rng.normal(0, s, n)).astype(np.float32)
-    o = oracle.mismatch_monitor(lt, lr, np.ones(n, np.uint8), tau)["batch"]
+    lr = wl.draw_train_logprobs(N, 51)
+    lt = (lr.astype(np.float64) + rng.normal(0, s, N)).astype(np.float32)
+    mask = (rng.random(N) >= 0.3).astype(np.uint8)
+    lt[mask == 0] = lr[mask == 0] + np.float32(1.0)
+    n = int(mask.sum())
+    o = oracle.mismatch_monitor(lt, lr, mask, tau)["batch"]
+    assert o[MF["n_used"]] == n
     z95 = scipy.stats.norm.ppf(0.975)
     se = math.sqrt(0.95 * 0.05 / n) / (2 * scipy.stats.norm.pdf(z95) / s)
     assert abs(o[MF["p95_abs_delta"]] - z95 * s) < 5 * se
