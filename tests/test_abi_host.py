@@ -88,6 +88,27 @@ def test_token_logprob_empty_is_noop(lib):
     assert tim.tim_token_logprob(None, None, None, 0, 64, 10, None, None, None) == tim.TIM_OK
 
 
+def test_noalloc_rejects_bad_arguments_on_the_host(lib):
+    """The no-alloc entry point checks sizes, pointers, alignment and its fixed
+    scratch (N x ceil(V / 1024) partials) before any CUDA call."""
+    E = tim.TIM_ERR_INVALID_ARG
+    call = tim.tim_token_logprob_noalloc
+    for N, D, V in ((-1, 64, 10), (4, 12, 10), (4, 64, 0), (1 << 31, 64, 10), (4, 65544, 10)):
+        assert call(16, 16, 16, N, D, V, 16, 16, None) == E, (N, D, V)
+    assert call(None, 16, 16, 4, 64, 10, 16, 16, None) == E
+    assert call(16, 8, 16, 4, 64, 10, 16, 16, None) == E
+    assert call(16, 16, 18, 4, 64, 10, 16, 16, None) == E
+    # 14080 rows of 149 chunks (V = 151936) need 16.8 MB of partials, more than the 16 MiB scratch
+    assert call(16, 16, 16, 14080, 4096, 151936, 16, 16, None) == E
+    assert "TIM_NOALLOC_SCRATCH_BYTES" in tim.tim_last_error()
+    assert call(None, None, None, 0, 64, 10, None, None, None) == tim.TIM_OK
+
+
+def test_selftest_rejects_bad_budget_on_the_host(lib):
+    for budget in (0, 1000001):
+        assert tim.tim_selftest_wait_timeout(budget, None) == tim.TIM_ERR_INVALID_ARG
+
+
 def _out(S=1, N=4, est=3, batch=16, seq=16, flags=16):
     d = tim.tim_mismatch_out()
     d.num_seqs, d.num_tokens, d.tau_seq, d.seq_estimator = S, N, math.nan, est
