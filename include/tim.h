@@ -168,10 +168,14 @@ TIM_API int tim_token_logprob_fp32_head(const void *h, const void *W_split, cons
  * tolerance as tim_token_logprob; it calls no cudaMalloc / cudaFree / pool
  * routine.  Its split-V scratch is one fixed device array inside libtim.so of
  * TIM_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
- * until the process exits.  Calls with
+ * until the process exits.  A call needs
  *   ceil(8 * N * ceil(V / 1024) / 256) * 256 + ceil(4 * N / 256) * 256
- * bytes above that limit (e.g. N > 14000 for V = 151936) return
- * TIM_ERR_INVALID_ARG without launching anything.
+ *   + (N % 16 != 0 ? ceil(256 * D / 256) * 256 : 0) + 256
+ * bytes of it (split-V partials, target logits, a zero-padded copy of the last
+ * 128-row tile of h when N is not a multiple of 16 -- the same fast loads as
+ * tim_token_logprob -- and a unit counter); calls needing more return
+ * TIM_ERR_INVALID_ARG without launching anything.  At V = 151936 and D = 4096
+ * that admits every N <= 13150 and multiples of 16 up to 14016.
  * The first call on a device sets that device up (it looks up the array's
  * device address, sets the kernel's shared-memory size and fetches the
  * tensor-map encoder); make that first call before any stream capture.

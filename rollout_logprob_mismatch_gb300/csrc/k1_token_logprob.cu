@@ -4,21 +4,24 @@
 // Inference Mismatch", section "log p"; LoongSage "Train-Inference Consistency"
 // section 3, FP32 LM head: here bf16 operands with fp32 accumulation).
 //
-// Persistent clusters of two CTAs (one CTA per SM) walk work units (two
-// m-tiles of 128 tokens, one per CTA, and a vocabulary chunk of 1024 ids).  Per
-// unit and 256-column tile:
-//   warp 0     TMA: the CTA's h tile [128 x 64] and half of the W tile
-//              [128 x 64], multicast to both CTAs of the cluster (each W byte
-//              leaves L2 once per cluster), 128-byte swizzle, into a 4-stage
-//              shared-memory ring; a stage is refilled only when the UMMA of
-//              both CTAs has released it (a batch of one m-tile runs in
-//              clusters of one CTA that load both halves of each W tile);
-//   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
-//              into one of two TMEM accumulators (2 x 256 columns), k ascending;
+// Persistent CTA pairs (one CTA per SM) walk work units (two m-tiles of 128
+// tokens, one per CTA, and a vocabulary chunk of 1024 ids).  Per unit and
+// 256-column tile:
+//   warp 0     TMA: the CTA's own h tile [128 x 64] and its own half of the W
+//              tile [128 x 64], 128-byte swizzle, into a 6-stage shared-memory
+//              ring; the bytes of both CTAs complete on the even CTA's barrier,
+//              and a stage is refilled when the pair UMMA has released it;
+//   warp 1     (even CTA) one thread issues the 2-SM tcgen05.mma (M = 256 over
+//              the pair, N = 256, K = 16, bf16 -> fp32): each CTA's TMEM gets
+//              its own 128 rows x 256 columns, from both CTAs' halves of W, so
+//              every W byte leaves L2 once per pair; two accumulators (2 x 256
+//              columns), k ascending;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
 //              token row) per thread, an online max / sum-of-exp over the columns
 //              in ascending order, and the target logit picked from the exact
 //              accumulator value.  The [N, V] logits never leave the SM.
+// A batch of one m-tile runs in single CTAs (1-SM UMMA, M = 128, both halves
+// of each W tile loaded by the CTA itself; same k order, same bits).
 // Each unit writes its chunk's (max, sum) per row; a second small kernel folds
 // the chunks of a row in a fixed order.  The split is a function of V alone and
 // every row is reduced in the same order whatever the batch holds, so a row's
@@ -38,7 +41,6 @@
 namespace tim {
 namespace {
 
-constexpr uint32_t IDESC = idesc_bf16_f32(K1_BM, K1_BN);
 constexpr uint32_t TMEM_COLS = 2 * K1_BN;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int SUBCOLS = 32;
@@ -86,33 +88,48 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     k1_main_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_h_tail, const K1Args a)
 {
+    constexpr bool PAIR = CL == 2;
+    constexpr int STAGES = k1_stages(CL);
+    constexpr uint32_t B_BYTES = k1_b_bytes(CL);
+    constexpr uint32_t STAGE_TX = K1_A_BYTES + B_BYTES;   // bytes this CTA loads per stage
+    constexpr uint32_t IDESC = idesc_bf16_f32(K1_BM * CL, K1_BN);
+    // the unit ring: the even CTA's producer claims units from a.sched and
+    // hands each to every role of the pair; these many roles release a slot
+    constexpr uint32_t SLOT_USERS = 1 + 4 * CL + (CL - 1);   // UMMA, epilogue warps, the odd CTA's producer
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sA = smem_u32(smem);
-    const uint32_t sB = sA + K1_STAGES * K1_A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K1_STAGES * K1_STAGE_BYTES);
+    const uint32_t sB = sA + STAGES * K1_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (K1_A_BYTES + B_BYTES));
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (K1_STAGES + s); };
-    auto tfull = [&](int b) { return bar0 + 8u * (2 * K1_STAGES + b); };
-    auto tempty = [&](int b) { return bar0 + 8u * (2 * K1_STAGES + 2 + b); };
-    const uint32_t drain = bar0 + 8u * (2 * K1_STAGES + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * K1_STAGES + 5);
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+    auto sfull = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + i); };
+    auto sempty = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + K1_SCHED_SLOTS + i); };
+    volatile int32_t *sunit = reinterpret_cast<volatile int32_t *>(bars + 2 * STAGES + 5 + 2 * K1_SCHED_SLOTS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(const_cast<int32_t *>(sunit) + K1_SCHED_SLOTS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < K1_STAGES; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), CL);   // released by the UMMA of every CTA of the cluster
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);    // in a pair the even CTA's, expecting the bytes of both CTAs
+            mbar_init(empty(s), 1);   // released by the (pair) UMMA
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), 4);
+            mbar_init(tempty(b), 4 * CL);   // in a pair the even CTA's: the epilogue warps of both
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < K1_SCHED_SLOTS; ++i) {
+            mbar_init(sfull(i), 1);
+            mbar_init(sempty(i), SLOT_USERS);   // in a pair the even CTA's
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -122,39 +139,95 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             tma_prefetch_desc(&tmap_h_tail);
         tma_prefetch_desc(&tmap_w);
     }
-    pdl_wait();                // h, W, targets may be written by the previous kernel
+    pdl_wait();                // h, W, targets, the unit counter may be written by earlier work
     pdl_launch_dependents();   // the combine kernel may start launching
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncwarp();
-    cluster_sync();   // every CTA's barriers exist before any multicast reaches them
+    cluster_sync();   // every CTA's barriers exist before the other CTA's TMA, UMMA or threads reach them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t rank = cluster_ctarank();
-    const int cid = blockIdx.x / CL;
-    const int ncl = gridDim.x / CL;
-    constexpr uint16_t kAllCtas = static_cast<uint16_t>((1u << CL) - 1);
     const int KBH = (a.D + K1_BK - 1) / K1_BK;   // k-tiles of h
     const int KB = KBH * a.w_segments;          // k-tiles of W: 1 or 3 bf16 parts of each weight
     const uint64_t budget = a.wait_budget_ns;
+    // shared::cluster addresses of the barriers both CTAs of a pair signal (the even CTA's)
+    auto full_pair = [&](int s) { return PAIR ? mapa_shared(full(s), 0) : full(s); };
+    auto tempty_pair = [&](int b) { return PAIR ? mapa_shared(tempty(b), 0) : tempty(b); };
+
+    // Units come in claim order from one counter shared by the whole grid, so
+    // the units in flight always form one window of consecutive indices (the
+    // same W tiles and h band for all pairs: read from HBM once, then from L2),
+    // however the pairs' speeds differ.  Which pair runs a unit changes no bit.
+    int slot = 0;
+    uint32_t slot_phase = 0;
+    // A role's next unit (-1: none left); false when a wait ran out of time.
+    // `arrive` (one lane per role) releases the slot once the unit is read.
+    auto take = [&](int &u, bool arrive) -> bool {
+        const bool got = rank == 0 ? mbar_wait(sfull(slot), slot_phase, abort_flag, budget)
+                                   : mbar_wait_cluster(sfull(slot), slot_phase, abort_flag, budget);
+        if (!got)
+            return false;
+        u = sunit[slot];
+        __syncwarp(__activemask());
+        if (arrive) {
+            if (PAIR)
+                mbar_arrive_remote(mapa_shared(sempty(slot), 0));
+            else
+                mbar_arrive(sempty(slot));
+        }
+        if (++slot == K1_SCHED_SLOTS) {
+            slot = 0;
+            slot_phase ^= 1u;
+        }
+        return true;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producer (every CTA)
             const uint64_t pol_h = l2_policy_evict_last();
             const uint64_t pol_w = l2_policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             bool ok = true;
-            for (int u = cid; ok && u < a.units; u += ncl) {
+            while (ok) {
+                int u = -1;
+                if (rank == 0) {
+                    // claim the next unit and hand it to every role of the pair
+                    if (!mbar_wait(sempty(slot), slot_phase ^ 1u, abort_flag, budget))
+                        break;
+                    u = atomicAdd(a.sched, 1);
+                    if (u >= a.units)
+                        u = -1;
+                    sunit[slot] = u;
+                    if (PAIR) {
+                        st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(sunit + slot)), 1), u);
+                        mbar_arrive_remote(mapa_shared(sfull(slot), 1));
+                    }
+                    mbar_arrive(sfull(slot));
+                    if (++slot == K1_SCHED_SLOTS) {
+                        slot = 0;
+                        slot_phase ^= 1u;
+                    }
+                } else if (!take(u, true)) {
+                    break;
+                }
+                if (u < 0)
+                    break;
                 const Unit w = unit_of(u, a);
                 const int mt = w.mt * CL + static_cast<int>(rank);
                 // the last m-tile of a batch whose size is not a multiple of 16 rows
                 // reads a zero-padded copy of its rows (same values, fast loads); an
-                // m-tile past the batch (the cluster peer of a last odd m-tile) reads
+                // m-tile past the batch (the pair peer of a last odd m-tile) reads
                 // past the end of that copy: zeros, again through a map of 16k rows
                 const bool tail = a.tail_mt >= 0 && mt >= a.tail_mt;
                 const CUtensorMap *hmap = tail ? &tmap_h_tail : &tmap_h;
@@ -164,47 +237,66 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                     const int v0 = w.ch * K1_VCHUNK + j * K1_BN;
                     int kh = 0;   // kb mod KBH: the h tile meets each part of W in turn
                     for (int kb = 0; kb < KB; ++kb) {
-                        // the stage is free once the UMMA of every CTA of the cluster is done with it
+                        // the stage is free once the UMMA that read it has completed
                         if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget)) {
                             ok = false;
                             break;
                         }
-                        // own h tile + this CTA's rows of the W tile, multicast to the whole
-                        // cluster; the barrier counts the W rows the other CTAs send as well
-                        mbar_arrive_expect_tx(full(stage), K1_STAGE_BYTES);
-                        tma_load_2d(sA + stage * K1_A_BYTES, hmap, full(stage), kh * K1_BK, hrow, pol_h);
+                        const uint32_t fb = full_pair(stage);
+                        if (PAIR) {
+                            // own h tile + own half of the W tile; both CTAs' bytes complete
+                            // on the even CTA's barrier, whose one arrival expects them all
+                            // (the other CTA's bytes may land first: the count goes below zero
+                            // and the phase still cannot complete before that arrival)
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(full(stage), 2 * STAGE_TX);
+                            tma_load_2d_pair(sA + stage * K1_A_BYTES, hmap, fb, kh * K1_BK, hrow, pol_h);
+                            tma_load_2d_pair(sB + stage * B_BYTES, &tmap_w, fb, kb * K1_BK,
+                                             v0 + static_cast<int>(rank) * K1_W_BOX_ROWS, pol_w);
+                        } else {   // h tile + both halves of the W tile
+                            mbar_arrive_expect_tx(fb, STAGE_TX);
+                            tma_load_2d(sA + stage * K1_A_BYTES, hmap, fb, kh * K1_BK, hrow, pol_h);
+                            tma_load_2d(sB + stage * B_BYTES, &tmap_w, fb, kb * K1_BK, v0, pol_w);
+                            tma_load_2d(sB + stage * B_BYTES + B_BYTES / 2, &tmap_w, fb, kb * K1_BK,
+                                        v0 + K1_W_BOX_ROWS, pol_w);
+                        }
                         if (++kh == KBH)
                             kh = 0;
-                        if (CL == 1) {   // both halves of the W tile, same layout as the multicast
-                            tma_load_2d(sB + stage * K1_B_BYTES, &tmap_w, full(stage), kb * K1_BK, v0, pol_w);
-                            tma_load_2d(sB + stage * K1_B_BYTES + K1_B_BYTES / 2, &tmap_w, full(stage),
-                                        kb * K1_BK, v0 + K1_W_BOX_ROWS, pol_w);
-                        } else {
-                            tma_load_2d_multicast(sB + stage * K1_B_BYTES + rank * (K1_B_BYTES / CL), &tmap_w,
-                                                  full(stage), kb * K1_BK, v0 + static_cast<int>(rank) * K1_W_BOX_ROWS,
-                                                  kAllCtas, pol_w);
-                        }
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                        if (++stage == K1_STAGES) {
+                        if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                 }
             }
-            // no TMA write may still be landing in shared memory when the CTA exits
-            for (int s = 0; s < K1_STAGES; ++s)
+            // no TMA write may still be landing in shared memory when the CTA
+            // exits: a stage's last fill has landed once the UMMA released it
+            // (after an abort the bounded wait lets it land anyway)
+            for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s))
-                    drain_wait(full(s), (last_par >> s) & 1u);
+                    drain_wait(empty(s), (last_par >> s) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ UMMA issuer
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ UMMA issuer (the even CTA of a pair)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int u = cid; ok && u < a.units; u += ncl) {
+            // a commit arrives on this CTA's barrier and, in a pair, on the peer's
+            auto commit_both = [&](uint32_t bar) {
+                if (PAIR) {
+                    umma_commit_pair(bar);
+                    umma_commit_pair(mapa_shared(bar, 1));
+                } else {
+                    umma_commit(bar);
+                }
+            };
+            while (ok) {
+                int u = -1;
+                if (!take(u, true) || u < 0)
+                    break;
                 const Unit w = unit_of(u, a);
                 const int nt = tiles_in_chunk(w.ch, a.V);
                 for (int j = 0; ok && j < nt; ++j) {
@@ -221,29 +313,33 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         }
                         tc_fence_after();
                         const uint64_t ad = sdesc_kmajor_sw128(sA + stage * K1_A_BYTES);
-                        const uint64_t bd = sdesc_kmajor_sw128(sB + stage * K1_B_BYTES);
+                        const uint64_t bd = sdesc_kmajor_sw128(sB + stage * B_BYTES);
 #pragma unroll
-                        for (int k = 0; k < K1_BK / 16; ++k)   // +32 bytes along K per step
-                            umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
-                        if (CL == 1)
-                            umma_commit(empty(stage));
-                        else
-                            umma_commit_multicast(empty(stage), kAllCtas);
-                        if (++stage == K1_STAGES) {
+                        for (int k = 0; k < K1_BK / 16; ++k) {   // +32 bytes along K per step
+                            if (PAIR)
+                                umma_bf16_pair(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
+                            else
+                                umma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) != 0);
+                        }
+                        commit_both(empty(stage));
+                        if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok)
                         break;
-                    umma_commit(tfull(acc));
+                    commit_both(tfull(acc));
                     acc ^= 1;
                     if (acc == 0)
                         acc_phase ^= 1u;
                 }
             }
-            // every UMMA issued has finished before TMEM is released
-            umma_commit(drain);
+            // every UMMA issued has finished (in both CTAs' TMEM) before TMEM is released
+            if (PAIR)
+                umma_commit_pair(drain);
+            else
+                umma_commit(drain);
             drain_wait(drain, 0);
         }
     } else if (MODE == 1) {
@@ -254,7 +350,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int u = cid; ok && u < a.units; u += ncl) {
+        while (ok) {
+            int u = -1;
+            if (!take(u, lane == 0) || u < 0)
+                break;
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
             const int row = (w.mt * CL + static_cast<int>(rank)) * K1_BM + r_in_tile;
@@ -304,8 +403,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(tempty(acc));
+                if (lane == 0) {
+                    if (PAIR)
+                        mbar_arrive_remote(tempty_pair(acc));
+                    else
+                        mbar_arrive(tempty(acc));
+                }
                 acc ^= 1;
                 if (acc == 0)
                     acc_phase ^= 1u;
@@ -319,7 +422,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int u = cid; ok && u < a.units; u += ncl) {
+        while (ok) {
+            int u = -1;
+            if (!take(u, lane == 0) || u < 0)
+                break;
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
             const int row = (w.mt * CL + static_cast<int>(rank)) * K1_BM + r_in_tile;
@@ -380,8 +486,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(tempty(acc));
+                if (lane == 0) {
+                    if (PAIR)
+                        mbar_arrive_remote(tempty_pair(acc));
+                    else
+                        mbar_arrive(tempty(acc));
+                }
                 acc ^= 1;
                 if (acc == 0)
                     acc_phase ^= 1u;
@@ -397,14 +507,17 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     }
 
     tc_fence_before();
-    // no CTA leaves while another CTA of the cluster may still multicast into its
-    // shared memory or arrive on its barriers
+    // no CTA leaves while the other CTA of its pair may still load into the
+    // pair's stages, arrive on its barriers or have UMMA write its TMEM
     __syncwarp();
     cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem, TMEM_COLS);
+        else
+            tmem_dealloc(tmem, TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag)
         atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
@@ -511,6 +624,8 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
         static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_clusters[ci][md][dev] : 1));
     cfg.gridDim = dim3(cl * clusters, 1, 1);
     cfg.numAttrs = 2;
+    if ((e = cudaMemsetAsync(a.sched, 0, sizeof(int), stream)) != cudaSuccess)   // units are claimed from 0
+        return e;
     return cudaLaunchKernelEx(&cfg, kernel, tmap_h, tmap_w, tmap_h_tail, a);
 }
 

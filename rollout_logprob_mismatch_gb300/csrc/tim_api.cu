@@ -291,7 +291,8 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     const size_t pad_bytes = tail_pad_bytes(N, D);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + za_bytes + pad_bytes, dev->pool, s);
+    cudaError_t e =
+        cudaMallocFromPoolAsync(&ws, part_bytes + za_bytes + pad_bytes + tim::K1_SCHED_BYTES, dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(token_logprob workspace)");
     CUtensorMap th_tail;
@@ -306,6 +307,7 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     a.targets = targets;
     a.part = static_cast<float2 *>(ws);
     a.za = reinterpret_cast<float *>(static_cast<char *>(ws) + part_bytes);
+    a.sched = reinterpret_cast<int *>(static_cast<char *>(ws) + part_bytes + za_bytes + pad_bytes);
     a.status = dev->status;
     a.inv_temp = inv_temp;
     a.N = static_cast<int32_t>(N);
@@ -474,7 +476,7 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
     const size_t dz_bytes = round_up(static_cast<size_t>(rows_max) * Vp * 2, 256);
     const size_t pad_bytes = round_up(static_cast<size_t>(tim::K1_BM) * D * 2, 256);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, dz_bytes + pad_bytes, dev->pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, dz_bytes + pad_bytes + tim::K1_SCHED_BYTES, dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(backward workspace)");
     CUtensorMap tw;
@@ -495,6 +497,7 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
         const int64_t m_tiles = (n + tim::K1_BM - 1) / tim::K1_BM;
         tim::K1Args a{};
         a.targets = targets + r0;
+        a.sched = reinterpret_cast<int *>(static_cast<char *>(ws) + dz_bytes + pad_bytes);
         a.status = dev->status;
         a.inv_temp = 1.f / temperature;
         a.N = static_cast<int32_t>(n);

@@ -11,8 +11,10 @@
 //
 // The array is a file-scope __device__ object, so every GPU that loads the
 // library holds TIM_NOALLOC_SCRATCH_BYTES of it until the process exits.  All
-// calls share it and it keeps the last call's contents; nothing in it has to
-// start at zero (every partial a call reads is written by that call first).
+// calls share it and it keeps the last call's contents: every partial a call
+// reads is written by that call first, and the one word that must start at
+// zero (the fused kernel's unit counter) is cleared on the stream before each
+// launch (cudaMemsetAsync, which allocates nothing).
 // Two calls whose kernels overlap on the GPU (other streams, other threads)
 // race on the array: the caller must order them.
 #include <cmath>
@@ -149,14 +151,18 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
         return err(TIM_ERR_INVALID_ARG, "targets / outputs must be 4-byte aligned");
     const int64_t m_tiles = (N + tim::K1_BM - 1) / tim::K1_BM;
     const int64_t chunks = tim::k1_num_chunks(V);
+    // scratch layout: per-chunk partials | target logits | padded last m-tile
+    // (only when N % 16 != 0) | the unit counter
     const size_t part_bytes = round_up(static_cast<size_t>(chunks) * N * sizeof(float2), 256);
     const size_t za_bytes = round_up(static_cast<size_t>(N) * sizeof(float), 256);
-    if (part_bytes + za_bytes > static_cast<size_t>(TIM_NOALLOC_SCRATCH_BYTES))
+    const size_t pad_bytes =
+        tim::k1_needs_tail_pad(N) ? round_up(static_cast<size_t>(tim::K1_BM) * D * 2, 256) : 0;
+    const size_t need = part_bytes + za_bytes + pad_bytes + tim::K1_SCHED_BYTES;
+    if (need > static_cast<size_t>(TIM_NOALLOC_SCRATCH_BYTES))
         return err(TIM_ERR_INVALID_ARG,
                    "N x ceil(V / 1024) too large for the fixed scratch: needs %lld bytes, the limit is %lld "
                    "(TIM_NOALLOC_SCRATCH_BYTES); use tim_token_logprob or split the rows",
-                   static_cast<long long>(part_bytes + za_bytes),
-                   static_cast<long long>(TIM_NOALLOC_SCRATCH_BYTES));
+                   static_cast<long long>(need), static_cast<long long>(TIM_NOALLOC_SCRATCH_BYTES));
 
     NoallocDevice *dev = nullptr;
     int rc = setup(&dev);
@@ -167,11 +173,28 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
         return rc;
     if ((rc = encode(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK)
         return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *pad = dev->scratch + part_bytes + za_bytes;
+    // TMA reads of h through a map whose row count is not a multiple of 16 are
+    // slow, so such a batch's last m-tile is read from a zero-padded copy in
+    // the scratch (same values, so the same result bits)
+    CUtensorMap th_tail = th;
+    int32_t tail_mt = -1;
+    if (pad_bytes > 0) {
+        const int64_t r0 = (m_tiles - 1) * tim::K1_BM;
+        const cudaError_t ep = tim::k1_launch_pad_tail(static_cast<const char *>(h) + r0 * D * 2, N - r0, D, pad, s);
+        if (ep != cudaSuccess)
+            return cuda_err(ep, "tail pad copy");
+        if ((rc = encode(&th_tail, pad, tim::K1_BM, D, tim::K1_BM)) != TIM_OK)
+            return rc;
+        tail_mt = static_cast<int32_t>(m_tiles - 1);
+    }
 
     tim::K1Args a{};
     a.targets = targets;
     a.part = reinterpret_cast<float2 *>(dev->scratch);
     a.za = reinterpret_cast<float *>(dev->scratch + part_bytes);
+    a.sched = reinterpret_cast<int *>(pad + pad_bytes);
     a.status = dev->status;
     a.inv_temp = 1.f;
     a.N = static_cast<int32_t>(N);
@@ -182,9 +205,8 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     a.num_chunks = static_cast<int32_t>(chunks);
     tim::k1_set_units(a, m_tiles, chunks, D);
     a.wait_budget_ns = wait_budget_ns();
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    a.tail_mt = -1;   // no room for a padded tail here: the same values through the plain map
-    cudaError_t e = tim::k1_launch_main(th, tw, th, a, s);
+    a.tail_mt = tail_mt;
+    cudaError_t e = tim::k1_launch_main(th, tw, th_tail, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
                                    s);

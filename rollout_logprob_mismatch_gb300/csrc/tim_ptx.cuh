@@ -167,17 +167,70 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 2-D tiled tensor load multicast to the CTAs of this cluster named in
-// `cta_mask`: the tile lands at the same shared-memory offset in each of them
-// and completes transaction bytes on the mbarrier at offset `bar` in each.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                      int32_t x, int32_t y, uint16_t cta_mask, uint64_t policy)
+// The same load issued by either CTA of a CTA pair (2-SM UMMA): the tile lands
+// in this CTA's shared memory at `dst`, and the transaction bytes complete on
+// the mbarrier at shared::cluster address `bar`, which may be the peer's.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
         : "memory");
+}
+
+// shared::cluster address of the object at shared::cta address `addr` in the
+// CTA of rank `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier anywhere in the cluster (shared::cluster address),
+// releasing this thread's earlier memory accesses at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 32-bit store to shared memory anywhere in the cluster.
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, int32_t v)
+{
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// mbar_wait with acquire at cluster scope, for a barrier that a thread of the
+// other CTA of a pair arrives on after writing data this thread then reads.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                  uint64_t budget_ns)
+{
+    auto done = [&] {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred P;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, P;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (done())
+            return true;
+        if ((i & 31u) == 31u) {
+            if (*abort)
+                return false;
+            if (global_ns() - t0 > budget_ns) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
 }
 
 // This CTA's rank in its cluster.
@@ -284,14 +337,47 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
                  : "memory");
 }
 
-// Like umma_commit, and the arrival also goes to the mbarrier at the same
-// offset in every CTA of the cluster named in `cta_mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask)
+// 2-SM UMMA (CTA pair): D[tmem of both CTAs] (+)= A * B^T with M = 256 rows,
+// 128 of A in each CTA's shared memory and N/2 rows of B in each, both at the
+// descriptors' addresses; issued by one thread of the pair's even CTA.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Arrives once on the mbarrier at shared::cluster address `bar` (in either CTA
+// of the pair) when every pair UMMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// TMEM allocation, permit release and deallocation for pair UMMA: one warp of
+// each CTA of the pair performs them together; the same columns are taken in
+// both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
