@@ -30,8 +30,7 @@ int64_t k1_band_bytes();
 constexpr uint32_t K1_A_BYTES = K1_BM * K1_BK * 2;
 constexpr uint32_t k1_b_bytes(int cl) { return static_cast<uint32_t>(cl == 1 ? K1_BN : K1_BN / 2) * K1_BK * 2; }
 constexpr int k1_stages(int cl) { return cl == 1 ? 4 : 7; }   // TMA -> UMMA pipeline depth
-constexpr uint32_t K1_BAR_BYTES = 512;   // mbarriers, the unit ring, TMEM address, abort flag
-constexpr int K1_SCHED_SLOTS = 4;        // units handed from the claiming producer to the other roles
+constexpr uint32_t K1_BAR_BYTES = 512;   // the unit ring, mbarriers, TMEM address, abort flag
 constexpr uint32_t k1_ring_bytes(int cl) { return static_cast<uint32_t>(k1_stages(cl)) * (K1_A_BYTES + k1_b_bytes(cl)); }
 constexpr uint32_t K1_SMEM_BYTES =
     (k1_ring_bytes(1) > k1_ring_bytes(K1_CLUSTER) ? k1_ring_bytes(1) : k1_ring_bytes(K1_CLUSTER)) + K1_BAR_BYTES + 1024;

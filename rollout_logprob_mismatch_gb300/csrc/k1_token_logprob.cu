@@ -36,6 +36,7 @@
 #include "k1_internal.h"
 #include "tim_internal.h"
 #include "tim_ptx.cuh"
+#include "unit_ring.cuh"
 #include "../../include/tim.h"
 
 namespace tim {
@@ -93,24 +94,22 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     constexpr uint32_t B_BYTES = k1_b_bytes(CL);
     constexpr uint32_t STAGE_TX = K1_A_BYTES + B_BYTES;   // bytes this CTA loads per stage
     constexpr uint32_t IDESC = idesc_bf16_f32(K1_BM * CL, K1_BN);
-    // the unit ring: the even CTA's producer claims units from a.sched and
-    // hands each to every role of the pair; these many roles release a slot
-    constexpr uint32_t SLOT_USERS = 1 + 4 * CL + (CL - 1);   // UMMA, epilogue warps, the odd CTA's producer
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sA = smem_u32(smem);
     const uint32_t sB = sA + STAGES * K1_A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (K1_A_BYTES + B_BYTES));
+    uint8_t *tail_area = smem + STAGES * (K1_A_BYTES + B_BYTES);
+    // units claimed in order (unit_ring.cuh); its users: the UMMA issuer, the
+    // epilogue warps of both CTAs, the odd CTA's producer
+    UnitRing<CL, 1 + 4 * CL + (CL - 1)> ring(tail_area);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tail_area + UNIT_RING_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
-    auto sfull = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + i); };
-    auto sempty = [&](int i) { return bar0 + 8u * (2 * STAGES + 5 + K1_SCHED_SLOTS + i); };
-    volatile int32_t *sunit = reinterpret_cast<volatile int32_t *>(bars + 2 * STAGES + 5 + 2 * K1_SCHED_SLOTS);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(const_cast<int32_t *>(sunit) + K1_SCHED_SLOTS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -126,10 +125,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             mbar_init(tempty(b), 4 * CL);   // in a pair the even CTA's: the epilogue warps of both
         }
         mbar_init(drain, 1);
-        for (int i = 0; i < K1_SCHED_SLOTS; ++i) {
-            mbar_init(sfull(i), 1);
-            mbar_init(sempty(i), SLOT_USERS);   // in a pair the even CTA's
-        }
+        ring.init();
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -163,34 +159,6 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
     auto full_pair = [&](int s) { return PAIR ? mapa_shared(full(s), 0) : full(s); };
     auto tempty_pair = [&](int b) { return PAIR ? mapa_shared(tempty(b), 0) : tempty(b); };
 
-    // Units come in claim order from one counter shared by the whole grid, so
-    // the units in flight always form one window of consecutive indices (the
-    // same W tiles and h band for all pairs: read from HBM once, then from L2),
-    // however the pairs' speeds differ.  Which pair runs a unit changes no bit.
-    int slot = 0;
-    uint32_t slot_phase = 0;
-    // A role's next unit (-1: none left); false when a wait ran out of time.
-    // `arrive` (one lane per role) releases the slot once the unit is read.
-    auto take = [&](int &u, bool arrive) -> bool {
-        const bool got = rank == 0 ? mbar_wait(sfull(slot), slot_phase, abort_flag, budget)
-                                   : mbar_wait_cluster(sfull(slot), slot_phase, abort_flag, budget);
-        if (!got)
-            return false;
-        u = sunit[slot];
-        __syncwarp(__activemask());
-        if (arrive) {
-            if (PAIR)
-                mbar_arrive_remote(mapa_shared(sempty(slot), 0));
-            else
-                mbar_arrive(sempty(slot));
-        }
-        if (++slot == K1_SCHED_SLOTS) {
-            slot = 0;
-            slot_phase ^= 1u;
-        }
-        return true;
-    };
-
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (every CTA)
@@ -198,29 +166,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             const uint64_t pol_w = l2_policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
-            bool ok = true;
+            int ahead = -1;   // the even CTA claims one unit ahead of its loads
+            bool ok = rank != 0 || ring.claim(a.sched, a.units, ahead, abort_flag, budget);
             while (ok) {
                 int u = -1;
-                if (rank == 0) {
-                    // claim the next unit and hand it to every role of the pair
-                    if (!mbar_wait(sempty(slot), slot_phase ^ 1u, abort_flag, budget))
-                        break;
-                    u = atomicAdd(a.sched, 1);
-                    if (u >= a.units)
-                        u = -1;
-                    sunit[slot] = u;
-                    if (PAIR) {
-                        st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(sunit + slot)), 1), u);
-                        mbar_arrive_remote(mapa_shared(sfull(slot), 1));
-                    }
-                    mbar_arrive(sfull(slot));
-                    if (++slot == K1_SCHED_SLOTS) {
-                        slot = 0;
-                        slot_phase ^= 1u;
-                    }
-                } else if (!take(u, true)) {
+                if (!(rank == 0 ? ring.next(a.sched, a.units, u, ahead, abort_flag, budget)
+                                : ring.take(u, true, rank, abort_flag, budget)))
                     break;
-                }
                 if (u < 0)
                     break;
                 const Unit w = unit_of(u, a);
@@ -295,7 +247,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             };
             while (ok) {
                 int u = -1;
-                if (!take(u, true) || u < 0)
+                if (!ring.take(u, true, rank, abort_flag, budget) || u < 0)
                     break;
                 const Unit w = unit_of(u, a);
                 const int nt = tiles_in_chunk(w.ch, a.V);
@@ -352,7 +304,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         bool ok = true;
         while (ok) {
             int u = -1;
-            if (!take(u, lane == 0) || u < 0)
+            if (!ring.take(u, lane == 0, rank, abort_flag, budget) || u < 0)
                 break;
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
@@ -405,7 +357,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if (PAIR)
-                        mbar_arrive_remote(tempty_pair(acc));
+                        mbar_arrive_remote_cta(tempty_pair(acc));
                     else
                         mbar_arrive(tempty(acc));
                 }
@@ -424,7 +376,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
         bool ok = true;
         while (ok) {
             int u = -1;
-            if (!take(u, lane == 0) || u < 0)
+            if (!ring.take(u, lane == 0, rank, abort_flag, budget) || u < 0)
                 break;
             const Unit w = unit_of(u, a);
             const int nt = tiles_in_chunk(w.ch, a.V);
@@ -488,7 +440,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if (PAIR)
-                        mbar_arrive_remote(tempty_pair(acc));
+                        mbar_arrive_remote_cta(tempty_pair(acc));
                     else
                         mbar_arrive(tempty(acc));
                 }

@@ -7,10 +7,10 @@
 #include <cstring>
 #include <mutex>
 
-#include <cublas_v2.h>
 #include <cudaTypedefs.h>
 
 #include "../../include/tim.h"
+#include "bwd_internal.h"
 #include "monitor_internal.h"
 #include "ppo_internal.h"
 #include "k1_internal.h"
@@ -105,7 +105,7 @@ int device_state(DeviceState **out)
     if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
         return cuda_fail(e, "cudaMemPoolSetAttribute");
     if ((e = tim::k1_prepare_device()) != cudaSuccess || (e = tim::k2_prepare_device()) != cudaSuccess ||
-        (e = tim::monitor_prepare_device()) != cudaSuccess)
+        (e = tim::monitor_prepare_device()) != cudaSuccess || (e = tim::gemm_prepare_device()) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
     if (!g_encode) {
         void *fn = nullptr;
@@ -122,12 +122,14 @@ int device_state(DeviceState **out)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a box of
-// [box_rows, 64] and 128-byte swizzling; out-of-range elements read as zero.
-int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows)
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix whose rows are
+// `row_bytes` apart (a multiple of 16), with a box of [box_rows, 64] and
+// 128-byte swizzling; out-of-range elements read as zero.
+int encode_bf16_strided(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t row_bytes,
+                        uint32_t box_rows)
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(tim::K1_BK), box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
@@ -136,6 +138,11 @@ int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, ui
     if (r != CUDA_SUCCESS)
         return fail(TIM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return TIM_OK;
+}
+
+int encode_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows)
+{
+    return encode_bf16_strided(m, base, rows, cols, cols * 2, box_rows);
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -171,31 +178,8 @@ int tail_map(const void *h, int64_t N, int64_t D, void *pad, const CUtensorMap &
 }
 
 // Rows of one backward chunk: the bf16 logit gradient of a chunk is rows x V
-// (1.2 GB at V = 151936); dh and dW are then two cuBLAS GEMMs per chunk.
-constexpr int64_t kBackwardRows = 4096;
-
-// cuBLAS handle of the current device, made once (never destroyed: it lives
-// as long as the process, like the device state).
-int cublas_handle(cublasHandle_t *out)
-{
-    static cublasHandle_t handles[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(TIM_ERR_UNSUPPORTED_DEVICE, "device index %d too large", dev);
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!handles[dev]) {
-        const cublasStatus_t bs = cublasCreate(&handles[dev]);
-        if (bs != CUBLAS_STATUS_SUCCESS) {
-            handles[dev] = nullptr;
-            return fail(TIM_ERR_CUDA, "cublasCreate: %d", static_cast<int>(bs));
-        }
-    }
-    *out = handles[dev];
-    return TIM_OK;
-}
+// (5 GB at V = 151936); dh and dW are then two GEMMs per chunk.
+constexpr int64_t kBackwardRows = 16384;
 
 // Largest float <= v, and smallest float >= v: a float x then satisfies
 // x > float_down(v) <=> x > v, and x < float_up(v) <=> x < v.
@@ -455,12 +439,6 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
     if (rc != TIM_OK)
         return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cublasHandle_t cb = nullptr;
-    if ((rc = cublas_handle(&cb)) != TIM_OK)
-        return rc;
-    cublasStatus_t bs = cublasSetStream(cb, s);
-    if (bs != CUBLAS_STATUS_SUCCESS)
-        return fail(TIM_ERR_CUDA, "cublasSetStream: %d", static_cast<int>(bs));
     if (N == 0) {   // no rows: dW = 0 unless accumulating
         if (!accumulate_dW) {
             const cudaError_t e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * D * sizeof(float), s);
@@ -479,25 +457,32 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
     cudaError_t e = cudaMallocFromPoolAsync(&ws, dz_bytes + pad_bytes + tim::K1_SCHED_BYTES, dev->pool, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMallocFromPoolAsync(backward workspace)");
-    CUtensorMap tw;
-    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK) {
+    int *sched = reinterpret_cast<int *>(static_cast<char *>(ws) + dz_bytes + pad_bytes);
+    CUtensorMap tw, tw_mn;
+    if ((rc = encode_bf16(&tw, W, V, D, tim::K1_W_BOX_ROWS)) != TIM_OK ||
+        (rc = encode_bf16(&tw_mn, W, V, D, tim::G_MNMAJOR_BOX_ROWS)) != TIM_OK) {
         cudaFreeAsync(ws, s);
         return rc;
     }
-    const float one = 1.f, zero = 0.f;
     const int64_t chunks_v = tim::k1_num_chunks(V);
+    const int32_t n_blocks = static_cast<int32_t>((D + tim::G_BN - 1) / tim::G_BN);
     for (int64_t r0 = 0; r0 < N && rc == TIM_OK; r0 += rows_max) {
         const int64_t n = std::min<int64_t>(rows_max, N - r0);
         const void *hc = static_cast<const uint16_t *>(h) + r0 * D;
-        CUtensorMap th, th_tail;
+        CUtensorMap th, th_tail, th_mn, tdz_k, tdz_mn;
         int32_t tail_mt = -1;
+        // dz is read up to column V only (the row padding past V holds no data
+        // and reads as zero), its rows Vp apart
         if ((rc = encode_bf16(&th, hc, n, D, tim::K1_BM)) != TIM_OK ||
-            (rc = tail_map(hc, n, D, static_cast<char *>(ws) + dz_bytes, th, s, &th_tail, &tail_mt)) != TIM_OK)
+            (rc = tail_map(hc, n, D, static_cast<char *>(ws) + dz_bytes, th, s, &th_tail, &tail_mt)) != TIM_OK ||
+            (rc = encode_bf16(&th_mn, hc, n, D, tim::G_MNMAJOR_BOX_ROWS)) != TIM_OK ||
+            (rc = encode_bf16_strided(&tdz_k, ws, n, V, Vp * 2, tim::G_KMAJOR_BOX_ROWS)) != TIM_OK ||
+            (rc = encode_bf16_strided(&tdz_mn, ws, n, V, Vp * 2, tim::G_MNMAJOR_BOX_ROWS)) != TIM_OK)
             break;
         const int64_t m_tiles = (n + tim::K1_BM - 1) / tim::K1_BM;
         tim::K1Args a{};
         a.targets = targets + r0;
-        a.sched = reinterpret_cast<int *>(static_cast<char *>(ws) + dz_bytes + pad_bytes);
+        a.sched = sched;
         a.status = dev->status;
         a.inv_temp = 1.f / temperature;
         a.N = static_cast<int32_t>(n);
@@ -517,18 +502,36 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
             rc = cuda_fail(e, "backward dz launch");
             break;
         }
-        // row-major dh[n, D] = dz[n, V] W[V, D]: column-major dh^T = W^T dz^T
-        bs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(D), static_cast<int>(n), static_cast<int>(V),
-                          &one, W, CUDA_R_16BF, static_cast<int>(D), ws, CUDA_R_16BF, static_cast<int>(Vp), &zero,
-                          dh + r0 * D, CUDA_R_32F, static_cast<int>(D), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-        // row-major dW[V, D] (+)= dz^T[V, n] h[n, D]: column-major dW^T = h^T dz; chunks in row order
-        if (bs == CUBLAS_STATUS_SUCCESS)
-            bs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(D), static_cast<int>(V), static_cast<int>(n),
-                              &one, hc, CUDA_R_16BF, static_cast<int>(D), ws, CUDA_R_16BF, static_cast<int>(Vp),
-                              (r0 == 0 && !accumulate_dW) ? &zero : &one, dW, CUDA_R_32F, static_cast<int>(D),
-                              CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-        if (bs != CUBLAS_STATUS_SUCCESS)
-            rc = fail(TIM_ERR_CUDA, "cublasGemmEx: %d", static_cast<int>(bs));
+        // dh rows of the chunk = dz W: A = dz [n][V] K-major, B = W [V][D] MN-major, K = V
+        tim::GemmArgs g{};
+        g.C = dh + r0 * D;
+        g.ldc = D;
+        g.M = static_cast<int32_t>(n);
+        g.N = static_cast<int32_t>(D);
+        g.K = static_cast<int32_t>(V);
+        g.n_blocks = n_blocks;
+        g.units = static_cast<int32_t>((n + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
+        g.accumulate = 0;
+        g.b_keep = 0;
+        g.sched = sched;
+        g.status = dev->status;
+        g.wait_budget_ns = wait_budget_ns();
+        if ((e = tim::gemm_launch(tdz_k, tw_mn, false, true, g, s)) != cudaSuccess) {
+            rc = cuda_fail(e, "backward dh launch");
+            break;
+        }
+        // dW (+)= dz^T h: A = dz^T (dz [n][V] read MN-major), B = h [n][D] MN-major,
+        // K = n; chunks in row order, each adding to the sum of the chunks before
+        g.C = dW;
+        g.M = static_cast<int32_t>(V);
+        g.K = static_cast<int32_t>(n);
+        g.units = static_cast<int32_t>((V + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
+        g.accumulate = (r0 > 0 || accumulate_dW) ? 1 : 0;
+        g.b_keep = 1;   // h of the chunk (at most 16384 x D bf16) is read by every dW tile
+        if ((e = tim::gemm_launch(tdz_mn, th_mn, true, true, g, s)) != cudaSuccess) {
+            rc = cuda_fail(e, "backward dW launch");
+            break;
+        }
     }
     const cudaError_t ef = cudaFreeAsync(ws, s);
     if (rc != TIM_OK)

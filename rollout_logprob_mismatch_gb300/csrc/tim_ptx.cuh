@@ -190,10 +190,21 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
 }
 
 // Arrive on an mbarrier anywhere in the cluster (shared::cluster address),
-// releasing this thread's earlier memory accesses at cluster scope.
+// releasing this thread's earlier memory accesses at cluster scope: for a
+// thread that has just written shared memory of the other CTA (which waits on
+// the barrier with mbar_wait_cluster).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on an mbarrier anywhere in the cluster with the default (CTA-scope)
+// release: it does not wait for this thread's global stores to become visible
+// to the cluster.  For releasing a buffer this thread has only read (a TMEM
+// accumulator after tcgen05.fence::before_thread_sync, a shared-memory slot).
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // 32-bit store to shared memory anywhere in the cluster.
@@ -397,12 +408,29 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
+// Shared-memory matrix descriptor for an MN-major operand tile written by TMA
+// with 128-byte swizzling: each k index is a 128-byte row of 64 consecutive
+// M (or N) elements, 8-row core groups 1024 bytes apart (stride byte offset),
+// and the next 64 M (or N) elements start `lbo` bytes further (leading byte
+// offset).  Other fields as for the K-major form.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor for tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A / B K-major (bit 15 / 16 = 0) or
+// MN-major (= 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape), with
