@@ -688,8 +688,9 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
 def backward_measure(tim, dev, stream, peaks, hd, Wd, ad, reps=5, warmup=2):
     """The token logprob's backward on the bench's head shape: g ~ N(0, 1) per
     token, lse from the forward; one call = per row chunk (up to 16384 rows)
-    the fused dz kernel (logits recomputed, never stored in fp32) and the two
-    pair-UMMA GEMMs dh = dz W and dW (+)= dz^T h; L2 flushed before each call.
+    the fused dz kernel (logits recomputed, never stored in fp32) and one
+    launch of the pair-UMMA GEMMs dh = dz W and dW (+)= dz^T h; L2 flushed
+    before each call.
     Work 3 x 2NVD FLOP (recompute, dh, dW) against the bf16 peak (burst and
     sustained: five back-to-back calls of ~18 ms run at the power cap)."""
     import torch
@@ -719,7 +720,7 @@ def backward_measure(tim, dev, stream, peaks, hd, Wd, ad, reps=5, warmup=2):
             "tflops": flops / t / 1e12, "bound": "tensor", "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": flops / t / 1e12 / peaks["bf16_tflops"],
             "frac_of_sustained": flops / t / 1e12 / peaks["bf16_tflops_sustained"],
-            "parts": "per row chunk: fused dz kernel + dh GEMM + dW GEMM (all tcgen05 pair UMMA, ours)"}
+            "parts": "per row chunk: fused dz kernel + one launch of both GEMMs dh, dW (tcgen05 pair UMMA, ours)"}
 
 
 def fp32_head_measure(tim, dev, stream, peaks, hd, ad, V, reps=5, warmup=3):

@@ -10,8 +10,10 @@
 // probability; icarus "RL: Training Inference Mismatch", the trainer's
 // recompute of log p).
 //
-// C[m, n] = sum_k A[m, k] B[n, k]: persistent CTA pairs claim 256 x 256 tiles
-// of C in order (unit_ring.cuh; n fastest), and per tile
+// C[m, n] = sum_k A[m, k] B[n, k]: one persistent launch computes both (dh's
+// tiles, long in k, claimed first, then dW's short ones, so pairs never idle
+// through a last partial wave of dh).  CTA pairs claim 256 x 256 tiles of C in
+// order (unit_ring.cuh; n fastest), and per tile
 //   warp 0     TMA: the CTA's 128 rows of A and its half (128) of the B tile,
 //              64 k per stage, 128-byte swizzle, into a 7-stage ring; both
 //              CTAs' bytes complete on the even CTA's barrier;
@@ -23,6 +25,7 @@
 // k steps ascending, the tensor core's fixed order inside a step): a row of dh
 // depends on its own dz row, W and V only, whatever else the batch holds.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -40,17 +43,16 @@ constexpr uint32_t MN_BLOCK_BYTES = G_MNMAJOR_BOX_ROWS * 128;   // 64 k rows of 
 static_assert(UNIT_RING_BYTES + 8 * (2 * G_STAGES + 5) + 8 <= G_TAIL_BYTES, "tail area too small");
 static_assert(G_A_BYTES == 2 * MN_BLOCK_BYTES && G_B_BYTES == 2 * MN_BLOCK_BYTES, "two MN blocks per operand tile");
 
-template <bool A_MN, bool B_MN>
+// Problem 0's A is K-major, problem 1's MN-major; B is MN-major in both.
 __global__ void __launch_bounds__(G_THREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const GemmArgs a)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a0, const __grid_constant__ CUtensorMap tmap_b0,
+                     const __grid_constant__ CUtensorMap tmap_a1, const __grid_constant__ CUtensorMap tmap_b1,
+                     const __grid_constant__ GemmArgs a)
 {
     constexpr uint32_t STAGE_TX = G_A_BYTES + G_B_BYTES;   // bytes each CTA loads per stage
-    constexpr uint32_t IDESC = idesc_bf16_f32(2 * G_BM, G_BN, A_MN, B_MN);
-    // descriptor start-address step (16-byte units) per K = 16: 32 bytes along a
-    // K-major row, or 16 rows of 128 bytes in an MN-major tile
-    constexpr uint32_t A_KSTEP = A_MN ? 128u : 2u;
-    constexpr uint32_t B_KSTEP = B_MN ? 128u : 2u;
+    constexpr uint32_t B_KSTEP = 128u;   // MN-major B: 16 rows of 128 bytes per K = 16 (16-byte units)
+    using AKmajor = std::integral_constant<bool, false>;
+    using AMNmajor = std::integral_constant<bool, true>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sA = smem_u32(smem);
@@ -86,8 +88,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmap_a);
-        tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_a0);
+        tma_prefetch_desc(&tmap_b0);
+        if (a.p[1].units > 0) {
+            tma_prefetch_desc(&tmap_a1);
+            tma_prefetch_desc(&tmap_b1);
+        }
     }
     pdl_wait();   // the operands and the unit counter are written by earlier work
     pdl_launch_dependents();
@@ -102,48 +108,39 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t rank = cluster_ctarank();
     const uint64_t budget = a.wait_budget_ns;
-    const int KT = (a.K + G_BK - 1) / G_BK;
+    const int units0 = a.p[0].units, units = a.p[0].units + a.p[1].units;
+
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
-            const uint64_t pol = l2_policy_evict_normal();
-            const uint64_t pol_b = a.b_keep ? l2_policy_evict_last() : pol;
+            const uint64_t pol = l2_policy_evict_normal(), pol_keep = l2_policy_evict_last();
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
-            int ahead = -1;   // the even CTA claims one unit ahead of its loads
-            bool ok = rank != 0 || ring.claim(a.sched, a.units, ahead, abort_flag, budget);
-            while (ok) {
-                int u = -1;
-                if (!(rank == 0 ? ring.next(a.sched, a.units, u, ahead, abort_flag, budget)
-                                : ring.take(u, true, rank, abort_flag, budget)))
-                    break;
-                if (u < 0)
-                    break;
-                const int mb = u / a.n_blocks, nb = u - (u / a.n_blocks) * a.n_blocks;
+            // the k loop of one tile of problem P (A K-major or MN-major)
+            auto produce = [&](auto a_mn, const GemmProblem &P, const CUtensorMap *ma, const CUtensorMap *mbm,
+                               int lu) -> bool {
+                constexpr bool A_MN = decltype(a_mn)::value;
+                const uint64_t pol_b = P.b_keep ? pol_keep : pol;
+                const int mb = lu / P.n_blocks, nb = lu - (lu / P.n_blocks) * P.n_blocks;
                 const int m0 = mb * (2 * G_BM) + static_cast<int>(rank) * G_BM;     // this CTA's rows of C
                 const int n0 = nb * G_BN + static_cast<int>(rank) * (G_BN / 2);    // this CTA's half of B
+                const int KT = (P.K + G_BK - 1) / G_BK;
                 for (int kb = 0; kb < KT; ++kb) {
-                    if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag, budget))
+                        return false;
                     const uint32_t f = mapa_shared(full(stage), 0);   // the even CTA's barrier
                     if (rank == 0)
                         mbar_arrive_expect_tx(full(stage), 2 * STAGE_TX);
                     const int k0 = kb * G_BK;
                     const uint32_t dA = sA + stage * G_A_BYTES, dB = sB + stage * G_B_BYTES;
                     if (A_MN) {
-                        tma_load_2d_pair(dA, &tmap_a, f, m0, k0, pol);
-                        tma_load_2d_pair(dA + MN_BLOCK_BYTES, &tmap_a, f, m0 + 64, k0, pol);
+                        tma_load_2d_pair(dA, ma, f, m0, k0, pol);
+                        tma_load_2d_pair(dA + MN_BLOCK_BYTES, ma, f, m0 + 64, k0, pol);
                     } else {
-                        tma_load_2d_pair(dA, &tmap_a, f, k0, m0, pol);
+                        tma_load_2d_pair(dA, ma, f, k0, m0, pol);
                     }
-                    if (B_MN) {
-                        tma_load_2d_pair(dB, &tmap_b, f, n0, k0, pol_b);
-                        tma_load_2d_pair(dB + MN_BLOCK_BYTES, &tmap_b, f, n0 + 64, k0, pol_b);
-                    } else {
-                        tma_load_2d_pair(dB, &tmap_b, f, k0, n0, pol_b);
-                    }
+                    tma_load_2d_pair(dB, mbm, f, n0, k0, pol_b);
+                    tma_load_2d_pair(dB + MN_BLOCK_BYTES, mbm, f, n0 + 64, k0, pol_b);
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == G_STAGES) {
@@ -151,6 +148,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         phase ^= 1u;
                     }
                 }
+                return true;
+            };
+            int ahead = -1;   // the even CTA claims one unit ahead of its loads
+            bool ok = rank != 0 || ring.claim(a.sched, units, ahead, abort_flag, budget);
+            while (ok) {
+                int u = -1;
+                if (!(rank == 0 ? ring.next(a.sched, units, u, ahead, abort_flag, budget)
+                                : ring.take(u, true, rank, abort_flag, budget)))
+                    break;
+                if (u < 0)
+                    break;
+                ok = u < units0 ? produce(AKmajor{}, a.p[0], &tmap_a0, &tmap_b0, u)
+                                : produce(AMNmajor{}, a.p[1], &tmap_a1, &tmap_b1, u - units0);
             }
             // a stage's last fill has landed once the UMMA released it
             for (int s = 0; s < G_STAGES; ++s)
@@ -162,28 +172,25 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             // ------------------------------------------------ UMMA issuer (the even CTA)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            bool ok = true;
             auto commit_both = [&](uint32_t bar) {
                 umma_commit_pair(bar);
                 umma_commit_pair(mapa_shared(bar, 1));
             };
-            while (ok) {
-                int u = -1;
-                if (!ring.take(u, true, rank, abort_flag, budget) || u < 0)
-                    break;
-                if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag, budget))
-                    break;
-                tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * G_BN);
+            // the k loop of one tile into accumulator d
+            auto mma = [&](auto a_mn, const GemmProblem &P, uint32_t d) -> bool {
+                constexpr bool A_MN = decltype(a_mn)::value;
+                constexpr uint32_t IDESC = idesc_bf16_f32(2 * G_BM, G_BN, A_MN, true);
+                // descriptor start-address step (16-byte units) per K = 16: 32 bytes
+                // along a K-major row, or 16 rows of 128 bytes in an MN-major tile
+                constexpr uint32_t A_KSTEP = A_MN ? 128u : 2u;
+                const int KT = (P.K + G_BK - 1) / G_BK;
                 for (int kb = 0; kb < KT; ++kb) {
-                    if (!mbar_wait(full(stage), phase, abort_flag, budget)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!mbar_wait(full(stage), phase, abort_flag, budget))
+                        return false;
                     tc_fence_after();
                     const uint32_t aa = sA + stage * G_A_BYTES, ba = sB + stage * G_B_BYTES;
                     const uint64_t ad = A_MN ? sdesc_mnmajor_sw128(aa, MN_BLOCK_BYTES) : sdesc_kmajor_sw128(aa);
-                    const uint64_t bd = B_MN ? sdesc_mnmajor_sw128(ba, MN_BLOCK_BYTES) : sdesc_kmajor_sw128(ba);
+                    const uint64_t bd = sdesc_mnmajor_sw128(ba, MN_BLOCK_BYTES);
 #pragma unroll
                     for (int k = 0; k < G_BK / 16; ++k)
                         umma_bf16_pair(d, ad + A_KSTEP * k, bd + B_KSTEP * k, IDESC, (kb | k) != 0);
@@ -193,7 +200,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         phase ^= 1u;
                     }
                 }
-                if (!ok)
+                return true;
+            };
+            while (true) {
+                int u = -1;
+                if (!ring.take(u, true, rank, abort_flag, budget) || u < 0)
+                    break;
+                if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag, budget))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * G_BN);
+                if (!(u < units0 ? mma(AKmajor{}, a.p[0], d) : mma(AMNmajor{}, a.p[1], d)))
                     break;
                 commit_both(tfull(acc));
                 acc ^= 1;
@@ -212,11 +229,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             int u = -1;
             if (!ring.take(u, lane == 0, rank, abort_flag, budget) || u < 0)
                 break;
-            const int mb = u / a.n_blocks, nb = u - (u / a.n_blocks) * a.n_blocks;
-            const int M = a.M, N = a.N;
-            const bool accumulate = a.accumulate != 0;
+            const GemmProblem &P = u < units0 ? a.p[0] : a.p[1];
+            const int lu = u < units0 ? u : u - units0;
+            const int mb = lu / P.n_blocks, nb = lu - (lu / P.n_blocks) * P.n_blocks;
+            const int M = P.M, N = P.N;
+            const bool accumulate = P.accumulate != 0;
             const int row = mb * (2 * G_BM) + static_cast<int>(rank) * G_BM + q * 32 + lane;
-            float *crow = a.C + static_cast<size_t>(row < M ? row : 0) * static_cast<size_t>(a.ldc);
+            float *crow = P.C + static_cast<size_t>(row < M ? row : 0) * static_cast<size_t>(P.ldc);
             if (!mbar_wait(tfull(acc), acc_phase, abort_flag, budget))
                 break;
             tc_fence_after();
@@ -275,22 +294,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
 cudaError_t gemm_prepare_device()
 {
-    cudaError_t e = cudaSuccess;
-    for (auto kernel : {gemm_pair_kernel<false, true>, gemm_pair_kernel<true, true>})
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(G_SMEM_BYTES));
-    return e;
+    return cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(G_SMEM_BYTES));
 }
 
-cudaError_t gemm_launch(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, bool a_mn, bool b_mn,
-                        const GemmArgs &a, cudaStream_t stream)
+cudaError_t gemm_launch(const CUtensorMap (&tmap_a)[2], const CUtensorMap (&tmap_b)[2], const GemmArgs &a,
+                        cudaStream_t stream)
 {
-    if (!b_mn)
-        return cudaErrorInvalidValue;   // the backward's two forms have an MN-major B
-    static int max_pairs[2][64] = {};   // per form and device, found once
-    auto kernel = a_mn ? gemm_pair_kernel<true, true> : gemm_pair_kernel<false, true>;
-    const int fi = a_mn ? 1 : 0;
+    static int max_pairs[64] = {};   // per device, found once
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -307,19 +318,20 @@ cudaError_t gemm_launch(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, bo
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev >= 0 && dev < 64 && max_pairs[fi][dev] == 0) {
+    if (dev >= 0 && dev < 64 && max_pairs[dev] == 0) {
         int n = 0;
         cfg.gridDim = dim3(2 * 1024, 1, 1);
-        if ((e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg)) != cudaSuccess)
+        if ((e = cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg)) != cudaSuccess)
             return e;
-        max_pairs[fi][dev] = n > 0 ? n : 1;
+        max_pairs[dev] = n > 0 ? n : 1;
     }
-    const int pairs = static_cast<int>(std::min<int64_t>(a.units, dev >= 0 && dev < 64 ? max_pairs[fi][dev] : 1));
+    const int64_t units = static_cast<int64_t>(a.p[0].units) + a.p[1].units;
+    const int pairs = static_cast<int>(std::min<int64_t>(units, dev >= 0 && dev < 64 ? max_pairs[dev] : 1));
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.numAttrs = 2;
     if ((e = cudaMemsetAsync(a.sched, 0, sizeof(int), stream)) != cudaSuccess)
         return e;
-    return cudaLaunchKernelEx(&cfg, kernel, tmap_a, tmap_b, a);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tmap_a[0], tmap_b[0], tmap_a[1], tmap_b[1], a);
 }
 
 } // namespace tim

@@ -24,7 +24,8 @@ constexpr uint32_t G_SMEM_BYTES = G_STAGES * (G_A_BYTES + G_B_BYTES) + G_TAIL_BY
 constexpr int G_KMAJOR_BOX_ROWS = 128;
 constexpr int G_MNMAJOR_BOX_ROWS = 64;
 
-struct GemmArgs {
+// One GEMM of a launch.
+struct GemmProblem {
     float *C;           // row-major [M][ldc] fp32, 16-byte aligned, ldc % 4 == 0
     int64_t ldc;
     int32_t M, N, K;    // N % 4 == 0
@@ -32,6 +33,15 @@ struct GemmArgs {
     int32_t units;      // ceil(M / 256) * n_blocks, n fastest
     int32_t accumulate; // 1: C += A B^T; 0: C = A B^T
     int32_t b_keep;     // B is small and read by every tile: loaded with an L2 evict-last hint
+};
+
+// Two independent GEMMs in one persistent launch: problem 0 with A K-major,
+// problem 1 with A MN-major (the m index contiguous: a [K][M] matrix), both
+// with B MN-major ([K][N]).  The pairs claim problem 0's tiles first, then
+// problem 1's, so a pair done with a long tile of the first takes short tiles
+// of the second instead of idling through a last partial wave.
+struct GemmArgs {
+    GemmProblem p[2];   // p[1].units may be 0
     int *sched;         // unit counter, zeroed by the launcher
     int *status;        // device status word
     uint64_t wait_budget_ns;
@@ -39,11 +49,10 @@ struct GemmArgs {
 
 cudaError_t gemm_prepare_device();
 
-// a_mn / b_mn: A (resp. B) is stored MN-major (the m (n) index contiguous, a
-// [K][M] ([K][N]) matrix); else K-major ([M][K], [N][K]); B must be MN-major.
-// tmap_a / tmap_b use the box shapes above.  Zeroes a.sched on the stream,
-// then launches at most as many pairs as fit on the device at once.
-cudaError_t gemm_launch(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b, bool a_mn, bool b_mn,
-                        const GemmArgs &a, cudaStream_t stream);
+// tmap_a[i] / tmap_b[i]: the operands of problem i with the box shapes above
+// (A of problem 0: K-major box; the others: MN-major boxes).  Zeroes a.sched on
+// the stream, then launches at most as many pairs as fit on the device at once.
+cudaError_t gemm_launch(const CUtensorMap (&tmap_a)[2], const CUtensorMap (&tmap_b)[2], const GemmArgs &a,
+                        cudaStream_t stream);
 
 } // namespace tim

@@ -502,34 +502,34 @@ int tim_token_logprob_backward(const void *h, const void *W, const int32_t *targ
             rc = cuda_fail(e, "backward dz launch");
             break;
         }
-        // dh rows of the chunk = dz W: A = dz [n][V] K-major, B = W [V][D] MN-major, K = V
+        // one launch, two GEMMs (dh's tiles claimed first, then dW's):
+        // dh rows of the chunk = dz W: A = dz [n][V] K-major, B = W [V][D] MN-major, K = V;
+        // dW (+)= dz^T h: A = dz^T (dz [n][V] read MN-major), B = h [n][D] MN-major,
+        // K = n; chunks in row order, each adding to the sum of the chunks before
         tim::GemmArgs g{};
-        g.C = dh + r0 * D;
-        g.ldc = D;
-        g.M = static_cast<int32_t>(n);
-        g.N = static_cast<int32_t>(D);
-        g.K = static_cast<int32_t>(V);
-        g.n_blocks = n_blocks;
-        g.units = static_cast<int32_t>((n + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
-        g.accumulate = 0;
-        g.b_keep = 0;
+        tim::GemmProblem &ph = g.p[0], &pw = g.p[1];
+        ph.C = dh + r0 * D;
+        ph.ldc = D;
+        ph.M = static_cast<int32_t>(n);
+        ph.N = static_cast<int32_t>(D);
+        ph.K = static_cast<int32_t>(V);
+        ph.n_blocks = n_blocks;
+        ph.units = static_cast<int32_t>((n + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
+        ph.accumulate = 0;
+        ph.b_keep = 0;
+        pw = ph;
+        pw.C = dW;
+        pw.M = static_cast<int32_t>(V);
+        pw.K = static_cast<int32_t>(n);
+        pw.units = static_cast<int32_t>((V + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
+        pw.accumulate = (r0 > 0 || accumulate_dW) ? 1 : 0;
+        pw.b_keep = 1;   // h of the chunk (at most 16384 x D bf16) is read by every dW tile
         g.sched = sched;
         g.status = dev->status;
         g.wait_budget_ns = wait_budget_ns();
-        if ((e = tim::gemm_launch(tdz_k, tw_mn, false, true, g, s)) != cudaSuccess) {
-            rc = cuda_fail(e, "backward dh launch");
-            break;
-        }
-        // dW (+)= dz^T h: A = dz^T (dz [n][V] read MN-major), B = h [n][D] MN-major,
-        // K = n; chunks in row order, each adding to the sum of the chunks before
-        g.C = dW;
-        g.M = static_cast<int32_t>(V);
-        g.K = static_cast<int32_t>(n);
-        g.units = static_cast<int32_t>((V + 2 * tim::G_BM - 1) / (2 * tim::G_BM)) * n_blocks;
-        g.accumulate = (r0 > 0 || accumulate_dW) ? 1 : 0;
-        g.b_keep = 1;   // h of the chunk (at most 16384 x D bf16) is read by every dW tile
-        if ((e = tim::gemm_launch(tdz_mn, th_mn, true, true, g, s)) != cudaSuccess) {
-            rc = cuda_fail(e, "backward dW launch");
+        const CUtensorMap maps_a[2] = {tdz_k, tdz_mn}, maps_b[2] = {tw_mn, th_mn};
+        if ((e = tim::gemm_launch(maps_a, maps_b, g, s)) != cudaSuccess) {
+            rc = cuda_fail(e, "backward dh / dW launch");
             break;
         }
     }

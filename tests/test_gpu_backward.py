@@ -83,7 +83,9 @@ def check_against_oracle(h, W, a, g, tau=1.0, what=""):
 
 
 @pytest.mark.parametrize("N,D,V", [(7, 72, 130), (130, 256, 1000), (300, 520, 2049), (200, 1024, 4099),
-                                   (5, 4096, 3000), (1, 64, 1)])
+                                   (5, 4096, 3000), (1, 64, 1),
+                                   # long k loops for dh (K = V) over several m-blocks
+                                   (130, 128, 45000), (257, 64, 83000)])
 def test_ragged_shapes(N, D, V):
     h, W, a, g = _case(N, D, V, N + 3 * D + V, w_std=0.3 / math.sqrt(D / 64))
     check_against_oracle(h, W, a, g, what=str((N, D, V)))
