@@ -26,10 +26,12 @@ constexpr int K2_REC_WORDS = 16;                   // 4-byte words per sequence 
 constexpr int K2_PART_WORDS = 40;                  // 4-byte words per fold partial
 static_assert(K2_STAGE_BYTES % 16 == 0 && K2_BAR_BYTES % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
 
+// Workspace: the sequence counter and the fold's ticket (256 bytes, zeroed per
+// call), the records (16 words per sequence), the fold partials.
+inline int64_t k2_blocks(int64_t S) { return (S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS; }
 inline size_t k2_workspace_bytes(int64_t S)
 {
-    const int64_t parts = (S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
-    return static_cast<size_t>(S) * K2_REC_WORDS * 4 + static_cast<size_t>(parts) * K2_PART_WORDS * 4 + 256;
+    return 256 + static_cast<size_t>(S) * K2_REC_WORDS * 4 + static_cast<size_t>(k2_blocks(S)) * K2_PART_WORDS * 4;
 }
 
 struct K2Args {
@@ -47,8 +49,11 @@ struct K2Args {
     float *seq_stats;      // [S][12]
     int32_t *seq_flags;    // [S]
     double *batch;         // [20]
-    uint32_t *rec;         // workspace: sequence records, [K2_REC_WORDS][S]
-    uint32_t *part;        // workspace: fold partials, [ceil(S / K2_FOLD_SEQS)][K2_PART_WORDS]
+    int *claim;            // workspace: sequence counter ...
+    int *blk_done;         // ... and the fold CTAs' ticket (zeroed by k2_launch)
+    uint32_t *rec;         // workspace: sequence records, [S][K2_REC_WORDS]
+    uint32_t *part;        // workspace: block partials, [ceil(S / K2_FOLD_SEQS)][K2_PART_WORDS]
+    int32_t stats_vec;     // seq_stats is 16-byte aligned (rows written as float4)
     int *status;
 };
 

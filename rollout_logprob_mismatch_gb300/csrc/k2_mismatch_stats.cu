@@ -10,10 +10,11 @@
 // "Algorithmic TIM Compensation"); per batch: token means, mean of sequence means
 // (icarus monitoring steps 2-3) and ratios.
 //
-// Two or three launches, in fp32 and integer arithmetic only (GB300 has very
-// little fp64 throughput):
+// Two launches, in fp32 and integer arithmetic only (GB300 has very little
+// fp64 throughput):
 //  1. k2_seq_kernel, three 256-thread CTAs per SM.  A sequence of at most 8192
-//     tokens is reduced by one warp, a longer one by a whole CTA.  Each warp
+//     tokens is reduced by one warp (warps claim sequences in index order from
+//     a counter), a longer one by a whole CTA.  Each warp
 //     stages its sequence through shared memory in chunks of 448 tokens with 1-D
 //     bulk copies (double-buffered: the next chunk is in flight while this one is
 //     reduced), so a few instructions keep ~75 KB per SM in flight.  Inside a
@@ -26,9 +27,8 @@
 //     sequence and on the sequence's length, so a sequence's record has the same
 //     bits wherever it is packed and whatever else is in the batch.
 //  2. k2_fold_kernel: CTA j folds sequences 1024 j .. 1024 j + 1023 (4 per
-//     thread, structure-of-arrays records, coalesced) with float-float (TwoSum)
-//     sums and integer counts in a fixed tree.
-//  3. k2_final_kernel (only when S > 1024): one CTA folds the partials in order.
+//     thread, 16-word records) with float-float (TwoSum) sums and integer
+//     counts in a fixed tree; the CTA that finishes last folds the partials.
 // The batch record depends on S and the sequence records only.
 #include <algorithm>
 #include <cfloat>
@@ -43,17 +43,17 @@ namespace {
 
 enum { F_D = 0, F_AD, F_K2, F_K3, F_W, F_REL, NSUM };
 
-// Sequence record, structure of arrays: word f of sequence s is rec[f * S + s].
+// Sequence record, 16 words per sequence: word f of sequence s is rec[16 s + f].
 enum {
     R_VALID = 0, R_N_MASK, R_N_USED, R_N_NAN, R_N_CLIP, R_FLAG,   // int32
     R_SD, R_SAD, R_SK2, R_SK3, R_SW, R_SREL, R_MAX, R_MK1, R_MK2, R_MK3,   // float
 };
 static_assert(R_MK3 + 1 == K2_REC_WORDS, "record layout");
 
-// Fold partial: 7 int64 counts, 9 float-float sums, 1 max (words).
+// Fold partial: 7 int32 counts (N < 2^31), 9 float-float sums, 1 max (words).
 enum { P_N_MASK = 0, P_N_USED, P_N_NAN, P_N_CLIP, P_NONEMPTY, P_REJ, P_INVALID, NCNT };
 enum { S_SD = 0, S_SAD, S_SK2, S_SK3, S_SW, S_SREL, S_MK1, S_MK2, S_MK3, NDF };
-static_assert(2 * NCNT + 2 * NDF + 1 <= K2_PART_WORDS, "partial layout");
+static_assert(NCNT + 2 * NDF + 1 <= K2_PART_WORDS, "partial layout");
 
 // Float-float value hi + lo and its addition (Knuth's TwoSum on the high
 // parts, low parts added to the error term, renormalised).
@@ -340,29 +340,238 @@ __device__ __forceinline__ void write_seq(const K2Args &a, int s, const SeqTot &
     o[TIM_SEQ_MEAN_W] = mean(t.sum[F_W]);
     o[TIM_SEQ_MEAN_REL] = mean(t.sum[F_REL]);
     o[12] = o[13] = o[14] = o[15] = 0.f;
-    if (lane < TIM_SEQ_FIELDS)
-        a.seq_stats[static_cast<size_t>(s) * TIM_SEQ_FIELDS + lane] = pick(o, lane);
-    float r[16];
-    r[R_VALID] = __uint_as_float(1u);
-    r[R_N_MASK] = __uint_as_float(static_cast<uint32_t>(t.cnt[0]));
-    r[R_N_USED] = __uint_as_float(static_cast<uint32_t>(t.cnt[1]));
-    r[R_N_NAN] = __uint_as_float(static_cast<uint32_t>(t.cnt[2]));
-    r[R_N_CLIP] = __uint_as_float(static_cast<uint32_t>(t.cnt[3]));
-    r[R_FLAG] = __uint_as_float(static_cast<uint32_t>(flag));
-    r[R_SD] = t.sum[F_D];
-    r[R_SAD] = t.sum[F_AD];
-    r[R_SK2] = t.sum[F_K2];
-    r[R_SK3] = t.sum[F_K3];
-    r[R_SW] = t.sum[F_W];
-    r[R_SREL] = t.sum[F_REL];
-    r[R_MAX] = t.mx;
-    r[R_MK1] = -md;
-    r[R_MK2] = mk2;
-    r[R_MK3] = mk3;
-    if (lane < K2_REC_WORDS)
-        a.rec[static_cast<size_t>(lane) * a.S + s] = __float_as_uint(pick(r, lane));
+    float *srow = a.seq_stats + static_cast<size_t>(s) * TIM_SEQ_FIELDS;
+    if (a.stats_vec) {   // 16-byte aligned rows: three float4 stores
+        if (lane < 3) {
+            const float4 v = lane == 0 ? make_float4(o[0], o[1], o[2], o[3])
+                           : lane == 1 ? make_float4(o[4], o[5], o[6], o[7])
+                                       : make_float4(o[8], o[9], o[10], o[11]);
+            reinterpret_cast<float4 *>(srow)[lane] = v;
+        }
+    } else if (lane < TIM_SEQ_FIELDS) {
+        srow[lane] = pick(o, lane);
+    }
+    uint32_t r[16];
+    r[R_VALID] = 1u;
+    r[R_N_MASK] = static_cast<uint32_t>(t.cnt[0]);
+    r[R_N_USED] = static_cast<uint32_t>(t.cnt[1]);
+    r[R_N_NAN] = static_cast<uint32_t>(t.cnt[2]);
+    r[R_N_CLIP] = static_cast<uint32_t>(t.cnt[3]);
+    r[R_FLAG] = static_cast<uint32_t>(flag);
+    r[R_SD] = __float_as_uint(t.sum[F_D]);
+    r[R_SAD] = __float_as_uint(t.sum[F_AD]);
+    r[R_SK2] = __float_as_uint(t.sum[F_K2]);
+    r[R_SK3] = __float_as_uint(t.sum[F_K3]);
+    r[R_SW] = __float_as_uint(t.sum[F_W]);
+    r[R_SREL] = __float_as_uint(t.sum[F_REL]);
+    r[R_MAX] = __float_as_uint(t.mx);
+    r[R_MK1] = __float_as_uint(-md);
+    r[R_MK2] = __float_as_uint(mk2);
+    r[R_MK3] = __float_as_uint(mk3);
+    if (lane < 4) {
+        const uint4 v = lane == 0 ? make_uint4(r[0], r[1], r[2], r[3])
+                      : lane == 1 ? make_uint4(r[4], r[5], r[6], r[7])
+                      : lane == 2 ? make_uint4(r[8], r[9], r[10], r[11])
+                                  : make_uint4(r[12], r[13], r[14], r[15]);
+        reinterpret_cast<uint4 *>(a.rec + static_cast<size_t>(s) * K2_REC_WORDS)[lane] = v;
+    }
     if (lane == 0)
         a.seq_flags[s] = flag;
+}
+
+struct FoldAcc {
+    int cnt[NCNT];
+    ff sum[NDF];
+    float mx;
+};
+
+__device__ __forceinline__ void fold_zero(FoldAcc &f)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        f.cnt[i] = 0;
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        f.sum[i] = {0.f, 0.f};
+    f.mx = 0.f;
+}
+
+__device__ __forceinline__ void fold_add(FoldAcc &x, const FoldAcc &y)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        x.cnt[i] += y.cnt[i];
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        x.sum[i] = ff_add(x.sum[i], y.sum[i]);
+    x.mx = fmaxf(x.mx, y.mx);
+}
+
+// One level of a fixed xor-shuffle tree: x += x of lane ^ o, field by field
+// (the float-float sum is symmetric, so both lanes get the same bits).
+__device__ __forceinline__ void fold_shfl_add(FoldAcc &x, int o)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        x.cnt[i] += __shfl_xor_sync(0xffffffffu, x.cnt[i], o);
+#pragma unroll
+    for (int i = 0; i < NDF; ++i) {
+        const ff y = {__shfl_xor_sync(0xffffffffu, x.sum[i].hi, o), __shfl_xor_sync(0xffffffffu, x.sum[i].lo, o)};
+        x.sum[i] = ff_add(x.sum[i], y);
+    }
+    x.mx = fmaxf(x.mx, __shfl_xor_sync(0xffffffffu, x.mx, o));
+}
+
+// The warp's total, on lane 0 (and on every lane): a fixed tree.
+__device__ __forceinline__ void fold_warp(FoldAcc &x)
+{
+#pragma unroll 1
+    for (int o = 16; o > 0; o >>= 1)
+        fold_shfl_add(x, o);
+}
+
+__device__ __forceinline__ void fold_store(uint32_t *p, const FoldAcc &f)
+{
+    for (int i = 0; i < NCNT; ++i)
+        p[i] = static_cast<uint32_t>(f.cnt[i]);
+    for (int i = 0; i < NDF; ++i) {
+        p[NCNT + 2 * i] = __float_as_uint(f.sum[i].hi);
+        p[NCNT + 2 * i + 1] = __float_as_uint(f.sum[i].lo);
+    }
+    p[NCNT + 2 * NDF] = __float_as_uint(f.mx);
+}
+
+// From shared memory.
+__device__ __forceinline__ void fold_load(FoldAcc &f, const uint32_t *p)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        f.cnt[i] = static_cast<int>(p[i]);
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        f.sum[i] = {__uint_as_float(p[NCNT + 2 * i]), __uint_as_float(p[NCNT + 2 * i + 1])};
+    f.mx = __uint_as_float(p[NCNT + 2 * NDF]);
+}
+
+// From global memory written by another CTA (read through L2).
+__device__ __forceinline__ void fold_load_global(FoldAcc &f, const uint32_t *p)
+{
+#pragma unroll
+    for (int i = 0; i < NCNT; ++i)
+        f.cnt[i] = static_cast<int>(__ldcg(p + i));
+#pragma unroll
+    for (int i = 0; i < NDF; ++i)
+        f.sum[i] = {__uint_as_float(__ldcg(p + NCNT + 2 * i)), __uint_as_float(__ldcg(p + NCNT + 2 * i + 1))};
+    f.mx = __uint_as_float(__ldcg(p + NCNT + 2 * NDF));
+}
+
+// fp32 -> fp64 by moving bits (exact; fp32 subnormals are renormalised).  The
+// batch record is written without fp64 arithmetic, which GB300 runs slowly.
+__device__ __forceinline__ double widen(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint64_t sign = static_cast<uint64_t>(u >> 31) << 63;
+    const uint32_t e = (u >> 23) & 0xffu, m = u & 0x7fffffu;
+    uint64_t bits;
+    if (e == 0u && m == 0u) {
+        bits = sign;
+    } else if (e == 0u) {
+        const int msb = 31 - __clz(static_cast<int>(m));   // value = m * 2^-149
+        bits = sign | (static_cast<uint64_t>(msb - 149 + 1023) << 52) |
+               ((static_cast<uint64_t>(m) << (52 - msb)) & ((uint64_t(1) << 52) - 1));
+    } else if (e == 255u) {
+        bits = sign | (uint64_t(0x7ff) << 52) | (static_cast<uint64_t>(m) << 29);
+    } else {
+        bits = sign | (static_cast<uint64_t>(e - 127 + 1023) << 52) | (static_cast<uint64_t>(m) << 29);
+    }
+    return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// A count (< 2^31) as fp64, by moving bits.
+__device__ __forceinline__ double widen_count(long long n)
+{
+    if (n <= 0)
+        return 0.0;
+    const uint64_t v = static_cast<uint64_t>(n);
+    const int lz = __clzll(static_cast<long long>(v));
+    const uint64_t frac = ((v << lz) << 1) >> 12;
+    return __longlong_as_double(static_cast<long long>((static_cast<uint64_t>(63 - lz + 1023) << 52) | frac));
+}
+
+// The batch record from the folded totals (thread 0).  Means and ratios are
+// fp32 quotients (relative error ~1e-7) of the float-float sums and counts.
+__device__ void write_batch(const K2Args &a, const FoldAcc &t, bool check_offsets)
+{
+    bool bad = t.cnt[P_INVALID] > 0;
+    if (check_offsets)
+        bad = bad || a.off[0] != 0 || static_cast<int64_t>(a.off[a.S]) != a.N;
+    if (bad)
+        atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
+    const float n_used = static_cast<float>(t.cnt[P_N_USED]);
+    const float n_ne = static_cast<float>(t.cnt[P_NONEMPTY]);
+    const float n_mask = static_cast<float>(t.cnt[P_N_MASK]);
+    auto mean = [&](int i, float n) { return n > 0.f ? widen((t.sum[i].hi + t.sum[i].lo) / n) : 0.0; };
+    auto ratio = [](int x, float n) { return n > 0.f ? widen(static_cast<float>(x) / n) : 0.0; };
+    double *o = a.batch;
+    o[TIM_BATCH_N_MASK] = widen_count(t.cnt[P_N_MASK]);
+    o[TIM_BATCH_N_USED] = widen_count(t.cnt[P_N_USED]);
+    o[TIM_BATCH_N_NAN] = widen_count(t.cnt[P_N_NAN]);
+    o[TIM_BATCH_N_CLIP] = widen_count(t.cnt[P_N_CLIP]);
+    o[TIM_BATCH_MEAN_DELTA] = mean(S_SD, n_used);
+    o[TIM_BATCH_MEAN_ABS_DELTA] = mean(S_SAD, n_used);
+    o[TIM_BATCH_MAX_ABS_DELTA] = widen(t.mx);
+    o[TIM_BATCH_MEAN_K1] = n_used > 0.f ? widen(-((t.sum[S_SD].hi + t.sum[S_SD].lo) / n_used)) : 0.0;
+    o[TIM_BATCH_MEAN_K2] = mean(S_SK2, n_used);
+    o[TIM_BATCH_MEAN_K3] = mean(S_SK3, n_used);
+    o[TIM_BATCH_MEAN_W] = mean(S_SW, n_used);
+    o[TIM_BATCH_MEAN_REL] = mean(S_SREL, n_used);
+    o[TIM_BATCH_SEQMEAN_K1] = mean(S_MK1, n_ne);
+    o[TIM_BATCH_SEQMEAN_K2] = mean(S_MK2, n_ne);
+    o[TIM_BATCH_SEQMEAN_K3] = mean(S_MK3, n_ne);
+    o[TIM_BATCH_CLIP_RATIO] = ratio(t.cnt[P_N_CLIP], n_mask);
+    o[TIM_BATCH_NAN_RATIO] = ratio(t.cnt[P_N_NAN], n_mask);
+    o[TIM_BATCH_REJECT_RATIO] = ratio(t.cnt[P_REJ], n_ne);
+    o[TIM_BATCH_N_SEQS_NONEMPTY] = widen_count(t.cnt[P_NONEMPTY]);
+    o[TIM_BATCH_N_REJECTED] = widen_count(t.cnt[P_REJ]);
+    if (bad)
+        for (int f = 0; f < TIM_BATCH_FIELDS; ++f)
+            o[f] = __longlong_as_double(0x7ff8000000000000ll);
+}
+
+// The fold term of sequence s (its 16-word record, read through L2: other
+// warps wrote it).
+__device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
+{
+    const uint4 *rp = reinterpret_cast<const uint4 *>(a.rec + static_cast<size_t>(s) * K2_REC_WORDS);
+    const uint4 q0 = __ldcg(rp), q1 = __ldcg(rp + 1), q2 = __ldcg(rp + 2), q3 = __ldcg(rp + 3);
+    const uint32_t rc[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                             q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+    FoldAcc y;
+    fold_zero(y);
+    if (rc[R_VALID] == 0u) {
+        y.cnt[P_INVALID] = 1;
+    } else {
+        const uint32_t nu = rc[R_N_USED];
+        y.cnt[P_N_MASK] = static_cast<int>(rc[R_N_MASK]);
+        y.cnt[P_N_USED] = static_cast<int>(nu);
+        y.cnt[P_N_NAN] = static_cast<int>(rc[R_N_NAN]);
+        y.cnt[P_N_CLIP] = static_cast<int>(rc[R_N_CLIP]);
+        y.sum[S_SD] = {__uint_as_float(rc[R_SD]), 0.f};
+        y.sum[S_SAD] = {__uint_as_float(rc[R_SAD]), 0.f};
+        y.sum[S_SK2] = {__uint_as_float(rc[R_SK2]), 0.f};
+        y.sum[S_SK3] = {__uint_as_float(rc[R_SK3]), 0.f};
+        y.sum[S_SW] = {__uint_as_float(rc[R_SW]), 0.f};
+        y.sum[S_SREL] = {__uint_as_float(rc[R_SREL]), 0.f};
+        y.mx = __uint_as_float(rc[R_MAX]);
+        if (nu > 0u) {
+            y.cnt[P_NONEMPTY] = 1;
+            y.cnt[P_REJ] = static_cast<int>(rc[R_FLAG]);
+            y.sum[S_MK1] = {__uint_as_float(rc[R_MK1]), 0.f};
+            y.sum[S_MK2] = {__uint_as_float(rc[R_MK2]), 0.f};
+            y.sum[S_MK3] = {__uint_as_float(rc[R_MK3]), 0.f};
+        }
+    }
+    fold_add(x, y);
 }
 
 __device__ __forceinline__ bool offsets_ok(const K2Args &a, int s, int64_t b, int64_t e)
@@ -391,7 +600,7 @@ __device__ __forceinline__ void write_plain(const K2Args &a, int s, bool bad, in
         if (lane < TIM_SEQ_FIELDS)
             a.seq_stats[static_cast<size_t>(s) * TIM_SEQ_FIELDS + lane] = qnan();
         if (lane < K2_REC_WORDS)
-            a.rec[static_cast<size_t>(lane) * a.S + s] = 0u;
+            a.rec[static_cast<size_t>(s) * K2_REC_WORDS + lane] = 0u;   // not valid
         if (lane == 0)
             a.seq_flags[s] = 0;
     } else {
@@ -405,12 +614,28 @@ __device__ __forceinline__ void write_plain(const K2Args &a, int s, bool bad, in
     }
 }
 
-// Next sequence from s on (stride `step`) that the warp reduces itself;
-// records of empty or bad sequences met on the way are written at once, long
-// ones are left for the CTA phase.  Returns S when there is none.
-__device__ __forceinline__ int next_short(const K2Args &a, int s, int step, int lane)
+// Claims the next sequence index for this warp (lane 0 takes it from the
+// call's counter; the value is not waited for until it is broadcast).
+__device__ __forceinline__ int claim_raw(const K2Args &a, int lane)
 {
-    for (; s < a.S; s += step) {
+    return lane == 0 ? atomicAdd(a.claim, 1) : 0;
+}
+
+// The next sequence the warp reduces itself.  The warp keeps two claims in
+// flight (lane 0: raw, then the later raw2); each step takes the older one and
+// claims a new one, so no claimed index is ever dropped while a smaller one is
+// held, and a claim's latency hides behind the sequences before it.  Records
+// of empty or bad sequences met on the way are written at once, long ones are
+// left for the CTA phase.  Returns S when there is none (every claim still in
+// flight is then past S too).
+__device__ __forceinline__ int next_short(const K2Args &a, int &raw, int &raw2, int lane)
+{
+    while (true) {
+        const int s = __shfl_sync(0xffffffffu, raw, 0);
+        raw = raw2;
+        raw2 = claim_raw(a, lane);
+        if (s >= a.S)
+            return a.S;
         const int64_t b = a.off[s], e = a.off[s + 1];
         if (!offsets_ok(a, s, b, e)) {
             write_plain(a, s, true, lane);
@@ -424,7 +649,6 @@ __device__ __forceinline__ int next_short(const K2Args &a, int s, int step, int 
         }
         return s;
     }
-    return a.S;
 }
 
 __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(const K2Args a)
@@ -462,10 +686,14 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     int stage = 0;
     bool ok = true;
 
-    // ---- phase 1: sequences of at most K2_LONG tokens, one warp each.  Warp w
-    // of CTA c takes sequences w * gridDim + c, + warps in the grid, ...
-    const int step = gridDim.x * K2_WARPS;
-    int s = next_short(a, warp * gridDim.x + blockIdx.x, step, lane);
+    // ---- phase 1: sequences of at most K2_LONG tokens, one warp each.  Warps
+    // claim sequences in index order from the call's counter, two ahead of the
+    // one they reduce, so the work stays balanced however the lengths vary (a
+    // record's bits depend on its own tokens only, not on the warp that reduces
+    // it).
+    int raw = claim_raw(a, lane);
+    int raw2 = claim_raw(a, lane);
+    int s = next_short(a, raw, raw2, lane);
     ChunkView cur;
     if (s < a.S) {
         const int64_t b = a.off[s], e = a.off[s + 1];
@@ -487,7 +715,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
                 nv = stage_chunk(a, nst, nbar, t0, min(e, t0 + K2_CHUNK), lane, pol);
                 pending |= 1u << (stage ^ 1);
             } else {
-                nxt = next_short(a, s + step, step, lane);
+                nxt = next_short(a, raw, raw2, lane);
                 if (nxt < a.S) {
                     const int64_t nb = a.off[nxt], ne = a.off[nxt + 1];
                     nv = stage_chunk(a, nst, nbar, nb, min(ne, nb + K2_CHUNK), lane, pol);
@@ -522,7 +750,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     }
 
     // ---- phase 2: longer sequences, one CTA each; warp w takes chunks w, w + K2_WARPS, ...
-    // (the CTA's phase-1 warps met exactly the sequences q = blockIdx.x + k gridDim.x)
+    // (the sequences q = blockIdx.x + k gridDim.x; phase 1 skipped every long one)
     if (!has_long)   // uniform over the CTA
         return;
     if (!ok)
@@ -603,250 +831,65 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     }
 }
 
-struct FoldAcc {
-    long long cnt[NCNT];
-    ff sum[NDF];
-    float mx;
-};
-
-__device__ __forceinline__ void fold_zero(FoldAcc &f)
-{
-#pragma unroll
-    for (int i = 0; i < NCNT; ++i)
-        f.cnt[i] = 0;
-#pragma unroll
-    for (int i = 0; i < NDF; ++i)
-        f.sum[i] = {0.f, 0.f};
-    f.mx = 0.f;
-}
-
-__device__ __forceinline__ void fold_add(FoldAcc &x, const FoldAcc &y)
-{
-#pragma unroll
-    for (int i = 0; i < NCNT; ++i)
-        x.cnt[i] += y.cnt[i];
-#pragma unroll
-    for (int i = 0; i < NDF; ++i)
-        x.sum[i] = ff_add(x.sum[i], y.sum[i]);
-    x.mx = fmaxf(x.mx, y.mx);
-}
-
-__device__ __forceinline__ FoldAcc fold_shfl_xor(const FoldAcc &x, int o)
-{
-    FoldAcc y;
-#pragma unroll
-    for (int i = 0; i < NCNT; ++i)
-        y.cnt[i] = __shfl_xor_sync(0xffffffffu, x.cnt[i], o);
-#pragma unroll
-    for (int i = 0; i < NDF; ++i) {
-        y.sum[i].hi = __shfl_xor_sync(0xffffffffu, x.sum[i].hi, o);
-        y.sum[i].lo = __shfl_xor_sync(0xffffffffu, x.sum[i].lo, o);
-    }
-    y.mx = __shfl_xor_sync(0xffffffffu, x.mx, o);
-    return y;
-}
-
-__device__ __forceinline__ void fold_store(uint32_t *p, const FoldAcc &f)
-{
-    for (int i = 0; i < NCNT; ++i) {
-        p[2 * i] = static_cast<uint32_t>(static_cast<unsigned long long>(f.cnt[i]));
-        p[2 * i + 1] = static_cast<uint32_t>(static_cast<unsigned long long>(f.cnt[i]) >> 32);
-    }
-    for (int i = 0; i < NDF; ++i) {
-        p[2 * NCNT + 2 * i] = __float_as_uint(f.sum[i].hi);
-        p[2 * NCNT + 2 * i + 1] = __float_as_uint(f.sum[i].lo);
-    }
-    p[2 * NCNT + 2 * NDF] = __float_as_uint(f.mx);
-}
-
-__device__ __forceinline__ void fold_load(FoldAcc &f, const uint32_t *p)
-{
-#pragma unroll
-    for (int i = 0; i < NCNT; ++i)
-        f.cnt[i] = static_cast<long long>(static_cast<unsigned long long>(p[2 * i]) |
-                                          (static_cast<unsigned long long>(p[2 * i + 1]) << 32));
-#pragma unroll
-    for (int i = 0; i < NDF; ++i)
-        f.sum[i] = {__uint_as_float(p[2 * NCNT + 2 * i]), __uint_as_float(p[2 * NCNT + 2 * i + 1])};
-    f.mx = __uint_as_float(p[2 * NCNT + 2 * NDF]);
-}
-
-// Fixed tree over a CTA: xor shuffles inside each warp (lane 0's value is
-// deterministic), then the same over the warp totals in warp 0.  Returns the
-// total on thread 0.
-template <int NTHREADS>
+// Fold of the sequence records into the batch record, one launch: CTA b folds
+// sequences 1024 b .. 1024 b + 1023 -- thread i takes 1024 b + i + 256 k for
+// k = 0..3 in order, a fixed xor tree per warp, then warp 0 adds the 8 warp
+// totals in warp order -- into the block's partial; the CTA that finishes
+// last (a ticket) folds the partials the same way (thread i: partials i,
+// i + 256, ...).  The order of every sum is fixed by S alone.
 __device__ __forceinline__ FoldAcc fold_cta(FoldAcc x)
 {
-    constexpr int NW = NTHREADS / 32;
-    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "warps per CTA");
-    __shared__ uint32_t sh[NW][K2_PART_WORDS];
-#pragma unroll 1
-    for (int o = 16; o > 0; o >>= 1) {
-        const FoldAcc y = fold_shfl_xor(x, o);
-        fold_add(x, y);
-    }
+    __shared__ uint32_t sh[K2_FOLD_THREADS / 32][K2_PART_WORDS];
+    fold_warp(x);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0)
         fold_store(sh[warp], x);
     __syncthreads();
     FoldAcc t;
     fold_zero(t);
-    if (warp == 0) {
-        if (lane < NW)
-            fold_load(t, sh[lane]);
-#pragma unroll 1
-        for (int o = NW / 2; o > 0; o >>= 1) {
-            const FoldAcc y = fold_shfl_xor(t, o);
+    if (warp == 0 && lane == 0)
+        for (int w = 0; w < K2_FOLD_THREADS / 32; ++w) {
+            FoldAcc y;
+            fold_load(y, sh[w]);
             fold_add(t, y);
         }
-    }
-    return t;
+    return t;   // on thread 0
 }
 
-// fp32 -> fp64 by moving bits (exact; fp32 subnormals are renormalised).  The
-// batch record is written without fp64 arithmetic, which GB300 runs slowly.
-__device__ __forceinline__ double widen(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    const uint64_t sign = static_cast<uint64_t>(u >> 31) << 63;
-    const uint32_t e = (u >> 23) & 0xffu, m = u & 0x7fffffu;
-    uint64_t bits;
-    if (e == 0u && m == 0u) {
-        bits = sign;
-    } else if (e == 0u) {
-        const int msb = 31 - __clz(static_cast<int>(m));   // value = m * 2^-149
-        bits = sign | (static_cast<uint64_t>(msb - 149 + 1023) << 52) |
-               ((static_cast<uint64_t>(m) << (52 - msb)) & ((uint64_t(1) << 52) - 1));
-    } else if (e == 255u) {
-        bits = sign | (uint64_t(0x7ff) << 52) | (static_cast<uint64_t>(m) << 29);
-    } else {
-        bits = sign | (static_cast<uint64_t>(e - 127 + 1023) << 52) | (static_cast<uint64_t>(m) << 29);
-    }
-    return __longlong_as_double(static_cast<long long>(bits));
-}
-
-// A count (< 2^53) as fp64, by moving bits.
-__device__ __forceinline__ double widen_count(long long n)
-{
-    if (n <= 0)
-        return 0.0;
-    const uint64_t v = static_cast<uint64_t>(n);
-    const int lz = __clzll(static_cast<long long>(v));
-    const uint64_t frac = ((v << lz) << 1) >> 12;
-    return __longlong_as_double(static_cast<long long>((static_cast<uint64_t>(63 - lz + 1023) << 52) | frac));
-}
-
-// The batch record from the folded totals (thread 0).  Means and ratios are
-// fp32 quotients (relative error ~1e-7) of the float-float sums and counts.
-__device__ void write_batch(const K2Args &a, const FoldAcc &t, bool check_offsets)
-{
-    bool bad = t.cnt[P_INVALID] > 0;
-    if (check_offsets)
-        bad = bad || a.off[0] != 0 || static_cast<int64_t>(a.off[a.S]) != a.N;
-    if (bad)
-        atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
-    const float n_used = static_cast<float>(t.cnt[P_N_USED]);
-    const float n_ne = static_cast<float>(t.cnt[P_NONEMPTY]);
-    const float n_mask = static_cast<float>(t.cnt[P_N_MASK]);
-    auto mean = [&](int i, float n) { return n > 0.f ? widen((t.sum[i].hi + t.sum[i].lo) / n) : 0.0; };
-    auto ratio = [](long long x, float n) { return n > 0.f ? widen(static_cast<float>(x) / n) : 0.0; };
-    double *o = a.batch;
-    o[TIM_BATCH_N_MASK] = widen_count(t.cnt[P_N_MASK]);
-    o[TIM_BATCH_N_USED] = widen_count(t.cnt[P_N_USED]);
-    o[TIM_BATCH_N_NAN] = widen_count(t.cnt[P_N_NAN]);
-    o[TIM_BATCH_N_CLIP] = widen_count(t.cnt[P_N_CLIP]);
-    o[TIM_BATCH_MEAN_DELTA] = mean(S_SD, n_used);
-    o[TIM_BATCH_MEAN_ABS_DELTA] = mean(S_SAD, n_used);
-    o[TIM_BATCH_MAX_ABS_DELTA] = widen(t.mx);
-    o[TIM_BATCH_MEAN_K1] = n_used > 0.f ? widen(-((t.sum[S_SD].hi + t.sum[S_SD].lo) / n_used)) : 0.0;
-    o[TIM_BATCH_MEAN_K2] = mean(S_SK2, n_used);
-    o[TIM_BATCH_MEAN_K3] = mean(S_SK3, n_used);
-    o[TIM_BATCH_MEAN_W] = mean(S_SW, n_used);
-    o[TIM_BATCH_MEAN_REL] = mean(S_SREL, n_used);
-    o[TIM_BATCH_SEQMEAN_K1] = mean(S_MK1, n_ne);
-    o[TIM_BATCH_SEQMEAN_K2] = mean(S_MK2, n_ne);
-    o[TIM_BATCH_SEQMEAN_K3] = mean(S_MK3, n_ne);
-    o[TIM_BATCH_CLIP_RATIO] = ratio(t.cnt[P_N_CLIP], n_mask);
-    o[TIM_BATCH_NAN_RATIO] = ratio(t.cnt[P_N_NAN], n_mask);
-    o[TIM_BATCH_REJECT_RATIO] = ratio(t.cnt[P_REJ], n_ne);
-    o[TIM_BATCH_N_SEQS_NONEMPTY] = widen_count(t.cnt[P_NONEMPTY]);
-    o[TIM_BATCH_N_REJECTED] = widen_count(t.cnt[P_REJ]);
-    if (bad)
-        for (int f = 0; f < TIM_BATCH_FIELDS; ++f)
-            o[f] = __longlong_as_double(0x7ff8000000000000ll);
-}
-
-// The fold term of sequence s (structure-of-arrays record).
-__device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
-{
-    const size_t S = static_cast<size_t>(a.S);
-    const uint32_t *rc = a.rec + s;
-    FoldAcc y;
-    fold_zero(y);
-    if (rc[R_VALID * S] == 0u) {
-        y.cnt[P_INVALID] = 1;
-    } else {
-        const uint32_t nu = rc[R_N_USED * S];
-        y.cnt[P_N_MASK] = rc[R_N_MASK * S];
-        y.cnt[P_N_USED] = nu;
-        y.cnt[P_N_NAN] = rc[R_N_NAN * S];
-        y.cnt[P_N_CLIP] = rc[R_N_CLIP * S];
-        y.sum[S_SD] = {__uint_as_float(rc[R_SD * S]), 0.f};
-        y.sum[S_SAD] = {__uint_as_float(rc[R_SAD * S]), 0.f};
-        y.sum[S_SK2] = {__uint_as_float(rc[R_SK2 * S]), 0.f};
-        y.sum[S_SK3] = {__uint_as_float(rc[R_SK3 * S]), 0.f};
-        y.sum[S_SW] = {__uint_as_float(rc[R_SW * S]), 0.f};
-        y.sum[S_SREL] = {__uint_as_float(rc[R_SREL * S]), 0.f};
-        y.mx = __uint_as_float(rc[R_MAX * S]);
-        if (nu > 0u) {
-            y.cnt[P_NONEMPTY] = 1;
-            y.cnt[P_REJ] = rc[R_FLAG * S];
-            y.sum[S_MK1] = {__uint_as_float(rc[R_MK1 * S]), 0.f};
-            y.sum[S_MK2] = {__uint_as_float(rc[R_MK2 * S]), 0.f};
-            y.sum[S_MK3] = {__uint_as_float(rc[R_MK3 * S]), 0.f};
-        }
-    }
-    fold_add(x, y);
-}
-
-// CTA j folds sequences 1024 j + i + 256 k (k = 0..3, in order) on thread i;
-// with a single CTA it writes the batch record directly.
 __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a)
 {
     pdl_wait();   // the records come from k2_seq_kernel
-    pdl_launch_dependents();
+    __shared__ int last_s;
     FoldAcc x;
     fold_zero(x);
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x;
-#pragma unroll 1
-    for (int k = 0; k < K2_FOLD_SEQS / K2_FOLD_THREADS; ++k) {
-        const int64_t s = base + static_cast<int64_t>(k) * K2_FOLD_THREADS;
-        if (s < a.S)
-            fold_seq(x, a, s);
-    }
-    const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
+    const int64_t s1 = min(static_cast<int64_t>(a.S), static_cast<int64_t>(blockIdx.x + 1) * K2_FOLD_SEQS);
+    for (int64_t s = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x; s < s1; s += K2_FOLD_THREADS)
+        fold_seq(x, a, s);
+    const FoldAcc t = fold_cta(x);
     if (threadIdx.x == 0) {
-        if (gridDim.x == 1)
+        if (gridDim.x == 1) {
             write_batch(a, t, false);
-        else
+            last_s = 0;
+        } else {
             fold_store(a.part + static_cast<size_t>(blockIdx.x) * K2_PART_WORDS, t);
+            __threadfence();
+            last_s = atomicAdd(a.blk_done, 1) == static_cast<int>(gridDim.x) - 1;
+        }
     }
-}
-
-// One CTA folds the partials: thread i takes partials i, i + 256, ... in order.
-__global__ void __launch_bounds__(K2_FOLD_THREADS) k2_final_kernel(const K2Args a, int parts)
-{
-    pdl_wait();   // the partials come from k2_fold_kernel
-    FoldAcc x;
-    fold_zero(x);
-    for (int p = threadIdx.x; p < parts; p += K2_FOLD_THREADS) {
-        FoldAcc y;
-        fold_load(y, a.part + static_cast<size_t>(p) * K2_PART_WORDS);
-        fold_add(x, y);
+    __syncthreads();
+    if (!last_s)
+        return;
+    __threadfence();   // every CTA's partial is visible
+    FoldAcc y;
+    fold_zero(y);
+    for (int p = threadIdx.x; p < static_cast<int>(gridDim.x); p += K2_FOLD_THREADS) {
+        FoldAcc z;
+        fold_load_global(z, a.part + static_cast<size_t>(p) * K2_PART_WORDS);
+        fold_add(y, z);
     }
-    const FoldAcc t = fold_cta<K2_FOLD_THREADS>(x);
+    const FoldAcc f = fold_cta(y);
     if (threadIdx.x == 0)
-        write_batch(a, t, false);
+        write_batch(a, f, false);
 }
 
 // S = 0: only the (all-zero) batch record, after checking the offsets cover [0, N).
@@ -875,23 +918,19 @@ cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // the sequence counter and the fold's ticket start at zero
+    cudaError_t e = cudaMemsetAsync(a.claim, 0, 256, stream);
+    if (e != cudaSuccess)
+        return e;
     cfg.gridDim = dim3(std::min(a.S, num_sms * K2_CTAS_PER_SM), 1, 1);
     cfg.blockDim = dim3(K2_THREADS, 1, 1);
     cfg.dynamicSmemBytes = K2_SMEM_BYTES;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k2_seq_kernel, a);
-    if (e != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, k2_seq_kernel, a)) != cudaSuccess)
         return e;
-    const int parts = (a.S + K2_FOLD_SEQS - 1) / K2_FOLD_SEQS;
-    cfg.gridDim = dim3(parts, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(k2_blocks(a.S)), 1, 1);
     cfg.blockDim = dim3(K2_FOLD_THREADS, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    if ((e = cudaLaunchKernelEx(&cfg, k2_fold_kernel, a)) != cudaSuccess)
-        return e;
-    if (parts > 1) {
-        cfg.gridDim = dim3(1, 1, 1);
-        e = cudaLaunchKernelEx(&cfg, k2_final_kernel, a, parts);
-    }
-    return e;
+    return cudaLaunchKernelEx(&cfg, k2_fold_kernel, a);
 }
 
 } // namespace tim

@@ -399,8 +399,11 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
     a.seq_stats = out->seq_stats;
     a.seq_flags = out->seq_flags;
     a.batch = out->batch_stats;
-    a.rec = static_cast<uint32_t *>(ws);
-    a.part = S > 0 ? a.rec + round_up(static_cast<size_t>(S) * tim::K2_REC_WORDS, 64) : nullptr;
+    a.claim = static_cast<int *>(ws);
+    a.blk_done = a.claim ? a.claim + 1 : nullptr;
+    a.rec = S > 0 ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + 256) : nullptr;
+    a.part = S > 0 ? a.rec + static_cast<size_t>(S) * tim::K2_REC_WORDS : nullptr;
+    a.stats_vec = aligned(out->seq_stats, 16) ? 1 : 0;
     a.status = dev->status;
     cudaError_t e = tim::k2_launch(a, dev->sms, s);
     cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
