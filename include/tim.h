@@ -385,6 +385,43 @@ TIM_API int tim_tis_ppo(const float *logp_theta, const float *logp_old, const fl
  */
 TIM_API int tim_selftest_wait_timeout(uint32_t budget_us, tim_stream_t stream);
 
+/* ------------------------------------------------------------------ checked build
+ *
+ * No counterpart on the pages (the stand-in for a memory checker, which this
+ * library's users may not have): libtim_debug.so is the same library built
+ * with TIM_DEBUG.  Its kernels also check, without ever trapping,
+ *   - their own invariants: every TMA coordinate's innermost part is a whole
+ *     16 bytes, every row or column they store lies inside its buffer, every
+ *     claimed work unit is below the unit count, every bulk copy is 16-byte
+ *     aligned and sized;
+ *   - the input contracts the release build passes over silently: a target id
+ *     >= V (negative ids are the ignore label and stay legal), a mask byte
+ *     other than 0 or 1, a non-finite logit (h or W holds inf or NaN), a
+ *     non-finite lse or upstream gradient in the backward, a non-finite
+ *     advantage in the PPO surrogate.
+ * The first violation on a device sets TIM_ERR_BAD_INPUT in the status word
+ * (tim_check returns it) and is recorded; later ones only set the status.
+ * tim_debug_violation(out, stream) synchronises `stream`, writes the record
+ *   out[0] = check (TIM_CHECK_*, 0 if none), out[1] = index (the token, row,
+ *   unit or coordinate concerned), out[2] = value (its bits), out[3] = 0,
+ * and clears it; returns TIM_OK or a CUDA error.  tim_debug_build() is 1 in
+ * libtim_debug.so and 0 in libtim.so (where the record stays zero).
+ */
+enum {
+    TIM_CHECK_NONE = 0,
+    TIM_CHECK_TARGET = 1,          /* target id >= V */
+    TIM_CHECK_MASK = 2,            /* mask byte not 0 or 1 */
+    TIM_CHECK_LOGIT = 3,           /* non-finite logit */
+    TIM_CHECK_BACKWARD_INPUT = 4,  /* non-finite lse or upstream gradient */
+    TIM_CHECK_ADVANTAGE = 5,       /* non-finite PPO advantage */
+    TIM_CHECK_TMA_COORD = 6,       /* a TMA load's innermost coordinate not a whole 16 bytes, or negative */
+    TIM_CHECK_STORE = 7,           /* a store outside its buffer */
+    TIM_CHECK_UNIT = 8,            /* a claimed work unit out of range */
+    TIM_CHECK_BULK = 9             /* a bulk copy not 16-byte aligned or sized */
+};
+TIM_API int tim_debug_violation(int64_t out[4], tim_stream_t stream);
+TIM_API int tim_debug_build(void);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronises `stream`, then returns and clears the status word the kernels

@@ -20,6 +20,7 @@ gradient and masked means (VeXact summary eq. (2)-(3)).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -30,11 +31,13 @@ __all__ = [
     "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
     "tim_tis_ppo", "tim_mismatch_monitor", "tim_split_weight_bytes", "tim_split_weight_fp32",
     "tim_token_logprob_fp32_head", "tim_token_logprob_backward", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
+    "tim_debug_violation", "tim_debug_build", "load_debug", "checked", "CHECKS",
     "token_logprob", "token_logprob_backward", "split_weight_fp32", "token_logprob_fp32_head", "mismatch_stats", "mismatch_monitor", "tis_ppo", "check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libtim.so")
+_DEBUG_LIB_PATH = os.path.join(_PKG, "libtim_debug.so")
 
 TIM_OK = 0
 TIM_ERR_INVALID_ARG = -1
@@ -43,6 +46,10 @@ TIM_ERR_CUDA = -3
 TIM_ERR_TIMEOUT = -4
 TIM_ERR_BAD_INPUT = -5
 NOALLOC_SCRATCH_BYTES = 16 << 20   # TIM_NOALLOC_SCRATCH_BYTES in include/tim.h
+
+# TIM_CHECK_* of include/tim.h: what the checked build (libtim_debug.so) records
+CHECKS = {0: "none", 1: "target", 2: "mask", 3: "logit", 4: "backward_input", 5: "advantage",
+          6: "tma_coord", 7: "store", 8: "unit", 9: "bulk"}
 
 SEQ_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
               "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel")
@@ -91,56 +98,93 @@ class tim_ppo_out(ctypes.Structure):
 
 
 _lock = threading.Lock()
-_lib = None
+_lib = None          # the library calls go to (libtim.so, or libtim_debug.so inside `checked()`)
+_release = None
+_debug = None
 
 
 def lib_path() -> str:
     return _LIB_PATH
 
 
+def _open(path: str, what: str):
+    if not os.path.exists(path):
+        raise TimError(TIM_ERR_CUDA, "%s is not built (%s); run "
+                       "`python -m rollout_logprob_mismatch_gb300.build`" % (what, path))
+    lib = ctypes.CDLL(path)
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    lib.tim_token_logprob.argtypes = [P, P, P, I64, I64, I64, P, P, P]
+    lib.tim_token_logprob.restype = ctypes.c_int
+    lib.tim_token_logprob_temperature.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
+    lib.tim_token_logprob_temperature.restype = ctypes.c_int
+    lib.tim_token_logprob_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, P]
+    lib.tim_token_logprob_noalloc.restype = ctypes.c_int
+    lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float, ctypes.POINTER(tim_mismatch_out), P]
+    lib.tim_mismatch_stats.restype = ctypes.c_int
+    F = ctypes.c_float
+    lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
+    lib.tim_tis_ppo.restype = ctypes.c_int
+    lib.tim_split_weight_bytes.argtypes = [I64, I64]
+    lib.tim_split_weight_bytes.restype = ctypes.c_int64
+    lib.tim_split_weight_fp32.argtypes = [P, I64, I64, P, P]
+    lib.tim_split_weight_fp32.restype = ctypes.c_int
+    lib.tim_token_logprob_fp32_head.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
+    lib.tim_token_logprob_fp32_head.restype = ctypes.c_int
+    lib.tim_token_logprob_backward.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, P, P,
+                                               ctypes.c_int, P]
+    lib.tim_token_logprob_backward.restype = ctypes.c_int
+    lib.tim_mismatch_monitor.argtypes = [P, P, P, I64, F, P, P, P]
+    lib.tim_mismatch_monitor.restype = ctypes.c_int
+    lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.tim_selftest_wait_timeout.restype = ctypes.c_int
+    lib.tim_check.argtypes = [P]
+    lib.tim_check.restype = ctypes.c_int
+    lib.tim_debug_violation.argtypes = [ctypes.POINTER(ctypes.c_int64), P]
+    lib.tim_debug_violation.restype = ctypes.c_int
+    lib.tim_debug_build.argtypes = []
+    lib.tim_debug_build.restype = ctypes.c_int
+    lib.tim_last_error.argtypes = []
+    lib.tim_last_error.restype = ctypes.c_char_p
+    lib.tim_version.argtypes = []
+    lib.tim_version.restype = ctypes.c_int
+    return lib
+
+
 def load():
-    """The loaded libtim.so; raises TimError when it has not been built."""
-    global _lib
+    """The library calls go to: libtim.so (libtim_debug.so inside `checked()`);
+    raises TimError when it has not been built."""
+    global _lib, _release
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise TimError(TIM_ERR_CUDA, "libtim.so is not built (%s); run "
-                               "`python -m rollout_logprob_mismatch_gb300.build`" % _LIB_PATH)
-            lib = ctypes.CDLL(_LIB_PATH)
-            P, I64 = ctypes.c_void_p, ctypes.c_int64
-            lib.tim_token_logprob.argtypes = [P, P, P, I64, I64, I64, P, P, P]
-            lib.tim_token_logprob.restype = ctypes.c_int
-            lib.tim_token_logprob_temperature.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
-            lib.tim_token_logprob_temperature.restype = ctypes.c_int
-            lib.tim_token_logprob_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, P]
-            lib.tim_token_logprob_noalloc.restype = ctypes.c_int
-            lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float,
-                                               ctypes.POINTER(tim_mismatch_out), P]
-            lib.tim_mismatch_stats.restype = ctypes.c_int
-            F = ctypes.c_float
-            lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
-            lib.tim_tis_ppo.restype = ctypes.c_int
-            lib.tim_split_weight_bytes.argtypes = [I64, I64]
-            lib.tim_split_weight_bytes.restype = ctypes.c_int64
-            lib.tim_split_weight_fp32.argtypes = [P, I64, I64, P, P]
-            lib.tim_split_weight_fp32.restype = ctypes.c_int
-            lib.tim_token_logprob_fp32_head.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P]
-            lib.tim_token_logprob_fp32_head.restype = ctypes.c_int
-            lib.tim_token_logprob_backward.argtypes = [P, P, P, P, P, I64, I64, I64, ctypes.c_float, P, P,
-                                                       ctypes.c_int, P]
-            lib.tim_token_logprob_backward.restype = ctypes.c_int
-            lib.tim_mismatch_monitor.argtypes = [P, P, P, I64, F, P, P, P]
-            lib.tim_mismatch_monitor.restype = ctypes.c_int
-            lib.tim_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
-            lib.tim_selftest_wait_timeout.restype = ctypes.c_int
-            lib.tim_check.argtypes = [P]
-            lib.tim_check.restype = ctypes.c_int
-            lib.tim_last_error.argtypes = []
-            lib.tim_last_error.restype = ctypes.c_char_p
-            lib.tim_version.argtypes = []
-            lib.tim_version.restype = ctypes.c_int
-            _lib = lib
+            if _release is None:
+                _release = _open(_LIB_PATH, "libtim.so")
+            _lib = _release
     return _lib
+
+
+def load_debug():
+    """libtim_debug.so: the same library built with TIM_DEBUG (its kernels also
+    check indices, TMA coordinates and input contracts; see include/tim.h)."""
+    global _debug
+    with _lock:
+        if _debug is None:
+            _debug = _open(_DEBUG_LIB_PATH, "libtim_debug.so")
+    return _debug
+
+
+@contextlib.contextmanager
+def checked():
+    """Within the block every call of this module goes to libtim_debug.so
+    (one thread at a time); tim_debug_violation() then reports the first
+    violation its kernels found."""
+    global _lib
+    dbg = load_debug()
+    prev = load()
+    _lib = dbg
+    try:
+        yield dbg
+    finally:
+        _lib = prev
 
 
 # ----------------------------------------------------------------------------- raw C ABI
@@ -213,6 +257,22 @@ def tim_last_error() -> str:
 
 def tim_version() -> int:
     return load().tim_version()
+
+
+def tim_debug_build() -> int:
+    """1 when calls go to the checked build (libtim_debug.so), else 0."""
+    return load().tim_debug_build()
+
+
+def tim_debug_violation(stream=None):
+    """The first violation the checked build's kernels recorded since the last
+    call, as (check name, index, value bits), cleared on read; ("none", 0, 0)
+    if none (always so in libtim.so).  Synchronises the stream."""
+    import torch
+    out = (ctypes.c_int64 * 4)()
+    s = 0 if stream is None and not torch.cuda.is_available() else _stream_handle(stream, None)
+    _raise_if(load().tim_debug_violation(out, s))
+    return CHECKS.get(int(out[0]), str(int(out[0]))), int(out[1]), int(out[2])
 
 
 def _raise_if(rc: int):

@@ -4,7 +4,10 @@
 
 Translation units compile in parallel into ``_build/``; the shared library
 links the CUDA runtime statically and no other CUDA library, so it loads on a
-machine without a GPU (the CPU tests check its exported symbols).
+machine without a GPU (the CPU tests check its exported symbols).  The same
+sources compiled with -DTIM_DEBUG give ``libtim_debug.so`` (``_build/debug/``),
+whose kernels also check their indices, TMA coordinates and input contracts
+and record the first violation (``tim_debug_violation``).
 """
 from __future__ import annotations
 
@@ -20,6 +23,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtim.so")
+DEBUG_LIB = os.path.join(PKG, "libtim_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,38 +45,56 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> str:
+def _build_one(lib: str, objdir: str, extra: list, force: bool, ptxas_verbose: bool, quiet: bool):
+    """Starts the compiles of one library; returns a function that waits for
+    them and links (so both libraries' compiles run at once)."""
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                      + glob.glob(os.path.join(INCLUDE, "*.h")))
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     exe = nvcc()
     procs = []
     objs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(objdir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or ptxas_verbose or _stale(o, [s] + headers):
-            cmd = [exe] + ARCH + CFLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", s, "-o", o]
+            cmd = [exe] + ARCH + CFLAGS + extra + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", s, "-o", o]
             procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
-    failed = []
-    for cmd, p in procs:
-        out, _ = p.communicate()
-        text = out.decode(errors="replace")
-        if p.returncode != 0:
-            failed.append(" ".join(cmd) + "\n" + text)
-        elif text.strip() and (ptxas_verbose or not quiet):
-            sys.stderr.write(text)
-    if failed:
-        raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".%d.tmp" % os.getpid()
-        cmd = [exe] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
-        r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
-        if r.returncode != 0:
-            raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout.decode(errors="replace"))
-        os.replace(tmp, LIB)
-    return LIB
+
+    def finish() -> str:
+        failed = []
+        for cmd, p in procs:
+            out, _ = p.communicate()
+            text = out.decode(errors="replace")
+            if p.returncode != 0:
+                failed.append(" ".join(cmd) + "\n" + text)
+            elif text.strip() and (ptxas_verbose or not quiet):
+                sys.stderr.write(text)
+        if failed:
+            raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+        if force or _stale(lib, objs):
+            tmp = lib + ".%d.tmp" % os.getpid()
+            cmd = [exe] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
+            r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+            if r.returncode != 0:
+                raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout.decode(errors="replace"))
+            os.replace(tmp, lib)
+        return lib
+
+    return finish
+
+
+def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True, debug: bool = True) -> str:
+    """Builds libtim.so (and, unless debug=False, libtim_debug.so); returns
+    the path of libtim.so."""
+    release = _build_one(LIB, BUILD, [], force, ptxas_verbose, quiet)
+    checked = _build_one(DEBUG_LIB, os.path.join(BUILD, "debug"), ["-DTIM_DEBUG"], force, False, quiet) \
+        if debug else None
+    path = release()
+    if checked is not None:
+        checked()
+    return path
 
 
 def main(argv=None):

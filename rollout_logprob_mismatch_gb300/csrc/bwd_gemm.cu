@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (rank == 0)
                         mbar_arrive_expect_tx(full(stage), 2 * STAGE_TX);
                     const int k0 = kb * G_BK;
+                    // innermost coordinates are whole 16 bytes (8 bf16) and none is negative
+                    TIM_DCHECK(((m0 | n0 | k0) & 7) == 0 && m0 >= 0 && n0 >= 0, a.status, TIM_CHECK_TMA_COORD, k0,
+                               static_cast<uint64_t>(m0) << 32 | static_cast<uint32_t>(n0));
                     const uint32_t dA = sA + stage * G_A_BYTES, dB = sB + stage * G_B_BYTES;
                     if (A_MN) {
                         tma_load_2d_pair(dA, ma, f, m0, k0, pol);
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     break;
                 if (u < 0)
                     break;
+                TIM_DCHECK(u < units, a.status, TIM_CHECK_UNIT, u, units);
                 ok = u < units0 ? produce(AKmajor{}, a.p[0], &tmap_a0, &tmap_b0, u)
                                 : produce(AMNmajor{}, a.p[1], &tmap_a1, &tmap_b1, u - units0);
             }
@@ -248,6 +252,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 float v[32];
                 __syncwarp();
                 tmem_load32(tb + static_cast<uint32_t>(sc * 32), v);
+                TIM_DCHECK(row >= M || c0 + 32 <= P.ldc || c0 + 4 * ((N - c0 + 3) / 4) <= P.ldc, a.status,
+                           TIM_CHECK_STORE, row, c0);
                 if (row < M) {
                     float4 *dst = reinterpret_cast<float4 *>(crow + c0);
 #pragma unroll

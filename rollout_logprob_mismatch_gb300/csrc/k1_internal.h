@@ -90,7 +90,7 @@ cudaError_t k1_launch_main(const CUtensorMap &tmap_h, const CUtensorMap &tmap_w,
                            const K1Args &a, cudaStream_t stream, int mode = 0);
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
-                              float *out_lse, cudaStream_t stream);
+                              float *out_lse, int *status, cudaStream_t stream);
 cudaError_t k1_prepare_device();   // per-device function attributes
 // Copies `rows` rows of h (D bf16 each, 16-byte aligned) into a K1_BM-row pad, zero past them.
 cudaError_t k1_launch_pad_tail(const void *src, int64_t rows, int64_t D, void *dst, cudaStream_t stream);

@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                     break;
                 if (u < 0)
                     break;
+                TIM_DCHECK(u < a.units, a.status, TIM_CHECK_UNIT, u, a.units);
                 const Unit w = unit_of(u, a);
                 const int mt = w.mt * CL + static_cast<int>(rank);
                 // the last m-tile of a batch whose size is not a multiple of 16 rows
@@ -195,6 +196,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                             break;
                         }
                         const uint32_t fb = full_pair(stage);
+                        // innermost coordinates are whole 16 bytes (8 bf16), rows not negative
+                        TIM_DCHECK((((kh | kb) * K1_BK) & 7) == 0 && hrow >= 0 && v0 >= 0, a.status,
+                                   TIM_CHECK_TMA_COORD, hrow,
+                                   (static_cast<uint64_t>(kb) << 32) | static_cast<uint32_t>(kh * K1_BK));
                         if (PAIR) {
                             // own h tile + own half of the W tile; both CTAs' bytes complete
                             // on the even CTA's barrier, whose one arrival expects them all
@@ -313,6 +318,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             const int tgt = live ? __ldg(a.targets + row) : -1;
             const float gs = live ? __ldg(a.grad + row) * a.inv_temp : 0.f;   // g / tau
             const float l2 = live ? __ldg(a.lse_in + row) * LOG2E : 0.f;     // p = 2^(z zscale - l2)
+            TIM_DCHECK(!live || (isfinite(gs) && isfinite(l2)), a.status, TIM_CHECK_BACKWARD_INPUT, row,
+                       __float_as_uint(isfinite(gs) ? l2 : gs));
             uint16_t *dzrow = a.dz + static_cast<size_t>(live ? row : 0) * static_cast<size_t>(a.dz_ld);
             for (int j = 0; j < nt; ++j) {
                 if (!mbar_wait(tfull(acc), acc_phase, abort_flag, budget)) {
@@ -339,6 +346,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                         const float d1 = gs * ((col0 + jj + 1 == tgt ? 1.f : 0.f) - p1);
                         pk[jj / 2] = pack_bf16x2(d0, d1);
                     }
+                    TIM_DCHECK(!live || (row < a.N && col0 < a.dz_ld), a.status, TIM_CHECK_STORE, row, col0);
                     if (live) {
                         if (col0 + SUBCOLS <= a.V) {   // 64 bytes at a 64-byte offset of a 16-byte aligned row
                             uint4 *dst = reinterpret_cast<uint4 *>(dzrow + col0);
@@ -406,6 +414,17 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
                             if (col0 + jj >= a.V)
                                 v[jj] = -INFINITY;
                     }
+#ifdef TIM_DEBUG
+                    if (row < a.N) {   // a logit of a real column is finite unless h or W is not
+                        int badc = -1;
+#pragma unroll
+                        for (int jj = 0; jj < SUBCOLS; ++jj)
+                            if (col0 + jj < a.V && !isfinite(v[jj]) && badc < 0)
+                                badc = jj;
+                        TIM_DCHECK(badc < 0, a.status, TIM_CHECK_LOGIT, row,
+                                   (static_cast<uint64_t>(col0 + badc) << 32) | __float_as_uint(v[badc < 0 ? 0 : badc]));
+                    }
+#endif
                     float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
 #pragma unroll
                     for (int jj = 4; jj < SUBCOLS; jj += 4) {
@@ -450,6 +469,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
             }
             if (!ok)
                 break;
+            TIM_DCHECK(w.ch < a.num_chunks, a.status, TIM_CHECK_STORE, row, w.ch);
             if (row < a.N) {
                 a.part[static_cast<size_t>(row) * a.num_chunks + w.ch] = make_float2(run_m, run_s);
                 if (found)
@@ -484,7 +504,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1)
 __global__ void __launch_bounds__(256)
     k1_combine_kernel(const float2 *__restrict__ part, const float *__restrict__ za,
                       const int32_t *__restrict__ targets, int32_t N, int32_t V, int32_t num_chunks,
-                      float inv_temp, float *__restrict__ out_logp, float *__restrict__ out_lse)
+                      float inv_temp, float *__restrict__ out_logp, float *__restrict__ out_lse, int *status)
 {
     pdl_wait();   // the partials come from k1_main_kernel
     pdl_launch_dependents();
@@ -511,6 +531,7 @@ __global__ void __launch_bounds__(256)
         const float lse = M * inv_temp + logf(S);
         out_lse[t] = lse;
         const int a = targets[t];
+        TIM_DCHECK(a < V, status, TIM_CHECK_TARGET, t, static_cast<uint32_t>(a));   // negative: ignore label
         out_logp[t] = (a >= 0 && a < V) ? za[t] * inv_temp - lse : __int_as_float(0x7fc00000);
     }
 }
@@ -603,7 +624,7 @@ cudaError_t k1_launch_pad_tail(const void *src, int64_t rows, int64_t D, void *d
 
 cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t *targets,
                               int32_t N, int32_t V, int32_t num_chunks, float inv_temp, float *out_logp,
-                              float *out_lse, cudaStream_t stream)
+                              float *out_lse, int *status, cudaStream_t stream)
 {
     const int threads = 256;   // 8 rows per CTA, one warp each
     const int blocks = static_cast<int>((static_cast<int64_t>(N) * 32 + threads - 1) / threads);
@@ -615,7 +636,7 @@ cudaError_t k1_launch_combine(const float2 *part, const float *za, const int32_t
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k1_combine_kernel, part, za, targets, N, V, num_chunks, inv_temp, out_logp,
-                              out_lse);
+                              out_lse, status);
 }
 
 } // namespace tim

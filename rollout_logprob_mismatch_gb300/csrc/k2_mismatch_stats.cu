@@ -174,6 +174,9 @@ __device__ __forceinline__ ChunkView stage_chunk(const K2Args &a, uint8_t *stp, 
         const int64_t mend = min((t1 + 15) & ~int64_t(15), mlim);
         const int mbytes = mend > Am ? static_cast<int>(mend - Am) : 0;
         const uint32_t st = smem_u32(stp);
+        TIM_DCHECK(((reinterpret_cast<uintptr_t>(a.l_tr + A) | reinterpret_cast<uintptr_t>(a.mask + Am) |
+                     static_cast<uintptr_t>(fbytes) | static_cast<uintptr_t>(mbytes)) & 15u) == 0u,
+                   a.status, TIM_CHECK_BULK, t0, static_cast<uint64_t>(fbytes) << 32 | static_cast<uint32_t>(mbytes));
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, 2u * fbytes + mbytes);
         if (fbytes > 0) {
@@ -210,6 +213,11 @@ __device__ __forceinline__ void reduce_chunk_t(TokenAcc &acc, const K2Args &a, c
     const float *lr_s = reinterpret_cast<const float *>(stp + K2_F_BYTES) + v.off_f + lane;
     const uint8_t *mk_s = stp + 2 * K2_F_BYTES + v.off_m + lane;
     float *wout = WEIGHTS ? a.token_weight + v.t0 + lane : nullptr;
+    TIM_DCHECK(v.t0 >= 0 && v.t0 + v.n <= a.N, a.status, TIM_CHECK_STORE, v.t0, v.n);
+#ifdef TIM_DEBUG
+    for (int j = lane; j < v.n; j += 32)   // mask bytes are 0 or 1
+        TIM_DCHECK(mk_s[j - lane] <= 1, a.status, TIM_CHECK_MASK, v.t0 + j, mk_s[j - lane]);
+#endif
     if (v.n == K2_CHUNK) {   // full chunk: no bounds checks
 #pragma unroll
         for (int q = 0; q < K2_CHUNK / 64; ++q) {

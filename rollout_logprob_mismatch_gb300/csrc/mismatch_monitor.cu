@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
                 lt[u] = reinterpret_cast<const float4 *>(src)[lane + 32 * u];
                 lr[u] = reinterpret_cast<const float4 *>(src + kChunkF)[lane + 32 * u];
                 mk[u] = reinterpret_cast<const uint32_t *>(src + 2 * kChunkF)[lane + 32 * u];
+                TIM_DCHECK((mk[u] & 0xfefefefeu) == 0u, a.status, TIM_CHECK_MASK, 4 * g, mk[u]);
             } else {
                 float v[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t mm = 0u;

@@ -38,8 +38,9 @@ int cuda_fail(cudaError_t e, const char *what)
     return fail(TIM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Status word written by the kernels of this library (first error wins).
-__device__ int g_status;
+// Status block written by the kernels of this library: the status (first error
+// wins) and, in the checked build, the first violation (tim::STATUS_WORDS).
+__device__ __align__(16) int g_status[tim::STATUS_WORDS];
 
 struct DeviceState {
     bool ready = false;
@@ -306,7 +307,7 @@ int token_logprob(const void *h, const void *W, const int32_t *targets, int64_t 
     e = tim::k1_launch_main(th, tw, th_tail, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
-                                   s);
+                                   a.status, s);
     const cudaError_t ef = cudaFreeAsync(ws, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "token_logprob launch");
@@ -718,10 +719,9 @@ int tim_check(tim_stream_t stream)
     if (rc != TIM_OK)
         return rc;
     int v = 0;
-    if ((e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof v, 0, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "read status");
-    const int zero = 0;
-    if ((e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(dev->status, 0, sizeof v, s)) != cudaSuccess)
         return cuda_fail(e, "clear status");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
         return cuda_fail(e, "cudaStreamSynchronize");
@@ -730,6 +730,46 @@ int tim_check(tim_stream_t stream)
                     v == TIM_ERR_TIMEOUT ? "pipeline wait ran out of time" : "bad input data");
     g_msg[0] = 0;
     return TIM_OK;
+}
+
+int tim_debug_violation(int64_t out[4], tim_stream_t stream)
+{
+    if (!out)
+        return fail(TIM_ERR_INVALID_ARG, "out is null");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    int w[tim::STATUS_WORDS] = {};
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(w, dev->status, sizeof w, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)   // words 1..7: the record (the status itself is tim_check's)
+        e = cudaMemsetAsync(dev->status + 1, 0, sizeof w - sizeof(int), s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "read the violation record");
+    long long index = 0;
+    unsigned long long value = 0;
+    std::memcpy(&index, w + 2, sizeof index);
+    std::memcpy(&value, w + 4, sizeof value);
+    out[0] = w[1];
+    out[1] = index;
+    out[2] = static_cast<int64_t>(value);
+    out[3] = 0;
+    g_msg[0] = 0;
+    return TIM_OK;
+}
+
+int tim_debug_build(void)
+{
+#ifdef TIM_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 } // extern "C"

@@ -209,7 +209,7 @@ extern "C" int tim_token_logprob_noalloc(const void *h, const void *W, const int
     cudaError_t e = tim::k1_launch_main(th, tw, th_tail, a, s);
     if (e == cudaSuccess)
         e = tim::k1_launch_combine(a.part, a.za, targets, a.N, a.V, a.num_chunks, a.inv_temp, out_logp, out_lse,
-                                   s);
+                                   a.status, s);
     if (e != cudaSuccess)
         return cuda_err(e, "token_logprob_noalloc launch");
     return tim::record_error(TIM_OK, "");

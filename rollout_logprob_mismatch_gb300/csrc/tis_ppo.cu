@@ -129,6 +129,8 @@ __device__ __forceinline__ void ppo_step(PpoAcc &acc, const PpoArgs &a, int64_t 
         const int j = 64 * (k >> 1) + 32 * (k & 1) + lane;
         const int64_t t = t0 + j;
         const bool in = FULL || j < n;
+        TIM_DCHECK(!in || m[k] <= 1, a.status, TIM_CHECK_MASK, t, m[k]);
+        TIM_DCHECK(!in || m[k] == 0 || isfinite(A[k]), a.status, TIM_CHECK_ADVANTAGE, t, __float_as_uint(A[k]));
         float g;
         const float loss = ppo_token(acc, a, lt[k], lo[k], lr[k], A[k], m[k] != 0, g);
         if (k & 1)

@@ -226,9 +226,28 @@ def test_backward_rejects_bad_arguments(lib):
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tim, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(tim, "_DEBUG_LIB_PATH", str(tmp_path / "absent_debug.so"))
     monkeypatch.setattr(tim, "_lib", None)
+    monkeypatch.setattr(tim, "_release", None)
+    monkeypatch.setattr(tim, "_debug", None)
     with pytest.raises(tim.TimError):
         tim.load()
+    with pytest.raises(tim.TimError):
+        tim.load_debug()
+
+
+def test_checked_build_exports_the_same_api_and_says_so(lib):
+    """libtim_debug.so (TIM_DEBUG) exports every declared symbol; the two
+    builds tell themselves apart without touching a GPU."""
+    out = subprocess.run(["nm", "-D", "--defined-only", tim._DEBUG_LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+    assert tim.tim_debug_build() == 0
+    with tim.checked():
+        assert tim.tim_debug_build() == 1
+    assert tim.tim_debug_build() == 0
 
 
 def test_torch_wrappers_reject_host_tensors_and_wrong_types():
