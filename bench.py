@@ -43,22 +43,23 @@ K2_BW_TOKENS = 1 << 27
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# the kernel, keyed by a hash of the kernel's sources at capture time; reported as `traffic`
-# only while the sources are unchanged (profiles/k1_main_kernel_qwen3_8b_n8192.md,
-# profiles/k2_seq_kernel_2e25_tokens.md).
+# the kernel at the benchmark's shape, keyed by a hash of the kernel's sources at capture time;
+# reported as `traffic` (with `traffic_source`) only while the sources are unchanged, else null.
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 3044126208 read + 18182144 written
-    ("k1", "2ff80d9024b65205"): 3044126208 + 18182144,
-    # mismatch pass, 2^25 tokens: 305287168 read + 98403840 written (traffic scales with tokens)
-    ("k2", "b52af0477f7a6c75"): 305287168 + 98403840,
-    # TIS-weighted PPO surrogate, 2^25 tokens: 612941056 read + 216222720 written (scales with tokens)
-    ("ppo", "aba850bed7b51939"): 612941056 + 216222720,
-    # mismatch monitor, 2^25 tokens, its five kernels: 316319232 read + 22924544 written (scales with tokens)
-    ("monitor", "778c660759a21d96"): 316319232 + 22924544,
+    # token logprob, N = 8192, D = 4096, V = 151936: 2709789184 read + 15962880 written
+    ("k1", "9053c2f6492f274e"): 2709789184 + 15962880,
+    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1231426304 read + 495642880 written
+    ("k2", "39a716ca4dca6072"): 1223959296 + 7467008 + 495642880,
+    # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2513547264 read + 1029856768 written
+    ("ppo", "0acf304a08c63dfc"): 2510266880 + 3280384 + 1029856768,
+    # mismatch monitor, 2^27 tokens, its five kernels: 1235754944 read + 99868416 written
+    ("monitor", "5bfdd1beefab0f71"): 9553920 + 1208104960 + 24064 + 9048320 + 9023744 + 99868416,
 }
-K2_TRAFFIC_TOKENS = 1 << 25
-PPO_TRAFFIC_TOKENS = 1 << 25
-MONITOR_TRAFFIC_TOKENS = 1 << 25
+TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at this shape, " \
+                 "stored with a hash of the kernel sources it was taken on"
+K2_TRAFFIC_TOKENS = 1 << 27       # the captures were taken at the bandwidth runs' size
+PPO_TRAFFIC_TOKENS = 1 << 27
+MONITOR_TRAFFIC_TOKENS = 1 << 27
 # L2 flush before each timed launch of a single call: 1 GiB, 8x the L2; its
 # ~0.15 ms fill also lets the host enqueue the timed call before the GPU
 # reaches the start event, so host-side call overhead stays out of the time.
@@ -68,7 +69,7 @@ FLUSH_BYTES = 1 << 30
 def source_hash(kind: str) -> str:
     import hashlib
     d = os.path.join(ROOT, "rollout_logprob_mismatch_gb300", "csrc")
-    files = {"k1": ("k1_token_logprob.cu", "k1_internal.h", "tim_ptx.cuh", "tim_internal.h"),
+    files = {"k1": ("k1_token_logprob.cu", "k1_internal.h", "tim_ptx.cuh", "tim_internal.h", "unit_ring.cuh"),
              "k2": ("k2_mismatch_stats.cu", "k2_internal.h", "tim_ptx.cuh", "tim_internal.h"),
              "ppo": ("tis_ppo.cu", "ppo_internal.h", "tim_ptx.cuh", "tim_internal.h"),
              "monitor": ("mismatch_monitor.cu", "monitor_internal.h", "tim_ptx.cuh", "tim_internal.h")}[kind]
@@ -241,10 +242,14 @@ def time_oracle(cfg, h, W, a, off, mask, budget_s: float, seed: int = 0):
     l_ro = wl.draw_rollout(cfg, l_tr, seed=seed)
     t0 = time.perf_counter()
     oracle.mismatch_stats(l_tr, l_ro, mask, off, C=cfg.C)
+    t_k2_1 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.mismatch_stats(l_tr, l_ro, mask, off, C=cfg.C, nthreads=threads)
     t_k2 = time.perf_counter() - t0
     sec_per_token = t_k1 / R + t_k2 / cfg.N
     desc = ("token logprob on %d of %d rows (%d threads, %.1f s) + mismatch stats on all %d tokens "
-            "(1 thread, %.3f s), extrapolated to tokens/s" % (R, cfg.N, threads, t_k1, cfg.N, t_k2))
+            "(%d threads %.4f s; 1 thread %.4f s), extrapolated to tokens/s"
+            % (R, cfg.N, threads, t_k1, cfg.N, threads, t_k2, t_k2_1))
     return 1.0 / sec_per_token, desc, threads, t_k1 + t_k2
 
 
@@ -500,6 +505,7 @@ def run_gb300(args):
                      "frac": achieved / peak, "peak_source": "%s bf16 burst" % peaks["source"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "traffic": measured_traffic("k1") if (N, D, V) == (8192, 4096, 151936) else None,
+                     "traffic_source": TRAFFIC_SOURCE if measured_traffic("k1") is not None else None,
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "algorithmic_bytes_per_launch": 2 * N * D + 2 * V * D + 12 * N,
                      "algorithmic_flops_per_launch": flops,
@@ -557,58 +563,112 @@ def k1_head_only(tim, dev, stream, name, reps, warmup):
             "tflops": 2.0 * N * V * D / t / 1e12}
 
 
+def draw_head_on_device(cfg, g, dev):
+    """h, W and targets with the laws of the workload config, drawn on the
+    device: h ~ N(0, h_std^2) with an iid fraction h_outlier_frac of entries
+    scaled by h_outlier_scale, W ~ N(0, w_std^2), both rounded to bf16;
+    targets uniform, or for "top5mix" 70% a uniform pick among the row's five
+    largest logits (from a plain torch matmul: input shaping only) and 30%
+    uniform."""
+    import torch
+    N, D, V = cfg.N, cfg.D, cfg.V
+    h = torch.randn((N, D), generator=g, device=dev) * cfg.h_std
+    if cfg.h_outlier_frac > 0.0:
+        hit = torch.rand((N, D), generator=g, device=dev) < cfg.h_outlier_frac
+        h = torch.where(hit, h * cfg.h_outlier_scale, h)
+        del hit
+    h = h.to(torch.bfloat16)
+    W = (torch.randn((V, D), generator=g, device=dev) * cfg.w_std).to(torch.bfloat16)
+    a = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
+    if cfg.target_mode == "top5mix":
+        top5 = torch.empty((N, 5), dtype=torch.int64, device=dev)
+        for s in range(0, N, 2048):
+            top5[s:s + 2048] = torch.topk((h[s:s + 2048] @ W.T).float(), 5, dim=-1).indices
+        pick = torch.rand(N, generator=g, device=dev) < 0.7
+        col = torch.randint(0, 5, (N, 1), generator=g, device=dev)
+        a = torch.where(pick, top5.gather(1, col)[:, 0].to(torch.int32), a)
+        del top5
+    return h, W, a
+
+
+def draw_rollout_on_device(cfg, lp, g):
+    """Rollout logprobs with the config's laws: trainer + N(0, rollout_std^2),
+    plus an iid fraction outlier_frac of tokens shifted by +-outlier_shift."""
+    import torch
+    ro = lp + cfg.rollout_std * torch.randn(lp.shape[0], generator=g, device=lp.device)
+    if cfg.outlier_frac > 0.0:
+        hit = torch.rand(lp.shape[0], generator=g, device=lp.device) < cfg.outlier_frac
+        sign = torch.where(torch.rand(lp.shape[0], generator=g, device=lp.device) < 0.5, -1.0, 1.0)
+        ro = torch.where(hit, ro + sign * cfg.outlier_shift, ro)
+    return ro
+
+
 def head_shapes_measure(tim, dev, stream, peaks, names=("llama3_8b", "dsv3"), reps=5, warmup=2):
     """The step (token logprob + mismatch statistics) on the other head shapes
     of the workloads: the Llama-3-8B-shaped head (N = 32768 in lognormal
-    sequences, 30% masked) and the DeepSeek-V3-shaped one (N = 16384, D = 7168,
-    32 x 512).  h ~ N(0, h_std^2) and W ~ N(0, w_std^2) in bf16 and uniform
-    targets drawn on the device (the values do not change the work), segments
-    and masks from the workload generators, rollout = trainer + N(0,
-    rollout_std^2); L2 flushed before each step."""
+    sequences, 30% masked, rollout outliers of +-1.0 on 0.5% of tokens) and
+    the DeepSeek-V3-shaped one (N = 16384, D = 7168, 32 x 512, 1% of h entries
+    scaled x20, 70% of targets among each row's top-5 logits), all inputs with
+    the configs' laws, drawn on the device; L2 flushed before each step.  The
+    token logprob is also timed on plain inputs (h, W Gaussian, uniform
+    targets) of the same shapes, to show what the values change."""
     import torch
     g = torch.Generator(device=dev)
     g.manual_seed(12)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     out = []
-    for name in names:
-        cfg = wl.CONFIGS[name]
-        N, D, V = cfg.N, cfg.D, cfg.V
-        h = (torch.randn((N, D), generator=g, device=dev) * cfg.h_std).to(torch.bfloat16)
-        W = (torch.randn((V, D), generator=g, device=dev) * cfg.w_std).to(torch.bfloat16)
-        a = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
-        off = wl.draw_segments(cfg, seed=0)
-        S = len(off) - 1
-        offd = torch.from_numpy(off).to(dev)
-        maskd = torch.from_numpy(wl.draw_mask(cfg, off, seed=0)).to(dev)
-        lp = torch.empty(N, dtype=torch.float32, device=dev)
-        lse = torch.empty(N, dtype=torch.float32, device=dev)
-        tim.token_logprob(h, W, a, lp, lse)
-        ro = lp + cfg.rollout_std * torch.randn(N, generator=g, device=dev)
-        k2out = {"seq_stats": torch.empty((S, 12), dtype=torch.float32, device=dev),
-                 "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
-                 "batch": torch.empty(20, dtype=torch.float64, device=dev), "token_weight": None}
+
+    def time_step(h, W, a, ro, maskd, offd, lp, lse, k2out, with_k2=True):
         for _ in range(warmup):
             tim.token_logprob(h, W, a, lp, lse)
-            tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
+            if with_k2:
+                tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
         for i in range(reps):
             flush.fill_(i)
             ev[i][0].record(stream)
             tim.token_logprob(h, W, a, lp, lse)
             ev[i][1].record(stream)
-            tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
+            if with_k2:
+                tim.mismatch_stats(lp, ro, maskd, offd, C=cfg.C, out=k2out)
             ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
-        t1 = float(np.mean([e[0].elapsed_time(e[1]) * 1e-3 for e in ev]))
-        t2 = float(np.mean([e[1].elapsed_time(e[2]) * 1e-3 for e in ev]))
+        return (float(np.mean([e[0].elapsed_time(e[1]) * 1e-3 for e in ev])),
+                float(np.mean([e[1].elapsed_time(e[2]) * 1e-3 for e in ev])))
+
+    for name in names:
+        cfg = wl.CONFIGS[name]
+        N, D, V = cfg.N, cfg.D, cfg.V
+        off = wl.draw_segments(cfg, seed=0)
+        S = len(off) - 1
+        offd = torch.from_numpy(off).to(dev)
+        maskd = torch.from_numpy(wl.draw_mask(cfg, off, seed=0)).to(dev)
+        lp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        k2out = {"seq_stats": torch.empty((S, 12), dtype=torch.float32, device=dev),
+                 "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
+                 "batch": torch.empty(20, dtype=torch.float64, device=dev), "token_weight": None}
+        h, W, a = draw_head_on_device(cfg, g, dev)
+        tim.token_logprob(h, W, a, lp, lse)
+        ro = draw_rollout_on_device(cfg, lp, g)
+        t1, t2 = time_step(h, W, a, ro, maskd, offd, lp, lse, k2out)
+        del h, W, a
+        # the same shapes on plain inputs: what the input values change
+        hp = (torch.randn((N, D), generator=g, device=dev) * cfg.h_std).to(torch.bfloat16)
+        Wp = (torch.randn((V, D), generator=g, device=dev) * cfg.w_std).to(torch.bfloat16)
+        ap = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
+        t1p, _ = time_step(hp, Wp, ap, ro, maskd, offd, lp, lse, k2out, with_k2=False)
+        del hp, Wp, ap
         flops = 2.0 * N * V * D
         out.append({"workload": "%s_head+mismatch" % name, "N": N, "D": D, "V": V, "num_seqs": S,
+                    "inputs": "the config's laws (outliers, top-5 targets where the config has them)",
                     "step_ms": (t1 + t2) * 1e3, "tokens_per_s": N / (t1 + t2),
                     "token_logprob_ms": t1 * 1e3, "tflops": flops / t1 / 1e12,
                     "frac": flops / t1 / 1e12 / peaks["bf16_tflops"], "bound": "tensor",
                     "frac_of_sustained": flops / t1 / 1e12 / peaks["bf16_tflops_sustained"],
-                    "mismatch_pass_us": t2 * 1e6})
-        del h, W, a, lp, lse, ro
+                    "mismatch_pass_us": t2 * 1e6,
+                    "token_logprob_ms_plain_inputs": t1p * 1e3})
+        del lp, lse, ro
     return out
 
 
@@ -682,7 +742,8 @@ def mismatch_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, wa
     return {"tokens": Nt, "num_seqs": S, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo,
             "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
             "frac_of_8000": gbs / 8000.0, "bound": "hbm",
-            "traffic": None if tr is None else tr * Nt / K2_TRAFFIC_TOKENS}
+            "traffic": None if tr is None or Nt != K2_TRAFFIC_TOKENS else tr,
+            "traffic_source": None if tr is None or Nt != K2_TRAFFIC_TOKENS else TRAFFIC_SOURCE}
 
 
 def backward_measure(tim, dev, stream, peaks, hd, Wd, ad, reps=5, warmup=2):
@@ -801,7 +862,8 @@ def monitor_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, war
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bound": "hbm",
             "passes_over_inputs": 1, "sample_tokens": min(Nt, 1 << 20),
             "tokens_per_s": Nt / t,
-            "traffic": None if tr is None else tr * Nt / MONITOR_TRAFFIC_TOKENS}
+            "traffic": None if tr is None or Nt != MONITOR_TRAFFIC_TOKENS else tr,
+            "traffic_source": None if tr is None or Nt != MONITOR_TRAFFIC_TOKENS else TRAFFIC_SOURCE}
 
 
 def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=3):
@@ -851,7 +913,8 @@ def ppo_bandwidth(tim, dev, stream, peaks, tokens=K2_BW_TOKENS, reps=10, warmup=
     return {"tokens": Nt, "num_seqs": S, "avg_launch_us": t * 1e6, "algorithmic_bytes": algo,
             "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
             "bound": "hbm", "tokens_per_s": Nt / t,
-            "traffic": None if tr is None else tr * Nt / PPO_TRAFFIC_TOKENS}
+            "traffic": None if tr is None or Nt != PPO_TRAFFIC_TOKENS else tr,
+            "traffic_source": None if tr is None or Nt != PPO_TRAFFIC_TOKENS else TRAFFIC_SOURCE}
 
 
 def main(argv=None):

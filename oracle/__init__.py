@@ -81,6 +81,8 @@ def _load():
                                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32,
                                                   P, P, P, P]
             lib.oracle_mismatch_stats.restype = ctypes.c_int
+            lib.oracle_mismatch_stats_threads.argtypes = lib.oracle_mismatch_stats.argtypes + [ctypes.c_int]
+            lib.oracle_mismatch_stats_threads.restype = ctypes.c_int
             lib.oracle_tis_ppo.argtypes = [P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
                                            ctypes.c_double, ctypes.c_double, P, P, P, P]
             lib.oracle_tis_ppo.restype = ctypes.c_int
@@ -180,9 +182,10 @@ def token_logprob_backward(h_bf16, W_bf16, targets, grad, temperature: float = 1
 
 
 def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
-                   tau_seq: float = float("nan"), seq_estimator: int = 3):
+                   tau_seq: float = float("nan"), seq_estimator: int = 3, nthreads: int = 1):
     """dict with token_weight [N], seq_stats [S, 12], seq_flags [S], batch [20]
-    (all float64 except seq_flags int32)."""
+    (all float64 except seq_flags int32).  nthreads > 1 sums the sequences on
+    that many threads; the arithmetic, and so every bit, is the same."""
     lib = _load()
     lt = np.ascontiguousarray(logp_train, dtype=np.float32)
     lr = np.ascontiguousarray(logp_rollout, dtype=np.float32)
@@ -195,9 +198,9 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
     seq = np.empty((S, len(SEQ_FIELDS)), dtype=np.float64)
     flags = np.empty(S, dtype=np.int32)
     batch = np.empty(len(BATCH_FIELDS), dtype=np.float64)
-    rc = lib.oracle_mismatch_stats(_ptr(lt), _ptr(lr), _ptr(m), _ptr(off), S, N, float(C),
-                                   float(tau_seq), int(seq_estimator), _ptr(w), _ptr(seq),
-                                   _ptr(flags), _ptr(batch))
+    rc = lib.oracle_mismatch_stats_threads(_ptr(lt), _ptr(lr), _ptr(m), _ptr(off), S, N, float(C),
+                                           float(tau_seq), int(seq_estimator), _ptr(w), _ptr(seq),
+                                           _ptr(flags), _ptr(batch), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_mismatch_stats rejected its arguments")
     return {"token_weight": w, "seq_stats": seq, "seq_flags": flags, "batch": batch}

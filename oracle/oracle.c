@@ -245,14 +245,70 @@ static token_terms oracle_token(float l_tr, float l_ro, uint8_t mask, double C, 
     return q;
 }
 
+/* Sums of one sequence over its tokens, in token order. */
+typedef struct {
+    double n_mask, n_used, n_nan, n_clip;
+    double sd, sad, sk1, sk2, sk3, sw, srel, mx;
+} seq_sums;
+
+static seq_sums oracle_sequence(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                                int64_t t0, int64_t t1, double C, double logC, double *token_weight)
+{
+    seq_sums z;
+    memset(&z, 0, sizeof z);
+    for (int64_t t = t0; t < t1; ++t) {
+        token_terms q = oracle_token(logp_train[t], logp_rollout[t], mask[t], C, logC);
+        z.n_mask += mask[t] != 0;
+        z.n_nan += q.nan;
+        if (!q.used)
+            continue;
+        z.n_used += 1;
+        z.n_clip += q.clip;
+        z.sd += q.delta;
+        z.sad += fabs(q.delta);
+        z.sk1 += q.k1;
+        z.sk2 += q.k2;
+        z.sk3 += q.k3;
+        z.sw += q.w;
+        z.srel += q.rel;
+        if (fabs(q.delta) > z.mx)
+            z.mx = fabs(q.delta);
+        if (token_weight)
+            token_weight[t] = q.w;
+    }
+    return z;
+}
+
+/* Sequences [s0, s1) of a batch, on one thread: their sums into `sums`. */
+typedef struct {
+    const float *lt, *lr;
+    const uint8_t *m;
+    const int32_t *off;
+    int32_t s0, s1;
+    double C, logC;
+    double *w;
+    seq_sums *sums;
+} seq_job;
+
+static void *seq_worker(void *p)
+{
+    seq_job *j = (seq_job *)p;
+    for (int32_t s = j->s0; s < j->s1; ++s)
+        j->sums[s] = oracle_sequence(j->lt, j->lr, j->m, j->off[s], j->off[s + 1], j->C, j->logC, j->w);
+    return NULL;
+}
+
 /* logp_train, logp_rollout fp32 [N]; mask uint8 [N]; seq_offsets int32 [S+1].
  * Outputs: token_weight double [N] (may be NULL), seq_stats double [S][SQ_FIELDS],
  * seq_flags int32 [S], batch double [BT_FIELDS].
- * Returns 0, or -1 on bad arguments / bad offsets. */
-int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
-                          const int32_t *seq_offsets, int32_t S, int64_t N, double C,
-                          double tau_seq, int32_t seq_estimator, double *token_weight,
-                          double *seq_stats, int32_t *seq_flags, double *batch)
+ * Each sequence is summed alone in token order (the sequences are spread over
+ * `nthreads` threads, which changes no arithmetic); then one thread adds the
+ * sequences' sums into the batch totals in sequence order.
+ * Returns 0, or -1 on bad arguments / bad offsets, -2 when out of memory. */
+int oracle_mismatch_stats_threads(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                                  const int32_t *seq_offsets, int32_t S, int64_t N, double C,
+                                  double tau_seq, int32_t seq_estimator, double *token_weight,
+                                  double *seq_stats, int32_t *seq_flags, double *batch, int nthreads)
 {
     if (S < 0 || N < 0 || !(C > 0.0) || !seq_offsets || !batch)
         return -1;
@@ -275,47 +331,60 @@ int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, co
         for (int64_t t = 0; t < N; ++t)
             token_weight[t] = 0.0;
 
+    seq_sums *sums = (seq_sums *)malloc(sizeof(seq_sums) * (size_t)(S > 0 ? S : 1));
+    if (!sums)
+        return -2;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > S)
+        nthreads = S > 0 ? S : 1;
+    seq_job *jobs = (seq_job *)calloc((size_t)nthreads, sizeof(seq_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int *started = (int *)calloc((size_t)nthreads, sizeof(int));
+    if (!jobs || !tids || !started) {
+        free(sums);
+        free(jobs);
+        free(tids);
+        free(started);
+        return -2;
+    }
+    for (int i = 0; i < nthreads; ++i)
+        jobs[i] = (seq_job){logp_train, logp_rollout, mask, seq_offsets, (int32_t)((int64_t)S * i / nthreads),
+                            (int32_t)((int64_t)S * (i + 1) / nthreads), C, logC, token_weight, sums};
+    for (int i = 1; i < nthreads; ++i)
+        started[i] = pthread_create(&tids[i], NULL, seq_worker, &jobs[i]) == 0;
+    seq_worker(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i) {
+        if (started[i])
+            pthread_join(tids[i], NULL);
+        else
+            seq_worker(&jobs[i]);   /* no thread could be made: run it here */
+    }
+    free(jobs);
+    free(tids);
+    free(started);
+
     /* batch totals, accumulated sequence by sequence in index order */
     double b_mask = 0, b_used = 0, b_nan = 0, b_clip = 0;
     double b_sd = 0, b_sad = 0, b_sk1 = 0, b_sk2 = 0, b_sk3 = 0, b_sw = 0, b_srel = 0, b_max = 0;
     double b_mk1 = 0, b_mk2 = 0, b_mk3 = 0, b_nonempty = 0, b_rej = 0;
 
     for (int32_t s = 0; s < S; ++s) {
-        double n_mask = 0, n_used = 0, n_nan = 0, n_clip = 0;
-        double sd = 0, sad = 0, sk1 = 0, sk2 = 0, sk3 = 0, sw = 0, srel = 0, mx = 0;
-        for (int64_t t = seq_offsets[s]; t < seq_offsets[s + 1]; ++t) {
-            token_terms q = oracle_token(logp_train[t], logp_rollout[t], mask[t], C, logC);
-            n_mask += mask[t] != 0;
-            n_nan += q.nan;
-            if (!q.used)
-                continue;
-            n_used += 1;
-            n_clip += q.clip;
-            sd += q.delta;
-            sad += fabs(q.delta);
-            sk1 += q.k1;
-            sk2 += q.k2;
-            sk3 += q.k3;
-            sw += q.w;
-            srel += q.rel;
-            if (fabs(q.delta) > mx)
-                mx = fabs(q.delta);
-            if (token_weight)
-                token_weight[t] = q.w;
-        }
+        const seq_sums *z = &sums[s];
+        const double n_used = z->n_used;
         double *o = seq_stats + (size_t)s * SQ_FIELDS;
-        o[SQ_N_MASK] = n_mask;
+        o[SQ_N_MASK] = z->n_mask;
         o[SQ_N_USED] = n_used;
-        o[SQ_N_NAN] = n_nan;
-        o[SQ_N_CLIP] = n_clip;
-        o[SQ_MAX_ABS_DELTA] = mx;
-        o[SQ_MEAN_DELTA] = mean_or_zero(sd, n_used);
-        o[SQ_MEAN_ABS_DELTA] = mean_or_zero(sad, n_used);
-        o[SQ_MEAN_K1] = mean_or_zero(sk1, n_used);
-        o[SQ_MEAN_K2] = mean_or_zero(sk2, n_used);
-        o[SQ_MEAN_K3] = mean_or_zero(sk3, n_used);
-        o[SQ_MEAN_W] = mean_or_zero(sw, n_used);
-        o[SQ_MEAN_REL] = mean_or_zero(srel, n_used);
+        o[SQ_N_NAN] = z->n_nan;
+        o[SQ_N_CLIP] = z->n_clip;
+        o[SQ_MAX_ABS_DELTA] = z->mx;
+        o[SQ_MEAN_DELTA] = mean_or_zero(z->sd, n_used);
+        o[SQ_MEAN_ABS_DELTA] = mean_or_zero(z->sad, n_used);
+        o[SQ_MEAN_K1] = mean_or_zero(z->sk1, n_used);
+        o[SQ_MEAN_K2] = mean_or_zero(z->sk2, n_used);
+        o[SQ_MEAN_K3] = mean_or_zero(z->sk3, n_used);
+        o[SQ_MEAN_W] = mean_or_zero(z->sw, n_used);
+        o[SQ_MEAN_REL] = mean_or_zero(z->srel, n_used);
         int flag = 0;
         if (n_used > 0) {
             double stat = seq_estimator == 3 ? o[SQ_MEAN_K3] : fabs(o[SQ_MEAN_K1]);
@@ -328,20 +397,21 @@ int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, co
         }
         seq_flags[s] = flag;
 
-        b_mask += n_mask;
+        b_mask += z->n_mask;
         b_used += n_used;
-        b_nan += n_nan;
-        b_clip += n_clip;
-        b_sd += sd;
-        b_sad += sad;
-        b_sk1 += sk1;
-        b_sk2 += sk2;
-        b_sk3 += sk3;
-        b_sw += sw;
-        b_srel += srel;
-        if (mx > b_max)
-            b_max = mx;
+        b_nan += z->n_nan;
+        b_clip += z->n_clip;
+        b_sd += z->sd;
+        b_sad += z->sad;
+        b_sk1 += z->sk1;
+        b_sk2 += z->sk2;
+        b_sk3 += z->sk3;
+        b_sw += z->sw;
+        b_srel += z->srel;
+        if (z->mx > b_max)
+            b_max = z->mx;
     }
+    free(sums);
 
     batch[BT_N_MASK] = b_mask;
     batch[BT_N_USED] = b_used;
@@ -364,6 +434,15 @@ int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, co
     batch[BT_N_SEQS_NONEMPTY] = b_nonempty;
     batch[BT_N_REJECTED] = b_rej;
     return 0;
+}
+
+int oracle_mismatch_stats(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+                          const int32_t *seq_offsets, int32_t S, int64_t N, double C,
+                          double tau_seq, int32_t seq_estimator, double *token_weight,
+                          double *seq_stats, int32_t *seq_flags, double *batch)
+{
+    return oracle_mismatch_stats_threads(logp_train, logp_rollout, mask, seq_offsets, S, N, C, tau_seq,
+                                         seq_estimator, token_weight, seq_stats, seq_flags, batch, 1);
 }
 
 /* ------------------------------------------------------------------ TIS-weighted PPO surrogate

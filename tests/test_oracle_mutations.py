@@ -65,8 +65,8 @@ MUTATIONS = {
                       "loss = ppo_clipped ? w * rclip * A : w * r * A;"),
     "ppo_clip_on_ties": ("(A > 0.0 && (double)dt32 > log_hi) || (A < 0.0 && (double)dt32 < log_lo)",
                          "(A > 0.0 && (double)dt32 >= log_hi) || (A < 0.0 && (double)dt32 <= log_lo)"),
-    "max_of_signed_delta": ("            if (fabs(q.delta) > mx)\n                mx = fabs(q.delta);",
-                            "            if (q.delta > mx)\n                mx = q.delta;"),
+    "max_of_signed_delta": ("        if (fabs(q.delta) > z.mx)\n            z.mx = fabs(q.delta);",
+                            "        if (q.delta > z.mx)\n            z.mx = q.delta;"),
     "nan_counted_when_masked_out": ("q.nan = in && !fin;", "q.nan = !fin;"),
     "quantile_interpolation_sign": ("return lo + (h - fl) * (hi - lo);", "return lo + (h - fl) * (hi + lo);"),
     "extreme_on_signed_delta": ("const int ext = used && fabs((double)d32) > tau_tok;",

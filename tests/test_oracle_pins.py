@@ -736,3 +736,23 @@ def test_backward_invariants():
     a2[0] = -100
     o2 = oracle.token_logprob_backward(h, W, a2, g)
     np.testing.assert_allclose(o2["dh"][0], o["dh"][0] - float(g[0]) * Wf[a[0]], rtol=0, atol=1e-12)
+
+
+def test_mismatch_stats_on_several_threads_gives_the_same_bits():
+    """The oracle sums each sequence alone in token order and folds the
+    sequences in index order, so spreading the sequences over threads changes
+    no bit of any output (empty sequences, masks and non-finite tokens
+    included)."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(0, 300, size=700)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(off[-1])
+    l_tr = wl.draw_train_logprobs(N, 77)
+    l_ro = (l_tr + rng.normal(0, 0.3, N)).astype(np.float32)
+    l_ro[::101] = np.inf
+    mask = (rng.random(N) < 0.7).astype(np.uint8)
+    one = oracle.mismatch_stats(l_tr, l_ro, mask, off, C=1.5)
+    for nt in (2, 3, 8, 1000):
+        many = oracle.mismatch_stats(l_tr, l_ro, mask, off, C=1.5, nthreads=nt)
+        for k in one:
+            assert np.array_equal(one[k].view(np.uint8), many[k].view(np.uint8)), (nt, k)
