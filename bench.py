@@ -49,7 +49,7 @@ MEASURED_TRAFFIC = {
     # token logprob, N = 8192, D = 4096, V = 151936: 2709789184 read + 15962880 written
     ("k1", "9053c2f6492f274e"): 2709789184 + 15962880,
     # mismatch pass, 2^27 tokens (sequence kernel + fold): 1231426304 read + 495642880 written
-    ("k2", "39a716ca4dca6072"): 1223959296 + 7467008 + 495642880,
+    ("k2", "407cfe470c6416f9"): 1223959296 + 7467008 + 495642880,
     # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2513547264 read + 1029856768 written
     ("ppo", "0acf304a08c63dfc"): 2510266880 + 3280384 + 1029856768,
     # mismatch monitor, 2^27 tokens, its five kernels: 1235754944 read + 99868416 written

@@ -22,7 +22,7 @@ constexpr int K2_SMEM_BYTES = K2_BAR_BYTES + K2_WARPS * K2_STAGES * K2_STAGE_BYT
 constexpr int64_t K2_LONG = 8192;                  // longer sequences are reduced by a whole CTA
 constexpr int K2_FOLD_THREADS = 256;               // fold CTA
 constexpr int K2_FOLD_SEQS = 4 * K2_FOLD_THREADS;  // sequences per fold CTA
-constexpr int K2_REC_WORDS = 16;                   // 4-byte words per sequence record (structure of arrays)
+constexpr int K2_REC_WORDS = 16;                   // 4-byte words per sequence record (64 bytes a sequence)
 constexpr int K2_PART_WORDS = 40;                  // 4-byte words per fold partial
 static_assert(K2_STAGE_BYTES % 16 == 0 && K2_BAR_BYTES % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
 
