@@ -622,28 +622,51 @@ __device__ __forceinline__ void write_plain(const K2Args &a, int s, bool bad, in
     }
 }
 
-// Claims the next sequence index for this warp (lane 0 takes it from the
-// call's counter; the value is not waited for until it is broadcast).
+// Claims the warp's next ticket (lane 0 takes it from the call's counter;
+// the value is not waited for until it is broadcast).
 __device__ __forceinline__ int claim_raw(const K2Args &a, int lane)
 {
     return lane == 0 ? atomicAdd(a.claim, 1) : 0;
 }
 
-// The next sequence the warp reduces itself.  The warp keeps two claims in
-// flight (lane 0: raw, then the later raw2); each step takes the older one and
-// claims a new one, so no claimed index is ever dropped while a smaller one is
-// held, and a claim's latency hides behind the sequences before it.  Records
-// of empty or bad sequences met on the way are written at once, long ones are
-// left for the CTA phase.  Returns S when there is none (every claim still in
-// flight is then past S too).
-__device__ __forceinline__ int next_short(const K2Args &a, int &raw, int &raw2, int lane)
+// The sequences of ticket t: the first k2_block_tickets(S) tickets hand out
+// K2_CLAIM_BLOCK consecutive sequences each, the later ones one each.  The
+// blocks cut the counter's traffic (one claim per sequence from every warp
+// queued on the counter's word, and how long varied from one device to
+// another); single sequences at the end keep the warps' finish times close.
+__device__ __forceinline__ int k2_block_tickets(int S) { return (S - S / 8) / K2_CLAIM_BLOCK; }
+
+__device__ __forceinline__ void ticket_range(int t, int S, int &lo, int &hi)
+{
+    const int t0 = k2_block_tickets(S);
+    if (t < t0) {
+        lo = t * K2_CLAIM_BLOCK;
+        hi = lo + K2_CLAIM_BLOCK;
+    } else {
+        lo = t0 * K2_CLAIM_BLOCK + (t - t0);   // t < S + (claims in flight): no overflow
+        hi = lo + 1;
+    }
+    hi = min(hi, S);
+}
+
+// The next sequence the warp reduces itself, from the range [cur, end) of its
+// current ticket; when that is used up, the ticket claimed one range earlier
+// (lane 0: pend) gives the next range and a new ticket is claimed, so a
+// claim's latency hides behind the sequences before it.  Records of empty or
+// bad sequences met on the way are written at once, long ones are left for
+// the CTA phase.  Returns S when there is none (every later ticket is past S
+// too).
+__device__ __forceinline__ int next_short(const K2Args &a, int &cur, int &end, int &pend, int lane)
 {
     while (true) {
-        const int s = __shfl_sync(0xffffffffu, raw, 0);
-        raw = raw2;
-        raw2 = claim_raw(a, lane);
-        if (s >= a.S)
-            return a.S;
+        if (cur >= end) {
+            const int t = __shfl_sync(0xffffffffu, pend, 0);
+            pend = claim_raw(a, lane);
+            ticket_range(t, a.S, cur, end);
+            if (cur >= a.S)
+                return a.S;
+        }
+        const int s = cur++;
         const int64_t b = a.off[s], e = a.off[s + 1];
         if (!offsets_ok(a, s, b, e)) {
             write_plain(a, s, true, lane);
@@ -695,13 +718,12 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     bool ok = true;
 
     // ---- phase 1: sequences of at most K2_LONG tokens, one warp each.  Warps
-    // claim sequences in index order from the call's counter, two ahead of the
-    // one they reduce, so the work stays balanced however the lengths vary (a
-    // record's bits depend on its own tokens only, not on the warp that reduces
-    // it).
-    int raw = claim_raw(a, lane);
-    int raw2 = claim_raw(a, lane);
-    int s = next_short(a, raw, raw2, lane);
+    // claim sequences in index order from the call's counter, one ticket ahead
+    // of the range they reduce, so the work stays balanced however the lengths
+    // vary (a record's bits depend on its own tokens only, not on the warp
+    // that reduces it).
+    int pend = claim_raw(a, lane), t_cur = 0, t_end = 0;   // lane 0: the next ticket; the current range
+    int s = next_short(a, t_cur, t_end, pend, lane);
     ChunkView cur;
     if (s < a.S) {
         const int64_t b = a.off[s], e = a.off[s + 1];
@@ -723,7 +745,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
                 nv = stage_chunk(a, nst, nbar, t0, min(e, t0 + K2_CHUNK), lane, pol);
                 pending |= 1u << (stage ^ 1);
             } else {
-                nxt = next_short(a, raw, raw2, lane);
+                nxt = next_short(a, t_cur, t_end, pend, lane);
                 if (nxt < a.S) {
                     const int64_t nb = a.off[nxt], ne = a.off[nxt + 1];
                     nv = stage_chunk(a, nst, nbar, nb, min(ne, nb + K2_CHUNK), lane, pol);
