@@ -21,15 +21,19 @@
 //                       n_extreme, rejection flags and, per quantile, the used
 //                       tokens below lo and the keys inside [lo, hi]
 //                       (typically a few percent), kept in a list with the
-//                       histogram of their first radix digit; its last CTA
-//                       takes the ranks from n_used, checks that each
-//                       quantile's order statistics fall inside its list (else,
-//                       or if a list overflowed, the selection runs over all
-//                       tokens) and selects the lists' first digit;
-//   mon_pass_kernel<1..3> radix selection in three digit passes (11, 11, 10
-//                       bits) over the lists, on key - lo, or over all tokens
-//                       (pass 1 only then); the last CTA of each selects the
-//                       digit, that of pass 3 writes the record.
+//                       histogram of their offsets' high digit (top 16 bits of
+//                       key - lo); its last CTA takes the ranks from n_used,
+//                       checks that each quantile's order statistics fall
+//                       inside its list (else, or if a list overflowed, the
+//                       selection runs over all tokens) and finds each
+//                       target's high digit;
+//   mon_select_kernel   one pass over the lists keeps, per target, the low
+//                       digits of the keys in its high bin (as values, or as a
+//                       histogram when there are many); the last CTA selects
+//                       the low digit and writes the record.  Over all tokens
+//                       instead it runs a radix selection in three digit
+//                       passes (11, 11, 10 bits) with grid barriers between
+//                       them (a cooperative launch).
 // The bounds only decide how much work the selection does; the result is the
 // same either way.
 #include <algorithm>
@@ -193,43 +197,6 @@ __device__ __forceinline__ int find_in_segment(const uint32_t (&v)[SEG], uint32_
 }
 
 // ---------------------------------------------------------------- sample and bounds
-// One kind of bound (KIND 0: delta's bins, quantiles 1..3; KIND 1: |delta|'s,
-// quantile 0), thread i holding bins [i SEG, (i + 1) SEG) in v: a CTA scan of
-// the segment totals, then the thread whose segment holds a target rank finds
-// its bin.
-template <int KIND, int SEG>
-__device__ __forceinline__ void bounds_kind(const uint32_t (&v)[SEG], long long m, const long long *rlo,
-                                            const long long *rhi, int *bin_s, uint32_t *wsum)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t c = segment_total(v);
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += x;
-    }
-    __syncthreads();   // earlier readers of wsum are done
-    if (lane == 31)
-        wsum[warp] = incl;
-    __syncthreads();
-    uint32_t before_warp = 0;
-    for (int w = 0; w < warp; ++w)
-        before_warp += wsum[w];
-    const long long excl = static_cast<long long>(before_warp + incl - c);
-    const int q_first = KIND == 0 ? 1 : 0, q_end = KIND == 0 ? MON_QUANTILES : 1;
-    for (int q = q_first; q < q_end; ++q)
-        for (int e = 0; e < 2; ++e) {
-            const long long R = e == 0 ? rlo[q] : rhi[q];
-            if (m > 0 && R > 0 && R < m - 1 && excl <= R && R < excl + static_cast<long long>(c)) {
-                uint32_t before;
-                bin_s[2 * q + e] = tid * SEG + find_in_segment(v, static_cast<uint32_t>(excl),
-                                                               static_cast<uint32_t>(R), before);
-            }
-        }
-}
-
 // For quantile q at level L with m sampled used tokens: sample ranks
 // floor(L (m - 1)) - w and ceil(L (m - 1)) + w, w = six standard deviations of
 // a sample quantile's rank (sqrt(m L (1 - L))) + 2; lo = the lowest key of the
@@ -238,18 +205,21 @@ __device__ __forceinline__ void bounds_kind(const uint32_t (&v)[SEG], long long 
 // above the sample's last).  The ranks are a heuristic (a rank off by one only
 // moves a bound; the check after the full pass keeps the result exact), so
 // they are taken in fp32.  Run by one CTA of MON_THREADS threads on the
-// global sample histogram of delta's key; both kinds' bins are loaded first.
-__device__ void compute_bounds(const MonArgs &a)
+// global sample histogram of delta's key: thread i loads bins [64 i, 64 i +
+// 64) (all loads in flight at once), the CTA writes the inclusive prefix sums
+// P of the histogram to shared memory `P` (SBD words), and one thread per
+// bound searches them: delta's bin holding rank R is the first x with
+// P[x] > R; |delta|'s bin c covers delta's bins SBA - 1 - c .. SBA + c, so the
+// |delta| bin holding R is the first c with P[SBA + c] - P[SBA - 2 - c] > R.
+__device__ void compute_bounds(const MonArgs &a, uint32_t *P)
 {
     __shared__ uint32_t wsum[MON_THREADS / 32];
-    __shared__ int bin_s[2 * MON_QUANTILES];
     __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     MonState *st = a.st;
-    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins, 32 |delta| bins per thread");
-    uint32_t vd[64], va[32];
-    load_segment<64>(a.shist + tid * 64, vd);
-    load_abs_segment<32>(a.shist, SBA, tid * 32, va);
+    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins per thread");
+    uint32_t v[64];
+    load_segment<64>(a.shist + tid * 64, v);
     const long long m = static_cast<long long>(__ldcg(&st->sample_used));
     if (tid < MON_QUANTILES) {
         const float L = static_cast<float>(level(tid));
@@ -259,17 +229,52 @@ __device__ void compute_bounds(const MonArgs &a)
         rlo_s[tid] = static_cast<long long>(floorf(j)) - w;
         rhi_s[tid] = static_cast<long long>(ceilf(j)) + w;
     }
-    if (tid < 2 * MON_QUANTILES)
-        bin_s[tid] = -1;
+    uint32_t run = 0;
+#pragma unroll
+    for (int x = 0; x < 64; ++x) {
+        run += v[x];
+        v[x] = run;
+    }
+    uint32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
     __syncthreads();
-    bounds_kind<0>(vd, m, rlo_s, rhi_s, bin_s, wsum);
-    bounds_kind<1>(va, m, rlo_s, rhi_s, bin_s, wsum);
+    uint32_t before = incl - run;
+    for (int w = 0; w < warp; ++w)
+        before += wsum[w];
+#pragma unroll
+    for (int x = 0; x < 64; x += 4)
+        *reinterpret_cast<uint4 *>(P + tid * 64 + x) =
+            make_uint4(before + v[x], before + v[x + 1], before + v[x + 2], before + v[x + 3]);
     __syncthreads();
-    if (tid < MON_QUANTILES) {
-        const int q = tid;
-        const int bl = bin_s[2 * q], bh = bin_s[2 * q + 1];
-        st->lo[q] = bl < 0 ? 0u : static_cast<uint32_t>(bl) << SAMPLE_SHIFT;
-        st->hi[q] = bh < 0 ? 0xffffffffu : (static_cast<uint32_t>(bh) << SAMPLE_SHIFT) | ((1u << SAMPLE_SHIFT) - 1u);
+    if (tid < 2 * MON_QUANTILES) {
+        const int q = tid >> 1, e = tid & 1;
+        const long long R = e == 0 ? rlo_s[q] : rhi_s[q];
+        int bin = -1;
+        if (m > 0 && R > 0 && R < m - 1) {   // then some bin holds R: P's last word is m
+            const uint32_t r = static_cast<uint32_t>(R);
+            int lo = 0, hi = q == 0 ? SBA - 1 : SBD - 1;   // the answer is in [lo, hi]
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const uint32_t c = q == 0 ? P[SBA + mid] - (mid <= SBA - 2 ? P[SBA - 2 - mid] : 0u) : P[mid];
+                if (c > r)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            bin = lo;
+        }
+        if (e == 0)
+            st->lo[q] = bin < 0 ? 0u : static_cast<uint32_t>(bin) << SAMPLE_SHIFT;
+        else
+            st->hi[q] = bin < 0 ? 0xffffffffu
+                                : (static_cast<uint32_t>(bin) << SAMPLE_SHIFT) | ((1u << SAMPLE_SHIFT) - 1u);
     }
 }
 
@@ -320,14 +325,15 @@ __device__ __forceinline__ bool last_cta(unsigned *ticket)
     return true;
 }
 
-// Run r: MON_SAMPLE_RUN tokens from s = r N / runs rounded down to a multiple
-// of 4 (runs back to back when they cover the batch); CTA c takes runs c, c +
+// Run r: MON_SAMPLE_RUN tokens from s = r (N - MON_SAMPLE_RUN) / (runs - 1)
+// rounded down to a multiple of 4 (runs back to back when they cover the
+// batch); CTA c takes runs c, c +
 // gridDim, ..., kRunsAtOnce of them loaded before any is used, into a
 // shared-memory histogram of delta's key (|delta|'s follows from it), thread
 // i the tokens s + 4i .. s + 4i + 3 (one 16-byte load per array), and adds
 // the non-zero bins to the global histogram.  The CTA that finishes last
 // computes the bounds.
-constexpr int kRunsAtOnce = 4;
+constexpr int kRunsAtOnce = 8;   // with one CTA per SM, all 1024 runs in one round of loads
 static_assert(MON_SAMPLE_RUN == 4 * MON_THREADS, "a run is one 4-token group per thread");
 __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
 {
@@ -336,6 +342,14 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
     zero_histogram<SBD>(sh);
     __syncthreads();
     pdl_wait();
+    {   // the fine histograms of the full pass and the selection pass start at zero
+        constexpr size_t n4 = (MON_HIF_WORDS + MON_LOF_WORDS) / 4;
+        static_assert((MON_HIF_WORDS + MON_LOF_WORDS) % 4 == 0, "whole 16-byte stores");
+        uint4 *z = reinterpret_cast<uint4 *>(a.hif);   // hif and lof are adjacent
+        for (size_t i = static_cast<size_t>(blockIdx.x) * MON_THREADS + tid; i < n4;
+             i += static_cast<size_t>(gridDim.x) * MON_THREADS)
+            z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     const int64_t N = a.N;
     const int64_t cover = static_cast<int64_t>(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN;
     const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
@@ -352,7 +366,11 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
                 v[k][i] = w[k][i] = 0.f;
             if (r >= runs)
                 continue;
-            const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN : (r * N / runs) & ~int64_t(3);
+            // spread over the batch: r (N - run) / (runs - 1), a spacing that is
+            // no power of two (runs at 2^k-token strides all met the same DRAM
+            // channels)
+            const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN
+                                          : (r * (N - MON_SAMPLE_RUN) / (runs - 1)) & ~int64_t(3);
             const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
             const int64_t t = s0 + 4 * tid;
             if (t + 4 <= s1) {
@@ -384,13 +402,13 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
     if (lane == 0 && used)
         atomicAdd(&a.st->sample_used, static_cast<unsigned long long>(used));
     __syncthreads();
-    // The full pass may launch now: earlier, its CTAs (82 KB of shared memory
-    // each) took the room of this kernel's second CTA per SM, which then
-    // started ~10 us late.
+    // The full pass's CTAs may launch now (they wait for the bounds).  (Earlier,
+    // when this kernel ran two CTAs per SM, they took the room of its second
+    // CTA, which then started ~10 us late.)
     pdl_launch_dependents();
     flush_histogram<SBD>(sh, a.shist);
     if (last_cta(&a.st->ticket[0]))
-        compute_bounds(a);
+        compute_bounds(a, sh);   // the shared histogram is spent: its room takes the prefix sums
 }
 
 // ---------------------------------------------------------------- the full pass
@@ -450,31 +468,44 @@ __device__ __forceinline__ int span_bits_of(uint32_t lo, uint32_t hi)
     return span == 0u ? 0 : 32 - __clz(static_cast<int>(span));
 }
 
+// The shift that leaves the high digit (top MON_HI_BITS bits) of an offset
+// key - lo of a list whose offsets have `bits` significant bits.
+__device__ __forceinline__ int high_shift(int bits) { return max(bits - MON_HI_BITS, 0); }
+
 // Collected keys of quantile q, one per lane with `has` set (a full warp
 // calls): each into the list at `at` (when there is room) and into the list's
-// pass-1 histogram of its offset's top digit, lanes with the same digit added
-// by one atomic (the keys near a quantile share few digits).
-__device__ __forceinline__ void collect(const MonArgs &a, int q, bool has, unsigned long long at, uint32_t key,
-                                        uint32_t lo, int bits)
+// histograms of its offset's high digit (fine: all 16 bits, in global memory;
+// coarse: the top 8, in the CTA's shared-memory copy `hic_s`, added to the
+// global one at the end: its few bins take most keys), lanes with the same
+// digit added by one atomic (the keys near a quantile share few digits).
+__device__ __forceinline__ void collect(const MonArgs &a, uint32_t *hic_s, int q, bool has, unsigned long long at,
+                                        uint32_t key, uint32_t lo, int shift)
 {
-    const uint32_t dg = has ? digit_of<1>(key - lo, bits) : 0xffffffffu;
-    const unsigned same = __match_any_sync(0xffffffffu, dg);
+    uint32_t hd = has ? (key - lo) >> shift : 0xffffffffu;   // < 2^16: lo <= key <= hi
+    TIM_DCHECK(!has || hd < static_cast<uint32_t>(MON_FINE), a.status, TIM_CHECK_UNIT, q, key);
+    has = has && hd < static_cast<uint32_t>(MON_FINE);
+    hd = has ? hd : 0xffffffffu;
+    const unsigned same = __match_any_sync(0xffffffffu, hd);
+    const unsigned same_c = __match_any_sync(0xffffffffu, has ? hd >> 8 : 0xffffffffu);
     if (has) {
-        if (at < a.cap)
-            a.cand[static_cast<size_t>(q) * a.cap + at] = key;
-        if ((threadIdx.x & 31) == __ffs(same) - 1)
-            atomicAdd(a.hist1 + q * MON_BINS1 + dg, static_cast<uint32_t>(__popc(same)));
+        const int lane = threadIdx.x & 31;
+        if (at < a.cap)   // kept in L2 (evict-last) for the selection pass that reads it next
+            st_global_hint(a.cand + static_cast<size_t>(q) * a.cap + at, key, l2_policy_evict_last());
+        if (lane == __ffs(same) - 1)
+            atomicAdd(a.hif + q * MON_FINE + hd, static_cast<uint32_t>(__popc(same)));
+        if (lane == __ffs(same_c) - 1)
+            atomicAdd(hic_s + q * MON_COARSE + (hd >> 8), static_cast<uint32_t>(__popc(same_c)));
     }
 }
 
-__device__ __forceinline__ void flush_stage(const MonArgs &a, const uint32_t *buf, int q, int n, int lane,
-                                            uint32_t lo, int bits)
+__device__ __forceinline__ void flush_stage(const MonArgs &a, uint32_t *hic_s, const uint32_t *buf, int q, int n,
+                                            int lane, uint32_t lo, int shift)
 {
     unsigned long long base = 0;
     if (lane == 0)
-        base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(n));
+        base = atomicAdd(a.hot + q * MON_HOT_STRIDE, static_cast<unsigned long long>(n));
     base = __shfl_sync(0xffffffffu, base, 0);
-    collect(a, q, lane < n, base + lane, lane < n ? buf[lane] : 0u, lo, bits);
+    collect(a, hic_s, q, lane < n, base + lane, lane < n ? buf[lane] : 0u, lo, shift);
 }
 
 // Float thresholds equal to the key bounds on canonical finite deltas:
@@ -571,15 +602,15 @@ __device__ __forceinline__ float pick(const float (&k)[kScanTokens], int s)
 }
 
 __device__ void check_ranks(const MonArgs &a);
-template <int PASS>
-__device__ void select_digit(const MonArgs &a);
+__device__ void select_high(const MonArgs &a);
 
 __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(const MonArgs a)
 {
     extern __shared__ __align__(16) uint8_t scan_smem[];   // rings [warp][kRing], staging, barriers
     __shared__ float flo_s[MON_QUANTILES], fhi_s[MON_QUANTILES];
     __shared__ uint32_t one_s, lo_s[MON_QUANTILES];
-    __shared__ int bits_s[MON_QUANTILES];
+    __shared__ int shift_s[MON_QUANTILES];
+    __shared__ __align__(16) uint32_t hic_s[MON_QUANTILES * MON_COARSE];   // the lists' coarse high digits
     __shared__ int abort_s;
     volatile int *abort_flag = &abort_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -596,23 +627,10 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
         one_s = 1u;
         abort_s = 0;
     }
-    pdl_wait();
-    pdl_launch_dependents();
-    if (tid < MON_QUANTILES) {
-        const uint32_t lo = a.st->lo[tid], hi = a.st->hi[tid];
-        flo_s[tid] = tid == 0 ? abs_lo_threshold(lo) : signed_lo_threshold(lo);
-        fhi_s[tid] = tid == 0 ? abs_hi_threshold(hi) : signed_hi_threshold(hi);
-        lo_s[tid] = lo;
-        bits_s[tid] = span_bits_of(lo, hi);
-    }
-    __syncthreads();
-    float flo[MON_QUANTILES], fhi[MON_QUANTILES];
-#pragma unroll
-    for (int q = 0; q < MON_QUANTILES; ++q) {
-        flo[q] = flo_s[q];
-        fhi[q] = fhi_s[q];
-    }
-    const uint32_t one = one_s;
+    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += MON_THREADS)
+        hic_s[i] = 0u;
+    float flo[MON_QUANTILES], fhi[MON_QUANTILES];   // set from the sample's bounds (below)
+    uint32_t one = 0u;
     const int64_t N = a.N;
     const int64_t G = (N + 3) >> 2;
     const int64_t full = N >> 2;
@@ -624,17 +642,25 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
     int staged[MON_QUANTILES] = {0, 0, 0, 0};   // uniform over the warp
     int at_or_above[MON_QUANTILES] = {0, 0, 0, 0};
 
-    // The warp's k-th chunk: groups [c_k kChunk, (c_k + 1) kChunk), c_k = w + k warps.
-    // (Drawing the last fifth of the chunks from a shared counter evened out
-    // the CTAs' finish times but not the pass's: it is bound by HBM.)
+    // Chunk c holds groups [c kChunk, (c + 1) kChunk); chunks below `whole_n`
+    // are whole (bulk-copied), chunk `whole_n` is the ragged last one when N is
+    // not a multiple of the chunk.  The warp takes chunks w, w + warps, ...
+    // (Handing the second half out in blocks from a counter evened the warps'
+    // finish times but made the pass slower: the claims' atomics on one word
+    // queue up, and how much varied from one device to another.)
     const int64_t w = static_cast<int64_t>(blockIdx.x) * kScanWarps + warp;
-    auto whole = [&](int64_t k) { return (w + k * warps + 1) * kChunk <= full; };
-    auto issue = [&](int64_t k) {   // lane 0: stage chunk k into ring slot k % kRing
-        if (lane != 0 || !whole(k))
+    const int64_t whole_n = full / kChunk;
+    const int64_t chunks = whole_n + (whole_n * kChunk < G ? 1 : 0);
+    auto chunk_of = [&](int64_t k) -> int64_t {   // the warp's k-th chunk, -1 past the last (uniform)
+        const int64_t c = w + k * warps;
+        return c < chunks ? c : -1;
+    };
+    auto issue = [&](int slot, int64_t c) {   // lane 0: stage whole chunk c into ring slot `slot`
+        if (lane != 0 || c < 0 || c >= whole_n)
             return;
-        const int64_t g0 = (w + k * warps) * kChunk;
-        const int slot = static_cast<int>(k % kRing);
+        const int64_t g0 = c * kChunk;
         const uint32_t dst = smem_u32(ring + slot * kChunkBytes), bar = bar0 + 8u * slot;
+        TIM_DCHECK(g0 + kChunk <= full, a.status, TIM_CHECK_UNIT, c, static_cast<uint64_t>(chunks));
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, kChunkBytes);
         bulk_load(dst, a.l_tr + 4 * g0, kChunkF, bar, pol);
@@ -718,11 +744,11 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
             if (staged[q] + total > kStage) {   // rare: straight to the list, one reservation
                 unsigned long long base = 0;
                 if (lane == 0)
-                    base = atomicAdd(&a.st->count[q], static_cast<unsigned long long>(total));
+                    base = atomicAdd(a.hot + q * MON_HOT_STRIDE, static_cast<unsigned long long>(total));
                 base = __shfl_sync(0xffffffffu, base, 0) + static_cast<unsigned long long>(excl);
                 for (uint32_t b = inbits[q]; __any_sync(0xffffffffu, b != 0u); b &= b - 1u, ++base) {
                     const float v = b != 0u ? pick(dv, __ffs(b) - 1) : 0.f;
-                    collect(a, q, b != 0u, base, q == 0 ? key_abs(v) : key_signed(v), lo_s[q], bits_s[q]);
+                    collect(a, hic_s, q, b != 0u, base, q == 0 ? key_abs(v) : key_signed(v), lo_s[q], shift_s[q]);
                 }
                 continue;
             }
@@ -735,7 +761,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
             staged[q] += total;
             __syncwarp();
             while (staged[q] >= 32) {   // uniform over the warp
-                flush_stage(a, buf, q, 32, lane, lo_s[q], bits_s[q]);
+                flush_stage(a, hic_s, buf, q, 32, lane, lo_s[q], shift_s[q]);
                 __syncwarp();
                 for (int i = lane; i + 32 < staged[q]; i += 32) {   // move the rest down
                     const uint32_t v = buf[i + 32];
@@ -749,36 +775,76 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
     };
 
     // Whole chunks through the ring; the ragged last one from global memory.
-    for (int k = 0; k < kRing; ++k)
-        issue(k);
+    // cs0, cs1: the chunks of ring slots 0 and 1; parity bit i: the phase of
+    // slot i's next completion (a slot's barrier completes only for a staged
+    // chunk).
+    static_assert(kRing == 2, "two ring slots");
+    int64_t cs0 = chunk_of(0);
+    issue(0, cs0);
+    int64_t cs1 = chunk_of(1);
+    issue(1, cs1);
+    // The inputs do not depend on the sample kernel (it waited for every
+    // earlier write before it let this kernel start): the first two chunks are
+    // in flight while the sample's last CTA sets the bounds.
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid < MON_QUANTILES) {
+        const uint32_t lo = a.st->lo[tid], hi = a.st->hi[tid];
+        flo_s[tid] = tid == 0 ? abs_lo_threshold(lo) : signed_lo_threshold(lo);
+        fhi_s[tid] = tid == 0 ? abs_hi_threshold(hi) : signed_hi_threshold(hi);
+        lo_s[tid] = lo;
+        shift_s[tid] = high_shift(span_bits_of(lo, hi));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        flo[q] = flo_s[q];
+        fhi[q] = fhi_s[q];
+    }
+    one = one_s;
+    uint32_t parity = 0;
     bool ok = true;
-    int64_t k = 0;
-    for (; whole(k); ++k) {
-        const int slot = static_cast<int>(k % kRing);
-        if (!mbar_wait_sleep(bar0 + 8u * slot, static_cast<uint32_t>((k / kRing) & 1), abort_flag,
-                             a.wait_budget_ns)) {
-            ok = false;
+    for (int64_t k = 0;; ++k) {
+        const int slot = static_cast<int>(k & 1);
+        const int64_t c = slot ? cs1 : cs0;   // uniform over the warp
+        if (c < 0)
             break;
+        if (c < whole_n) {
+            if (!mbar_wait_sleep(bar0 + 8u * slot, (parity >> slot) & 1u, abort_flag, a.wait_budget_ns)) {
+                ok = false;
+                break;
+            }
+            parity ^= 1u << slot;
+            step(c * kChunk, ring + slot * kChunkBytes, std::false_type{});
+        } else {
+            step(c * kChunk, nullptr, std::true_type{});
         }
-        step((w + k * warps) * kChunk, ring + slot * kChunkBytes, std::false_type{});
         __syncwarp();   // every lane has read the slot
-        issue(k + kRing);
+        const int64_t cn = chunk_of(k + kRing);
+        if (slot)
+            cs1 = cn;
+        else
+            cs0 = cn;
+        issue(slot, cn);
     }
     if (!ok) {   // copies may still be landing: let them, then report
-        for (int64_t j = k; j < k + kRing; ++j)
-            if (whole(j))
-                drain_wait(bar0 + 8u * static_cast<uint32_t>(j % kRing), static_cast<uint32_t>((j / kRing) & 1));
+        if (cs0 >= 0 && cs0 < whole_n)
+            drain_wait(bar0, parity & 1u);
+        if (cs1 >= 0 && cs1 < whole_n)
+            drain_wait(bar0 + 8u, (parity >> 1) & 1u);
         if (lane == 0)
             atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
-    } else if ((w + k * warps) * kChunk < G) {
-        step((w + k * warps) * kChunk, nullptr, std::true_type{});
     }
 
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q)
         if (staged[q] > 0)
-            flush_stage(a, stage_all + (warp * MON_QUANTILES + q) * kStage, q, staged[q], lane, lo_s[q], bits_s[q]);
+            flush_stage(a, hic_s, stage_all + (warp * MON_QUANTILES + q) * kStage, q, staged[q], lane, lo_s[q],
+                        shift_s[q]);
+    // the CTA's counts (warp sums, then thread 0 adds the warps': one atomic
+    // per counter and CTA)
+    __shared__ int red_s[kScanWarps][2 + MON_QUANTILES];
     const int wu = __reduce_add_sync(0xffffffffu, n_used);
     const int we = __reduce_add_sync(0xffffffffu, n_ext);
     int wb[MON_QUANTILES];
@@ -786,20 +852,31 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
     for (int q = 0; q < MON_QUANTILES; ++q)
         wb[q] = __reduce_add_sync(0xffffffffu, n_used - at_or_above[q]);
     if (lane == 0) {
-        atomicAdd(&a.st->n_used, static_cast<unsigned long long>(wu));
-        atomicAdd(&a.st->n_extreme, static_cast<unsigned long long>(we));
+        red_s[warp][0] = wu;
+        red_s[warp][1] = we;
 #pragma unroll
         for (int q = 0; q < MON_QUANTILES; ++q)
-            if (wb[q])
-                atomicAdd(&a.st->below[q], static_cast<unsigned long long>(wb[q]));
+            red_s[warp][2 + q] = wb[q];
     }
-    // The last CTA: ranks and mode, then (collected lists) the first digit.
+    __syncthreads();
+    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += MON_THREADS)   // the CTA's coarse counts
+        if (hic_s[i] != 0u)
+            atomicAdd(a.hic + i, hic_s[i]);
+    if (tid < 2 + MON_QUANTILES) {
+        unsigned long long t = 0;
+        for (int w2 = 0; w2 < kScanWarps; ++w2)
+            t += static_cast<unsigned long long>(red_s[w2][tid]);
+        unsigned long long *dst = tid == 0 ? &a.st->n_used : tid == 1 ? &a.st->n_extreme : &a.st->below[tid - 2];
+        if (t)
+            atomicAdd(dst, t);
+    }
+    // The last CTA: ranks and mode, then (collected lists) the targets' high digits.
     if (last_cta(&a.st->ticket[1])) {
         if (tid == 0)
             check_ranks(a);
         __syncthreads();
         if (!a.st->empty && !a.st->fallback)   // uniform over the CTA
-            select_digit<1>(a);
+            select_high(a);
     }
 }
 
@@ -822,7 +899,7 @@ __device__ void check_ranks(const MonArgs &a)
 #pragma unroll
     for (int q = 0; q < MON_QUANTILES; ++q) {   // all loads first: they are independent
         below[q] = static_cast<long long>(__ldcg(&st->below[q]));
-        cnt[q] = static_cast<long long>(__ldcg(&st->count[q]));
+        cnt[q] = static_cast<long long>(__ldcg(a.hot + q * MON_HOT_STRIDE));
     }
     for (int q = 0; q < MON_QUANTILES; ++q) {
         const double h = static_cast<double>(n - 1) * level(q);
@@ -841,74 +918,36 @@ __device__ void check_ranks(const MonArgs &a)
     }
 }
 
-// ---------------------------------------------------------------- radix passes
-template <int PASS>
-constexpr int pass_bins() { return PASS == 3 ? MON_BINS3 : MON_BINS2; }
 
-// Shared-memory histogram words of a pass: pass 1 runs only over all tokens
-// (delta's key), passes 2 and 3 keep one histogram per target.
-template <int PASS>
-constexpr int pass_smem_words()
+// ---------------------------------------------------------------- bin search in a warp
+// The first bin x of a segment with cum + v[0] + ... + v[x] > r, or -1;
+// `before` gets the count below bin x and `in` its count.
+template <int SEG>
+__device__ __forceinline__ int find_bin_in_segment(const uint32_t (&v)[SEG], uint32_t cum, uint32_t r,
+                                                   uint32_t &before, uint32_t &in)
 {
-    return PASS == 1 ? MON_BINS1 : MON_TARGETS * pass_bins<PASS>();
-}
-
-// v[q] for a quantile index q in 0..3, by selects (v stays in registers).
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&v)[MON_QUANTILES], int q)
-{
-    const uint32_t lo = (q & 1) ? v[1] : v[0], hi = (q & 1) ? v[3] : v[2];
-    return (q & 2) ? hi : lo;
-}
-
-// Does v carry the digits that `prefix` fixed in the passes before PASS?
-template <int PASS>
-__device__ __forceinline__ bool in_prefix(uint32_t v, uint32_t prefix, int b)
-{
-    if (PASS == 1)
-        return true;
-    const int s = digit_shift(PASS - 1, b);
-    return (static_cast<uint64_t>(v) >> s) == (static_cast<uint64_t>(prefix) >> s);
-}
-
-// Per target (warp j of the calling CTA): the bin of pass PASS that holds the
-// target's rank, and the rank left inside it.  Pass 1 reads the lists'
-// histograms (built by the full pass) or the all-token one.  Lane l owns bins
-// [l seg, (l + 1) seg), read from L2 in chunks of 16: their total, a warp
-// scan, then the lane whose segment holds the rank reads its chunks again to
-// find the bin.  Needs a CTA of MON_TARGETS warps.
-template <int PASS>
-__device__ void select_digit(const MonArgs &a)
-{
-    constexpr int NB = pass_bins<PASS>();
-    constexpr int CH = 16;
-    const int tid = threadIdx.x, lane = tid & 31, j = tid >> 5, q = j >> 1;
-    MonState *st = a.st;
-    if (st->empty)
-        return;
-    const bool all_tokens = st->fallback != 0;
-    const int b = all_tokens ? 32 : st->span_bits[q];
-    // The all-token pass 1 counted delta's key only (2048 bins); |delta|'s
-    // 1024 bins follow from it.
-    const bool abs1 = PASS == 1 && all_tokens && j < 2;
-    const uint32_t *hg = PASS == 1 ? a.hist1 + (all_tokens ? MON_QUANTILES : q) * MON_BINS1
-                       : PASS == 2 ? a.hist2 + j * NB
-                                   : a.hist3 + j * NB;
-    const int seg = (abs1 ? 1024 : NB) / 32;
-    auto chunk = [&](int k, uint32_t (&t)[CH]) {
-        const int c0 = lane * seg + CH * k;
-        if (abs1)
-            load_abs_segment<CH>(hg, 1024, c0, t);
-        else
-            load_segment<CH>(hg + c0, t);
-    };
-    const uint32_t r = static_cast<uint32_t>(st->rank[j]);   // < N < 2^31
-    uint32_t c = 0;
-#pragma unroll 1
-    for (int k = 0; k < seg / CH; ++k) {
-        uint32_t t[CH];
-        chunk(k, t);
-        c += segment_total(t);
+    int bin = -1;
+#pragma unroll
+    for (int x = 0; x < SEG; ++x) {
+        if (bin < 0 && cum + v[x] > r) {
+            bin = x;
+            before = cum;
+            in = v[x];
+        }
+        cum += v[x];
     }
+    return bin;
+}
+
+// The bin of a histogram that holds rank r, lane l holding bins [l SEG,
+// (l + 1) SEG) in v (the whole warp calls): segment totals, a warp scan, then
+// the lane whose segment holds the rank finds the bin.  -1 when the counts
+// end at or before r; `before` gets the count below the bin, `in` its count.
+template <int SEG>
+__device__ __forceinline__ int warp_find_bin(const uint32_t (&v)[SEG], uint32_t r, uint32_t &before, uint32_t &in)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t c = segment_total(v);
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -917,37 +956,58 @@ __device__ void select_digit(const MonArgs &a)
             incl += x;
     }
     const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
+    if (hit == 0u)
+        return -1;
+    const int L = __ffs(hit) - 1;
     int bin = -1;
-    uint32_t before = 0;
-    if (hit != 0u) {
-        const int L = __ffs(hit) - 1;
-        if (lane == L) {
-            uint32_t cum = incl - c;
-#pragma unroll 1
-            for (int k = 0; k < seg / CH && bin < 0; ++k) {
-                uint32_t t[CH];
-                chunk(k, t);
-                const int x = find_in_segment(t, cum, r, before);
-                if (x >= 0)
-                    bin = lane * seg + CH * k + x;
-                cum += segment_total(t);
-            }
-        }
-        bin = __shfl_sync(0xffffffffu, bin, L);
-        before = __shfl_sync(0xffffffffu, before, L);
+    uint32_t b = 0, n = 0;
+    if (lane == L)
+        bin = lane * SEG + find_bin_in_segment(v, incl - c, r, b, n);
+    before = __shfl_sync(0xffffffffu, b, L);
+    in = __shfl_sync(0xffffffffu, n, L);
+    return __shfl_sync(0xffffffffu, bin, L);
+}
+
+// Records that the counts disagree with the ranks (cannot happen with
+// consistent counts): no record but NaNs, and TIM_ERR_BAD_INPUT.
+__device__ __forceinline__ void counts_inconsistent(const MonArgs &a)
+{
+    atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
+    a.st->empty = 1;
+}
+
+// ---------------------------------------------------------------- the high digit
+// The full pass's last CTA, warp j per target (lists mode): the high digit of
+// the target's offset from the list's coarse then fine histogram (one round
+// trip each) and the rank left inside that bin.
+__device__ void select_high(const MonArgs &a)
+{
+    const int lane = threadIdx.x & 31, j = threadIdx.x >> 5, q = j >> 1;
+    MonState *st = a.st;
+    const uint32_t r = static_cast<uint32_t>(st->rank[j]);   // < count[q] <= cap < 2^31
+    uint32_t v[8], before = 0, in = 0;
+    load_segment<8>(a.hic + q * MON_COARSE + lane * 8, v);
+    const int cb = warp_find_bin<8>(v, r, before, in);
+    if (cb < 0) {
+        if (lane == 0)
+            counts_inconsistent(a);
+        return;
     }
+    const uint32_t r1 = r - before;
+    load_segment<8>(a.hif + q * MON_FINE + cb * MON_COARSE + lane * 8, v);
+    const int fb = warp_find_bin<8>(v, r1, before, in);
     if (lane == 0) {
-        if (bin < 0) {   // cannot happen when the counts are consistent
-            atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_BAD_INPUT));
-            st->empty = 1;
+        if (fb < 0) {
+            counts_inconsistent(a);
         } else {
-            st->rank[j] = static_cast<long long>(r - before);
-            st->prefix[j] |= static_cast<uint32_t>(bin) << digit_shift(PASS, b);
+            st->prefix[j] = static_cast<uint32_t>(cb * MON_COARSE + fb);
+            st->rank[j] = static_cast<long long>(r1 - before);
         }
     }
 }
 
-// Thread 0: the batch record from the selected keys.
+// ---------------------------------------------------------------- the record
+// Thread 0: the batch record from the selected keys (st->prefix).
 __device__ void write_record(const MonArgs &a)
 {
     MonState *st = a.st;
@@ -956,14 +1016,14 @@ __device__ void write_record(const MonArgs &a)
     o[TIM_MON_N_USED] = static_cast<double>(n);
     o[TIM_MON_N_EXTREME] = static_cast<double>(ne);
     o[TIM_MON_FRAC_EXTREME] = n > 0 ? static_cast<double>(ne) / static_cast<double>(n) : 0.0;
-    if (st->empty) {
+    if (__ldcg(&st->empty)) {
         const double nan = __longlong_as_double(0x7ff8000000000000ll);
         o[TIM_MON_P95_ABS_DELTA] = o[TIM_MON_RATIO_Q01] = o[TIM_MON_RATIO_Q50] = o[TIM_MON_RATIO_Q99] = nan;
         return;
     }
     uint32_t key[MON_TARGETS];
     for (int t = 0; t < MON_TARGETS; ++t)
-        key[t] = st->fallback ? st->prefix[t] : st->lo[t >> 1] + st->prefix[t];
+        key[t] = __ldcg(&st->prefix[t]);
     const double a0 = __uint_as_float(key[0]), a1 = __uint_as_float(key[1]);
     o[TIM_MON_P95_ABS_DELTA] = a0 + st->frac[0] * (a1 - a0);
     const int field[3] = {TIM_MON_RATIO_Q01, TIM_MON_RATIO_Q50, TIM_MON_RATIO_Q99};
@@ -974,132 +1034,291 @@ __device__ void write_record(const MonArgs &a)
     }
 }
 
-// Radix pass PASS over the collected lists (passes 2 and 3; pass 1 of the
-// lists came with the full pass) or over all tokens (the fallback, all three
-// passes), into shared-memory histograms added to the global ones; the CTA
-// that finishes last then selects the digit, and after pass 3 writes the
-// record.
+// ---------------------------------------------------------------- selection over all tokens
+// (When a bound missed or a list overflowed.)  Radix selection on the full
+// 32-bit keys in three digit passes of 11, 11 and 10 bits.
 template <int PASS>
-__global__ void __launch_bounds__(MON_THREADS, MON_CTAS_PER_SM) mon_pass_kernel(const MonArgs a)
+constexpr int pass_bins() { return PASS == 3 ? MON_BINS3 : MON_BINS2; }
+
+// Shared-memory histogram words of a pass: pass 1 counts delta's key only
+// (|delta|'s bins follow from it), passes 2 and 3 keep one histogram per target.
+template <int PASS>
+constexpr int pass_smem_words() { return PASS == 1 ? MON_BINS1 : MON_TARGETS * pass_bins<PASS>(); }
+
+// Does key k carry the digits that `prefix` fixed in the passes before PASS?
+template <int PASS>
+__device__ __forceinline__ bool in_prefix(uint32_t k, uint32_t prefix)
+{
+    if (PASS == 1)
+        return true;
+    const int s = digit_shift(PASS - 1, 32);
+    return (k >> s) == (prefix >> s);
+}
+
+// One pass over all tokens into a shared-memory histogram (`sh`), added to
+// the global one of the pass.
+template <int PASS>
+__device__ void all_token_pass(const MonArgs &a, uint32_t *sh)
 {
     constexpr int NB = pass_bins<PASS>();
-    extern __shared__ __align__(16) uint32_t mon_sh[];
-    __shared__ uint32_t pref_s[MON_TARGETS], lo_s[MON_QUANTILES];
-    __shared__ int bits_s[MON_QUANTILES];
-    __shared__ int mode_s;   // 0 nothing to do, 1 the collected lists, 2 all tokens
-    __shared__ unsigned long long cnt_s[MON_QUANTILES], start_s[MON_QUANTILES];
-    const int tid = threadIdx.x;
-    pdl_wait();
-    pdl_launch_dependents();
+    zero_histogram<pass_smem_words<PASS>()>(sh);
+    uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
+#pragma unroll
+    for (int j = 0; j < MON_TARGETS; ++j)
+        pr[j] = __ldcg(&a.st->prefix[j]);   // set by CTA 0 before the last grid barrier
+    __syncthreads();
+    for_token_groups<MON_UNROLL>(a, [&](int64_t, const float (&d)[4], const bool (&m)[4], const bool (&valid)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool used = valid[i] && usable(m[i], d[i]);
+            const uint32_t kd = key_signed(d[i]);
+            if (PASS == 1) {
+                if (used)
+                    atomicAdd(sh + (kd >> 21), 1u);
+            } else {
+                const uint32_t ka = key_abs(d[i]);
+#pragma unroll
+                for (int j = 0; j < MON_TARGETS; ++j) {
+                    const uint32_t k = j < 2 ? ka : kd;
+                    if (used && in_prefix<PASS>(k, pr[j]))
+                        atomicAdd(sh + j * NB + digit_of<PASS>(k, 32), 1u);
+                }
+            }
+        }
+    });
+    __syncthreads();
+    flush_histogram<pass_smem_words<PASS>()>(sh, PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 : a.hist3);
+}
+
+// CTA of MON_TARGETS warps, warp j = target j: the digit of pass PASS that
+// holds the target's rank (the prefix and rank updated).
+template <int PASS>
+__device__ void select_digit(const MonArgs &a)
+{
+    constexpr int NB = pass_bins<PASS>();
+    constexpr int SEG = NB / 32;
+    const int lane = threadIdx.x & 31, j = threadIdx.x >> 5;
     MonState *st = a.st;
-    if (tid < MON_TARGETS)
-        pref_s[tid] = st->prefix[tid];
+    const uint32_t r = static_cast<uint32_t>(__ldcg(&st->rank[j]));   // < N < 2^31
+    uint32_t before = 0, in = 0;
+    int bin;
+    if (PASS == 1 && j < 2) {   // |delta|'s 1024 bins from delta's 2048
+        uint32_t v[32];
+        load_abs_segment<32>(a.hist1, 1024, lane * 32, v);
+        bin = warp_find_bin<32>(v, r, before, in);
+    } else {
+        const uint32_t *hg = PASS == 1 ? a.hist1 : PASS == 2 ? a.hist2 + j * NB : a.hist3 + j * NB;
+        uint32_t v[SEG];
+        load_segment<SEG>(hg + lane * SEG, v);
+        bin = warp_find_bin<SEG>(v, r, before, in);
+    }
+    if (lane == 0) {
+        if (bin < 0) {
+            counts_inconsistent(a);
+        } else {
+            st->rank[j] = static_cast<long long>(r - before);
+            st->prefix[j] = __ldcg(&st->prefix[j]) | (static_cast<uint32_t>(bin) << digit_shift(PASS, 32));
+        }
+    }
+}
+
+// Grid barrier of the selection pass (a cooperative launch: every CTA is
+// resident).  Bounded: a CTA whose wait runs out records TIM_ERR_TIMEOUT and
+// raises the call's abort word, on which every other waiting CTA leaves too.
+__device__ bool grid_barrier(const MonArgs &a, unsigned &gen)
+{
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        MonState *st = a.st;
+        __threadfence();
+        atomicAdd(&st->barrier, 1u);
+        const unsigned target = (gen + 1u) * gridDim.x;
+        const uint64_t t0 = global_ns();
+        bool ok = true;
+        while (*reinterpret_cast<volatile unsigned *>(&st->barrier) < target) {
+            if (*reinterpret_cast<volatile int *>(&st->abort)) {
+                ok = false;
+                break;
+            }
+            if (global_ns() - t0 > a.wait_budget_ns) {
+                ok = false;
+                atomicExch(&st->abort, 1);
+                atomicCAS(a.status, 0, static_cast<int>(TIM_ERR_TIMEOUT));
+                break;
+            }
+            __nanosleep(128);
+        }
+        __threadfence();
+        ok_s = ok;
+    }
+    __syncthreads();
+    ++gen;
+    return ok_s != 0;
+}
+
+__device__ void select_over_all_tokens(const MonArgs &a, uint32_t *sh)
+{
+    unsigned gen = 0;
+    all_token_pass<1>(a, sh);
+    if (!grid_barrier(a, gen))
+        return;
+    if (blockIdx.x == 0)
+        select_digit<1>(a);
+    if (!grid_barrier(a, gen))
+        return;
+    all_token_pass<2>(a, sh);
+    if (!grid_barrier(a, gen))
+        return;
+    if (blockIdx.x == 0)
+        select_digit<2>(a);
+    if (!grid_barrier(a, gen))
+        return;
+    all_token_pass<3>(a, sh);
+    if (last_cta(&a.st->ticket[2])) {
+        select_digit<3>(a);
+        __syncthreads();
+        if (threadIdx.x == 0)
+            write_record(a);
+    }
+}
+
+// ---------------------------------------------------------------- the selection pass (lists)
+// Every list key whose offset has a target's high digit gives the target its
+// low digit (offset bits below the high digit, at most 16), counted in the
+// target's coarse (top 8 bits) and fine (all 16) low-digit histograms, lanes
+// with equal digits added by one atomic.  (Appending the keys to a per-target
+// buffer instead made ~2000 keys meet on one counter: 30 us of serialised
+// atomics.)  When a quantile's two targets share their high bin, the second
+// reads the first's histograms.  Then the last CTA, warp j per target, selects
+// the low digit from the two histograms (one round trip each); the target's
+// key is lo + (high << shift) + low.
+// Counts low digit `low` of target j (a key in the target's high bin) in the
+// target's two histograms, lanes with equal digits added by one atomic (a
+// full warp calls; lanes with hit unset take no part).  Kept out of line: the
+// gather loop stays small (it had been bound by instruction fetch).
+__device__ __noinline__ void count_low_digit(const MonArgs &a, bool hit, int j, uint32_t low)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t tag = hit ? static_cast<uint32_t>(j) << 16 | low : 0xffffffffu;
+    const unsigned same = __match_any_sync(0xffffffffu, tag);
+    const unsigned same_c = __match_any_sync(0xffffffffu, hit ? tag >> 8 : 0xffffffffu);
+    if (hit && lane == __ffs(same) - 1)
+        atomicAdd(a.lof + static_cast<size_t>(j) * MON_FINE + low, static_cast<uint32_t>(__popc(same)));
+    if (hit && lane == __ffs(same_c) - 1)
+        atomicAdd(a.loc + j * MON_COARSE + (low >> 8), static_cast<uint32_t>(__popc(same_c)));
+}
+
+__device__ void select_in_lists(const MonArgs &a)
+{
+    __shared__ uint32_t lo_s[MON_QUANTILES], hd_s[MON_TARGETS];
+    __shared__ int shift_s[MON_QUANTILES], dup_s[MON_TARGETS];
+    __shared__ unsigned long long cnt_s[MON_QUANTILES];
+    const int tid = threadIdx.x, lane = tid & 31;
+    MonState *st = a.st;
     if (tid < MON_QUANTILES) {
         lo_s[tid] = st->lo[tid];
-        bits_s[tid] = st->span_bits[tid];
-        cnt_s[tid] = std::min<unsigned long long>(st->count[tid], a.cap);
+        shift_s[tid] = high_shift(st->span_bits[tid]);
+        cnt_s[tid] = std::min<unsigned long long>(a.hot[tid * MON_HOT_STRIDE], a.cap);
     }
-    if (tid == 0)
-        mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
+    if (tid < MON_TARGETS) {
+        hd_s[tid] = st->prefix[tid];
+        dup_s[tid] = (tid & 1) && st->prefix[tid] == st->prefix[tid - 1];
+    }
     __syncthreads();
-    if (PASS == 1 && mode_s != 2)   // uniform over the grid
+    // One list after another (the list's bound, shift and high digits stay in
+    // registers), each grid-strided, kBatch keys per lane loaded before use;
+    // the trip count is uniform over the warp (the vote needs every lane).
+    // (The four lists as one index space, with fewer rounds of loads but each
+    // key's list parameters read from shared memory, measured ~3 us slower.)
+    constexpr int kBatch = 16;
+    const uint32_t stride = gridDim.x * MON_THREADS;
+    const uint64_t pol = l2_policy_evict_first();
+    for (int q = 0; q < MON_QUANTILES; ++q) {
+        const uint32_t n = static_cast<uint32_t>(cnt_s[q]);   // <= cap < 2^31
+        const uint32_t lo = lo_s[q], hd0 = hd_s[2 * q], hd1 = hd_s[2 * q + 1];
+        const int sh = shift_s[q];
+        const bool dup1 = dup_s[2 * q + 1] != 0;
+        const uint32_t *list = a.cand + static_cast<size_t>(q) * a.cap;
+        for (uint32_t w0 = blockIdx.x * MON_THREADS + (tid & ~31); w0 < n; w0 += kBatch * stride) {
+            uint32_t v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const uint32_t i = w0 + lane + u * stride;
+                v[u] = i < n ? ld_global_hint(list + i, pol) : 0u;   // demoted once read
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const bool in = w0 + lane + u * stride < n;
+                const uint32_t x = v[u] - lo;
+                const uint32_t hd = x >> sh;
+                const bool h0 = in && hd == hd0, h1 = in && hd == hd1 && !dup1;
+                if (__any_sync(0xffffffffu, h0 || h1)) {
+                    const uint32_t low = x & ((1u << sh) - 1u);   // sh <= 16
+                    count_low_digit(a, h0, 2 * q, low);
+                    count_low_digit(a, h1, 2 * q + 1, low);
+                }
+            }
+        }
+    }
+    uint32_t dup = 0;   // bit j: target j reads target j - 1's histograms
+#pragma unroll
+    for (int j = 0; j < MON_TARGETS; ++j)
+        dup |= static_cast<uint32_t>(dup_s[j]) << j;
+    if (!last_cta(&st->ticket[2]))
         return;
-    if (tid == 0) {
-        start_s[0] = 0;
-        for (int q = 1; q < MON_QUANTILES; ++q)
-            start_s[q] = start_s[q - 1] + cnt_s[q - 1];
+    // warp j: target j
+    const int j = tid >> 5, q = j >> 1;
+    const int src = ((dup >> j) & 1u) ? j - 1 : j;
+    const int sh = shift_s[q];
+    uint32_t r = static_cast<uint32_t>(__ldcg(&st->rank[j]));
+    uint32_t low = 0, before = 0, in = 0;
+    bool ok = true;
+    if (sh > 0) {   // else the high digit is the whole offset
+        uint32_t c8[8];
+        load_segment<8>(a.loc + src * MON_COARSE + lane * 8, c8);
+        const int cb = warp_find_bin<8>(c8, r, before, in);
+        ok = cb >= 0;
+        if (ok) {
+            r -= before;
+            load_segment<8>(a.lof + static_cast<size_t>(src) * MON_FINE + cb * MON_COARSE + lane * 8, c8);
+            const int fb = warp_find_bin<8>(c8, r, before, in);
+            ok = fb >= 0;
+            low = static_cast<uint32_t>(cb * MON_COARSE + (fb < 0 ? 0 : fb));
+        }
+    }
+    if (lane == 0) {
+        if (!ok)
+            counts_inconsistent(a);
+        else
+            st->prefix[j] = lo_s[q] + (hd_s[j] << sh) + low;
     }
     __syncthreads();
-    const unsigned long long total = cnt_s[0] + cnt_s[1] + cnt_s[2] + cnt_s[3];
-    // Collected keys: at least kKeysPerCta per CTA, so that few CTAs pay for
-    // clearing and adding their histograms; the others only take the ticket.
-    constexpr unsigned long long kKeysPerCta = 16 * MON_THREADS;
-    const unsigned long long ctas = std::min<unsigned long long>(gridDim.x, (total + kKeysPerCta - 1) / kKeysPerCta);
-    const bool work = mode_s == 2 || (mode_s == 1 && blockIdx.x < ctas);   // uniform over the CTA
-    if (work) {
-        zero_histogram<pass_smem_words<PASS>()>(mon_sh);
-        __syncthreads();
-        if (PASS != 1 && mode_s == 1) {
-            // the collected keys of the four lists, one list after another;
-            // kBatch keys per thread loaded before any is used
-            uint32_t lo_r[MON_QUANTILES], bits_r[MON_QUANTILES], pr0[MON_QUANTILES], pr1[MON_QUANTILES];
-#pragma unroll
-            for (int q = 0; q < MON_QUANTILES; ++q) {
-                lo_r[q] = lo_s[q];
-                bits_r[q] = static_cast<uint32_t>(bits_s[q]);
-                pr0[q] = pref_s[2 * q];
-                pr1[q] = pref_s[2 * q + 1];
-            }
-            constexpr int kBatch = 16;
-            const unsigned long long stride = ctas * MON_THREADS;
-            for (unsigned long long i0 = static_cast<unsigned long long>(blockIdx.x) * MON_THREADS + tid; i0 < total;
-                 i0 += kBatch * stride) {
-                uint32_t v[kBatch];
-                int qs[kBatch];
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const unsigned long long i = i0 + u * stride;
-                    qs[u] = -1;
-                    if (i < total) {
-                        const int q = (i >= start_s[1]) + (i >= start_s[2]) + (i >= start_s[3]);
-                        qs[u] = q;
-                        v[u] = __ldcs(a.cand + static_cast<size_t>(q) * a.cap + (i - start_s[q]));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int q = qs[u];
-                    if (q < 0)
-                        continue;
-                    // the list's bound, width and the two targets' prefixes, chosen
-                    // from registers (no shared-memory lookup on the key's path)
-                    const uint32_t x = v[u] - pick4(lo_r, q);
-                    const int b = static_cast<int>(pick4(bits_r, q));
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = 2 * q + e;
-                        if (in_prefix<PASS>(x, pick4(e == 0 ? pr0 : pr1, q), b))
-                            atomicAdd(mon_sh + j * NB + digit_of<PASS>(x, b), 1u);
-                    }
-                }
-            }
-        } else {
-            uint32_t pr[MON_TARGETS];   // in registers: the histogram atomics may alias shared memory
-#pragma unroll
-            for (int j = 0; j < MON_TARGETS; ++j)
-                pr[j] = pref_s[j];
-            for_token_groups<MON_UNROLL>(a, [&](int64_t, const float (&d)[4], const bool (&m)[4],
-                                                const bool (&valid)[4]) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool used = valid[i] && usable(m[i], d[i]);
-                    const uint32_t kd = key_signed(d[i]);
-                    if (PASS == 1) {
-                        if (used)   // delta's key only; |delta|'s histogram follows (select_digit<1>)
-                            atomicAdd(mon_sh + (kd >> 21), 1u);
-                    } else {
-                        const uint32_t ka = key_abs(d[i]);
-#pragma unroll
-                        for (int j = 0; j < MON_TARGETS; ++j) {
-                            const uint32_t k = j < 2 ? ka : kd;
-                            if (used && in_prefix<PASS>(k, pr[j], 32))
-                                atomicAdd(mon_sh + j * NB + digit_of<PASS>(k, 32), 1u);
-                        }
-                    }
-                }
-            });
-        }
-        __syncthreads();
-        flush_histogram<pass_smem_words<PASS>()>(
-            mon_sh, PASS == 1 ? a.hist1 + MON_QUANTILES * MON_BINS1 : PASS == 2 ? a.hist2 : a.hist3);
+    if (tid == 0)
+        write_record(a);
+}
+
+// ---------------------------------------------------------------- the selection kernel
+constexpr int kSelCtasPerSm = 2;
+constexpr size_t kSelSmem = 4 * MON_TARGETS * MON_BINS2;   // the all-token pass 2's histograms
+
+__global__ void __launch_bounds__(MON_THREADS, kSelCtasPerSm) mon_select_kernel(const MonArgs a)
+{
+    extern __shared__ __align__(16) uint32_t sel_sh[];
+    __shared__ int mode_s;   // 0 no used token (or inconsistent counts), 1 the lists, 2 all tokens
+    pdl_wait();   // the full pass's results
+    if (threadIdx.x == 0) {
+        const MonState *st = a.st;
+        mode_s = st->empty ? 0 : st->fallback ? 2 : 1;
     }
-    if (last_cta(&st->ticket[1 + PASS])) {
-        select_digit<PASS>(a);
-        if (PASS == 3) {
-            __syncthreads();
-            if (tid == 0)
-                write_record(a);
-        }
+    __syncthreads();
+    if (mode_s == 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            write_record(a);
+    } else if (mode_s == 1) {
+        select_in_lists(a);
+    } else {
+        select_over_all_tokens(a, sel_sh);
     }
 }
 
@@ -1119,9 +1338,6 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 constexpr size_t kSampleSmem = 4 * SBD;
 
-template <int PASS>
-constexpr size_t pass_smem() { return 4 * pass_smem_words<PASS>(); }
-
 // Each kernel's dynamic shared memory.  (The largest shared-memory carveout
 // as a hint made the call ~6 us slower.)
 template <typename K>
@@ -1129,6 +1345,8 @@ cudaError_t smem_attributes(K kernel, size_t bytes)
 {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
+
+int g_sel_ctas_per_sm = 0;   // resident selection CTAs per SM (a cooperative launch needs them all at once)
 
 } // namespace
 
@@ -1138,17 +1356,19 @@ cudaError_t monitor_prepare_device()
     if (e == cudaSuccess)
         e = smem_attributes(mon_scan_kernel, kScanSmem);
     if (e == cudaSuccess)
-        e = smem_attributes(mon_pass_kernel<1>, pass_smem<1>());
+        e = smem_attributes(mon_select_kernel, kSelSmem);
+    int per_sm = 0;
     if (e == cudaSuccess)
-        e = smem_attributes(mon_pass_kernel<2>, pass_smem<2>());
-    if (e == cudaSuccess)
-        e = smem_attributes(mon_pass_kernel<3>, pass_smem<3>());
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mon_select_kernel, MON_THREADS, kSelSmem);
+    if (e == cudaSuccess && per_sm < 1)
+        e = cudaErrorInvalidConfiguration;
+    g_sel_ctas_per_sm = std::min(per_sm, kSelCtasPerSm);
     return e;
 }
 
-// memset of the state and histograms, then sample (+ bounds), the full pass
-// (+ ranks and the lists' first digit), radix passes 1 (all tokens only), 2
-// and 3 (+ their digits and the record), chained by dependent launches.
+// memset of the state and small histograms, then the sample (+ bounds), the
+// full pass (+ ranks and high digits) chained by dependent launches, and the
+// selection pass (a cooperative launch: its all-token mode has grid barriers).
 cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
 {
     cudaError_t e = cudaMemsetAsync(a.st, 0, MON_ZEROED_BYTES, stream);
@@ -1156,21 +1376,27 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
         return e;
     const int64_t groups = (a.N + 3) / 4;
     const int64_t want = (groups + MON_THREADS - 1) / MON_THREADS;
-    const dim3 grid(static_cast<unsigned>(
-        std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(MON_CTAS_PER_SM) * num_sms))));
     const dim3 scan_grid(static_cast<unsigned>(
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(kScanCtasPerSm) * num_sms))));
-    const int64_t runs = std::min<int64_t>(MON_SAMPLE_RUNS, (a.N + MON_SAMPLE_RUN - 1) / MON_SAMPLE_RUN);
-    const int64_t sample_ctas =   // one CTA per SM at most: all start at once
-        std::max<int64_t>(1, std::min<int64_t>((runs + kRunsAtOnce - 1) / kRunsAtOnce, num_sms));
+    // one CTA per SM: all start at once; every one of them also zeroes its
+    // share of the fine histograms
     const dim3 block(MON_THREADS);
-    if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(sample_ctas)), block, kSampleSmem, stream, a)) !=
+    if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(num_sms)), block, kSampleSmem, stream, a)) !=
             cudaSuccess ||
-        (e = launch_pdl(mon_scan_kernel, scan_grid, block, kScanSmem, stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<1>, grid, block, pass_smem<1>(), stream, a)) != cudaSuccess ||
-        (e = launch_pdl(mon_pass_kernel<2>, grid, block, pass_smem<2>(), stream, a)) != cudaSuccess)
+        (e = launch_pdl(mon_scan_kernel, scan_grid, block, kScanSmem, stream, a)) != cudaSuccess)
         return e;
-    return launch_pdl(mon_pass_kernel<3>, grid, block, pass_smem<3>(), stream, a);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1] = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, g_sel_ctas_per_sm) * num_sms));
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = kSelSmem;
+    return cudaLaunchKernelEx(&cfg, mon_select_kernel, a);
 }
 
 } // namespace tim

@@ -613,13 +613,7 @@ int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, con
     a.tau_tok = tau_tok;
     a.reject = token_reject;
     a.out = out;
-    a.st = static_cast<tim::MonState *>(ws);
-    a.hist1 = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + tim::MON_STATE_BYTES);
-    a.hist2 = a.hist1 + tim::MON_HIST1_WORDS;
-    a.hist3 = a.hist2 + tim::MON_HIST2_WORDS;
-    a.shist = a.hist3 + tim::MON_HIST3_WORDS;
-    a.cand = a.shist + tim::MON_SHIST_WORDS;
-    a.cap = tim::monitor_cap(N);
+    tim::monitor_bind(a, ws, N);
     a.status = dev->status;
     a.wait_budget_ns = wait_budget_ns();
     e = tim::monitor_launch(a, dev->sms, s);

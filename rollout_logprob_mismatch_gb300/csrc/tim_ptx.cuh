@@ -291,6 +291,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last()
     return p;
 }
 
+// 4-byte global store / load with an L2 eviction-priority hint (a policy from
+// the createpolicy helpers here).
+__device__ __forceinline__ void st_global_hint(uint32_t *p, uint32_t v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_global_hint(const uint32_t *p, uint64_t pol)
+{
+    uint32_t v;
+    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_normal()
 {
     uint64_t p;

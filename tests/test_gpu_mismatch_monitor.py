@@ -115,17 +115,27 @@ def test_full_size_batch():
     assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^27")
 
 
+def sampled_tokens(N, runs=1024, run=1024):
+    """The tokens the monitor's sample reads when N exceeds runs x run: run r
+    starts at r (N - run) / (runs - 1), rounded down to a multiple of 4."""
+    s = np.zeros(N, bool)
+    for r in range(runs):
+        s0 = (r * (N - run) // (runs - 1)) & ~3
+        s[s0:s0 + run] = True
+    return s
+
+
 def test_sample_that_misses_the_bulk_and_mass_ties():
     """Batches larger than the 2^20-token sample where the sample misleads:
-    the sampled runs (the first 1024 of every 2048 tokens at N = 2^21) hold
-    delta = 0 and the rest delta = 1, so the quantiles lie outside the sample's
-    bounds; and a batch of identical deltas, so the collected list overflows.
-    Both take the selection over all tokens and stay exact."""
+    the sampled runs (half the tokens at N = 2^21) hold delta = 0 and the rest
+    delta = 1, so the quantiles lie outside the sample's bounds; and a batch
+    of identical deltas, so the collected list overflows.  Both take the
+    selection over all tokens (three radix passes with grid barriers) and stay
+    exact."""
     N = 1 << 21
     rng = np.random.default_rng(9)
     lr = wl.draw_train_logprobs(N, 9)
-    t = np.arange(N)
-    lt = (lr + np.where((t % 2048) < 1024, np.float32(0.0), np.float32(1.0))).astype(np.float32)
+    lt = (lr + np.where(sampled_tokens(N), np.float32(0.0), np.float32(1.0))).astype(np.float32)
     mask = (rng.random(N) < 0.9).astype(np.uint8)
     tau = float(np.float32(0.5))
     g, rej = gpu_monitor(lt, lr, mask, tau)
