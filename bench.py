@@ -48,12 +48,12 @@ K2_BW_TOKENS = 1 << 27
 MEASURED_TRAFFIC = {
     # token logprob, N = 8192, D = 4096, V = 151936: 2709789184 read + 15962880 written
     ("k1", "9053c2f6492f274e"): 2709789184 + 15962880,
-    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1231426304 read + 495642880 written
-    ("k2", "407cfe470c6416f9"): 1223959296 + 7467008 + 495642880,
+    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229717248 read + 496890880 written
+    ("k2", "aeafde5936697951"): 1222252288 + 7464960 + 496890880,
     # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2513547264 read + 1029856768 written
     ("ppo", "0acf304a08c63dfc"): 2510266880 + 3280384 + 1029856768,
-    # mismatch monitor, 2^27 tokens, its five kernels: 1235754944 read + 99868416 written
-    ("monitor", "5bfdd1beefab0f71"): 9553920 + 1208104960 + 24064 + 9048320 + 9023744 + 99868416,
+    # mismatch monitor, 2^27 tokens, its three kernels: 1227744512 read + 109986816 written
+    ("monitor", "feb4bfd7d7a2c580"): 9917952 + 1208892416 + 8934144 + 109986816,
 }
 TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at this shape, " \
                  "stored with a hash of the kernel sources it was taken on"
