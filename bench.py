@@ -46,12 +46,12 @@ K2_BW_TOKENS = 1 << 27
 # the kernel at the benchmark's shape, keyed by a hash of the kernel's sources at capture time;
 # reported as `traffic` (with `traffic_source`) only while the sources are unchanged, else null.
 MEASURED_TRAFFIC = {
-    # token logprob, N = 8192, D = 4096, V = 151936: 2709789184 read + 15962880 written
-    ("k1", "9053c2f6492f274e"): 2709789184 + 15962880,
-    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229717248 read + 496890880 written
-    ("k2", "aeafde5936697951"): 1222252288 + 7464960 + 496890880,
-    # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2513547264 read + 1029856768 written
-    ("ppo", "0acf304a08c63dfc"): 2510266880 + 3280384 + 1029856768,
+    # token logprob, N = 8192, D = 4096, V = 151936: 2666996480 read + 15407872 written
+    ("k1", "78fc418be590bdf5"): 2666996480 + 15407872,
+    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229416960 read + 496860416 written
+    ("k2", "92bd5a06957f57ff"): 1221953024 + 7463936 + 496860416,
+    # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2512521728 read + 1029964544 written
+    ("ppo", "c37a526d1c3280ce"): 2509241344 + 3280384 + 1029964544,
     # mismatch monitor, 2^27 tokens, its three kernels: 1227744512 read + 109986816 written
     ("monitor", "feb4bfd7d7a2c580"): 9917952 + 1208892416 + 8934144 + 109986816,
 }

@@ -20,7 +20,7 @@ constexpr int K2_STAGE_BYTES = 2 * K2_F_BYTES + K2_M_BYTES;
 constexpr int K2_BAR_BYTES = K2_WARPS * K2_STAGES * 8;
 constexpr int K2_SMEM_BYTES = K2_BAR_BYTES + K2_WARPS * K2_STAGES * K2_STAGE_BYTES;
 constexpr int64_t K2_LONG = 8192;                  // longer sequences are reduced by a whole CTA
-constexpr int K2_CLAIM_BLOCK = 4;                  // sequences per ticket in the first 7/8 of a batch
+constexpr int K2_CLAIM_BLOCK = 4;                  // sequences per ticket in the bulk of a large batch
 constexpr int K2_FOLD_THREADS = 256;               // fold CTA
 constexpr int K2_FOLD_SEQS = 4 * K2_FOLD_THREADS;  // sequences per fold CTA
 constexpr int K2_REC_WORDS = 16;                   // 4-byte words per sequence record (64 bytes a sequence)

@@ -629,16 +629,21 @@ __device__ __forceinline__ int claim_raw(const K2Args &a, int lane)
     return lane == 0 ? atomicAdd(a.claim, 1) : 0;
 }
 
-// The sequences of ticket t: the first k2_block_tickets(S) tickets hand out
+// The sequences of ticket t: the first t0 = block_tickets(S) tickets hand out
 // K2_CLAIM_BLOCK consecutive sequences each, the later ones one each.  The
 // blocks cut the counter's traffic (one claim per sequence from every warp
 // queued on the counter's word, and how long varied from one device to
-// another); single sequences at the end keep the warps' finish times close.
-__device__ __forceinline__ int k2_block_tickets(int S) { return (S - S / 8) / K2_CLAIM_BLOCK; }
-
-__device__ __forceinline__ void ticket_range(int t, int S, int &lo, int &hi)
+// another); single sequences at the end keep the warps' finish times close,
+// and a batch of few sequences (at most two per warp of the grid) goes out
+// one sequence at a time, spread over as many warps as it can.
+__device__ __forceinline__ int block_tickets(int S)
 {
-    const int t0 = k2_block_tickets(S);
+    const int singles = min(S, max(S / 8, 2 * static_cast<int>(gridDim.x) * K2_WARPS));
+    return (S - singles) / K2_CLAIM_BLOCK;
+}
+
+__device__ __forceinline__ void ticket_range(int t, int S, int t0, int &lo, int &hi)
+{
     if (t < t0) {
         lo = t * K2_CLAIM_BLOCK;
         hi = lo + K2_CLAIM_BLOCK;
@@ -656,13 +661,13 @@ __device__ __forceinline__ void ticket_range(int t, int S, int &lo, int &hi)
 // bad sequences met on the way are written at once, long ones are left for
 // the CTA phase.  Returns S when there is none (every later ticket is past S
 // too).
-__device__ __forceinline__ int next_short(const K2Args &a, int &cur, int &end, int &pend, int lane)
+__device__ __forceinline__ int next_short(const K2Args &a, int t0, int &cur, int &end, int &pend, int lane)
 {
     while (true) {
         if (cur >= end) {
             const int t = __shfl_sync(0xffffffffu, pend, 0);
             pend = claim_raw(a, lane);
-            ticket_range(t, a.S, cur, end);
+            ticket_range(t, a.S, t0, cur, end);
             if (cur >= a.S)
                 return a.S;
         }
@@ -722,8 +727,9 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
     // of the range they reduce, so the work stays balanced however the lengths
     // vary (a record's bits depend on its own tokens only, not on the warp
     // that reduces it).
+    const int t0 = block_tickets(a.S);
     int pend = claim_raw(a, lane), t_cur = 0, t_end = 0;   // lane 0: the next ticket; the current range
-    int s = next_short(a, t_cur, t_end, pend, lane);
+    int s = next_short(a, t0, t_cur, t_end, pend, lane);
     ChunkView cur;
     if (s < a.S) {
         const int64_t b = a.off[s], e = a.off[s + 1];
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(K2_THREADS, K2_CTAS_PER_SM) k2_seq_kernel(cons
                 nv = stage_chunk(a, nst, nbar, t0, min(e, t0 + K2_CHUNK), lane, pol);
                 pending |= 1u << (stage ^ 1);
             } else {
-                nxt = next_short(a, t_cur, t_end, pend, lane);
+                nxt = next_short(a, t0, t_cur, t_end, pend, lane);
                 if (nxt < a.S) {
                     const int64_t nb = a.off[nxt], ne = a.off[nxt + 1];
                     nv = stage_chunk(a, nst, nbar, nb, min(ne, nb + K2_CHUNK), lane, pol);
