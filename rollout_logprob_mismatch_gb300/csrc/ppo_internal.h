@@ -13,6 +13,7 @@ constexpr int PPO_THREADS = PPO_WARPS * 32;
 constexpr int PPO_CTAS_PER_SM = 3;
 constexpr int PPO_CHUNK = 256;                      // tokens per warp step: 8 per lane, loaded before use
 constexpr int64_t PPO_LONG = 8192;                  // longer sequences are reduced by a whole CTA
+constexpr int PPO_CLAIM_BLOCK = 4;                  // sequences per ticket in the bulk of a large batch
 constexpr int PPO_FOLD_THREADS = 256;
 constexpr int PPO_FOLD_SEQS = 4 * PPO_FOLD_THREADS; // sequences per fold CTA
 constexpr int PPO_REC_WORDS = 6;                    // 4-byte words per sequence record (structure of arrays)
@@ -22,7 +23,7 @@ static_assert(PPO_CHUNK % 64 == 0, "a chunk is whole 64-token lane groups");
 inline size_t ppo_workspace_bytes(int64_t S)
 {
     const int64_t parts = (S + PPO_FOLD_SEQS - 1) / PPO_FOLD_SEQS;
-    return static_cast<size_t>(S) * PPO_REC_WORDS * 4 + static_cast<size_t>(parts) * PPO_PART_WORDS * 4 + 512;
+    return static_cast<size_t>(S) * PPO_REC_WORDS * 4 + static_cast<size_t>(parts) * PPO_PART_WORDS * 4 + 1024;
 }
 
 struct PpoArgs {
@@ -43,6 +44,7 @@ struct PpoArgs {
     uint32_t *rec;         // workspace: sequence records, [PPO_REC_WORDS][S]
     uint32_t *part;        // workspace: fold partials, [ceil(S / PPO_FOLD_SEQS)][PPO_PART_WORDS]
     unsigned *ticket;      // workspace: fold CTAs finished (zeroed by ppo_seq_kernel)
+    int *claim;            // workspace: the sequences' ticket counter (zeroed before ppo_seq_kernel)
     int *status;
 };
 

@@ -691,6 +691,7 @@ int tim_tis_ppo(const float *logp_theta, const float *logp_old, const float *log
     a.ticket = S > 0 ? a.part + round_up(static_cast<size_t>((S + tim::PPO_FOLD_SEQS - 1) / tim::PPO_FOLD_SEQS) *
                                              tim::PPO_PART_WORDS, 64)
                      : nullptr;
+    a.claim = S > 0 ? reinterpret_cast<int *>(a.ticket + 32) : nullptr;   // its own 128-byte line
     a.status = dev->status;
     cudaError_t e = tim::ppo_launch(a, dev->sms, s);
     cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;

@@ -260,14 +260,36 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
     }
     const bool has_long = __syncthreads_or(mine) != 0;
 
-    // ---- phase 1: sequences of at most PPO_LONG tokens, one warp each.  Warp w
-    // of CTA c takes sequences w * gridDim + c, + warps in the grid, ...
-    // Each sequence is prefetched into L2 ahead of the warp's loads: its first
-    // two steps when it starts, step c + 2 during step c.  (Prefetching the
-    // warp's next sequence as well was measured slower: ~20% of it was fetched
-    // from DRAM twice.)
-    const int step = gridDim.x * PPO_WARPS;
-    for (int s = warp * gridDim.x + blockIdx.x; s < a.S; s += step) {
+    // ---- phase 1: sequences of at most PPO_LONG tokens, one warp each.  Warps
+    // claim tickets in index order from the call's counter, one ticket ahead of
+    // the range they reduce: in a large batch the first tickets hand out
+    // PPO_CLAIM_BLOCK consecutive sequences each (few claims on the counter's
+    // word), the last ones, and every ticket of a batch of at most two
+    // sequences per warp, one sequence each.  Which warp handles a sequence
+    // never changes its record's bits.  Each sequence is prefetched into L2
+    // ahead of the warp's loads: its first two steps when it starts, step c + 2
+    // during step c.  (Prefetching the warp's next sequence as well was
+    // measured slower: ~20% of it was fetched from DRAM twice.)
+    const int singles = min(a.S, max(a.S / 8, 2 * static_cast<int>(gridDim.x) * PPO_WARPS));
+    const int t_blocks = (a.S - singles) / PPO_CLAIM_BLOCK;   // tickets of PPO_CLAIM_BLOCK sequences
+    int pend = lane == 0 ? atomicAdd(a.claim, 1) : 0;       // lane 0: the next ticket
+    int t_cur = 0, t_end = 0;                               // the current ticket's sequences
+    while (true) {
+        if (t_cur >= t_end) {
+            const int t = __shfl_sync(0xffffffffu, pend, 0);
+            pend = lane == 0 ? atomicAdd(a.claim, 1) : 0;
+            if (t < t_blocks) {
+                t_cur = t * PPO_CLAIM_BLOCK;
+                t_end = t_cur + PPO_CLAIM_BLOCK;
+            } else {
+                t_cur = t_blocks * PPO_CLAIM_BLOCK + (t - t_blocks);   // t < S + claims in flight: no overflow
+                t_end = t_cur + 1;
+            }
+            if (t_cur >= a.S)   // every later ticket is past S too
+                break;
+            t_end = min(t_end, a.S);
+        }
+        const int s = t_cur++;
         const int64_t b = a.off[s], e = a.off[s + 1];
         if (!offsets_ok(a, s, b, e)) {
             write_plain(a, s, true, lane);
@@ -285,8 +307,8 @@ __global__ void __launch_bounds__(PPO_THREADS, PPO_CTAS_PER_SM) ppo_seq_kernel(c
         write_seq(a, s, warp_total(acc), lane);
     }
 
-    // ---- phase 2: longer sequences, one CTA each; warp w takes steps w, w + PPO_WARPS, ...
-    // (the CTA's phase-1 warps met exactly the sequences q = blockIdx.x + k gridDim.x)
+    // ---- phase 2: longer sequences, one CTA each (q = blockIdx.x + k gridDim.x, as
+    // the pre-scan above); warp w takes steps w, w + PPO_WARPS, ...
     if (!has_long)   // uniform over the CTA
         return;
     for (int q = blockIdx.x; q < a.S; q += gridDim.x) {
@@ -596,7 +618,9 @@ cudaError_t ppo_launch(const PpoArgs &a, int num_sms, cudaStream_t stream)
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(std::min(a.S, num_sms * PPO_CTAS_PER_SM), 1, 1);
     cfg.blockDim = dim3(PPO_THREADS, 1, 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ppo_seq_kernel, a);
+    cudaError_t e = cudaMemsetAsync(a.claim, 0, sizeof(int), stream);
+    if (e == cudaSuccess)
+        e = cudaLaunchKernelEx(&cfg, ppo_seq_kernel, a);
     if (e != cudaSuccess)
         return e;
     const int parts = (a.S + PPO_FOLD_SEQS - 1) / PPO_FOLD_SEQS;
