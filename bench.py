@@ -50,8 +50,8 @@ MEASURED_TRAFFIC = {
     ("k1", "78fc418be590bdf5"): 2666996480 + 15407872,
     # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229416960 read + 496860416 written
     ("k2", "92bd5a06957f57ff"): 1221953024 + 7463936 + 496860416,
-    # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2512521728 read + 1029964544 written
-    ("ppo", "c37a526d1c3280ce"): 2509241344 + 3280384 + 1029964544,
+    # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2497949440 read + 1027808000 written
+    ("ppo", "a17407344a379435"): 2494668800 + 3280640 + 1027808000,
     # mismatch monitor, 2^27 tokens, its three kernels: 1227744512 read + 109986816 written
     ("monitor", "feb4bfd7d7a2c580"): 9917952 + 1208892416 + 8934144 + 109986816,
 }
