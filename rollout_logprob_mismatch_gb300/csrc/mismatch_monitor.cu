@@ -325,15 +325,19 @@ __device__ __forceinline__ bool last_cta(unsigned *ticket)
     return true;
 }
 
-// Run r: MON_SAMPLE_RUN tokens from s = r (N - MON_SAMPLE_RUN) / (runs - 1)
-// rounded down to a multiple of 4 (runs back to back when they cover the
-// batch); CTA c takes runs c, c +
+// Run r: MON_SAMPLE_RUN tokens from s = g (N - R) / 63 rounded down to a
+// multiple of 4, plus j R / 16 (g = r / 16, j = r mod 16, R = kSampleRegion;
+// runs back to back when they cover the batch); CTA c takes runs c, c +
 // gridDim, ..., kRunsAtOnce of them loaded before any is used, into a
 // shared-memory histogram of delta's key (|delta|'s follows from it), thread
 // i the tokens s + 4i .. s + 4i + 3 (one 16-byte load per array), and adds
 // the non-zero bins to the global histogram.  The CTA that finishes last
 // computes the bounds.
 constexpr int kRunsAtOnce = 8;   // with one CTA per SM, all 1024 runs in one round of loads
+constexpr int64_t kSampleRegion = int64_t(1) << 18;   // tokens of one of the sample's 64 regions
+static_assert(MON_SAMPLE_RUNS == 64 * 16 && kSampleRegion / 16 >= MON_SAMPLE_RUN &&
+                  kSampleRegion <= int64_t(MON_SAMPLE_RUNS) * MON_SAMPLE_RUN,
+              "64 regions of 16 runs, within the batch whenever the sample does not cover it");
 static_assert(MON_SAMPLE_RUN == 4 * MON_THREADS, "a run is one 4-token group per thread");
 __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a)
 {
@@ -366,11 +370,14 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
                 v[k][i] = w[k][i] = 0.f;
             if (r >= runs)
                 continue;
-            // spread over the batch: r (N - run) / (runs - 1), a spacing that is
-            // no power of two (runs at 2^k-token strides all met the same DRAM
-            // channels)
-            const int64_t s0 = N <= cover ? r * MON_SAMPLE_RUN
-                                          : (r * (N - MON_SAMPLE_RUN) / (runs - 1)) & ~int64_t(3);
+            // 64 regions of kSampleRegion tokens spread over the batch, 16 runs
+            // spread over each region: the runs still come from 1024 places
+            // (sequences) but touch ~1/3 of the pages that runs spread over the
+            // whole batch touch (the sample's loads wait mostly on page-table
+            // walks)
+            const int64_t s0 =
+                N <= cover ? r * MON_SAMPLE_RUN
+                           : (((r >> 4) * (N - kSampleRegion) / 63) & ~int64_t(3)) + (r & 15) * (kSampleRegion / 16);
             const int64_t s1 = std::min<int64_t>(N, s0 + MON_SAMPLE_RUN);
             const int64_t t = s0 + 4 * tid;
             if (t + 4 <= s1) {

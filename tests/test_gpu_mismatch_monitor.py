@@ -115,12 +115,13 @@ def test_full_size_batch():
     assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^27")
 
 
-def sampled_tokens(N, runs=1024, run=1024):
+def sampled_tokens(N, runs=1024, run=1024, region=1 << 18):
     """The tokens the monitor's sample reads when N exceeds runs x run: run r
-    starts at r (N - run) / (runs - 1), rounded down to a multiple of 4."""
+    starts at g (N - region) / 63 rounded down to a multiple of 4, plus
+    j region / 16 (g = r / 16, j = r mod 16)."""
     s = np.zeros(N, bool)
     for r in range(runs):
-        s0 = (r * (N - run) // (runs - 1)) & ~3
+        s0 = ((r >> 4) * (N - region) // 63 & ~3) + (r & 15) * (region // 16)
         s[s0:s0 + run] = True
     return s
 
