@@ -165,3 +165,15 @@ def test_signed_zeros_and_subnormals_at_the_ranks():
     for tau in (0.0, float(np.float32(2.0 ** -140))):
         g, rej = gpu_monitor(lt, lr, mask, tau)
         assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, tau), "zeros tau=%g" % tau)
+
+
+def test_just_above_the_sample_with_a_ragged_tail():
+    """N just above the 2^20 tokens the sample reads, not a multiple of 4 or of
+    the full pass's chunk: the sample's 64 regions overlap (some tokens are
+    sampled twice) and the last chunk is read from global memory; the
+    collected lists are used and the result stays exact."""
+    N = (1 << 20) + 12345
+    off, mask, _, lo, lr, _ = wl.draw_ppo_inputs(N, 21)
+    tau = float(np.float32(0.03))
+    g, rej = gpu_monitor(lo, lr, mask, tau)
+    assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^20 + 12345")
