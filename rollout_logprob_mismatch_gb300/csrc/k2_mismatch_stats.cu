@@ -548,12 +548,11 @@ __device__ void write_batch(const K2Args &a, const FoldAcc &t, bool check_offset
 
 // The fold term of sequence s (its 16-word record, read through L2: other
 // warps wrote it).
-__device__ __forceinline__ void fold_seq(FoldAcc &x, const K2Args &a, int64_t s)
+// One sequence record (16 words, loaded as four 16-byte words) folded into x.
+__device__ __forceinline__ void fold_rec(FoldAcc &x, const uint4 (&q)[4])
 {
-    const uint4 *rp = reinterpret_cast<const uint4 *>(a.rec + static_cast<size_t>(s) * K2_REC_WORDS);
-    const uint4 q0 = __ldcg(rp), q1 = __ldcg(rp + 1), q2 = __ldcg(rp + 2), q3 = __ldcg(rp + 3);
-    const uint32_t rc[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                             q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+    const uint32_t rc[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
+                             q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
     FoldAcc y;
     fold_zero(y);
     if (rc[R_VALID] == 0u) {
@@ -898,9 +897,26 @@ __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a
     __shared__ int last_s;
     FoldAcc x;
     fold_zero(x);
+    // the thread's records s0, s0 + K2_FOLD_THREADS, ...: all loaded first,
+    // then folded in that order
+    constexpr int PER = K2_FOLD_SEQS / K2_FOLD_THREADS;
     const int64_t s1 = min(static_cast<int64_t>(a.S), static_cast<int64_t>(blockIdx.x + 1) * K2_FOLD_SEQS);
-    for (int64_t s = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x; s < s1; s += K2_FOLD_THREADS)
-        fold_seq(x, a, s);
+    const int64_t s0 = static_cast<int64_t>(blockIdx.x) * K2_FOLD_SEQS + threadIdx.x;
+    uint4 q[PER][4];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int64_t s = s0 + static_cast<int64_t>(k) * K2_FOLD_THREADS;
+        if (s < s1) {
+            const uint4 *rp = reinterpret_cast<const uint4 *>(a.rec + static_cast<size_t>(s) * K2_REC_WORDS);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                q[k][w] = __ldcg(rp + w);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+        if (s0 + static_cast<int64_t>(k) * K2_FOLD_THREADS < s1)
+            fold_rec(x, q[k]);
     const FoldAcc t = fold_cta(x);
     if (threadIdx.x == 0) {
         if (gridDim.x == 1) {

@@ -179,23 +179,6 @@ __device__ __forceinline__ uint32_t segment_total(const uint32_t (&v)[SEG])
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
-// The first bin x of the segment with cum + v[0] + ... + v[x] > r (cum: the
-// count before the segment), or -1; `before` gets the count before bin x.
-template <int SEG>
-__device__ __forceinline__ int find_in_segment(const uint32_t (&v)[SEG], uint32_t cum, uint32_t r, uint32_t &before)
-{
-    int bin = -1;
-#pragma unroll
-    for (int x = 0; x < SEG; ++x) {
-        if (bin < 0 && cum + v[x] > r) {
-            bin = x;
-            before = cum;
-        }
-        cum += v[x];
-    }
-    return bin;
-}
-
 // ---------------------------------------------------------------- sample and bounds
 // For quantile q at level L with m sampled used tokens: sample ranks
 // floor(L (m - 1)) - w and ceil(L (m - 1)) + w, w = six standard deviations of
