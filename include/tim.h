@@ -245,6 +245,10 @@ enum tim_batch_field {
     TIM_BATCH_N_REJECTED
 };
 
+/* Words of one sequence record: the per-sequence sums and counts the batch
+ * record is folded from (see tim_mismatch_fold). */
+#define TIM_SEQ_RECORD_WORDS 16
+
 /* Sizes and outputs of tim_mismatch_stats.  The struct lives in host memory;
  * the pointers in it are device pointers.  It carries N and S so that the host
  * never has to read seq_offsets back from the device. */
@@ -258,6 +262,8 @@ typedef struct {
     float *seq_stats;        /* out: fp32 [S][TIM_SEQ_FIELDS] */
     int32_t *seq_flags;      /* out: int32 [S], 1 = rejected */
     double *batch_stats;     /* out: fp64 [TIM_BATCH_FIELDS] */
+    uint32_t *seq_records;   /* out, optional (NULL = kept internal): [S][TIM_SEQ_RECORD_WORDS],
+                                16-byte aligned; a record depends on its own sequence only */
 } tim_mismatch_out;
 
 /*   logp_train, logp_rollout  fp32 [N], 16-byte aligned
@@ -272,6 +278,22 @@ typedef struct {
 TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollout,
                        const uint8_t *mask, const int32_t *seq_offsets, float C,
                        const tim_mismatch_out *out, tim_stream_t stream);
+
+/* The batch record of a batch whose sequences were scored in parts (a batch
+ * sharded across data-parallel ranks, or across calls): the sequence records
+ * of the parts (tim_mismatch_out.seq_records), concatenated in the batch's
+ * sequence order, folded exactly as tim_mismatch_stats folds its own.  A
+ * sequence's record does not depend on where it was packed, so the result has
+ * the bits tim_mismatch_stats gives over the whole batch (the per-batch
+ * aggregation of the icarus page's monitoring steps 2-3, across parts).
+ *   seq_records  [S][TIM_SEQ_RECORD_WORDS] device memory, 16-byte aligned
+ *   num_seqs     S >= 0 (S = 0: an all-zero record)
+ *   batch_stats  out: fp64 [TIM_BATCH_FIELDS], 8-byte aligned device memory
+ * A record marked invalid (bad offsets in its part) makes the record NaN and
+ * sets TIM_ERR_BAD_INPUT, as in tim_mismatch_stats.  Scratch: about S / 6
+ * bytes from the library's stream-ordered pool. */
+TIM_API int tim_mismatch_fold(const uint32_t *seq_records, int32_t num_seqs, double *batch_stats,
+                              tim_stream_t stream);
 
 /* ------------------------------------------------------------------ mismatch monitor
  *

@@ -29,6 +29,7 @@ import threading
 __all__ = [
     "TimError", "SEQ_FIELDS", "BATCH_FIELDS", "PPO_FIELDS", "MONITOR_FIELDS", "tim_mismatch_out", "tim_ppo_out", "lib_path", "load",
     "tim_token_logprob", "tim_token_logprob_temperature", "tim_token_logprob_noalloc", "tim_mismatch_stats",
+    "tim_mismatch_fold", "SEQ_RECORD_WORDS", "mismatch_fold",
     "tim_tis_ppo", "tim_mismatch_monitor", "tim_split_weight_bytes", "tim_split_weight_fp32",
     "tim_token_logprob_fp32_head", "tim_token_logprob_backward", "tim_selftest_wait_timeout", "tim_check", "tim_last_error", "tim_version",
     "tim_debug_violation", "tim_debug_build", "load_debug", "checked", "CHECKS",
@@ -51,6 +52,7 @@ NOALLOC_SCRATCH_BYTES = 16 << 20   # TIM_NOALLOC_SCRATCH_BYTES in include/tim.h
 CHECKS = {0: "none", 1: "target", 2: "mask", 3: "logit", 4: "backward_input", 5: "advantage",
           6: "tma_coord", 7: "store", 8: "unit", 9: "bulk"}
 
+SEQ_RECORD_WORDS = 16   # TIM_SEQ_RECORD_WORDS
 SEQ_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
               "max_abs_delta", "mean_k1", "mean_k2", "mean_k3", "mean_w", "mean_rel")
 BATCH_FIELDS = ("n_mask", "n_used", "n_nan", "n_clip", "mean_delta", "mean_abs_delta",
@@ -82,6 +84,7 @@ class tim_mismatch_out(ctypes.Structure):
         ("seq_stats", ctypes.c_void_p),
         ("seq_flags", ctypes.c_void_p),
         ("batch_stats", ctypes.c_void_p),
+        ("seq_records", ctypes.c_void_p),
     ]
 
 
@@ -121,6 +124,8 @@ def _open(path: str, what: str):
     lib.tim_token_logprob_noalloc.restype = ctypes.c_int
     lib.tim_mismatch_stats.argtypes = [P, P, P, P, ctypes.c_float, ctypes.POINTER(tim_mismatch_out), P]
     lib.tim_mismatch_stats.restype = ctypes.c_int
+    lib.tim_mismatch_fold.argtypes = [P, ctypes.c_int32, P, P]
+    lib.tim_mismatch_fold.restype = ctypes.c_int
     F = ctypes.c_float
     lib.tim_tis_ppo.argtypes = [P, P, P, P, P, P, F, F, F, ctypes.POINTER(tim_ppo_out), P]
     lib.tim_tis_ppo.restype = ctypes.c_int
@@ -209,6 +214,10 @@ def tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C, out: tim_
                        stream) -> int:
     return load().tim_mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, float(C),
                                      ctypes.byref(out), stream)
+
+
+def tim_mismatch_fold(seq_records, num_seqs, batch_stats, stream) -> int:
+    return load().tim_mismatch_fold(seq_records, int(num_seqs), batch_stats, stream)
 
 
 def tim_tis_ppo(logp_theta, logp_old, logp_rollout, advantages, mask, seq_offsets, eps_low, eps_high, C,
@@ -426,12 +435,14 @@ def token_logprob_fp32_head(h, W_split, targets, out_logp=None, out_lse=None, st
 
 def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
                    tau_seq: float = math.nan, seq_estimator: int = 3, token_weight: bool = False,
-                   stream=None, out=None):
+                   stream=None, out=None, seq_records: bool = False):
     """Mismatch statistics of packed sequences.
 
     logp_train, logp_rollout fp32 [N]; mask bool/uint8 [N]; seq_offsets int32 [S + 1].
     Returns a dict: seq_stats fp32 [S, 12] (SEQ_FIELDS), seq_flags int32 [S],
-    batch fp64 [20] (BATCH_FIELDS), token_weight fp32 [N] or None.
+    batch fp64 [20] (BATCH_FIELDS), token_weight fp32 [N] or None, and with
+    seq_records=True seq_records int32 [S, SEQ_RECORD_WORDS] (the records the
+    batch record is folded from; see mismatch_fold).
     """
     import torch
     _need(logp_train, "logp_train", torch.float32, 1)
@@ -449,12 +460,18 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
             "seq_flags": torch.empty(S, dtype=torch.int32, device=dev),
             "batch": torch.empty(len(BATCH_FIELDS), dtype=torch.float64, device=dev),
             "token_weight": torch.empty(N, dtype=torch.float32, device=dev) if token_weight else None,
+            "seq_records": torch.empty((S, SEQ_RECORD_WORDS), dtype=torch.int32, device=dev)
+            if seq_records else None,
         }
     _need_out(out["seq_stats"], "seq_stats", torch.float32, (S, len(SEQ_FIELDS)), dev)
     _need_out(out["seq_flags"], "seq_flags", torch.int32, (S,), dev)
     _need_out(out["batch"], "batch", torch.float64, (len(BATCH_FIELDS),), dev)
     if out.get("token_weight") is not None:
         _need_out(out["token_weight"], "token_weight", torch.float32, (N,), dev)
+    if out.get("seq_records") is not None:
+        _need_out(out["seq_records"], "seq_records", torch.int32, (S, SEQ_RECORD_WORDS), dev)
+        if out["seq_records"].data_ptr() % 16:
+            raise ValueError("seq_records must be 16-byte aligned")
     d = tim_mismatch_out()
     d.num_seqs = S
     d.num_tokens = N
@@ -464,9 +481,32 @@ def mismatch_stats(logp_train, logp_rollout, mask, seq_offsets, C: float = 2.0,
     d.seq_stats = out["seq_stats"].data_ptr()
     d.seq_flags = out["seq_flags"].data_ptr()
     d.batch_stats = out["batch"].data_ptr()
+    d.seq_records = out["seq_records"].data_ptr() if out.get("seq_records") is not None else None
     with torch.cuda.device(dev):
         rc = tim_mismatch_stats(logp_train.data_ptr(), logp_rollout.data_ptr(), mask.data_ptr(),
                                 seq_offsets.data_ptr(), C, d, _stream_handle(stream, dev))
+    _raise_if(rc)
+    return out
+
+
+def mismatch_fold(seq_records, out=None, stream=None):
+    """The batch record (fp64 [20], BATCH_FIELDS) of a batch scored in parts:
+    the parts' seq_records (int32 [S_part, SEQ_RECORD_WORDS] each, from
+    mismatch_stats(..., seq_records=True)) concatenated in the batch's sequence
+    order.  Bit-identical to mismatch_stats over the whole batch."""
+    import torch
+    _need(seq_records, "seq_records", torch.int32, 2)
+    dev = seq_records.device
+    if seq_records.shape[1] != SEQ_RECORD_WORDS:
+        raise ValueError("seq_records must have %d columns" % SEQ_RECORD_WORDS)
+    if seq_records.data_ptr() % 16:
+        raise ValueError("seq_records must be 16-byte aligned")
+    if out is None:
+        out = torch.empty(len(BATCH_FIELDS), dtype=torch.float64, device=dev)
+    _need_out(out, "out", torch.float64, (len(BATCH_FIELDS),), dev)
+    with torch.cuda.device(dev):
+        rc = tim_mismatch_fold(seq_records.data_ptr(), seq_records.shape[0], out.data_ptr(),
+                               _stream_handle(stream, dev))
     _raise_if(rc)
     return out
 

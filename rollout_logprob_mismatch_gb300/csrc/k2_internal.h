@@ -58,7 +58,12 @@ struct K2Args {
     int *status;
 };
 
+// The fold alone, over a.rec (a.S records): 256 bytes (the ticket, zeroed
+// here) then the fold partials.
+inline size_t k2_fold_workspace_bytes(int64_t S) { return 256 + static_cast<size_t>(k2_blocks(S)) * K2_PART_WORDS * 4; }
+
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream);
+cudaError_t k2_launch_fold(const K2Args &a, cudaStream_t stream);
 cudaError_t k2_prepare_device();   // per-device function attributes
 
 } // namespace tim

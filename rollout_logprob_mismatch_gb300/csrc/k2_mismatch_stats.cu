@@ -944,12 +944,13 @@ __global__ void __launch_bounds__(K2_FOLD_THREADS) k2_fold_kernel(const K2Args a
         write_batch(a, f, false);
 }
 
-// S = 0: only the (all-zero) batch record, after checking the offsets cover [0, N).
+// S = 0: only the (all-zero) batch record, after checking the offsets cover
+// [0, N) when there are offsets.
 __global__ void k2_empty_kernel(const K2Args a)
 {
     FoldAcc t;
     fold_zero(t);
-    write_batch(a, t, true);
+    write_batch(a, t, a.off != nullptr);
 }
 
 } // namespace
@@ -957,6 +958,19 @@ __global__ void k2_empty_kernel(const K2Args a)
 cudaError_t k2_prepare_device()
 {
     return cudaFuncSetAttribute(k2_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K2_SMEM_BYTES);
+}
+
+cudaError_t k2_launch_fold(const K2Args &a, cudaStream_t stream)
+{
+    if (a.S == 0) {
+        k2_empty_kernel<<<1, 1, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    cudaError_t e = cudaMemsetAsync(a.claim, 0, 256, stream);   // the fold's ticket
+    if (e != cudaSuccess)
+        return e;
+    k2_fold_kernel<<<static_cast<unsigned>(k2_blocks(a.S)), K2_FOLD_THREADS, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t k2_launch(const K2Args &a, int num_sms, cudaStream_t stream)

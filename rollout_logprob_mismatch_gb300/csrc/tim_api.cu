@@ -363,7 +363,7 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
         return fail(TIM_ERR_INVALID_ARG, "logp_train, logp_rollout and mask must be 16-byte aligned");
     if (!aligned(seq_offsets, 4) ||
         !aligned(out->seq_stats, 4) || !aligned(out->seq_flags, 4) || !aligned(out->token_weight, 4) ||
-        !aligned(out->batch_stats, 8))
+        !aligned(out->batch_stats, 8) || !aligned(out->seq_records, 16))
         return fail(TIM_ERR_INVALID_ARG, "misaligned array");
 
     DeviceState *dev = nullptr;
@@ -402,8 +402,9 @@ int tim_mismatch_stats(const float *logp_train, const float *logp_rollout, const
     a.batch = out->batch_stats;
     a.claim = static_cast<int *>(ws);
     a.blk_done = a.claim ? a.claim + 1 : nullptr;
-    a.rec = S > 0 ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + 256) : nullptr;
-    a.part = S > 0 ? a.rec + static_cast<size_t>(S) * tim::K2_REC_WORDS : nullptr;
+    uint32_t *const ws_rec = S > 0 ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + 256) : nullptr;
+    a.rec = out->seq_records ? out->seq_records : ws_rec;
+    a.part = S > 0 ? ws_rec + static_cast<size_t>(S) * tim::K2_REC_WORDS : nullptr;
     a.stats_vec = aligned(out->seq_stats, 16) ? 1 : 0;
     a.status = dev->status;
     cudaError_t e = tim::k2_launch(a, dev->sms, s);
@@ -578,6 +579,44 @@ int tim_token_logprob_fp32_head(const void *h, const void *W_split, const int32_
     if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature))
         return fail(TIM_ERR_INVALID_ARG, "temperature must be positive and finite");
     return token_logprob(h, W_split, targets, N, D, V, 1.f / temperature, out_logp, out_lse, stream, 3);
+}
+
+int tim_mismatch_fold(const uint32_t *seq_records, int32_t num_seqs, double *batch_stats, tim_stream_t stream)
+{
+    const int32_t S = num_seqs;
+    if (S < 0)
+        return fail(TIM_ERR_INVALID_ARG, "num_seqs must be >= 0");
+    if (!batch_stats || (S > 0 && !seq_records))
+        return fail(TIM_ERR_INVALID_ARG, "seq_records and batch_stats are required");
+    if (!aligned(seq_records, 16) || !aligned(batch_stats, 8))
+        return fail(TIM_ERR_INVALID_ARG, "misaligned array");
+    DeviceState *dev = nullptr;
+    int rc = device_state(&dev);
+    if (rc != TIM_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (S > 0) {
+        const cudaError_t e = cudaMallocFromPoolAsync(&ws, tim::k2_fold_workspace_bytes(S), dev->pool, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMallocFromPoolAsync(fold workspace)");
+    }
+    tim::K2Args a{};
+    a.S = S;
+    a.batch = batch_stats;
+    a.claim = static_cast<int *>(ws);
+    a.blk_done = a.claim ? a.claim + 1 : nullptr;
+    a.rec = const_cast<uint32_t *>(seq_records);   // read only by the fold
+    a.part = S > 0 ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + 256) : nullptr;
+    a.status = dev->status;
+    const cudaError_t e = tim::k2_launch_fold(a, s);
+    const cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "mismatch_fold launch");
+    if (ef != cudaSuccess)
+        return cuda_fail(ef, "cudaFreeAsync(fold workspace)");
+    g_msg[0] = 0;
+    return TIM_OK;
 }
 
 int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask, int64_t N,

@@ -46,12 +46,13 @@ def test_header_compiles_as_c_and_struct_layout_matches(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "tim.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(tim_mismatch_out),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(tim_mismatch_out),"
         "offsetof(tim_mismatch_out,num_seqs),offsetof(tim_mismatch_out,num_tokens),"
         "offsetof(tim_mismatch_out,tau_seq),offsetof(tim_mismatch_out,seq_estimator),"
         "offsetof(tim_mismatch_out,token_weight),offsetof(tim_mismatch_out,seq_stats),"
-        "offsetof(tim_mismatch_out,seq_flags),offsetof(tim_mismatch_out,batch_stats));"
-        "return TIM_SEQ_FIELDS == 12 && TIM_BATCH_FIELDS == 20 ? 0 : 1;}\n")
+        "offsetof(tim_mismatch_out,seq_flags),offsetof(tim_mismatch_out,batch_stats),"
+        "offsetof(tim_mismatch_out,seq_records));"
+        "return TIM_SEQ_FIELDS == 12 && TIM_BATCH_FIELDS == 20 && TIM_SEQ_RECORD_WORDS == 16 ? 0 : 1;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
                     "-o", str(exe)], check=True)
@@ -60,9 +61,9 @@ def test_header_compiles_as_c_and_struct_layout_matches(tmp_path):
     S = tim.tim_mismatch_out
     want = [ctypes.sizeof(S)] + [getattr(S, f).offset for f in
                                  ("num_seqs", "num_tokens", "tau_seq", "seq_estimator", "token_weight",
-                                  "seq_stats", "seq_flags", "batch_stats")]
+                                  "seq_stats", "seq_flags", "batch_stats", "seq_records")]
     assert vals == want
-    assert len(tim.SEQ_FIELDS) == 12 and len(tim.BATCH_FIELDS) == 20
+    assert len(tim.SEQ_FIELDS) == 12 and len(tim.BATCH_FIELDS) == 20 and tim.SEQ_RECORD_WORDS == 16
 
 
 def test_version(lib):
@@ -131,6 +132,19 @@ def test_mismatch_stats_rejects_bad_arguments(lib):
     assert tim.tim_mismatch_stats(16, 16, 16, None, 2.0, _out(), None) == E
     assert tim.tim_mismatch_stats(18, 16, 16, 16, 2.0, _out(), None) == E
     assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, _out(batch=20), None) == E
+    d = _out()
+    d.seq_records = 24   # caller-owned records must be 16-byte aligned
+    assert tim.tim_mismatch_stats(*ok_ptrs, 2.0, d, None) == E
+
+
+def test_mismatch_fold_rejects_bad_arguments(lib):
+    E = tim.TIM_ERR_INVALID_ARG
+    assert tim.tim_mismatch_fold(16, -1, 16, None) == E
+    assert tim.tim_mismatch_fold(None, 3, 16, None) == E
+    assert tim.tim_mismatch_fold(16, 3, None, None) == E
+    assert tim.tim_mismatch_fold(24, 3, 16, None) == E      # records not 16-byte aligned
+    assert tim.tim_mismatch_fold(16, 3, 20, None) == E      # batch record not 8-byte aligned
+    assert "aligned" in tim.tim_last_error()
 
 
 def test_ppo_struct_layout_matches(tmp_path):

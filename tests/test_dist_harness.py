@@ -58,3 +58,42 @@ def test_single_process_needs_no_process_group():
     assert bench.dist_init(1, "gloo") is None
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.aggregate_value(1, 8192, 30, 0.2) == pytest.approx(8192 * 30 / 0.2)
+
+
+def _gather_worker(rank, world, port, q):
+    import torch.distributed as dist
+    from rollout_logprob_mismatch_gb300 import sharded
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.dist_init(world, "gloo")
+    sizes = [3, 0, 5][:world]
+    # rank r's part: records whose first word is its global sequence index
+    first = sum(sizes[:rank])
+    local = torch.arange(first, first + sizes[rank], dtype=torch.int32).repeat_interleave(16).view(-1, 16)
+    local[:, 1] = rank
+    got = sharded.gather_seq_records(local)   # the default group
+    q.put((rank, got.tolist()))
+    dist.destroy_process_group()
+
+
+def test_sharded_records_are_gathered_in_the_batch_order():
+    """The sharded batch record's one exchange: every rank gets all ranks'
+    sequence records in rank order (parts of 3, 0 and 5 sequences), which is
+    the batch's sequence order the fold needs."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    world = 3
+    procs = [ctx.Process(target=_gather_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    owner = [0, 0, 0, 2, 2, 2, 2, 2]
+    for _, rows in out:
+        assert [r[0] for r in rows] == list(range(8))
+        assert [r[1] for r in rows] == owner
+        assert all(len(r) == 16 for r in rows)

@@ -236,3 +236,41 @@ def test_full_size_bandwidth_batch():
     off, mask, _, l_tr, l_ro, _ = wl.draw_ppo_inputs(1 << 27, 22)
     gs, o = run_both(l_tr, l_ro, mask, off)
     check_all(gs, o)
+
+
+def _part(l_tr, l_ro, mask, off, s0, s1):
+    """Sequences s0 .. s1 - 1 of a packed batch as a batch of their own."""
+    b, e = int(off[s0]), int(off[s1])
+    return l_tr[b:e], l_ro[b:e], mask[b:e], (off[s0:s1 + 1] - off[s0]).astype(np.int32)
+
+
+@pytest.mark.parametrize("cuts", [(0, 1, 5000), (0, 1700, 1701, 3333, 5000), (0, 2500, 2500, 5000)])
+def test_batch_scored_in_parts_folds_to_the_same_bits(cuts):
+    """A batch split into parts (as across data-parallel ranks; a part may be
+    empty): each part's sequence records, concatenated in sequence order and
+    folded by mismatch_fold, give the whole batch's record bit for bit, and
+    the records themselves are the whole call's; the oracle agrees."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 60, size=5000)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(off[-1])
+    l_tr = wl.draw_train_logprobs(N, 31)
+    l_ro = (l_tr + rng.normal(0, 0.05, N)).astype(np.float32)
+    mask = (rng.random(N) < 0.8).astype(np.uint8)
+    whole = tim.mismatch_stats(_dev(l_tr), _dev(l_ro), _dev(mask), _dev(off), seq_records=True)
+    recs = []
+    for s0, s1 in zip(cuts[:-1], cuts[1:]):
+        p = _part(l_tr, l_ro, mask, off, s0, s1)
+        recs.append(tim.mismatch_stats(*(_dev(x) for x in p), seq_records=True)["seq_records"])
+    folded = tim.mismatch_fold(torch.cat(recs, 0).contiguous())
+    tim.check()
+    assert torch.equal(torch.cat(recs, 0), whole["seq_records"])
+    assert torch.equal(folded.view(torch.int64), whole["batch"].view(torch.int64))
+    o = oracle.mismatch_stats(l_tr, l_ro, mask, off)
+    assert_batch_match(folded.cpu().numpy(), o["batch"])
+
+
+def test_fold_of_no_sequences_is_all_zero():
+    out = tim.mismatch_fold(torch.zeros((0, tim.SEQ_RECORD_WORDS), dtype=torch.int32, device="cuda"))
+    tim.check()
+    assert torch.count_nonzero(out).item() == 0
