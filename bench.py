@@ -48,8 +48,8 @@ K2_BW_TOKENS = 1 << 27
 MEASURED_TRAFFIC = {
     # token logprob, N = 8192, D = 4096, V = 151936: 2666996480 read + 15407872 written
     ("k1", "78fc418be590bdf5"): 2666996480 + 15407872,
-    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229385216 read + 496305408 written
-    ("k2", "14aadbfd96b712cb"): 1221917696 + 7467520 + 496305408,
+    # mismatch pass, 2^27 tokens (sequence kernel + fold): 1229469952 read + 496668160 written
+    ("k2", "c4e714ca643ef1b7"): 1222002176 + 7467776 + 496668160,
     # TIS-weighted PPO surrogate, 2^27 tokens (sequence + fold): 2497949440 read + 1027808000 written
     ("ppo", "a17407344a379435"): 2494668800 + 3280640 + 1027808000,
     # mismatch monitor, 2^27 tokens, its three kernels: 1227758848 read + 109751296 written
