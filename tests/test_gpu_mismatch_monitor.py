@@ -177,3 +177,24 @@ def test_just_above_the_sample_with_a_ragged_tail():
     tau = float(np.float32(0.03))
     g, rej = gpu_monitor(lo, lr, mask, tau)
     assert_monitor_match(g, rej, oracle.mismatch_monitor(lo, lr, mask, tau), "2^20 + 12345")
+
+
+def test_sequences_that_differ_in_their_mismatch():
+    """Each sequence has its own mismatch scale and shift (lognormal scales
+    spread by a factor e^1.5): the sample's runs (mostly one sequence each)
+    are then the independent units and its quantile estimates far noisier
+    than their token count says, so a bound misses and the selection runs
+    over all tokens; the result stays exact."""
+    rng = np.random.default_rng(41)
+    lens = rng.integers(256, 2048, size=4096)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    N = int(off[-1])
+    seq = np.repeat(np.arange(len(lens)), lens)
+    scale = (0.02 * np.exp(1.5 * rng.standard_normal(len(lens)))).astype(np.float32)[seq]
+    shift = (0.02 * rng.standard_normal(len(lens))).astype(np.float32)[seq]
+    lr = wl.draw_train_logprobs(N, 41)
+    lt = (lr + shift + scale * rng.standard_normal(N).astype(np.float32)).astype(np.float32)
+    mask = (rng.random(N) < 0.7).astype(np.uint8)
+    tau = float(np.float32(0.05))
+    g, rej = gpu_monitor(lt, lr, mask, tau)
+    assert_monitor_match(g, rej, oracle.mismatch_monitor(lt, lr, mask, tau), "per-sequence mismatch")
