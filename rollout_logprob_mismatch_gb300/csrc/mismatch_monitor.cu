@@ -188,21 +188,27 @@ __device__ __forceinline__ uint32_t segment_total(const uint32_t (&v)[SEG])
 // above the sample's last).  The ranks are a heuristic (a rank off by one only
 // moves a bound; the check after the full pass keeps the result exact), so
 // they are taken in fp32.  Run by one CTA of MON_THREADS threads on the
-// global sample histogram of delta's key: thread i loads bins [64 i, 64 i +
-// 64) (all loads in flight at once), the CTA writes the inclusive prefix sums
-// P of the histogram to shared memory `P` (SBD words), and one thread per
-// bound searches them: delta's bin holding rank R is the first x with
-// P[x] > R; |delta|'s bin c covers delta's bins SBA - 1 - c .. SBA + c, so the
-// |delta| bin holding R is the first c with P[SBA + c] - P[SBA - 2 - c] > R.
+// global sample histogram of delta's key, seen as rows of 32 bins: warp w
+// takes rows [64 w, 64 w + 64), lane l bin l of each (coalesced loads, all in
+// flight at once; a warp scan per row, the rows independent of one another,
+// then the rows' totals carried), the CTA writes the inclusive prefix sums P
+// of the histogram to shared memory `P` (SBD words, lane l word l of a row:
+// no bank conflicts), and one thread per bound searches them: delta's bin
+// holding rank R is the first x with P[x] > R; |delta|'s bin c covers delta's
+// bins SBA - 1 - c .. SBA + c, so the |delta| bin holding R is the first c
+// with P[SBA + c] - P[SBA - 2 - c] > R.
 __device__ void compute_bounds(const MonArgs &a, uint32_t *P)
 {
     __shared__ uint32_t wsum[MON_THREADS / 32];
     __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     MonState *st = a.st;
-    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 delta bins per thread");
+    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 rows of 32 bins per warp");
     uint32_t v[64];
-    load_segment<64>(a.shist + tid * 64, v);
+    const uint32_t *row0 = a.shist + warp * 2048 + lane;
+#pragma unroll
+    for (int r = 0; r < 64; ++r)
+        v[r] = __ldcg(row0 + 32 * r);
     const long long m = static_cast<long long>(__ldcg(&st->sample_used));
     if (tid < MON_QUANTILES) {
         const float L = static_cast<float>(level(tid));
@@ -212,29 +218,31 @@ __device__ void compute_bounds(const MonArgs &a, uint32_t *P)
         rlo_s[tid] = static_cast<long long>(floorf(j)) - w;
         rhi_s[tid] = static_cast<long long>(ceilf(j)) + w;
     }
-    uint32_t run = 0;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) {
-        run += v[x];
-        v[x] = run;
-    }
-    uint32_t incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += y;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, v[r], o);
+            if (lane >= o)
+                v[r] += y;
+        }
     }
-    if (lane == 31)
-        wsum[warp] = incl;
+    uint32_t carry = 0;   // the warp's rows before row r
+#pragma unroll
+    for (int r = 0; r < 64; ++r) {
+        const uint32_t t = __shfl_sync(0xffffffffu, v[r], 31);
+        v[r] += carry;
+        carry += t;
+    }
+    if (lane == 0)
+        wsum[warp] = carry;
     __syncthreads();
-    uint32_t before = incl - run;
+    uint32_t before = 0;
     for (int w = 0; w < warp; ++w)
         before += wsum[w];
 #pragma unroll
-    for (int x = 0; x < 64; x += 4)
-        *reinterpret_cast<uint4 *>(P + tid * 64 + x) =
-            make_uint4(before + v[x], before + v[x + 1], before + v[x + 2], before + v[x + 3]);
+    for (int r = 0; r < 64; ++r)
+        P[warp * 2048 + 32 * r + lane] = before + v[r];
     __syncthreads();
     if (tid < 2 * MON_QUANTILES) {
         const int q = tid >> 1, e = tid & 1;
