@@ -436,8 +436,12 @@ constexpr int kRing = 2;                                // ring slots per warp
 constexpr int kChunkTokens = 32 * kScanTokens;
 constexpr int kChunkF = 4 * kChunkTokens;               // bytes of one fp32 array's chunk
 constexpr int kChunkBytes = 2 * kChunkF + kChunkTokens; // l_train, l_rollout, mask
-constexpr int kScanWarps = MON_THREADS / 32;
-constexpr int kScanCtasPerSm = 2;                       // the rings and stages: 82 KB of shared memory per CTA
+// One CTA of 16 warps per SM (rings and stages: 160 KB of shared memory).
+// (Two CTAs of 8 warps per SM had the younger CTA of each SM finish ~26 us
+// after the older one, ~11 % of the pass: the warp schedulers favour the
+// older CTA's warps, and the pass is bound by instruction issue.)
+constexpr int kScanThreads = 512;
+constexpr int kScanWarps = kScanThreads / 32;
 constexpr size_t kRingBytes = static_cast<size_t>(kScanWarps) * kRing * kChunkBytes;
 constexpr size_t kStageBytes = sizeof(uint32_t) * kScanWarps * MON_QUANTILES * kStage;
 constexpr size_t kScanSmem = kRingBytes + kStageBytes + 8 * kScanWarps * kRing;
@@ -602,7 +606,7 @@ __device__ __forceinline__ float pick(const float (&k)[kScanTokens], int s)
 __device__ void check_ranks(const MonArgs &a);
 __device__ void select_high(const MonArgs &a);
 
-__global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(const MonArgs a)
+__global__ void __launch_bounds__(kScanThreads, 1) mon_scan_kernel(const MonArgs a)
 {
     extern __shared__ __align__(16) uint8_t scan_smem[];   // rings [warp][kRing], staging, barriers
     __shared__ float flo_s[MON_QUANTILES], fhi_s[MON_QUANTILES];
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
         one_s = 1u;
         abort_s = 0;
     }
-    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += MON_THREADS)
+    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += kScanThreads)
         hic_s[i] = 0u;
     float flo[MON_QUANTILES], fhi[MON_QUANTILES];   // set from the sample's bounds (below)
     uint32_t one = 0u;
@@ -857,7 +861,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
             red_s[warp][2 + q] = wb[q];
     }
     __syncthreads();
-    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += MON_THREADS)   // the CTA's coarse counts
+    for (int i = tid; i < MON_QUANTILES * MON_COARSE; i += kScanThreads)   // the CTA's coarse counts
         if (hic_s[i] != 0u)
             atomicAdd(a.hic + i, hic_s[i]);
     if (tid < 2 + MON_QUANTILES) {
@@ -873,7 +877,7 @@ __global__ void __launch_bounds__(MON_THREADS, kScanCtasPerSm) mon_scan_kernel(c
         if (tid == 0)
             check_ranks(a);
         __syncthreads();
-        if (!a.st->empty && !a.st->fallback)   // uniform over the CTA
+        if (!a.st->empty && !a.st->fallback && tid < 32 * MON_TARGETS)   // uniform over each warp
             select_high(a);
     }
 }
@@ -1373,15 +1377,14 @@ cudaError_t monitor_launch(const MonArgs &a, int num_sms, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     const int64_t groups = (a.N + 3) / 4;
-    const int64_t want = (groups + MON_THREADS - 1) / MON_THREADS;
-    const dim3 scan_grid(static_cast<unsigned>(
-        std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(kScanCtasPerSm) * num_sms))));
+    const int64_t want = (groups + kScanThreads - 1) / kScanThreads;
+    const dim3 scan_grid(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, num_sms))));
     // one CTA per SM: all start at once; every one of them also zeroes its
     // share of the fine histograms
     const dim3 block(MON_THREADS);
     if ((e = launch_pdl(mon_sample_kernel, dim3(static_cast<unsigned>(num_sms)), block, kSampleSmem, stream, a)) !=
             cudaSuccess ||
-        (e = launch_pdl(mon_scan_kernel, scan_grid, block, kScanSmem, stream, a)) != cudaSuccess)
+        (e = launch_pdl(mon_scan_kernel, scan_grid, dim3(kScanThreads), kScanSmem, stream, a)) != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
