@@ -188,80 +188,115 @@ __device__ __forceinline__ uint32_t segment_total(const uint32_t (&v)[SEG])
 // above the sample's last).  The ranks are a heuristic (a rank off by one only
 // moves a bound; the check after the full pass keeps the result exact), so
 // they are taken in fp32.  Run by one CTA of MON_THREADS threads on the
-// global sample histogram of delta's key, seen as rows of 32 bins: warp w
-// takes rows [64 w, 64 w + 64), lane l bin l of each (coalesced loads, all in
-// flight at once; a warp scan per row, the rows independent of one another,
-// then the rows' totals carried), the CTA writes the inclusive prefix sums P
-// of the histogram to shared memory `P` (SBD words, lane l word l of a row:
-// no bank conflicts), and one thread per bound searches them: delta's bin
-// holding rank R is the first x with P[x] > R; |delta|'s bin c covers delta's
-// bins SBA - 1 - c .. SBA + c, so the |delta| bin holding R is the first c
-// with P[SBA + c] - P[SBA - 2 - c] > R.
-__device__ void compute_bounds(const MonArgs &a, uint32_t *P)
+// global sample histogram of delta's key, seen as 512 rows of 32 bins: warp w
+// loads rows [64 w, 64 w + 64), lane l bin l of each (coalesced, all in
+// flight at once), copies them to shared memory `H` (SBD words) and sums each
+// row (one warp reduction per row).  |delta|'s row k (its bins 32 k .. 32 k +
+// 31, bin c holding delta's bins SBA - 1 - c and SBA + c) is delta's rows
+// SBA / 32 + k and SBA / 32 - 1 - k, so its total is theirs.  Warps 0 and 1
+// take the prefix sums of the 512 delta and 256 |delta| row totals; then warp
+// b finds bound b's bin: the first row whose prefix exceeds the rank R (two
+// ballots), then, in that row, the first bin whose cumulative count exceeds
+// R (a warp scan and a ballot).
+__device__ void compute_bounds(const MonArgs &a, uint32_t *H)
 {
-    __shared__ uint32_t wsum[MON_THREADS / 32];
-    __shared__ long long rlo_s[MON_QUANTILES], rhi_s[MON_QUANTILES];
+    constexpr int ROWS = SBD / 32, AROWS = SBA / 32;   // 512 and 256
+    __shared__ uint32_t rowt[ROWS];                    // delta's row totals
+    __shared__ uint32_t rowp[ROWS], arowp[AROWS];      // inclusive prefix sums of delta's and |delta|'s
+    __shared__ long long R_s[2 * MON_QUANTILES];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     MonState *st = a.st;
-    static_assert(SBD == 64 * MON_THREADS && SBA == SBD / 2, "64 rows of 32 bins per warp");
+    static_assert(ROWS == 64 * (MON_THREADS / 32) && AROWS == 32 * 8 && ROWS == 32 * 16 &&
+                      MON_THREADS / 32 == 2 * MON_QUANTILES, "row split; a warp per bound");
     uint32_t v[64];
     const uint32_t *row0 = a.shist + warp * 2048 + lane;
 #pragma unroll
     for (int r = 0; r < 64; ++r)
         v[r] = __ldcg(row0 + 32 * r);
     const long long m = static_cast<long long>(__ldcg(&st->sample_used));
-    if (tid < MON_QUANTILES) {
-        const float L = static_cast<float>(level(tid));
+    if (tid < 2 * MON_QUANTILES) {
+        const float L = static_cast<float>(level(tid >> 1));
         const float j = static_cast<float>(m - 1) * L;
         const long long w = static_cast<long long>(ceilf(static_cast<float>(kSigmas) *
                                                          sqrtf(static_cast<float>(m) * L * (1.f - L)))) + 2;
-        rlo_s[tid] = static_cast<long long>(floorf(j)) - w;
-        rhi_s[tid] = static_cast<long long>(ceilf(j)) + w;
+        R_s[tid] = (tid & 1) == 0 ? static_cast<long long>(floorf(j)) - w : static_cast<long long>(ceilf(j)) + w;
     }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-        for (int r = 0; r < 64; ++r) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, v[r], o);
-            if (lane >= o)
-                v[r] += y;
-        }
-    }
-    uint32_t carry = 0;   // the warp's rows before row r
+    uint32_t t0 = 0, t1 = 0;   // lane l: the totals of the warp's rows l and 32 + l
 #pragma unroll
     for (int r = 0; r < 64; ++r) {
-        const uint32_t t = __shfl_sync(0xffffffffu, v[r], 31);
-        v[r] += carry;
-        carry += t;
-    }
-    if (lane == 0)
-        wsum[warp] = carry;
-    __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w)
-        before += wsum[w];
-#pragma unroll
-    for (int r = 0; r < 64; ++r)
-        P[warp * 2048 + 32 * r + lane] = before + v[r];
-    __syncthreads();
-    if (tid < 2 * MON_QUANTILES) {
-        const int q = tid >> 1, e = tid & 1;
-        const long long R = e == 0 ? rlo_s[q] : rhi_s[q];
-        int bin = -1;
-        if (m > 0 && R > 0 && R < m - 1) {   // then some bin holds R: P's last word is m
-            const uint32_t r = static_cast<uint32_t>(R);
-            int lo = 0, hi = q == 0 ? SBA - 1 : SBD - 1;   // the answer is in [lo, hi]
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                const uint32_t c = q == 0 ? P[SBA + mid] - (mid <= SBA - 2 ? P[SBA - 2 - mid] : 0u) : P[mid];
-                if (c > r)
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            bin = lo;
+        H[warp * 2048 + 32 * r + lane] = v[r];
+        const uint32_t t = __reduce_add_sync(0xffffffffu, v[r]);
+        if (lane == (r & 31)) {
+            if (r < 32)
+                t0 = t;
+            else
+                t1 = t;
         }
-        if (e == 0)
+    }
+    rowt[warp * 64 + lane] = t0;
+    rowt[warp * 64 + 32 + lane] = t1;
+    __syncthreads();
+    if (warp == 0) {   // delta's rows: lane l the rows [16 l, 16 l + 16)
+        uint32_t x[16], run = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            run += rowt[16 * lane + i];
+            x[i] = run;
+        }
+        uint32_t incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            rowp[16 * lane + i] = incl - run + x[i];
+    } else if (warp == 1) {   // |delta|'s rows: lane l the rows [8 l, 8 l + 8)
+        uint32_t x[8], run = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = 8 * lane + i;
+            run += rowt[AROWS + k] + rowt[AROWS - 1 - k];
+            x[i] = run;
+        }
+        uint32_t incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            arowp[8 * lane + i] = incl - run + x[i];
+    }
+    __syncthreads();
+    // warp b: bound b (quantile b / 2; b even: lo, odd: hi)
+    const int b = warp, q = b >> 1;
+    const long long R = R_s[b];
+    int bin = -1;
+    if (m > 0 && R > 0 && R < m - 1) {   // then some bin holds R: the last prefix is m
+        const uint32_t r = static_cast<uint32_t>(R);
+        const uint32_t *pp = q == 0 ? arowp : rowp;
+        const int per = q == 0 ? AROWS / 32 : ROWS / 32;   // rows per lane in the first ballot
+        const unsigned big = __ballot_sync(0xffffffffu, pp[per * lane + per - 1] > r);
+        const int L = __ffs(big) - 1;                       // big != 0: the last prefix is m > r
+        const unsigned in = __ballot_sync(0xffffffffu, lane < per && pp[per * L + lane] > r);
+        const int row = per * L + __ffs(in) - 1;
+        const uint32_t before = row > 0 ? pp[row - 1] : 0u;
+        uint32_t c = q == 0 ? H[SBA + 32 * row + lane] + H[SBA - 1 - 32 * row - lane] : H[32 * row + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o)
+                c += y;
+        }
+        bin = 32 * row + __ffs(__ballot_sync(0xffffffffu, before + c > r)) - 1;
+    }
+    if (lane == 0) {
+        if ((b & 1) == 0)
             st->lo[q] = bin < 0 ? 0u : static_cast<uint32_t>(bin) << SAMPLE_SHIFT;
         else
             st->hi[q] = bin < 0 ? 0xffffffffu
@@ -406,7 +441,7 @@ __global__ void __launch_bounds__(MON_THREADS) mon_sample_kernel(const MonArgs a
     pdl_launch_dependents();
     flush_histogram<SBD>(sh, a.shist);
     if (last_cta(&a.st->ticket[0]))
-        compute_bounds(a, sh);   // the shared histogram is spent: its room takes the prefix sums
+        compute_bounds(a, sh);   // the CTA's histogram is spent: its room takes the global one
 }
 
 // ---------------------------------------------------------------- the full pass
