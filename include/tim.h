@@ -274,7 +274,7 @@ typedef struct {
  *   out                       host struct described above
  * Bad offsets found on the device set TIM_ERR_BAD_INPUT (see tim_check) and
  * make every output NaN for the affected sequences and for the batch record.
- * Scratch: about 128 * S bytes from the library's stream-ordered pool. */
+ * Scratch: about 64 * S bytes from the library's stream-ordered pool. */
 TIM_API int tim_mismatch_stats(const float *logp_train, const float *logp_rollout,
                        const uint8_t *mask, const int32_t *seq_offsets, float C,
                        const tim_mismatch_out *out, tim_stream_t stream);
@@ -328,7 +328,8 @@ enum tim_monitor_field {
  * One pass over the tokens (9 bytes read per token) after a sample of at most
  * 2^20 of them; exact selection among the few percent of tokens near each
  * quantile (over all tokens when a sample-based bound misses).  Scratch:
- * 205 KB + N bytes + 1 MB from the library's stream-ordered pool. */
+ * 3254 KB + N bytes + 1 MB from the library's stream-ordered pool (the state
+ * and histograms, then four lists of N / 16 + 65536 keys). */
 TIM_API int tim_mismatch_monitor(const float *logp_train, const float *logp_rollout, const uint8_t *mask,
                                  int64_t N, float tau_tok, uint8_t *token_reject, double *out,
                                  tim_stream_t stream);
