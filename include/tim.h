@@ -82,7 +82,8 @@ typedef enum {
  *            outside [0, V) (e.g. the -100 ignore label) gives out_logp = NaN
  *   N        rows, N >= 0 (N = 0 is a no-op returning TIM_OK), N < 2^31
  *   D        hidden size, D > 0 and D % 8 == 0 (16-byte row stride), D <= 65536
- *   V        vocabulary size, 0 < V < 2^31
+ *   V        vocabulary size, 0 < V < 2^31, with ceil(N / 128) * ceil(V / 1024)
+ *            < 2^31 (N * V below about 2^48)
  *   out_logp fp32 [N]: l_t in nats
  *   out_lse  fp32 [N]: log-sum-exp of the raw logits, in nats
  *
