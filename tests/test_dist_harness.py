@@ -54,6 +54,38 @@ def test_reference_arm_prints_only_on_rank_zero(monkeypatch, capsys):
     assert capsys.readouterr().out == ""
 
 
+def test_reference_arm_line_carries_the_contract_keys(monkeypatch, capsys):
+    """Rank 0's reference line, on the tiny head so that it runs in a second: the
+    oracle timed on the host cores, reported with its cpu_baseline and an e2e
+    entry that moves no bytes, on the same metric, unit and workload names as the
+    GB300 arm."""
+    import json
+
+    import workloads as wl
+    tiny = wl.CONFIGS["tiny"]
+
+    def tiny_workload(seed=0, tokens=None):
+        h, W = wl.draw_head(tiny, seed=seed)
+        off = wl.draw_segments(tiny, seed=seed)
+        return tiny, h, W, wl.draw_targets(tiny, tiny.N, seed=seed), off, wl.draw_mask(tiny, off, seed=seed)
+
+    monkeypatch.setattr(bench, "make_workload", tiny_workload)
+    monkeypatch.setenv("TIM_BENCH_ORACLE_SECONDS", "0.2")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, bench.UNIT, True)
+    assert (line["n_gpus"], line["steps"], line["warmup"]) == (1, 2, 3)
+    assert line["value"] > 0 and line["ms_per_step"] == pytest.approx(tiny.N / line["value"] * 1e3)
+    assert line["config"]["workload"] == "%s_head+mismatch" % tiny.name
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == line["value"] and cpu["cores"] >= 1 and cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
 def test_single_process_needs_no_process_group():
     assert bench.dist_init(1, "gloo") is None
     assert bench.max_over_ranks(3.5, None) == 3.5
